@@ -1,0 +1,250 @@
+"""fp64 CPU oracle for the speculative-decoding verify step.
+
+TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check of
+``__graft_entry__`` and the CPU-baseline leg of ``bench.py`` may import this
+package.  The product library never calls it and shares no source with it.
+
+The arithmetic lives in ``sd_oracle.c`` (plain C, double precision, written
+step by step from the pages; see the header of that file for the passages
+each function follows).  This module only compiles it with gcc and marshals
+numpy arrays through ctypes.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "sd_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+F32, BF16 = 0, 1
+ST_BAD_TOKEN, ST_NONFINITE, ST_BAD_PARENT, ST_ZERO_MASS = 1, 2, 4, 8
+
+
+def build(force: bool = False) -> str:
+    """Compile sd_oracle.c into liboracle.so (gcc, -O2, no -march flags)."""
+    stale = (not os.path.exists(_LIB)) or (
+        os.path.getmtime(_LIB) < os.path.getmtime(_SRC))
+    if force or stale:
+        tmp = _LIB + ".%d.tmp" % os.getpid()
+        subprocess.check_call(
+            ["gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-Wall",
+             "-fno-fast-math", "-ffp-contract=off", _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _bind(path):
+    lib = ctypes.CDLL(path)
+    P = ctypes.c_void_p
+    I = ctypes.c_int
+    D = ctypes.c_double
+    lib.orc_verify_linear.argtypes = [P, P, I, P, P, I, I, I, D,
+                                      P, P, P, P, P, P, P]
+    lib.orc_verify_kcand.argtypes = [P, P, I, P, P, I, I, I, I, D,
+                                     P, P, P, P, P, P, P]
+    lib.orc_verify_tree.argtypes = [P, P, I, P, P, P, I, I, I, D,
+                                    P, P, P, P, P, P]
+    lib.orc_fanout_schedule.argtypes = [I, I, D, D, P]
+    lib.orc_fanout_topk.argtypes = [P, I, I, I, I, P, P, P, P]
+    for f in (lib.orc_verify_linear, lib.orc_verify_kcand,
+              lib.orc_verify_tree, lib.orc_fanout_schedule,
+              lib.orc_fanout_topk):
+        f.restype = ctypes.c_int
+    return lib
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            _lib = _bind(_LIB)
+    return _lib
+
+
+class swapped_library:
+    """Context manager for the mutation tests: route every call to another
+    build of the oracle (a copy of sd_oracle.c with a planted mistake)."""
+
+    def __init__(self, path):
+        self.path = path
+
+    def __enter__(self):
+        global _lib
+        _load()
+        self._saved = _lib
+        _lib = _bind(self.path)
+        return self
+
+    def __exit__(self, *exc):
+        global _lib
+        _lib = self._saved
+        return False
+
+
+def _logits(a):
+    """Return (contiguous array, dtype code).  bf16 logits travel as their
+    raw uint16 bit patterns; fp32 as float32."""
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        return a, BF16
+    if a.dtype == np.float32:
+        return a, F32
+    raise TypeError("logits must be float32 or raw bf16 bits (uint16)")
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def verify_linear(target, draft, tokens, uniforms, T, want_resid=False):
+    """Linear verify of B sequences.
+
+    target [B, gamma+1, V], draft [B, gamma, V] (float32, or uint16 bf16 bits;
+    draft may be None when T == 0), tokens [B, gamma] int32, uniforms
+    [B, gamma+1] float32.  Returns a dict of numpy arrays: n, tokens, prob,
+    accept, margin, status and (when asked) resid [B, V].
+    """
+    target, dt = _logits(target)
+    B, G1, V = target.shape
+    gamma = G1 - 1
+    if draft is None:
+        if T != 0:
+            raise ValueError("draft logits are required when T > 0")
+        draft_p = None
+    else:
+        draft, dt2 = _logits(draft)
+        if dt2 != dt or draft.shape != (B, gamma, V):
+            raise ValueError("draft must match target in dtype and shape")
+        draft_p = _ptr(draft)
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32).reshape(B, gamma)
+    uniforms = np.ascontiguousarray(uniforms, dtype=np.float32).reshape(B, G1)
+    out = {
+        "n": np.empty(B, np.int32),
+        "tokens": np.empty((B, G1), np.int32),
+        "prob": np.empty(B, np.float64),
+        "accept": np.empty((B, max(gamma, 1)), np.float64),
+        "margin": np.empty(B, np.float64),
+        "status": np.empty(B, np.int32),
+    }
+    resid = np.empty((B, V), np.float64) if want_resid else None
+    rc = _load().orc_verify_linear(
+        _ptr(target), draft_p, dt, _ptr(tokens), _ptr(uniforms), B, gamma, V,
+        float(T), _ptr(out["n"]), _ptr(out["tokens"]), _ptr(out["prob"]),
+        _ptr(out["accept"]), _ptr(out["margin"]), _ptr(resid),
+        _ptr(out["status"]))
+    if rc:
+        raise MemoryError("oracle allocation failed")
+    out["accept"] = out["accept"][:, :gamma]
+    if want_resid:
+        out["resid"] = resid
+    return out
+
+
+def verify_kcand(target, draft, tokens, uniforms, T):
+    """K-candidate verify with longest-streak self-selection.
+
+    target [B, K, gamma+1, V], draft [B, gamma, V] shared marginals, tokens
+    [B, K, gamma], uniforms [B, K, gamma+1].
+    """
+    target, dt = _logits(target)
+    B, K, G1, V = target.shape
+    gamma = G1 - 1
+    draft, dt2 = _logits(draft)
+    if dt2 != dt or draft.shape != (B, gamma, V):
+        raise ValueError("draft must be [B, gamma, V] in the target's dtype")
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32).reshape(B, K, gamma)
+    uniforms = np.ascontiguousarray(uniforms, np.float32).reshape(B, K, G1)
+    out = {
+        "n": np.empty(B, np.int32),
+        "k": np.empty(B, np.int32),
+        "tokens": np.empty((B, G1), np.int32),
+        "n_per_cand": np.empty((B, K), np.int32),
+        "prob": np.empty(B, np.float64),
+        "margin": np.empty(B, np.float64),
+        "status": np.empty(B, np.int32),
+    }
+    rc = _load().orc_verify_kcand(
+        _ptr(target), _ptr(draft), dt, _ptr(tokens), _ptr(uniforms), B, K,
+        gamma, V, float(T), _ptr(out["n"]), _ptr(out["k"]),
+        _ptr(out["tokens"]), _ptr(out["n_per_cand"]), _ptr(out["prob"]),
+        _ptr(out["margin"]), _ptr(out["status"]))
+    if rc:
+        raise MemoryError("oracle allocation failed")
+    return out
+
+
+def verify_tree(target, draft, parent, node_tokens, uniforms, T):
+    """Token-tree verify with sequential sibling rejection.
+
+    target, draft [B, N, V]; parent, node_tokens [B, N] int32; uniforms
+    [B, N] float32 (slot 0 is the final draw).
+    """
+    target, dt = _logits(target)
+    B, N, V = target.shape
+    draft, dt2 = _logits(draft)
+    if dt2 != dt or draft.shape != (B, N, V):
+        raise ValueError("draft must match target in dtype and shape")
+    parent = np.ascontiguousarray(parent, np.int32).reshape(B, N)
+    node_tokens = np.ascontiguousarray(node_tokens, np.int32).reshape(B, N)
+    uniforms = np.ascontiguousarray(uniforms, np.float32).reshape(B, N)
+    out = {
+        "n": np.empty(B, np.int32),
+        "tokens": np.empty((B, N), np.int32),
+        "nodes": np.empty((B, N), np.int32),
+        "prob": np.empty(B, np.float64),
+        "margin": np.empty(B, np.float64),
+        "status": np.empty(B, np.int32),
+    }
+    rc = _load().orc_verify_tree(
+        _ptr(target), _ptr(draft), dt, _ptr(parent), _ptr(node_tokens),
+        _ptr(uniforms), B, N, V, float(T), _ptr(out["n"]),
+        _ptr(out["tokens"]), _ptr(out["nodes"]), _ptr(out["prob"]),
+        _ptr(out["margin"]), _ptr(out["status"]))
+    if rc:
+        raise MemoryError("oracle allocation failed")
+    return out
+
+
+def fanout_schedule(K, budget, a, r):
+    """Geometric fan-out F[0..K] with sum == budget (Theorem 12 + largest
+    remainder)."""
+    F = np.zeros(K + 1, np.int32)
+    if _load().orc_fanout_schedule(int(K), int(budget), float(a), float(r),
+                                   _ptr(F)):
+        raise ValueError("bad fan-out arguments")
+    return F
+
+
+def fanout_topk(draft, F):
+    """Top-F_k tokens of lookahead row k; draft [B, K+1, V]."""
+    draft, dt = _logits(draft)
+    B, K1, V = draft.shape
+    F = np.ascontiguousarray(F, np.int32)
+    if F.shape != (K1,):
+        raise ValueError("F must have K+1 entries")
+    total = int(F.sum())
+    out = {
+        "tokens": np.empty((B, total), np.int32),
+        "logit": np.empty((B, total), np.float64),
+        "status": np.empty(B, np.int32),
+    }
+    rc = _load().orc_fanout_topk(_ptr(draft), dt, B, K1 - 1, V, _ptr(F),
+                                 _ptr(out["tokens"]), _ptr(out["logit"]),
+                                 _ptr(out["status"]))
+    if rc:
+        raise MemoryError("oracle allocation failed")
+    return out
+
+
+FLAG_MARGIN = 1e-5
+"""A draw whose margin is below this is 'flagged': a correct fp32
+implementation may land on the other side of the threshold there."""

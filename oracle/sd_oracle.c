@@ -1,0 +1,612 @@
+/*
+ * sd_oracle.c -- plain, slow, fp64 CPU oracle for the verify step of
+ * speculative decoding.  TEST INFRASTRUCTURE ONLY: it is called by the test
+ * suite, by the smoke check and by the CPU-baseline leg of the benchmark,
+ * never by the product path.  It shares no source with the CUDA library.
+ *
+ * Every function follows the pages step by step, in double precision, with
+ * no blocking, fusion or reordering:
+ *
+ *  - "01 · Draft-then-verify" (llm-infra-atlas), section 1, Algorithm 1:
+ *    draft gamma tokens, one target pass gives p_1..p_{gamma+1}, scan left
+ *    to right drawing r_i and rejecting at the first r_i > p_i(x_i)/q_i(x_i),
+ *    then sample a correction from norm(max(0, p_{n+1} - q_{n+1})) or, when
+ *    every draft is accepted, a bonus token from p_{gamma+1}.
+ *  - same page, section 2.1: single-step accept probability min(1, p/q) and
+ *    the residual p' = norm(max(0, p - q)).
+ *  - same page, section 2.2: greedy (temperature 0) reduces to comparing the
+ *    draft id with argmax p.
+ *  - same page, section 4, the spec_step listing: 0-based indexing, ps[n]
+ *    minus qs[n] for the residual, ps[gamma] for the bonus.
+ *  - SpecDiff-2 (MLSys'26), "core method", self-selection acceptance: K
+ *    candidate drafts from shared position-wise marginals, the verifier keeps
+ *    the candidate with the longest accepted streak.
+ *  - PRESTO, section 2.1 "tree-based speculative decoding": prefix-wise
+ *    verification from the root, acceptance factorised along the path.
+ *  - Speculative Speculative Decoding / Saguaro, "speculation cache
+ *    strategy": Definition 11 (power-law cache miss) and Theorem 12
+ *    (geometric fan-out F_k = F_0 a^{k/(1+r)}, capped at position K), and
+ *    the top-F_k-per-position cache fill.
+ *
+ * Readings where the pages are silent (all listed in the design notes):
+ *  - accept iff r <= p(x)/q(x) (reject on '>', Algorithm 1 step 3);
+ *  - p = softmax(z / T) for target and draft with the same T; T == 0 is
+ *    greedy on the raw logits (lowest index wins a tie);
+ *  - inverse CDF: the smallest j with C_j > u * N (strict), C_j the running
+ *    sum of the weights in index order; if rounding leaves no such j, the
+ *    last j with positive weight;
+ *  - a residual of exactly zero mass falls back to sampling p and sets
+ *    status bit 8;
+ *  - a draft token outside [0, V) is a rejection (status bit 1);
+ *  - a row holding NaN or +inf, or only -inf, makes its sequence invalid
+ *    (status bit 2; n = -1, every token -1);
+ *  - a parent array with parent[0] != -1 or parent[v] outside [0, v) makes
+ *    its tree invalid (status bit 4);
+ *  - tree siblings are tried in increasing node index against the fixed
+ *    draft row of their parent, with p <- norm(max(0, p - q)) after each
+ *    rejection; the final draw of a tree uses uniform slot 0;
+ *  - kcand selection: the largest accepted count, ties to the lowest k; the
+ *    final draw uses uniform slot [b][k*][gamma];
+ *  - fan-out integerisation: floor of F_0 w_k, the remainder handed out by
+ *    largest fractional part, ties to the lower k; top-F orders by
+ *    (value descending, index ascending), -0 equal to +0.
+ *
+ * Every draw also records a margin: |r - p/q| for an accept test and the
+ * distance of u to the two CDF boundaries of the chosen token for an
+ * inverse-CDF draw.  The smallest margin of a sequence tells the tests
+ * whether a finite-precision implementation may legitimately disagree.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_F32 0
+#define ORC_BF16 1
+
+#define ORC_ST_BAD_TOKEN 1
+#define ORC_ST_NONFINITE 2
+#define ORC_ST_BAD_PARENT 4
+#define ORC_ST_ZERO_MASS 8
+
+/* ---- input access: fp32 as is, bf16 widened exactly (it is the top half
+ * of an fp32 bit pattern) ---- */
+static double logit_at(const void *base, int dtype, size_t i) {
+  if (dtype == ORC_F32) return (double)((const float *)base)[i];
+  uint32_t w = (uint32_t)((const uint16_t *)base)[i] << 16;
+  float f;
+  memcpy(&f, &w, sizeof f);
+  return (double)f;
+}
+
+/* A row is usable iff no entry is NaN or +inf and at least one entry is
+ * finite.  Returns 1 if usable. */
+static int row_ok(const void *base, int dtype, size_t off, int V) {
+  int any_finite = 0;
+  for (int j = 0; j < V; ++j) {
+    double z = logit_at(base, dtype, off + (size_t)j);
+    if (isnan(z) || z == INFINITY) return 0;
+    if (z > -INFINITY) any_finite = 1;
+  }
+  return any_finite;
+}
+
+/* p = softmax(z / T), T > 0, with max subtraction.  Returns 0 on an
+ * unusable row. */
+static int softmax_row(const void *base, int dtype, size_t off, int V,
+                       double T, double *p) {
+  if (!row_ok(base, dtype, off, V)) return 0;
+  double m = -INFINITY;
+  for (int j = 0; j < V; ++j) {
+    double z = logit_at(base, dtype, off + (size_t)j);
+    if (z > m) m = z;
+  }
+  double Z = 0.0;
+  for (int j = 0; j < V; ++j) {
+    p[j] = exp((logit_at(base, dtype, off + (size_t)j) - m) / T);
+    Z += p[j];
+  }
+  for (int j = 0; j < V; ++j) p[j] /= Z;
+  return 1;
+}
+
+/* argmax over the raw logits, lowest index on ties.  -1 on an unusable row. */
+static int argmax_row(const void *base, int dtype, size_t off, int V) {
+  if (!row_ok(base, dtype, off, V)) return -1;
+  int best = 0;
+  double bv = logit_at(base, dtype, off);
+  for (int j = 1; j < V; ++j) {
+    double z = logit_at(base, dtype, off + (size_t)j);
+    if (z > bv) { bv = z; best = j; }
+  }
+  return best;
+}
+
+/* Inverse-CDF draw from the weights w (not necessarily normalised, total
+ * N > 0): the smallest j with C_j > u N.  Writes w_t / N and the margin
+ * min(|u - C_{t-1}/N|, |u - C_t/N|). */
+static int sample_icdf(const double *w, int V, double u, double *prob,
+                       double *margin) {
+  double N = 0.0;
+  for (int j = 0; j < V; ++j) N += w[j];
+  double target = u * N;
+  double C = 0.0, Cprev = 0.0;
+  int t = -1;
+  for (int j = 0; j < V; ++j) {
+    Cprev = C;
+    C += w[j];
+    if (C > target) { t = j; break; }
+  }
+  if (t < 0) { /* rounding left no crossing: last token with mass */
+    for (int j = V - 1; j >= 0; --j)
+      if (w[j] > 0.0) { t = j; break; }
+    C = N;
+    Cprev = N - w[t];
+  }
+  *prob = w[t] / N;
+  double m1 = fabs(u - Cprev / N), m2 = fabs(u - C / N);
+  *margin = m1 < m2 ? m1 : m2;
+  return t;
+}
+
+/* The accept ratio p(x)/q(x); 0 when p(x) == 0, +inf when only q(x) == 0. */
+static double accept_ratio(double px, double qx) {
+  if (px == 0.0) return 0.0;
+  if (qx == 0.0) return INFINITY;
+  return px / qx;
+}
+
+static void note_margin(double *margin, double m) {
+  if (m < *margin) *margin = m;
+}
+
+/* ------------------------------------------------------------------------
+ * Linear verify ("01 · Draft-then-verify", Algorithm 1 and spec_step).
+ * target [B, gamma+1, V], draft [B, gamma, V] (unused when T == 0),
+ * tokens [B, gamma], uniforms [B, gamma+1] (slot gamma is the final draw).
+ * out_accept [B, gamma]: min(1, p/q) of each evaluated test (1/0 when
+ * T == 0), -1 where no test was made.  out_resid [B, V] (nullable): the
+ * normalised distribution the last token was drawn from.
+ * ---------------------------------------------------------------------- */
+int orc_verify_linear(const void *target, const void *draft, int dtype,
+                      const int32_t *tokens, const float *uniforms, int B,
+                      int gamma, int V, double T, int32_t *n_acc,
+                      int32_t *out_tokens, double *out_prob,
+                      double *out_accept, double *margin, double *out_resid,
+                      int32_t *status) {
+  double *p = malloc(sizeof(double) * (size_t)V);
+  double *q = malloc(sizeof(double) * (size_t)V);
+  double *w = malloc(sizeof(double) * (size_t)V);
+  if (!p || !q || !w) { free(p); free(q); free(w); return 1; }
+  const int G1 = gamma + 1;
+  for (int b = 0; b < B; ++b) {
+    int st = 0, n = 0, t = -1, invalid = 0;
+    double mg = INFINITY, prob = 0.0;
+    for (int i = 0; i < gamma; ++i) out_accept[(size_t)b * gamma + i] = -1.0;
+    if (T == 0.0) {
+      for (int i = 0; i < gamma; ++i) {
+        int a = argmax_row(target, dtype, ((size_t)b * G1 + i) * V, V);
+        if (a < 0) { invalid = 1; break; }
+        int x = tokens[(size_t)b * gamma + i];
+        if (x < 0 || x >= V) st |= ORC_ST_BAD_TOKEN;
+        int ok = (x == a);
+        out_accept[(size_t)b * gamma + i] = ok ? 1.0 : 0.0;
+        if (!ok) break;
+        ++n;
+      }
+      if (!invalid) {
+        t = argmax_row(target, dtype, ((size_t)b * G1 + n) * V, V);
+        if (t < 0) invalid = 1;
+        prob = 1.0;
+        if (out_resid && !invalid) {
+          for (int j = 0; j < V; ++j) out_resid[(size_t)b * V + j] = 0.0;
+          out_resid[(size_t)b * V + t] = 1.0;
+        }
+      }
+    } else {
+      int rejected = 0;
+      for (int i = 0; i < gamma; ++i) {
+        if (!softmax_row(target, dtype, ((size_t)b * G1 + i) * V, V, T, p) ||
+            !softmax_row(draft, dtype, ((size_t)b * gamma + i) * V, V, T, q)) {
+          invalid = 1;
+          break;
+        }
+        int x = tokens[(size_t)b * gamma + i];
+        double r = (double)uniforms[(size_t)b * G1 + i];
+        int ok;
+        if (x < 0 || x >= V) {
+          st |= ORC_ST_BAD_TOKEN;
+          ok = 0;
+          out_accept[(size_t)b * gamma + i] = 0.0;
+        } else {
+          double rho = accept_ratio(p[x], q[x]);
+          if (isfinite(rho)) note_margin(&mg, fabs(r - rho));
+          ok = (r <= rho);
+          out_accept[(size_t)b * gamma + i] = rho < 1.0 ? rho : 1.0;
+        }
+        if (!ok) { rejected = 1; break; }
+        ++n;
+      }
+      if (!invalid) {
+        if (rejected) { /* residual norm(max(0, p_n - q_n)) */
+          double N = 0.0;
+          for (int j = 0; j < V; ++j) {
+            double d = p[j] - q[j];
+            w[j] = d > 0.0 ? d : 0.0;
+            N += w[j];
+          }
+          if (N == 0.0) { /* nothing left to correct with: sample p_n */
+            st |= ORC_ST_ZERO_MASS;
+            for (int j = 0; j < V; ++j) w[j] = p[j];
+          }
+        } else { /* bonus from p_{gamma+1} */
+          if (!softmax_row(target, dtype, ((size_t)b * G1 + gamma) * V, V, T,
+                           p))
+            invalid = 1;
+          else
+            for (int j = 0; j < V; ++j) w[j] = p[j];
+        }
+      }
+      if (!invalid) {
+        double mc;
+        double u = (double)uniforms[(size_t)b * G1 + gamma];
+        t = sample_icdf(w, V, u, &prob, &mc);
+        note_margin(&mg, mc);
+        if (out_resid) {
+          double N = 0.0;
+          for (int j = 0; j < V; ++j) N += w[j];
+          for (int j = 0; j < V; ++j) out_resid[(size_t)b * V + j] = w[j] / N;
+        }
+      }
+    }
+    if (invalid) {
+      st |= ORC_ST_NONFINITE;
+      n = -1;
+      prob = 0.0;
+      mg = INFINITY;
+    }
+    n_acc[b] = n;
+    for (int i = 0; i < G1; ++i) {
+      int32_t v = -1;
+      if (!invalid) {
+        if (i < n) v = tokens[(size_t)b * gamma + i];
+        else if (i == n) v = t;
+      }
+      out_tokens[(size_t)b * G1 + i] = v;
+    }
+    out_prob[b] = prob;
+    margin[b] = (T == 0.0) ? INFINITY : mg;
+    status[b] = st;
+  }
+  free(p); free(q); free(w);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------
+ * K-candidate verify with verifier self-selection (SpecDiff-2, "core
+ * method").  target [B, K, gamma+1, V]: candidate k's own target rows;
+ * draft [B, gamma, V]: the position-wise marginals shared by all K
+ * candidates; tokens [B, K, gamma]; uniforms [B, K, gamma+1].
+ * Each candidate is scanned with the linear rule; the selected candidate is
+ * the one with the most accepted tokens (lowest k on ties); its residual
+ * or bonus draw uses uniform [b][k*][gamma].
+ * ---------------------------------------------------------------------- */
+int orc_verify_kcand(const void *target, const void *draft, int dtype,
+                     const int32_t *tokens, const float *uniforms, int B,
+                     int K, int gamma, int V, double T, int32_t *n_acc,
+                     int32_t *sel_k, int32_t *out_tokens, int32_t *n_per_cand,
+                     double *out_prob, double *margin, int32_t *status) {
+  double *p = malloc(sizeof(double) * (size_t)V);
+  double *q = malloc(sizeof(double) * (size_t)V);
+  double *w = malloc(sizeof(double) * (size_t)V);
+  if (!p || !q || !w) { free(p); free(q); free(w); return 1; }
+  const int G1 = gamma + 1;
+#define TROW(b, k, j) ((((size_t)(b) * K + (k)) * G1 + (j)) * (size_t)V)
+#define DROW(b, j) (((size_t)(b) * gamma + (j)) * (size_t)V)
+  for (int b = 0; b < B; ++b) {
+    int st = 0, invalid = 0;
+    double mg = INFINITY, prob = 0.0;
+    int best_k = 0, best_n = -1, t = -1;
+    for (int k = 0; k < K && !invalid; ++k) {
+      int n = 0;
+      for (int j = 0; j < gamma; ++j) {
+        int x = tokens[((size_t)b * K + k) * gamma + j];
+        int ok;
+        if (T == 0.0) {
+          int a = argmax_row(target, dtype, TROW(b, k, j), V);
+          if (a < 0) { invalid = 1; break; }
+          if (x < 0 || x >= V) st |= ORC_ST_BAD_TOKEN;
+          ok = (x == a);
+        } else {
+          if (!softmax_row(target, dtype, TROW(b, k, j), V, T, p) ||
+              !softmax_row(draft, dtype, DROW(b, j), V, T, q)) {
+            invalid = 1;
+            break;
+          }
+          if (x < 0 || x >= V) {
+            st |= ORC_ST_BAD_TOKEN;
+            ok = 0;
+          } else {
+            double r = (double)uniforms[((size_t)b * K + k) * G1 + j];
+            double rho = accept_ratio(p[x], q[x]);
+            if (isfinite(rho)) note_margin(&mg, fabs(r - rho));
+            ok = (r <= rho);
+          }
+        }
+        if (!ok) break;
+        ++n;
+      }
+      if (invalid) break;
+      n_per_cand[(size_t)b * K + k] = n;
+      if (n > best_n) { best_n = n; best_k = k; }
+    }
+    if (!invalid) {
+      const int n = best_n, k = best_k;
+      if (T == 0.0) {
+        t = argmax_row(target, dtype, TROW(b, k, n), V);
+        if (t < 0) invalid = 1;
+        prob = 1.0;
+      } else {
+        if (n < gamma) {
+          if (!softmax_row(target, dtype, TROW(b, k, n), V, T, p) ||
+              !softmax_row(draft, dtype, DROW(b, n), V, T, q))
+            invalid = 1;
+          else {
+            double N = 0.0;
+            for (int j = 0; j < V; ++j) {
+              double d = p[j] - q[j];
+              w[j] = d > 0.0 ? d : 0.0;
+              N += w[j];
+            }
+            if (N == 0.0) {
+              st |= ORC_ST_ZERO_MASS;
+              for (int j = 0; j < V; ++j) w[j] = p[j];
+            }
+          }
+        } else {
+          if (!softmax_row(target, dtype, TROW(b, k, gamma), V, T, p))
+            invalid = 1;
+          else
+            for (int j = 0; j < V; ++j) w[j] = p[j];
+        }
+        if (!invalid) {
+          double mc;
+          double u = (double)uniforms[((size_t)b * K + k) * G1 + gamma];
+          t = sample_icdf(w, V, u, &prob, &mc);
+          note_margin(&mg, mc);
+        }
+      }
+    }
+    if (invalid) {
+      st |= ORC_ST_NONFINITE;
+      for (int k = 0; k < K; ++k) n_per_cand[(size_t)b * K + k] = -1;
+      n_acc[b] = -1;
+      sel_k[b] = -1;
+      prob = 0.0;
+      mg = INFINITY;
+    } else {
+      n_acc[b] = best_n;
+      sel_k[b] = best_k;
+    }
+    for (int i = 0; i < G1; ++i) {
+      int32_t v = -1;
+      if (!invalid) {
+        if (i < best_n) v = tokens[((size_t)b * K + best_k) * gamma + i];
+        else if (i == best_n) v = t;
+      }
+      out_tokens[(size_t)b * G1 + i] = v;
+    }
+    out_prob[b] = prob;
+    margin[b] = (T == 0.0) ? INFINITY : mg;
+    status[b] = st;
+  }
+#undef TROW
+#undef DROW
+  free(p); free(q); free(w);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------
+ * Tree verify.  target [B, N, V]: row u is p(. | path to u); draft [B, N, V]:
+ * row u is the q that drafted u's children.  parent [B, N] with parent[0]
+ * == -1 and parent[v] < v; node_tokens [B, N] (slot 0 unused); uniforms
+ * [B, N]: slot v tests node v, slot 0 is the final draw.
+ * The walk starts at the root; the children of the current node are tried
+ * in increasing node index; each rejection replaces p by norm(max(0, p-q))
+ * with q the parent's draft row; an accepted child becomes the current node
+ * with fresh rows.  When no child is accepted (or at a leaf) the last token
+ * is drawn from the current p.
+ * Outputs: n_acc = number of accepted nodes; out_nodes [B, N] the accepted
+ * path (-1 padded); out_tokens [B, N] the accepted tokens then the final
+ * token (-1 padded).
+ * ---------------------------------------------------------------------- */
+int orc_verify_tree(const void *target, const void *draft, int dtype,
+                    const int32_t *parent, const int32_t *node_tokens,
+                    const float *uniforms, int B, int N, int V, double T,
+                    int32_t *n_acc, int32_t *out_tokens, int32_t *out_nodes,
+                    double *out_prob, double *margin, int32_t *status) {
+  double *p = malloc(sizeof(double) * (size_t)V);
+  double *q = malloc(sizeof(double) * (size_t)V);
+  if (!p || !q) { free(p); free(q); return 1; }
+  for (int b = 0; b < B; ++b) {
+    const int32_t *par = parent + (size_t)b * N;
+    const int32_t *tok = node_tokens + (size_t)b * N;
+    const float *U = uniforms + (size_t)b * N;
+    int st = 0, invalid = 0, depth = 0, t = -1;
+    double mg = INFINITY, prob = 0.0;
+    for (int i = 0; i < N; ++i) {
+      out_nodes[(size_t)b * N + i] = -1;
+      out_tokens[(size_t)b * N + i] = -1;
+    }
+    if (par[0] != -1) invalid = 4;
+    for (int v = 1; v < N && !invalid; ++v)
+      if (par[v] < 0 || par[v] >= v) invalid = 4;
+    int cur = 0;
+    while (!invalid) {
+      size_t off = ((size_t)b * N + cur) * (size_t)V;
+      int has_child = 0;
+      for (int v = cur + 1; v < N; ++v)
+        if (par[v] == cur) { has_child = 1; break; }
+      int next = -1;
+      if (T == 0.0) {
+        int a = argmax_row(target, dtype, off, V);
+        if (a < 0) { invalid = 2; break; }
+        for (int v = cur + 1; v < N; ++v) {
+          if (par[v] != cur) continue;
+          if (tok[v] < 0 || tok[v] >= V) st |= ORC_ST_BAD_TOKEN;
+          if (tok[v] == a) { next = v; break; }
+        }
+        if (next < 0) { t = a; prob = 1.0; break; }
+      } else {
+        if (!softmax_row(target, dtype, off, V, T, p)) { invalid = 2; break; }
+        if (has_child && !softmax_row(draft, dtype, off, V, T, q)) {
+          invalid = 2;
+          break;
+        }
+        int zero_mass = 0;
+        for (int v = cur + 1; v < N && next < 0 && !zero_mass; ++v) {
+          if (par[v] != cur) continue;
+          int x = tok[v];
+          int ok = 0;
+          if (x < 0 || x >= V) {
+            st |= ORC_ST_BAD_TOKEN;
+          } else {
+            double rho = accept_ratio(p[x], q[x]);
+            if (isfinite(rho)) note_margin(&mg, fabs((double)U[v] - rho));
+            ok = ((double)U[v] <= rho);
+          }
+          if (ok) { next = v; break; }
+          /* rejected: p <- norm(max(0, p - q)) */
+          double S = 0.0;
+          for (int j = 0; j < V; ++j) {
+            double d = p[j] - q[j];
+            p[j] = d > 0.0 ? d : 0.0;
+            S += p[j];
+          }
+          if (S == 0.0) { /* fall back to the un-subtracted p of this node */
+            st |= ORC_ST_ZERO_MASS;
+            softmax_row(target, dtype, off, V, T, p);
+            zero_mass = 1;
+          } else {
+            for (int j = 0; j < V; ++j) p[j] /= S;
+          }
+        }
+        if (next < 0) {
+          double mc;
+          t = sample_icdf(p, V, (double)U[0], &prob, &mc);
+          note_margin(&mg, mc);
+          break;
+        }
+      }
+      out_nodes[(size_t)b * N + depth] = next;
+      out_tokens[(size_t)b * N + depth] = tok[next];
+      ++depth;
+      cur = next;
+    }
+    if (invalid) {
+      st |= invalid == 4 ? ORC_ST_BAD_PARENT : ORC_ST_NONFINITE;
+      for (int i = 0; i < N; ++i) {
+        out_nodes[(size_t)b * N + i] = -1;
+        out_tokens[(size_t)b * N + i] = -1;
+      }
+      n_acc[b] = -1;
+      prob = 0.0;
+      mg = INFINITY;
+    } else {
+      n_acc[b] = depth;
+      out_tokens[(size_t)b * N + depth] = t;
+    }
+    out_prob[b] = prob;
+    margin[b] = (T == 0.0) ? INFINITY : mg;
+    status[b] = st;
+  }
+  free(p); free(q);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------
+ * Geometric fan-out schedule (Saguaro, Theorem 12): w_k = a^{k/(1+r)} for
+ * k < K, w_K = a^{K/(1+r)} (1-a)^{-1/(1+r)}, F_0 = budget / sum w, then the
+ * real F_0 w_k made integer by largest remainder (ties to the lower k).
+ * Returns nonzero on bad arguments.
+ * ---------------------------------------------------------------------- */
+int orc_fanout_schedule(int K, int budget, double a, double r, int32_t *F) {
+  if (K < 0 || budget < 0 || !(a > 0.0 && a < 1.0) || !(r > 0.0)) return 1;
+  double *w = malloc(sizeof(double) * (size_t)(K + 1));
+  double *frac = malloc(sizeof(double) * (size_t)(K + 1));
+  if (!w || !frac) { free(w); free(frac); return 1; }
+  double s = 0.0;
+  for (int k = 0; k < K; ++k) {
+    w[k] = pow(a, (double)k / (1.0 + r));
+    s += w[k];
+  }
+  w[K] = pow(a, (double)K / (1.0 + r)) * pow(1.0 - a, -1.0 / (1.0 + r));
+  s += w[K];
+  double F0 = (double)budget / s;
+  int used = 0;
+  for (int k = 0; k <= K; ++k) {
+    double real = F0 * w[k];
+    double fl = floor(real);
+    F[k] = (int32_t)fl;
+    frac[k] = real - fl;
+    used += F[k];
+  }
+  for (int left = budget - used; left > 0; --left) {
+    int best = -1;
+    for (int k = 0; k <= K; ++k)
+      if (frac[k] >= 0.0 && (best < 0 || frac[k] > frac[best])) best = k;
+    if (best < 0) break;
+    F[best] += 1;
+    frac[best] = -1.0;
+  }
+  free(w); free(frac);
+  return 0;
+}
+
+typedef struct { double v; int idx; } orc_entry;
+
+static int entry_cmp(const void *x, const void *y) {
+  const orc_entry *a = x, *b = y;
+  if (a->v > b->v) return -1;
+  if (a->v < b->v) return 1;
+  return (a->idx > b->idx) - (a->idx < b->idx);
+}
+
+/* Top-F_k tokens of lookahead row k of every sequence (Saguaro, "speculation
+ * cache strategy": the cache holds the top-F_k draft tokens at each
+ * lookahead position).  draft [B, K+1, V]; out_tokens / out_logit [B, sum F]
+ * grouped by k at offset sum_{k' < k} F_{k'}, best first.  A row holding a
+ * NaN yields -1 tokens and status bit 2. */
+int orc_fanout_topk(const void *draft, int dtype, int B, int K, int V,
+                    const int32_t *F, int32_t *out_tokens, double *out_logit,
+                    int32_t *status) {
+  int total = 0;
+  for (int k = 0; k <= K; ++k) total += F[k];
+  orc_entry *e = malloc(sizeof(orc_entry) * (size_t)V);
+  if (!e) return 1;
+  for (int b = 0; b < B; ++b) {
+    int st = 0, off = 0;
+    for (int k = 0; k <= K; ++k) {
+      size_t row = ((size_t)b * (K + 1) + k) * (size_t)V;
+      int bad = 0;
+      for (int j = 0; j < V; ++j) {
+        double z = logit_at(draft, dtype, row + (size_t)j);
+        if (isnan(z)) bad = 1;
+        e[j].v = (z == 0.0) ? 0.0 : z; /* -0 and +0 are the same value */
+        e[j].idx = j;
+      }
+      if (bad) st |= ORC_ST_NONFINITE;
+      else qsort(e, (size_t)V, sizeof(orc_entry), entry_cmp);
+      for (int i = 0; i < F[k]; ++i) {
+        size_t o = (size_t)b * total + off + i;
+        int ok = !bad && i < V;
+        out_tokens[o] = ok ? e[i].idx : -1;
+        if (out_logit) out_logit[o] = ok ? e[i].v : NAN;
+      }
+      off += F[k];
+    }
+    status[b] = st;
+  }
+  free(e);
+  return 0;
+}

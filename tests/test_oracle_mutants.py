@@ -1,0 +1,115 @@
+"""The oracle's pins must catch plausible mistakes.
+
+Each case copies oracle/sd_oracle.c, plants one mistake (a wrong comparison,
+a flipped sign, a dropped term, an off-by-one index, swapped operands),
+builds it with gcc and runs the pins of tests/test_oracle_pins.py that
+should notice.  The test passes only if at least one of them fails on the
+planted mistake.  Nothing here touches a GPU.
+"""
+import os
+import subprocess
+import tempfile
+
+import pytest
+
+import oracle
+from tests import test_oracle_pins as pins
+
+MUTANTS = [
+    # (id, text in sd_oracle.c, replacement, nth occurrence, pins)
+    ("accept_direction", "ok = (r <= rho);", "ok = (r >= rho);", 1,
+     ["test_beta_closed_form_and_empirical_accept_rate"]),
+    ("ratio_swapped", "double rho = accept_ratio(p[x], q[x]);",
+     "double rho = accept_ratio(q[x], p[x]);", 1,
+     ["test_beta_closed_form_and_empirical_accept_rate",
+      "test_worked_residual_examples"]),
+    ("residual_sign", "double d = p[j] - q[j];", "double d = q[j] - p[j];", 1,
+     ["test_first_token_marginal_is_p", "test_worked_residual_examples"]),
+    ("residual_no_clamp", "w[j] = d > 0.0 ? d : 0.0;", "w[j] = d;", 1,
+     ["test_worked_residual_examples", "test_first_token_marginal_is_p"]),
+    ("temperature_dropped",
+     "p[j] = exp((logit_at(base, dtype, off + (size_t)j) - m) / T);",
+     "p[j] = exp((logit_at(base, dtype, off + (size_t)j) - m));", 1,
+     ["test_first_token_marginal_is_p"]),
+    ("bonus_row_off_by_one",
+     "if (!softmax_row(target, dtype, ((size_t)b * G1 + gamma) * V, V, T,",
+     "if (!softmax_row(target, dtype, ((size_t)b * G1 + gamma - 1) * V, V, T,",
+     1, ["test_bruteforce_enumeration",
+         "test_second_token_conditional_with_prefix_dependent_target"]),
+    ("cdf_unnormalised", "double target = u * N;", "double target = u;", 1,
+     ["test_worked_residual_examples", "test_first_token_marginal_is_p"]),
+    ("residual_wrong_position_draft",
+     "!softmax_row(draft, dtype, ((size_t)b * gamma + i) * V, V, T, q)",
+     "!softmax_row(draft, dtype, ((size_t)b * gamma + 0) * V, V, T, q)", 1,
+     ["test_second_token_conditional_with_prefix_dependent_target",
+      "test_bruteforce_enumeration"]),
+    ("greedy_tie_highest", "if (z > bv) { bv = z; best = j; }",
+     "if (z >= bv) { bv = z; best = j; }", 1,
+     ["test_greedy_is_id_equality_with_argmax"]),
+    ("kcand_tie_highest_k", "if (n > best_n) { best_n = n; best_k = k; }",
+     "if (n >= best_n) { best_n = n; best_k = k; }", 1,
+     ["test_kcand_selection_is_max_streak_lowest_k"]),
+    ("kcand_shared_draft_row_wrong",
+     "!softmax_row(draft, dtype, DROW(b, j), V, T, q)) {",
+     "!softmax_row(draft, dtype, DROW(b, 0), V, T, q)) {", 1,
+     ["test_kcand_max_streak_law_bruteforce"]),
+    ("tree_no_residual_update", "p[j] = d > 0.0 ? d : 0.0;\n            S += p[j];",
+     "S += (d > 0.0 ? d : 0.0);", 1,
+     ["test_tree_iid_siblings_lossless"]),
+    ("tree_final_uniform_slot", "t = sample_icdf(p, V, (double)U[0], &prob, &mc);",
+     "t = sample_icdf(p, V, (double)U[1], &prob, &mc);", 1,
+     ["test_tree_chain_equals_linear", "test_tree_iid_siblings_lossless"]),
+    ("fanout_exponent", "w[k] = pow(a, (double)k / (1.0 + r));",
+     "w[k] = pow(a, (double)k / r);", 1,
+     ["test_fanout_schedule_golden_and_theorem12"]),
+    ("fanout_cap_sign",
+     "pow(1.0 - a, -1.0 / (1.0 + r));", "pow(1.0 - a, 1.0 / (1.0 + r));", 1,
+     ["test_fanout_schedule_golden_and_theorem12"]),
+    ("topk_tie_order", "return (a->idx > b->idx) - (a->idx < b->idx);",
+     "return (a->idx < b->idx) - (a->idx > b->idx);", 1,
+     ["test_fanout_topk_against_stable_sort_and_ties"]),
+]
+
+
+def _build_mutant(src, pattern, repl, nth, outdir, name):
+    idx = -1
+    for _ in range(nth):
+        idx = src.index(pattern, idx + 1)
+    mutated = src[:idx] + repl + src[idx + len(pattern):]
+    cpath = os.path.join(outdir, name + ".c")
+    so = os.path.join(outdir, name + ".so")
+    with open(cpath, "w") as f:
+        f.write(mutated)
+    subprocess.check_call(["gcc", "-std=c11", "-O2", "-fPIC", "-shared",
+                           "-ffp-contract=off", cpath, "-o", so, "-lm"])
+    return so
+
+
+def _run_pin(name):
+    fn = getattr(pins, name)
+    params = {
+        "test_first_token_marginal_is_p": [dict(T=1.0), dict(T=0.7)],
+        "test_bruteforce_enumeration": [dict(V=3, gamma=3),
+                                        dict(V=5, gamma=2)],
+        "test_tree_chain_equals_linear": [dict(T=1.0)],
+    }.get(name, [dict()])
+    for kw in params:
+        fn(**kw)
+
+
+@pytest.mark.parametrize("mid,pattern,repl,nth,catchers", MUTANTS,
+                         ids=[m[0] for m in MUTANTS])
+def test_pins_catch_planted_mistake(mid, pattern, repl, nth, catchers):
+    with open(oracle._SRC) as f:
+        src = f.read()
+    assert pattern in src, "mutation site vanished: " + mid
+    with tempfile.TemporaryDirectory() as d:
+        so = _build_mutant(src, pattern, repl, nth, d, mid)
+        caught = []
+        with oracle.swapped_library(so):
+            for name in catchers:
+                try:
+                    _run_pin(name)
+                except AssertionError:
+                    caught.append(name)
+    assert caught, "no pin caught the planted mistake " + mid

@@ -1,0 +1,532 @@
+"""Pins of the fp64 oracle against what the pages and mathematics fix.
+
+None of these re-types the oracle's arithmetic: each checks a closed form,
+an invariant, a worked example, a brute-force enumeration or a statistical
+law that a dropped term, a wrong sign, a wrong index or a swapped operand in
+the oracle would break (tests/test_oracle_mutants.py plants such mistakes
+and checks that these pins catch them).
+"""
+import itertools
+import math
+
+import numpy as np
+import pytest
+from scipy import stats
+
+import oracle
+from speculative_decoding_verification_temperature_gb300 import synth
+
+P_MIN = 1e-4  # chi-square p-value floor (seeds are fixed: deterministic)
+
+
+# ---------------------------------------------------------------- helpers
+def softmax(z, T=1.0):
+    z = np.asarray(z, np.float64) / T
+    e = np.exp(z - z.max())
+    return e / e.sum()
+
+
+def draw_from(p, n, seed):
+    """n iid draws from the probability vector p (Gumbel-max, numpy)."""
+    rng = np.random.default_rng(seed)
+    g = -np.log(-np.log(rng.random((n, len(p))).clip(1e-300)))
+    with np.errstate(divide="ignore"):
+        return np.argmax(np.log(p)[None, :] + g, axis=1).astype(np.int32)
+
+
+def chi2_p(counts, probs):
+    counts = np.asarray(counts, np.float64)
+    probs = np.asarray(probs, np.float64)
+    keep = probs > 0
+    assert counts[~keep].sum() == 0, "mass on a zero-probability outcome"
+    exp = probs[keep] * counts.sum()
+    stat = ((counts[keep] - exp) ** 2 / exp).sum()
+    return stats.chi2.sf(stat, keep.sum() - 1)
+
+
+def f32(x):
+    """The float32 value the oracle will see, back in float64."""
+    return np.asarray(x, np.float32).astype(np.float64)
+
+
+def tile_rows(rows, B):
+    rows = np.asarray(rows, np.float32)
+    return np.ascontiguousarray(np.broadcast_to(rows, (B,) + rows.shape))
+
+
+# ------------------------------------------- "01 · Draft-then-verify" 2.2
+def test_beta_closed_form_and_empirical_accept_rate():
+    """beta = sum min(p, q) = 1 - TV (section 2.2); the oracle's empirical
+    acceptance of position 0, with x ~ q, is beta within 5 sigma, and the
+    residual mass equals 1 - beta (2.1 derivation)."""
+    rng = np.random.default_rng(1)
+    V, B = 8, 1_000_000
+    zt = f32(rng.normal(0, 1.5, V))
+    zd = f32(zt + rng.normal(0, 1.0, V))
+    p, q = softmax(zt), softmax(zd)
+    beta = np.minimum(p, q).sum()
+    assert abs(beta - (1 - 0.5 * np.abs(p - q).sum())) < 1e-12
+    x = draw_from(q, B, 2)[:, None]
+    u = synth.uniforms(3, (B, 2))
+    target = tile_rows([zt, zt], B)
+    draft = tile_rows([zd], B)
+    out = oracle.verify_linear(target, draft, x, u, 1.0)
+    rate = (out["n"] == 1).mean()
+    sd = math.sqrt(beta * (1 - beta) / B)
+    assert abs(rate - beta) < 5 * sd
+    # one sequence with out_resid: residual weights sum to 1 - beta before
+    # normalisation, i.e. the normalised residual times (1-beta) is max(0,p-q)
+    o1 = oracle.verify_linear(target[:1], draft[:1], np.array([[0]]),
+                              np.array([[0.999999, 0.5]], np.float32), 1.0,
+                              want_resid=True)
+    if o1["n"][0] == 0:
+        np.testing.assert_allclose(o1["resid"][0] * (1 - beta),
+                                   np.maximum(0, p - q), atol=1e-12)
+
+
+# -------------------------------- section 2.1 invariance P_alg(x) = p(x)
+@pytest.mark.parametrize("T", [1.0, 0.7])
+def test_first_token_marginal_is_p(T):
+    """The emitted token of a gamma = 1 round is distributed as p_1 for any
+    q (section 2.1, distribution invariance).  Chi-square over 1e6 trials,
+    V = 8."""
+    rng = np.random.default_rng(11)
+    V, B = 8, 1_000_000
+    zt = rng.normal(0, 2.0, V)
+    zd = rng.normal(0, 2.0, V)  # a poor drafter: q far from p
+    p, q = softmax(zt, T), softmax(zd, T)
+    x = draw_from(q, B, 12)[:, None]
+    out = oracle.verify_linear(tile_rows([zt, zt + 5], B), tile_rows([zd], B),
+                               x, synth.uniforms(13, (B, 2)), T)
+    first = out["tokens"][:, 0]
+    assert chi2_p(np.bincount(first, minlength=V), p) > P_MIN
+
+
+def test_second_token_conditional_with_prefix_dependent_target():
+    """Target rows depend on the prefix: p_2 = p(. | x_1).  Given that the
+    first emitted token is a draft a that was accepted, the second emitted
+    token is distributed as p(. | a) (2.1 applied at position 2, 2.3 prefix
+    structure)."""
+    rng = np.random.default_rng(21)
+    V, B = 6, 1_000_000
+    z1 = rng.normal(0, 1.5, V)
+    cond = rng.normal(0, 1.5, (V, V))          # row a: logits of p(. | a)
+    q1 = softmax(z1 + rng.normal(0, 0.7, V))
+    zq1 = np.log(q1)
+    zq2 = cond + rng.normal(0, 0.7, (V, V))    # q(. | a)
+    x1 = draw_from(q1, B, 22)
+    x2 = np.empty(B, np.int32)
+    for a in range(V):
+        idx = np.nonzero(x1 == a)[0]
+        x2[idx] = draw_from(softmax(zq2[a]), len(idx), 23 + a)
+    target = np.empty((B, 3, V), np.float32)
+    target[:, 0] = z1
+    target[:, 1] = cond[x1]
+    target[:, 2] = 0.0
+    draft = np.empty((B, 2, V), np.float32)
+    draft[:, 0] = zq1
+    draft[:, 1] = zq2[x1]
+    out = oracle.verify_linear(target, draft, np.stack([x1, x2], 1),
+                               synth.uniforms(24, (B, 3)), 1.0)
+    assert chi2_p(np.bincount(out["tokens"][:, 0], minlength=V),
+                  softmax(z1)) > P_MIN
+    sel = out["n"] >= 1
+    for a in range(V):
+        m = sel & (out["tokens"][:, 0] == a)
+        if m.sum() < 20000:
+            continue
+        assert chi2_p(np.bincount(out["tokens"][m, 1], minlength=V),
+                      softmax(cond[a])) > P_MIN
+
+
+# ------------------------------------------------ brute-force enumeration
+def enumerate_first_token(zt, zq, gamma):
+    """Exact distribution of the first emitted token of one round, by
+    enumerating every draft x in V^gamma and every accept/reject branch.
+    Rows do not depend on the prefix here.  Written from section 2.1: a
+    token accepted at position 1 is emitted first; if position 1 rejects,
+    the correction from norm(max(0, p1 - q1)) is emitted first."""
+    p, q = softmax(zt[0]), softmax(zq[0])
+    V = len(p)
+    dist = np.zeros(V)
+    for xs in itertools.product(range(V), repeat=gamma):
+        w = np.prod([softmax(zq[i])[xs[i]] for i in range(gamma)])
+        acc = min(1.0, p[xs[0]] / q[xs[0]])
+        dist[xs[0]] += w * acc
+        res = np.maximum(0, p - q)
+        if res.sum() > 0:
+            dist += w * (1 - acc) * res / res.sum()
+    return dist
+
+
+def enumerate_outcomes(zt, zq, gamma):
+    """Exact law of (n accepted, emitted tuple) of one round (fixed rows),
+    by enumeration over drafts and branches."""
+    V = zt.shape[1]
+    P = [softmax(zt[i]) for i in range(gamma + 1)]
+    Q = [softmax(zq[i]) for i in range(gamma)]
+    law = {}
+    for xs in itertools.product(range(V), repeat=gamma):
+        w = np.prod([Q[i][xs[i]] for i in range(gamma)])
+        reach = w
+        for i in range(gamma):
+            acc = min(1.0, P[i][xs[i]] / Q[i][xs[i]])
+            res = np.maximum(0, P[i] - Q[i])
+            if res.sum() > 0 and acc < 1:
+                for t in range(V):
+                    key = (i, xs[:i] + (t,))
+                    law[key] = law.get(key, 0) + reach * (1 - acc) * \
+                        res[t] / res.sum()
+            reach *= acc
+        for t in range(V):
+            key = (gamma, xs + (t,))
+            law[key] = law.get(key, 0) + reach * P[gamma][t]
+    return law
+
+
+@pytest.mark.parametrize("V,gamma", [(3, 3), (5, 2), (6, 1)])
+def test_bruteforce_enumeration(V, gamma):
+    """Enumeration gives p_1 exactly for the first token (to 1e-12); the
+    oracle's sampled (n, tokens) frequencies follow the enumerated law."""
+    rng = np.random.default_rng(100 + V)
+    zt = rng.normal(0, 1.2, (gamma + 1, V))
+    zq = zt[:gamma] + rng.normal(0, 1.0, (gamma, V))
+    first = enumerate_first_token(zt, zq, gamma)
+    np.testing.assert_allclose(first, softmax(zt[0]), atol=1e-12)
+    law = enumerate_outcomes(zt, zq, gamma)
+    assert abs(sum(law.values()) - 1) < 1e-12
+    B = 400_000
+    xs = np.stack([draw_from(softmax(zq[i]), B, 200 + i)
+                   for i in range(gamma)], 1)
+    out = oracle.verify_linear(tile_rows(zt, B), tile_rows(zq, B), xs,
+                               synth.uniforms(300 + V, (B, gamma + 1)), 1.0)
+    keys = list(law)
+    index = {k: i for i, k in enumerate(keys)}
+    counts = np.zeros(len(keys))
+    for n, toks in zip(out["n"], out["tokens"]):
+        counts[index[(int(n), tuple(int(t) for t in toks[:n + 1]))]] += 1
+    assert chi2_p(counts, [law[k] for k in keys]) > P_MIN
+
+
+# ------------------------------- accepted-length law (iid alpha) 3 / SpecBranch
+def test_truncated_geometric_length_law():
+    """With identical (p, q) at every position the accepted count is
+    truncated-geometric: P(n=k) = (1-a) a^k for k < gamma, a^gamma at gamma
+    (SpecBranch, background); the mean emitted count is
+    (1 - a^{gamma+1}) / (1 - a) ("01 · Draft-then-verify", section 3)."""
+    rng = np.random.default_rng(31)
+    V, gamma, B = 8, 5, 1_000_000
+    zt = rng.normal(0, 1.5, V)
+    zd = zt + rng.normal(0, 0.8, V)
+    p, q = softmax(zt), softmax(zd)
+    a = np.minimum(p, q).sum()
+    xs = np.stack([draw_from(q, B, 40 + i) for i in range(gamma)], 1)
+    out = oracle.verify_linear(tile_rows([zt] * (gamma + 1), B),
+                               tile_rows([zd] * gamma, B), xs,
+                               synth.uniforms(41, (B, gamma + 1)), 1.0)
+    law = [(1 - a) * a ** k for k in range(gamma)] + [a ** gamma]
+    assert chi2_p(np.bincount(out["n"], minlength=gamma + 1), law) > P_MIN
+    mean = (out["n"] + 1).mean()
+    expect = (1 - a ** (gamma + 1)) / (1 - a)
+    sd = np.sqrt(np.sum(np.array(law) * (np.arange(gamma + 1) + 1) ** 2)
+                 - expect ** 2) / np.sqrt(B)
+    assert abs(mean - expect) < 5 * sd
+
+
+# ------------------------------------------------------ greedy (2.2)
+def test_greedy_is_id_equality_with_argmax():
+    """T = 0: accept iff the draft id equals argmax p (section 2.2), ties to
+    the lowest index; the correction/bonus is argmax of row n.  Compared with
+    numpy's argmax on the same bf16 values, including rows with ties."""
+    rng = np.random.default_rng(51)
+    B, gamma, V = 4000, 4, 40
+    z = rng.integers(-6, 7, (B, gamma + 1, V)).astype(np.float32)  # ties
+    import torch
+    bits = synth.bf16_bits(torch.from_numpy(z).to(torch.bfloat16))
+    am = np.argmax(z, axis=2)
+    # drafts: the argmax with probability 0.7 each, else a random id
+    xs = np.where(rng.random((B, gamma)) < 0.7, am[:, :gamma],
+                  rng.integers(0, V, (B, gamma))).astype(np.int32)
+    out = oracle.verify_linear(bits, None, xs,
+                               np.full((B, gamma + 1), 0.5, np.float32), 0.0)
+    match = xs == am[:, :gamma]
+    n_ref = np.where(match.all(1), gamma, np.argmin(match, axis=1))
+    np.testing.assert_array_equal(out["n"], n_ref)
+    t_ref = am[np.arange(B), n_ref]
+    np.testing.assert_array_equal(out["tokens"][np.arange(B), n_ref], t_ref)
+    assert np.all(out["prob"] == 1.0)
+    assert np.all(np.isinf(out["margin"]))
+
+
+# ------------------------------------------ worked examples (golden files)
+def _golden(name):
+    import json
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", name)
+    with open(path) as f:
+        return json.load(f)
+
+
+def test_worked_residual_examples():
+    """Hand-worked single-step examples of section 2.1 (accept probability
+    min(1, p/q), residual norm(max(0, p - q))), stored in
+    tests/golden/single_step_examples.json."""
+    for ex in _golden("single_step_examples.json")["cases"]:
+        p = np.array(ex["p"])
+        q = np.array(ex["q"])
+        tgt = np.log(np.stack([p, p])).astype(np.float32)[None]
+        drf = np.log(q).astype(np.float32)[None, None]
+        x = np.array([[ex["x"]]], np.int32)
+        for r, u, n, t in ex["draws"]:
+            o = oracle.verify_linear(tgt, drf, x,
+                                     np.array([[r, u]], np.float32), 1.0,
+                                     want_resid=True)
+            assert o["n"][0] == n and o["tokens"][0, n] == t, (ex, r, u)
+            if n == 0:
+                np.testing.assert_allclose(o["resid"][0], ex["residual"],
+                                           atol=1e-6)
+            np.testing.assert_allclose(o["accept"][0, 0], ex["accept"],
+                                       atol=1e-6)
+
+
+# ----------------------------------------- kcand (SpecDiff-2 self-selection)
+def test_kcand_one_candidate_equals_linear():
+    c = synth.kcand_case(64, 1, 5, 300, T=1.0, seed=5)
+    tg = synth.host_logits(c.target)
+    dr = synth.host_logits(c.draft)
+    ok = oracle.verify_kcand(tg, dr, c.tokens.numpy(), c.uniforms.numpy(), 1.0)
+    ol = oracle.verify_linear(tg[:, 0], dr, c.tokens.numpy()[:, 0],
+                              c.uniforms.numpy()[:, 0], 1.0)
+    np.testing.assert_array_equal(ok["n"], ol["n"])
+    np.testing.assert_array_equal(ok["tokens"], ol["tokens"])
+    np.testing.assert_array_equal(ok["prob"], ol["prob"])
+    assert np.all(ok["k"] == 0)
+
+
+def test_kcand_selection_is_max_streak_lowest_k():
+    c = synth.kcand_case(200, 6, 6, 200, T=1.0, seed=6, sigma_k=1.0)
+    o = oracle.verify_kcand(synth.host_logits(c.target),
+                            synth.host_logits(c.draft), c.tokens.numpy(),
+                            c.uniforms.numpy(), 1.0)
+    npc = o["n_per_cand"]
+    np.testing.assert_array_equal(o["n"], npc.max(1))
+    np.testing.assert_array_equal(o["k"], np.argmax(npc, axis=1))
+    toks = c.tokens.numpy()
+    for b in range(200):
+        n, k = o["n"][b], o["k"][b]
+        np.testing.assert_array_equal(o["tokens"][b, :n], toks[b, k, :n])
+        assert o["tokens"][b, n] >= 0 and np.all(o["tokens"][b, n + 1:] == -1)
+
+
+def test_kcand_max_streak_law_bruteforce():
+    """Candidates are independent given the marginals, so with fixed rows
+    P(n_sel >= m) = 1 - prod_k (1 - P(n_k >= m)), P(n_k >= m) = prod_{j<m}
+    beta_{k,j}, beta = sum min(p, q) (section 2.2)."""
+    rng = np.random.default_rng(61)
+    V, K, gamma, B = 6, 3, 3, 300_000
+    zq = rng.normal(0, 1.2, (gamma, V))
+    zt = zq[None, :, :] + rng.normal(0, 0.9, (K, gamma, V))
+    zt = np.concatenate([zt, rng.normal(0, 1, (K, 1, V))], 1)
+    beta = np.array([[np.minimum(softmax(zt[k, j]), softmax(zq[j])).sum()
+                      for j in range(gamma)] for k in range(K)])
+    xs = np.stack([np.stack([draw_from(softmax(zq[j]), B, 70 + 10 * k + j)
+                             for j in range(gamma)], 1) for k in range(K)], 1)
+    o = oracle.verify_kcand(tile_rows(zt, B), tile_rows(zq, B), xs,
+                            synth.uniforms(71, (B, K, gamma + 1)), 1.0)
+    for m in range(1, gamma + 1):
+        pk = np.prod(beta[:, :m], axis=1)
+        expect = 1 - np.prod(1 - pk)
+        got = (o["n"] >= m).mean()
+        assert abs(got - expect) < 5 * math.sqrt(expect * (1 - expect) / B)
+
+
+def test_kcand_selection_bias_counterexample():
+    """Longest-streak selection is not lossless for K > 1: V = 2,
+    p = (1/2, 1/2), both candidates draft token 0 with q = delta_0.  Each
+    candidate accepts with probability 1/2, the selection keeps an accepted
+    one unless both reject, so the first token is 0 with probability 3/4."""
+    B = 400_000
+    zt = np.zeros((2, 2, 2), np.float32)             # [K, gamma+1, V]
+    zq = np.array([[0.0, -np.inf]], np.float32)      # q = delta_0
+    xs = np.zeros((B, 2, 1), np.int32)
+    o = oracle.verify_kcand(tile_rows(zt, B), tile_rows(zq, B), xs,
+                            synth.uniforms(81, (B, 2, 2)), 1.0)
+    frac0 = (o["tokens"][:, 0] == 0).mean()
+    assert abs(frac0 - 0.75) < 5 * math.sqrt(0.75 * 0.25 / B)
+
+
+# ------------------------------------------------------------- tree
+def chain_tree_from_linear(tg, dr, xs, u):
+    """Rearrange a linear case as a one-child-per-node tree."""
+    B, G1, V = tg.shape
+    gamma = G1 - 1
+    ttree = tg
+    dtree = np.concatenate([dr, np.zeros((B, 1, V), dr.dtype)], 1)
+    parent = np.tile(np.arange(-1, gamma, dtype=np.int32), (B, 1))
+    ntok = np.concatenate([np.full((B, 1), -1, np.int32), xs], 1)
+    U = np.concatenate([u[:, gamma:gamma + 1], u[:, :gamma]], 1)
+    return ttree, dtree, parent, ntok, U
+
+
+@pytest.mark.parametrize("T", [0.0, 1.0])
+def test_tree_chain_equals_linear(T):
+    c = synth.linear_case(300, 5, 257, T=T, seed=91)
+    tg, dr = synth.host_logits(c.target), synth.host_logits(c.draft)
+    xs, u = c.tokens.numpy(), c.uniforms.numpy()
+    ol = oracle.verify_linear(tg, dr, xs, u, T)
+    ot = oracle.verify_tree(*chain_tree_from_linear(tg, dr, xs, u), T)
+    np.testing.assert_array_equal(ot["n"], ol["n"])
+    np.testing.assert_array_equal(ot["tokens"][:, :6], ol["tokens"])
+    # the tree renormalises before drawing, the chain after: same value up
+    # to the last bits
+    np.testing.assert_allclose(ot["prob"], ol["prob"], rtol=1e-12)
+    for b in range(300):
+        np.testing.assert_array_equal(ot["nodes"][b, :ol["n"][b]],
+                                      np.arange(1, ol["n"][b] + 1))
+
+
+def test_tree_iid_siblings_lossless():
+    """Siblings drawn iid from the parent's q, tried in turn with
+    p <- norm(max(0, p - q)) after each rejection, keep the emitted token's
+    marginal equal to p (the 2.1 argument applied repeatedly).  Chi-square,
+    V = 8, three siblings under the root, 1e6 trials."""
+    rng = np.random.default_rng(95)
+    V, S, B = 8, 3, 1_000_000
+    zt = rng.normal(0, 1.5, V)
+    zq = zt + rng.normal(0, 1.2, V)
+    N = S + 1
+    tg = tile_rows([zt] + [rng.normal(0, 1, V)] * S, B)
+    dr = tile_rows([zq] + [np.zeros(V)] * S, B)
+    parent = np.tile(np.array([-1] + [0] * S, np.int32), (B, 1))
+    kids = np.stack([draw_from(softmax(zq), B, 96 + s) for s in range(S)], 1)
+    ntok = np.concatenate([np.full((B, 1), -1, np.int32), kids], 1)
+    o = oracle.verify_tree(tg, dr, parent, ntok,
+                           synth.uniforms(97, (B, N)), 1.0)
+    assert chi2_p(np.bincount(o["tokens"][:, 0], minlength=V),
+                  softmax(zt)) > P_MIN
+
+
+def test_tree_scalar_c_closed_form():
+    """The iterated residual p <- norm(max(0, p - q)) equals
+    max(0, p - c_k q) / N_k with c_0 = 0, c_{k+1} = c_k + N_k and
+    N_k = sum max(0, p - c_k q): the closed form the CUDA tree walk uses.
+    Checked numerically in double against the literal iteration."""
+    rng = np.random.default_rng(98)
+    for _ in range(200):
+        V = rng.integers(2, 60)
+        p = softmax(rng.normal(0, 2, V))
+        q = softmax(rng.normal(0, 2, V))
+        it = p.copy()
+        c = 0.0
+        for _k in range(6):
+            res = np.maximum(0, p - c * q)
+            Nk = res.sum()
+            if Nk <= 1e-12:
+                break
+            np.testing.assert_allclose(it, res / Nk, atol=1e-12)
+            nxt = np.maximum(0, it - q)
+            if nxt.sum() <= 1e-12:
+                break
+            it = nxt / nxt.sum()
+            c = c + Nk
+
+
+def test_tree_topk_sibling_counterexample():
+    """Deterministic top-k siblings are not lossless: V = 2, q = (1/2, 1/2),
+    p = (0.9, 0.1), children tokens 0 then 1: the first child has
+    p/q = 1.8 and is always accepted, so the first token is always 0."""
+    B = 10000
+    zt = np.log(np.array([[0.9, 0.1], [0.5, 0.5], [0.5, 0.5]]))
+    zq = np.zeros((3, 2))
+    parent = np.tile(np.array([-1, 0, 0], np.int32), (B, 1))
+    ntok = np.tile(np.array([-1, 0, 1], np.int32), (B, 1))
+    o = oracle.verify_tree(tile_rows(zt, B), tile_rows(zq, B), parent, ntok,
+                           synth.uniforms(99, (B, 3)), 1.0)
+    assert np.all(o["tokens"][:, 0] == 0) and np.all(o["nodes"][:, 0] == 1)
+
+
+def test_tree_greedy_follows_argmax_child():
+    c = synth.tree_case(20, 24, 50, dtype=__import__("torch").float32, T=0.0,
+                        seed=100)
+    tg = synth.host_logits(c.target)
+    o = oracle.verify_tree(tg, synth.host_logits(c.draft), c.parent.numpy(),
+                           c.node_tokens.numpy(), c.uniforms.numpy(), 0.0)
+    par, tok = c.parent.numpy(), c.node_tokens.numpy()
+    for b in range(20):
+        cur, path = 0, []
+        while True:
+            a = int(np.argmax(tg[b, cur]))
+            nxt = [v for v in range(1, 24) if par[b, v] == cur and
+                   tok[b, v] == a]
+            if not nxt:
+                break
+            cur = nxt[0]
+            path.append(cur)
+        assert o["n"][b] == len(path)
+        np.testing.assert_array_equal(o["nodes"][b, :len(path)], path)
+        assert o["tokens"][b, len(path)] == a
+
+
+def test_tree_invalid_parent_flagged():
+    c = synth.tree_case(3, 8, 30, dtype=__import__("torch").float32, seed=101)
+    par = c.parent.numpy().copy()
+    par[1, 5] = 6          # parent after child
+    par[2, 0] = 0          # root with a parent
+    o = oracle.verify_tree(synth.host_logits(c.target),
+                           synth.host_logits(c.draft), par,
+                           c.node_tokens.numpy(), c.uniforms.numpy(), 0.8)
+    assert o["n"][0] >= 0 and o["status"][0] & oracle.ST_BAD_PARENT == 0
+    for b in (1, 2):
+        assert o["n"][b] == -1 and o["status"][b] & oracle.ST_BAD_PARENT
+
+
+# ------------------------------------------------------- fan-out (Saguaro)
+def bruteforce_fanout(K, budget, a, r):
+    """Integer maximiser of the power-law hit rate sum_k P(k) (1 - F_k^-r),
+    P(k) = (1-a) a^k for k < K and a^K for k = K (Definition 11, the capped
+    geometric law of the verify length), by greedy marginal gain from
+    F_k = 1 (the objective is separable and concave in each F_k)."""
+    P = [(1 - a) * a ** k for k in range(K)] + [a ** K]
+    F = [1] * (K + 1)
+    for _ in range(budget - (K + 1)):
+        gain = [P[k] * (F[k] ** -r - (F[k] + 1) ** -r) for k in range(K + 1)]
+        F[int(np.argmax(gain))] += 1
+    return F
+
+
+def test_fanout_schedule_golden_and_theorem12():
+    g = _golden("fanout_schedule.json")
+    for case in g["cases"]:
+        K, B, a, r = case["K"], case["budget"], case["a"], case["r"]
+        F = oracle.fanout_schedule(K, B, a, r)
+        assert F.sum() == B
+        assert list(F) == case["F"]
+        assert list(F) == bruteforce_fanout(K, B, a, r)
+    # Theorem 12 ratios of the real-valued schedule: F_{k+1}/F_k =
+    # a^{1/(1+r)}; the capped last position has the extra (1-a)^{-1/(1+r)}.
+    # With a huge budget the rounding is negligible.
+    K, a, r = 6, 0.7, 1.5
+    F = oracle.fanout_schedule(K, 10 ** 7, a, r).astype(np.float64)
+    ratio = a ** (1 / (1 + r))
+    np.testing.assert_allclose(F[1:K] / F[:K - 1], ratio, rtol=1e-5)
+    np.testing.assert_allclose(F[K] / F[K - 1],
+                               ratio * (1 - a) ** (-1 / (1 + r)), rtol=1e-5)
+
+
+def test_fanout_topk_against_stable_sort_and_ties():
+    import torch
+    rng = np.random.default_rng(111)
+    B, K, V = 7, 3, 500
+    z = rng.integers(-20, 20, (B, K + 1, V)).astype(np.float32) / 4  # ties
+    z[0, 0, :] = 0.0
+    z[0, 0, ::3] = -0.0                     # -0 equals +0
+    F = np.array([5, 3, 0, 9], np.int32)
+    for host in (z, synth.bf16_bits(torch.from_numpy(z).to(torch.bfloat16))):
+        o = oracle.fanout_topk(host, F)
+        off = 0
+        for k in range(K + 1):
+            for b in range(B):
+                order = np.lexsort((np.arange(V), -z[b, k]))[:F[k]]
+                np.testing.assert_array_equal(
+                    o["tokens"][b, off:off + F[k]], order)
+            off += F[k]
