@@ -1,0 +1,347 @@
+"""Benchmark of the verify step on the large-batch workload.
+
+Workload (one "step" = one verify round over the whole batch):
+  B = 256 sequences, gamma = 8 drafts, V = 128256 (LLaMA-3 vocabulary),
+  fp32 logits; target ~ N(0, 3^2), draft = target + N(0, 1); draft tokens
+  drawn from softmax(draft / T); T = 1.0; uniforms from splitmix64.
+  Geometric fan-out a = 0.8, r = 1, K = 8, budget 64 -> F = [10,9,8,7,6,6,
+  5,4,9] on the 9 draft rows when the fused call is available.
+
+Prints one JSON line (rank 0).  `--impl reference` times the fp64 CPU
+oracle on the same workload instead (the only reference this method has).
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from speculative_decoding_verification_temperature_gb300 import synth  # noqa
+
+METRIC = ("verify rounds/s and achieved HBM GB/s over logits vs ~8 TB/s "
+          "roofline (1 GB300)")
+B, GAMMA, V, T = 256, 8, 128256, 1.0
+FAN = dict(K=8, budget=64, a=0.8, r=1.0)
+ELT = 4
+WORKLOAD = ("large-batch verify + fan-out: B=256, gamma=8, V=128256, fp32, "
+            "T=1.0, fan-out a=0.8 r=1 K=8 budget=64")
+FALLBACK_HBM = 6800.0
+
+
+# ------------------------------------------------------------ clocks
+class ClockSampler:
+    """Samples SM clock and throttle reasons through NVML (ctypes) every
+    ~2 ms while running; reading only, no setting is touched."""
+    REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown",
+               0x20: "sw_thermal_slowdown", 0x4: "sw_power_cap",
+               0x80: "hw_power_brake_slowdown", 0x1: "gpu_idle"}
+
+    def __init__(self, index=0):
+        self.ok = False
+        self.samples = []
+        try:
+            self.nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nv.nvmlInit_v2() != 0:
+                return
+            self.h = ctypes.c_void_p()
+            if self.nv.nvmlDeviceGetHandleByIndex_v2(
+                    ctypes.c_uint(index), ctypes.byref(self.h)) != 0:
+                return
+            self.ok = True
+            mx = ctypes.c_uint()
+            self.nv.nvmlDeviceGetMaxClockInfo(self.h, ctypes.c_uint(1),
+                                              ctypes.byref(mx))
+            self.max_mhz = mx.value
+        except OSError:
+            pass
+
+    def _read(self):
+        c = ctypes.c_uint()
+        r = ctypes.c_ulonglong()
+        self.nv.nvmlDeviceGetClockInfo(self.h, ctypes.c_uint(1),
+                                       ctypes.byref(c))
+        self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h,
+                                                       ctypes.byref(r))
+        return c.value, r.value
+
+    def start(self):
+        self.samples = []
+        self._stop = threading.Event()
+        if not self.ok:
+            return
+        def loop():
+            while not self._stop.is_set():
+                self.samples.append(self._read())
+                time.sleep(0.002)
+        self.t = threading.Thread(target=loop, daemon=True)
+        self.t.start()
+
+    def stop(self):
+        if not self.ok:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
+                    "source": "unavailable"}
+        self._stop.set()
+        self.t.join()
+        mhz = [s[0] for s in self.samples] or [0]
+        reasons = set()
+        for _, r in self.samples:
+            for bit, name in self.REASONS.items():
+                if r & bit and name != "gpu_idle":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(reasons), "samples": len(self.samples),
+                "source": "nvml"}
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM, "fallback"
+
+
+def needed_bytes(n, gamma, V, elt):
+    """Logit bytes the method must read for one round: target rows 0..n and
+    draft rows 0..min(n, gamma-1) of every sequence."""
+    n = np.asarray(n, np.int64)
+    rows = (n + 1) + np.minimum(n + 1, gamma)
+    return int(rows.sum()) * V * elt
+
+
+# ---------------------------------------------------------- GPU arm
+def make_sets(nsets, device):
+    sets = []
+    for s in range(nsets):
+        c = synth.large(s, device=device)
+        c.draft_v = c.draft[:, :GAMMA].contiguous()
+        sets.append(c)
+    return sets
+
+
+def gpu_arm(args, rank, world):
+    from speculative_decoding_verification_temperature_gb300 import api
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    sets = make_sets(args.sets, dev)
+    stream = torch.cuda.current_stream(dev)
+    ws = api.Workspace()
+
+    def step(c):
+        return api.verify_linear(c.target, c.draft_v, c.tokens, c.uniforms,
+                                 T, workspace=ws)
+
+    # bytes the method needs per set (deterministic outputs)
+    need = []
+    for c in sets:
+        o = step(c)
+        need.append(needed_bytes(o["n"].cpu().numpy(), GAMMA, V, ELT))
+    for i in range(args.warmup):
+        step(sets[i % len(sets)])
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = ClockSampler(dev.index or 0)
+    clocks.start()
+    ev = [(torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step(sets[i % len(sets)])
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    clk = clocks.stop()
+    per = [a.elapsed_time(b) for a, b in ev]   # ms per step (device)
+    total_ms = sum(per)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms = total_ms / args.steps
+    rounds_s = world * args.steps / (total_ms / 1e3)
+    need_avg = sum(need[i % len(sets)] for i in range(args.steps)) / args.steps
+    tensor_bytes = B * (2 * GAMMA + 1) * V * ELT
+    peak, src = hbm_peak()
+    achieved = need_avg / (ms / 1e3) / 1e9
+    res = {
+        "metric": METRIC, "value": rounds_s, "unit": "rounds/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": B, "gamma": GAMMA, "V": V,
+                   "T": T, "input_sets": len(sets),
+                   "l2": "inputs %.2f GB per set (> 129 MB L2), %d sets "
+                         "rotated" % (2 * tensor_bytes / 1e9, len(sets)),
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": None,
+                     "peak_source": "MEASURED_PEAKS.json hbm_gbs (%s)" % src,
+                     "kernel": "linear_verify_kernel<0,4,false>",
+                     "bytes_per_launch": need_avg,
+                     "full_tensor_bytes": tensor_bytes,
+                     "median_ms": statistics.median(per)},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+        "wall_s": wall,
+    }
+    res["e2e"] = e2e_arm(args, sets, dev, ws, world)
+    if rank == 0:
+        res["cpu_baseline"] = cpu_baseline(sets, args.oracle_seqs)
+    return res
+
+
+def e2e_arm(args, sets, dev, ws, world):
+    """Same metric through the public API with host buffers: per step the
+    pinned-host inputs are copied to the device, verified, and the results
+    copied back."""
+    from speculative_decoding_verification_temperature_gb300 import api
+    c = sets[0]
+    h = {k: getattr(c, k).cpu().pin_memory()
+         for k in ("target", "draft_v", "tokens", "uniforms")}
+    d = {k: torch.empty_like(v, device=dev) for k, v in h.items()}
+    out_h = {"n": torch.empty(B, dtype=torch.int32).pin_memory(),
+             "tokens": torch.empty((B, GAMMA + 1),
+                                   dtype=torch.int32).pin_memory(),
+             "prob": torch.empty(B, dtype=torch.float32).pin_memory()}
+    stream = torch.cuda.current_stream(dev)
+    steps = max(3, min(args.steps, args.e2e_steps))
+
+    def step():
+        for k in h:
+            d[k].copy_(h[k], non_blocking=True)
+        o = api.verify_linear(d["target"], d["draft_v"], d["tokens"],
+                              d["uniforms"], T, workspace=ws)
+        for k in out_h:
+            out_h[k].copy_(o[k], non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(
+        enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b)
+    h2d = sum(v.numel() * v.element_size() for v in h.values())
+    d2h = sum(v.numel() * v.element_size() for v in out_h.values())
+    return {"value": world * steps / (ms / 1e3), "unit": "rounds/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": steps}
+
+
+# --------------------------------------------------------- CPU oracle
+def oracle_sample(c, seqs):
+    import oracle
+    t = synth.host_logits(c.target[seqs])
+    d = synth.host_logits(c.draft[seqs, :GAMMA])
+    tk = c.tokens[seqs].cpu().numpy()
+    u = c.uniforms[seqs].cpu().numpy()
+    t0 = time.perf_counter()
+    oracle.verify_linear(t, d, tk, u, T)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(sets, nseq):
+    seqs = list(range(nseq))
+    dt = oracle_sample(sets[0], seqs)
+    per_round = dt / nseq * B
+    return {"value": 1.0 / per_round, "unit": "rounds/s", "cores": 1,
+            "kind": "oracle",
+            "sample": "fp64 C oracle, single thread, on %d of the %d "
+                      "sequences of one round (%.1f s), scaled to a full "
+                      "round" % (nseq, B, dt)}
+
+
+def reference_arm(args):
+    """The oracle as the reference arm: each step verifies one sequence of
+    the workload on the host (cycling through the batch); rounds/s is
+    scaled from the mean time per sequence."""
+    import oracle
+    oracle.build()
+    c = synth.large(0, device="cuda" if torch.cuda.is_available() else "cpu")
+    t_all = synth.host_logits(c.target)
+    d_all = synth.host_logits(c.draft[:, :GAMMA])
+    tk = c.tokens.cpu().numpy()
+    u = c.uniforms.cpu().numpy()
+    del c
+
+    def step(i):
+        b = i % B
+        oracle.verify_linear(t_all[b:b + 1], d_all[b:b + 1], tk[b:b + 1],
+                             u[b:b + 1], T)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    dt = time.perf_counter() - t0
+    per_seq = dt / args.steps
+    value = 1.0 / (per_seq * B)
+    cores = 1
+    sample = ("fp64 C oracle, single thread; each step verifies one of the "
+              "%d sequences of a round; rounds/s = 1 / (B x mean time per "
+              "sequence)" % B)
+    return {"metric": METRIC, "value": value, "unit": "rounds/s",
+            "impl": "reference", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": per_seq * 1e3,
+            "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "B": B, "gamma": GAMMA,
+                       "V": V, "T": T},
+            "cpu_baseline": {"value": value, "unit": "rounds/s",
+                             "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "rounds/s",
+                    "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="native",
+                    choices=["native", "reference"])
+    ap.add_argument("--sets", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--oracle-seqs", type=int, default=16)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(reference_arm(args)))
+        return
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    res = gpu_arm(args, rank, world)
+    if rank == 0:
+        print(json.dumps(res))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

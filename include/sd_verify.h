@@ -1,0 +1,227 @@
+/*
+ * sd_verify.h -- C ABI of the GB300 (sm_103a) verify step of speculative
+ * decoding ("draft-then-verify" at temperature T).
+ *
+ * What is computed (citations are to the pages this library implements):
+ *
+ *  - "01 · Draft-then-verify" (llm-infra-atlas), section 1, Algorithm 1 and
+ *    section 4, the spec_step listing: for each sequence, with p_i the target
+ *    distribution and q_i the draft distribution at position i, draw r_i and
+ *    accept draft token x_i iff r_i <= p_i(x_i) / q_i(x_i), scanning left to
+ *    right and stopping at the first rejection; a rejection at position n
+ *    emits a correction drawn from norm(max(0, p_n - q_n)) (section 2.1);
+ *    when all gamma drafts are accepted a bonus token is drawn from p_gamma
+ *    (0-based).  Temperature reduces to sampling softmax(z / T) (section 1,
+ *    notation); T == 0 is greedy: accept iff x_i == argmax p_i (section 2.2).
+ *  - SpecDiff-2 (MLSys 2026), "core method", self-selection acceptance: K
+ *    candidate drafts sampled from shared position-wise marginals; all are
+ *    verified and the one with the longest accepted streak is kept.
+ *  - PRESTO, section 2.1 (tree-based speculative decoding): a token tree is
+ *    verified prefix-wise from the root; siblings are tried in turn with
+ *    p <- norm(max(0, p - q)) after each rejection.
+ *  - Speculative Speculative Decoding / Saguaro, "speculation cache
+ *    strategy", Theorem 12: geometric fan-out F_k = F_0 a^{k/(1+r)} (k < K),
+ *    F_K = F_0 a^{K/(1+r)} (1-a)^{-1/(1+r)}, sum F_k = budget; the cache holds
+ *    the top-F_k draft tokens of each lookahead position k.
+ *
+ * Conventions shared by every call:
+ *  - Every tensor argument is a DEVICE pointer owned by the caller, row-major
+ *    and contiguous, unless marked "host".  The library never allocates,
+ *    frees or synchronises inside a verify call; all work is enqueued on
+ *    `stream` (a cudaStream_t; NULL is the legacy default stream).
+ *  - Logits are fp32 (SD_F32) or bf16 (SD_BF16); all arithmetic is fp32.
+ *  - Uniform numbers are inputs, each in (0, 1).
+ *  - The return value reports host-side validation and launch errors only;
+ *    it is SD_OK when the work was enqueued.  Problems found in the data
+ *    are reported by OR-ing SD_DEV_* bits into *dev_status (nullable, a
+ *    device int32 the caller zeroes) and by the per-sequence outputs
+ *    described below.  Kernels never trap.
+ *  - Workspace: a device buffer of at least the size the matching
+ *    *_workspace() query returns (may be NULL when that size is 0).  It
+ *    holds a work-queue counter that each call resets on its stream, so two
+ *    calls that may overlap on the GPU must not share a workspace.
+ *  - Only sm_103 devices are supported; other devices get
+ *    SD_ERR_UNSUPPORTED.  There is no fallback path.
+ *  - sd_last_error() returns a short thread-local text for the last failed
+ *    call of this thread.
+ */
+#ifndef SD_VERIFY_H
+#define SD_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SD_OK = 0,
+  SD_ERR_INVALID_ARG = 1, /* null pointer, bad size, T < 0 or NaN, ... */
+  SD_ERR_UNSUPPORTED = 2, /* not an sm_103 device, or a size beyond a limit */
+  SD_ERR_CUDA = 3         /* a CUDA runtime call failed */
+} sd_status;
+
+typedef enum { SD_F32 = 0, SD_BF16 = 1 } sd_dtype;
+
+/* device status bits */
+#define SD_DEV_BAD_TOKEN 1  /* a draft token outside [0, V): that test rejects */
+#define SD_DEV_NONFINITE 2  /* a row read held NaN or +inf, or only -inf:
+                               the sequence's outputs are -1 */
+#define SD_DEV_BAD_PARENT 4 /* tree: parent[0] != -1 or parent[v] not in
+                               [0, v): the tree's outputs are -1 */
+#define SD_DEV_ZERO_MASS 8  /* a residual had zero mass: drawn from p instead */
+
+/* Limits (SD_ERR_UNSUPPORTED beyond them). */
+#define SD_MAX_V (1 << 24)     /* vocabulary size */
+#define SD_MAX_GAMMA 64        /* draft length (linear, kcand) */
+#define SD_MAX_K 32            /* candidates (kcand); lookahead positions - 1 (fan-out) */
+#define SD_MAX_TREE_NODES 1024 /* nodes per tree */
+#define SD_MAX_FANOUT 64       /* F_k per position */
+
+const char *sd_version(void);
+const char *sd_last_error(void);
+
+/* ---------------------------------------------------------------------
+ * Linear verify ("01 · Draft-then-verify", Algorithm 1 / spec_step).
+ *
+ * target_logits [B, gamma+1, V]: row i is the target logits p_i given the
+ *     prefix and x_0..x_{i-1}; row gamma feeds the bonus draw.
+ * draft_logits [B, gamma, V]: row i is the draft logits that produced
+ *     x_i.  May be NULL when T == 0 (greedy reads no draft logits).
+ * draft_tokens [B, gamma] int32.
+ * uniforms [B, gamma+1] float: slot i < gamma is r_i of the accept test,
+ *     slot gamma is the draw of the correction or bonus token.
+ * T: temperature, >= 0 (0 = greedy).
+ *
+ * Outputs (device):
+ *   n_accepted [B]: accepted drafts n in [0, gamma] (-1: invalid rows).
+ *   out_tokens [B, gamma+1]: x_0..x_{n-1}, then the correction/bonus
+ *       token, then -1 padding.
+ *   out_prob [B] (nullable): probability of the last token under the
+ *       distribution it was drawn from (1 when T == 0).
+ *   out_accept_prob [B, gamma] (nullable): min(1, p_i(x_i)/q_i(x_i)) of
+ *       each test made (1/0 when T == 0), -1 for positions after the first
+ *       rejection (never tested: their logits are never read).
+ *   out_resid [B, V] (nullable, debug): the normalised distribution the last
+ *       token was drawn from (one-hot when T == 0).  Costs an extra pass.
+ * The call reads only the rows the method needs: target rows 0..n, draft
+ * rows 0..min(n, gamma-1).
+ * ------------------------------------------------------------------- */
+size_t sd_verify_linear_workspace(int B, int gamma, int V, sd_dtype dt);
+
+sd_status sd_verify_linear(const void *target_logits, const void *draft_logits,
+                           sd_dtype dt, const int32_t *draft_tokens,
+                           const float *uniforms, int B, int gamma, int V,
+                           float T, int32_t *n_accepted, int32_t *out_tokens,
+                           float *out_prob, float *out_accept_prob,
+                           float *out_resid, int32_t *dev_status,
+                           void *workspace, size_t ws_bytes, void *stream);
+
+/* ---------------------------------------------------------------------
+ * K-candidate verify with verifier self-selection (SpecDiff-2, "core
+ * method").
+ *
+ * target_logits [B, K, gamma+1, V]: candidate k's own target rows.
+ * draft_logits [B, gamma, V]: the position-wise draft marginals shared by
+ *     all K candidates.
+ * draft_tokens [B, K, gamma]; uniforms [B, K, gamma+1] (slot [b][k][i] is
+ *     the accept draw of candidate k at position i; [b][k*][gamma] is the
+ *     final draw of the selected candidate).
+ * Every candidate is verified with the linear rule; k* is the candidate
+ * with the largest accepted count (lowest k on ties); the correction or
+ * bonus token is drawn for k* only.
+ * Outputs: n_accepted [B], selected_k [B], out_tokens [B, gamma+1],
+ *   n_per_cand [B, K] (nullable), out_prob [B] (nullable).
+ * This selection is not distribution-preserving for K > 1.
+ * ------------------------------------------------------------------- */
+size_t sd_verify_kcand_workspace(int B, int K, int gamma, int V, sd_dtype dt);
+
+sd_status sd_verify_kcand(const void *target_logits, const void *draft_logits,
+                          sd_dtype dt, const int32_t *draft_tokens,
+                          const float *uniforms, int B, int K, int gamma,
+                          int V, float T, int32_t *n_accepted,
+                          int32_t *selected_k, int32_t *out_tokens,
+                          int32_t *n_per_cand, float *out_prob,
+                          int32_t *dev_status, void *workspace,
+                          size_t ws_bytes, void *stream);
+
+/* ---------------------------------------------------------------------
+ * Token-tree verify (PRESTO section 2.1; sibling rule as stated above).
+ *
+ * target_logits [B, N, V]: row u is p(. | path to u).
+ * draft_logits [B, N, V]: row u is the q that drafted u's children (rows
+ *     of leaves are never read).
+ * parent [B, N] int32: parent[0] = -1, 0 <= parent[v] < v.
+ * node_tokens [B, N] int32: token of node v (slot 0 unused).
+ * uniforms [B, N] float: slot v tests node v, slot 0 is the final draw.
+ * From the root, the children of the current node are tried in increasing
+ * node index, each against the current p and the parent's draft row q;
+ * after a rejection p becomes norm(max(0, p - q)); an accepted child becomes
+ * the current node.  When no child is accepted, or at a leaf, the last token
+ * is drawn from the current p.
+ * Outputs: n_accepted [B] (accepted depth), out_tokens [B, N] (accepted
+ *   tokens then the final token, -1 padded), out_nodes [B, N] (accepted
+ *   node ids, -1 padded), out_prob [B] (nullable).
+ * ------------------------------------------------------------------- */
+size_t sd_verify_tree_workspace(int B, int N, int V, sd_dtype dt);
+
+sd_status sd_verify_tree(const void *target_logits, const void *draft_logits,
+                         sd_dtype dt, const int32_t *parent,
+                         const int32_t *node_tokens, const float *uniforms,
+                         int B, int N, int V, float T, int32_t *n_accepted,
+                         int32_t *out_tokens, int32_t *out_nodes,
+                         float *out_prob, int32_t *dev_status,
+                         void *workspace, size_t ws_bytes, void *stream);
+
+/* ---------------------------------------------------------------------
+ * Geometric fan-out schedule (Saguaro, Theorem 12).  Host only.
+ * F (host) [K+1]: F_0 w_k made integer by largest remainder (ties to the
+ * lower k); sum F == budget.  Requires 0 <= K <= SD_MAX_K, budget >= 0,
+ * 0 < a < 1, r > 0.
+ * ------------------------------------------------------------------- */
+sd_status sd_fanout_schedule(int K, int budget, double a, double r,
+                             int32_t *F);
+
+/* ---------------------------------------------------------------------
+ * Top-F_k per lookahead position (Saguaro, "speculation cache strategy").
+ *
+ * draft_logits [B, K+1, V]; F (host) [K+1], each F_k in [0, min(V,
+ * SD_MAX_FANOUT)].
+ * out_tokens [B, sum F] int32: for each k, the F_k token ids with the
+ *   largest logit of row k, ordered by (logit descending, id ascending; -0
+ *   equals +0), at offset sum_{k' < k} F_{k'}.
+ * out_logit [B, sum F] (nullable): their logits.
+ * A row holding a NaN gives -1 tokens and SD_DEV_NONFINITE.
+ * ------------------------------------------------------------------- */
+size_t sd_fanout_topk_workspace(int B, int K, int V, sd_dtype dt);
+
+sd_status sd_fanout_topk(const void *draft_logits, sd_dtype dt, int B, int K,
+                         int V, const int32_t *F, int32_t *out_tokens,
+                         float *out_logit, int32_t *dev_status,
+                         void *workspace, size_t ws_bytes, void *stream);
+
+/* ---------------------------------------------------------------------
+ * Linear verify fused with the fan-out of the same draft logits, in one
+ * pass over each draft row (the two calls above, same results).
+ *
+ * draft_logits [B, K+1, V] with K == gamma: rows 0..gamma-1 are the draft
+ * rows of the verify, all K+1 rows feed the fan-out.  Other arguments as in
+ * sd_verify_linear and sd_fanout_topk.  T must be > 0.
+ * ------------------------------------------------------------------- */
+size_t sd_verify_linear_fanout_workspace(int B, int gamma, int V,
+                                         sd_dtype dt);
+
+sd_status sd_verify_linear_fanout(
+    const void *target_logits, const void *draft_logits, sd_dtype dt,
+    const int32_t *draft_tokens, const float *uniforms, int B, int gamma,
+    int V, float T, const int32_t *F, int32_t *n_accepted,
+    int32_t *out_tokens, float *out_prob, int32_t *fan_tokens,
+    float *fan_logit, int32_t *dev_status, void *workspace, size_t ws_bytes,
+    void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SD_VERIFY_H */

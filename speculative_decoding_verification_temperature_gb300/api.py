@@ -1,0 +1,309 @@
+"""Thin torch binding over libsdverify.so (the C ABI of include/sd_verify.h).
+
+Only argument marshalling happens here: shapes and dtypes are checked, raw
+device pointers and the current CUDA stream are passed through ctypes, and
+outputs are allocated with torch.  Every step of the verify path runs in the
+library's CUDA kernels; there is no other implementation behind these
+functions, and they raise if the library cannot be loaded.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+SD_OK, SD_ERR_INVALID_ARG, SD_ERR_UNSUPPORTED, SD_ERR_CUDA = 0, 1, 2, 3
+SD_F32, SD_BF16 = 0, 1
+DEV_BAD_TOKEN, DEV_NONFINITE, DEV_BAD_PARENT, DEV_ZERO_MASS = 1, 2, 4, 8
+
+_lock = threading.Lock()
+_lib = None
+
+
+class SdError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__("sd_verify error %d: %s" % (code, msg))
+        self.code = code
+
+
+def lib() -> ctypes.CDLL:
+    """Load libsdverify.so (compiling it first if it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build()
+            if not os.path.exists(path):
+                raise RuntimeError("libsdverify.so is missing: run "
+                                   "__graft_entry__.build()")
+            L = ctypes.CDLL(path)
+            _declare(L)
+            _lib = L
+    return _lib
+
+
+def _declare(L):
+    P, I, F, D, Z = (ctypes.c_void_p, ctypes.c_int, ctypes.c_float,
+                     ctypes.c_double, ctypes.c_size_t)
+    sig = {
+        "sd_version": ([], ctypes.c_char_p),
+        "sd_last_error": ([], ctypes.c_char_p),
+        "sd_verify_linear_workspace": ([I, I, I, I], Z),
+        "sd_verify_linear": ([P, P, I, P, P, I, I, I, F, P, P, P, P, P, P, P,
+                              Z, P], I),
+        "sd_verify_kcand_workspace": ([I, I, I, I, I], Z),
+        "sd_verify_kcand": ([P, P, I, P, P, I, I, I, I, F, P, P, P, P, P, P,
+                             P, Z, P], I),
+        "sd_verify_tree_workspace": ([I, I, I, I], Z),
+        "sd_verify_tree": ([P, P, I, P, P, P, I, I, I, F, P, P, P, P, P, P,
+                            Z, P], I),
+        "sd_fanout_schedule": ([I, I, D, D, P], I),
+        "sd_fanout_topk_workspace": ([I, I, I, I], Z),
+        "sd_fanout_topk": ([P, I, I, I, I, P, P, P, P, P, Z, P], I),
+        "sd_verify_linear_fanout_workspace": ([I, I, I, I], Z),
+        "sd_verify_linear_fanout": ([P, P, I, P, P, I, I, I, F, P, P, P, P,
+                                     P, P, P, P, Z, P], I),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(L, name)
+        fn.argtypes = args
+        fn.restype = res
+
+
+def version() -> str:
+    return lib().sd_version().decode()
+
+
+def _check(rc):
+    if rc != SD_OK:
+        raise SdError(rc, lib().sd_last_error().decode())
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return SD_F32
+    if t.dtype == torch.bfloat16:
+        return SD_BF16
+    raise TypeError("logits must be float32 or bfloat16, got %s" % t.dtype)
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dev(t, device, name, dtype=None):
+    if t is None:
+        return None
+    if not t.is_cuda or t.device != device:
+        raise ValueError("%s must live on %s" % (name, device))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError("%s must be %s" % (name, dtype))
+    return t
+
+
+def _stream(device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+class Workspace:
+    """Per-device scratch buffer for the library's work-queue counter.
+    Reused across calls on the same stream; give each concurrent stream its
+    own Workspace."""
+
+    def __init__(self):
+        self._buf = {}
+
+    def get(self, device, nbytes):
+        b = self._buf.get(device)
+        if b is None or b.numel() < nbytes:
+            b = torch.empty(max(nbytes, 256), dtype=torch.uint8,
+                            device=device)
+            self._buf[device] = b
+        return b
+
+
+_default_ws = Workspace()
+
+
+def verify_linear(target, draft, tokens, uniforms, T, *, want_accept=False,
+                  want_resid=False, status=None, workspace=None, out=None):
+    """Linear verify (sd_verify_linear).
+
+    target [B, gamma+1, V], draft [B, gamma, V] (may be None when T == 0),
+    both float32 or bfloat16 on one CUDA device; tokens [B, gamma] int32;
+    uniforms [B, gamma+1] float32.  Returns a dict with n [B], tokens
+    [B, gamma+1], prob [B] (and accept [B, gamma], resid [B, V] on request).
+    ``status``: optional int32 [1] device tensor OR-ed with SD_DEV_* bits.
+    """
+    dev = target.device
+    _dev(target, dev, "target")
+    B, G1, V = target.shape
+    gamma = G1 - 1
+    if draft is not None:
+        _dev(draft, dev, "draft", target.dtype)
+        if draft.shape[0] != B or draft.shape[2] != V or \
+                draft.shape[1] != gamma:
+            raise ValueError("draft must be [B, gamma, V]")
+    tokens = _dev(tokens, dev, "tokens", torch.int32)
+    uniforms = _dev(uniforms, dev, "uniforms", torch.float32)
+    if out is None:
+        out = {}
+    n = out.get("n")
+    if n is None:
+        n = torch.empty(B, dtype=torch.int32, device=dev)
+    toks = out.get("tokens")
+    if toks is None:
+        toks = torch.empty((B, G1), dtype=torch.int32, device=dev)
+    prob = out.get("prob")
+    if prob is None:
+        prob = torch.empty(B, dtype=torch.float32, device=dev)
+    acc = torch.empty((B, max(gamma, 1)), dtype=torch.float32,
+                      device=dev) if want_accept else None
+    res = torch.empty((B, V), dtype=torch.float32,
+                      device=dev) if want_resid else None
+    L = lib()
+    nbytes = L.sd_verify_linear_workspace(B, gamma, V, _dt(target))
+    ws = (workspace or _default_ws).get(dev, nbytes)
+    _check(L.sd_verify_linear(
+        _p(target), _p(draft), _dt(target), _p(tokens), _p(uniforms), B,
+        gamma, V, float(T), _p(n), _p(toks), _p(prob), _p(acc), _p(res),
+        _p(status), _p(ws), ws.numel(), _stream(dev)))
+    r = {"n": n, "tokens": toks, "prob": prob}
+    if want_accept:
+        r["accept"] = acc[:, :gamma]
+    if want_resid:
+        r["resid"] = res
+    return r
+
+
+def verify_kcand(target, draft, tokens, uniforms, T, *, status=None,
+                 workspace=None):
+    """K-candidate verify with longest-streak selection (sd_verify_kcand).
+
+    target [B, K, gamma+1, V], draft [B, gamma, V] shared marginals, tokens
+    [B, K, gamma] int32, uniforms [B, K, gamma+1] float32.  Returns n, k,
+    tokens [B, gamma+1], n_per_cand [B, K], prob."""
+    dev = target.device
+    _dev(target, dev, "target")
+    B, K, G1, V = target.shape
+    gamma = G1 - 1
+    _dev(draft, dev, "draft", target.dtype)
+    if tuple(draft.shape) != (B, gamma, V):
+        raise ValueError("draft must be [B, gamma, V]")
+    tokens = _dev(tokens, dev, "tokens", torch.int32)
+    uniforms = _dev(uniforms, dev, "uniforms", torch.float32)
+    n = torch.empty(B, dtype=torch.int32, device=dev)
+    ks = torch.empty(B, dtype=torch.int32, device=dev)
+    toks = torch.empty((B, G1), dtype=torch.int32, device=dev)
+    npc = torch.empty((B, K), dtype=torch.int32, device=dev)
+    prob = torch.empty(B, dtype=torch.float32, device=dev)
+    L = lib()
+    nbytes = L.sd_verify_kcand_workspace(B, K, gamma, V, _dt(target))
+    ws = (workspace or _default_ws).get(dev, nbytes)
+    _check(L.sd_verify_kcand(
+        _p(target), _p(draft), _dt(target), _p(tokens), _p(uniforms), B, K,
+        gamma, V, float(T), _p(n), _p(ks), _p(toks), _p(npc), _p(prob),
+        _p(status), _p(ws), ws.numel(), _stream(dev)))
+    return {"n": n, "k": ks, "tokens": toks, "n_per_cand": npc, "prob": prob}
+
+
+def verify_tree(target, draft, parent, node_tokens, uniforms, T, *,
+                status=None, workspace=None):
+    """Token-tree verify (sd_verify_tree).  target, draft [B, N, V]; parent,
+    node_tokens [B, N] int32; uniforms [B, N] float32.  Returns n, tokens
+    [B, N], nodes [B, N], prob."""
+    dev = target.device
+    _dev(target, dev, "target")
+    B, N, V = target.shape
+    _dev(draft, dev, "draft", target.dtype)
+    if tuple(draft.shape) != (B, N, V):
+        raise ValueError("draft must be [B, N, V]")
+    parent = _dev(parent, dev, "parent", torch.int32)
+    node_tokens = _dev(node_tokens, dev, "node_tokens", torch.int32)
+    uniforms = _dev(uniforms, dev, "uniforms", torch.float32)
+    n = torch.empty(B, dtype=torch.int32, device=dev)
+    toks = torch.empty((B, N), dtype=torch.int32, device=dev)
+    nodes = torch.empty((B, N), dtype=torch.int32, device=dev)
+    prob = torch.empty(B, dtype=torch.float32, device=dev)
+    L = lib()
+    nbytes = L.sd_verify_tree_workspace(B, N, V, _dt(target))
+    ws = (workspace or _default_ws).get(dev, nbytes)
+    _check(L.sd_verify_tree(
+        _p(target), _p(draft), _dt(target), _p(parent), _p(node_tokens),
+        _p(uniforms), B, N, V, float(T), _p(n), _p(toks), _p(nodes),
+        _p(prob), _p(status), _p(ws), ws.numel(), _stream(dev)))
+    return {"n": n, "tokens": toks, "nodes": nodes, "prob": prob}
+
+
+def fanout_schedule(K, budget, a, r):
+    """Geometric fan-out F[0..K] (sd_fanout_schedule, host only)."""
+    F = (ctypes.c_int32 * (K + 1))()
+    _check(lib().sd_fanout_schedule(int(K), int(budget), float(a), float(r),
+                                    ctypes.cast(F, ctypes.c_void_p)))
+    return [int(x) for x in F]
+
+
+def fanout_topk(draft, F, *, want_logit=False, status=None, workspace=None):
+    """Top-F_k tokens per lookahead row (sd_fanout_topk).  draft [B, K+1, V];
+    F a list of K+1 ints.  Returns tokens [B, sum F] (and logit)."""
+    dev = draft.device
+    _dev(draft, dev, "draft")
+    B, K1, V = draft.shape
+    F = [int(x) for x in F]
+    if len(F) != K1:
+        raise ValueError("F must have K+1 entries")
+    Fh = (ctypes.c_int32 * K1)(*F)
+    total = sum(F)
+    toks = torch.empty((B, max(total, 1)), dtype=torch.int32, device=dev)
+    lg = torch.empty((B, max(total, 1)), dtype=torch.float32,
+                     device=dev) if want_logit else None
+    L = lib()
+    nbytes = L.sd_fanout_topk_workspace(B, K1 - 1, V, _dt(draft))
+    ws = (workspace or _default_ws).get(dev, nbytes)
+    _check(L.sd_fanout_topk(
+        _p(draft), _dt(draft), B, K1 - 1, V, ctypes.cast(Fh, ctypes.c_void_p),
+        _p(toks), _p(lg), _p(status), _p(ws), ws.numel(), _stream(dev)))
+    r = {"tokens": toks[:, :total]}
+    if want_logit:
+        r["logit"] = lg[:, :total]
+    return r
+
+
+def verify_linear_fanout(target, draft, tokens, uniforms, T, F, *,
+                         status=None, workspace=None):
+    """Linear verify fused with the fan-out of the same draft logits
+    (sd_verify_linear_fanout).  draft [B, gamma+1, V] (K == gamma)."""
+    dev = target.device
+    _dev(target, dev, "target")
+    B, G1, V = target.shape
+    gamma = G1 - 1
+    _dev(draft, dev, "draft", target.dtype)
+    if tuple(draft.shape) != (B, gamma + 1, V):
+        raise ValueError("draft must be [B, gamma+1, V]")
+    tokens = _dev(tokens, dev, "tokens", torch.int32)
+    uniforms = _dev(uniforms, dev, "uniforms", torch.float32)
+    F = [int(x) for x in F]
+    if len(F) != gamma + 1:
+        raise ValueError("F must have gamma+1 entries")
+    Fh = (ctypes.c_int32 * (gamma + 1))(*F)
+    total = sum(F)
+    n = torch.empty(B, dtype=torch.int32, device=dev)
+    toks = torch.empty((B, G1), dtype=torch.int32, device=dev)
+    prob = torch.empty(B, dtype=torch.float32, device=dev)
+    ftok = torch.empty((B, max(total, 1)), dtype=torch.int32, device=dev)
+    flog = torch.empty((B, max(total, 1)), dtype=torch.float32, device=dev)
+    L = lib()
+    nbytes = L.sd_verify_linear_fanout_workspace(B, gamma, V, _dt(target))
+    ws = (workspace or _default_ws).get(dev, nbytes)
+    _check(L.sd_verify_linear_fanout(
+        _p(target), _p(draft), _dt(target), _p(tokens), _p(uniforms), B,
+        gamma, V, float(T), ctypes.cast(Fh, ctypes.c_void_p), _p(n),
+        _p(toks), _p(prob), _p(ftok), _p(flog), _p(status), _p(ws),
+        ws.numel(), _stream(dev)))
+    return {"n": n, "tokens": toks, "prob": prob,
+            "fan_tokens": ftok[:, :total], "fan_logit": flog[:, :total]}

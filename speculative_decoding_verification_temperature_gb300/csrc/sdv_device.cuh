@@ -1,0 +1,590 @@
+// sdv_device.cuh -- device building blocks shared by the verify kernels.
+//
+// Everything here is fp32 arithmetic on logits streamed from HBM: 16-byte
+// read-only loads, bf16 widening, the online (max, sum) softmax state at
+// temperature T, the greedy argmax state, warp / block reductions with a
+// fixed combination order (so every CTA of a cluster that merges the same
+// partials gets bit-identical results), and the three-level inverse-CDF
+// draw (cluster slices -> 32-vector segments -> elements).
+#pragma once
+
+#include <cooperative_groups.h>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "sd_verify.h"
+
+namespace sdv {
+
+namespace cg = cooperative_groups;
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr float kInf = __builtin_huge_valf();
+
+// ---------------------------------------------------------------- loads
+// DT 0 = fp32, 1 = bf16.  VW = elements per load: 16 bytes (4 fp32 / 8
+// bf16) on the vector path, 1 on the scalar path used when rows are not
+// 16-byte aligned.
+template <int DT, int VW> struct Raw;
+template <> struct Raw<0, 4> { uint4 w; };
+template <> struct Raw<1, 8> { uint4 w; };
+template <> struct Raw<0, 1> { uint32_t w; };
+template <> struct Raw<1, 1> { uint32_t w; };
+
+template <int DT> __host__ __device__ constexpr int vec_width() { return DT == 0 ? 4 : 8; }
+template <int DT> __host__ __device__ constexpr int elt_bytes() { return DT == 0 ? 4 : 2; }
+
+__device__ __forceinline__ uint4 ld_nc_v4(const void *p) {
+  uint4 r;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(p));
+  return r;
+}
+__device__ __forceinline__ uint32_t ld_nc_u32(const void *p) {
+  uint32_t r;
+  asm("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(r) : "l"(p));
+  return r;
+}
+__device__ __forceinline__ uint32_t ld_nc_u16(const void *p) {
+  unsigned short r;
+  asm("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(r) : "l"(p));
+  return (uint32_t)r;
+}
+
+// Load vector v (elements v*VW .. v*VW+VW-1) of a row.
+template <int DT, int VW>
+__device__ __forceinline__ Raw<DT, VW> load_vec(const void *row, int v) {
+  Raw<DT, VW> r;
+  if constexpr (VW > 1) {
+    r.w = ld_nc_v4(static_cast<const char *>(row) + (size_t)v * 16);
+  } else if constexpr (DT == 0) {
+    r.w = ld_nc_u32(static_cast<const float *>(row) + v);
+  } else {
+    r.w = ld_nc_u16(static_cast<const uint16_t *>(row) + v);
+  }
+  return r;
+}
+
+// Element e of a loaded vector, widened to fp32 (bf16 widening is exact).
+template <int DT, int VW>
+__device__ __forceinline__ float elt(const Raw<DT, VW> &r, int e) {
+  if constexpr (VW == 1) {
+    return DT == 0 ? __uint_as_float(r.w) : __uint_as_float(r.w << 16);
+  } else {
+    const uint32_t words[4] = {r.w.x, r.w.y, r.w.z, r.w.w};
+    if constexpr (DT == 0) {
+      return __uint_as_float(words[e]);
+    } else {
+      const uint32_t u = words[e >> 1];
+      return (e & 1) ? __uint_as_float(u & 0xffff0000u)
+                     : __uint_as_float(u << 16);
+    }
+  }
+}
+
+// One logit at column j of a row (scalar, cached: used for gathers).
+template <int DT>
+__device__ __forceinline__ float load_logit(const void *row, int j) {
+  if constexpr (DT == 0) return __ldg(static_cast<const float *>(row) + j);
+  const unsigned short h = __ldg(static_cast<const unsigned short *>(row) + j);
+  return __uint_as_float((uint32_t)h << 16);
+}
+
+// ----------------------------------------------------------- fast exp2
+// The SFU's approximate 2^x (ex2.approx, flush-to-zero): relative error a
+// few ulp, far inside the 1e-5 decision margins the tests allow.
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// ------------------------------------------------- online softmax state
+// Row statistics at temperature T with k2 = log2(e) / T:
+//   m = max_j z_j,  s = sum_j 2^(z_j k2 - m k2)
+// so that p_j = 2^(z_j k2 - m k2) / s.  NaN anywhere makes s NaN; +inf makes
+// m infinite; a row of only -inf leaves m = -inf: all three are "invalid".
+struct MS {
+  float m;
+  float s;
+};
+
+__device__ __forceinline__ MS ms_empty() { return {-kInf, 0.f}; }
+
+__device__ __forceinline__ MS ms_merge(MS a, MS b, float k2) {
+  const float m = fmaxf(a.m, b.m);
+  if (m == -kInf) return {m, a.s + b.s};  // keeps a NaN marker
+  return {m, a.s * ex2((a.m - m) * k2) + b.s * ex2((b.m - m) * k2)};
+}
+
+template <int DT, int VW>
+__device__ __forceinline__ void ms_add(MS &st, const Raw<DT, VW> &r,
+                                       float k2) {
+  float vmax = elt<DT, VW>(r, 0);
+#pragma unroll
+  for (int e = 1; e < VW; ++e) vmax = fmaxf(vmax, elt<DT, VW>(r, e));
+  if (vmax > st.m) {
+    st.s *= ex2((st.m - vmax) * k2);
+    st.m = vmax;
+  }
+  if (st.m == -kInf) {  // nothing finite yet: only look for NaN
+#pragma unroll
+    for (int e = 0; e < VW; ++e) {
+      const float z = elt<DT, VW>(r, e);
+      if (z != z) st.s = z;
+    }
+    return;
+  }
+  const float mk = st.m * k2;
+  float acc = 0.f;
+#pragma unroll
+  for (int e = 0; e < VW; ++e) acc += ex2(fmaf(elt<DT, VW>(r, e), k2, -mk));
+  st.s += acc;
+}
+
+__device__ __forceinline__ bool ms_valid(MS st) {
+  return isfinite(st.m) && isfinite(st.s) && st.s > 0.f;
+}
+
+// --------------------------------------------------------- argmax state
+// Greedy: largest logit, lowest index on ties; `bad` marks NaN / +inf.
+struct AM {
+  float v;
+  int i;
+  int bad;
+};
+
+__device__ __forceinline__ AM am_empty() { return {-kInf, 0x7fffffff, 0}; }
+
+__device__ __forceinline__ AM am_merge(AM a, AM b) {
+  AM r = (b.v > a.v || (b.v == a.v && b.i < a.i)) ? b : a;
+  r.bad = a.bad | b.bad;
+  return r;
+}
+
+template <int DT, int VW>
+__device__ __forceinline__ void am_add(AM &st, const Raw<DT, VW> &r,
+                                       int j0) {
+#pragma unroll
+  for (int e = 0; e < VW; ++e) {
+    const float z = elt<DT, VW>(r, e);
+    st.bad |= !(z < kInf);
+    if (z > st.v) {
+      st.v = z;
+      st.i = j0 + e;
+    }
+  }
+}
+
+// ------------------------------------------------------ warp shuffles
+__device__ __forceinline__ MS warp_down_ms(MS v, float k2) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    MS o{__shfl_down_sync(0xffffffffu, v.m, off),
+         __shfl_down_sync(0xffffffffu, v.s, off)};
+    v = ms_merge(v, o, k2);
+  }
+  return v;
+}
+
+__device__ __forceinline__ AM warp_down_am(AM v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    AM o{__shfl_down_sync(0xffffffffu, v.v, off),
+         __shfl_down_sync(0xffffffffu, v.i, off),
+         __shfl_down_sync(0xffffffffu, v.bad, off)};
+    v = am_merge(v, o);
+  }
+  return v;
+}
+
+__device__ __forceinline__ float warp_down_sum(float v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1)
+    v += __shfl_down_sync(0xffffffffu, v, off);
+  return v;
+}
+
+// Block reduction of NR online states (result valid in thread 0).
+template <int NR>
+__device__ __forceinline__ void block_reduce_ms(MS (&v)[NR], float k2,
+                                                MS (*scratch)[kWarps]) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int r = 0; r < NR; ++r) {
+    v[r] = warp_down_ms(v[r], k2);
+    if (lane == 0) scratch[r][warp] = v[r];
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+      MS a = scratch[r][0];
+      for (int w = 1; w < kWarps; ++w) a = ms_merge(a, scratch[r][w], k2);
+      v[r] = a;
+    }
+  }
+}
+
+__device__ __forceinline__ AM block_reduce_am(AM v, AM *scratch) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  v = warp_down_am(v);
+  if (lane == 0) scratch[warp] = v;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    AM a = scratch[0];
+    for (int w = 1; w < kWarps; ++w) a = am_merge(a, scratch[w]);
+    v = a;
+  }
+  return v;
+}
+
+// --------------------------------------------------------- slice layout
+// A row of nvec vectors is cut into CL contiguous slices, one per CTA of
+// the cluster; a slice is cut into segments of 32 consecutive vectors.
+struct Slice {
+  int vbeg, vend, nseg;
+};
+
+__device__ __forceinline__ Slice make_slice(int nvec, int rank, int CL) {
+  Slice s;
+  s.vbeg = (int)((long long)rank * nvec / CL);
+  s.vend = (int)((long long)(rank + 1) * nvec / CL);
+  s.nseg = (s.vend - s.vbeg + 31) >> 5;
+  return s;
+}
+
+// ---------------------------------------- three-level inverse-CDF draw
+// After every warp has written segmass[s] (fp32 sum of the weights of
+// segment s), warp 0 forms 32 chunk sums (lane l: segments l*cs ..
+// l*cs+cs-1, summed in order in double) and lane 0 their running total.
+// chunk_pre[l] is the inclusive prefix; the slice total is chunk_pre[31].
+__device__ __forceinline__ void slice_prefix(const float *segmass, int nseg,
+                                             double *chunk_pre) {
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const int cs = (nseg + 31) >> 5;
+    double acc = 0.0;
+    const int s0 = lane * cs, s1 = min(nseg, s0 + cs);
+    for (int s = s0; s < s1; ++s) acc += (double)segmass[s];
+    // sequential prefix over the 32 chunk sums, in lane order
+    double pre = 0.0;
+    for (int l = 0; l < 32; ++l) {
+      const double c = __shfl_sync(0xffffffffu, acc, l);
+      pre += c;
+      if (l == lane) chunk_pre[lane] = pre;
+    }
+  }
+}
+
+// Find the segment holding the crossing C > tau inside this slice (tau
+// relative to the slice start).  Returns the segment and writes the
+// remaining target within it; falls back to the last segment with mass if
+// rounding leaves no crossing.  Thread-0 only.
+__device__ __forceinline__ int find_segment(const float *segmass, int nseg,
+                                            const double *chunk_pre,
+                                            double tau, double *tau_in_seg) {
+  const int cs = (nseg + 31) >> 5;
+  int l = 0;
+  while (l < 31 && !(chunk_pre[l] > tau)) ++l;
+  double before = l ? chunk_pre[l - 1] : 0.0;
+  const int s0 = l * cs, s1 = min(nseg, s0 + cs);
+  double acc = 0.0;
+  for (int s = s0; s < s1; ++s) {
+    const double nxt = acc + (double)segmass[s];
+    if (nxt > tau - before) {
+      *tau_in_seg = tau - before - acc;
+      return s;
+    }
+    acc = nxt;
+  }
+  // no crossing (rounding at a chunk edge): last segment with mass in the
+  // chunk, else in the slice
+  for (int s = s1 - 1; s >= s0; --s)
+    if (segmass[s] > 0.f) {
+      *tau_in_seg = (double)segmass[s];
+      return s;
+    }
+  for (int s = nseg - 1; s >= 0; --s)
+    if (segmass[s] > 0.f) {
+      *tau_in_seg = (double)segmass[s];
+      return s;
+    }
+  *tau_in_seg = 0.0;
+  return 0;
+}
+
+// Within one segment: given per-lane weights w[VW] (lane = vector index in
+// the segment, ascending elements), return (in every lane) the element index
+// of the first inclusive prefix > tau, or the last positive weight if none.
+// out_w receives the chosen weight.
+template <int VW>
+__device__ __forceinline__ int warp_pick(const float (&w)[VW], float tau,
+                                         int seg_first_elt, float *out_w) {
+  const int lane = threadIdx.x & 31;
+  float pre[VW];
+  float run = 0.f;
+#pragma unroll
+  for (int e = 0; e < VW; ++e) {
+    run += w[e];
+    pre[e] = run;
+  }
+  // inclusive scan of lane totals
+  float incl = run;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const float o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  const float excl = incl - run;
+  int first = -1;
+#pragma unroll
+  for (int e = VW - 1; e >= 0; --e)
+    if (excl + pre[e] > tau) first = e;
+  const unsigned hit = __ballot_sync(0xffffffffu, first >= 0);
+  int src_lane, src_e;
+  if (hit) {
+    src_lane = __ffs(hit) - 1;
+    src_e = __shfl_sync(0xffffffffu, first, src_lane);
+  } else {
+    int lastpos = -1;
+#pragma unroll
+    for (int e = 0; e < VW; ++e)
+      if (w[e] > 0.f) lastpos = e;
+    const unsigned has = __ballot_sync(0xffffffffu, lastpos >= 0);
+    src_lane = has ? 31 - __clz(has) : 0;
+    src_e = __shfl_sync(0xffffffffu, has ? lastpos : 0, src_lane);
+  }
+  float mine = 0.f;
+#pragma unroll
+  for (int e = 0; e < VW; ++e)
+    if (e == src_e) mine = w[e];
+  *out_w = __shfl_sync(0xffffffffu, mine, src_lane);
+  return seg_first_elt + src_lane * VW + src_e;
+}
+
+// ------------------------------------------------------- streaming passes
+constexpr int kU = 4;  // vectors per thread in flight per row
+
+// Accumulate the online softmax state of one or two rows over a slice.
+template <int DT, int VW>
+__device__ __forceinline__ void stats_pass(const char *ra, const char *rb,
+                                           const Slice &sl, float k2, MS &a,
+                                           MS &b) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int v0 = sl.vbeg + warp * 32 * kU + lane; v0 < sl.vend;
+       v0 += kWarps * 32 * kU) {
+    Raw<DT, VW> xa[kU], xb[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u)
+      if (v0 + u * 32 < sl.vend) {
+        xa[u] = load_vec<DT, VW>(ra, v0 + u * 32);
+        if (rb) xb[u] = load_vec<DT, VW>(rb, v0 + u * 32);
+      }
+#pragma unroll
+    for (int u = 0; u < kU; ++u)
+      if (v0 + u * 32 < sl.vend) {
+        ms_add<DT, VW>(a, xa[u], k2);
+        if (rb) ms_add<DT, VW>(b, xb[u], k2);
+      }
+  }
+}
+
+// Accumulate the greedy argmax state of one row over a slice.
+template <int DT, int VW>
+__device__ __forceinline__ void argmax_pass(const char *ra, const Slice &sl,
+                                            AM &a) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int v0 = sl.vbeg + warp * 32 * kU + lane; v0 < sl.vend;
+       v0 += kWarps * 32 * kU) {
+    Raw<DT, VW> xa[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u)
+      if (v0 + u * 32 < sl.vend) xa[u] = load_vec<DT, VW>(ra, v0 + u * 32);
+#pragma unroll
+    for (int u = 0; u < kU; ++u)
+      if (v0 + u * 32 < sl.vend) am_add<DT, VW>(a, xa[u], (v0 + u * 32) * VW);
+  }
+}
+
+// Weights of a final draw: with a draft row,
+//   w_j = max(0, p_j - c q_j) = max(0, 2^(zt k2 - mtk) ist - 2^(zd k2 - mdk) cq)
+// (cq = c / s_q; c = 1 is the residual of section 2.1, c >= 1 the tree's
+// repeated residual); without one, w_j = p_j = 2^(zt k2 - mtk) ist.
+struct Weight {
+  float k2, mtk, ist, mdk, cq;
+};
+
+template <int DT, int VW>
+__device__ __forceinline__ void weights(const Raw<DT, VW> &a,
+                                        const Raw<DT, VW> &b, bool has_q,
+                                        const Weight &W, float (&w)[VW]) {
+#pragma unroll
+  for (int e = 0; e < VW; ++e) {
+    const float pt = ex2(fmaf(elt<DT, VW>(a, e), W.k2, -W.mtk)) * W.ist;
+    if (has_q) {
+      const float qd = ex2(fmaf(elt<DT, VW>(b, e), W.k2, -W.mdk)) * W.cq;
+      w[e] = fmaxf(0.f, pt - qd);
+    } else {
+      w[e] = pt;
+    }
+  }
+}
+
+// Per-segment masses of the weights over this CTA's slice.
+template <int DT, int VW>
+__device__ __forceinline__ void mass_pass(const char *ra, const char *rb,
+                                          const Weight &W, const Slice &sl,
+                                          float *segmass) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const bool has_q = rb != nullptr;
+  for (int s0 = warp; s0 < sl.nseg; s0 += kWarps * kU) {
+    Raw<DT, VW> xa[kU], xb[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int v = sl.vbeg + (s0 + u * kWarps) * 32 + lane;
+      if (s0 + u * kWarps < sl.nseg && v < sl.vend) {
+        xa[u] = load_vec<DT, VW>(ra, v);
+        if (has_q) xb[u] = load_vec<DT, VW>(rb, v);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int s = s0 + u * kWarps;
+      if (s < sl.nseg) {  // warp-uniform
+        const int v = sl.vbeg + s * 32 + lane;
+        float acc = 0.f;
+        if (v < sl.vend) {
+          float w[VW];
+          weights<DT, VW>(xa[u], xb[u], has_q, W, w);
+#pragma unroll
+          for (int e = 0; e < VW; ++e) acc += w[e];
+        }
+        acc = warp_down_sum(acc);
+        if (lane == 0) segmass[s] = acc;
+      }
+    }
+  }
+}
+
+// Shared state of a cluster-wide inverse-CDF draw (one per CTA).
+struct DrawSmem {
+  double slice[2];  // [parity] this CTA's slice mass (read by peers)
+  double chunk_pre[32];
+  double N;      // total mass (all CTAs agree)
+  double tau;    // u * N minus the mass of the slices before the owner
+  int owner;     // CTA holding the crossing (-1: zero mass)
+  int seg;       // owner: segment of the crossing
+  float tau_seg; // owner: target left inside that segment
+};
+
+struct DrawOut {
+  double N;
+  int owner;
+  int t;     // warp 0 of the owner CTA: drawn token
+  float wt;  // its weight (probability wt / N)
+};
+
+// Draw one token from the weights W over the row(s) by inverse CDF with
+// uniform u: the smallest j with C_j > u * N.  Every thread of every CTA of
+// the cluster must call it (it holds one cluster barrier); `par` is the
+// caller's parity of the double-buffered slot.
+template <int DT, int VW>
+__device__ DrawOut cluster_draw(cg::cluster_group &cluster, DrawSmem &ds,
+                                float *segmass, const char *ra,
+                                const char *rb, const Weight &W,
+                                const Slice &sl, float u, int &par) {
+  const int tid = threadIdx.x;
+  const int rank = (int)cluster.block_rank();
+  const int CL = (int)cluster.num_blocks();
+  mass_pass<DT, VW>(ra, rb, W, sl, segmass);
+  __syncthreads();
+  slice_prefix(segmass, sl.nseg, ds.chunk_pre);
+  __syncthreads();
+  if (tid == 0) ds.slice[par] = sl.nseg ? ds.chunk_pre[31] : 0.0;
+  cluster.sync();
+  if (tid == 0) {
+    double tot = 0.0;
+    for (int r = 0; r < CL; ++r)
+      tot += cluster.map_shared_rank(&ds, r)->slice[par];
+    const double tau = (double)u * tot;
+    double run = 0.0, bef = 0.0;
+    int own = -1;
+    for (int r = 0; r < CL && own < 0; ++r) {
+      const double sr = cluster.map_shared_rank(&ds, r)->slice[par];
+      if (run + sr > tau) {
+        own = r;
+        bef = run;
+      }
+      run += sr;
+    }
+    if (own < 0 && tot > 0.0) {  // rounding: last slice with mass
+      run = 0.0;
+      for (int r = 0; r < CL; ++r) {
+        const double sr = cluster.map_shared_rank(&ds, r)->slice[par];
+        if (sr > 0.0) {
+          own = r;
+          bef = run;
+        }
+        run += sr;
+      }
+    }
+    ds.N = tot;
+    ds.owner = tot > 0.0 ? own : -1;
+    ds.tau = tau - bef;
+  }
+  __syncthreads();
+  par ^= 1;
+  DrawOut out;
+  out.N = ds.N;
+  out.owner = ds.owner;
+  out.t = -1;
+  out.wt = 0.f;
+  if (out.owner == rank) {
+    if (tid == 0) {
+      double tin = 0.0;
+      ds.seg = find_segment(segmass, sl.nseg, ds.chunk_pre, ds.tau, &tin);
+      ds.tau_seg = (float)tin;
+    }
+    __syncthreads();
+    if (tid < 32) {
+      const int s = ds.seg;
+      const int v = sl.vbeg + s * 32 + tid;
+      float w[VW];
+      if (v < sl.vend) {
+        Raw<DT, VW> a = load_vec<DT, VW>(ra, v), b;
+        if (rb) b = load_vec<DT, VW>(rb, v);
+        weights<DT, VW>(a, b, rb != nullptr, W, w);
+      } else {
+#pragma unroll
+        for (int e = 0; e < VW; ++e) w[e] = 0.f;
+      }
+      out.t = warp_pick<VW>(w, ds.tau_seg, (sl.vbeg + s * 32) * VW, &out.wt);
+    }
+  }
+  return out;
+}
+
+// Debug output: the normalised weights w_j / N over this CTA's slice.
+template <int DT, int VW>
+__device__ __forceinline__ void write_resid(float *res, const char *ra,
+                                            const char *rb, const Weight &W,
+                                            const Slice &sl, double N) {
+  const float invN = (float)(1.0 / N);
+  for (int v = sl.vbeg + threadIdx.x; v < sl.vend; v += kThreads) {
+    Raw<DT, VW> a = load_vec<DT, VW>(ra, v), b;
+    if (rb) b = load_vec<DT, VW>(rb, v);
+    float w[VW];
+    weights<DT, VW>(a, b, rb != nullptr, W, w);
+#pragma unroll
+    for (int e = 0; e < VW; ++e) res[(size_t)v * VW + e] = w[e] * invN;
+  }
+}
+
+__device__ __forceinline__ void status_or(int32_t *dev_status, int bits) {
+  if (dev_status && bits) atomicOr(dev_status, bits);
+}
+
+}  // namespace sdv

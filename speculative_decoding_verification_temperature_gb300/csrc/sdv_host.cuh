@@ -1,0 +1,62 @@
+// sdv_host.cuh -- host-side helpers shared by the entry points: argument
+// checks with a thread-local error text, the sm_103 device check, cluster
+// sizing and the cluster launch itself.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <mutex>
+#include <unordered_map>
+
+#include "sd_verify.h"
+
+namespace sdv {
+
+sd_status fail(sd_status st, const char *fmt, ...);
+sd_status check_device(int *sm_count);
+int env_int(const char *name, int dflt);
+
+#define SDV_REQUIRE(cond, ...)                              \
+  do {                                                      \
+    if (!(cond)) return ::sdv::fail(SD_ERR_INVALID_ARG, __VA_ARGS__); \
+  } while (0)
+
+#define SDV_CUDA(call)                                                   \
+  do {                                                                   \
+    cudaError_t e_ = (call);                                             \
+    if (e_ != cudaSuccess)                                               \
+      return ::sdv::fail(SD_ERR_CUDA, "%s: %s", #call,                   \
+                         cudaGetErrorString(e_));                        \
+  } while (0)
+
+inline bool aligned16(const void *p) {
+  return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+// Cluster size for rows of nvec vectors: slices of at least ~512 vectors
+// (one load batch per thread), at most 16 CTAs.  SDV_CLUSTER overrides it
+// (1, 2, 4, 8 or 16) for tuning.
+inline int choose_cluster(long long nvec) {
+  int forced = env_int("SDV_CLUSTER", 0);
+  if (forced == 1 || forced == 2 || forced == 4 || forced == 8 ||
+      forced == 16)
+    return forced;
+  int cl = 1;
+  while (cl < 16 && nvec / (2 * cl) >= 512) cl *= 2;
+  return cl;
+}
+
+// Largest number of co-resident clusters of `cl` CTAs for a kernel (cached
+// per kernel, cluster size and shared-memory size).
+sd_status max_active_clusters(const void *kernel, int cl, size_t smem,
+                              int *out);
+
+// Launch `kernel` with a 1-D grid of nclusters * cl CTAs in clusters of cl.
+sd_status launch_clusters(const void *kernel, int nclusters, int cl,
+                          size_t smem, cudaStream_t stream, void **args);
+
+}  // namespace sdv

@@ -1,0 +1,384 @@
+// sdv_linear.cu -- linear verify ("01 · Draft-then-verify", Algorithm 1 and
+// the spec_step listing of section 4) as one persistent kernel.
+//
+// Design.  One thread-block cluster verifies one sequence at a time; the
+// vocabulary axis of every row is cut into one slice per CTA of the
+// cluster.  Positions are scanned left to right: at position i each CTA
+// streams its slice of target row i and draft row i once (16-byte loads,
+// single-pass online max / sum of 2^(z log2e / T)), the CTAs exchange their
+// partial (max, sum) pairs through distributed shared memory, and every CTA
+// merges them in rank order, so all CTAs reach the same accept decision
+// r_i <= p_i(x_i) / q_i(x_i) without another barrier.  The scan stops at the
+// first rejection: rows after it are never read.  The correction
+// norm(max(0, p_n - q_n)) (section 2.1) or the bonus p_gamma is then drawn by
+// inverse CDF over the same slices: a second pass (from L2: the rows were
+// just read) writes per-segment masses, the cluster agrees on the slice
+// holding u * N, and one warp scans one 32-vector segment.
+//
+// Clusters take sequences from a work counter, so short and long scans
+// balance across the GPU.  Greedy (T == 0) compares draft ids with the
+// row argmax (section 2.2) and reads no draft logits.
+#include "sdv_device.cuh"
+#include "sdv_host.cuh"
+
+namespace sdv {
+
+struct LinearParams {
+  const void *target;  // [B, gamma+1, V]
+  const void *draft;   // [B, d_seq_rows, V]
+  const int32_t *tokens;
+  const float *uniforms;
+  int B, gamma, V;
+  long long d_seq_rows;  // rows per sequence in the draft tensor
+  float k2;              // log2(e) / T
+  int32_t *n_acc;
+  int32_t *out_tokens;
+  float *out_prob;
+  float *out_accept;
+  float *out_resid;
+  int32_t *dev_status;
+  int *queue;  // nullable: then cluster c verifies sequence c only
+  int nclusters;
+};
+
+struct Decision {
+  int invalid;  // a row read is unusable
+  int accept;   // draft accepted at this position
+  int tok;      // greedy: argmax of the row
+  float acc_prob;
+  MS mt, md;  // merged stats of target / draft row
+};
+
+struct LinearSmem {
+  MS red[2][kWarps];
+  AM ared[kWarps];
+  MS part[2][2];  // [parity][target, draft]: read by peers
+  AM apart[2];    // [parity]: read by peers
+  int next_seq[2];
+  Decision dec;
+  // gathered by thread 0 for the accept test, [step parity]
+  int gx[2];
+  float gzt[2], gzd[2], gr[2];
+  DrawSmem draw;
+};
+
+template <int DT, int VW, bool GREEDY>
+__global__ void __launch_bounds__(kThreads, 2)
+    linear_verify_kernel(const LinearParams p) {
+  extern __shared__ float segmass[];
+  __shared__ LinearSmem sh;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = (int)cluster.block_rank();
+  const int CL = (int)cluster.num_blocks();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int V = p.V, gamma = p.gamma;
+  const Slice sl = make_slice(V / VW, rank, CL);
+  const size_t rowb = (size_t)V * elt_bytes<DT>();
+  const char *tbase = static_cast<const char *>(p.target);
+  const char *dbase = static_cast<const char *>(p.draft);
+  const float k2 = p.k2;
+
+  int par = 0, seqpar = 0;
+  int seq = (int)(blockIdx.x / CL);
+  while (seq < p.B) {
+    if (rank == 0 && tid == 0)
+      sh.next_seq[seqpar] =
+          p.queue ? p.nclusters + atomicAdd(p.queue, 1) : p.B;
+    int n = 0, kind = 0;  // kind: 1 reject at n, 2 bonus, 3 invalid row
+    int greedy_tok = -1, bad_token = 0;
+    MS fmt = ms_empty(), fmd = ms_empty();
+    for (int i = 0; i <= gamma; ++i) {
+      const bool has_d = (!GREEDY) && i < gamma;
+      const char *trow = tbase + ((size_t)seq * (gamma + 1) + i) * rowb;
+      const char *drow =
+          has_d ? dbase + ((size_t)seq * p.d_seq_rows + i) * rowb : nullptr;
+      if (tid == 0) {  // gathers for the accept test (used after the merge)
+        int x = -1;
+        float zt = 0.f, zd = 0.f;
+        if (i < gamma) {
+          x = p.tokens[(size_t)seq * gamma + i];
+          if (!GREEDY && x >= 0 && x < V) {
+            zt = load_logit<DT>(trow, x);
+            zd = load_logit<DT>(drow, x);
+          }
+        }
+        sh.gx[par] = x;
+        sh.gzt[par] = zt;
+        sh.gzd[par] = zd;
+        sh.gr[par] =
+            GREEDY ? 0.f : p.uniforms[(size_t)seq * (gamma + 1) + i];
+      }
+      if constexpr (GREEDY) {
+        AM a = am_empty();
+        argmax_pass<DT, VW>(trow, sl, a);
+        a = block_reduce_am(a, sh.ared);
+        if (tid == 0) sh.apart[par] = a;
+      } else {
+        MS st[2] = {ms_empty(), ms_empty()};
+        stats_pass<DT, VW>(trow, drow, sl, k2, st[0], st[1]);
+        block_reduce_ms<2>(st, k2, sh.red);
+        if (tid == 0) {
+          sh.part[par][0] = st[0];
+          sh.part[par][1] = st[1];
+        }
+      }
+      cluster.sync();
+      // every CTA merges the CL partials in the same order: same decision
+      if (warp == 0) {
+        Decision d{};
+        const int x = sh.gx[par];
+        if constexpr (GREEDY) {
+          AM a = am_empty();
+          if (lane < CL) a = cluster.map_shared_rank(&sh, lane)->apart[par];
+          a = warp_down_am(a);
+          d.invalid = a.bad || !(a.v > -kInf);
+          d.tok = a.i;
+          d.accept = (i < gamma) && !d.invalid && x == a.i;
+          d.acc_prob = d.accept ? 1.f : 0.f;
+        } else {
+          MS mt = ms_empty(), md = ms_empty();
+          if (lane < CL) {
+            const LinearSmem *rs = cluster.map_shared_rank(&sh, lane);
+            mt = rs->part[par][0];
+            md = rs->part[par][1];
+          }
+          mt = warp_down_ms(mt, k2);
+          md = warp_down_ms(md, k2);
+          d.mt = mt;
+          d.md = md;
+          d.invalid = !ms_valid(mt) || (has_d && !ms_valid(md));
+          if (!d.invalid && has_d && x >= 0 && x < V) {
+            // p(x)/q(x) with the same scaled exponents the draw uses
+            const float e = fmaf(sh.gzt[par], k2, -mt.m * k2) -
+                            fmaf(sh.gzd[par], k2, -md.m * k2);
+            const float rho = exp2f(e) * (md.s / mt.s);
+            d.accept = sh.gr[par] <= rho;
+            d.acc_prob = fminf(1.f, rho);
+          }
+        }
+        if (lane == 0) sh.dec = d;
+      }
+      __syncthreads();
+      const Decision d = sh.dec;
+      const int x = sh.gx[par];
+      par ^= 1;
+      if (i < gamma && (x < 0 || x >= V)) bad_token = 1;
+      if (rank == 0 && tid == 0 && p.out_accept && i < gamma && !d.invalid)
+        p.out_accept[(size_t)seq * gamma + i] = d.acc_prob;
+      if (d.invalid) {
+        kind = 3;
+        break;
+      }
+      greedy_tok = d.tok;
+      fmt = d.mt;
+      fmd = d.md;
+      if (i == gamma) {
+        kind = 2;
+        break;
+      }
+      if (!d.accept) {
+        kind = 1;
+        break;
+      }
+      ++n;
+    }
+
+    if (kind == 3) {  // unusable row: outputs -1
+      if (rank == 0) {
+        for (int i = tid; i <= gamma; i += kThreads)
+          p.out_tokens[(size_t)seq * (gamma + 1) + i] = -1;
+        if (p.out_accept)
+          for (int i = n + tid; i < gamma; i += kThreads)
+            p.out_accept[(size_t)seq * gamma + i] = -1.f;
+        if (tid == 0) {
+          p.n_acc[seq] = -1;
+          if (p.out_prob) p.out_prob[seq] = 0.f;
+          status_or(p.dev_status,
+                    SD_DEV_NONFINITE | (bad_token ? SD_DEV_BAD_TOKEN : 0));
+        }
+      }
+    } else if (GREEDY) {
+      if (rank == 0) {
+        for (int i = tid; i <= gamma; i += kThreads) {
+          int v = -1;
+          if (i < n) v = p.tokens[(size_t)seq * gamma + i];
+          else if (i == n) v = greedy_tok;
+          p.out_tokens[(size_t)seq * (gamma + 1) + i] = v;
+        }
+        if (p.out_accept)
+          for (int i = n + 1 + tid; i < gamma; i += kThreads)
+            p.out_accept[(size_t)seq * gamma + i] = -1.f;
+        if (tid == 0) {
+          p.n_acc[seq] = n;
+          if (p.out_prob) p.out_prob[seq] = 1.f;
+          status_or(p.dev_status, bad_token ? SD_DEV_BAD_TOKEN : 0);
+        }
+      }
+      if (p.out_resid) {
+        float *res = p.out_resid + (size_t)seq * V;
+        for (int j = sl.vbeg * VW + tid; j < sl.vend * VW; j += kThreads)
+          res[j] = (j == greedy_tok) ? 1.f : 0.f;
+      }
+    } else {
+      // correction (kind 1) or bonus (kind 2) by inverse CDF
+      const char *trow = tbase + ((size_t)seq * (gamma + 1) + n) * rowb;
+      const char *drow =
+          kind == 1 ? dbase + ((size_t)seq * p.d_seq_rows + n) * rowb
+                    : nullptr;
+      Weight W;
+      W.k2 = k2;
+      W.mtk = fmt.m * k2;
+      W.ist = 1.f / fmt.s;
+      W.mdk = fmd.m * k2;
+      W.cq = 1.f / fmd.s;
+      const float u = p.uniforms[(size_t)seq * (gamma + 1) + gamma];
+      DrawOut o = cluster_draw<DT, VW>(cluster, sh.draw, segmass, trow, drow,
+                                       W, sl, u, par);
+      int zero_mass = 0;
+      if (o.owner < 0) {  // residual of zero mass: draw from p_n instead
+        zero_mass = 1;
+        drow = nullptr;
+        __syncthreads();
+        o = cluster_draw<DT, VW>(cluster, sh.draw, segmass, trow, nullptr, W,
+                                 sl, u, par);
+      }
+      if (o.owner == rank && warp == 0) {
+        for (int i = lane; i <= gamma; i += 32) {
+          int v = -1;
+          if (i < n) v = p.tokens[(size_t)seq * gamma + i];
+          else if (i == n) v = o.t;
+          p.out_tokens[(size_t)seq * (gamma + 1) + i] = v;
+        }
+        if (p.out_accept)
+          for (int i = n + 1 + lane; i < gamma; i += 32)
+            p.out_accept[(size_t)seq * gamma + i] = -1.f;
+        if (lane == 0) {
+          p.n_acc[seq] = n;
+          if (p.out_prob) p.out_prob[seq] = (float)((double)o.wt / o.N);
+          status_or(p.dev_status, (bad_token ? SD_DEV_BAD_TOKEN : 0) |
+                                      (zero_mass ? SD_DEV_ZERO_MASS : 0));
+        }
+      }
+      if (p.out_resid)
+        write_resid<DT, VW>(p.out_resid + (size_t)seq * V, trow, drow, W, sl,
+                            o.N);
+    }
+    // next sequence (rank 0 published it before this sequence's first sync)
+    seq = cluster.map_shared_rank(&sh, 0)->next_seq[seqpar];
+    seqpar ^= 1;
+    __syncthreads();
+  }
+  cluster.sync();  // no CTA leaves while a peer may still read its smem
+}
+
+// ------------------------------------------------------------------ host
+
+using LinearKernel = void (*)(const LinearParams);
+
+static LinearKernel pick_linear(int dt, bool vec, bool greedy) {
+  if (dt == SD_F32) {
+    if (vec)
+      return greedy ? linear_verify_kernel<0, 4, true>
+                    : linear_verify_kernel<0, 4, false>;
+    return greedy ? linear_verify_kernel<0, 1, true>
+                  : linear_verify_kernel<0, 1, false>;
+  }
+  if (vec)
+    return greedy ? linear_verify_kernel<1, 8, true>
+                  : linear_verify_kernel<1, 8, false>;
+  return greedy ? linear_verify_kernel<1, 1, true>
+                : linear_verify_kernel<1, 1, false>;
+}
+
+sd_status linear_launch(const void *target, const void *draft, sd_dtype dt,
+                        long long d_seq_rows, const int32_t *tokens,
+                        const float *uniforms, int B, int gamma, int V,
+                        float T, int32_t *n_acc, int32_t *out_tokens,
+                        float *out_prob, float *out_accept, float *out_resid,
+                        int32_t *dev_status, void *ws, size_t ws_bytes,
+                        cudaStream_t stream) {
+  int sms = 0;
+  sd_status st = check_device(&sms);
+  if (st != SD_OK) return st;
+  const bool greedy = (T == 0.f);
+  const int eb = dt == SD_F32 ? 4 : 2, vw = dt == SD_F32 ? 4 : 8;
+  const bool vec = aligned16(target) && (greedy || gamma == 0 ||
+                                         aligned16(draft)) &&
+                   ((size_t)V * eb) % 16 == 0;
+  const int VW = vec ? vw : 1;
+  const long long nvec = V / VW;
+  const int CL = choose_cluster(nvec);
+  const long long per_cta = (nvec + CL - 1) / CL;
+  const size_t smem = (size_t)((per_cta + 31) / 32) * sizeof(float) + 16;
+  if (smem > 96 * 1024)
+    return fail(SD_ERR_UNSUPPORTED, "V=%d needs %zu B of shared memory", V,
+                smem);
+  LinearKernel kern = pick_linear(dt, vec, greedy);
+  int maxc = 0;
+  st = max_active_clusters((const void *)kern, CL, smem, &maxc);
+  if (st != SD_OK) return st;
+  const int nclusters = B < maxc ? B : maxc;
+  LinearParams prm;
+  prm.target = target;
+  prm.draft = draft;
+  prm.tokens = tokens;
+  prm.uniforms = uniforms;
+  prm.B = B;
+  prm.gamma = gamma;
+  prm.V = V;
+  prm.d_seq_rows = d_seq_rows;
+  prm.k2 = greedy ? 0.f : (float)(1.4426950408889634 / (double)T);
+  prm.n_acc = n_acc;
+  prm.out_tokens = out_tokens;
+  prm.out_prob = out_prob;
+  prm.out_accept = out_accept;
+  prm.out_resid = out_resid;
+  prm.dev_status = dev_status;
+  prm.queue = nullptr;
+  prm.nclusters = nclusters;
+  if (B > nclusters) {
+    if (!ws || ws_bytes < 256)
+      return fail(SD_ERR_INVALID_ARG, "workspace of >= 256 bytes required");
+    prm.queue = static_cast<int *>(ws);
+    SDV_CUDA(cudaMemsetAsync(ws, 0, sizeof(int), stream));
+  }
+  void *args[] = {&prm};
+  return launch_clusters((const void *)kern, nclusters, CL, smem, stream,
+                         args);
+}
+
+}  // namespace sdv
+
+extern "C" size_t sd_verify_linear_workspace(int B, int gamma, int V,
+                                             sd_dtype dt) {
+  (void)B;
+  (void)gamma;
+  (void)V;
+  (void)dt;
+  return 256;
+}
+
+extern "C" sd_status sd_verify_linear(
+    const void *target_logits, const void *draft_logits, sd_dtype dt,
+    const int32_t *draft_tokens, const float *uniforms, int B, int gamma,
+    int V, float T, int32_t *n_accepted, int32_t *out_tokens, float *out_prob,
+    float *out_accept_prob, float *out_resid, int32_t *dev_status,
+    void *workspace, size_t ws_bytes, void *stream) {
+  SDV_REQUIRE(dt == SD_F32 || dt == SD_BF16, "bad dtype %d", (int)dt);
+  SDV_REQUIRE(B >= 0, "B < 0");
+  SDV_REQUIRE(gamma >= 0 && gamma <= SD_MAX_GAMMA, "gamma=%d outside [0, %d]",
+              gamma, SD_MAX_GAMMA);
+  SDV_REQUIRE(V >= 1 && V <= SD_MAX_V, "V=%d outside [1, %d]", V, SD_MAX_V);
+  SDV_REQUIRE(T >= 0.f && std::isfinite(T), "T must be finite and >= 0");
+  if (B == 0) return SD_OK;
+  SDV_REQUIRE(target_logits && n_accepted && out_tokens, "null pointer");
+  SDV_REQUIRE(gamma == 0 || draft_tokens, "draft_tokens is null");
+  SDV_REQUIRE(T == 0.f || uniforms, "uniforms is null");
+  SDV_REQUIRE(T == 0.f || gamma == 0 || draft_logits,
+              "draft_logits is null with T > 0");
+  return sdv::linear_launch(target_logits, draft_logits, dt, gamma,
+                            draft_tokens, uniforms, B, gamma, V, T,
+                            n_accepted, out_tokens, out_prob, out_accept_prob,
+                            out_resid, dev_status, workspace, ws_bytes,
+                            static_cast<cudaStream_t>(stream));
+}
