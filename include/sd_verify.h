@@ -71,6 +71,8 @@ typedef enum { SD_F32 = 0, SD_BF16 = 1 } sd_dtype;
 #define SD_DEV_BAD_PARENT 4 /* tree: parent[0] != -1 or parent[v] not in
                                [0, v): the tree's outputs are -1 */
 #define SD_DEV_ZERO_MASS 8  /* a residual had zero mass: drawn from p instead */
+#define SD_DEV_TIMEOUT 16   /* a bounded wait on an asynchronous copy gave up:
+                               the call's outputs are not to be trusted */
 
 /* Limits (SD_ERR_UNSUPPORTED beyond them). */
 #define SD_MAX_V (1 << 24)     /* vocabulary size */

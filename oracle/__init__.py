@@ -47,11 +47,11 @@ def _bind(path):
     I = ctypes.c_int
     D = ctypes.c_double
     lib.orc_verify_linear.argtypes = [P, P, I, P, P, I, I, I, D,
-                                      P, P, P, P, P, P, P]
+                                      P, P, P, P, P, P, P, P, P, P]
     lib.orc_verify_kcand.argtypes = [P, P, I, P, P, I, I, I, I, D,
-                                     P, P, P, P, P, P, P]
+                                     P, P, P, P, P, P, P, P, P, P]
     lib.orc_verify_tree.argtypes = [P, P, I, P, P, P, I, I, I, D,
-                                    P, P, P, P, P, P]
+                                    P, P, P, P, P, P, P, P, P]
     lib.orc_fanout_schedule.argtypes = [I, I, D, D, P]
     lib.orc_fanout_topk.argtypes = [P, I, I, I, I, P, P, P, P]
     for f in (lib.orc_verify_linear, lib.orc_verify_kcand,
@@ -105,6 +105,24 @@ def _ptr(a):
     return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
 
 
+def _margins(B):
+    return {"margin_acc": np.empty(B, np.float64),
+            "margin_cdf": np.empty(B, np.float64),
+            "cdf_lo": np.empty(B, np.int32),
+            "cdf_hi": np.empty(B, np.int32)}
+
+
+def _margin_ptrs(m):
+    return (_ptr(m["margin_acc"]), _ptr(m["margin_cdf"]), _ptr(m["cdf_lo"]),
+            _ptr(m["cdf_hi"]))
+
+
+def _finish(out, m):
+    out.update(m)
+    out["margin"] = np.minimum(m["margin_acc"], m["margin_cdf"])
+    return out
+
+
 def verify_linear(target, draft, tokens, uniforms, T, want_resid=False):
     """Linear verify of B sequences.
 
@@ -132,21 +150,21 @@ def verify_linear(target, draft, tokens, uniforms, T, want_resid=False):
         "tokens": np.empty((B, G1), np.int32),
         "prob": np.empty(B, np.float64),
         "accept": np.empty((B, max(gamma, 1)), np.float64),
-        "margin": np.empty(B, np.float64),
         "status": np.empty(B, np.int32),
     }
+    m = _margins(B)
     resid = np.empty((B, V), np.float64) if want_resid else None
     rc = _load().orc_verify_linear(
         _ptr(target), draft_p, dt, _ptr(tokens), _ptr(uniforms), B, gamma, V,
         float(T), _ptr(out["n"]), _ptr(out["tokens"]), _ptr(out["prob"]),
-        _ptr(out["accept"]), _ptr(out["margin"]), _ptr(resid),
+        _ptr(out["accept"]), *_margin_ptrs(m), _ptr(resid),
         _ptr(out["status"]))
     if rc:
         raise MemoryError("oracle allocation failed")
     out["accept"] = out["accept"][:, :gamma]
     if want_resid:
         out["resid"] = resid
-    return out
+    return _finish(out, m)
 
 
 def verify_kcand(target, draft, tokens, uniforms, T):
@@ -169,17 +187,17 @@ def verify_kcand(target, draft, tokens, uniforms, T):
         "tokens": np.empty((B, G1), np.int32),
         "n_per_cand": np.empty((B, K), np.int32),
         "prob": np.empty(B, np.float64),
-        "margin": np.empty(B, np.float64),
         "status": np.empty(B, np.int32),
     }
+    m = _margins(B)
     rc = _load().orc_verify_kcand(
         _ptr(target), _ptr(draft), dt, _ptr(tokens), _ptr(uniforms), B, K,
         gamma, V, float(T), _ptr(out["n"]), _ptr(out["k"]),
         _ptr(out["tokens"]), _ptr(out["n_per_cand"]), _ptr(out["prob"]),
-        _ptr(out["margin"]), _ptr(out["status"]))
+        *_margin_ptrs(m), _ptr(out["status"]))
     if rc:
         raise MemoryError("oracle allocation failed")
-    return out
+    return _finish(out, m)
 
 
 def verify_tree(target, draft, parent, node_tokens, uniforms, T):
@@ -201,17 +219,17 @@ def verify_tree(target, draft, parent, node_tokens, uniforms, T):
         "tokens": np.empty((B, N), np.int32),
         "nodes": np.empty((B, N), np.int32),
         "prob": np.empty(B, np.float64),
-        "margin": np.empty(B, np.float64),
         "status": np.empty(B, np.int32),
     }
+    m = _margins(B)
     rc = _load().orc_verify_tree(
         _ptr(target), _ptr(draft), dt, _ptr(parent), _ptr(node_tokens),
         _ptr(uniforms), B, N, V, float(T), _ptr(out["n"]),
         _ptr(out["tokens"]), _ptr(out["nodes"]), _ptr(out["prob"]),
-        _ptr(out["margin"]), _ptr(out["status"]))
+        *_margin_ptrs(m), _ptr(out["status"]))
     if rc:
         raise MemoryError("oracle allocation failed")
-    return out
+    return _finish(out, m)
 
 
 def fanout_schedule(K, budget, a, r):
@@ -247,4 +265,5 @@ def fanout_topk(draft, F):
 
 FLAG_MARGIN = 1e-5
 """A draw whose margin is below this is 'flagged': a correct fp32
-implementation may land on the other side of the threshold there."""
+implementation may land on the other side of the threshold there (for an
+inverse-CDF draw it may then return any token in [cdf_lo, cdf_hi])."""

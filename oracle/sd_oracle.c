@@ -51,10 +51,12 @@
  *    largest fractional part, ties to the lower k; top-F orders by
  *    (value descending, index ascending), -0 equal to +0.
  *
- * Every draw also records a margin: |r - p/q| for an accept test and the
- * distance of u to the two CDF boundaries of the chosen token for an
- * inverse-CDF draw.  The smallest margin of a sequence tells the tests
- * whether a finite-precision implementation may legitimately disagree.
+ * Every draw also records a margin: |r - p/q| for an accept test (the
+ * smallest over the tests of a sequence) and the distance of u to the two
+ * CDF boundaries of the chosen token for the inverse-CDF draw, plus the
+ * range of tokens whose CDF interval lies within ORC_BAND of u.  The margins
+ * tell the tests where a finite-precision implementation may legitimately
+ * disagree, and the range which tokens it may then return.
  */
 #include <math.h>
 #include <stdint.h>
@@ -123,10 +125,13 @@ static int argmax_row(const void *base, int dtype, size_t off, int V) {
 }
 
 /* Inverse-CDF draw from the weights w (not necessarily normalised, total
- * N > 0): the smallest j with C_j > u N.  Writes w_t / N and the margin
- * min(|u - C_{t-1}/N|, |u - C_t/N|). */
+ * N > 0): the smallest j with C_j > u N.  Writes w_t / N, the margin
+ * min(|u - C_{t-1}/N|, |u - C_t/N|), and the range [lo, hi] of every token
+ * whose interval [C_{j-1}/N, C_j/N] comes within ORC_BAND of u: the tokens a
+ * correct finite-precision draw may return. */
+#define ORC_BAND 1e-5
 static int sample_icdf(const double *w, int V, double u, double *prob,
-                       double *margin) {
+                       double *margin, int *lo, int *hi) {
   double N = 0.0;
   for (int j = 0; j < V; ++j) N += w[j];
   double target = u * N;
@@ -146,6 +151,21 @@ static int sample_icdf(const double *w, int V, double u, double *prob,
   *prob = w[t] / N;
   double m1 = fabs(u - Cprev / N), m2 = fabs(u - C / N);
   *margin = m1 < m2 ? m1 : m2;
+  /* walk outwards while neighbouring intervals touch [u - band, u + band] */
+  int a = t;
+  double left = Cprev; /* C_{a-1} */
+  while (a > 0 && left / N > u - ORC_BAND) {
+    --a;
+    left -= w[a];
+  }
+  int b = t;
+  double right = C; /* C_b */
+  while (b < V - 1 && right / N < u + ORC_BAND) {
+    ++b;
+    right += w[b];
+  }
+  *lo = a;
+  *hi = b;
   return t;
 }
 
@@ -172,16 +192,17 @@ int orc_verify_linear(const void *target, const void *draft, int dtype,
                       const int32_t *tokens, const float *uniforms, int B,
                       int gamma, int V, double T, int32_t *n_acc,
                       int32_t *out_tokens, double *out_prob,
-                      double *out_accept, double *margin, double *out_resid,
-                      int32_t *status) {
+                      double *out_accept, double *margin_acc,
+                      double *margin_cdf, int32_t *cdf_lo, int32_t *cdf_hi,
+                      double *out_resid, int32_t *status) {
   double *p = malloc(sizeof(double) * (size_t)V);
   double *q = malloc(sizeof(double) * (size_t)V);
   double *w = malloc(sizeof(double) * (size_t)V);
   if (!p || !q || !w) { free(p); free(q); free(w); return 1; }
   const int G1 = gamma + 1;
   for (int b = 0; b < B; ++b) {
-    int st = 0, n = 0, t = -1, invalid = 0;
-    double mg = INFINITY, prob = 0.0;
+    int st = 0, n = 0, t = -1, invalid = 0, lo = -1, hi = -1;
+    double mg = INFINITY, mc = INFINITY, prob = 0.0;
     for (int i = 0; i < gamma; ++i) out_accept[(size_t)b * gamma + i] = -1.0;
     if (T == 0.0) {
       for (int i = 0; i < gamma; ++i) {
@@ -198,6 +219,7 @@ int orc_verify_linear(const void *target, const void *draft, int dtype,
         t = argmax_row(target, dtype, ((size_t)b * G1 + n) * V, V);
         if (t < 0) invalid = 1;
         prob = 1.0;
+        lo = hi = t;
         if (out_resid && !invalid) {
           for (int j = 0; j < V; ++j) out_resid[(size_t)b * V + j] = 0.0;
           out_resid[(size_t)b * V + t] = 1.0;
@@ -248,10 +270,8 @@ int orc_verify_linear(const void *target, const void *draft, int dtype,
         }
       }
       if (!invalid) {
-        double mc;
         double u = (double)uniforms[(size_t)b * G1 + gamma];
-        t = sample_icdf(w, V, u, &prob, &mc);
-        note_margin(&mg, mc);
+        t = sample_icdf(w, V, u, &prob, &mc, &lo, &hi);
         if (out_resid) {
           double N = 0.0;
           for (int j = 0; j < V; ++j) N += w[j];
@@ -263,7 +283,8 @@ int orc_verify_linear(const void *target, const void *draft, int dtype,
       st |= ORC_ST_NONFINITE;
       n = -1;
       prob = 0.0;
-      mg = INFINITY;
+      mg = mc = INFINITY;
+      lo = hi = -1;
     }
     n_acc[b] = n;
     for (int i = 0; i < G1; ++i) {
@@ -275,7 +296,10 @@ int orc_verify_linear(const void *target, const void *draft, int dtype,
       out_tokens[(size_t)b * G1 + i] = v;
     }
     out_prob[b] = prob;
-    margin[b] = (T == 0.0) ? INFINITY : mg;
+    margin_acc[b] = (T == 0.0) ? INFINITY : mg;
+    margin_cdf[b] = (T == 0.0) ? INFINITY : mc;
+    cdf_lo[b] = lo;
+    cdf_hi[b] = hi;
     status[b] = st;
   }
   free(p); free(q); free(w);
@@ -295,7 +319,9 @@ int orc_verify_kcand(const void *target, const void *draft, int dtype,
                      const int32_t *tokens, const float *uniforms, int B,
                      int K, int gamma, int V, double T, int32_t *n_acc,
                      int32_t *sel_k, int32_t *out_tokens, int32_t *n_per_cand,
-                     double *out_prob, double *margin, int32_t *status) {
+                     double *out_prob, double *margin_acc,
+                     double *margin_cdf, int32_t *cdf_lo, int32_t *cdf_hi,
+                     int32_t *status) {
   double *p = malloc(sizeof(double) * (size_t)V);
   double *q = malloc(sizeof(double) * (size_t)V);
   double *w = malloc(sizeof(double) * (size_t)V);
@@ -304,8 +330,8 @@ int orc_verify_kcand(const void *target, const void *draft, int dtype,
 #define TROW(b, k, j) ((((size_t)(b) * K + (k)) * G1 + (j)) * (size_t)V)
 #define DROW(b, j) (((size_t)(b) * gamma + (j)) * (size_t)V)
   for (int b = 0; b < B; ++b) {
-    int st = 0, invalid = 0;
-    double mg = INFINITY, prob = 0.0;
+    int st = 0, invalid = 0, lo = -1, hi = -1;
+    double mg = INFINITY, mc = INFINITY, prob = 0.0;
     int best_k = 0, best_n = -1, t = -1;
     for (int k = 0; k < K && !invalid; ++k) {
       int n = 0;
@@ -346,6 +372,7 @@ int orc_verify_kcand(const void *target, const void *draft, int dtype,
         t = argmax_row(target, dtype, TROW(b, k, n), V);
         if (t < 0) invalid = 1;
         prob = 1.0;
+        lo = hi = t;
       } else {
         if (n < gamma) {
           if (!softmax_row(target, dtype, TROW(b, k, n), V, T, p) ||
@@ -370,10 +397,8 @@ int orc_verify_kcand(const void *target, const void *draft, int dtype,
             for (int j = 0; j < V; ++j) w[j] = p[j];
         }
         if (!invalid) {
-          double mc;
           double u = (double)uniforms[((size_t)b * K + k) * G1 + gamma];
-          t = sample_icdf(w, V, u, &prob, &mc);
-          note_margin(&mg, mc);
+          t = sample_icdf(w, V, u, &prob, &mc, &lo, &hi);
         }
       }
     }
@@ -383,7 +408,8 @@ int orc_verify_kcand(const void *target, const void *draft, int dtype,
       n_acc[b] = -1;
       sel_k[b] = -1;
       prob = 0.0;
-      mg = INFINITY;
+      mg = mc = INFINITY;
+      lo = hi = -1;
     } else {
       n_acc[b] = best_n;
       sel_k[b] = best_k;
@@ -397,7 +423,10 @@ int orc_verify_kcand(const void *target, const void *draft, int dtype,
       out_tokens[(size_t)b * G1 + i] = v;
     }
     out_prob[b] = prob;
-    margin[b] = (T == 0.0) ? INFINITY : mg;
+    margin_acc[b] = (T == 0.0) ? INFINITY : mg;
+    margin_cdf[b] = (T == 0.0) ? INFINITY : mc;
+    cdf_lo[b] = lo;
+    cdf_hi[b] = hi;
     status[b] = st;
   }
 #undef TROW
@@ -424,7 +453,8 @@ int orc_verify_tree(const void *target, const void *draft, int dtype,
                     const int32_t *parent, const int32_t *node_tokens,
                     const float *uniforms, int B, int N, int V, double T,
                     int32_t *n_acc, int32_t *out_tokens, int32_t *out_nodes,
-                    double *out_prob, double *margin, int32_t *status) {
+                    double *out_prob, double *margin_acc, double *margin_cdf,
+                    int32_t *cdf_lo, int32_t *cdf_hi, int32_t *status) {
   double *p = malloc(sizeof(double) * (size_t)V);
   double *q = malloc(sizeof(double) * (size_t)V);
   if (!p || !q) { free(p); free(q); return 1; }
@@ -432,8 +462,8 @@ int orc_verify_tree(const void *target, const void *draft, int dtype,
     const int32_t *par = parent + (size_t)b * N;
     const int32_t *tok = node_tokens + (size_t)b * N;
     const float *U = uniforms + (size_t)b * N;
-    int st = 0, invalid = 0, depth = 0, t = -1;
-    double mg = INFINITY, prob = 0.0;
+    int st = 0, invalid = 0, depth = 0, t = -1, lo = -1, hi = -1;
+    double mg = INFINITY, mc = INFINITY, prob = 0.0;
     for (int i = 0; i < N; ++i) {
       out_nodes[(size_t)b * N + i] = -1;
       out_tokens[(size_t)b * N + i] = -1;
@@ -456,7 +486,7 @@ int orc_verify_tree(const void *target, const void *draft, int dtype,
           if (tok[v] < 0 || tok[v] >= V) st |= ORC_ST_BAD_TOKEN;
           if (tok[v] == a) { next = v; break; }
         }
-        if (next < 0) { t = a; prob = 1.0; break; }
+        if (next < 0) { t = a; prob = 1.0; lo = hi = a; break; }
       } else {
         if (!softmax_row(target, dtype, off, V, T, p)) { invalid = 2; break; }
         if (has_child && !softmax_row(draft, dtype, off, V, T, q)) {
@@ -492,9 +522,7 @@ int orc_verify_tree(const void *target, const void *draft, int dtype,
           }
         }
         if (next < 0) {
-          double mc;
-          t = sample_icdf(p, V, (double)U[0], &prob, &mc);
-          note_margin(&mg, mc);
+          t = sample_icdf(p, V, (double)U[0], &prob, &mc, &lo, &hi);
           break;
         }
       }
@@ -511,13 +539,17 @@ int orc_verify_tree(const void *target, const void *draft, int dtype,
       }
       n_acc[b] = -1;
       prob = 0.0;
-      mg = INFINITY;
+      mg = mc = INFINITY;
+      lo = hi = -1;
     } else {
       n_acc[b] = depth;
       out_tokens[(size_t)b * N + depth] = t;
     }
     out_prob[b] = prob;
-    margin[b] = (T == 0.0) ? INFINITY : mg;
+    margin_acc[b] = (T == 0.0) ? INFINITY : mg;
+    margin_cdf[b] = (T == 0.0) ? INFINITY : mc;
+    cdf_lo[b] = lo;
+    cdf_hi[b] = hi;
     status[b] = st;
   }
   free(p); free(q);

@@ -365,47 +365,84 @@ __device__ __forceinline__ int warp_pick(const float (&w)[VW], float tau,
   return seg_first_elt + src_lane * VW + src_e;
 }
 
+// ------------------------------------------------------- row accessors
+// A row slice is read either straight from global memory (16-byte read-only
+// loads, several in flight per thread) or from a copy a TMA bulk load put
+// in shared memory.  Both give vector v (absolute index in the row).
+template <int DT, int VW>
+struct GRow {
+  const char *p;
+  static constexpr bool kSmem = false;
+  __device__ __forceinline__ Raw<DT, VW> get(int v) const {
+    return load_vec<DT, VW>(p, v);
+  }
+};
+
+template <int DT, int VW>
+struct SRow {
+  const uint4 *p;  // shared copy of the slice, vector vbeg at p[0]
+  int vbeg;
+  static constexpr bool kSmem = true;
+  __device__ __forceinline__ Raw<DT, VW> get(int v) const {
+    Raw<DT, VW> r;
+    r.w = p[v - vbeg];
+    return r;
+  }
+};
+
 // ------------------------------------------------------- streaming passes
-constexpr int kU = 4;  // vectors per thread in flight per row
+constexpr int kU = 4;  // vectors per thread in flight per row (global)
 
 // Accumulate the online softmax state of one or two rows over a slice.
-template <int DT, int VW>
-__device__ __forceinline__ void stats_pass(const char *ra, const char *rb,
-                                           const Slice &sl, float k2, MS &a,
-                                           MS &b) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int v0 = sl.vbeg + warp * 32 * kU + lane; v0 < sl.vend;
-       v0 += kWarps * 32 * kU) {
-    Raw<DT, VW> xa[kU], xb[kU];
+template <int DT, int VW, class Row>
+__device__ __forceinline__ void stats_pass(const Row &ra, const Row &rb,
+                                           bool has_b, const Slice &sl,
+                                           float k2, MS &a, MS &b) {
+  if constexpr (Row::kSmem) {
+    for (int v = sl.vbeg + (int)threadIdx.x; v < sl.vend; v += kThreads) {
+      ms_add<DT, VW>(a, ra.get(v), k2);
+      if (has_b) ms_add<DT, VW>(b, rb.get(v), k2);
+    }
+  } else {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int v0 = sl.vbeg + warp * 32 * kU + lane; v0 < sl.vend;
+         v0 += kWarps * 32 * kU) {
+      Raw<DT, VW> xa[kU], xb[kU];
 #pragma unroll
-    for (int u = 0; u < kU; ++u)
-      if (v0 + u * 32 < sl.vend) {
-        xa[u] = load_vec<DT, VW>(ra, v0 + u * 32);
-        if (rb) xb[u] = load_vec<DT, VW>(rb, v0 + u * 32);
-      }
+      for (int u = 0; u < kU; ++u)
+        if (v0 + u * 32 < sl.vend) {
+          xa[u] = ra.get(v0 + u * 32);
+          if (has_b) xb[u] = rb.get(v0 + u * 32);
+        }
 #pragma unroll
-    for (int u = 0; u < kU; ++u)
-      if (v0 + u * 32 < sl.vend) {
-        ms_add<DT, VW>(a, xa[u], k2);
-        if (rb) ms_add<DT, VW>(b, xb[u], k2);
-      }
+      for (int u = 0; u < kU; ++u)
+        if (v0 + u * 32 < sl.vend) {
+          ms_add<DT, VW>(a, xa[u], k2);
+          if (has_b) ms_add<DT, VW>(b, xb[u], k2);
+        }
+    }
   }
 }
 
 // Accumulate the greedy argmax state of one row over a slice.
-template <int DT, int VW>
-__device__ __forceinline__ void argmax_pass(const char *ra, const Slice &sl,
+template <int DT, int VW, class Row>
+__device__ __forceinline__ void argmax_pass(const Row &ra, const Slice &sl,
                                             AM &a) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int v0 = sl.vbeg + warp * 32 * kU + lane; v0 < sl.vend;
-       v0 += kWarps * 32 * kU) {
-    Raw<DT, VW> xa[kU];
+  if constexpr (Row::kSmem) {
+    for (int v = sl.vbeg + (int)threadIdx.x; v < sl.vend; v += kThreads)
+      am_add<DT, VW>(a, ra.get(v), v * VW);
+  } else {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int v0 = sl.vbeg + warp * 32 * kU + lane; v0 < sl.vend;
+         v0 += kWarps * 32 * kU) {
+      Raw<DT, VW> xa[kU];
 #pragma unroll
-    for (int u = 0; u < kU; ++u)
-      if (v0 + u * 32 < sl.vend) xa[u] = load_vec<DT, VW>(ra, v0 + u * 32);
+      for (int u = 0; u < kU; ++u)
+        if (v0 + u * 32 < sl.vend) xa[u] = ra.get(v0 + u * 32);
 #pragma unroll
-    for (int u = 0; u < kU; ++u)
-      if (v0 + u * 32 < sl.vend) am_add<DT, VW>(a, xa[u], (v0 + u * 32) * VW);
+      for (int u = 0; u < kU; ++u)
+        if (v0 + u * 32 < sl.vend) am_add<DT, VW>(a, xa[u], (v0 + u * 32) * VW);
+    }
   }
 }
 
@@ -421,37 +458,42 @@ template <int DT, int VW>
 __device__ __forceinline__ void weights(const Raw<DT, VW> &a,
                                         const Raw<DT, VW> &b, bool has_q,
                                         const Weight &W, float (&w)[VW]) {
+  // __fmul_rn keeps both products rounded before the subtraction (no FMA
+  // contraction), so identical p and q rows give exactly zero residual.
 #pragma unroll
   for (int e = 0; e < VW; ++e) {
-    const float pt = ex2(fmaf(elt<DT, VW>(a, e), W.k2, -W.mtk)) * W.ist;
+    const float pt =
+        __fmul_rn(ex2(fmaf(elt<DT, VW>(a, e), W.k2, -W.mtk)), W.ist);
     if (has_q) {
-      const float qd = ex2(fmaf(elt<DT, VW>(b, e), W.k2, -W.mdk)) * W.cq;
-      w[e] = fmaxf(0.f, pt - qd);
+      const float qd =
+          __fmul_rn(ex2(fmaf(elt<DT, VW>(b, e), W.k2, -W.mdk)), W.cq);
+      w[e] = fmaxf(0.f, __fsub_rn(pt, qd));
     } else {
       w[e] = pt;
     }
   }
 }
 
-// Per-segment masses of the weights over this CTA's slice.
-template <int DT, int VW>
-__device__ __forceinline__ void mass_pass(const char *ra, const char *rb,
-                                          const Weight &W, const Slice &sl,
-                                          float *segmass) {
+// Per-segment masses of the weights over this CTA's slice (segment s =
+// vectors vbeg + 32 s .. vbeg + 32 s + 31; one warp per segment).
+template <int DT, int VW, class Row>
+__device__ __forceinline__ void mass_pass(const Row &ra, const Row &rb,
+                                          bool has_q, const Weight &W,
+                                          const Slice &sl, float *segmass) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const bool has_q = rb != nullptr;
-  for (int s0 = warp; s0 < sl.nseg; s0 += kWarps * kU) {
-    Raw<DT, VW> xa[kU], xb[kU];
+  constexpr int UU = Row::kSmem ? 1 : kU;
+  for (int s0 = warp; s0 < sl.nseg; s0 += kWarps * UU) {
+    Raw<DT, VW> xa[UU], xb[UU];
 #pragma unroll
-    for (int u = 0; u < kU; ++u) {
+    for (int u = 0; u < UU; ++u) {
       const int v = sl.vbeg + (s0 + u * kWarps) * 32 + lane;
       if (s0 + u * kWarps < sl.nseg && v < sl.vend) {
-        xa[u] = load_vec<DT, VW>(ra, v);
-        if (has_q) xb[u] = load_vec<DT, VW>(rb, v);
+        xa[u] = ra.get(v);
+        if (has_q) xb[u] = rb.get(v);
       }
     }
 #pragma unroll
-    for (int u = 0; u < kU; ++u) {
+    for (int u = 0; u < UU; ++u) {
       const int s = s0 + u * kWarps;
       if (s < sl.nseg) {  // warp-uniform
         const int v = sl.vbeg + s * 32 + lane;
@@ -491,15 +533,15 @@ struct DrawOut {
 // uniform u: the smallest j with C_j > u * N.  Every thread of every CTA of
 // the cluster must call it (it holds one cluster barrier); `par` is the
 // caller's parity of the double-buffered slot.
-template <int DT, int VW>
+template <int DT, int VW, class Row>
 __device__ DrawOut cluster_draw(cg::cluster_group &cluster, DrawSmem &ds,
-                                float *segmass, const char *ra,
-                                const char *rb, const Weight &W,
-                                const Slice &sl, float u, int &par) {
+                                float *segmass, const Row &ra, const Row &rb,
+                                bool has_q, const Weight &W, const Slice &sl,
+                                float u, int &par) {
   const int tid = threadIdx.x;
   const int rank = (int)cluster.block_rank();
   const int CL = (int)cluster.num_blocks();
-  mass_pass<DT, VW>(ra, rb, W, sl, segmass);
+  mass_pass<DT, VW>(ra, rb, has_q, W, sl, segmass);
   __syncthreads();
   slice_prefix(segmass, sl.nseg, ds.chunk_pre);
   __syncthreads();
@@ -554,9 +596,9 @@ __device__ DrawOut cluster_draw(cg::cluster_group &cluster, DrawSmem &ds,
       const int v = sl.vbeg + s * 32 + tid;
       float w[VW];
       if (v < sl.vend) {
-        Raw<DT, VW> a = load_vec<DT, VW>(ra, v), b;
-        if (rb) b = load_vec<DT, VW>(rb, v);
-        weights<DT, VW>(a, b, rb != nullptr, W, w);
+        Raw<DT, VW> a = ra.get(v), b;
+        if (has_q) b = rb.get(v);
+        weights<DT, VW>(a, b, has_q, W, w);
       } else {
 #pragma unroll
         for (int e = 0; e < VW; ++e) w[e] = 0.f;
@@ -568,16 +610,17 @@ __device__ DrawOut cluster_draw(cg::cluster_group &cluster, DrawSmem &ds,
 }
 
 // Debug output: the normalised weights w_j / N over this CTA's slice.
-template <int DT, int VW>
-__device__ __forceinline__ void write_resid(float *res, const char *ra,
-                                            const char *rb, const Weight &W,
-                                            const Slice &sl, double N) {
+template <int DT, int VW, class Row>
+__device__ __forceinline__ void write_resid(float *res, const Row &ra,
+                                            const Row &rb, bool has_q,
+                                            const Weight &W, const Slice &sl,
+                                            double N) {
   const float invN = (float)(1.0 / N);
   for (int v = sl.vbeg + threadIdx.x; v < sl.vend; v += kThreads) {
-    Raw<DT, VW> a = load_vec<DT, VW>(ra, v), b;
-    if (rb) b = load_vec<DT, VW>(rb, v);
+    Raw<DT, VW> a = ra.get(v), b;
+    if (has_q) b = rb.get(v);
     float w[VW];
-    weights<DT, VW>(a, b, rb != nullptr, W, w);
+    weights<DT, VW>(a, b, has_q, W, w);
 #pragma unroll
     for (int e = 0; e < VW; ++e) res[(size_t)v * VW + e] = w[e] * invN;
   }

@@ -1,0 +1,229 @@
+// sdv_fanout.cu -- top-F_k draft tokens per lookahead position (Speculative
+// Speculative Decoding / Saguaro, "speculation cache strategy": the cache
+// is filled with the top-F_k tokens of the draft logits at each lookahead
+// position k; F follows the geometric fan-out of Theorem 12).
+//
+// One cluster (often a single CTA) owns one row at a time; rows all have
+// the same cost, so clusters take them round-robin.  Each CTA streams its
+// slice once, keeping a per-thread top-4 list, selects the slice's exact
+// top-F (sdv_topf.cuh), and for clusters of several CTAs rank 0 merges the
+// slice lists read through distributed shared memory.
+#include "sdv_host.cuh"
+#include "sdv_topf.cuh"
+
+namespace sdv {
+
+struct FanParams {
+  const void *draft;  // [B, K+1, V]
+  int B, K, V;
+  int F[SD_MAX_K + 1];
+  int off[SD_MAX_K + 2];
+  int32_t *out_tokens;  // [B, total]
+  float *out_logit;
+  int32_t *dev_status;
+  int nclusters;
+};
+
+struct FanSmem {
+  TopSmem top;
+  uint64_t slot[2][SD_MAX_FANOUT];  // [parity] this CTA's list (peers read)
+  int slot_n[2];
+  int slot_nan[2];
+  int nan_flag;
+};
+
+// Stream one row slice into a per-thread top list.
+template <int DT, int VW>
+__device__ __forceinline__ void topr_pass(const char *row, const Slice &sl,
+                                          TopR &t) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int v0 = sl.vbeg + warp * 32 * kU + lane; v0 < sl.vend;
+       v0 += kWarps * 32 * kU) {
+    Raw<DT, VW> x[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u)
+      if (v0 + u * 32 < sl.vend) x[u] = load_vec<DT, VW>(row, v0 + u * 32);
+#pragma unroll
+    for (int u = 0; u < kU; ++u)
+      if (v0 + u * 32 < sl.vend) topr_add_vec<DT, VW>(t, x[u], (v0 + u * 32) * VW);
+  }
+}
+
+// The same traversal, rebuilding a full descending top-F list (rescans).
+template <int DT, int VW>
+__device__ void topf_rescan(const char *row, const Slice &sl, uint64_t *loc,
+                            int F) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int r = 0; r < F; ++r) loc[r] = 0;
+  for (int v0 = sl.vbeg + warp * 32 * kU + lane; v0 < sl.vend;
+       v0 += kWarps * 32 * kU)
+    for (int u = 0; u < kU; ++u)
+      if (v0 + u * 32 < sl.vend) {
+        const Raw<DT, VW> x = load_vec<DT, VW>(row, v0 + u * 32);
+        for (int e = 0; e < VW; ++e) {
+          const float z = elt<DT, VW>(x, e);
+          if (z == z) local_insert(loc, F, make_key(ord32(z),
+                                                     (v0 + u * 32) * VW + e));
+        }
+      }
+}
+
+// Select the exact top-F of a row over a cluster and (rank 0) write it.
+template <int DT, int VW>
+__device__ void row_topf(cg::cluster_group &cluster, FanSmem &sh,
+                         const char *row, const Slice &sl, int F,
+                         int32_t *otok, float *olog, int32_t *dev_status,
+                         int &par) {
+  const int tid = threadIdx.x;
+  const int rank = (int)cluster.block_rank(), CL = (int)cluster.num_blocks();
+  TopR t;
+  topr_init(t);
+  topr_pass<DT, VW>(row, sl, t);
+  const int anynan = __syncthreads_or(t.nan);
+  const int nout = cta_topf(t, F, sh.top, [&](uint64_t *loc, int f) {
+    topf_rescan<DT, VW>(row, sl, loc, f);
+  });
+  if (CL == 1) {
+    for (int i = tid; i < F; i += kThreads) {
+      const bool ok = !anynan && i < nout;
+      otok[i] = ok ? key_idx(sh.top.out[i]) : -1;
+      if (olog) olog[i] = ok ? key_val(sh.top.out[i]) : __int_as_float(0x7fc00000);
+    }
+    if (tid == 0 && anynan) status_or(dev_status, SD_DEV_NONFINITE);
+    __syncthreads();
+    return;
+  }
+  for (int i = tid; i < F; i += kThreads)
+    sh.slot[par][i] = i < nout ? sh.top.out[i] : 0;
+  if (tid == 0) {
+    sh.slot_n[par] = nout;
+    sh.slot_nan[par] = anynan;
+  }
+  cluster.sync();
+  if (rank == 0) {
+    // gather the CL lists and rank them (keys unique, 0 = empty)
+    int C = 0;
+    if (tid == 0) sh.nan_flag = 0;
+    __syncthreads();
+    for (int r = 0; r < CL; ++r) {
+      const FanSmem *rs = cluster.map_shared_rank(&sh, r);
+      const int nr = rs->slot_n[par];
+      for (int i = tid; i < nr; i += kThreads) sh.top.list[C + i] = rs->slot[par][i];
+      if (tid == 0 && rs->slot_nan[par]) sh.nan_flag = 1;
+      C += nr;
+    }
+    __syncthreads();
+    const int n = rank_select(sh.top, C, F);
+    const int bad = sh.nan_flag;
+    for (int i = tid; i < F; i += kThreads) {
+      const bool ok = !bad && i < n;
+      otok[i] = ok ? key_idx(sh.top.out[i]) : -1;
+      if (olog) olog[i] = ok ? key_val(sh.top.out[i]) : __int_as_float(0x7fc00000);
+    }
+    if (tid == 0 && bad) status_or(dev_status, SD_DEV_NONFINITE);
+  }
+  par ^= 1;
+  __syncthreads();
+}
+
+template <int DT, int VW>
+__global__ void __launch_bounds__(kThreads, 2) fanout_kernel(const FanParams p) {
+  __shared__ FanSmem sh;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = (int)cluster.block_rank(), CL = (int)cluster.num_blocks();
+  const int V = p.V, K1 = p.K + 1;
+  const Slice sl = make_slice(V / VW, rank, CL);
+  const size_t rowb = (size_t)V * elt_bytes<DT>();
+  const char *base = static_cast<const char *>(p.draft);
+  const int total = p.off[K1];
+  int par = 0;
+  const long long rows = (long long)p.B * K1;
+  for (long long r = blockIdx.x / CL; r < rows; r += p.nclusters) {
+    const int b = (int)(r / K1), k = (int)(r % K1);
+    const int F = p.F[k];
+    if (F == 0) continue;
+    int32_t *otok = p.out_tokens + (size_t)b * total + p.off[k];
+    float *olog = p.out_logit ? p.out_logit + (size_t)b * total + p.off[k]
+                              : nullptr;
+    row_topf<DT, VW>(cluster, sh, base + (size_t)r * rowb, sl, F, otok, olog,
+                     p.dev_status, par);
+  }
+  cluster.sync();
+}
+
+using FanKernel = void (*)(const FanParams);
+
+static FanKernel pick_fanout(int dt, bool vec) {
+  if (dt == SD_F32) return vec ? fanout_kernel<0, 4> : fanout_kernel<0, 1>;
+  return vec ? fanout_kernel<1, 8> : fanout_kernel<1, 1>;
+}
+
+}  // namespace sdv
+
+extern "C" size_t sd_fanout_topk_workspace(int B, int K, int V, sd_dtype dt) {
+  (void)B;
+  (void)K;
+  (void)V;
+  (void)dt;
+  return 0;
+}
+
+extern "C" sd_status sd_fanout_topk(const void *draft_logits, sd_dtype dt,
+                                    int B, int K, int V, const int32_t *F,
+                                    int32_t *out_tokens, float *out_logit,
+                                    int32_t *dev_status, void *workspace,
+                                    size_t ws_bytes, void *stream) {
+  using namespace sdv;
+  (void)workspace;
+  (void)ws_bytes;
+  SDV_REQUIRE(dt == SD_F32 || dt == SD_BF16, "bad dtype %d", (int)dt);
+  SDV_REQUIRE(B >= 0, "B < 0");
+  SDV_REQUIRE(K >= 0 && K <= SD_MAX_K, "K=%d outside [0, %d]", K, SD_MAX_K);
+  SDV_REQUIRE(V >= 1 && V <= SD_MAX_V, "V=%d outside [1, %d]", V, SD_MAX_V);
+  SDV_REQUIRE(F != nullptr, "F is null");
+  FanParams prm;
+  int total = 0;
+  for (int k = 0; k <= K; ++k) {
+    SDV_REQUIRE(F[k] >= 0, "F[%d] < 0", k);
+    if (F[k] > SD_MAX_FANOUT || F[k] > V)
+      return fail(SD_ERR_UNSUPPORTED, "F[%d]=%d exceeds min(V, %d)", k, F[k],
+                  SD_MAX_FANOUT);
+    prm.F[k] = F[k];
+    prm.off[k] = total;
+    total += F[k];
+  }
+  prm.off[K + 1] = total;
+  if (B == 0 || total == 0) return SD_OK;
+  SDV_REQUIRE(draft_logits && out_tokens, "null pointer");
+  int sms = 0;
+  sd_status st = check_device(&sms);
+  if (st != SD_OK) return st;
+  const int eb = dt == SD_F32 ? 4 : 2, vw = dt == SD_F32 ? 4 : 8;
+  const bool vec = aligned16(draft_logits) && ((size_t)V * eb) % 16 == 0;
+  const long long nvec = V / (vec ? vw : 1);
+  FanKernel kern = pick_fanout(dt, vec);
+  // rows of equal cost: a single CTA per row unless the rows are too few to
+  // fill the GPU, then clusters that split each row
+  const long long rows = (long long)B * (K + 1);
+  int CL = 1;
+  const int forced = env_int("SDV_FANOUT_CLUSTER", 0);
+  if (forced == 1 || forced == 2 || forced == 4 || forced == 8 || forced == 16)
+    CL = forced;
+  else
+    while (CL < 16 && rows * CL < 4LL * sms && nvec / (2 * CL) >= 512) CL *= 2;
+  int maxc = 0;
+  st = max_active_clusters((const void *)kern, CL, 0, &maxc);
+  if (st != SD_OK) return st;
+  const long long want = (rows + 0) < (long long)maxc ? rows : maxc;
+  prm.draft = draft_logits;
+  prm.B = B;
+  prm.K = K;
+  prm.V = V;
+  prm.out_tokens = out_tokens;
+  prm.out_logit = out_logit;
+  prm.dev_status = dev_status;
+  prm.nclusters = (int)want;
+  void *args[] = {&prm};
+  return launch_clusters((const void *)kern, (int)want, CL, 0,
+                         static_cast<cudaStream_t>(stream), args);
+}

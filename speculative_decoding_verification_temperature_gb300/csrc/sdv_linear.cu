@@ -18,8 +18,17 @@
 // Clusters take sequences from a work counter, so short and long scans
 // balance across the GPU.  Greedy (T == 0) compares draft ids with the
 // row argmax (section 2.2) and reads no draft logits.
+//
+// Two ways to read a step's slices: TMA bulk copies (cp.async.bulk with an
+// mbarrier) into shared memory, where the slice then stays for the draw
+// (no second read at all), used when rows are 16-byte aligned and the
+// slices fit; or 16-byte loads from global memory with several in flight
+// per thread (the draw then re-reads the slice, from L2).
+#include <type_traits>
+
 #include "sdv_device.cuh"
 #include "sdv_host.cuh"
+#include "sdv_tma.cuh"
 
 namespace sdv {
 
@@ -39,6 +48,8 @@ struct LinearParams {
   int32_t *dev_status;
   int *queue;  // nullable: then cluster c verifies sequence c only
   int nclusters;
+  int seg_bytes;   // bytes of the segment-mass array (multiple of 128)
+  int slice_vecs;  // capacity of each slice buffer in 16-byte vectors (TMA)
 };
 
 struct Decision {
@@ -62,11 +73,13 @@ struct LinearSmem {
   DrawSmem draw;
 };
 
-template <int DT, int VW, bool GREEDY>
-__global__ void __launch_bounds__(kThreads, 2)
+template <int DT, int VW, bool GREEDY, bool TMA>
+__global__ void __launch_bounds__(kThreads, TMA ? 3 : 2)
     linear_verify_kernel(const LinearParams p) {
-  extern __shared__ float segmass[];
+  extern __shared__ __align__(128) unsigned char dsm[];
   __shared__ LinearSmem sh;
+  __shared__ uint64_t bar;  // TMA completion barrier
+  using Row = std::conditional_t<TMA, SRow<DT, VW>, GRow<DT, VW>>;
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
   const int CL = (int)cluster.num_blocks();
@@ -77,6 +90,28 @@ __global__ void __launch_bounds__(kThreads, 2)
   const char *tbase = static_cast<const char *>(p.target);
   const char *dbase = static_cast<const char *>(p.draft);
   const float k2 = p.k2;
+  // dynamic shared memory: segment masses, then the two slice buffers
+  float *segmass = reinterpret_cast<float *>(dsm);
+  uint4 *tbuf = reinterpret_cast<uint4 *>(dsm + p.seg_bytes);
+  uint4 *dbuf = tbuf + p.slice_vecs;
+  const uint32_t slice_bytes = (uint32_t)(sl.vend - sl.vbeg) * 16u;
+  uint32_t phase = 0;
+  if (TMA) {
+    if (tid == 0) {
+      mbar_init(&bar, 1);
+      fence_mbar_init();
+    }
+    __syncthreads();
+  }
+  auto row_of = [&](const char *g, uint4 *buf) {
+    if constexpr (TMA) {
+      (void)g;
+      return Row{buf, sl.vbeg};
+    } else {
+      (void)buf;
+      return Row{g};
+    }
+  };
 
   int par = 0, seqpar = 0;
   int seq = (int)(blockIdx.x / CL);
@@ -92,6 +127,14 @@ __global__ void __launch_bounds__(kThreads, 2)
       const char *trow = tbase + ((size_t)seq * (gamma + 1) + i) * rowb;
       const char *drow =
           has_d ? dbase + ((size_t)seq * p.d_seq_rows + i) * rowb : nullptr;
+      if (TMA && tid == 0) {  // this step's slices -> shared memory
+        fence_proxy_async();
+        mbar_expect_tx(&bar, slice_bytes * (has_d ? 2u : 1u));
+        if (slice_bytes) {
+          bulk_g2s(tbuf, trow + (size_t)sl.vbeg * 16, slice_bytes, &bar);
+          if (has_d) bulk_g2s(dbuf, drow + (size_t)sl.vbeg * 16, slice_bytes, &bar);
+        }
+      }
       if (tid == 0) {  // gathers for the accept test (used after the merge)
         int x = -1;
         float zt = 0.f, zd = 0.f;
@@ -108,14 +151,19 @@ __global__ void __launch_bounds__(kThreads, 2)
         sh.gr[par] =
             GREEDY ? 0.f : p.uniforms[(size_t)seq * (gamma + 1) + i];
       }
+      if (TMA) {
+        mbar_wait(&bar, phase, p.dev_status);
+        phase ^= 1;
+      }
+      const Row ra = row_of(trow, tbuf), rb = row_of(drow, dbuf);
       if constexpr (GREEDY) {
         AM a = am_empty();
-        argmax_pass<DT, VW>(trow, sl, a);
+        argmax_pass<DT, VW>(ra, sl, a);
         a = block_reduce_am(a, sh.ared);
         if (tid == 0) sh.apart[par] = a;
       } else {
         MS st[2] = {ms_empty(), ms_empty()};
-        stats_pass<DT, VW>(trow, drow, sl, k2, st[0], st[1]);
+        stats_pass<DT, VW>(ra, rb, has_d, sl, k2, st[0], st[1]);
         block_reduce_ms<2>(st, k2, sh.red);
         if (tid == 0) {
           sh.part[par][0] = st[0];
@@ -221,10 +269,14 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
     } else {
       // correction (kind 1) or bonus (kind 2) by inverse CDF
+      // the rows of the draw are the last step's (already in shared memory
+      // on the TMA path)
       const char *trow = tbase + ((size_t)seq * (gamma + 1) + n) * rowb;
       const char *drow =
           kind == 1 ? dbase + ((size_t)seq * p.d_seq_rows + n) * rowb
                     : nullptr;
+      const Row ra = row_of(trow, tbuf), rb = row_of(drow, dbuf);
+      bool has_q = kind == 1;
       Weight W;
       W.k2 = k2;
       W.mtk = fmt.m * k2;
@@ -232,14 +284,14 @@ __global__ void __launch_bounds__(kThreads, 2)
       W.mdk = fmd.m * k2;
       W.cq = 1.f / fmd.s;
       const float u = p.uniforms[(size_t)seq * (gamma + 1) + gamma];
-      DrawOut o = cluster_draw<DT, VW>(cluster, sh.draw, segmass, trow, drow,
-                                       W, sl, u, par);
+      DrawOut o = cluster_draw<DT, VW>(cluster, sh.draw, segmass, ra, rb,
+                                       has_q, W, sl, u, par);
       int zero_mass = 0;
       if (o.owner < 0) {  // residual of zero mass: draw from p_n instead
         zero_mass = 1;
-        drow = nullptr;
+        has_q = false;
         __syncthreads();
-        o = cluster_draw<DT, VW>(cluster, sh.draw, segmass, trow, nullptr, W,
+        o = cluster_draw<DT, VW>(cluster, sh.draw, segmass, ra, rb, false, W,
                                  sl, u, par);
       }
       if (o.owner == rank && warp == 0) {
@@ -260,8 +312,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
       }
       if (p.out_resid)
-        write_resid<DT, VW>(p.out_resid + (size_t)seq * V, trow, drow, W, sl,
-                            o.N);
+        write_resid<DT, VW>(p.out_resid + (size_t)seq * V, ra, rb, has_q, W,
+                            sl, o.N);
     }
     // next sequence (rank 0 published it before this sequence's first sync)
     seq = cluster.map_shared_rank(&sh, 0)->next_seq[seqpar];
@@ -275,20 +327,26 @@ __global__ void __launch_bounds__(kThreads, 2)
 
 using LinearKernel = void (*)(const LinearParams);
 
-static LinearKernel pick_linear(int dt, bool vec, bool greedy) {
-  if (dt == SD_F32) {
-    if (vec)
-      return greedy ? linear_verify_kernel<0, 4, true>
-                    : linear_verify_kernel<0, 4, false>;
-    return greedy ? linear_verify_kernel<0, 1, true>
-                  : linear_verify_kernel<0, 1, false>;
-  }
-  if (vec)
-    return greedy ? linear_verify_kernel<1, 8, true>
-                  : linear_verify_kernel<1, 8, false>;
-  return greedy ? linear_verify_kernel<1, 1, true>
-                : linear_verify_kernel<1, 1, false>;
+template <int DT, int VW, bool TMA>
+static LinearKernel pick_linear_t(bool greedy) {
+  return greedy ? linear_verify_kernel<DT, VW, true, TMA>
+                : linear_verify_kernel<DT, VW, false, TMA>;
 }
+
+static LinearKernel pick_linear(int dt, bool vec, bool tma, bool greedy) {
+  if (dt == SD_F32) {
+    if (!vec) return pick_linear_t<0, 1, false>(greedy);
+    return tma ? pick_linear_t<0, 4, true>(greedy)
+               : pick_linear_t<0, 4, false>(greedy);
+  }
+  if (!vec) return pick_linear_t<1, 1, false>(greedy);
+  return tma ? pick_linear_t<1, 8, true>(greedy)
+             : pick_linear_t<1, 8, false>(greedy);
+}
+
+// Largest dynamic shared memory per CTA for the TMA path (two slice
+// buffers + segment masses), chosen so that three CTAs share an SM.
+constexpr size_t kTmaSmemMax = 72 * 1024;
 
 sd_status linear_launch(const void *target, const void *draft, sd_dtype dt,
                         long long d_seq_rows, const int32_t *tokens,
@@ -309,11 +367,15 @@ sd_status linear_launch(const void *target, const void *draft, sd_dtype dt,
   const long long nvec = V / VW;
   const int CL = choose_cluster(nvec);
   const long long per_cta = (nvec + CL - 1) / CL;
-  const size_t smem = (size_t)((per_cta + 31) / 32) * sizeof(float) + 16;
+  const size_t seg_bytes = ((size_t)((per_cta + 31) / 32) * 4 + 127) / 128 * 128;
+  const size_t tma_smem = seg_bytes + 2 * (size_t)per_cta * 16;
+  const bool tma = vec && tma_smem <= kTmaSmemMax &&
+                   env_int("SDV_NO_TMA", 0) == 0;
+  const size_t smem = tma ? tma_smem : seg_bytes;
   if (smem > 96 * 1024)
     return fail(SD_ERR_UNSUPPORTED, "V=%d needs %zu B of shared memory", V,
                 smem);
-  LinearKernel kern = pick_linear(dt, vec, greedy);
+  LinearKernel kern = pick_linear(dt, vec, tma, greedy);
   int maxc = 0;
   st = max_active_clusters((const void *)kern, CL, smem, &maxc);
   if (st != SD_OK) return st;
@@ -336,6 +398,8 @@ sd_status linear_launch(const void *target, const void *draft, sd_dtype dt,
   prm.dev_status = dev_status;
   prm.queue = nullptr;
   prm.nclusters = nclusters;
+  prm.seg_bytes = (int)seg_bytes;
+  prm.slice_vecs = (int)per_cta;
   if (B > nclusters) {
     if (!ws || ws_bytes < 256)
       return fail(SD_ERR_INVALID_ARG, "workspace of >= 256 bytes required");

@@ -22,14 +22,6 @@ extern "C" sd_status sd_verify_tree(const void *, const void *, sd_dtype,
                                     int32_t *, void *, size_t, void *) {
   return sdv::fail(SD_ERR_UNSUPPORTED, "sd_verify_tree: not built");
 }
-extern "C" size_t sd_fanout_topk_workspace(int, int, int, sd_dtype) {
-  return 256;
-}
-extern "C" sd_status sd_fanout_topk(const void *, sd_dtype, int, int, int,
-                                    const int32_t *, int32_t *, float *,
-                                    int32_t *, void *, size_t, void *) {
-  return sdv::fail(SD_ERR_UNSUPPORTED, "sd_fanout_topk: not built");
-}
 extern "C" size_t sd_verify_linear_fanout_workspace(int, int, int, sd_dtype) {
   return 256;
 }

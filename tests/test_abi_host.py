@@ -1,0 +1,81 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads and
+exports every entry point include/sd_verify.h declares, argument validation
+rejects bad calls before any launch, and the host-only fan-out schedule
+matches the oracle."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from speculative_decoding_verification_temperature_gb300 import api
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include",
+                      "sd_verify.h")
+
+
+def declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(sd_[a-z_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported():
+    L = api.lib()
+    names = declared()
+    assert len(names) >= 13
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_version_and_last_error():
+    assert "sm_103a" in api.version()
+    L = api.lib()
+    rc = L.sd_verify_linear(None, None, 0, None, None, 1, 4, 0, 1.0, None,
+                            None, None, None, None, None, None, 0, None)
+    assert rc == api.SD_ERR_INVALID_ARG
+    assert b"V=0" in L.sd_last_error()
+
+
+@pytest.mark.parametrize("args", [
+    dict(B=-1), dict(gamma=-1), dict(gamma=65), dict(V=0), dict(V=1 << 25),
+    dict(T=-1.0), dict(T=float("nan")), dict(T=float("inf")), dict(dt=7),
+    dict(target=None), dict(draft=None), dict(tokens=None), dict(uni=None),
+])
+def test_linear_validation(args):
+    L = api.lib()
+    p = ctypes.c_void_p(16)
+    a = dict(target=p, draft=p, dt=0, tokens=p, uni=p, B=2, gamma=3, V=100,
+             T=1.0)
+    a.update(args)
+    rc = L.sd_verify_linear(a["target"], a["draft"], a["dt"], a["tokens"],
+                            a["uni"], a["B"], a["gamma"], a["V"], a["T"], p,
+                            p, None, None, None, None, p, 256, None)
+    assert rc == api.SD_ERR_INVALID_ARG, args
+
+
+def test_empty_batch_is_a_no_op():
+    L = api.lib()
+    rc = L.sd_verify_linear(None, None, 0, None, None, 0, 3, 100, 1.0, None,
+                            None, None, None, None, None, None, 0, None)
+    assert rc == api.SD_OK
+
+
+@pytest.mark.parametrize("K,budget,a,r", [
+    (8, 64, 0.8, 1.0), (4, 20, 0.6, 0.5), (6, 40, 0.7, 1.0),
+    (8, 128, 0.9, 2.0), (0, 5, 0.5, 1.0), (3, 0, 0.5, 1.0), (32, 1000, 0.95, 1.0),
+    (2, 9, 0.5, 1.0), (5, 7, 0.3, 3.0)])
+def test_fanout_schedule_matches_oracle(K, budget, a, r):
+    F = api.fanout_schedule(K, budget, a, r)
+    assert F == [int(x) for x in oracle.fanout_schedule(K, budget, a, r)]
+    assert sum(F) == budget
+
+
+@pytest.mark.parametrize("K,budget,a,r", [
+    (-1, 5, 0.5, 1.0), (33, 5, 0.5, 1.0), (3, -1, 0.5, 1.0),
+    (3, 5, 0.0, 1.0), (3, 5, 1.0, 1.0), (3, 5, 0.5, 0.0)])
+def test_fanout_schedule_rejects(K, budget, a, r):
+    with pytest.raises(api.SdError):
+        api.fanout_schedule(K, budget, a, r)

@@ -1,0 +1,84 @@
+"""Parity of sd_fanout_topk (CUDA, through the C ABI) with the oracle: the
+top-F_k draft tokens of every lookahead row, ordered by (logit desc, id
+asc), on the large workload's rows and on rows built to stress the exact
+selection (ties, sorted rows, constant rows, NaN, F up to 64)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from speculative_decoding_verification_temperature_gb300 import api, synth
+from tests.parity import host
+
+pytestmark = pytest.mark.gpu
+
+
+def check(draft, F):
+    g = api.fanout_topk(draft, F, want_logit=True)
+    o = oracle.fanout_topk(synth.host_logits(draft), np.array(F, np.int32))
+    np.testing.assert_array_equal(host(g["tokens"]), o["tokens"])
+    ok = o["tokens"] >= 0
+    np.testing.assert_array_equal(host(g["logit"])[ok].astype(np.float64),
+                                  o["logit"][ok])
+    return g, o
+
+
+def test_large_workload_rows_sampled():
+    """The 9 draft rows of 12 sequences of the large workload (V=128256
+    fp32), geometric F = [10,9,8,7,6,6,5,4,9]."""
+    c = synth.large(0, device="cuda")
+    F = api.fanout_schedule(8, 64, 0.8, 1.0)
+    assert F == [10, 9, 8, 7, 6, 6, 5, 4, 9]
+    idx = torch.tensor([0, 1, 2, 50, 100, 127, 128, 200, 250, 253, 254, 255],
+                       device="cuda")
+    check(c.draft[idx].contiguous(), F)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("V", [5, 64, 1000, 4099, 32000, 151936])
+def test_random_rows(dtype, V):
+    g = torch.Generator().manual_seed(V)
+    d = (torch.randn((6, 4, V), generator=g) * 3).to(dtype)
+    F = [min(V, f) for f in (10, 1, 0, 64)]
+    check(d.cuda(), F)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_ties_sorted_and_constant_rows(dtype):
+    """Integer logits (many exact ties), rows sorted ascending and
+    descending (the best keys crowd into few threads: exercises the exact
+    rescan), constant rows (ties everywhere) and -0 / +0."""
+    V = 20000
+    g = torch.Generator().manual_seed(1)
+    rows = [torch.randint(-5, 6, (V,), generator=g).float(),
+            torch.arange(V).float(),
+            -torch.arange(V).float(),
+            torch.zeros(V),
+            torch.where(torch.arange(V) % 2 == 0, torch.tensor(-0.0),
+                        torch.tensor(0.0))]
+    d = torch.stack(rows)[:, None, :].expand(5, 3, V).contiguous().to(dtype)
+    check(d.cuda(), [64, 17, 1])
+
+
+def test_nan_row_and_status():
+    d = torch.randn((3, 2, 3000))
+    d[1, 0, 123] = float("nan")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = api.fanout_topk(d.cuda(), [5, 3], status=st)
+    o = oracle.fanout_topk(d.numpy(), np.array([5, 3], np.int32))
+    np.testing.assert_array_equal(host(out["tokens"]), o["tokens"])
+    assert int(st.item()) & api.DEV_NONFINITE
+
+
+def test_misaligned_rows_scalar_path():
+    V = 1003
+    d = torch.randn((4, 3, V)) * 2
+    check(d.cuda(), [7, 0, 12])
+
+
+def test_limits_rejected():
+    d = torch.randn((2, 2, 100), device="cuda")
+    with pytest.raises(api.SdError):
+        api.fanout_topk(d, [65, 1])
+    with pytest.raises(api.SdError):
+        api.fanout_topk(torch.randn((2, 2, 10), device="cuda"), [11, 1])

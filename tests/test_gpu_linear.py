@@ -36,9 +36,9 @@ def test_tiny_workload_single_calls():
         c = to_device(synth.tiny(rnd))
         g = run(c, want_accept=True)
         o = linear_oracle(c)
-        f, _ = compare(g, o)
-        flagged += f
-        if not f:
+        r = compare(g, o)
+        flagged += r["acc_flagged"]
+        if not r["acc_flagged"]:
             ev = o["accept"] >= 0
             np.testing.assert_allclose(host(g["accept"])[ev], o["accept"][ev],
                                        atol=1e-5)
@@ -50,9 +50,8 @@ def test_tiny_workload_batched_1000_rounds():
     """1000 independent tiny rounds in one call (queue path)."""
     c = to_device(synth.linear_case(1000, 4, 1000, torch.float32, 1.0,
                                     seed=1000, sigma_t=2.0, sigma_d=1.0))
-    g = run(c)
-    f, n = compare(g, linear_oracle(c))
-    assert f / n < 5e-3
+    r = compare(run(c), linear_oracle(c))
+    assert r["acc_flagged"] / r["seqs"] < 5e-3
 
 
 @pytest.mark.parametrize("T", [0.0, 0.7, 1.0])
@@ -62,11 +61,11 @@ def test_linear_workload(T):
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     g = run(c, want_accept=True, status=st)
     o = linear_oracle(c)
-    f, n = compare(g, o)
+    r = compare(g, o)
     if T == 0:
-        assert f == 0
+        assert r["acc_flagged"] == 0 and r["cdf_flagged"] == 0
     assert int(st.item()) == 0
-    ok = o["margin"] >= oracle.FLAG_MARGIN
+    ok = o["margin_acc"] >= oracle.FLAG_MARGIN
     ev = (o["accept"] >= 0) & ok[:, None]
     np.testing.assert_allclose(host(g["accept"])[ev], o["accept"][ev],
                                atol=1e-5)
@@ -124,7 +123,8 @@ def test_resid_and_accept_debug_outputs():
         g = run(c, want_resid=True)
         o = linear_oracle(c, want_resid=True)
         compare(g, o)
-        ok = o["margin"] >= oracle.FLAG_MARGIN
+        ok = (o["margin_acc"] >= oracle.FLAG_MARGIN) & \
+            (host(g["tokens"]) == o["tokens"]).all(axis=1)
         np.testing.assert_allclose(host(g["resid"])[ok], o["resid"][ok],
                                    atol=1e-5)
 
@@ -199,10 +199,14 @@ def test_emitted_token_law_on_gpu():
     assert stats.chi2.sf(stat, V - 1) > 1e-4
 
 
-def test_flagged_fraction_is_small():
-    """Over 20000 sequences of the tiny workload the oracle flags well under
-    1e-3 of the sequences and every unflagged one matches exactly."""
+def test_flagged_fractions():
+    """Over 20000 sequences of the tiny workload: accept tests within 1e-5
+    of their threshold stay under 1e-3 of the sequences; every other
+    sequence matches exactly, and near-boundary final draws (counted) stay
+    inside the oracle's admissible range and almost always equal its
+    token."""
     c = to_device(synth.linear_case(20000, 4, 1000, torch.float32, 1.0,
                                     seed=77, sigma_t=2.0, sigma_d=1.0))
-    f, n = compare(run(c), linear_oracle(c))
-    assert f / n < 1e-3
+    r = compare(run(c), linear_oracle(c))
+    assert r["acc_flagged"] / r["seqs"] < 1e-3
+    assert r["cdf_diff"] <= max(2, r["cdf_flagged"] // 20)

@@ -56,8 +56,8 @@ MUTANTS = [
     ("tree_no_residual_update", "p[j] = d > 0.0 ? d : 0.0;\n            S += p[j];",
      "S += (d > 0.0 ? d : 0.0);", 1,
      ["test_tree_iid_siblings_lossless"]),
-    ("tree_final_uniform_slot", "t = sample_icdf(p, V, (double)U[0], &prob, &mc);",
-     "t = sample_icdf(p, V, (double)U[1], &prob, &mc);", 1,
+    ("tree_final_uniform_slot", "sample_icdf(p, V, (double)U[0],",
+     "sample_icdf(p, V, (double)U[1],", 1,
      ["test_tree_chain_equals_linear", "test_tree_iid_siblings_lossless"]),
     ("fanout_exponent", "w[k] = pow(a, (double)k / (1.0 + r));",
      "w[k] = pow(a, (double)k / r);", 1,
