@@ -201,8 +201,9 @@ def gpu_arm(args, rank, world):
         "clocks": clk,
         "wall_s": wall,
     }
-    res["e2e"] = e2e_arm(args, sets, dev, ws, world)
-    if rank == 0:
+    if args.e2e_steps > 0:
+        res["e2e"] = e2e_arm(args, sets, dev, ws, world)
+    if rank == 0 and args.oracle_seqs > 0:
         res["cpu_baseline"] = cpu_baseline(sets, args.oracle_seqs)
     return res
 
@@ -268,7 +269,7 @@ def cpu_baseline(sets, nseq):
     return {"value": 1.0 / per_round, "unit": "rounds/s", "cores": 1,
             "kind": "oracle",
             "sample": "fp64 C oracle, single thread, on %d of the %d "
-                      "sequences of one round (%.1f s), scaled to a full "
+                      "sequences of one round (%.2f s), scaled to a full "
                       "round" % (nseq, B, dt)}
 
 
@@ -323,9 +324,13 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="native",
                     choices=["native", "reference"])
-    ap.add_argument("--sets", type=int, default=3)
-    ap.add_argument("--e2e-steps", type=int, default=20)
-    ap.add_argument("--oracle-seqs", type=int, default=16)
+    ap.add_argument("--sets", type=int, default=3,
+                    help="input sets rotated between steps")
+    ap.add_argument("--e2e-steps", type=int, default=20,
+                    help="steps of the host-buffer leg (0: skip it)")
+    ap.add_argument("--oracle-seqs", type=int, default=256,
+                    help="sequences of one round the CPU oracle times "
+                         "(0: skip the CPU baseline)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world = int(os.environ.get("WORLD_SIZE", "1"))

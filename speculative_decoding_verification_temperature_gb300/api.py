@@ -35,7 +35,8 @@ def lib() -> ctypes.CDLL:
     global _lib
     with _lock:
         if _lib is None:
-            path = _build.build()
+            # SDV_LIB selects another build of the same library
+            path = os.environ.get("SDV_LIB") or _build.build()
             if not os.path.exists(path):
                 raise RuntimeError("libsdverify.so is missing: run "
                                    "__graft_entry__.build()")

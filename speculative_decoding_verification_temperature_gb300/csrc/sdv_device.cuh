@@ -529,6 +529,55 @@ struct DrawOut {
   float wt;  // its weight (probability wt / N)
 };
 
+// Cluster-wide total of the weights W over the row(s): every CTA writes its
+// per-segment masses and slice total, one cluster barrier, then warp 0 of
+// every CTA forms the running sums of the slice totals in rank order (all
+// CTAs do the same arithmetic, so all agree).  With `u` >= 0 it also finds
+// the CTA whose slice holds the crossing C > u N and the target left in it.
+// Every thread of every CTA of the cluster must call it.
+template <int DT, int VW, class Row>
+__device__ double cluster_mass(cg::cluster_group &cluster, DrawSmem &ds,
+                               float *segmass, const Row &ra, const Row &rb,
+                               bool has_q, const Weight &W, const Slice &sl,
+                               float u, int &par) {
+  const int tid = threadIdx.x;
+  const int CL = (int)cluster.num_blocks();
+  mass_pass<DT, VW>(ra, rb, has_q, W, sl, segmass);
+  __syncthreads();
+  slice_prefix(segmass, sl.nseg, ds.chunk_pre);
+  __syncthreads();
+  if (tid == 0) ds.slice[par] = sl.nseg ? ds.chunk_pre[31] : 0.0;
+  cluster.sync();
+  if (tid < 32) {
+    // lane r reads slice r; running sums in rank order
+    const int lane = tid;
+    const double sr =
+        lane < CL ? cluster.map_shared_rank(&ds, lane)->slice[par] : 0.0;
+    double run = 0.0, pre = 0.0, before = 0.0;
+    for (int r = 0; r < CL; ++r) {
+      const double c = __shfl_sync(0xffffffffu, sr, r);
+      if (r == lane) before = run;
+      run += c;
+      if (r == lane) pre = run;
+    }
+    const double tot = run;
+    const double tau = (double)u * tot;
+    unsigned hit = __ballot_sync(0xffffffffu, lane < CL && pre > tau);
+    if (!hit && tot > 0.0)  // rounding: last slice with mass
+      hit = 1u << (31 - __clz(__ballot_sync(0xffffffffu, lane < CL && sr > 0.0)));
+    const int own = hit ? __ffs(hit) - 1 : -1;
+    const double bef = __shfl_sync(0xffffffffu, before, own < 0 ? 0 : own);
+    if (lane == 0) {
+      ds.N = tot;
+      ds.owner = tot > 0.0 ? own : -1;
+      ds.tau = tau - bef;
+    }
+  }
+  __syncthreads();
+  par ^= 1;
+  return ds.N;
+}
+
 // Draw one token from the weights W over the row(s) by inverse CDF with
 // uniform u: the smallest j with C_j > u * N.  Every thread of every CTA of
 // the cluster must call it (it holds one cluster barrier); `par` is the
@@ -540,45 +589,7 @@ __device__ DrawOut cluster_draw(cg::cluster_group &cluster, DrawSmem &ds,
                                 float u, int &par) {
   const int tid = threadIdx.x;
   const int rank = (int)cluster.block_rank();
-  const int CL = (int)cluster.num_blocks();
-  mass_pass<DT, VW>(ra, rb, has_q, W, sl, segmass);
-  __syncthreads();
-  slice_prefix(segmass, sl.nseg, ds.chunk_pre);
-  __syncthreads();
-  if (tid == 0) ds.slice[par] = sl.nseg ? ds.chunk_pre[31] : 0.0;
-  cluster.sync();
-  if (tid == 0) {
-    double tot = 0.0;
-    for (int r = 0; r < CL; ++r)
-      tot += cluster.map_shared_rank(&ds, r)->slice[par];
-    const double tau = (double)u * tot;
-    double run = 0.0, bef = 0.0;
-    int own = -1;
-    for (int r = 0; r < CL && own < 0; ++r) {
-      const double sr = cluster.map_shared_rank(&ds, r)->slice[par];
-      if (run + sr > tau) {
-        own = r;
-        bef = run;
-      }
-      run += sr;
-    }
-    if (own < 0 && tot > 0.0) {  // rounding: last slice with mass
-      run = 0.0;
-      for (int r = 0; r < CL; ++r) {
-        const double sr = cluster.map_shared_rank(&ds, r)->slice[par];
-        if (sr > 0.0) {
-          own = r;
-          bef = run;
-        }
-        run += sr;
-      }
-    }
-    ds.N = tot;
-    ds.owner = tot > 0.0 ? own : -1;
-    ds.tau = tau - bef;
-  }
-  __syncthreads();
-  par ^= 1;
+  cluster_mass<DT, VW>(cluster, ds, segmass, ra, rb, has_q, W, sl, u, par);
   DrawOut out;
   out.N = ds.N;
   out.owner = ds.owner;

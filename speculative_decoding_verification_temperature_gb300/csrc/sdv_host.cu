@@ -86,9 +86,22 @@ sd_status max_active_clusters(const void *kernel, int cl, size_t smem,
   if (cl > 8)
     SDV_CUDA(cudaFuncSetAttribute(
         kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1));
-  if (smem > 48 * 1024)
+  {
+    // allow every dynamic size the device can give next to the kernel's
+    // static shared memory (the launch's own size sets the occupancy)
+    cudaFuncAttributes fa;
+    SDV_CUDA(cudaFuncGetAttributes(&fa, kernel));
+    int optin = 0;
+    SDV_CUDA(cudaDeviceGetAttribute(&optin,
+                                    cudaDevAttrMaxSharedMemoryPerBlockOptin,
+                                    dev));
+    const int room = optin - (int)fa.sharedSizeBytes;
+    if ((long long)smem > room)
+      return fail(SD_ERR_UNSUPPORTED, "%zu B of shared memory do not fit",
+                  smem);
     SDV_CUDA(cudaFuncSetAttribute(
-        kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+        kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, room));
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(cl, 1, 1);
   cfg.blockDim = dim3(256, 1, 1);

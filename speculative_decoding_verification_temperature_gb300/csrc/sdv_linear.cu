@@ -50,6 +50,8 @@ struct LinearParams {
   int nclusters;
   int seg_bytes;   // bytes of the segment-mass array (multiple of 128)
   int slice_vecs;  // capacity of each slice buffer in 16-byte vectors (TMA)
+  int prefetch;    // L2 prefetch: bit 0 next sequence's first rows,
+                   // bit 1 the next position's rows (speculative)
 };
 
 struct Decision {
@@ -133,6 +135,13 @@ __global__ void __launch_bounds__(kThreads, TMA ? 3 : 2)
         if (slice_bytes) {
           bulk_g2s(tbuf, trow + (size_t)sl.vbeg * 16, slice_bytes, &bar);
           if (has_d) bulk_g2s(dbuf, drow + (size_t)sl.vbeg * 16, slice_bytes, &bar);
+          // speculative: the next position's slices, read only if this
+          // position accepts
+          if ((p.prefetch & 2) && i < gamma) {
+            prefetch_l2(trow + rowb + (size_t)sl.vbeg * 16, slice_bytes);
+            if (!GREEDY && i + 1 < gamma)
+              prefetch_l2(drow + rowb + (size_t)sl.vbeg * 16, slice_bytes);
+          }
         }
       }
       if (tid == 0) {  // gathers for the accept test (used after the merge)
@@ -229,6 +238,17 @@ __global__ void __launch_bounds__(kThreads, TMA ? 3 : 2)
         break;
       }
       ++n;
+    }
+    if (TMA && (p.prefetch & 1) && tid == 0 && slice_bytes) {
+      // the next sequence's first rows, into L2 while this one draws
+      const int nxt = cluster.map_shared_rank(&sh, 0)->next_seq[seqpar];
+      if (nxt < p.B) {
+        prefetch_l2(tbase + (size_t)nxt * (gamma + 1) * rowb +
+                        (size_t)sl.vbeg * 16, slice_bytes);
+        if (!GREEDY && gamma > 0)
+          prefetch_l2(dbase + (size_t)nxt * p.d_seq_rows * rowb +
+                          (size_t)sl.vbeg * 16, slice_bytes);
+      }
     }
 
     if (kind == 3) {  // unusable row: outputs -1
@@ -400,6 +420,7 @@ sd_status linear_launch(const void *target, const void *draft, sd_dtype dt,
   prm.nclusters = nclusters;
   prm.seg_bytes = (int)seg_bytes;
   prm.slice_vecs = (int)per_cta;
+  prm.prefetch = env_int("SDV_PREFETCH", 3);
   if (B > nclusters) {
     if (!ws || ws_bytes < 256)
       return fail(SD_ERR_INVALID_ARG, "workspace of >= 256 bytes required");

@@ -1,0 +1,75 @@
+"""Parity of sd_verify_kcand (CUDA, through the C ABI) with the oracle:
+K candidates verified against shared draft marginals, the longest accepted
+streak kept (lowest k on ties), then its correction or bonus token."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from speculative_decoding_verification_temperature_gb300 import api, synth
+from tests.parity import compare, host, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+def kc_oracle(c):
+    return oracle.verify_kcand(synth.host_logits(c.target),
+                               synth.host_logits(c.draft), host(c.tokens),
+                               host(c.uniforms), c.T)
+
+
+def run(c, **kw):
+    return api.verify_kcand(c.target, c.draft, c.tokens, c.uniforms, c.T, **kw)
+
+
+@pytest.mark.parametrize("T", [0.0, 0.6, 1.0])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("K,gamma,V", [(1, 5, 300), (3, 4, 1001), (8, 6, 5000),
+                                       (8, 0, 700), (5, 1, 64)])
+def test_small_cases(T, dtype, K, gamma, V):
+    c = to_device(synth.kcand_case(40, K, gamma, V, dtype, T, seed=K * 100 + V,
+                                   sigma_t=2.0, sigma_d=1.0, sigma_k=0.7))
+    compare(run(c), kc_oracle(c), extra_equal=("k", "n_per_cand"))
+
+
+def test_one_candidate_equals_linear():
+    c = to_device(synth.kcand_case(64, 1, 6, 2000, torch.bfloat16, 1.0,
+                                   seed=3))
+    gk = run(c)
+    gl = api.verify_linear(c.target[:, 0].contiguous(), c.draft,
+                           c.tokens[:, 0].contiguous(),
+                           c.uniforms[:, 0].contiguous(), 1.0)
+    assert torch.equal(gk["n"], gl["n"]) and torch.equal(gk["tokens"],
+                                                         gl["tokens"])
+    assert torch.all(gk["k"] == 0)
+
+
+def test_kcand_workload_sampled():
+    """B=64, K=8, gamma=16, V=152064 bf16, T=1 (the diffusion self-selection
+    workload, full size on the device); 10 sequences checked one by one."""
+    c = synth.kcand(0, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    g = run(c, status=st)
+    assert int(st.item()) == 0
+    npc = host(g["n_per_cand"])
+    assert np.array_equal(host(g["n"]), npc.max(1))
+    idx = [0, 1, 7, 20, 33, 47, 60, 63] + [int(np.argmax(host(g["n"])))]
+    sub = synth.KcandCase(c.target[idx], c.draft[idx], c.tokens[idx],
+                          c.uniforms[idx], 1.0)
+    compare({k: v[idx] for k, v in g.items()}, kc_oracle(sub),
+            extra_equal=("k", "n_per_cand"))
+
+
+def test_invalid_rows_and_bad_tokens():
+    c = synth.kcand_case(6, 3, 4, 500, torch.float32, 1.0, seed=8)
+    c.target[1, 2, 0, 7] = float("nan")        # candidate 2's first row
+    c.draft[2, 1, 3] = float("inf")             # shared draft row 1
+    c.tokens[3, 0, 0] = 500                     # bad token
+    c.target[4, 0, 0, :] = -float("inf")
+    to_device(c)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    g = run(c, status=st)
+    o = kc_oracle(c)
+    compare(g, o, extra_equal=("k", "n_per_cand"))
+    assert int(st.item()) & api.DEV_NONFINITE
+    assert int(st.item()) & api.DEV_BAD_TOKEN
