@@ -203,6 +203,8 @@ def gpu_arm(args, rank, world):
     }
     if args.e2e_steps > 0:
         res["e2e"] = e2e_arm(args, sets, dev, ws, world)
+    if args.aux_steps > 0:
+        res["other_workloads"] = other_workloads(args, dev, peak)
     if rank == 0 and args.oracle_seqs > 0:
         res["cpu_baseline"] = cpu_baseline(sets, args.oracle_seqs)
     return res
@@ -248,6 +250,114 @@ def e2e_arm(args, sets, dev, ws, world):
     return {"value": world * steps / (ms / 1e3), "unit": "rounds/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": steps}
+
+
+# ------------------------------------------------- the other workloads
+def _rows_linear(n, gamma, greedy):
+    n = np.asarray(n, np.int64)
+    return int(((n + 1) + (0 if greedy else np.minimum(n + 1, gamma))).sum())
+
+
+def _rows_kcand(npc, n, gamma):
+    npc = np.asarray(npc, np.int64)
+    n = np.asarray(n, np.int64)
+    tgt = np.minimum(npc + 1, gamma).sum(1) + (n == gamma)
+    drf = np.minimum(n + 1, gamma)
+    return int((tgt + drf).sum())
+
+
+def _rows_tree(parent, nodes, n, greedy):
+    parent = np.asarray(parent)
+    rows = 0
+    for b in range(parent.shape[0]):
+        visited = [0] + [int(v) for v in nodes[b, :n[b]]]
+        for u in visited:
+            rows += 1
+            if not greedy and np.any(parent[b] == u):
+                rows += 1
+    return rows
+
+
+def _time(fn, sets, steps, warmup, dev):
+    stream = torch.cuda.current_stream(dev)
+    for i in range(warmup):
+        fn(sets[i % len(sets)])
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for i in range(steps):
+        fn(sets[i % len(sets)])
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps  # ms per round
+
+
+def other_workloads(args, dev, peak):
+    """rounds/s, logit bytes the method read (counted from the outputs) and
+    the HBM fraction for the other four workloads, measured in this run."""
+    from speculative_decoding_verification_temperature_gb300 import api
+    out = {}
+    steps = args.aux_steps
+
+    def entry(name, ms, rows, V, elt, full_rows, extra=None):
+        gbs = rows * V * elt / (ms / 1e3) / 1e9
+        e = {"rounds_s": 1e3 / ms, "ms_per_round": ms,
+             "bytes_read": rows * V * elt,
+             "full_tensor_bytes": full_rows * V * elt,
+             "achieved_gbs": gbs, "frac_of_measured_hbm": gbs / peak}
+        if extra:
+            e.update(extra)
+        out[name] = e
+
+    # tiny: B=1, gamma=4, V=1000 fp32 (launch-latency bound)
+    sets = [synth.tiny(r, device=dev) for r in range(64)]
+    fn = lambda c: api.verify_linear(c.target, c.draft, c.tokens,
+                                     c.uniforms, 1.0)
+    ms = _time(fn, sets, max(steps, 200), 10, dev)
+    rows = np.mean([_rows_linear(fn(c)["n"].cpu().numpy(), 4, False)
+                    for c in sets[:16]])
+    entry("tiny", ms, rows, 1000, 4, 9, {"note": "launch-latency bound"})
+    # linear: B=32, gamma=8, V=32000 bf16 at T in {0, 0.7, 1.0}; 16 sets
+    # rotated (16 x 34.8 MB > 4 x L2)
+    for T in (0.0, 0.7, 1.0):
+        sets = [synth.linear(T, r, device=dev) for r in range(16)]
+        for c in sets:
+            c.draft = c.draft.contiguous()
+        fn = (lambda c, T=T: api.verify_linear(
+            c.target, None if T == 0 else c.draft, c.tokens, c.uniforms, T))
+        ms = _time(fn, sets, max(steps, 100), 10, dev)
+        rows = np.mean([_rows_linear(fn(c)["n"].cpu().numpy(), 8, T == 0)
+                        for c in sets])
+        full = 32 * (9 if T == 0 else 17)
+        entry("linear_T%g" % T, ms, rows, 32000, 2, full)
+        del sets
+    # kcand: B=64, K=8, gamma=16, V=152064 bf16, T=1; 2 sets (2.9 GB each)
+    sets = [synth.kcand(r, device=dev) for r in range(2)]
+    fn = lambda c: api.verify_kcand(c.target, c.draft, c.tokens, c.uniforms,
+                                    1.0)
+    ms = _time(fn, sets, steps, 3, dev)
+    rows = []
+    for c in sets:
+        o = fn(c)
+        rows.append(_rows_kcand(o["n_per_cand"].cpu().numpy(),
+                                o["n"].cpu().numpy(), 16))
+    entry("kcand", ms, np.mean(rows), 152064, 2, 64 * (8 * 17 + 16))
+    del sets
+    # tree: B=16, N=64, V=151936 bf16, T=0.8; 4 sets (622 MB each)
+    sets = [synth.tree(r, device=dev) for r in range(4)]
+    fn = lambda c: api.verify_tree(c.target, c.draft, c.parent,
+                                   c.node_tokens, c.uniforms, 0.8)
+    ms = _time(fn, sets, steps, 3, dev)
+    rows = []
+    for c in sets:
+        o = fn(c)
+        rows.append(_rows_tree(c.parent.cpu().numpy(),
+                               o["nodes"].cpu().numpy(),
+                               o["n"].cpu().numpy(), False))
+    entry("tree", ms, np.mean(rows), 151936, 2, 16 * 128)
+    del sets
+    return out
 
 
 # --------------------------------------------------------- CPU oracle
@@ -328,6 +438,9 @@ def main():
                     help="input sets rotated between steps")
     ap.add_argument("--e2e-steps", type=int, default=20,
                     help="steps of the host-buffer leg (0: skip it)")
+    ap.add_argument("--aux-steps", type=int, default=30,
+                    help="timed rounds of each of the other workloads "
+                         "(0: skip them)")
     ap.add_argument("--oracle-seqs", type=int, default=256,
                     help="sequences of one round the CPU oracle times "
                          "(0: skip the CPU baseline)")
