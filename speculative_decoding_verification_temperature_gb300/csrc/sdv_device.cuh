@@ -529,20 +529,19 @@ struct DrawOut {
   float wt;  // its weight (probability wt / N)
 };
 
-// Cluster-wide total of the weights W over the row(s): every CTA writes its
-// per-segment masses and slice total, one cluster barrier, then warp 0 of
-// every CTA forms the running sums of the slice totals in rank order (all
-// CTAs do the same arithmetic, so all agree).  With `u` >= 0 it also finds
-// the CTA whose slice holds the crossing C > u N and the target left in it.
-// Every thread of every CTA of the cluster must call it.
-template <int DT, int VW, class Row>
-__device__ double cluster_mass(cg::cluster_group &cluster, DrawSmem &ds,
-                               float *segmass, const Row &ra, const Row &rb,
-                               bool has_q, const Weight &W, const Slice &sl,
-                               float u, int &par) {
+// Cluster-wide total of the weights over the row(s): `fill()` makes every
+// CTA write its per-segment masses, then the slice totals are exchanged
+// (one cluster barrier) and warp 0 of every CTA forms their running sums in
+// rank order (all CTAs do the same arithmetic, so all agree).  With u in
+// (0, 1) it also finds the CTA whose slice holds the crossing C > u N and
+// the target left in it.  Every thread of every CTA must call it.
+template <class Fill>
+__device__ double cluster_total(cg::cluster_group &cluster, DrawSmem &ds,
+                                float *segmass, const Slice &sl, float u,
+                                int &par, Fill &&fill) {
   const int tid = threadIdx.x;
   const int CL = (int)cluster.num_blocks();
-  mass_pass<DT, VW>(ra, rb, has_q, W, sl, segmass);
+  fill();
   __syncthreads();
   slice_prefix(segmass, sl.nseg, ds.chunk_pre);
   __syncthreads();
@@ -578,18 +577,25 @@ __device__ double cluster_mass(cg::cluster_group &cluster, DrawSmem &ds,
   return ds.N;
 }
 
-// Draw one token from the weights W over the row(s) by inverse CDF with
-// uniform u: the smallest j with C_j > u * N.  Every thread of every CTA of
-// the cluster must call it (it holds one cluster barrier); `par` is the
-// caller's parity of the double-buffered slot.
 template <int DT, int VW, class Row>
-__device__ DrawOut cluster_draw(cg::cluster_group &cluster, DrawSmem &ds,
-                                float *segmass, const Row &ra, const Row &rb,
-                                bool has_q, const Weight &W, const Slice &sl,
-                                float u, int &par) {
+__device__ double cluster_mass(cg::cluster_group &cluster, DrawSmem &ds,
+                               float *segmass, const Row &ra, const Row &rb,
+                               bool has_q, const Weight &W, const Slice &sl,
+                               float u, int &par) {
+  return cluster_total(cluster, ds, segmass, sl, u, par, [&] {
+    mass_pass<DT, VW>(ra, rb, has_q, W, sl, segmass);
+  });
+}
+
+// After cluster_total: the owner CTA finds the segment of the crossing and
+// one warp scans it (reading the vectors through `ra` / `rb`).
+template <int DT, int VW, class Row>
+__device__ DrawOut draw_pick(cg::cluster_group &cluster, DrawSmem &ds,
+                             const float *segmass, const Row &ra,
+                             const Row &rb, bool has_q, const Weight &W,
+                             const Slice &sl) {
   const int tid = threadIdx.x;
   const int rank = (int)cluster.block_rank();
-  cluster_mass<DT, VW>(cluster, ds, segmass, ra, rb, has_q, W, sl, u, par);
   DrawOut out;
   out.N = ds.N;
   out.owner = ds.owner;
@@ -618,6 +624,19 @@ __device__ DrawOut cluster_draw(cg::cluster_group &cluster, DrawSmem &ds,
     }
   }
   return out;
+}
+
+// Draw one token from the weights W over the row(s) by inverse CDF with
+// uniform u: the smallest j with C_j > u * N.  Every thread of every CTA of
+// the cluster must call it (it holds one cluster barrier); `par` is the
+// caller's parity of the double-buffered slot.
+template <int DT, int VW, class Row>
+__device__ DrawOut cluster_draw(cg::cluster_group &cluster, DrawSmem &ds,
+                                float *segmass, const Row &ra, const Row &rb,
+                                bool has_q, const Weight &W, const Slice &sl,
+                                float u, int &par) {
+  cluster_mass<DT, VW>(cluster, ds, segmass, ra, rb, has_q, W, sl, u, par);
+  return draw_pick<DT, VW>(cluster, ds, segmass, ra, rb, has_q, W, sl);
 }
 
 // Debug output: the normalised weights w_j / N over this CTA's slice.

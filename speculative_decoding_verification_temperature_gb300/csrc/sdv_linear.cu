@@ -19,16 +19,21 @@
 // balance across the GPU.  Greedy (T == 0) compares draft ids with the
 // row argmax (section 2.2) and reads no draft logits.
 //
-// Two ways to read a step's slices: TMA bulk copies (cp.async.bulk with an
-// mbarrier) into shared memory, where the slice then stays for the draw
-// (no second read at all), used when rows are 16-byte aligned and the
-// slices fit; or 16-byte loads from global memory with several in flight
-// per thread (the draw then re-reads the slice, from L2).
+// Two ways to read a step's slices: through a ring of shared-memory stages
+// filled by TMA bulk copies (cp.async.bulk, one mbarrier per stage), used
+// when rows are 16-byte aligned; or 16-byte loads from global memory with
+// several in flight per thread.  The draw streams the last step's slices
+// again (they were just read: from L2).
 #include <type_traits>
 
 #include "sdv_device.cuh"
 #include "sdv_host.cuh"
+#include "sdv_ring.cuh"
 #include "sdv_tma.cuh"
+
+#ifndef SDV_LDG_MINB
+#define SDV_LDG_MINB 2
+#endif
 
 namespace sdv {
 
@@ -75,13 +80,13 @@ struct LinearSmem {
   DrawSmem draw;
 };
 
-template <int DT, int VW, bool GREEDY, bool TMA>
-__global__ void __launch_bounds__(kThreads, TMA ? 3 : 2)
+template <int DT, int VW, bool GREEDY, bool RING>
+__global__ void __launch_bounds__(kThreads, RING ? 4 : 2)
     linear_verify_kernel(const LinearParams p) {
   extern __shared__ __align__(128) unsigned char dsm[];
   __shared__ LinearSmem sh;
-  __shared__ uint64_t bar;  // TMA completion barrier
-  using Row = std::conditional_t<TMA, SRow<DT, VW>, GRow<DT, VW>>;
+  __shared__ uint64_t bars[kStages];
+  using GR = GRow<DT, VW>;
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
   const int CL = (int)cluster.num_blocks();
@@ -92,28 +97,14 @@ __global__ void __launch_bounds__(kThreads, TMA ? 3 : 2)
   const char *tbase = static_cast<const char *>(p.target);
   const char *dbase = static_cast<const char *>(p.draft);
   const float k2 = p.k2;
-  // dynamic shared memory: segment masses, then the two slice buffers
+  // dynamic shared memory: segment masses, then the ring stages
   float *segmass = reinterpret_cast<float *>(dsm);
-  uint4 *tbuf = reinterpret_cast<uint4 *>(dsm + p.seg_bytes);
-  uint4 *dbuf = tbuf + p.slice_vecs;
+  Ring rg;
+  rg.buf = reinterpret_cast<uint4 *>(dsm + p.seg_bytes);
+  rg.full = bars;
+  rg.dev_status = p.dev_status;
+  if (RING) ring_init(rg);
   const uint32_t slice_bytes = (uint32_t)(sl.vend - sl.vbeg) * 16u;
-  uint32_t phase = 0;
-  if (TMA) {
-    if (tid == 0) {
-      mbar_init(&bar, 1);
-      fence_mbar_init();
-    }
-    __syncthreads();
-  }
-  auto row_of = [&](const char *g, uint4 *buf) {
-    if constexpr (TMA) {
-      (void)g;
-      return Row{buf, sl.vbeg};
-    } else {
-      (void)buf;
-      return Row{g};
-    }
-  };
 
   int par = 0, seqpar = 0;
   int seq = (int)(blockIdx.x / CL);
@@ -129,22 +120,14 @@ __global__ void __launch_bounds__(kThreads, TMA ? 3 : 2)
       const char *trow = tbase + ((size_t)seq * (gamma + 1) + i) * rowb;
       const char *drow =
           has_d ? dbase + ((size_t)seq * p.d_seq_rows + i) * rowb : nullptr;
-      if (TMA && tid == 0) {  // this step's slices -> shared memory
-        fence_proxy_async();
-        mbar_expect_tx(&bar, slice_bytes * (has_d ? 2u : 1u));
-        if (slice_bytes) {
-          bulk_g2s(tbuf, trow + (size_t)sl.vbeg * 16, slice_bytes, &bar);
-          if (has_d) bulk_g2s(dbuf, drow + (size_t)sl.vbeg * 16, slice_bytes, &bar);
-          // speculative: the next position's slices, read only if this
-          // position accepts
-          if ((p.prefetch & 2) && i < gamma) {
-            prefetch_l2(trow + rowb + (size_t)sl.vbeg * 16, slice_bytes);
-            if (!GREEDY && i + 1 < gamma)
-              prefetch_l2(drow + rowb + (size_t)sl.vbeg * 16, slice_bytes);
-          }
-        }
-      }
       if (tid == 0) {  // gathers for the accept test (used after the merge)
+        if (RING && (p.prefetch & 2) && i < gamma && slice_bytes) {
+          // speculative: the next position's slices, used only if this
+          // position accepts
+          prefetch_l2(trow + rowb + (size_t)sl.vbeg * 16, slice_bytes);
+          if (!GREEDY && i + 1 < gamma)
+            prefetch_l2(drow + rowb + (size_t)sl.vbeg * 16, slice_bytes);
+        }
         int x = -1;
         float zt = 0.f, zd = 0.f;
         if (i < gamma) {
@@ -160,19 +143,16 @@ __global__ void __launch_bounds__(kThreads, TMA ? 3 : 2)
         sh.gr[par] =
             GREEDY ? 0.f : p.uniforms[(size_t)seq * (gamma + 1) + i];
       }
-      if (TMA) {
-        mbar_wait(&bar, phase, p.dev_status);
-        phase ^= 1;
-      }
-      const Row ra = row_of(trow, tbuf), rb = row_of(drow, dbuf);
       if constexpr (GREEDY) {
         AM a = am_empty();
-        argmax_pass<DT, VW>(ra, sl, a);
+        if constexpr (RING) ring_argmax<DT, VW>(rg, trow, sl, a);
+        else argmax_pass<DT, VW>(GR{trow}, sl, a);
         a = block_reduce_am(a, sh.ared);
         if (tid == 0) sh.apart[par] = a;
       } else {
         MS st[2] = {ms_empty(), ms_empty()};
-        stats_pass<DT, VW>(ra, rb, has_d, sl, k2, st[0], st[1]);
+        if constexpr (RING) ring_stats<DT, VW>(rg, trow, drow, sl, k2, st[0], st[1]);
+        else stats_pass<DT, VW>(GR{trow}, GR{drow}, has_d, sl, k2, st[0], st[1]);
         block_reduce_ms<2>(st, k2, sh.red);
         if (tid == 0) {
           sh.part[par][0] = st[0];
@@ -239,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, TMA ? 3 : 2)
       }
       ++n;
     }
-    if (TMA && (p.prefetch & 1) && tid == 0 && slice_bytes) {
+    if (RING && (p.prefetch & 1) && tid == 0 && slice_bytes) {
       // the next sequence's first rows, into L2 while this one draws
       const int nxt = cluster.map_shared_rank(&sh, 0)->next_seq[seqpar];
       if (nxt < p.B) {
@@ -288,14 +268,13 @@ __global__ void __launch_bounds__(kThreads, TMA ? 3 : 2)
           res[j] = (j == greedy_tok) ? 1.f : 0.f;
       }
     } else {
-      // correction (kind 1) or bonus (kind 2) by inverse CDF
-      // the rows of the draw are the last step's (already in shared memory
-      // on the TMA path)
+      // correction (kind 1) or bonus (kind 2) by inverse CDF over the rows
+      // of the last step (streamed again: they were just read, so from L2)
       const char *trow = tbase + ((size_t)seq * (gamma + 1) + n) * rowb;
       const char *drow =
           kind == 1 ? dbase + ((size_t)seq * p.d_seq_rows + n) * rowb
                     : nullptr;
-      const Row ra = row_of(trow, tbuf), rb = row_of(drow, dbuf);
+      const GR ra{trow}, rb{drow ? drow : trow};
       bool has_q = kind == 1;
       Weight W;
       W.k2 = k2;
@@ -304,15 +283,18 @@ __global__ void __launch_bounds__(kThreads, TMA ? 3 : 2)
       W.mdk = fmd.m * k2;
       W.cq = 1.f / fmd.s;
       const float u = p.uniforms[(size_t)seq * (gamma + 1) + gamma];
-      DrawOut o = cluster_draw<DT, VW>(cluster, sh.draw, segmass, ra, rb,
-                                       has_q, W, sl, u, par);
       int zero_mass = 0;
-      if (o.owner < 0) {  // residual of zero mass: draw from p_n instead
-        zero_mass = 1;
+      DrawOut o;
+      for (int attempt = 0; attempt < 2; ++attempt) {
+        cluster_total(cluster, sh.draw, segmass, sl, u, par, [&] {
+          if constexpr (RING) ring_mass<DT, VW>(rg, trow, drow, has_q, W, sl, segmass);
+          else mass_pass<DT, VW>(ra, rb, has_q, W, sl, segmass);
+        });
+        o = draw_pick<DT, VW>(cluster, sh.draw, segmass, ra, rb, has_q, W, sl);
+        if (o.owner >= 0) break;
+        zero_mass = 1;  // residual of zero mass: draw from p_n instead
         has_q = false;
         __syncthreads();
-        o = cluster_draw<DT, VW>(cluster, sh.draw, segmass, ra, rb, false, W,
-                                 sl, u, par);
       }
       if (o.owner == rank && warp == 0) {
         for (int i = lane; i <= gamma; i += 32) {
@@ -347,26 +329,22 @@ __global__ void __launch_bounds__(kThreads, TMA ? 3 : 2)
 
 using LinearKernel = void (*)(const LinearParams);
 
-template <int DT, int VW, bool TMA>
+template <int DT, int VW, bool RING>
 static LinearKernel pick_linear_t(bool greedy) {
-  return greedy ? linear_verify_kernel<DT, VW, true, TMA>
-                : linear_verify_kernel<DT, VW, false, TMA>;
+  return greedy ? linear_verify_kernel<DT, VW, true, RING>
+                : linear_verify_kernel<DT, VW, false, RING>;
 }
 
-static LinearKernel pick_linear(int dt, bool vec, bool tma, bool greedy) {
+static LinearKernel pick_linear(int dt, bool vec, bool ring, bool greedy) {
   if (dt == SD_F32) {
     if (!vec) return pick_linear_t<0, 1, false>(greedy);
-    return tma ? pick_linear_t<0, 4, true>(greedy)
-               : pick_linear_t<0, 4, false>(greedy);
+    return ring ? pick_linear_t<0, 4, true>(greedy)
+                : pick_linear_t<0, 4, false>(greedy);
   }
   if (!vec) return pick_linear_t<1, 1, false>(greedy);
-  return tma ? pick_linear_t<1, 8, true>(greedy)
-             : pick_linear_t<1, 8, false>(greedy);
+  return ring ? pick_linear_t<1, 8, true>(greedy)
+              : pick_linear_t<1, 8, false>(greedy);
 }
-
-// Largest dynamic shared memory per CTA for the TMA path (two slice
-// buffers + segment masses), chosen so that three CTAs share an SM.
-constexpr size_t kTmaSmemMax = 72 * 1024;
 
 sd_status linear_launch(const void *target, const void *draft, sd_dtype dt,
                         long long d_seq_rows, const int32_t *tokens,
@@ -385,17 +363,18 @@ sd_status linear_launch(const void *target, const void *draft, sd_dtype dt,
                    ((size_t)V * eb) % 16 == 0;
   const int VW = vec ? vw : 1;
   const long long nvec = V / VW;
-  const int CL = choose_cluster(nvec);
+  // many sequences: smaller clusters keep more of them in flight (measured
+  // on the 256 x 128256 fp32 workload: 8 beats 16)
+  int CL = choose_cluster(nvec);
+  if (B >= 128 && CL > 8 && env_int("SDV_CLUSTER", 0) == 0) CL = 8;
   const long long per_cta = (nvec + CL - 1) / CL;
   const size_t seg_bytes = ((size_t)((per_cta + 31) / 32) * 4 + 127) / 128 * 128;
-  const size_t tma_smem = seg_bytes + 2 * (size_t)per_cta * 16;
-  const bool tma = vec && tma_smem <= kTmaSmemMax &&
-                   env_int("SDV_NO_TMA", 0) == 0;
-  const size_t smem = tma ? tma_smem : seg_bytes;
+  const bool ring = vec && env_int("SDV_NO_TMA", 0) == 0;
+  const size_t smem = seg_bytes + (ring ? kRingBytes : 0);
   if (smem > 96 * 1024)
     return fail(SD_ERR_UNSUPPORTED, "V=%d needs %zu B of shared memory", V,
                 smem);
-  LinearKernel kern = pick_linear(dt, vec, tma, greedy);
+  LinearKernel kern = pick_linear(dt, vec, ring, greedy);
   int maxc = 0;
   st = max_active_clusters((const void *)kern, CL, smem, &maxc);
   if (st != SD_OK) return st;
@@ -420,7 +399,7 @@ sd_status linear_launch(const void *target, const void *draft, sd_dtype dt,
   prm.nclusters = nclusters;
   prm.seg_bytes = (int)seg_bytes;
   prm.slice_vecs = (int)per_cta;
-  prm.prefetch = env_int("SDV_PREFETCH", 3);
+  prm.prefetch = env_int("SDV_PREFETCH", 0);
   if (B > nclusters) {
     if (!ws || ws_bytes < 256)
       return fail(SD_ERR_INVALID_ARG, "workspace of >= 256 bytes required");

@@ -1,0 +1,135 @@
+// sdv_ring.cuh -- streaming a CTA's slice of one or two rows through a ring
+// of shared-memory stages filled by TMA bulk copies (cp.async.bulk with one
+// mbarrier per stage).
+//
+// Thread 0 keeps kStages chunks in flight; every thread consumes chunk c
+// as soon as its stage's barrier completes, and after a block barrier the
+// stage is refilled with chunk c + kStages.  The bytes in flight per CTA
+// are the whole ring, independent of registers, so several CTAs per SM
+// keep HBM busy while each one also spends time in cluster barriers.
+#pragma once
+
+#include "sdv_device.cuh"
+#include "sdv_tma.cuh"
+
+namespace sdv {
+
+constexpr int kStg = 256;    // 16-byte vectors per row per stage
+constexpr int kStages = 4;   // stages in flight
+constexpr int kRingBytes = kStages * 2 * kStg * 16;  // 32 KB
+
+struct Ring {
+  uint4 *buf;          // [kStages][2][kStg]
+  uint64_t *full;      // [kStages] mbarriers
+  uint32_t phase;      // bit s: parity of the next completion of stage s
+  int32_t *dev_status;
+};
+
+__device__ __forceinline__ void ring_init(Ring &rg) {
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) mbar_init(&rg.full[s], 1);
+    fence_mbar_init();
+  }
+  rg.phase = 0;
+  __syncthreads();
+}
+
+// One pass over this CTA's slice of row A (and row B when non-null).
+// f(a, b, v0, n) is called by every thread for each chunk: a / b point at
+// the chunk's n vectors in shared memory, v0 is the absolute index of the
+// chunk's first vector.  Block-uniform control flow is required.
+template <class F>
+__device__ __forceinline__ void ring_pass(Ring &rg, const char *rowA,
+                                          const char *rowB, const Slice &sl,
+                                          F &&f) {
+  const int nv = sl.vend - sl.vbeg;
+  const int nch = (nv + kStg - 1) / kStg;
+  auto issue = [&](int c) {
+    const int s = c % kStages;
+    const int v0 = c * kStg;
+    const int cnt = min(kStg, nv - v0);
+    const uint32_t bytes = (uint32_t)cnt * 16u;
+    fence_proxy_async();
+    mbar_expect_tx(&rg.full[s], bytes * (rowB ? 2u : 1u));
+    bulk_g2s(rg.buf + (size_t)(2 * s) * kStg,
+             rowA + (size_t)(sl.vbeg + v0) * 16, bytes, &rg.full[s]);
+    if (rowB)
+      bulk_g2s(rg.buf + (size_t)(2 * s + 1) * kStg,
+               rowB + (size_t)(sl.vbeg + v0) * 16, bytes, &rg.full[s]);
+  };
+  if (threadIdx.x == 0)
+    for (int c = 0; c < nch && c < kStages; ++c) issue(c);
+  for (int c = 0; c < nch; ++c) {
+    const int s = c % kStages;
+    mbar_wait(&rg.full[s], (rg.phase >> s) & 1u, rg.dev_status);
+    rg.phase ^= 1u << s;
+    f(rg.buf + (size_t)(2 * s) * kStg, rg.buf + (size_t)(2 * s + 1) * kStg,
+      sl.vbeg + c * kStg, min(kStg, nv - c * kStg));
+    __syncthreads();
+    if (threadIdx.x == 0 && c + kStages < nch) issue(c + kStages);
+  }
+}
+
+template <int DT, int VW>
+__device__ __forceinline__ Raw<DT, VW> sget(const uint4 *p, int i) {
+  Raw<DT, VW> r;
+  r.w = p[i];
+  return r;
+}
+
+// Online softmax states of row A (and B) over the slice.
+template <int DT, int VW>
+__device__ __forceinline__ void ring_stats(Ring &rg, const char *rowA,
+                                           const char *rowB, const Slice &sl,
+                                           float k2, MS &a, MS &b) {
+  const bool hb = rowB != nullptr;
+  ring_pass(rg, rowA, rowB, sl, [&](const uint4 *A, const uint4 *Bp, int,
+                                    int n) {
+    for (int i = threadIdx.x; i < n; i += kThreads) {
+      ms_add<DT, VW>(a, sget<DT, VW>(A, i), k2);
+      if (hb) ms_add<DT, VW>(b, sget<DT, VW>(Bp, i), k2);
+    }
+  });
+}
+
+// Greedy argmax state of row A over the slice.
+template <int DT, int VW>
+__device__ __forceinline__ void ring_argmax(Ring &rg, const char *rowA,
+                                            const Slice &sl, AM &a) {
+  ring_pass(rg, rowA, nullptr, sl, [&](const uint4 *A, const uint4 *, int v0,
+                                       int n) {
+    for (int i = threadIdx.x; i < n; i += kThreads)
+      am_add<DT, VW>(a, sget<DT, VW>(A, i), (v0 + i) * VW);
+  });
+}
+
+// Per-segment masses (segment s = vectors vbeg + 32 s ..) of the weights
+// W over the slice; a chunk holds kStg / 32 segments, one per warp.
+template <int DT, int VW>
+__device__ __forceinline__ void ring_mass(Ring &rg, const char *rowA,
+                                          const char *rowB, bool has_q,
+                                          const Weight &W, const Slice &sl,
+                                          float *segmass) {
+  static_assert(kStg == 32 * kWarps, "one segment per warp per chunk");
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  ring_pass(rg, rowA, has_q ? rowB : nullptr, sl,
+            [&](const uint4 *A, const uint4 *Bp, int v0, int n) {
+              const int i = warp * 32 + lane;
+              const int seg0 = (v0 - sl.vbeg) / 32;
+              if (warp * 32 < n) {  // warp-uniform
+                float acc = 0.f;
+                if (i < n) {
+                  float w[VW];
+                  weights<DT, VW>(sget<DT, VW>(A, i),
+                                  sget<DT, VW>(has_q ? Bp : A, i), has_q, W,
+                                  w);
+#pragma unroll
+                  for (int e = 0; e < VW; ++e) acc += w[e];
+                }
+                acc = warp_down_sum(acc);
+                if (lane == 0) segmass[seg0 + warp] = acc;
+              }
+            });
+}
+
+}  // namespace sdv
