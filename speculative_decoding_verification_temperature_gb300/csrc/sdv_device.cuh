@@ -104,48 +104,72 @@ __device__ __forceinline__ float ex2(float x) {
 // ------------------------------------------------- online softmax state
 // Row statistics at temperature T with k2 = log2(e) / T:
 //   m = max_j z_j,  s = sum_j 2^(z_j k2 - m k2)
-// so that p_j = 2^(z_j k2 - m k2) / s.  NaN anywhere makes s NaN; +inf makes
-// m infinite; a row of only -inf leaves m = -inf: all three are "invalid".
+// so that p_j = 2^(z_j k2 - m k2) / s.  The empty state holds m = kMEmpty
+// (finite, below any usable logit) so the hot loop needs no test for
+// "nothing seen yet": -inf entries add 2^-inf = 0.  NaN anywhere makes s
+// NaN; +inf makes m infinite; a row of only -inf leaves m at kMEmpty and
+// s = 0: all three are "invalid".
+constexpr float kMEmpty = -3.0e38f;
+
 struct MS {
   float m;
   float s;
 };
 
-__device__ __forceinline__ MS ms_empty() { return {-kInf, 0.f}; }
+__device__ __forceinline__ MS ms_empty() { return {kMEmpty, 0.f}; }
 
 __device__ __forceinline__ MS ms_merge(MS a, MS b, float k2) {
   const float m = fmaxf(a.m, b.m);
-  if (m == -kInf) return {m, a.s + b.s};  // keeps a NaN marker
   return {m, a.s * ex2((a.m - m) * k2) + b.s * ex2((b.m - m) * k2)};
+}
+
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+template <int VW>
+__device__ __forceinline__ float vmax_of(const float (&z)[VW]) {
+  if constexpr (VW == 1) {
+    return z[0];
+  } else if constexpr (VW == 4) {
+    return fmaxf(max3f(z[0], z[1], z[2]), z[3]);
+  } else {
+    return max3f(max3f(z[0], z[1], z[2]), max3f(z[3], z[4], z[5]),
+                 fmaxf(z[6], z[7]));
+  }
 }
 
 template <int DT, int VW>
 __device__ __forceinline__ void ms_add(MS &st, const Raw<DT, VW> &r,
                                        float k2) {
-  float vmax = elt<DT, VW>(r, 0);
+  float z[VW];
 #pragma unroll
-  for (int e = 1; e < VW; ++e) vmax = fmaxf(vmax, elt<DT, VW>(r, e));
-  if (vmax > st.m) {
+  for (int e = 0; e < VW; ++e) z[e] = elt<DT, VW>(r, e);
+  const float vmax = vmax_of<VW>(z);
+  if (vmax > st.m) {  // rare once the row's large values have been seen
     st.s *= ex2((st.m - vmax) * k2);
     st.m = vmax;
   }
-  if (st.m == -kInf) {  // nothing finite yet: only look for NaN
+  const float mk = -st.m * k2;
+  if constexpr (VW == 1) {
+    st.s += ex2(fmaf(z[0], k2, mk));
+  } else {
+    // packed fp32x2 arithmetic (two lanes per instruction)
+    float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int e = 0; e < VW; ++e) {
-      const float z = elt<DT, VW>(r, e);
-      if (z != z) st.s = z;
+    for (int e = 0; e < VW; e += 2) {
+      const float2 t = __ffma2_rn(make_float2(z[e], z[e + 1]),
+                                  make_float2(k2, k2), make_float2(mk, mk));
+      acc = __fadd2_rn(acc, make_float2(ex2(t.x), ex2(t.y)));
     }
-    return;
+    st.s += acc.x + acc.y;
   }
-  const float mk = st.m * k2;
-  float acc = 0.f;
-#pragma unroll
-  for (int e = 0; e < VW; ++e) acc += ex2(fmaf(elt<DT, VW>(r, e), k2, -mk));
-  st.s += acc;
 }
 
 __device__ __forceinline__ bool ms_valid(MS st) {
-  return isfinite(st.m) && isfinite(st.s) && st.s > 0.f;
+  return st.m > -1.0e38f && isfinite(st.m) && isfinite(st.s) && st.s > 0.f;
 }
 
 // --------------------------------------------------------- argmax state

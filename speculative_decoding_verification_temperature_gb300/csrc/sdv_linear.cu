@@ -55,28 +55,31 @@ struct LinearParams {
   int nclusters;
   int seg_bytes;   // bytes of the segment-mass array (multiple of 128)
   int slice_vecs;  // capacity of each slice buffer in 16-byte vectors (TMA)
-  int prefetch;    // L2 prefetch: bit 0 next sequence's first rows,
-                   // bit 1 the next position's rows (speculative)
+  int spec;        // let a cluster's last sequence read ahead (0: never)
 };
 
-struct Decision {
-  int invalid;  // a row read is unusable
-  int accept;   // draft accepted at this position
-  int tok;      // greedy: argmax of the row
-  float acc_prob;
-  MS mt, md;  // merged stats of target / draft row
+constexpr int kMaxW = 8;  // positions per step when a cluster speculates
+
+struct StepResult {
+  int kind;   // 0 continue, 1 reject at n, 2 bonus, 3 unusable row
+  int n;      // accepted drafts so far
+  int tok;    // greedy: argmax of the final row
+  int bad;    // a bad token was seen
+  MS mt, md;  // merged stats of the final rows
 };
 
 struct LinearSmem {
   MS red[2][kWarps];
   AM ared[kWarps];
-  MS part[2][2];  // [parity][target, draft]: read by peers
-  AM apart[2];    // [parity]: read by peers
+  MS part[2][2 * kMaxW];  // [parity][2 * position + target/draft] (peers read)
+  AM apart[2][kMaxW];     // [parity][position] (peers read)
+  MS mrg[2 * kMaxW];      // merged stats of this step's rows
+  AM amrg[kMaxW];
   int next_seq[2];
-  Decision dec;
-  // gathered by thread 0 for the accept test, [step parity]
-  int gx[2];
-  float gzt[2], gzd[2], gr[2];
+  // gathered for the accept tests of this step's positions
+  int gx[kMaxW];
+  float gzt[kMaxW], gzd[kMaxW], gr[kMaxW];
+  StepResult res;
   DrawSmem draw;
 };
 
@@ -104,7 +107,12 @@ __global__ void __launch_bounds__(kThreads, RING ? 4 : 2)
   rg.full = bars;
   rg.dev_status = p.dev_status;
   if (RING) ring_init(rg);
-  const uint32_t slice_bytes = (uint32_t)(sl.vend - sl.vbeg) * 16u;
+  auto trow_of = [&](int s, int j) {
+    return tbase + ((size_t)s * (gamma + 1) + j) * rowb;
+  };
+  auto drow_of = [&](int s, int j) {
+    return dbase + ((size_t)s * p.d_seq_rows + j) * rowb;
+  };
 
   int par = 0, seqpar = 0;
   int seq = (int)(blockIdx.x / CL);
@@ -112,132 +120,144 @@ __global__ void __launch_bounds__(kThreads, RING ? 4 : 2)
     if (rank == 0 && tid == 0)
       sh.next_seq[seqpar] =
           p.queue ? p.nclusters + atomicAdd(p.queue, 1) : p.B;
-    int n = 0, kind = 0;  // kind: 1 reject at n, 2 bonus, 3 invalid row
-    int greedy_tok = -1, bad_token = 0;
-    MS fmt = ms_empty(), fmd = ms_empty();
-    for (int i = 0; i <= gamma; ++i) {
-      const bool has_d = (!GREEDY) && i < gamma;
-      const char *trow = tbase + ((size_t)seq * (gamma + 1) + i) * rowb;
-      const char *drow =
-          has_d ? dbase + ((size_t)seq * p.d_seq_rows + i) * rowb : nullptr;
-      if (tid == 0) {  // gathers for the accept test (used after the merge)
-        if (RING && (p.prefetch & 2) && i < gamma && slice_bytes) {
-          // speculative: the next position's slices, used only if this
-          // position accepts
-          prefetch_l2(trow + rowb + (size_t)sl.vbeg * 16, slice_bytes);
-          if (!GREEDY && i + 1 < gamma)
-            prefetch_l2(drow + rowb + (size_t)sl.vbeg * 16, slice_bytes);
-        }
+    // ---------------- scan: positions [i, i + w) per step -----------------
+    // w stays 1 while the work counter still hands out sequences; once this
+    // cluster holds its last sequence (nothing else to overlap with), w
+    // doubles each step: later positions are read speculatively, which
+    // shortens the longest scans at the end of the call.
+    int i = 0, w = 1;
+    bool last_seq = false, first = true;
+    StepResult R;
+    for (;;) {
+      const int jend = min(i + w, gamma + 1);
+      const int np = jend - i;
+      if (tid < np) {  // gathers for the accept tests (used after the merge)
+        const int j = i + tid;
         int x = -1;
-        float zt = 0.f, zd = 0.f;
-        if (i < gamma) {
-          x = p.tokens[(size_t)seq * gamma + i];
+        float zt = 0.f, zd = 0.f, r = 0.f;
+        if (j < gamma) {
+          x = p.tokens[(size_t)seq * gamma + j];
           if (!GREEDY && x >= 0 && x < V) {
-            zt = load_logit<DT>(trow, x);
-            zd = load_logit<DT>(drow, x);
+            zt = load_logit<DT>(trow_of(seq, j), x);
+            zd = load_logit<DT>(drow_of(seq, j), x);
           }
+          if (!GREEDY) r = p.uniforms[(size_t)seq * (gamma + 1) + j];
         }
-        sh.gx[par] = x;
-        sh.gzt[par] = zt;
-        sh.gzd[par] = zd;
-        sh.gr[par] =
-            GREEDY ? 0.f : p.uniforms[(size_t)seq * (gamma + 1) + i];
+        sh.gx[tid] = x;
+        sh.gzt[tid] = zt;
+        sh.gzd[tid] = zd;
+        sh.gr[tid] = r;
       }
-      if constexpr (GREEDY) {
-        AM a = am_empty();
-        if constexpr (RING) ring_argmax<DT, VW>(rg, trow, sl, a);
-        else argmax_pass<DT, VW>(GR{trow}, sl, a);
-        a = block_reduce_am(a, sh.ared);
-        if (tid == 0) sh.apart[par] = a;
-      } else {
-        MS st[2] = {ms_empty(), ms_empty()};
-        if constexpr (RING) ring_stats<DT, VW>(rg, trow, drow, sl, k2, st[0], st[1]);
-        else stats_pass<DT, VW>(GR{trow}, GR{drow}, has_d, sl, k2, st[0], st[1]);
-        block_reduce_ms<2>(st, k2, sh.red);
-        if (tid == 0) {
-          sh.part[par][0] = st[0];
-          sh.part[par][1] = st[1];
+      if (RING && last_seq && p.spec >= 2 && tid == 0) {
+        // the GPU is emptying out: ask for this step's and the next step's
+        // rows at once (into L2), so the ring below streams from L2
+        const uint32_t sb = (uint32_t)(sl.vend - sl.vbeg) * 16u;
+        const int jpre = min(i + 3 * w, gamma + 1);
+        for (int j = i; j < jpre && sb; ++j) {
+          prefetch_l2(trow_of(seq, j) + (size_t)sl.vbeg * 16, sb);
+          if (!GREEDY && j < gamma)
+            prefetch_l2(drow_of(seq, j) + (size_t)sl.vbeg * 16, sb);
         }
       }
-      cluster.sync();
-      // every CTA merges the CL partials in the same order: same decision
-      if (warp == 0) {
-        Decision d{};
-        const int x = sh.gx[par];
+      for (int t = 0; t < np; ++t) {
+        const int j = i + t;
+        const bool has_d = (!GREEDY) && j < gamma;
+        const char *trow = trow_of(seq, j);
+        const char *drow = has_d ? drow_of(seq, j) : nullptr;
         if constexpr (GREEDY) {
           AM a = am_empty();
-          if (lane < CL) a = cluster.map_shared_rank(&sh, lane)->apart[par];
-          a = warp_down_am(a);
-          d.invalid = a.bad || !(a.v > -kInf);
-          d.tok = a.i;
-          d.accept = (i < gamma) && !d.invalid && x == a.i;
-          d.acc_prob = d.accept ? 1.f : 0.f;
+          if constexpr (RING) ring_argmax<DT, VW>(rg, trow, sl, a);
+          else argmax_pass<DT, VW>(GR{trow}, sl, a);
+          a = block_reduce_am(a, sh.ared);
+          if (tid == 0) sh.apart[par][t] = a;
         } else {
-          MS mt = ms_empty(), md = ms_empty();
-          if (lane < CL) {
-            const LinearSmem *rs = cluster.map_shared_rank(&sh, lane);
-            mt = rs->part[par][0];
-            md = rs->part[par][1];
-          }
-          mt = warp_down_ms(mt, k2);
-          md = warp_down_ms(md, k2);
-          d.mt = mt;
-          d.md = md;
-          d.invalid = !ms_valid(mt) || (has_d && !ms_valid(md));
-          if (!d.invalid && has_d && x >= 0 && x < V) {
-            // p(x)/q(x) with the same scaled exponents the draw uses
-            const float e = fmaf(sh.gzt[par], k2, -mt.m * k2) -
-                            fmaf(sh.gzd[par], k2, -md.m * k2);
-            const float rho = exp2f(e) * (md.s / mt.s);
-            d.accept = sh.gr[par] <= rho;
-            d.acc_prob = fminf(1.f, rho);
+          MS st[2] = {ms_empty(), ms_empty()};
+          if constexpr (RING) ring_stats<DT, VW>(rg, trow, drow, sl, k2, st[0], st[1]);
+          else stats_pass<DT, VW>(GR{trow}, GR{drow}, has_d, sl, k2, st[0], st[1]);
+          block_reduce_ms<2>(st, k2, sh.red);
+          if (tid == 0) {
+            sh.part[par][2 * t] = st[0];
+            sh.part[par][2 * t + 1] = st[1];
           }
         }
-        if (lane == 0) sh.dec = d;
+        __syncthreads();
+      }
+      cluster.sync();
+      // every CTA merges the CL partials of every row in the same order
+      const int nrows = GREEDY ? np : 2 * np;
+      for (int r = warp; r < nrows; r += kWarps) {
+        if constexpr (GREEDY) {
+          AM a = am_empty();
+          if (lane < CL) a = cluster.map_shared_rank(&sh, lane)->apart[par][r];
+          a = warp_down_am(a);
+          if (lane == 0) sh.amrg[r] = a;
+        } else {
+          MS m = ms_empty();
+          if (lane < CL) m = cluster.map_shared_rank(&sh, lane)->part[par][r];
+          m = warp_down_ms(m, k2);
+          if (lane == 0) sh.mrg[r] = m;
+        }
       }
       __syncthreads();
-      const Decision d = sh.dec;
-      const int x = sh.gx[par];
       par ^= 1;
-      if (i < gamma && (x < 0 || x >= V)) bad_token = 1;
-      if (rank == 0 && tid == 0 && p.out_accept && i < gamma && !d.invalid)
-        p.out_accept[(size_t)seq * gamma + i] = d.acc_prob;
-      if (d.invalid) {
-        kind = 3;
-        break;
+      if (tid == 0) {  // the accept tests of this step, in position order
+        StepResult q = (i == 0) ? StepResult{0, 0, -1, 0, ms_empty(), ms_empty()} : sh.res;
+        q.kind = 0;
+        for (int t = 0; t < np && !q.kind; ++t) {
+          const int j = i + t;
+          const int x = sh.gx[t];
+          const bool bad = j < gamma && (x < 0 || x >= V);
+          q.bad |= bad;
+          bool invalid, acc = false;
+          float accp = 0.f;
+          if constexpr (GREEDY) {
+            const AM a = sh.amrg[t];
+            invalid = a.bad || !(a.v > -kInf);
+            acc = !invalid && j < gamma && x == a.i;
+            accp = acc ? 1.f : 0.f;
+            q.tok = a.i;
+          } else {
+            const MS mt = sh.mrg[2 * t], md = sh.mrg[2 * t + 1];
+            invalid = !ms_valid(mt) || (j < gamma && !ms_valid(md));
+            if (!invalid && j < gamma && !bad) {
+              // p(x)/q(x) with the same scaled exponents the draw uses
+              const float e = fmaf(sh.gzt[t], k2, -mt.m * k2) -
+                              fmaf(sh.gzd[t], k2, -md.m * k2);
+              const float rho = exp2f(e) * (md.s / mt.s);
+              acc = sh.gr[t] <= rho;
+              accp = fminf(1.f, rho);
+            }
+            q.mt = mt;
+            q.md = md;
+          }
+          if (rank == 0 && p.out_accept && j < gamma && !invalid)
+            p.out_accept[(size_t)seq * gamma + j] = accp;
+          if (invalid) q.kind = 3;
+          else if (j == gamma) q.kind = 2;
+          else if (!acc) q.kind = 1;
+          else ++q.n;
+        }
+        sh.res = q;
       }
-      greedy_tok = d.tok;
-      fmt = d.mt;
-      fmd = d.md;
-      if (i == gamma) {
-        kind = 2;
-        break;
+      __syncthreads();
+      R = sh.res;
+      if (R.kind) break;
+      i = jend;
+      if (first) {  // after the first step: is this the cluster's last?
+        last_seq = cluster.map_shared_rank(&sh, 0)->next_seq[seqpar] >= p.B;
+        first = false;
       }
-      if (!d.accept) {
-        kind = 1;
-        break;
-      }
-      ++n;
+      w = (last_seq && p.spec) ? min(2 * w, kMaxW) : 1;
     }
-    if (RING && (p.prefetch & 1) && tid == 0 && slice_bytes) {
-      // the next sequence's first rows, into L2 while this one draws
-      const int nxt = cluster.map_shared_rank(&sh, 0)->next_seq[seqpar];
-      if (nxt < p.B) {
-        prefetch_l2(tbase + (size_t)nxt * (gamma + 1) * rowb +
-                        (size_t)sl.vbeg * 16, slice_bytes);
-        if (!GREEDY && gamma > 0)
-          prefetch_l2(dbase + (size_t)nxt * p.d_seq_rows * rowb +
-                          (size_t)sl.vbeg * 16, slice_bytes);
-      }
-    }
+    const int n = R.n, kind = R.kind, bad_token = R.bad;
 
     if (kind == 3) {  // unusable row: outputs -1
       if (rank == 0) {
-        for (int i = tid; i <= gamma; i += kThreads)
-          p.out_tokens[(size_t)seq * (gamma + 1) + i] = -1;
+        for (int t = tid; t <= gamma; t += kThreads)
+          p.out_tokens[(size_t)seq * (gamma + 1) + t] = -1;
         if (p.out_accept)
-          for (int i = n + tid; i < gamma; i += kThreads)
-            p.out_accept[(size_t)seq * gamma + i] = -1.f;
+          for (int t = n + tid; t < gamma; t += kThreads)
+            p.out_accept[(size_t)seq * gamma + t] = -1.f;
         if (tid == 0) {
           p.n_acc[seq] = -1;
           if (p.out_prob) p.out_prob[seq] = 0.f;
@@ -247,15 +267,15 @@ __global__ void __launch_bounds__(kThreads, RING ? 4 : 2)
       }
     } else if (GREEDY) {
       if (rank == 0) {
-        for (int i = tid; i <= gamma; i += kThreads) {
+        for (int t = tid; t <= gamma; t += kThreads) {
           int v = -1;
-          if (i < n) v = p.tokens[(size_t)seq * gamma + i];
-          else if (i == n) v = greedy_tok;
-          p.out_tokens[(size_t)seq * (gamma + 1) + i] = v;
+          if (t < n) v = p.tokens[(size_t)seq * gamma + t];
+          else if (t == n) v = R.tok;
+          p.out_tokens[(size_t)seq * (gamma + 1) + t] = v;
         }
         if (p.out_accept)
-          for (int i = n + 1 + tid; i < gamma; i += kThreads)
-            p.out_accept[(size_t)seq * gamma + i] = -1.f;
+          for (int t = n + 1 + tid; t < gamma; t += kThreads)
+            p.out_accept[(size_t)seq * gamma + t] = -1.f;
         if (tid == 0) {
           p.n_acc[seq] = n;
           if (p.out_prob) p.out_prob[seq] = 1.f;
@@ -265,23 +285,21 @@ __global__ void __launch_bounds__(kThreads, RING ? 4 : 2)
       if (p.out_resid) {
         float *res = p.out_resid + (size_t)seq * V;
         for (int j = sl.vbeg * VW + tid; j < sl.vend * VW; j += kThreads)
-          res[j] = (j == greedy_tok) ? 1.f : 0.f;
+          res[j] = (j == R.tok) ? 1.f : 0.f;
       }
     } else {
       // correction (kind 1) or bonus (kind 2) by inverse CDF over the rows
-      // of the last step (streamed again: they were just read, so from L2)
-      const char *trow = tbase + ((size_t)seq * (gamma + 1) + n) * rowb;
-      const char *drow =
-          kind == 1 ? dbase + ((size_t)seq * p.d_seq_rows + n) * rowb
-                    : nullptr;
+      // of position n (streamed again: they were just read, so from L2)
+      const char *trow = trow_of(seq, n);
+      const char *drow = kind == 1 ? drow_of(seq, n) : nullptr;
       const GR ra{trow}, rb{drow ? drow : trow};
       bool has_q = kind == 1;
       Weight W;
       W.k2 = k2;
-      W.mtk = fmt.m * k2;
-      W.ist = 1.f / fmt.s;
-      W.mdk = fmd.m * k2;
-      W.cq = 1.f / fmd.s;
+      W.mtk = R.mt.m * k2;
+      W.ist = 1.f / R.mt.s;
+      W.mdk = R.md.m * k2;
+      W.cq = 1.f / R.md.s;
       const float u = p.uniforms[(size_t)seq * (gamma + 1) + gamma];
       int zero_mass = 0;
       DrawOut o;
@@ -297,15 +315,15 @@ __global__ void __launch_bounds__(kThreads, RING ? 4 : 2)
         __syncthreads();
       }
       if (o.owner == rank && warp == 0) {
-        for (int i = lane; i <= gamma; i += 32) {
+        for (int t = lane; t <= gamma; t += 32) {
           int v = -1;
-          if (i < n) v = p.tokens[(size_t)seq * gamma + i];
-          else if (i == n) v = o.t;
-          p.out_tokens[(size_t)seq * (gamma + 1) + i] = v;
+          if (t < n) v = p.tokens[(size_t)seq * gamma + t];
+          else if (t == n) v = o.t;
+          p.out_tokens[(size_t)seq * (gamma + 1) + t] = v;
         }
         if (p.out_accept)
-          for (int i = n + 1 + lane; i < gamma; i += 32)
-            p.out_accept[(size_t)seq * gamma + i] = -1.f;
+          for (int t = n + 1 + lane; t < gamma; t += 32)
+            p.out_accept[(size_t)seq * gamma + t] = -1.f;
         if (lane == 0) {
           p.n_acc[seq] = n;
           if (p.out_prob) p.out_prob[seq] = (float)((double)o.wt / o.N);
@@ -399,7 +417,7 @@ sd_status linear_launch(const void *target, const void *draft, sd_dtype dt,
   prm.nclusters = nclusters;
   prm.seg_bytes = (int)seg_bytes;
   prm.slice_vecs = (int)per_cta;
-  prm.prefetch = env_int("SDV_PREFETCH", 0);
+  prm.spec = env_int("SDV_SPEC", 1);
   if (B > nclusters) {
     if (!ws || ws_bytes < 256)
       return fail(SD_ERR_INVALID_ARG, "workspace of >= 256 bytes required");
@@ -411,15 +429,35 @@ sd_status linear_launch(const void *target, const void *draft, sd_dtype dt,
                          args);
 }
 
+size_t wide_workspace(int B, int gamma, int V, sd_dtype dt);
+sd_status wide_launch(const void *target, const void *draft, sd_dtype dt,
+                      long long d_seq_rows, const int32_t *tokens,
+                      const float *uniforms, int B, int gamma, int V, float T,
+                      int32_t *n_acc, int32_t *out_tokens, float *out_prob,
+                      float *out_accept, int32_t *dev_status, void *ws,
+                      size_t ws_bytes, cudaStream_t stream);
+
+// The position-by-position kernels over the whole batch (sdv_wide.cu) are
+// selected with SDV_WIDE=1; the cluster kernel below is faster on the
+// measured workloads, so that path is opt-in.
+bool use_wide(int B, int V, sd_dtype dt, const void *target,
+              const void *draft, float T, const float *out_resid) {
+  const int eb = dt == SD_F32 ? 4 : 2;
+  const bool vec = aligned16(target) && (T == 0.f || aligned16(draft)) &&
+                   ((size_t)V * eb) % 16 == 0;
+  if (!vec || out_resid) return false;
+  (void)B;
+  return env_int("SDV_WIDE", 0) != 0;
+}
+
 }  // namespace sdv
 
 extern "C" size_t sd_verify_linear_workspace(int B, int gamma, int V,
                                              sd_dtype dt) {
-  (void)B;
-  (void)gamma;
-  (void)V;
-  (void)dt;
-  return 256;
+  const size_t w = (B > 0 && V > 0 && gamma >= 0)
+                       ? sdv::wide_workspace(B, gamma, V, dt)
+                       : 0;
+  return w > 256 ? w : 256;
 }
 
 extern "C" sd_status sd_verify_linear(
@@ -440,6 +478,12 @@ extern "C" sd_status sd_verify_linear(
   SDV_REQUIRE(T == 0.f || uniforms, "uniforms is null");
   SDV_REQUIRE(T == 0.f || gamma == 0 || draft_logits,
               "draft_logits is null with T > 0");
+  if (sdv::use_wide(B, V, dt, target_logits, draft_logits, T, out_resid))
+    return sdv::wide_launch(target_logits, draft_logits, dt, gamma,
+                            draft_tokens, uniforms, B, gamma, V, T,
+                            n_accepted, out_tokens, out_prob, out_accept_prob,
+                            dev_status, workspace, ws_bytes,
+                            static_cast<cudaStream_t>(stream));
   return sdv::linear_launch(target_logits, draft_logits, dt, gamma,
                             draft_tokens, uniforms, B, gamma, V, T,
                             n_accepted, out_tokens, out_prob, out_accept_prob,

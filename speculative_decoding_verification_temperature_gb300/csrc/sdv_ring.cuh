@@ -14,9 +14,15 @@
 
 namespace sdv {
 
-constexpr int kStg = 256;    // 16-byte vectors per row per stage
-constexpr int kStages = 4;   // stages in flight
-constexpr int kRingBytes = kStages * 2 * kStg * 16;  // 32 KB
+#ifndef SDV_STAGES
+#define SDV_STAGES 3
+#endif
+#ifndef SDV_STG
+#define SDV_STG 512
+#endif
+constexpr int kStg = SDV_STG;         // 16-byte vectors per row per stage
+constexpr int kStages = SDV_STAGES;   // stages in flight
+constexpr int kRingBytes = kStages * 2 * kStg * 16;  // 48 KB
 
 struct Ring {
   uint4 *buf;          // [kStages][2][kStg]
@@ -104,19 +110,20 @@ __device__ __forceinline__ void ring_argmax(Ring &rg, const char *rowA,
 }
 
 // Per-segment masses (segment s = vectors vbeg + 32 s ..) of the weights
-// W over the slice; a chunk holds kStg / 32 segments, one per warp.
+// W over the slice; a chunk holds kStg / 32 segments, warp w takes
+// segments w, w + 8, ...
 template <int DT, int VW>
 __device__ __forceinline__ void ring_mass(Ring &rg, const char *rowA,
                                           const char *rowB, bool has_q,
                                           const Weight &W, const Slice &sl,
                                           float *segmass) {
-  static_assert(kStg == 32 * kWarps, "one segment per warp per chunk");
+  static_assert(kStg % 32 == 0, "whole segments per chunk");
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   ring_pass(rg, rowA, has_q ? rowB : nullptr, sl,
             [&](const uint4 *A, const uint4 *Bp, int v0, int n) {
-              const int i = warp * 32 + lane;
               const int seg0 = (v0 - sl.vbeg) / 32;
-              if (warp * 32 < n) {  // warp-uniform
+              for (int g = warp; g * 32 < n; g += kWarps) {  // warp-uniform
+                const int i = g * 32 + lane;
                 float acc = 0.f;
                 if (i < n) {
                   float w[VW];
@@ -127,7 +134,7 @@ __device__ __forceinline__ void ring_mass(Ring &rg, const char *rowA,
                   for (int e = 0; e < VW; ++e) acc += w[e];
                 }
                 acc = warp_down_sum(acc);
-                if (lane == 0) segmass[seg0 + warp] = acc;
+                if (lane == 0) segmass[seg0 + g] = acc;
               }
             });
 }
