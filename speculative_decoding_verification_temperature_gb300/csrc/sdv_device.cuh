@@ -536,8 +536,10 @@ __device__ __forceinline__ void mass_pass(const Row &ra, const Row &rb,
 }
 
 // Shared state of a cluster-wide inverse-CDF draw (one per CTA).
+constexpr int kMaxCL = 16;  // CTAs per cluster
+
 struct DrawSmem {
-  double slice[2];  // [parity] this CTA's slice mass (read by peers)
+  double slice[2];  // [parity] this CTA's slice mass (peers read)
   double chunk_pre[32];
   double N;      // total mass (all CTAs agree)
   double tau;    // u * N minus the mass of the slices before the owner

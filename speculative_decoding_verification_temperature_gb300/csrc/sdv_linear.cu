@@ -58,7 +58,7 @@ struct LinearParams {
   int spec;        // let a cluster's last sequence read ahead (0: never)
 };
 
-constexpr int kMaxW = 8;  // positions per step when a cluster speculates
+constexpr int kMaxW = 4;  // positions per step when a cluster speculates
 
 struct StepResult {
   int kind;   // 0 continue, 1 reject at n, 2 bonus, 3 unusable row
@@ -71,8 +71,11 @@ struct StepResult {
 struct LinearSmem {
   MS red[2][kWarps];
   AM ared[kWarps];
-  MS part[2][2 * kMaxW];  // [parity][2 * position + target/draft] (peers read)
-  AM apart[2][kMaxW];     // [parity][position] (peers read)
+  // [parity][row]: this CTA's partials of the step's rows (peers read)
+  union {
+    MS part[2][2 * kMaxW];
+    AM apart[2][kMaxW];
+  };
   MS mrg[2 * kMaxW];      // merged stats of this step's rows
   AM amrg[kMaxW];
   int next_seq[2];
@@ -88,7 +91,7 @@ __global__ void __launch_bounds__(kThreads, RING ? 4 : 2)
     linear_verify_kernel(const LinearParams p) {
   extern __shared__ __align__(128) unsigned char dsm[];
   __shared__ LinearSmem sh;
-  __shared__ uint64_t bars[kStages];
+  __shared__ uint64_t bars[2 * kStages];
   using GR = GRow<DT, VW>;
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
@@ -105,6 +108,7 @@ __global__ void __launch_bounds__(kThreads, RING ? 4 : 2)
   Ring rg;
   rg.buf = reinterpret_cast<uint4 *>(dsm + p.seg_bytes);
   rg.full = bars;
+  rg.empty = bars + kStages;
   rg.dev_status = p.dev_status;
   if (RING) ring_init(rg);
   auto trow_of = [&](int s, int j) {
@@ -182,9 +186,9 @@ __global__ void __launch_bounds__(kThreads, RING ? 4 : 2)
         }
         __syncthreads();
       }
+      const int nrows = GREEDY ? np : 2 * np;
       cluster.sync();
       // every CTA merges the CL partials of every row in the same order
-      const int nrows = GREEDY ? np : 2 * np;
       for (int r = warp; r < nrows; r += kWarps) {
         if constexpr (GREEDY) {
           AM a = am_empty();

@@ -3,10 +3,13 @@
 // mbarrier per stage).
 //
 // Thread 0 keeps kStages chunks in flight; every thread consumes chunk c
-// as soon as its stage's barrier completes, and after a block barrier the
-// stage is refilled with chunk c + kStages.  The bytes in flight per CTA
-// are the whole ring, independent of registers, so several CTAs per SM
-// keep HBM busy while each one also spends time in cluster barriers.
+// as soon as its stage's "full" barrier completes, and the stage is refilled
+// with chunk c + kStages after a block barrier (SDV_RING_SYNC=1, measured
+// faster) or once every warp has arrived on the stage's "empty" barrier
+// (SDV_RING_SYNC=0: warps then run ahead of each other by up to kStages - 1
+// chunks).  The bytes in flight per CTA are the whole ring, independent of
+// registers, so several CTAs per SM keep HBM busy while each one also
+// spends time in cluster barriers.
 #pragma once
 
 #include "sdv_device.cuh"
@@ -20,23 +23,34 @@ namespace sdv {
 #ifndef SDV_STG
 #define SDV_STG 512
 #endif
+#ifndef SDV_RING_SYNC
+#define SDV_RING_SYNC 1
+#endif
 constexpr int kStg = SDV_STG;         // 16-byte vectors per row per stage
 constexpr int kStages = SDV_STAGES;   // stages in flight
 constexpr int kRingBytes = kStages * 2 * kStg * 16;  // 48 KB
 
 struct Ring {
   uint4 *buf;          // [kStages][2][kStg]
-  uint64_t *full;      // [kStages] mbarriers
-  uint32_t phase;      // bit s: parity of the next completion of stage s
+  uint64_t *full;      // [kStages] mbarriers: data landed (tx bytes)
+  uint64_t *empty;     // [kStages] mbarriers: every warp is done with it
+  uint32_t phase;      // bit s: parity of stage s's next "full" completion
+  uint32_t used;       // thread 0: bit s set once stage s was filled
+  uint32_t epar;       // thread 0: bit s: parity of the "empty" wait due
   int32_t *dev_status;
 };
 
 __device__ __forceinline__ void ring_init(Ring &rg) {
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(&rg.full[s], 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&rg.full[s], 1);
+      mbar_init(&rg.empty[s], kWarps);
+    }
     fence_mbar_init();
   }
   rg.phase = 0;
+  rg.used = 0;
+  rg.epar = 0;
   __syncthreads();
 }
 
@@ -50,11 +64,16 @@ __device__ __forceinline__ void ring_pass(Ring &rg, const char *rowA,
                                           F &&f) {
   const int nv = sl.vend - sl.vbeg;
   const int nch = (nv + kStg - 1) / kStg;
-  auto issue = [&](int c) {
+  auto issue = [&](int c) {  // thread 0 only
     const int s = c % kStages;
     const int v0 = c * kStg;
     const int cnt = min(kStg, nv - v0);
     const uint32_t bytes = (uint32_t)cnt * 16u;
+    if (!SDV_RING_SYNC && (rg.used >> s & 1u)) {  // every warp released it
+      mbar_wait(&rg.empty[s], (rg.epar >> s) & 1u, rg.dev_status);
+      rg.epar ^= 1u << s;
+    }
+    rg.used |= 1u << s;
     fence_proxy_async();
     mbar_expect_tx(&rg.full[s], bytes * (rowB ? 2u : 1u));
     bulk_g2s(rg.buf + (size_t)(2 * s) * kStg,
@@ -71,8 +90,14 @@ __device__ __forceinline__ void ring_pass(Ring &rg, const char *rowA,
     rg.phase ^= 1u << s;
     f(rg.buf + (size_t)(2 * s) * kStg, rg.buf + (size_t)(2 * s + 1) * kStg,
       sl.vbeg + c * kStg, min(kStg, nv - c * kStg));
+#if SDV_RING_SYNC
     __syncthreads();
     if (threadIdx.x == 0 && c + kStages < nch) issue(c + kStages);
+#else
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&rg.empty[s]);
+    if (threadIdx.x == 0 && c + kStages < nch) issue(c + kStages);
+#endif
   }
 }
 

@@ -13,7 +13,11 @@
 
 namespace sdv {
 
-constexpr unsigned kWaitLimit = 1u << 26;  // polls (seconds of waiting)
+#ifndef SDV_SUSPEND
+#define SDV_SUSPEND 0
+#endif
+constexpr unsigned kWaitLimit = 1u << 26;  // polls: seconds of waiting
+constexpr unsigned kSuspendNs = 1000;      // suspend hint per poll
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -62,8 +66,19 @@ __device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
                : "memory");
 }
 
+// One poll; the thread may be suspended (up to kSuspendNs) until the
+// phase completes, so a waiting warp issues almost nothing.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   uint32_t ok;
+#if SDV_SUSPEND
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(kSuspendNs)
+      : "memory");
+#else
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
@@ -71,7 +86,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
       : "=r"(ok)
       : "r"(smem_addr(bar)), "r"(parity)
       : "memory");
+#endif
   return ok != 0;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar))
+               : "memory");
 }
 
 // Wait for phase `parity` of the barrier to complete; bounded.

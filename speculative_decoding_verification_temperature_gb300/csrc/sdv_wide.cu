@@ -84,11 +84,12 @@ template <int DT, int VW, bool GREEDY>
 __global__ void __launch_bounds__(kThreads, 4) wide_level_kernel(const WideParams p) {
   extern __shared__ __align__(128) unsigned char dsm[];
   __shared__ WideSmem sh;
-  __shared__ uint64_t bars[kStages];
+  __shared__ uint64_t bars[2 * kStages];
   float *segmass = reinterpret_cast<float *>(dsm);
   Ring rg;
   rg.buf = reinterpret_cast<uint4 *>(dsm + p.seg_bytes);
   rg.full = bars;
+  rg.empty = bars + kStages;
   rg.dev_status = p.dev_status;
   ring_init(rg);
 #if defined(__CUDA_ARCH__)
