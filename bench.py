@@ -139,98 +139,134 @@ def gpu_arm(args, rank, world):
     sets = make_sets(args.sets, dev)
     stream = torch.cuda.current_stream(dev)
     ws = api.Workspace()
+    F = api.fanout_schedule(FAN["K"], FAN["budget"], FAN["a"], FAN["r"])
 
-    def step(c):
+    def verify(c):
         return api.verify_linear(c.target, c.draft_v, c.tokens, c.uniforms,
                                  T, workspace=ws)
 
-    # bytes the method needs per set (deterministic outputs)
-    need = []
+    def fanout(c):
+        return api.fanout_topk(c.draft, F, workspace=ws)
+
+    # bytes the method needs per set (deterministic outputs): target rows
+    # 0..n of every sequence and all K+1 draft rows (the fan-out reads them
+    # all; the verify's draft rows are a subset)
+    need, need_v = [], []
     for c in sets:
-        o = step(c)
-        need.append(needed_bytes(o["n"].cpu().numpy(), GAMMA, V, ELT))
+        n = verify(c)["n"].cpu().numpy().astype(np.int64)
+        fanout(c)
+        need_v.append(needed_bytes(n, GAMMA, V, ELT))
+        need.append(int((n + 1).sum()) * V * ELT + B * (FAN["K"] + 1) * V * ELT)
     for i in range(args.warmup):
-        step(sets[i % len(sets)])
+        verify(sets[i % len(sets)])
+        fanout(sets[i % len(sets)])
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     clocks = ClockSampler(dev.index or 0)
     clocks.start()
-    ev = [(torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)]
+          for _ in range(args.steps)]
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for i in range(args.steps):
+        c = sets[i % len(sets)]
         ev[i][0].record(stream)
-        step(sets[i % len(sets)])
+        verify(c)
         ev[i][1].record(stream)
+        fanout(c)
+        ev[i][2].record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
     clk = clocks.stop()
-    per = [a.elapsed_time(b) for a, b in ev]   # ms per step (device)
+    per = [e[0].elapsed_time(e[2]) for e in ev]       # ms per step (device)
+    per_v = [e[0].elapsed_time(e[1]) for e in ev]     # of which verify
+    per_f = [e[1].elapsed_time(e[2]) for e in ev]     # of which fan-out
     total_ms = sum(per)
     if world > 1:
         t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         total_ms = float(t.item())
     ms = total_ms / args.steps
+    ms_v = sum(per_v) / args.steps
+    ms_f = sum(per_f) / args.steps
     rounds_s = world * args.steps / (total_ms / 1e3)
-    need_avg = sum(need[i % len(sets)] for i in range(args.steps)) / args.steps
-    tensor_bytes = B * (2 * GAMMA + 1) * V * ELT
+    avg = lambda xs: sum(xs[i % len(sets)] for i in range(args.steps)) / args.steps
+    need_avg, need_v_avg = avg(need), avg(need_v)
+    fan_bytes = B * (FAN["K"] + 1) * V * ELT
+    tensor_bytes = B * (GAMMA + 1) * V * ELT + fan_bytes
     peak, src = hbm_peak()
-    achieved = need_avg / (ms / 1e3) / 1e9
+    # dominant kernel: the larger of the two shares of the step
+    if ms_v >= ms_f:
+        kern, kb, kms = "linear_verify_kernel<0,4,false,true>", need_v_avg, ms_v
+    else:
+        kern, kb, kms = "fanout_kernel<0,4>", fan_bytes, ms_f
+    achieved = kb / (kms / 1e3) / 1e9
     res = {
         "metric": METRIC, "value": rounds_s, "unit": "rounds/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": WORKLOAD, "B": B, "gamma": GAMMA, "V": V,
-                   "T": T, "input_sets": len(sets),
+                   "T": T, "fanout_F": F, "input_sets": len(sets),
+                   "step": "sd_verify_linear then sd_fanout_topk",
                    "l2": "inputs %.2f GB per set (> 129 MB L2), %d sets "
-                         "rotated" % (2 * tensor_bytes / 1e9, len(sets)),
+                         "rotated" % (2 * B * (GAMMA + 1) * V * ELT / 1e9,
+                                      len(sets)),
                    "parallelism": "replicas" if world > 1 else "single"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak,
                      "traffic": None,
                      "peak_source": "MEASURED_PEAKS.json hbm_gbs (%s)" % src,
-                     "kernel": "linear_verify_kernel<0,4,false>",
-                     "bytes_per_launch": need_avg,
-                     "full_tensor_bytes": tensor_bytes,
-                     "median_ms": statistics.median(per)},
-        "gpu_launches": args.steps,
+                     "kernel": kern, "bytes_per_launch": kb,
+                     "ms_per_launch": kms},
+        "step_bytes_read": need_avg,
+        "step_gbs": need_avg / (ms / 1e3) / 1e9,
+        "step_frac": need_avg / (ms / 1e3) / 1e9 / peak,
+        "full_tensor_bytes": tensor_bytes,
+        "verify": {"ms": ms_v, "bytes": need_v_avg,
+                   "gbs": need_v_avg / (ms_v / 1e3) / 1e9},
+        "fanout": {"ms": ms_f, "bytes": fan_bytes,
+                   "gbs": fan_bytes / (ms_f / 1e3) / 1e9},
+        "gpu_launches": 2 * args.steps,
         "clocks": clk,
         "wall_s": wall,
     }
     if args.e2e_steps > 0:
-        res["e2e"] = e2e_arm(args, sets, dev, ws, world)
+        res["e2e"] = e2e_arm(args, sets, dev, ws, world, F)
     if args.aux_steps > 0:
         res["other_workloads"] = other_workloads(args, dev, peak)
     if rank == 0 and args.oracle_seqs > 0:
-        res["cpu_baseline"] = cpu_baseline(sets, args.oracle_seqs)
+        res["cpu_baseline"] = cpu_baseline(sets, args.oracle_seqs, F)
     return res
 
 
-def e2e_arm(args, sets, dev, ws, world):
+def e2e_arm(args, sets, dev, ws, world, F):
     """Same metric through the public API with host buffers: per step the
     pinned-host inputs are copied to the device, verified, and the results
     copied back."""
     from speculative_decoding_verification_temperature_gb300 import api
     c = sets[0]
     h = {k: getattr(c, k).cpu().pin_memory()
-         for k in ("target", "draft_v", "tokens", "uniforms")}
+         for k in ("target", "draft", "tokens", "uniforms")}
     d = {k: torch.empty_like(v, device=dev) for k, v in h.items()}
     out_h = {"n": torch.empty(B, dtype=torch.int32).pin_memory(),
              "tokens": torch.empty((B, GAMMA + 1),
                                    dtype=torch.int32).pin_memory(),
-             "prob": torch.empty(B, dtype=torch.float32).pin_memory()}
+             "prob": torch.empty(B, dtype=torch.float32).pin_memory(),
+             "fan_tokens": torch.empty((B, sum(F)),
+                                       dtype=torch.int32).pin_memory()}
     stream = torch.cuda.current_stream(dev)
     steps = max(3, min(args.steps, args.e2e_steps))
 
     def step():
         for k in h:
             d[k].copy_(h[k], non_blocking=True)
-        o = api.verify_linear(d["target"], d["draft_v"], d["tokens"],
-                              d["uniforms"], T, workspace=ws)
+        dv = d["draft"][:, :GAMMA].contiguous()
+        o = api.verify_linear(d["target"], dv, d["tokens"], d["uniforms"], T,
+                              workspace=ws)
+        o["fan_tokens"] = api.fanout_topk(d["draft"], F,
+                                          workspace=ws)["tokens"]
         for k in out_h:
             out_h[k].copy_(o[k], non_blocking=True)
 
@@ -361,26 +397,28 @@ def other_workloads(args, dev, peak):
 
 
 # --------------------------------------------------------- CPU oracle
-def oracle_sample(c, seqs):
+def oracle_sample(c, seqs, F):
     import oracle
     t = synth.host_logits(c.target[seqs])
-    d = synth.host_logits(c.draft[seqs, :GAMMA])
+    dall = synth.host_logits(c.draft[seqs])
+    d = np.ascontiguousarray(dall[:, :GAMMA])
     tk = c.tokens[seqs].cpu().numpy()
     u = c.uniforms[seqs].cpu().numpy()
     t0 = time.perf_counter()
     oracle.verify_linear(t, d, tk, u, T)
+    oracle.fanout_topk(dall, np.array(F, np.int32))
     return time.perf_counter() - t0
 
 
-def cpu_baseline(sets, nseq):
+def cpu_baseline(sets, nseq, F):
     seqs = list(range(nseq))
-    dt = oracle_sample(sets[0], seqs)
+    dt = oracle_sample(sets[0], seqs, F)
     per_round = dt / nseq * B
     return {"value": 1.0 / per_round, "unit": "rounds/s", "cores": 1,
             "kind": "oracle",
-            "sample": "fp64 C oracle, single thread, on %d of the %d "
-                      "sequences of one round (%.2f s), scaled to a full "
-                      "round" % (nseq, B, dt)}
+            "sample": "fp64 C oracle (verify + fan-out), single thread, "
+                      "on %d of the %d sequences of one round (%.2f s), "
+                      "scaled to a full round" % (nseq, B, dt)}
 
 
 def reference_arm(args):
@@ -391,15 +429,19 @@ def reference_arm(args):
     oracle.build()
     c = synth.large(0, device="cuda" if torch.cuda.is_available() else "cpu")
     t_all = synth.host_logits(c.target)
-    d_all = synth.host_logits(c.draft[:, :GAMMA])
+    dfull = synth.host_logits(c.draft)
+    d_all = np.ascontiguousarray(dfull[:, :GAMMA])
     tk = c.tokens.cpu().numpy()
     u = c.uniforms.cpu().numpy()
+    F = np.array(oracle.fanout_schedule(FAN["K"], FAN["budget"], FAN["a"],
+                                        FAN["r"]), np.int32)
     del c
 
     def step(i):
         b = i % B
         oracle.verify_linear(t_all[b:b + 1], d_all[b:b + 1], tk[b:b + 1],
                              u[b:b + 1], T)
+        oracle.fanout_topk(dfull[b:b + 1], F)
 
     for i in range(args.warmup):
         step(i)
@@ -411,8 +453,8 @@ def reference_arm(args):
     value = 1.0 / (per_seq * B)
     cores = 1
     sample = ("fp64 C oracle, single thread; each step verifies one of the "
-              "%d sequences of a round; rounds/s = 1 / (B x mean time per "
-              "sequence)" % B)
+              "%d sequences of a round and takes its fan-out; rounds/s = "
+              "1 / (B x mean time per sequence)" % B)
     return {"metric": METRIC, "value": value, "unit": "rounds/s",
             "impl": "reference", "n_gpus": 1, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": per_seq * 1e3,

@@ -148,7 +148,7 @@ __device__ __forceinline__ void ms_add(MS &st, const Raw<DT, VW> &r,
 #pragma unroll
   for (int e = 0; e < VW; ++e) z[e] = elt<DT, VW>(r, e);
   const float vmax = vmax_of<VW>(z);
-  if (vmax > st.m) {  // rare once the row's large values have been seen
+  if (__builtin_expect(vmax > st.m, 0)) {  // rare once the large values are in
     st.s *= ex2((st.m - vmax) * k2);
     st.m = vmax;
   }

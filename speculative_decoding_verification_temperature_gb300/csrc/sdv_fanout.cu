@@ -3,12 +3,14 @@
 // is filled with the top-F_k tokens of the draft logits at each lookahead
 // position k; F follows the geometric fan-out of Theorem 12).
 //
-// One cluster (often a single CTA) owns one row at a time; rows all have
+// One cluster (usually a single CTA) owns one row at a time; rows all have
 // the same cost, so clusters take them round-robin.  Each CTA streams its
-// slice once, keeping a per-thread top-4 list, selects the slice's exact
-// top-F (sdv_topf.cuh), and for clusters of several CTAs rank 0 merges the
-// slice lists read through distributed shared memory.
+// slice once through the TMA ring (16-byte aligned rows) or with 16-byte
+// loads, keeping a per-thread top-4 list, selects the slice's exact top-F
+// (sdv_topf.cuh), and for clusters of several CTAs rank 0 merges the slice
+// lists read through distributed shared memory.
 #include "sdv_host.cuh"
+#include "sdv_ring.cuh"
 #include "sdv_topf.cuh"
 
 namespace sdv {
@@ -22,6 +24,7 @@ struct FanParams {
   float *out_logit;
   int32_t *dev_status;
   int nclusters;
+  int seg_bytes;
 };
 
 struct FanSmem {
@@ -49,6 +52,33 @@ __device__ __forceinline__ void topr_pass(const char *row, const Slice &sl,
   }
 }
 
+// Through the TMA ring: thread t takes vectors t, t + 256, ... of every
+// chunk (increasing index order within the thread).
+template <int DT, int VW>
+__device__ __forceinline__ void topr_pass_ring(Ring &rg, const char *row,
+                                               const Slice &sl, TopR &t) {
+  ring_pass(rg, row, nullptr, sl, [&](const uint4 *A, const uint4 *, int v0,
+                                      int n) {
+    for (int i = threadIdx.x; i < n; i += kThreads)
+      topr_add_vec<DT, VW>(t, sget<DT, VW>(A, i), (v0 + i) * VW);
+  });
+}
+
+template <int DT, int VW>
+__device__ void topf_rescan_ring(const char *row, const Slice &sl,
+                                 uint64_t *loc, int F) {
+  for (int r = 0; r < F; ++r) loc[r] = 0;
+  for (int v0 = sl.vbeg; v0 < sl.vend; v0 += kStg)
+    for (int v = v0 + (int)threadIdx.x; v < min(sl.vend, v0 + kStg);
+         v += kThreads) {
+      const Raw<DT, VW> x = load_vec<DT, VW>(row, v);
+      for (int e = 0; e < VW; ++e) {
+        const float z = elt<DT, VW>(x, e);
+        if (z == z) local_insert(loc, F, make_key(ord32(z), v * VW + e));
+      }
+    }
+}
+
 // The same traversal, rebuilding a full descending top-F list (rescans).
 template <int DT, int VW>
 __device__ void topf_rescan(const char *row, const Slice &sl, uint64_t *loc,
@@ -69,8 +99,8 @@ __device__ void topf_rescan(const char *row, const Slice &sl, uint64_t *loc,
 }
 
 // Select the exact top-F of a row over a cluster and (rank 0) write it.
-template <int DT, int VW>
-__device__ void row_topf(cg::cluster_group &cluster, FanSmem &sh,
+template <int DT, int VW, bool RING>
+__device__ void row_topf(cg::cluster_group &cluster, FanSmem &sh, Ring &rg,
                          const char *row, const Slice &sl, int F,
                          int32_t *otok, float *olog, int32_t *dev_status,
                          int &par) {
@@ -78,10 +108,12 @@ __device__ void row_topf(cg::cluster_group &cluster, FanSmem &sh,
   const int rank = (int)cluster.block_rank(), CL = (int)cluster.num_blocks();
   TopR t;
   topr_init(t);
-  topr_pass<DT, VW>(row, sl, t);
+  if constexpr (RING) topr_pass_ring<DT, VW>(rg, row, sl, t);
+  else topr_pass<DT, VW>(row, sl, t);
   const int anynan = __syncthreads_or(t.nan);
   const int nout = cta_topf(t, F, sh.top, [&](uint64_t *loc, int f) {
-    topf_rescan<DT, VW>(row, sl, loc, f);
+    if constexpr (RING) topf_rescan_ring<DT, VW>(row, sl, loc, f);
+    else topf_rescan<DT, VW>(row, sl, loc, f);
   });
   if (CL == 1) {
     for (int i = tid; i < F; i += kThreads) {
@@ -126,9 +158,18 @@ __device__ void row_topf(cg::cluster_group &cluster, FanSmem &sh,
   __syncthreads();
 }
 
-template <int DT, int VW>
-__global__ void __launch_bounds__(kThreads, 2) fanout_kernel(const FanParams p) {
+template <int DT, int VW, bool RING>
+__global__ void __launch_bounds__(kThreads, RING ? 3 : 2)
+    fanout_kernel(const FanParams p) {
+  extern __shared__ __align__(128) unsigned char dsm[];
   __shared__ FanSmem sh;
+  __shared__ uint64_t bars[2 * kStages];
+  Ring rg;
+  rg.buf = reinterpret_cast<uint4 *>(dsm + p.seg_bytes);
+  rg.full = bars;
+  rg.empty = bars + kStages;
+  rg.dev_status = p.dev_status;
+  if (RING) ring_init(rg);
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank(), CL = (int)cluster.num_blocks();
   const int V = p.V, K1 = p.K + 1;
@@ -145,8 +186,8 @@ __global__ void __launch_bounds__(kThreads, 2) fanout_kernel(const FanParams p) 
     int32_t *otok = p.out_tokens + (size_t)b * total + p.off[k];
     float *olog = p.out_logit ? p.out_logit + (size_t)b * total + p.off[k]
                               : nullptr;
-    row_topf<DT, VW>(cluster, sh, base + (size_t)r * rowb, sl, F, otok, olog,
-                     p.dev_status, par);
+    row_topf<DT, VW, RING>(cluster, sh, rg, base + (size_t)r * rowb, sl, F,
+                           otok, olog, p.dev_status, par);
   }
   cluster.sync();
 }
@@ -154,8 +195,8 @@ __global__ void __launch_bounds__(kThreads, 2) fanout_kernel(const FanParams p) 
 using FanKernel = void (*)(const FanParams);
 
 static FanKernel pick_fanout(int dt, bool vec) {
-  if (dt == SD_F32) return vec ? fanout_kernel<0, 4> : fanout_kernel<0, 1>;
-  return vec ? fanout_kernel<1, 8> : fanout_kernel<1, 1>;
+  if (dt == SD_F32) return vec ? fanout_kernel<0, 4, true> : fanout_kernel<0, 1, false>;
+  return vec ? fanout_kernel<1, 8, true> : fanout_kernel<1, 1, false>;
 }
 
 }  // namespace sdv
@@ -211,8 +252,9 @@ extern "C" sd_status sd_fanout_topk(const void *draft_logits, sd_dtype dt,
     CL = forced;
   else
     while (CL < 16 && rows * CL < 4LL * sms && nvec / (2 * CL) >= 512) CL *= 2;
+  const size_t smem = vec ? 128 + (size_t)kRingBytes : 0;
   int maxc = 0;
-  st = max_active_clusters((const void *)kern, CL, 0, &maxc);
+  st = max_active_clusters((const void *)kern, CL, smem, &maxc);
   if (st != SD_OK) return st;
   const long long want = (rows + 0) < (long long)maxc ? rows : maxc;
   prm.draft = draft_logits;
@@ -223,7 +265,8 @@ extern "C" sd_status sd_fanout_topk(const void *draft_logits, sd_dtype dt,
   prm.out_logit = out_logit;
   prm.dev_status = dev_status;
   prm.nclusters = (int)want;
+  prm.seg_bytes = 128;
   void *args[] = {&prm};
-  return launch_clusters((const void *)kern, (int)want, CL, 0,
+  return launch_clusters((const void *)kern, (int)want, CL, smem,
                          static_cast<cudaStream_t>(stream), args);
 }

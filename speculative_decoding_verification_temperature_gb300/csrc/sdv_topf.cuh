@@ -37,6 +37,7 @@ __device__ __forceinline__ float key_val(uint64_t k) {
 
 struct TopR {
   uint64_t k[kTopR];  // descending; 0 = empty
+  float thr;          // value of k[kTopR - 1] (-inf while not full)
   int nan;
   int dropped;
 };
@@ -44,6 +45,7 @@ struct TopR {
 __device__ __forceinline__ void topr_init(TopR &t) {
 #pragma unroll
   for (int r = 0; r < kTopR; ++r) t.k[r] = 0;
+  t.thr = -__builtin_huge_valf();
   t.nan = 0;
   t.dropped = 0;
 }
@@ -68,13 +70,43 @@ __device__ __forceinline__ void topr_add(TopR &t, float z, int j) {
     t.k[r] = hi;
     x = lo;
   }
+  if (t.k[kTopR - 1] != 0) t.thr = key_val(t.k[kTopR - 1]);
 }
 
+// A vector: once the thread's list is full, one compare of the vector's
+// maximum against the list's kTopR-th value on the fast path (an equal
+// value comes later in index order, so it loses); NaN shows up in a packed
+// sum of the vector (a vector holding both +inf and -inf also gives NaN
+// there and is then checked element by element).
 template <int DT, int VW>
 __device__ __forceinline__ void topr_add_vec(TopR &t, const Raw<DT, VW> &r,
                                              int j0) {
+  float z[VW];
 #pragma unroll
-  for (int e = 0; e < VW; ++e) topr_add(t, elt<DT, VW>(r, e), j0 + e);
+  for (int e = 0; e < VW; ++e) z[e] = elt<DT, VW>(r, e);
+  float chk;
+  if constexpr (VW == 1) {
+    chk = z[0];
+  } else {
+    float2 acc = make_float2(z[0], z[1]);
+#pragma unroll
+    for (int e = 2; e < VW; e += 2) acc = __fadd2_rn(acc, make_float2(z[e], z[e + 1]));
+    chk = acc.x + acc.y;
+  }
+  const float vmax = vmax_of<VW>(z);
+  const bool need = vmax > t.thr || t.k[kTopR - 1] == 0 || chk != chk;
+  // vote so that the rare insertion is a real (warp-uniform) branch rather
+  // than predicated work done for every element
+  if (__builtin_expect(__any_sync(__activemask(), need), 0)) {
+    if (need) {
+#pragma unroll
+      for (int e = 0; e < VW; ++e) topr_add(t, z[e], j0 + e);
+    } else {
+      t.dropped = 1;
+    }
+  } else {
+    t.dropped = 1;
+  }
 }
 
 struct TopSmem {
