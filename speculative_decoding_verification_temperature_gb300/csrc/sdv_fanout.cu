@@ -5,10 +5,11 @@
 //
 // One cluster (usually a single CTA) owns one row at a time; rows all have
 // the same cost, so clusters take them round-robin.  Each CTA streams its
-// slice once through the TMA ring (16-byte aligned rows) or with 16-byte
-// loads, keeping a per-thread top-4 list, selects the slice's exact top-F
-// (sdv_topf.cuh), and for clusters of several CTAs rank 0 merges the slice
-// lists read through distributed shared memory.
+// slice once through the TMA ring (16-byte aligned rows; SDV_FANOUT_LDG=1
+// takes 16-byte loads instead) or with scalar loads, filtering it through
+// per-warp sorted lists against a CTA-wide threshold (sdv_topf.cuh); the
+// warps' lists are ranked together, and for clusters of several CTAs rank 0
+// merges the slice lists read through distributed shared memory.
 #include "sdv_host.cuh"
 #include "sdv_ring.cuh"
 #include "sdv_topf.cuh"
@@ -35,67 +36,66 @@ struct FanSmem {
   int nan_flag;
 };
 
-// Stream one row slice into a per-thread top list.
+constexpr int kUF = 8;  // vectors in flight per thread on the load path
+
+// Stream one row slice through the warp filters with 16-byte loads; warp w
+// takes the blocks of 32 * kUF vectors w, w + kWarps, ...
 template <int DT, int VW>
-__device__ __forceinline__ void topr_pass(const char *row, const Slice &sl,
-                                          TopR &t) {
+__device__ __forceinline__ void filter_pass(const char *row, const Slice &sl,
+                                            WarpFilter &w, uint32_t *cta_th) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int v0 = sl.vbeg + warp * 32 * kU + lane; v0 < sl.vend;
-       v0 += kWarps * 32 * kU) {
-    Raw<DT, VW> x[kU];
+  for (int vb = sl.vbeg + warp * 32 * kUF; vb < sl.vend;
+       vb += kWarps * 32 * kUF) {  // warp-uniform
+    Raw<DT, VW> x[kUF];
 #pragma unroll
-    for (int u = 0; u < kU; ++u)
-      if (v0 + u * 32 < sl.vend) x[u] = load_vec<DT, VW>(row, v0 + u * 32);
+    for (int u = 0; u < kUF; ++u) {
+      const int v = vb + u * 32 + lane;
+      if (v < sl.vend) x[u] = load_vec<DT, VW>(row, v);
+    }
+    wf_sync(w, cta_th);
 #pragma unroll
-    for (int u = 0; u < kU; ++u)
-      if (v0 + u * 32 < sl.vend) topr_add_vec<DT, VW>(t, x[u], (v0 + u * 32) * VW);
+    for (int u = 0; u < kUF; ++u) {
+      const int v = vb + u * 32 + lane;
+      wf_offer<DT, VW>(w, cta_th, x[u], v < sl.vend, v * VW);
+    }
   }
 }
 
-// Through the TMA ring: thread t takes vectors t, t + 256, ... of every
-// chunk (increasing index order within the thread).
+// The same through the TMA ring: warp w takes vectors 32 w .. 32 w + 31,
+// 32 (w + kWarps) .., ... of every chunk.
 template <int DT, int VW>
-__device__ __forceinline__ void topr_pass_ring(Ring &rg, const char *row,
-                                               const Slice &sl, TopR &t) {
+__device__ __forceinline__ void filter_pass_ring(Ring &rg, const char *row,
+                                                 const Slice &sl,
+                                                 WarpFilter &w,
+                                                 uint32_t *cta_th) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   ring_pass(rg, row, nullptr, sl, [&](const uint4 *A, const uint4 *, int v0,
                                       int n) {
-    for (int i = threadIdx.x; i < n; i += kThreads)
-      topr_add_vec<DT, VW>(t, sget<DT, VW>(A, i), (v0 + i) * VW);
+    wf_sync(w, cta_th);
+    for (int base = warp * 32; base < n; base += kThreads) {  // warp-uniform
+      const int i = base + lane;
+      Raw<DT, VW> r{};
+      if (i < n) r = sget<DT, VW>(A, i);
+      wf_offer<DT, VW>(w, cta_th, r, i < n, (v0 + i) * VW);
+    }
   });
 }
 
+// A lane's running sum turns NaN for a NaN element, but also for +inf and
+// -inf together: confirm by looking at the elements.  Block-wide.
 template <int DT, int VW>
-__device__ void topf_rescan_ring(const char *row, const Slice &sl,
-                                 uint64_t *loc, int F) {
-  for (int r = 0; r < F; ++r) loc[r] = 0;
-  for (int v0 = sl.vbeg; v0 < sl.vend; v0 += kStg)
-    for (int v = v0 + (int)threadIdx.x; v < min(sl.vend, v0 + kStg);
-         v += kThreads) {
-      const Raw<DT, VW> x = load_vec<DT, VW>(row, v);
-      for (int e = 0; e < VW; ++e) {
-        const float z = elt<DT, VW>(x, e);
-        if (z == z) local_insert(loc, F, make_key(ord32(z), v * VW + e));
-      }
+__device__ int slice_has_nan(const char *row, const Slice &sl, bool maybe) {
+  if (!__syncthreads_or(maybe)) return 0;
+  bool f = false;
+  for (int v = sl.vbeg + (int)threadIdx.x; v < sl.vend; v += kThreads) {
+    const Raw<DT, VW> x = load_vec<DT, VW>(row, v);
+#pragma unroll
+    for (int e = 0; e < VW; ++e) {
+      const float z = elt<DT, VW>(x, e);
+      f |= z != z;
     }
-}
-
-// The same traversal, rebuilding a full descending top-F list (rescans).
-template <int DT, int VW>
-__device__ void topf_rescan(const char *row, const Slice &sl, uint64_t *loc,
-                            int F) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int r = 0; r < F; ++r) loc[r] = 0;
-  for (int v0 = sl.vbeg + warp * 32 * kU + lane; v0 < sl.vend;
-       v0 += kWarps * 32 * kU)
-    for (int u = 0; u < kU; ++u)
-      if (v0 + u * 32 < sl.vend) {
-        const Raw<DT, VW> x = load_vec<DT, VW>(row, v0 + u * 32);
-        for (int e = 0; e < VW; ++e) {
-          const float z = elt<DT, VW>(x, e);
-          if (z == z) local_insert(loc, F, make_key(ord32(z),
-                                                     (v0 + u * 32) * VW + e));
-        }
-      }
+  }
+  return __syncthreads_or(f);
 }
 
 // Select the exact top-F of a row over a cluster and (rank 0) write it.
@@ -106,15 +106,16 @@ __device__ void row_topf(cg::cluster_group &cluster, FanSmem &sh, Ring &rg,
                          int &par) {
   const int tid = threadIdx.x;
   const int rank = (int)cluster.block_rank(), CL = (int)cluster.num_blocks();
-  TopR t;
-  topr_init(t);
-  if constexpr (RING) topr_pass_ring<DT, VW>(rg, row, sl, t);
-  else topr_pass<DT, VW>(row, sl, t);
-  const int anynan = __syncthreads_or(t.nan);
-  const int nout = cta_topf(t, F, sh.top, [&](uint64_t *loc, int f) {
-    if constexpr (RING) topf_rescan_ring<DT, VW>(row, sl, loc, f);
-    else topf_rescan<DT, VW>(row, sl, loc, f);
-  });
+  WarpFilter w;
+  wf_init(w, F);
+  if constexpr (RING) filter_pass_ring<DT, VW>(rg, row, sl, w, &sh.top.th);
+  else filter_pass<DT, VW>(row, sl, w, &sh.top.th);
+  const int anynan = slice_has_nan<DT, VW>(
+      row, sl, w.nacc.x != w.nacc.x || w.nacc.y != w.nacc.y);
+  wf_export(w, sh.top);
+  __syncthreads();
+  const int nout = rank_select(sh.top, kWarps * F, F);
+  if (tid == 0) sh.top.th = 0;  // every warp has finished filtering
   if (CL == 1) {
     for (int i = tid; i < F; i += kThreads) {
       const bool ok = !anynan && i < nout;
@@ -133,14 +134,14 @@ __device__ void row_topf(cg::cluster_group &cluster, FanSmem &sh, Ring &rg,
   }
   cluster.sync();
   if (rank == 0) {
-    // gather the CL lists and rank them (keys unique, 0 = empty)
+    // gather the CL lists (CL * F <= kWarps * SD_MAX_FANOUT) and rank them
     int C = 0;
     if (tid == 0) sh.nan_flag = 0;
     __syncthreads();
     for (int r = 0; r < CL; ++r) {
       const FanSmem *rs = cluster.map_shared_rank(&sh, r);
       const int nr = rs->slot_n[par];
-      for (int i = tid; i < nr; i += kThreads) sh.top.list[C + i] = rs->slot[par][i];
+      for (int i = tid; i < nr; i += kThreads) sh.top.flat[C + i] = rs->slot[par][i];
       if (tid == 0 && rs->slot_nan[par]) sh.nan_flag = 1;
       C += nr;
     }
@@ -158,8 +159,12 @@ __device__ void row_topf(cg::cluster_group &cluster, FanSmem &sh, Ring &rg,
   __syncthreads();
 }
 
+#ifndef SDV_FAN_MINB
+#define SDV_FAN_MINB 4
+#endif
+
 template <int DT, int VW, bool RING>
-__global__ void __launch_bounds__(kThreads, RING ? 3 : 2)
+__global__ void __launch_bounds__(kThreads, SDV_FAN_MINB)
     fanout_kernel(const FanParams p) {
   extern __shared__ __align__(128) unsigned char dsm[];
   __shared__ FanSmem sh;
@@ -169,7 +174,9 @@ __global__ void __launch_bounds__(kThreads, RING ? 3 : 2)
   rg.full = bars;
   rg.empty = bars + kStages;
   rg.dev_status = p.dev_status;
-  if (RING) ring_init(rg);
+  if (threadIdx.x == 0) sh.top.th = 0;
+  if (RING) ring_init(rg, 1);
+  else __syncthreads();
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank(), CL = (int)cluster.num_blocks();
   const int V = p.V, K1 = p.K + 1;
@@ -194,9 +201,13 @@ __global__ void __launch_bounds__(kThreads, RING ? 3 : 2)
 
 using FanKernel = void (*)(const FanParams);
 
-static FanKernel pick_fanout(int dt, bool vec) {
-  if (dt == SD_F32) return vec ? fanout_kernel<0, 4, true> : fanout_kernel<0, 1, false>;
-  return vec ? fanout_kernel<1, 8, true> : fanout_kernel<1, 1, false>;
+static FanKernel pick_fanout(int dt, bool vec, bool ring) {
+  if (dt == SD_F32) {
+    if (!vec) return fanout_kernel<0, 1, false>;
+    return ring ? fanout_kernel<0, 4, true> : fanout_kernel<0, 4, false>;
+  }
+  if (!vec) return fanout_kernel<1, 1, false>;
+  return ring ? fanout_kernel<1, 8, true> : fanout_kernel<1, 8, false>;
 }
 
 }  // namespace sdv
@@ -223,7 +234,7 @@ extern "C" sd_status sd_fanout_topk(const void *draft_logits, sd_dtype dt,
   SDV_REQUIRE(V >= 1 && V <= SD_MAX_V, "V=%d outside [1, %d]", V, SD_MAX_V);
   SDV_REQUIRE(F != nullptr, "F is null");
   FanParams prm;
-  int total = 0;
+  int total = 0, maxF = 0;
   for (int k = 0; k <= K; ++k) {
     SDV_REQUIRE(F[k] >= 0, "F[%d] < 0", k);
     if (F[k] > SD_MAX_FANOUT || F[k] > V)
@@ -232,6 +243,7 @@ extern "C" sd_status sd_fanout_topk(const void *draft_logits, sd_dtype dt,
     prm.F[k] = F[k];
     prm.off[k] = total;
     total += F[k];
+    maxF = F[k] > maxF ? F[k] : maxF;
   }
   prm.off[K + 1] = total;
   if (B == 0 || total == 0) return SD_OK;
@@ -242,7 +254,8 @@ extern "C" sd_status sd_fanout_topk(const void *draft_logits, sd_dtype dt,
   const int eb = dt == SD_F32 ? 4 : 2, vw = dt == SD_F32 ? 4 : 8;
   const bool vec = aligned16(draft_logits) && ((size_t)V * eb) % 16 == 0;
   const long long nvec = V / (vec ? vw : 1);
-  FanKernel kern = pick_fanout(dt, vec);
+  const bool ring = vec && env_int("SDV_FANOUT_LDG", 0) == 0;
+  FanKernel kern = pick_fanout(dt, vec, ring);
   // rows of equal cost: a single CTA per row unless the rows are too few to
   // fill the GPU, then clusters that split each row
   const long long rows = (long long)B * (K + 1);
@@ -252,7 +265,9 @@ extern "C" sd_status sd_fanout_topk(const void *draft_logits, sd_dtype dt,
     CL = forced;
   else
     while (CL < 16 && rows * CL < 4LL * sms && nvec / (2 * CL) >= 512) CL *= 2;
-  const size_t smem = vec ? 128 + (size_t)kRingBytes : 0;
+  // rank 0 gathers the CL lists into kWarps * SD_MAX_FANOUT keys
+  while (CL > 1 && CL * maxF > kWarps * SD_MAX_FANOUT) CL /= 2;
+  const size_t smem = ring ? 128 + (size_t)kRingBytes1 : 0;
   int maxc = 0;
   st = max_active_clusters((const void *)kern, CL, smem, &maxc);
   if (st != SD_OK) return st;

@@ -28,10 +28,12 @@ namespace sdv {
 #endif
 constexpr int kStg = SDV_STG;         // 16-byte vectors per row per stage
 constexpr int kStages = SDV_STAGES;   // stages in flight
-constexpr int kRingBytes = kStages * 2 * kStg * 16;  // 48 KB
+constexpr int kRingBytes = kStages * 2 * kStg * 16;  // 48 KB, two rows
+constexpr int kRingBytes1 = kStages * kStg * 16;     // 24 KB, one row
 
 struct Ring {
-  uint4 *buf;          // [kStages][2][kStg]
+  uint4 *buf;          // [kStages][nrow][kStg]
+  int nrow;            // rows a stage holds (1 or 2), fixed per kernel
   uint64_t *full;      // [kStages] mbarriers: data landed (tx bytes)
   uint64_t *empty;     // [kStages] mbarriers: every warp is done with it
   uint32_t phase;      // bit s: parity of stage s's next "full" completion
@@ -40,7 +42,8 @@ struct Ring {
   int32_t *dev_status;
 };
 
-__device__ __forceinline__ void ring_init(Ring &rg) {
+__device__ __forceinline__ void ring_init(Ring &rg, int nrow = 2) {
+  rg.nrow = nrow;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&rg.full[s], 1);
@@ -57,7 +60,8 @@ __device__ __forceinline__ void ring_init(Ring &rg) {
 // One pass over this CTA's slice of row A (and row B when non-null).
 // f(a, b, v0, n) is called by every thread for each chunk: a / b point at
 // the chunk's n vectors in shared memory, v0 is the absolute index of the
-// chunk's first vector.  Block-uniform control flow is required.
+// chunk's first vector.  Block-uniform control flow is required; a ring
+// initialised for one row per stage takes no row B.
 template <class F>
 __device__ __forceinline__ void ring_pass(Ring &rg, const char *rowA,
                                           const char *rowB, const Slice &sl,
@@ -76,10 +80,10 @@ __device__ __forceinline__ void ring_pass(Ring &rg, const char *rowA,
     rg.used |= 1u << s;
     fence_proxy_async();
     mbar_expect_tx(&rg.full[s], bytes * (rowB ? 2u : 1u));
-    bulk_g2s(rg.buf + (size_t)(2 * s) * kStg,
+    bulk_g2s(rg.buf + (size_t)(rg.nrow * s) * kStg,
              rowA + (size_t)(sl.vbeg + v0) * 16, bytes, &rg.full[s]);
     if (rowB)
-      bulk_g2s(rg.buf + (size_t)(2 * s + 1) * kStg,
+      bulk_g2s(rg.buf + (size_t)(rg.nrow * s + 1) * kStg,
                rowB + (size_t)(sl.vbeg + v0) * 16, bytes, &rg.full[s]);
   };
   if (threadIdx.x == 0)
@@ -88,7 +92,8 @@ __device__ __forceinline__ void ring_pass(Ring &rg, const char *rowA,
     const int s = c % kStages;
     mbar_wait(&rg.full[s], (rg.phase >> s) & 1u, rg.dev_status);
     rg.phase ^= 1u << s;
-    f(rg.buf + (size_t)(2 * s) * kStg, rg.buf + (size_t)(2 * s + 1) * kStg,
+    f(rg.buf + (size_t)(rg.nrow * s) * kStg,
+      rg.buf + (size_t)(rg.nrow * s + rg.nrow - 1) * kStg,
       sl.vbeg + c * kStg, min(kStg, nv - c * kStg));
 #if SDV_RING_SYNC
     __syncthreads();

@@ -1,24 +1,28 @@
 // sdv_topf.cuh -- exact top-F selection of (logit, token id) pairs over a
 // row slice, ordered by logit descending then id ascending (-0 == +0).
 //
-// Streaming keeps a sorted top-kTopR list per thread (64-bit keys, one
-// compare per element on the fast path).  The CTA then takes the F-th best
-// of the per-thread maxima as a threshold, gathers the kept keys above it,
-// ranks them by counting, and checks that no thread could have dropped a
-// key that belongs in the result (a thread whose kTopR kept keys all reach
-// the F-th result and that dropped something).  In that rare case the
-// suspect threads rescan their own elements for a full top-F list and the
-// selection is repeated over the union, which is exact.
+// Each warp keeps a sorted list of its best keys in registers (lane l holds
+// entries l and 32 + l) and filters its elements against one CTA-wide
+// threshold: the largest, over the warps, of each warp's F-th best value so
+// far.  An element below it has F strictly better elements in that warp's
+// list, which only ever improves, so it cannot be in the answer; elements at
+// or above it (ties included, since another warp's equal value may carry a
+// smaller token id) are inserted.  On the fast path a vector costs one
+// compare of its maximum against the threshold and a warp vote.  The warps'
+// lists are ranked together at the end.
+//
+// Before its first vector is filtered, a warp seeds its threshold with a
+// value that at least F of its first elements reach (the F-th largest of
+// the lanes' vector maxima, for F <= 32), so that the first round inserts
+// about F keys instead of all of them.
 #pragma once
 
 #include "sdv_device.cuh"
 
 namespace sdv {
 
-constexpr int kTopR = 4;
-constexpr int kTopCap = 2048;  // candidate list capacity (keys)
-
 // Order-preserving map of a non-NaN float to uint32 (-0 mapped like +0).
+// Every non-NaN float maps above 0, which marks an empty key.
 __device__ __forceinline__ uint32_t ord32(float f) {
   const uint32_t u = __float_as_uint(f == 0.f ? 0.f : f);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
@@ -35,166 +39,160 @@ __device__ __forceinline__ float key_val(uint64_t k) {
   return unord32((uint32_t)(k >> 32));
 }
 
-struct TopR {
-  uint64_t k[kTopR];  // descending; 0 = empty
-  float thr;          // value of k[kTopR - 1] (-inf while not full)
+struct TopSmem {
+  uint64_t flat[kWarps * SD_MAX_FANOUT];  // warps' lists / gathered lists
+  uint64_t out[SD_MAX_FANOUT];            // result, descending
+  uint32_t th;                            // ord32 of the CTA threshold, 0 = none
   int nan;
-  int dropped;
 };
 
-__device__ __forceinline__ void topr_init(TopR &t) {
-#pragma unroll
-  for (int r = 0; r < kTopR; ++r) t.k[r] = 0;
-  t.thr = -__builtin_huge_valf();
-  t.nan = 0;
-  t.dropped = 0;
+// Per-thread view of its warp's filter.  All fields but nacc are
+// warp-uniform.
+struct WarpFilter {
+  uint64_t a, b;  // list entries lane and 32 + lane (descending, 0 = empty)
+  float th;       // filter threshold
+  float2 nacc;    // running sum of the lane's elements: NaN if one was NaN
+  int F;
+  bool two;       // list of 64 (F > 32)
+  bool seeded;
+};
+
+__device__ __forceinline__ void wf_init(WarpFilter &w, int F) {
+  w.a = 0;
+  w.b = 0;
+  w.th = -__builtin_huge_valf();
+  w.nacc = make_float2(0.f, 0.f);
+  w.F = F;
+  w.two = F > 32;
+  w.seeded = false;
 }
 
-// Elements must be offered in increasing index order within a thread.
-__device__ __forceinline__ void topr_add(TopR &t, float z, int j) {
-  if (z != z) {
-    t.nan = 1;
-    return;
-  }
-  const uint32_t o = ord32(z);
-  if (o <= (uint32_t)(t.k[kTopR - 1] >> 32)) {
-    t.dropped |= (t.k[kTopR - 1] != 0);
-    return;
-  }
-  t.dropped |= (t.k[kTopR - 1] != 0);
-  uint64_t x = make_key(o, (uint32_t)j);
-#pragma unroll
-  for (int r = 0; r < kTopR; ++r) {
-    const uint64_t hi = t.k[r] > x ? t.k[r] : x;
-    const uint64_t lo = t.k[r] > x ? x : t.k[r];
-    t.k[r] = hi;
-    x = lo;
-  }
-  if (t.k[kTopR - 1] != 0) t.thr = key_val(t.k[kTopR - 1]);
+__device__ __forceinline__ uint64_t shfl64(uint64_t v, int src) {
+  const uint32_t lo = __shfl_sync(0xffffffffu, (uint32_t)v, src);
+  const uint32_t hi = __shfl_sync(0xffffffffu, (uint32_t)(v >> 32), src);
+  return ((uint64_t)hi << 32) | lo;
+}
+__device__ __forceinline__ uint64_t shfl_up64(uint64_t v) {
+  const uint32_t lo = __shfl_up_sync(0xffffffffu, (uint32_t)v, 1);
+  const uint32_t hi = __shfl_up_sync(0xffffffffu, (uint32_t)(v >> 32), 1);
+  return ((uint64_t)hi << 32) | lo;
 }
 
-// A vector: once the thread's list is full, one compare of the vector's
-// maximum against the list's kTopR-th value on the fast path (an equal
-// value comes later in index order, so it loses); NaN shows up in a packed
-// sum of the vector (a vector holding both +inf and -inf also gives NaN
-// there and is then checked element by element).
+// Insert key x (the same in every lane) into the warp's sorted list; the
+// last entry falls off.  Full warp.
+__device__ __forceinline__ void wf_insert(WarpFilter &w, uint64_t x) {
+  const int lane = threadIdx.x & 31;
+  int p = __popc(__ballot_sync(0xffffffffu, w.a > x));
+  if (w.two) {
+    p += __popc(__ballot_sync(0xffffffffu, w.b > x));
+    const uint64_t a31 = shfl64(w.a, 31);
+    const uint64_t bu = shfl_up64(w.b);
+    const int pb = 32 + lane;
+    w.b = pb < p ? w.b : (pb == p ? x : (lane == 0 ? a31 : bu));
+  }
+  const uint64_t au = shfl_up64(w.a);
+  w.a = lane < p ? w.a : (lane == p ? x : au);
+}
+
+// Raise the threshold to the F-th entry once the list holds F keys, and
+// publish it to the CTA.  Full warp.
+__device__ __forceinline__ void wf_raise(WarpFilter &w, uint32_t *cta_th) {
+  const int f = w.F - 1;
+  const uint64_t kf = f < 32 ? shfl64(w.a, f) : shfl64(w.b, f - 32);
+  if (kf != 0) {
+    const float v = key_val(kf);
+    if (v > w.th) {
+      w.th = v;
+      if ((threadIdx.x & 31) == 0) atomicMax(cta_th, ord32(v));
+    }
+  }
+}
+
+// Pick up a higher threshold published by another warp (stale is fine: the
+// published value only grows).
+__device__ __forceinline__ void wf_sync(WarpFilter &w, const uint32_t *cta_th) {
+  const uint32_t o = *(const volatile uint32_t *)cta_th;
+  if (o != 0) w.th = fmaxf(w.th, unord32(o));
+}
+
+// Seed the threshold from the lanes' vector maxima m (-inf for idle lanes):
+// the largest m that at least F lanes reach.  Full warp.
+__device__ __forceinline__ void wf_seed(WarpFilter &w, float m) {
+  w.seeded = true;
+  if (w.two) return;
+  int c = 0;
+#pragma unroll 8
+  for (int j = 0; j < 32; ++j) c += __shfl_sync(0xffffffffu, m, j) >= m;
+  float s = c >= w.F ? m : -__builtin_huge_valf();
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+    s = fmaxf(s, __shfl_xor_sync(0xffffffffu, s, o));
+  w.th = fmaxf(w.th, s);
+}
+
+// Offer one vector per lane (ok = false for idle lanes); j0 is the token id
+// of the vector's first element.  Full, converged warp.
 template <int DT, int VW>
-__device__ __forceinline__ void topr_add_vec(TopR &t, const Raw<DT, VW> &r,
-                                             int j0) {
+__device__ __forceinline__ void wf_offer(WarpFilter &w, uint32_t *cta_th,
+                                         const Raw<DT, VW> &r, bool ok,
+                                         int j0) {
   float z[VW];
 #pragma unroll
-  for (int e = 0; e < VW; ++e) z[e] = elt<DT, VW>(r, e);
-  float chk;
-  if constexpr (VW == 1) {
-    chk = z[0];
-  } else {
-    float2 acc = make_float2(z[0], z[1]);
+  for (int e = 0; e < VW; ++e)
+    z[e] = ok ? elt<DT, VW>(r, e) : -__builtin_huge_valf();
+  if (ok) {
+    if constexpr (VW == 1) {
+      w.nacc.x += z[0];
+    } else {
 #pragma unroll
-    for (int e = 2; e < VW; e += 2) acc = __fadd2_rn(acc, make_float2(z[e], z[e + 1]));
-    chk = acc.x + acc.y;
+      for (int e = 0; e < VW; e += 2)
+        w.nacc = __fadd2_rn(w.nacc, make_float2(z[e], z[e + 1]));
+    }
   }
   const float vmax = vmax_of<VW>(z);
-  const bool need = vmax > t.thr || t.k[kTopR - 1] == 0 || chk != chk;
-  // vote so that the rare insertion is a real (warp-uniform) branch rather
-  // than predicated work done for every element
-  if (__builtin_expect(__any_sync(__activemask(), need), 0)) {
-    if (need) {
+  if (__builtin_expect(!w.seeded, 0)) wf_seed(w, vmax);
+  if (__builtin_expect(__any_sync(0xffffffffu, vmax >= w.th), 0)) {
 #pragma unroll
-      for (int e = 0; e < VW; ++e) topr_add(t, z[e], j0 + e);
-    } else {
-      t.dropped = 1;
+    for (int e = 0; e < VW; ++e) {
+      const bool take = ok && z[e] >= w.th;
+      unsigned m = __ballot_sync(0xffffffffu, take);
+      if (m == 0) continue;
+      const uint64_t key = make_key(ord32(z[e]), (uint32_t)(j0 + e));
+      while (m) {
+        const int src = __ffs(m) - 1;
+        m &= m - 1;
+        wf_insert(w, shfl64(key, src));
+      }
+      wf_raise(w, cta_th);
     }
-  } else {
-    t.dropped = 1;
   }
 }
 
-struct TopSmem {
-  uint64_t maxk[kThreads];
-  uint64_t list[kTopCap];
-  uint64_t out[SD_MAX_FANOUT];
-  uint64_t theta0;
-  int cnt;
-  int nout;
-};
+// Write the warp's best F keys to s.flat[warp * F ..].
+__device__ __forceinline__ void wf_export(const WarpFilter &w, TopSmem &s) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint64_t *dst = s.flat + warp * w.F;
+  if (lane < w.F) dst[lane] = w.a;
+  if (32 + lane < w.F) dst[32 + lane] = w.b;
+}
 
-// Rank the first C keys of `list` by counting and place the best F in out
-// (descending).  Keys are unique.  Returns min(F, C).  Block-wide.
+// Rank the first C keys of s.flat (0 = empty, skipped) by counting and
+// place the best F in s.out (descending).  Non-empty keys are unique.
+// Returns min(F, non-empty keys); block-wide, every thread gets it.
 __device__ __forceinline__ int rank_select(TopSmem &s, int C, int F) {
-  for (int i = threadIdx.x; i < C; i += kThreads) {
-    const uint64_t me = s.list[i];
-    int rank = 0;
-    for (int j = 0; j < C; ++j) rank += s.list[j] > me;
-    if (rank < F) s.out[rank] = me;
+  int nz = 0;
+  for (int i0 = 0; i0 < C; i0 += kThreads) {
+    const int i = i0 + (int)threadIdx.x;
+    const uint64_t me = i < C ? s.flat[i] : 0;
+    if (me != 0) {
+      int rank = 0;
+      for (int j = 0; j < C; ++j) rank += s.flat[j] > me;
+      if (rank < F) s.out[rank] = me;
+    }
+    nz += __syncthreads_count(me != 0);
   }
   __syncthreads();
-  return C < F ? C : F;
-}
-
-// Exact CTA-level top-F of the elements the threads offered to `mine`.
-// `rescan(loc, F)` must rebuild this thread's own full top-F list (keys,
-// descending, 0-padded) from its elements; it is called only by suspect
-// threads.  Returns the number of keys in s.out; every thread gets it.
-template <typename Rescan>
-__device__ int cta_topf(const TopR &mine, int F, TopSmem &s, Rescan rescan) {
-  const int tid = threadIdx.x;
-  s.maxk[tid] = mine.k[0];
-  if (tid == 0) {
-    s.cnt = 0;
-    s.theta0 = 1;  // fewer than F non-empty threads: take every key
-  }
-  __syncthreads();
-  if (mine.k[0] != 0) {
-    int rank = 0;
-    for (int j = 0; j < kThreads; ++j) rank += s.maxk[j] > mine.k[0];
-    if (rank == F - 1) s.theta0 = mine.k[0];
-  }
-  __syncthreads();
-  const uint64_t th0 = s.theta0;
-#pragma unroll
-  for (int r = 0; r < kTopR; ++r)
-    if (mine.k[r] != 0 && mine.k[r] >= th0) s.list[atomicAdd(&s.cnt, 1)] = mine.k[r];
-  __syncthreads();
-  int nout = rank_select(s, s.cnt, F);
-  const uint64_t th = (nout == F) ? s.out[F - 1] : 1;
-  const bool suspect =
-      mine.dropped && (nout < F || mine.k[kTopR - 1] >= th);
-  if (!__syncthreads_or(suspect)) return nout;
-
-  // ---- rare: rebuild from full per-thread lists of the suspects ----
-  __syncthreads();
-  if (tid == 0) s.cnt = 0;
-  __syncthreads();
-  if (suspect) {
-    uint64_t loc[SD_MAX_FANOUT];
-    rescan(loc, F);
-    for (int r = 0; r < F; ++r)
-      if (loc[r] != 0 && loc[r] >= th) {
-        const int pos = atomicAdd(&s.cnt, 1);
-        if (pos < kTopCap) s.list[pos] = loc[r];
-      }
-  } else {
-#pragma unroll
-    for (int r = 0; r < kTopR; ++r)
-      if (mine.k[r] != 0 && mine.k[r] >= th) {
-        const int pos = atomicAdd(&s.cnt, 1);
-        if (pos < kTopCap) s.list[pos] = mine.k[r];
-      }
-  }
-  __syncthreads();
-  const int C = s.cnt < kTopCap ? s.cnt : kTopCap;
-  return rank_select(s, C, F);
-}
-
-// Insert a key into a descending local list of length F (suspect rescans).
-__device__ __forceinline__ void local_insert(uint64_t *loc, int F, uint64_t x) {
-  if (x <= loc[F - 1]) return;
-  int r = F - 1;
-  while (r > 0 && loc[r - 1] < x) {
-    loc[r] = loc[r - 1];
-    --r;
-  }
-  loc[r] = x;
+  return nz < F ? nz : F;
 }
 
 }  // namespace sdv

@@ -82,3 +82,55 @@ def test_limits_rejected():
         api.fanout_topk(d, [65, 1])
     with pytest.raises(api.SdError):
         api.fanout_topk(torch.randn((2, 2, 10), device="cuda"), [11, 1])
+
+
+def test_infinite_rows():
+    """Masked (-inf) logits, a row holding both +inf and -inf (a running sum
+    turns NaN there without any NaN element: must not be flagged), and a row
+    that is -inf everywhere."""
+    V = 9000
+    g = torch.Generator().manual_seed(7)
+    base = torch.randn((4, V), generator=g)
+    base[0, ::3] = float("-inf")
+    base[1, 17] = float("inf")
+    base[1, 4000] = float("-inf")
+    base[1, 8999] = float("inf")
+    base[2, :] = float("-inf")
+    base[3, 100:8000] = float("-inf")
+    d = base[:, None, :].expand(4, 2, V).contiguous()
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for dtype in (torch.float32, torch.bfloat16):
+        dd = d.to(dtype).cuda()
+        out = api.fanout_topk(dd, [12, 40], want_logit=True, status=st)
+        o = oracle.fanout_topk(synth.host_logits(dd), np.array([12, 40], np.int32))
+        np.testing.assert_array_equal(host(out["tokens"]), o["tokens"])
+        np.testing.assert_array_equal(host(out["logit"]).astype(np.float64),
+                                      o["logit"])
+    assert int(st.item()) == 0
+
+
+@pytest.mark.parametrize("mode", ["ring", "ldg"])
+@pytest.mark.parametrize("cluster", ["1", "2", "16"])
+def test_streaming_variants_and_clusters(monkeypatch, mode, cluster):
+    """Both streaming variants (TMA ring, 16-byte loads) with rows split
+    over clusters of 1, 2 and 16 CTAs (F = 64 caps the cluster at 8)."""
+    monkeypatch.setenv("SDV_FANOUT_LDG", "1" if mode == "ldg" else "0")
+    monkeypatch.setenv("SDV_FANOUT_CLUSTER", cluster)
+    g = torch.Generator().manual_seed(int(cluster))
+    for dtype in (torch.float32, torch.bfloat16):
+        d = (torch.randn((3, 3, 50000), generator=g) * 2).to(dtype)
+        d[0, 1] = torch.arange(50000).to(dtype)  # best keys in the last warp
+        d[1, 2] = torch.randint(-3, 3, (50000,), generator=g).to(dtype)
+        check(d.cuda(), [64, 33, 10])
+
+
+def test_best_keys_in_one_warp():
+    """The top keys all fall in one warp's vectors (every 256th vector
+    block), so that warp's list and threshold decide alone."""
+    V = 65536
+    d = torch.randn((2, 1, V)) - 10
+    idx = torch.arange(V)
+    sel = ((idx // 4) % 256) // 32 == 3
+    d[:, 0, sel] += 20 + torch.rand(int(sel.sum()))
+    check(d.cuda(), [64])
+    check(d.cuda(), [20])
