@@ -121,6 +121,30 @@ sd_status sd_verify_linear(const void *target_logits, const void *draft_logits,
                            void *workspace, size_t ws_bytes, void *stream);
 
 /* ---------------------------------------------------------------------
+ * Linear verify without a caller workspace (no counterpart in the pages:
+ * a deployment convenience for callers that must not allocate).
+ *
+ * Arguments and results as sd_verify_linear, minus workspace / ws_bytes.
+ * The scratch is a file-scope device array of SD_STATIC_WS_BYTES per
+ * device.  A call whose sd_verify_linear_workspace(B, gamma, V, dt)
+ * exceeds it returns SD_ERR_UNSUPPORTED (nothing is launched).  The first
+ * call on a device looks the array's address up (cudaGetSymbolAddress,
+ * with that device current) and caches it: make that first call before
+ * any stream capture.  The call allocates and frees nothing; it clears the
+ * counters that must start at zero with a memset on `stream`.  Calls whose
+ * work overlaps on the GPU (other streams, other host threads) share the
+ * array and race: serialise them.
+ * ------------------------------------------------------------------- */
+#define SD_STATIC_WS_BYTES (1u << 20)
+
+sd_status sd_verify_linear_static(
+    const void *target_logits, const void *draft_logits, sd_dtype dt,
+    const int32_t *draft_tokens, const float *uniforms, int B, int gamma,
+    int V, float T, int32_t *n_accepted, int32_t *out_tokens, float *out_prob,
+    float *out_accept_prob, float *out_resid, int32_t *dev_status,
+    void *stream);
+
+/* ---------------------------------------------------------------------
  * K-candidate verify with verifier self-selection (SpecDiff-2, "core
  * method").
  *

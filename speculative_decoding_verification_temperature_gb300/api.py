@@ -64,6 +64,8 @@ def _declare(L):
         "sd_fanout_schedule": ([I, I, D, D, P], I),
         "sd_fanout_topk_workspace": ([I, I, I, I], Z),
         "sd_fanout_topk": ([P, I, I, I, I, P, P, P, P, P, Z, P], I),
+        "sd_verify_linear_static": ([P, P, I, P, P, I, I, I, F, P, P, P, P,
+                                     P, P, P], I),
         "sd_verify_linear_fanout_workspace": ([I, I, I, I], Z),
         "sd_verify_linear_fanout": ([P, P, I, P, P, I, I, I, F, P, P, P, P,
                                      P, P, P, P, Z, P], I),
@@ -179,6 +181,36 @@ def verify_linear(target, draft, tokens, uniforms, T, *, want_accept=False,
         r["accept"] = acc[:, :gamma]
     if want_resid:
         r["resid"] = res
+    return r
+
+
+def verify_linear_static(target, draft, tokens, uniforms, T, *,
+                         want_accept=False, status=None):
+    """Linear verify with the library's static per-device scratch instead of
+    a workspace (sd_verify_linear_static): same arguments and results as
+    verify_linear.  Calls that overlap on the GPU race on that scratch."""
+    dev = target.device
+    _dev(target, dev, "target")
+    B, G1, V = target.shape
+    gamma = G1 - 1
+    if draft is not None:
+        _dev(draft, dev, "draft", target.dtype)
+        if tuple(draft.shape) != (B, gamma, V):
+            raise ValueError("draft must be [B, gamma, V]")
+    tokens = _dev(tokens, dev, "tokens", torch.int32)
+    uniforms = _dev(uniforms, dev, "uniforms", torch.float32)
+    n = torch.empty(B, dtype=torch.int32, device=dev)
+    toks = torch.empty((B, G1), dtype=torch.int32, device=dev)
+    prob = torch.empty(B, dtype=torch.float32, device=dev)
+    acc = torch.empty((B, max(gamma, 1)), dtype=torch.float32,
+                      device=dev) if want_accept else None
+    _check(lib().sd_verify_linear_static(
+        _p(target), _p(draft), _dt(target), _p(tokens), _p(uniforms), B,
+        gamma, V, float(T), _p(n), _p(toks), _p(prob), _p(acc), None,
+        _p(status), _stream(dev)))
+    r = {"n": n, "tokens": toks, "prob": prob}
+    if want_accept:
+        r["accept"] = acc[:, :gamma]
     return r
 
 
