@@ -123,10 +123,16 @@ def needed_bytes(n, gamma, V, elt):
 
 
 # ---------------------------------------------------------- GPU arm
+def workload_name():
+    if B == 256:
+        return WORKLOAD
+    return WORKLOAD.replace("B=256", "B=%d (profiling case)" % B)
+
+
 def make_sets(nsets, device):
     sets = []
     for s in range(nsets):
-        c = synth.large(s, device=device)
+        c = synth.large(s, device=device, B=B)
         c.draft_v = c.draft[:, :GAMMA].contiguous()
         sets.append(c)
     return sets
@@ -207,7 +213,7 @@ def gpu_arm(args, rank, world):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "B": B, "gamma": GAMMA, "V": V,
+        "config": {"workload": workload_name(), "B": B, "gamma": GAMMA, "V": V,
                    "T": T, "fanout_F": F, "input_sets": len(sets),
                    "step": "sd_verify_linear then sd_fanout_topk",
                    "l2": "inputs %.2f GB per set (> 129 MB L2), %d sets "
@@ -460,7 +466,7 @@ def reference_arm(args):
             "warmup": args.warmup, "ms_per_step": per_seq * 1e3,
             "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "B": B, "gamma": GAMMA,
+            "config": {"workload": workload_name(), "B": B, "gamma": GAMMA,
                        "V": V, "T": T},
             "cpu_baseline": {"value": value, "unit": "rounds/s",
                              "cores": cores, "kind": "oracle",
@@ -476,6 +482,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="native",
                     choices=["native", "reference"])
+    ap.add_argument("--batch", type=int, default=256,
+                    help="sequences per step (smaller only to profile a "
+                         "small case of the same kernels)")
     ap.add_argument("--sets", type=int, default=3,
                     help="input sets rotated between steps")
     ap.add_argument("--e2e-steps", type=int, default=20,
@@ -488,6 +497,8 @@ def main():
                          "(0: skip the CPU baseline)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    global B
+    B = args.batch
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":

@@ -129,6 +129,31 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
   return r;
 }
 
+// NaN-propagating maxima (PTX max.NaN: NaN if any input is NaN).
+__device__ __forceinline__ float max_nan(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ float max3_nan(float a, float b, float c) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// Maximum of a vector that is NaN when any element is NaN.
+template <int VW>
+__device__ __forceinline__ float vmax_nan_of(const float (&z)[VW]) {
+  if constexpr (VW == 1) {
+    return z[0];
+  } else if constexpr (VW == 4) {
+    return max_nan(max3_nan(z[0], z[1], z[2]), z[3]);
+  } else {
+    return max3_nan(max3_nan(z[0], z[1], z[2]), max3_nan(z[3], z[4], z[5]),
+                    max_nan(z[6], z[7]));
+  }
+}
+
 template <int VW>
 __device__ __forceinline__ float vmax_of(const float (&z)[VW]) {
   if constexpr (VW == 1) {

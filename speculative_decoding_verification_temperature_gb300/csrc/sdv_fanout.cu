@@ -61,41 +61,33 @@ __device__ __forceinline__ void filter_pass(const char *row, const Slice &sl,
   }
 }
 
-// The same through the TMA ring: warp w takes vectors 32 w .. 32 w + 31,
-// 32 (w + kWarps) .., ... of every chunk.
+// The same through the TMA ring in chunks of kStageVecs vectors: warp w
+// takes vectors 32 w .. 32 w + 31, 32 (w + kWarps) .., ... of every chunk.
 template <int DT, int VW>
 __device__ __forceinline__ void filter_pass_ring(Ring &rg, const char *row,
                                                  const Slice &sl,
                                                  WarpFilter &w,
                                                  uint32_t *cta_th) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  ring_pass(rg, row, nullptr, sl, [&](const uint4 *A, const uint4 *, int v0,
-                                      int n) {
+  ring_pass<kStageVecs>(rg, row, nullptr, sl, [&](const uint4 *A,
+                                                  const uint4 *, int v0,
+                                                  int n) {
     wf_sync(w, cta_th);
-    for (int base = warp * 32; base < n; base += kThreads) {  // warp-uniform
-      const int i = base + lane;
-      Raw<DT, VW> r{};
-      if (i < n) r = sget<DT, VW>(A, i);
-      wf_offer<DT, VW>(w, cta_th, r, i < n, (v0 + i) * VW);
+    if (n == kStageVecs) {  // full chunk: no idle lanes
+#pragma unroll 2
+      for (int base = warp * 32; base < kStageVecs; base += kThreads) {
+        const int i = base + lane;
+        wf_offer<DT, VW>(w, cta_th, sget<DT, VW>(A, i), true, (v0 + i) * VW);
+      }
+    } else {
+      for (int base = warp * 32; base < n; base += kThreads) {  // warp-uniform
+        const int i = base + lane;
+        Raw<DT, VW> r{};
+        if (i < n) r = sget<DT, VW>(A, i);
+        wf_offer<DT, VW>(w, cta_th, r, i < n, (v0 + i) * VW);
+      }
     }
   });
-}
-
-// A lane's running sum turns NaN for a NaN element, but also for +inf and
-// -inf together: confirm by looking at the elements.  Block-wide.
-template <int DT, int VW>
-__device__ int slice_has_nan(const char *row, const Slice &sl, bool maybe) {
-  if (!__syncthreads_or(maybe)) return 0;
-  bool f = false;
-  for (int v = sl.vbeg + (int)threadIdx.x; v < sl.vend; v += kThreads) {
-    const Raw<DT, VW> x = load_vec<DT, VW>(row, v);
-#pragma unroll
-    for (int e = 0; e < VW; ++e) {
-      const float z = elt<DT, VW>(x, e);
-      f |= z != z;
-    }
-  }
-  return __syncthreads_or(f);
 }
 
 // Select the exact top-F of a row over a cluster and (rank 0) write it.
@@ -110,8 +102,7 @@ __device__ void row_topf(cg::cluster_group &cluster, FanSmem &sh, Ring &rg,
   wf_init(w, F);
   if constexpr (RING) filter_pass_ring<DT, VW>(rg, row, sl, w, &sh.top.th);
   else filter_pass<DT, VW>(row, sl, w, &sh.top.th);
-  const int anynan = slice_has_nan<DT, VW>(
-      row, sl, w.nacc.x != w.nacc.x || w.nacc.y != w.nacc.y);
+  const int anynan = __syncthreads_or(w.nseen != w.nseen);
   wf_export(w, sh.top);
   __syncthreads();
   const int nout = rank_select(sh.top, kWarps * F, F);
@@ -175,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, SDV_FAN_MINB)
   rg.empty = bars + kStages;
   rg.dev_status = p.dev_status;
   if (threadIdx.x == 0) sh.top.th = 0;
-  if (RING) ring_init(rg, 1);
+  if (RING) ring_init(rg);
   else __syncthreads();
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank(), CL = (int)cluster.num_blocks();
@@ -267,11 +258,13 @@ extern "C" sd_status sd_fanout_topk(const void *draft_logits, sd_dtype dt,
     while (CL < 16 && rows * CL < 4LL * sms && nvec / (2 * CL) >= 512) CL *= 2;
   // rank 0 gathers the CL lists into kWarps * SD_MAX_FANOUT keys
   while (CL > 1 && CL * maxF > kWarps * SD_MAX_FANOUT) CL /= 2;
-  const size_t smem = ring ? 128 + (size_t)kRingBytes1 : 0;
+  const size_t smem = ring ? 128 + (size_t)kRingBytes : 0;
   int maxc = 0;
   st = max_active_clusters((const void *)kern, CL, smem, &maxc);
   if (st != SD_OK) return st;
-  const long long want = (rows + 0) < (long long)maxc ? rows : maxc;
+  // rows of equal cost: give every cluster the same number of them
+  const long long per = (rows + maxc - 1) / maxc;
+  const long long want = (rows + per - 1) / per;
   prm.draft = draft_logits;
   prm.B = B;
   prm.K = K;

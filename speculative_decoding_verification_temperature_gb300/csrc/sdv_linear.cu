@@ -135,8 +135,10 @@ __global__ void __launch_bounds__(kThreads, RING ? 4 : 2)
     for (;;) {
       const int jend = min(i + w, gamma + 1);
       const int np = jend - i;
-      if (tid < np) {  // gathers for the accept tests (used after the merge)
-        const int j = i + tid;
+      // gathers for the accept tests (used after the merge), by warp 1:
+      // thread 0 goes straight on to issue the step's copies
+      if (tid >= 32 && tid < 32 + np) {
+        const int j = i + tid - 32;
         int x = -1;
         float zt = 0.f, zd = 0.f, r = 0.f;
         if (j < gamma) {
@@ -147,10 +149,10 @@ __global__ void __launch_bounds__(kThreads, RING ? 4 : 2)
           }
           if (!GREEDY) r = p.uniforms[(size_t)seq * (gamma + 1) + j];
         }
-        sh.gx[tid] = x;
-        sh.gzt[tid] = zt;
-        sh.gzd[tid] = zd;
-        sh.gr[tid] = r;
+        sh.gx[tid - 32] = x;
+        sh.gzt[tid - 32] = zt;
+        sh.gzd[tid - 32] = zd;
+        sh.gr[tid - 32] = r;
       }
       if (RING && last_seq && p.spec >= 2 && tid == 0) {
         // the GPU is emptying out: ask for this step's and the next step's

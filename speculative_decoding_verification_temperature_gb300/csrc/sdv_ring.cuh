@@ -28,12 +28,11 @@ namespace sdv {
 #endif
 constexpr int kStg = SDV_STG;         // 16-byte vectors per row per stage
 constexpr int kStages = SDV_STAGES;   // stages in flight
-constexpr int kRingBytes = kStages * 2 * kStg * 16;  // 48 KB, two rows
-constexpr int kRingBytes1 = kStages * kStg * 16;     // 24 KB, one row
+constexpr int kStageVecs = 2 * kStg;  // a stage: two rows of kStg or one of 2 kStg
+constexpr int kRingBytes = kStages * kStageVecs * 16;  // 48 KB
 
 struct Ring {
-  uint4 *buf;          // [kStages][nrow][kStg]
-  int nrow;            // rows a stage holds (1 or 2), fixed per kernel
+  uint4 *buf;          // [kStages][kStageVecs]
   uint64_t *full;      // [kStages] mbarriers: data landed (tx bytes)
   uint64_t *empty;     // [kStages] mbarriers: every warp is done with it
   uint32_t phase;      // bit s: parity of stage s's next "full" completion
@@ -42,8 +41,7 @@ struct Ring {
   int32_t *dev_status;
 };
 
-__device__ __forceinline__ void ring_init(Ring &rg, int nrow = 2) {
-  rg.nrow = nrow;
+__device__ __forceinline__ void ring_init(Ring &rg) {
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&rg.full[s], 1);
@@ -57,21 +55,22 @@ __device__ __forceinline__ void ring_init(Ring &rg, int nrow = 2) {
   __syncthreads();
 }
 
-// One pass over this CTA's slice of row A (and row B when non-null).
+// One pass over this CTA's slice of row A (and row B when non-null), in
+// chunks of STG vectors: kStg for two rows, up to 2 kStg for row A alone.
 // f(a, b, v0, n) is called by every thread for each chunk: a / b point at
 // the chunk's n vectors in shared memory, v0 is the absolute index of the
-// chunk's first vector.  Block-uniform control flow is required; a ring
-// initialised for one row per stage takes no row B.
-template <class F>
+// chunk's first vector.  Block-uniform control flow is required.
+template <int STG = kStg, class F>
 __device__ __forceinline__ void ring_pass(Ring &rg, const char *rowA,
                                           const char *rowB, const Slice &sl,
                                           F &&f) {
+  static_assert(STG == kStg || STG == kStageVecs, "chunk of one stage");
   const int nv = sl.vend - sl.vbeg;
-  const int nch = (nv + kStg - 1) / kStg;
+  const int nch = (nv + STG - 1) / STG;
   auto issue = [&](int c) {  // thread 0 only
     const int s = c % kStages;
-    const int v0 = c * kStg;
-    const int cnt = min(kStg, nv - v0);
+    const int v0 = c * STG;
+    const int cnt = min(STG, nv - v0);
     const uint32_t bytes = (uint32_t)cnt * 16u;
     if (!SDV_RING_SYNC && (rg.used >> s & 1u)) {  // every warp released it
       mbar_wait(&rg.empty[s], (rg.epar >> s) & 1u, rg.dev_status);
@@ -79,11 +78,11 @@ __device__ __forceinline__ void ring_pass(Ring &rg, const char *rowA,
     }
     rg.used |= 1u << s;
     fence_proxy_async();
-    mbar_expect_tx(&rg.full[s], bytes * (rowB ? 2u : 1u));
-    bulk_g2s(rg.buf + (size_t)(rg.nrow * s) * kStg,
+    mbar_expect_tx(&rg.full[s], bytes * ((STG == kStg && rowB) ? 2u : 1u));
+    bulk_g2s(rg.buf + (size_t)s * kStageVecs,
              rowA + (size_t)(sl.vbeg + v0) * 16, bytes, &rg.full[s]);
-    if (rowB)
-      bulk_g2s(rg.buf + (size_t)(rg.nrow * s + 1) * kStg,
+    if (STG == kStg && rowB)
+      bulk_g2s(rg.buf + (size_t)s * kStageVecs + kStg,
                rowB + (size_t)(sl.vbeg + v0) * 16, bytes, &rg.full[s]);
   };
   if (threadIdx.x == 0)
@@ -92,9 +91,8 @@ __device__ __forceinline__ void ring_pass(Ring &rg, const char *rowA,
     const int s = c % kStages;
     mbar_wait(&rg.full[s], (rg.phase >> s) & 1u, rg.dev_status);
     rg.phase ^= 1u << s;
-    f(rg.buf + (size_t)(rg.nrow * s) * kStg,
-      rg.buf + (size_t)(rg.nrow * s + rg.nrow - 1) * kStg,
-      sl.vbeg + c * kStg, min(kStg, nv - c * kStg));
+    f(rg.buf + (size_t)s * kStageVecs, rg.buf + (size_t)s * kStageVecs + kStg,
+      sl.vbeg + c * STG, min(STG, nv - c * STG));
 #if SDV_RING_SYNC
     __syncthreads();
     if (threadIdx.x == 0 && c + kStages < nch) issue(c + kStages);

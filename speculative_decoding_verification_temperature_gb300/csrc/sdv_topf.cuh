@@ -46,12 +46,12 @@ struct TopSmem {
   int nan;
 };
 
-// Per-thread view of its warp's filter.  All fields but nacc are
+// Per-thread view of its warp's filter.  All fields but nseen are
 // warp-uniform.
 struct WarpFilter {
   uint64_t a, b;  // list entries lane and 32 + lane (descending, 0 = empty)
   float th;       // filter threshold
-  float2 nacc;    // running sum of the lane's elements: NaN if one was NaN
+  float nseen;    // NaN-propagating maximum of the lane's elements
   int F;
   bool two;       // list of 64 (F > 32)
   bool seeded;
@@ -61,7 +61,7 @@ __device__ __forceinline__ void wf_init(WarpFilter &w, int F) {
   w.a = 0;
   w.b = 0;
   w.th = -__builtin_huge_valf();
-  w.nacc = make_float2(0.f, 0.f);
+  w.nseen = -__builtin_huge_valf();
   w.F = F;
   w.two = F > 32;
   w.seeded = false;
@@ -115,8 +115,8 @@ __device__ __forceinline__ void wf_sync(WarpFilter &w, const uint32_t *cta_th) {
   if (o != 0) w.th = fmaxf(w.th, unord32(o));
 }
 
-// Seed the threshold from the lanes' vector maxima m (-inf for idle lanes):
-// the largest m that at least F lanes reach.  Full warp.
+// Seed the threshold from the lanes' vector maxima m (-inf for idle lanes,
+// NaN never counts): the largest m that at least F lanes reach.  Full warp.
 __device__ __forceinline__ void wf_seed(WarpFilter &w, float m) {
   w.seeded = true;
   if (w.two) return;
@@ -140,16 +140,8 @@ __device__ __forceinline__ void wf_offer(WarpFilter &w, uint32_t *cta_th,
 #pragma unroll
   for (int e = 0; e < VW; ++e)
     z[e] = ok ? elt<DT, VW>(r, e) : -__builtin_huge_valf();
-  if (ok) {
-    if constexpr (VW == 1) {
-      w.nacc.x += z[0];
-    } else {
-#pragma unroll
-      for (int e = 0; e < VW; e += 2)
-        w.nacc = __fadd2_rn(w.nacc, make_float2(z[e], z[e + 1]));
-    }
-  }
-  const float vmax = vmax_of<VW>(z);
+  const float vmax = vmax_nan_of<VW>(z);  // NaN: never >= th
+  w.nseen = max_nan(w.nseen, vmax);
   if (__builtin_expect(!w.seeded, 0)) wf_seed(w, vmax);
   if (__builtin_expect(__any_sync(0xffffffffu, vmax >= w.th), 0)) {
 #pragma unroll

@@ -289,7 +289,9 @@ def tree(round_index=0, device="cpu") -> TreeCase:
                      seed=1003 + 97 * round_index, device=device)
 
 
-def large(round_index=0, device="cpu") -> LinearCase:
-    return linear_case(256, 8, 128256, torch.float32, 1.0,
+def large(round_index=0, device="cpu", B=256) -> LinearCase:
+    """The large workload: B=256 sequences (fewer only for profiling runs),
+    gamma=8, V=128256 fp32, T=1, 9 draft rows."""
+    return linear_case(B, 8, 128256, torch.float32, 1.0,
                        seed=1004 + 97 * round_index, sigma_t=3.0,
                        sigma_d=1.0, draft_rows=9, device=device)
