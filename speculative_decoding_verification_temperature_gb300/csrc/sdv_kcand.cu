@@ -1,6 +1,8 @@
 // sdv_kcand.cu -- K-candidate verify with verifier self-selection
 // (SpecDiff-2, "core method": K joint drafts sampled from the drafter's
 // position-wise marginals, all verified, the longest accepted streak kept).
+// Rows that are 16-byte aligned go to the streaming kernel of
+// sdv_kcand_ring.cu; this file's kernel (plain loads) takes the rest.
 //
 // One cluster verifies one sequence b at a time.  Position j is one step:
 // the CTAs stream their slices of the shared draft marginal row (b, j) and
@@ -324,6 +326,15 @@ __global__ void __launch_bounds__(kThreads, 2)
   cluster.sync();
 }
 
+sd_status kcand_ring_launch(const void *target, const void *draft,
+                            sd_dtype dt, const int32_t *tokens,
+                            const float *uniforms, int B, int K, int gamma,
+                            int V, float T, int32_t *n_acc, int32_t *sel_k,
+                            int32_t *out_tokens, int32_t *n_per_cand,
+                            float *out_prob, int32_t *dev_status, void *ws,
+                            size_t ws_bytes, cudaStream_t stream,
+                            bool *launched);
+
 using KcandKernel = void (*)(const KcandParams);
 
 static KcandKernel pick_kcand(int dt, bool vec, bool greedy) {
@@ -376,6 +387,15 @@ extern "C" sd_status sd_verify_kcand(
   const bool vec = aligned16(target_logits) &&
                    (greedy || gamma == 0 || aligned16(draft_logits)) &&
                    ((size_t)V * eb) % 16 == 0;
+  if (vec) {  // 16-byte aligned rows: the streaming kernel
+    bool launched = false;
+    st = kcand_ring_launch(target_logits, draft_logits, dt, draft_tokens,
+                           uniforms, B, K, gamma, V, T, n_accepted,
+                           selected_k, out_tokens, n_per_cand, out_prob,
+                           dev_status, workspace, ws_bytes,
+                           static_cast<cudaStream_t>(stream), &launched);
+    if (st != SD_OK || launched) return st;
+  }
   const long long nvec = V / (vec ? vw : 1);
   const int CL = choose_cluster(nvec);
   const long long per_cta = (nvec + CL - 1) / CL;

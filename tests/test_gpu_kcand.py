@@ -73,3 +73,32 @@ def test_invalid_rows_and_bad_tokens():
     compare(g, o, extra_equal=("k", "n_per_cand"))
     assert int(st.item()) & api.DEV_NONFINITE
     assert int(st.item()) & api.DEV_BAD_TOKEN
+
+
+@pytest.mark.parametrize("cluster", ["1", "2", "8"])
+def test_streaming_kernel_cluster_sizes(monkeypatch, cluster):
+    """The streaming kernel (aligned rows) split over 1, 2 and 8 CTAs."""
+    monkeypatch.setenv("SDV_CLUSTER", cluster)
+    for T in (0.0, 1.0):
+        c = to_device(synth.kcand_case(12, 5, 6, 40000, torch.bfloat16, T,
+                                       seed=int(cluster), sigma_t=2.0,
+                                       sigma_d=1.0, sigma_k=0.7))
+        compare(run(c), kc_oracle(c), extra_equal=("k", "n_per_cand"))
+
+
+def test_streaming_kernel_work_queue():
+    """More sequences than resident clusters."""
+    c = to_device(synth.kcand_case(700, 3, 3, 2048, torch.float32, 1.0,
+                                   seed=11, sigma_t=2.0, sigma_d=1.0,
+                                   sigma_k=0.7))
+    r = compare(run(c), kc_oracle(c), extra_equal=("k", "n_per_cand"))
+    assert r["acc_flagged"] / r["seqs"] < 5e-3
+
+
+def test_plain_load_kernel_on_aligned_rows(monkeypatch):
+    """SDV_KCAND_RING=0 sends aligned rows to the plain-load kernel."""
+    monkeypatch.setenv("SDV_KCAND_RING", "0")
+    c = to_device(synth.kcand_case(16, 4, 5, 4096, torch.bfloat16, 0.8,
+                                   seed=12, sigma_t=2.0, sigma_d=1.0,
+                                   sigma_k=0.7))
+    compare(run(c), kc_oracle(c), extra_equal=("k", "n_per_cand"))
