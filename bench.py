@@ -105,6 +105,14 @@ class ClockSampler:
                 "source": "nvml"}
 
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch
+# from one ncu capture of each kernel on B=128 sequences of this workload
+# (profiles/), with the units that launch processed: the fan-out reads every
+# row once, so its traffic scales with the rows; the verify's with the bytes
+# the method needs (its early exit decides how many rows it reads).
+TRAFFIC = {"fanout": (594.38e6, 128 * 9), "linear": (426.53e6, 343.73e6)}
+
+
 def hbm_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -205,8 +213,10 @@ def gpu_arm(args, rank, world):
     # dominant kernel: the larger of the two shares of the step
     if ms_v >= ms_f:
         kern, kb, kms = "linear_verify_kernel<0,4,false,true>", need_v_avg, ms_v
+        traffic = TRAFFIC["linear"][0] / TRAFFIC["linear"][1] * need_v_avg
     else:
-        kern, kb, kms = "fanout_kernel<0,4>", fan_bytes, ms_f
+        kern, kb, kms = "fanout_kernel<0,4,true>", fan_bytes, ms_f
+        traffic = TRAFFIC["fanout"][0] / TRAFFIC["fanout"][1] * B * (FAN["K"] + 1)
     achieved = kb / (kms / 1e3) / 1e9
     res = {
         "metric": METRIC, "value": rounds_s, "unit": "rounds/s",
@@ -222,7 +232,9 @@ def gpu_arm(args, rank, world):
                    "parallelism": "replicas" if world > 1 else "single"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": None,
+                     "traffic": traffic,
+                     "traffic_source": "ncu capture on B=128 (profiles/), "
+                                       "scaled by the units processed",
                      "peak_source": "MEASURED_PEAKS.json hbm_gbs (%s)" % src,
                      "kernel": kern, "bytes_per_launch": kb,
                      "ms_per_launch": kms},
@@ -320,6 +332,35 @@ def _rows_tree(parent, nodes, n, greedy):
     return rows
 
 
+def _time_graph(fn, sets, steps, warmup, dev):
+    """Device time per round with the `steps` calls captured once in a CUDA
+    graph and replayed (a small round is shorter than the host's cost of
+    one call).  Falls back to the host loop if capture fails; returns
+    (ms, how)."""
+    for i in range(warmup):  # also fills the library's per-kernel caches
+        fn(sets[i % len(sets)])
+    torch.cuda.synchronize()
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(steps):
+                fn(sets[i % len(sets)])
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        s = torch.cuda.current_stream(dev)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(s)
+        g.replay()
+        b.record(s)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / steps, "cuda graph of %d calls" % steps
+    except RuntimeError as e:
+        torch.cuda.synchronize()
+        return _time(fn, sets, steps, 0, dev), "host loop (%s)" % str(e)[:60]
+
+
 def _time(fn, sets, steps, warmup, dev):
     stream = torch.cuda.current_stream(dev)
     for i in range(warmup):
@@ -352,14 +393,33 @@ def other_workloads(args, dev, peak):
             e.update(extra)
         out[name] = e
 
+    want = lambda name: not args.only or args.only == name
+    if want("tiny"):
+        _tiny(args, dev, entry, steps)
+    if want("linear"):
+        _linear(args, dev, entry, steps)
+    if want("kcand"):
+        _kcand(args, dev, entry, steps)
+    if want("tree"):
+        _tree(args, dev, entry, steps)
+    return out
+
+
+def _tiny(args, dev, entry, steps):
+    from speculative_decoding_verification_temperature_gb300 import api
     # tiny: B=1, gamma=4, V=1000 fp32 (launch-latency bound)
     sets = [synth.tiny(r, device=dev) for r in range(64)]
     fn = lambda c: api.verify_linear(c.target, c.draft, c.tokens,
                                      c.uniforms, 1.0)
-    ms = _time(fn, sets, max(steps, 200), 10, dev)
+    ms, how = _time_graph(fn, sets, max(steps, 200), 10, dev)
     rows = np.mean([_rows_linear(fn(c)["n"].cpu().numpy(), 4, False)
                     for c in sets[:16]])
-    entry("tiny", ms, rows, 1000, 4, 9, {"note": "launch-latency bound"})
+    entry("tiny", ms, rows, 1000, 4, 9, {"note": "launch-latency bound",
+                                          "timing": how})
+
+
+def _linear(args, dev, entry, steps):
+    from speculative_decoding_verification_temperature_gb300 import api
     # linear: B=32, gamma=8, V=32000 bf16 at T in {0, 0.7, 1.0}; 16 sets
     # rotated (16 x 34.8 MB > 4 x L2)
     for T in (0.0, 0.7, 1.0):
@@ -368,14 +428,18 @@ def other_workloads(args, dev, peak):
             c.draft = c.draft.contiguous()
         fn = (lambda c, T=T: api.verify_linear(
             c.target, None if T == 0 else c.draft, c.tokens, c.uniforms, T))
-        ms = _time(fn, sets, max(steps, 100), 10, dev)
+        ms, how = _time_graph(fn, sets, max(steps, 100), 10, dev)
         rows = np.mean([_rows_linear(fn(c)["n"].cpu().numpy(), 8, T == 0)
                         for c in sets])
         full = 32 * (9 if T == 0 else 17)
-        entry("linear_T%g" % T, ms, rows, 32000, 2, full)
+        entry("linear_T%g" % T, ms, rows, 32000, 2, full, {"timing": how})
         del sets
+
+
+def _kcand(args, dev, entry, steps):
+    from speculative_decoding_verification_temperature_gb300 import api
     # kcand: B=64, K=8, gamma=16, V=152064 bf16, T=1; 2 sets (2.9 GB each)
-    sets = [synth.kcand(r, device=dev) for r in range(2)]
+    sets = [synth.kcand(r, device=dev) for r in range(min(2, args.sets))]
     fn = lambda c: api.verify_kcand(c.target, c.draft, c.tokens, c.uniforms,
                                     1.0)
     ms = _time(fn, sets, steps, 3, dev)
@@ -386,8 +450,12 @@ def other_workloads(args, dev, peak):
                                 o["n"].cpu().numpy(), 16))
     entry("kcand", ms, np.mean(rows), 152064, 2, 64 * (8 * 17 + 16))
     del sets
+
+
+def _tree(args, dev, entry, steps):
+    from speculative_decoding_verification_temperature_gb300 import api
     # tree: B=16, N=64, V=151936 bf16, T=0.8; 4 sets (622 MB each)
-    sets = [synth.tree(r, device=dev) for r in range(4)]
+    sets = [synth.tree(r, device=dev) for r in range(min(4, max(2, args.sets)))]
     fn = lambda c: api.verify_tree(c.target, c.draft, c.parent,
                                    c.node_tokens, c.uniforms, 0.8)
     ms = _time(fn, sets, steps, 3, dev)
@@ -399,7 +467,6 @@ def other_workloads(args, dev, peak):
                                o["n"].cpu().numpy(), False))
     entry("tree", ms, np.mean(rows), 151936, 2, 16 * 128)
     del sets
-    return out
 
 
 # --------------------------------------------------------- CPU oracle
@@ -482,6 +549,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="native",
                     choices=["native", "reference"])
+    ap.add_argument("--only", default=None,
+                    choices=["tiny", "linear", "kcand", "tree"],
+                    help="time only this other workload (profiling runs); "
+                         "no main line")
     ap.add_argument("--batch", type=int, default=256,
                     help="sequences per step (smaller only to profile a "
                          "small case of the same kernels)")
@@ -504,6 +575,14 @@ def main():
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(reference_arm(args)))
+        return
+    if args.only:  # one other workload alone (for profiler runs)
+        dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+        torch.cuda.set_device(dev)
+        peak, _ = hbm_peak()
+        if rank == 0:
+            print(json.dumps({"only": args.only,
+                              "workloads": other_workloads(args, dev, peak)}))
         return
     if world > 1:
         torch.distributed.init_process_group("nccl")
