@@ -318,13 +318,13 @@ __device__ __forceinline__ void slice_prefix(const float *segmass, int nseg,
     double acc = 0.0;
     const int s0 = lane * cs, s1 = min(nseg, s0 + cs);
     for (int s = s0; s < s1; ++s) acc += (double)segmass[s];
-    // sequential prefix over the 32 chunk sums, in lane order
-    double pre = 0.0;
-    for (int l = 0; l < 32; ++l) {
-      const double c = __shfl_sync(0xffffffffu, acc, l);
-      pre += c;
-      if (l == lane) chunk_pre[lane] = pre;
+    // inclusive prefix over the 32 chunk sums, in lane order
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const double up = __shfl_up_sync(0xffffffffu, acc, o);
+      if (lane >= o) acc += up;
     }
+    chunk_pre[lane] = acc;
   }
 }
 
@@ -603,14 +603,15 @@ __device__ double cluster_total(cg::cluster_group &cluster, DrawSmem &ds,
     const int lane = tid;
     const double sr =
         lane < CL ? cluster.map_shared_rank(&ds, lane)->slice[par] : 0.0;
-    double run = 0.0, pre = 0.0, before = 0.0;
-    for (int r = 0; r < CL; ++r) {
-      const double c = __shfl_sync(0xffffffffu, sr, r);
-      if (r == lane) before = run;
-      run += c;
-      if (r == lane) pre = run;
+    double pre = sr;  // inclusive prefix of the slice masses, rank order
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const double up = __shfl_up_sync(0xffffffffu, pre, o);
+      if (lane >= o) pre += up;
     }
-    const double tot = run;
+    const double up1 = __shfl_up_sync(0xffffffffu, pre, 1);
+    const double before = lane ? up1 : 0.0;
+    const double tot = __shfl_sync(0xffffffffu, pre, 31);
     const double tau = (double)u * tot;
     unsigned hit = __ballot_sync(0xffffffffu, lane < CL && pre > tau);
     if (!hit && tot > 0.0)  // rounding: last slice with mass
