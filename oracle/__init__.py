@@ -54,6 +54,7 @@ def _bind(path):
                                     P, P, P, P, P, P, P, P, P]
     lib.orc_fanout_schedule.argtypes = [I, I, D, D, P]
     lib.orc_fanout_topk.argtypes = [P, I, I, I, I, P, P, P, P]
+    lib.orc_fanout_hits.argtypes = [P, P, P, P, I, I, P]
     for f in (lib.orc_verify_linear, lib.orc_verify_kcand,
               lib.orc_verify_tree, lib.orc_fanout_schedule,
               lib.orc_fanout_topk):
@@ -261,6 +262,26 @@ def fanout_topk(draft, F):
     if rc:
         raise MemoryError("oracle allocation failed")
     return out
+
+
+def fanout_hits(n, tokens, fan_tokens, F):
+    """Saguaro cache hit of each sequence's outcome (n accepted, then the
+    token tokens[b, n]): 1 if that token is among the F[n] fan-out tokens of
+    position n, 0 if not, -1 where n < 0.  tokens [B, K+1], fan_tokens
+    [B, sum F]."""
+    n = np.ascontiguousarray(n, np.int32)
+    tokens = np.ascontiguousarray(tokens, np.int32)
+    fan_tokens = np.ascontiguousarray(fan_tokens, np.int32)
+    F = np.ascontiguousarray(F, np.int32)
+    B, K1 = tokens.shape
+    if F.shape != (K1,) or n.shape != (B,) or \
+            fan_tokens.shape != (B, int(F.sum())):
+        raise ValueError("shapes: n [B], tokens [B, K+1], F [K+1], "
+                         "fan_tokens [B, sum F]")
+    hit = np.empty(B, np.int32)
+    _load().orc_fanout_hits(_ptr(n), _ptr(tokens), _ptr(fan_tokens), _ptr(F),
+                            B, K1 - 1, _ptr(hit))
+    return hit
 
 
 FLAG_MARGIN = 1e-5

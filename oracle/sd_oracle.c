@@ -26,7 +26,9 @@
  *  - Speculative Speculative Decoding / Saguaro, "speculation cache
  *    strategy": Definition 11 (power-law cache miss) and Theorem 12
  *    (geometric fan-out F_k = F_0 a^{k/(1+r)}, capped at position K), and
- *    the top-F_k-per-position cache fill.
+ *    the top-F_k-per-position cache fill; "technical architecture": the
+ *    speculator serves the next round from its cache when the verification
+ *    outcome (k accepted, then t*) is in the cache.
  *
  * Readings where the pages are silent (all listed in the design notes):
  *  - accept iff r <= p(x)/q(x) (reject on '>', Algorithm 1 step 3);
@@ -640,5 +642,36 @@ int orc_fanout_topk(const void *draft, int dtype, int B, int K, int V,
     status[b] = st;
   }
   free(e);
+  return 0;
+}
+
+/*
+ * Cache hit of each sequence's verification outcome (Speculative Speculative
+ * Decoding / Saguaro: the outcome is v = (k, t*), k accepted drafts and the
+ * correction or bonus token t*; the cache holds, for each lookahead
+ * position k, the F_k tokens of the fan-out row k).  hit[b] = 1 if t* is
+ * one of the F_{n_b} tokens stored for position n_b, 0 if not, -1 for a
+ * sequence without an outcome (n_b < 0).  tokens [B, K+1] (x_0..x_{n-1},
+ * t*, ...), fan_tokens [B, sum F] grouped by position.
+ */
+int orc_fanout_hits(const int32_t *n_acc, const int32_t *tokens,
+                    const int32_t *fan_tokens, const int32_t *F, int B,
+                    int K, int32_t *hit) {
+  int total = 0;
+  for (int k = 0; k <= K; ++k) total += F[k];
+  for (int b = 0; b < B; ++b) {
+    const int n = n_acc[b];
+    if (n < 0 || n > K) {
+      hit[b] = -1;
+      continue;
+    }
+    const int32_t t = tokens[(size_t)b * (K + 1) + n];
+    int off = 0;
+    for (int k = 0; k < n; ++k) off += F[k];
+    int found = 0;
+    for (int i = 0; i < F[n]; ++i)
+      if (fan_tokens[(size_t)b * total + off + i] == t) found = 1;
+    hit[b] = found;
+  }
   return 0;
 }

@@ -65,6 +65,14 @@ MUTANTS = [
     ("fanout_cap_sign",
      "pow(1.0 - a, -1.0 / (1.0 + r));", "pow(1.0 - a, 1.0 / (1.0 + r));", 1,
      ["test_fanout_schedule_golden_and_theorem12"]),
+    ("hits_position_off_by_one", "for (int k = 0; k < n; ++k) off += F[k];",
+     "for (int k = 0; k <= n && k < K; ++k) off += F[k];", 1,
+     ["test_cache_hits_golden"]),
+    ("hits_outcome_token_off_by_one",
+     "const int32_t t = tokens[(size_t)b * (K + 1) + n];",
+     "const int32_t t = tokens[(size_t)b * (K + 1) + (n > 0 ? n - 1 : 0)];",
+     1, ["test_cache_hits_golden",
+         "test_cache_hit_rate_equals_top_f_mass_when_p_equals_q"]),
     ("topk_tie_order", "return (a->idx > b->idx) - (a->idx < b->idx);",
      "return (a->idx < b->idx) - (a->idx > b->idx);", 1,
      ["test_fanout_topk_against_stable_sort_and_ties"]),

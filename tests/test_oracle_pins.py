@@ -530,3 +530,45 @@ def test_fanout_topk_against_stable_sort_and_ties():
                 np.testing.assert_array_equal(
                     o["tokens"][b, off:off + F[k]], order)
             off += F[k]
+
+
+# --------------------------- Saguaro: cache hit of the verification outcome
+def test_cache_hits_golden():
+    """Hand-worked outcomes and caches (tests/golden/cache_hits.json)."""
+    g = _golden("cache_hits.json")
+    F = np.array(g["F"], np.int32)
+    for c in g["cases"]:
+        h = oracle.fanout_hits([c["n"]], [c["tokens"]], [c["fan_tokens"]], F)
+        assert h[0] == c["hit"], c["why"]
+    e = g["empty_position"]
+    h = oracle.fanout_hits([e["n"]], [e["tokens"]], [e["fan_tokens"]],
+                           np.array(e["F"], np.int32))
+    assert h[0] == e["hit"], e["why"]
+
+
+def test_cache_hit_rate_equals_top_f_mass_when_p_equals_q():
+    """With identical target and draft rows every draft is accepted
+    (p/q = 1), so the outcome is (gamma, t*) with t* ~ p_gamma, and the
+    speculation cache of position gamma holds the top-F tokens of the draft
+    row gamma = p_gamma's own top-F: the hit rate is the top-F mass of
+    p_gamma.  The oracle's verify + fan-out + hit pipeline over 40000
+    seeded rounds matches that mass within 5 sigma, for F = 1, 3 and V."""
+    V, gamma, B = 12, 2, 40000
+    rng = np.random.default_rng(21)
+    rows = rng.normal(0.0, 1.5, (gamma + 1, V)).astype(np.float32)
+    target = tile_rows(rows, B)
+    draft = np.ascontiguousarray(target[:, :gamma])
+    p_last = softmax(f32(rows[gamma]))
+    x = np.stack([draw_from(softmax(f32(rows[j])), B, 100 + j)
+                  for j in range(gamma)], axis=1)
+    u = synth.uniforms(22, (B, gamma + 1))
+    o = oracle.verify_linear(target, draft, x, u, 1.0)
+    assert np.all(o["n"] == gamma)
+    for Fl in (1, 3, V):
+        F = np.array([1] * gamma + [Fl], np.int32)
+        fan = oracle.fanout_topk(target, F)["tokens"]
+        hit = oracle.fanout_hits(o["n"], o["tokens"], fan, F)
+        mass = np.sort(p_last)[::-1][:Fl].sum()
+        rate = hit.mean()
+        sd = math.sqrt(max(mass * (1 - mass), 1e-12) / B)
+        assert abs(rate - mass) <= 5 * sd + 1e-12, (Fl, rate, mass)
