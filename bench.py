@@ -402,7 +402,42 @@ def other_workloads(args, dev, peak):
         _kcand(args, dev, entry, steps)
     if want("tree"):
         _tree(args, dev, entry, steps)
+    if want("cache_hit"):
+        out["cache_hit"] = _cache_hit(args, dev)
     return out
+
+
+def uniform_schedule(K, budget):
+    """budget / (K+1) per position, the remainder to the lowest positions."""
+    F = [budget // (K + 1)] * (K + 1)
+    for k in range(budget - sum(F)):
+        F[k] += 1
+    return F
+
+
+def _cache_hit(args, dev):
+    """Saguaro cache-hit rate of the verification outcomes on the large
+    workload's shape: verify, fan-out with the geometric schedule and with
+    a uniform one of the same budget, then sd_fanout_hits."""
+    from speculative_decoding_verification_temperature_gb300 import api
+    Fg = api.fanout_schedule(FAN["K"], FAN["budget"], FAN["a"], FAN["r"])
+    Fu = uniform_schedule(FAN["K"], FAN["budget"])
+    res = {"F_geometric": Fg, "F_uniform": Fu, "B": B}
+    for T in (0.0, 0.5, 1.0):
+        c = synth.linear_case(B, GAMMA, V, torch.float32, T,
+                              seed=1004 + int(T * 10), sigma_t=3.0,
+                              sigma_d=1.0, draft_rows=GAMMA + 1, device=dev)
+        v = api.verify_linear(c.target, None if T == 0 else
+                              c.draft[:, :GAMMA].contiguous(), c.tokens,
+                              c.uniforms, T)
+        row = {"mean_accepted": float(v["n"].float().mean())}
+        for name, F in (("geometric", Fg), ("uniform", Fu)):
+            f = api.fanout_topk(c.draft, F)
+            h = api.fanout_hits(v["n"], v["tokens"], f["tokens"], F)
+            row[name] = float((h == 1).float().mean())
+        res["T%g" % T] = row
+        del c
+    return res
 
 
 def _tiny(args, dev, entry, steps):
@@ -550,7 +585,7 @@ def main():
     ap.add_argument("--impl", default="native",
                     choices=["native", "reference"])
     ap.add_argument("--only", default=None,
-                    choices=["tiny", "linear", "kcand", "tree"],
+                    choices=["tiny", "linear", "kcand", "tree", "cache_hit"],
                     help="time only this other workload (profiling runs); "
                          "no main line")
     ap.add_argument("--batch", type=int, default=256,

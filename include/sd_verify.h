@@ -228,12 +228,30 @@ sd_status sd_fanout_topk(const void *draft_logits, sd_dtype dt, int B, int K,
                          void *workspace, size_t ws_bytes, void *stream);
 
 /* ---------------------------------------------------------------------
+ * Cache hit of the verification outcome (Speculative Speculative Decoding
+ * / Saguaro, "technical architecture": the speculator serves the next
+ * round from its speculation cache when the verification outcome is in
+ * it; "speculation cache strategy": an outcome is (k, t*), k accepted
+ * drafts then the correction or bonus token t*, and the cache holds the
+ * top-F_k draft tokens of each lookahead position k).
+ *
+ * n_accepted [B] and out_tokens [B, K+1] as returned by the verify (so
+ * t* = out_tokens[b, n_b]); fan_tokens [B, sum F] as returned by
+ * sd_fanout_topk with the same F (host [K+1]).  hit [B] int32: 1 if t* is
+ * one of the F_{n_b} tokens stored for position n_b, 0 if not, -1 where
+ * n_b is outside [0, K] (an unusable row).  All device pointers.
+ * ------------------------------------------------------------------- */
+sd_status sd_fanout_hits(const int32_t *n_accepted, const int32_t *out_tokens,
+                         const int32_t *fan_tokens, int B, int K,
+                         const int32_t *F, int32_t *hit, void *stream);
+
+/* ---------------------------------------------------------------------
  * Linear verify fused with the fan-out of the same draft logits, in one
  * pass over each draft row (the two calls above, same results).
  *
  * draft_logits [B, K+1, V] with K == gamma: rows 0..gamma-1 are the draft
  * rows of the verify, all K+1 rows feed the fan-out.  Other arguments as in
- * sd_verify_linear and sd_fanout_topk.  T must be > 0.
+ * sd_verify_linear and sd_fanout_topk (T == 0 is greedy, as there).
  * ------------------------------------------------------------------- */
 size_t sd_verify_linear_fanout_workspace(int B, int gamma, int V,
                                          sd_dtype dt);

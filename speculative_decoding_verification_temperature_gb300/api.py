@@ -66,6 +66,7 @@ def _declare(L):
         "sd_fanout_topk": ([P, I, I, I, I, P, P, P, P, P, Z, P], I),
         "sd_verify_linear_static": ([P, P, I, P, P, I, I, I, F, P, P, P, P,
                                      P, P, P], I),
+        "sd_fanout_hits": ([P, P, P, I, I, P, P, P], I),
         "sd_verify_linear_fanout_workspace": ([I, I, I, I], Z),
         "sd_verify_linear_fanout": ([P, P, I, P, P, I, I, I, F, P, P, P, P,
                                      P, P, P, P, Z, P], I),
@@ -305,6 +306,29 @@ def fanout_topk(draft, F, *, want_logit=False, status=None, workspace=None):
     if want_logit:
         r["logit"] = lg[:, :total]
     return r
+
+
+def fanout_hits(n, tokens, fan_tokens, F):
+    """Saguaro cache hit of each sequence's verification outcome
+    (sd_fanout_hits): 1 if tokens[b, n[b]] is among the F[n[b]] fan-out
+    tokens of position n[b], 0 if not, -1 where n[b] < 0.  n [B], tokens
+    [B, K+1] and fan_tokens [B, sum F] int32 on one CUDA device."""
+    dev = n.device
+    n = _dev(n, dev, "n", torch.int32)
+    tokens = _dev(tokens, dev, "tokens", torch.int32)
+    F = [int(x) for x in F]
+    B, K1 = tokens.shape
+    if len(F) != K1:
+        raise ValueError("F must have K+1 entries")
+    fan_tokens = _dev(fan_tokens, dev, "fan_tokens", torch.int32)
+    if tuple(fan_tokens.shape) != (B, sum(F)):
+        raise ValueError("fan_tokens must be [B, sum F]")
+    Fh = (ctypes.c_int32 * K1)(*F)
+    hit = torch.empty(B, dtype=torch.int32, device=dev)
+    _check(lib().sd_fanout_hits(_p(n), _p(tokens), _p(fan_tokens), B, K1 - 1,
+                                ctypes.cast(Fh, ctypes.c_void_p), _p(hit),
+                                _stream(dev)))
+    return hit
 
 
 def verify_linear_fanout(target, draft, tokens, uniforms, T, F, *,

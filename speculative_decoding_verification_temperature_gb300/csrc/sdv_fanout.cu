@@ -278,3 +278,75 @@ extern "C" sd_status sd_fanout_topk(const void *draft_logits, sd_dtype dt,
   return launch_clusters((const void *)kern, (int)want, CL, smem,
                          static_cast<cudaStream_t>(stream), args);
 }
+
+// ---------------------------------------------------------------- hits
+// Saguaro cache hit of each sequence's verification outcome: the speculator
+// serves the next round from its cache when the outcome (n accepted, then
+// t*) is stored, i.e. when t* is one of the F_n fan-out tokens of position
+// n.  One warp per sequence.
+namespace sdv {
+
+struct HitParams {
+  const int32_t *n_acc;       // [B]
+  const int32_t *tokens;      // [B, K+1]
+  const int32_t *fan_tokens;  // [B, total]
+  int32_t *hit;               // [B]
+  int B, K, total;
+  int F[SD_MAX_K + 1];
+  int off[SD_MAX_K + 2];
+};
+
+__global__ void __launch_bounds__(kThreads) fanout_hits_kernel(const HitParams p) {
+  const int lane = threadIdx.x & 31;
+  const long long b = (long long)blockIdx.x * kWarps + (threadIdx.x >> 5);
+  if (b >= p.B) return;
+  const int n = p.n_acc[b];
+  if (n < 0 || n > p.K) {
+    if (lane == 0) p.hit[b] = -1;
+    return;
+  }
+  const int32_t t = p.tokens[b * (p.K + 1) + n];
+  const int32_t *cache = p.fan_tokens + b * p.total + p.off[n];
+  bool found = false;
+  for (int i = lane; i < p.F[n]; i += 32) found |= cache[i] == t;
+  const unsigned any = __ballot_sync(0xffffffffu, found);
+  if (lane == 0) p.hit[b] = any ? 1 : 0;
+}
+
+}  // namespace sdv
+
+extern "C" sd_status sd_fanout_hits(const int32_t *n_accepted,
+                                    const int32_t *out_tokens,
+                                    const int32_t *fan_tokens, int B, int K,
+                                    const int32_t *F, int32_t *hit,
+                                    void *stream) {
+  using namespace sdv;
+  SDV_REQUIRE(B >= 0, "B < 0");
+  SDV_REQUIRE(K >= 0 && K <= SD_MAX_K, "K=%d outside [0, %d]", K, SD_MAX_K);
+  SDV_REQUIRE(F != nullptr, "F is null");
+  HitParams prm;
+  int total = 0;
+  for (int k = 0; k <= K; ++k) {
+    SDV_REQUIRE(F[k] >= 0, "F[%d] < 0", k);
+    prm.F[k] = F[k];
+    prm.off[k] = total;
+    total += F[k];
+  }
+  if (B == 0) return SD_OK;
+  SDV_REQUIRE(n_accepted && out_tokens && hit, "null pointer");
+  SDV_REQUIRE(total == 0 || fan_tokens, "fan_tokens is null");
+  int sms = 0;
+  sd_status st = check_device(&sms);
+  if (st != SD_OK) return st;
+  prm.n_acc = n_accepted;
+  prm.tokens = out_tokens;
+  prm.fan_tokens = fan_tokens;
+  prm.hit = hit;
+  prm.B = B;
+  prm.K = K;
+  prm.total = total;
+  const int grid = (B + kWarps - 1) / kWarps;
+  fanout_hits_kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(prm);
+  SDV_CUDA(cudaGetLastError());
+  return SD_OK;
+}

@@ -134,3 +134,52 @@ def test_best_keys_in_one_warp():
     d[:, 0, sel] += 20 + torch.rand(int(sel.sum()))
     check(d.cuda(), [64])
     check(d.cuda(), [20])
+
+
+def test_cache_hits_against_oracle():
+    """sd_fanout_hits on the GPU's own verify and fan-out outputs equals the
+    oracle's hit function on the same integers, and the whole pipeline
+    (verify, fan-out, hits) equals the oracle's pipeline on sequences whose
+    draws are not near a boundary."""
+    for T in (0.0, 1.0):
+        c = synth.linear_case(64, 4, 3000, torch.float32, T, seed=31,
+                              sigma_t=2.0, sigma_d=1.0, draft_rows=5)
+        cd = synth.LinearCase(c.target.cuda(), c.draft.cuda(),
+                              c.tokens.cuda(), c.uniforms.cuda(), T)
+        F = [3, 0, 2, 5, 4]
+        v = api.verify_linear(cd.target, None if T == 0 else
+                              cd.draft[:, :4].contiguous(), cd.tokens,
+                              cd.uniforms, T)
+        f = api.fanout_topk(cd.draft, F)
+        h = host(api.fanout_hits(v["n"], v["tokens"], f["tokens"], F))
+        o = oracle.fanout_hits(host(v["n"]), host(v["tokens"]),
+                               host(f["tokens"]), np.array(F, np.int32))
+        np.testing.assert_array_equal(h, o)
+        ov = oracle.verify_linear(
+            synth.host_logits(c.target),
+            None if T == 0 else np.ascontiguousarray(
+                synth.host_logits(c.draft)[:, :4]),
+            host(c.tokens), host(c.uniforms), T)
+        of = oracle.fanout_topk(synth.host_logits(c.draft),
+                                np.array(F, np.int32))
+        oh = oracle.fanout_hits(ov["n"], ov["tokens"], of["tokens"],
+                                np.array(F, np.int32))
+        keep = (ov["margin"] >= oracle.FLAG_MARGIN) | (T == 0)
+        np.testing.assert_array_equal(h[keep], oh[keep])
+        assert keep.mean() > 0.8
+
+
+def test_cache_hits_edge_cases():
+    """Unusable rows (-1), empty positions, F = 64 wide positions."""
+    n = torch.tensor([-1, 0, 1, 2, 2], dtype=torch.int32, device="cuda")
+    toks = torch.tensor([[-1, -1, -1], [5, 0, 0], [1, 6, 0], [1, 2, 63],
+                         [1, 2, 64]], dtype=torch.int32, device="cuda")
+    F = [1, 0, 64]
+    fan = torch.zeros((5, 65), dtype=torch.int32, device="cuda")
+    fan[:, 0] = 5
+    fan[:, 1:] = torch.arange(64, dtype=torch.int32, device="cuda")
+    h = host(api.fanout_hits(n, toks, fan, F))
+    o = oracle.fanout_hits(host(n), host(toks), host(fan),
+                           np.array(F, np.int32))
+    np.testing.assert_array_equal(h, o)
+    assert h.tolist() == [-1, 1, 0, 1, 0]
