@@ -55,6 +55,8 @@ def _bind(path):
     lib.orc_fanout_schedule.argtypes = [I, I, D, D, P]
     lib.orc_fanout_topk.argtypes = [P, I, I, I, I, P, P, P, P]
     lib.orc_fanout_hits.argtypes = [P, P, P, P, I, I, P]
+    lib.orc_verify_linear_filtered.argtypes = [P, P, I, P, P, I, I, I, D, I,
+                                               D, P, P, P, P, P, P, P, P]
     for f in (lib.orc_verify_linear, lib.orc_verify_kcand,
               lib.orc_verify_tree, lib.orc_fanout_schedule,
               lib.orc_fanout_topk):
@@ -165,6 +167,43 @@ def verify_linear(target, draft, tokens, uniforms, T, want_resid=False):
     out["accept"] = out["accept"][:, :gamma]
     if want_resid:
         out["resid"] = resid
+    return _finish(out, m)
+
+
+def verify_linear_filtered(target, draft, tokens, uniforms, T, top_k,
+                           top_p=1.0):
+    """Linear verify with top_k / top_p filtered sampling applied to p and q
+    before the ratio (same shapes as verify_linear).  Returns n, tokens,
+    prob, the margins (margin_acc also covers the nucleus cuts) and status.
+    """
+    target, dt = _logits(target)
+    B, G1, V = target.shape
+    gamma = G1 - 1
+    if draft is None:
+        if T != 0:
+            raise ValueError("draft logits are required when T > 0")
+        draft_p = None
+    else:
+        draft, dt2 = _logits(draft)
+        if dt2 != dt or draft.shape != (B, gamma, V):
+            raise ValueError("draft must match target in dtype and shape")
+        draft_p = _ptr(draft)
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32).reshape(B, gamma)
+    uniforms = np.ascontiguousarray(uniforms, dtype=np.float32).reshape(B, G1)
+    out = {
+        "n": np.empty(B, np.int32),
+        "tokens": np.empty((B, G1), np.int32),
+        "prob": np.empty(B, np.float64),
+        "status": np.empty(B, np.int32),
+    }
+    m = _margins(B)
+    rc = _load().orc_verify_linear_filtered(
+        _ptr(target), draft_p, dt, _ptr(tokens), _ptr(uniforms), B, gamma, V,
+        float(T), int(top_k), float(top_p), _ptr(out["n"]),
+        _ptr(out["tokens"]), _ptr(out["prob"]), *_margin_ptrs(m),
+        _ptr(out["status"]))
+    if rc:
+        raise MemoryError("oracle allocation failed")
     return _finish(out, m)
 
 

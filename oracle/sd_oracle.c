@@ -39,6 +39,11 @@
  *    last j with positive weight;
  *  - a residual of exactly zero mass falls back to sampling p and sets
  *    status bit 8;
+ *  - filtered sampling ("01 · Draft-then-verify", section 4, standardised
+ *    sampling: top-k / nucleus act on p and q before the ratio): softmax at
+ *    temperature T, keep the top_k tokens by (logit desc, index asc), then
+ *    the smallest prefix of them, in that order, whose renormalised mass
+ *    reaches top_p, and renormalise over what is kept;
  *  - a draft token outside [0, V) is a rejection (status bit 1);
  *  - a row holding NaN or +inf, or only -inf, makes its sequence invalid
  *    (status bit 2; n = -1, every token -1);
@@ -673,5 +678,154 @@ int orc_fanout_hits(const int32_t *n_acc, const int32_t *tokens,
       if (fan_tokens[(size_t)b * total + off + i] == t) found = 1;
     hit[b] = found;
   }
+  return 0;
+}
+
+/* ------------------------------------------------------------------------
+ * Filtered sampling of one row ("01 · Draft-then-verify", section 4,
+ * standardised sampling): p = softmax(z / T); keep the top_k tokens in
+ * (logit desc, index asc) order; of those, keep the smallest prefix whose
+ * mass, renormalised over the top_k, reaches top_p (token i stays iff the
+ * mass before it is below top_p); renormalise over the kept tokens.  p gets
+ * the filtered distribution (0 outside the kept set).  *margin is lowered to
+ * the distance of every prefix mass from top_p (where an fp32 computation
+ * may cut the nucleus differently).  Returns 0 on an unusable row. */
+static int filtered_row(const void *base, int dtype, size_t off, int V,
+                        double T, int top_k, double top_p, double *p,
+                        orc_entry *e, double *margin) {
+  if (!softmax_row(base, dtype, off, V, T, p)) return 0;
+  for (int j = 0; j < V; ++j) {
+    double z = logit_at(base, dtype, off + (size_t)j);
+    e[j].v = (z == 0.0) ? 0.0 : z;
+    e[j].idx = j;
+  }
+  qsort(e, (size_t)V, sizeof(orc_entry), entry_cmp);
+  int k = top_k < V ? top_k : V;
+  double mk = 0.0;
+  for (int i = 0; i < k; ++i) mk += p[e[i].idx];
+  int keep = k;
+  if (top_p < 1.0) {
+    double before = 0.0;
+    keep = 0;
+    for (int i = 0; i < k; ++i) {
+      double f = before / mk;
+      note_margin(margin, fabs(f - top_p));
+      if (f < top_p) keep = i + 1;
+      before += p[e[i].idx];
+    }
+  }
+  double S = 0.0;
+  for (int i = 0; i < keep; ++i) S += p[e[i].idx];
+  double *kept = malloc(sizeof(double) * (size_t)keep);
+  if (!kept) return 0;
+  for (int i = 0; i < keep; ++i) kept[i] = p[e[i].idx] / S;
+  for (int j = 0; j < V; ++j) p[j] = 0.0;
+  for (int i = 0; i < keep; ++i) p[e[i].idx] = kept[i];
+  free(kept);
+  return 1;
+}
+
+/* ------------------------------------------------------------------------
+ * Linear verify with filtered sampling: the rule of orc_verify_linear with
+ * p_i and q_i replaced by their top_k / top_p filtered versions (same
+ * filter for target and draft).  T == 0 is greedy (the filters keep the
+ * argmax), as in orc_verify_linear.  margin_acc also covers the nucleus
+ * cuts (see filtered_row).
+ * ---------------------------------------------------------------------- */
+int orc_verify_linear_filtered(const void *target, const void *draft,
+                               int dtype, const int32_t *tokens,
+                               const float *uniforms, int B, int gamma, int V,
+                               double T, int top_k, double top_p,
+                               int32_t *n_acc, int32_t *out_tokens,
+                               double *out_prob, double *margin_acc,
+                               double *margin_cdf, int32_t *cdf_lo,
+                               int32_t *cdf_hi, int32_t *status) {
+  if (T == 0.0) {
+    double *acc = malloc(sizeof(double) * (size_t)(B * (gamma > 0 ? gamma : 1)));
+    if (!acc) return 1;
+    int rc = orc_verify_linear(target, draft, dtype, tokens, uniforms, B,
+                               gamma, V, T, n_acc, out_tokens, out_prob, acc,
+                               margin_acc, margin_cdf, cdf_lo, cdf_hi, NULL,
+                               status);
+    free(acc);
+    return rc;
+  }
+  double *p = malloc(sizeof(double) * (size_t)V);
+  double *q = malloc(sizeof(double) * (size_t)V);
+  double *w = malloc(sizeof(double) * (size_t)V);
+  orc_entry *e = malloc(sizeof(orc_entry) * (size_t)V);
+  if (!p || !q || !w || !e) { free(p); free(q); free(w); free(e); return 1; }
+  const int G1 = gamma + 1;
+  for (int b = 0; b < B; ++b) {
+    int st = 0, n = 0, t = -1, invalid = 0, lo = -1, hi = -1, rejected = 0;
+    double mg = INFINITY, mc = INFINITY, prob = 0.0;
+    for (int i = 0; i < gamma; ++i) {
+      if (!filtered_row(target, dtype, ((size_t)b * G1 + i) * V, V, T, top_k,
+                        top_p, p, e, &mg) ||
+          !filtered_row(draft, dtype, ((size_t)b * gamma + i) * V, V, T,
+                        top_k, top_p, q, e, &mg)) {
+        invalid = 1;
+        break;
+      }
+      int x = tokens[(size_t)b * gamma + i];
+      double r = (double)uniforms[(size_t)b * G1 + i];
+      int ok;
+      if (x < 0 || x >= V) {
+        st |= ORC_ST_BAD_TOKEN;
+        ok = 0;
+      } else {
+        double rho = accept_ratio(p[x], q[x]);
+        if (isfinite(rho)) note_margin(&mg, fabs(r - rho));
+        ok = (r <= rho);
+      }
+      if (!ok) { rejected = 1; break; }
+      ++n;
+    }
+    if (!invalid) {
+      if (rejected) { /* residual norm(max(0, p~_n - q~_n)) */
+        double N = 0.0;
+        for (int j = 0; j < V; ++j) {
+          double d = p[j] - q[j];
+          w[j] = d > 0.0 ? d : 0.0;
+          N += w[j];
+        }
+        if (N == 0.0) {
+          st |= ORC_ST_ZERO_MASS;
+          for (int j = 0; j < V; ++j) w[j] = p[j];
+        }
+      } else if (!filtered_row(target, dtype, ((size_t)b * G1 + gamma) * V, V,
+                               T, top_k, top_p, p, e, &mg)) {
+        invalid = 1;
+      } else {
+        for (int j = 0; j < V; ++j) w[j] = p[j];
+      }
+    }
+    if (!invalid) {
+      double u = (double)uniforms[(size_t)b * G1 + gamma];
+      t = sample_icdf(w, V, u, &prob, &mc, &lo, &hi);
+    } else {
+      st |= ORC_ST_NONFINITE;
+      n = -1;
+      prob = 0.0;
+      mg = mc = INFINITY;
+      lo = hi = -1;
+    }
+    n_acc[b] = n;
+    for (int i = 0; i < G1; ++i) {
+      int32_t v = -1;
+      if (!invalid) {
+        if (i < n) v = tokens[(size_t)b * gamma + i];
+        else if (i == n) v = t;
+      }
+      out_tokens[(size_t)b * G1 + i] = v;
+    }
+    out_prob[b] = prob;
+    margin_acc[b] = mg;
+    margin_cdf[b] = mc;
+    cdf_lo[b] = lo;
+    cdf_hi[b] = hi;
+    status[b] = st;
+  }
+  free(p); free(q); free(w); free(e);
   return 0;
 }

@@ -73,6 +73,17 @@ MUTANTS = [
      "const int32_t t = tokens[(size_t)b * (K + 1) + (n > 0 ? n - 1 : 0)];",
      1, ["test_cache_hits_golden",
          "test_cache_hit_rate_equals_top_f_mass_when_p_equals_q"]),
+    ("nucleus_one_too_many", "if (f < top_p) keep = i + 1;",
+     "if (f < top_p) keep = i + 2 < k ? i + 2 : k;", 1,
+     ["test_filtered_sampling_golden"]),
+    ("nucleus_not_renormalised_over_top_k", "double f = before / mk;",
+     "double f = before;", 1,
+     ["test_filtered_sampling_golden"]),
+    ("filter_kept_not_renormalised",
+     "for (int i = 0; i < keep; ++i) kept[i] = p[e[i].idx] / S;",
+     "for (int i = 0; i < keep; ++i) kept[i] = p[e[i].idx];", 1,
+     ["test_filtered_sampling_golden",
+      "test_filtered_first_token_marginal_is_filtered_p"]),
     ("topk_tie_order", "return (a->idx > b->idx) - (a->idx < b->idx);",
      "return (a->idx < b->idx) - (a->idx > b->idx);", 1,
      ["test_fanout_topk_against_stable_sort_and_ties"]),
@@ -100,6 +111,8 @@ def _run_pin(name):
         "test_bruteforce_enumeration": [dict(V=3, gamma=3),
                                         dict(V=5, gamma=2)],
         "test_tree_chain_equals_linear": [dict(T=1.0)],
+        "test_filtered_first_token_marginal_is_filtered_p": [
+            dict(top_k=5, top_p=1.0), dict(top_k=4, top_p=0.6)],
     }.get(name, [dict()])
     for kw in params:
         fn(**kw)

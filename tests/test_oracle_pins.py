@@ -572,3 +572,99 @@ def test_cache_hit_rate_equals_top_f_mass_when_p_equals_q():
         rate = hit.mean()
         sd = math.sqrt(max(mass * (1 - mass), 1e-12) / B)
         assert abs(rate - mass) <= 5 * sd + 1e-12, (Fl, rate, mass)
+
+
+# ---------------- "01 · Draft-then-verify" 4: standardised (filtered) sampling
+def filtered(z, T, top_k, top_p):
+    """top_k / top_p filtered softmax(z / T) (the reading of section 4):
+    top_k by (logit desc, index asc), then the smallest prefix whose mass,
+    renormalised over the top_k, reaches top_p; renormalised."""
+    z = np.asarray(z, np.float64)
+    p = softmax(z, T)
+    order = np.lexsort((np.arange(len(z)), -z))[:top_k]
+    mk = p[order].sum()
+    before = np.concatenate([[0.0], np.cumsum(p[order])[:-1]]) / mk
+    keep = order[before < top_p] if top_p < 1.0 else order
+    out = np.zeros_like(p)
+    out[keep] = p[keep] / p[keep].sum()
+    return out
+
+
+@pytest.mark.parametrize("T,dtype", [(1.0, "f32"), (0.7, "bf16")])
+def test_filtered_without_filter_equals_linear(T, dtype):
+    """top_k = V and top_p = 1 keep every token: the filtered verify is the
+    plain linear verify, output for output."""
+    import torch
+    c = synth.linear_case(300, 4, 37, torch.float32 if dtype == "f32"
+                          else torch.bfloat16, T, seed=61, sigma_t=2.0,
+                          sigma_d=1.0)
+    t, d = synth.host_logits(c.target), synth.host_logits(c.draft)
+    a = oracle.verify_linear(t, d, c.tokens.numpy(), c.uniforms.numpy(), T)
+    b = oracle.verify_linear_filtered(t, d, c.tokens.numpy(),
+                                      c.uniforms.numpy(), T, 37, 1.0)
+    for k in ("n", "tokens", "cdf_lo", "cdf_hi"):
+        np.testing.assert_array_equal(a[k], b[k], k)
+    for k in ("prob", "margin_cdf"):  # the kept mass is 1 up to rounding
+        np.testing.assert_allclose(a[k], b[k], rtol=1e-12, atol=1e-14)
+
+
+def test_filtered_sampling_golden():
+    """Hand-worked top-k / top-p cuts (tests/golden/filtered_sampling.json)
+    seen through the bonus draw: with identical target and draft rows every
+    draft is accepted, and uniforms placed inside each kept token's interval
+    of the filtered CDF (index order) must draw that token with probability
+    p_j / mass; kept-out tokens are never drawn."""
+    g = _golden("filtered_sampling.json")
+    p = np.array(g["p"])
+    z = np.log(p).astype(np.float32)
+    for c in g["cases"]:
+        kept = c["kept"]
+        pt = np.zeros_like(p)
+        pt[kept] = p[kept] / c["mass"]
+        cdf = np.cumsum(pt)
+        us, want = [], []
+        for j in kept:  # the middle of token j's interval
+            us.append((cdf[j] - pt[j] / 2))
+            want.append(j)
+        B = len(us)
+        rows = np.stack([z, z])  # gamma = 1: row 0 tested, row 1 bonus
+        x = np.full((B, 1), kept[0], np.int32)
+        u = np.zeros((B, 2), np.float32)
+        u[:, 0] = 0.5
+        u[:, 1] = np.array(us, np.float32)
+        o = oracle.verify_linear_filtered(tile_rows(rows, B),
+                                          tile_rows(rows[:1], B), x, u, 1.0,
+                                          c["top_k"], c["top_p"])
+        assert np.all(o["n"] == 1), c["why"]
+        assert o["tokens"][:, 1].tolist() == want, c["why"]
+        np.testing.assert_allclose(o["prob"], pt[want], rtol=1e-6,
+                                   err_msg=c["why"])
+    a = g["accept_case"]
+    zt = np.log(np.array([a["p"], a["p"]])).astype(np.float32)
+    zq = np.log(np.array([a["q"]])).astype(np.float32)
+    o = oracle.verify_linear_filtered(zt[None], zq[None], [[a["x"]]],
+                                      [[a["r"], a["u"]]], 1.0, a["top_k"],
+                                      a["top_p"])
+    assert o["n"][0] == a["n"] and o["tokens"][0, 0] == a["token"], a["why"]
+    np.testing.assert_allclose(o["prob"][0], a["prob"], rtol=1e-6)
+
+
+@pytest.mark.parametrize("top_k,top_p", [(5, 1.0), (8, 0.85), (4, 0.6)])
+def test_filtered_first_token_marginal_is_filtered_p(top_k, top_p):
+    """Drafts drawn from the filtered q~; the first emitted token follows
+    the filtered p~ (chi-square over 400000 rounds), the lossless property
+    section 4 asks of standardised sampling; tokens outside p~'s support
+    never appear."""
+    rng = np.random.default_rng(71 + top_k)
+    V, gamma, B, T = 8, 2, 400_000, 0.8
+    zt = rng.normal(0, 1.3, (gamma + 1, V))
+    zq = zt[:gamma] + rng.normal(0, 0.9, (gamma, V))
+    zt, zq = f32(zt), f32(zq)
+    xs = np.stack([draw_from(filtered(zq[i], T, top_k, top_p), B, 80 + i)
+                   for i in range(gamma)], 1)
+    out = oracle.verify_linear_filtered(
+        tile_rows(zt, B), tile_rows(zq, B), xs,
+        synth.uniforms(90 + top_k, (B, gamma + 1)), T, top_k, top_p)
+    first = out["tokens"][:, 0]
+    p0 = filtered(zt[0], T, top_k, top_p)
+    assert chi2_p(np.bincount(first, minlength=V), p0) > P_MIN
