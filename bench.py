@@ -402,9 +402,30 @@ def other_workloads(args, dev, peak):
         _kcand(args, dev, entry, steps)
     if want("tree"):
         _tree(args, dev, entry, steps)
+    if want("filtered"):
+        _filtered(args, dev, entry, steps)
     if want("cache_hit"):
         out["cache_hit"] = _cache_hit(args, dev)
     return out
+
+
+def _filtered(args, dev, entry, steps):
+    """Filtered sampling (top_k = 50, top_p = 0.9) on the large workload's
+    shape: B=256, gamma=8, V=128256 fp32, T=1."""
+    from speculative_decoding_verification_temperature_gb300 import api
+    sets = []
+    for r in range(min(2, args.sets)):
+        c = synth.large(r, device=dev, B=B)
+        c.draft = c.draft[:, :GAMMA].contiguous()
+        sets.append(c)
+    fn = lambda c: api.verify_linear_filtered(c.target, c.draft, c.tokens,
+                                              c.uniforms, 1.0, 50, 0.9)
+    ms = _time(fn, sets, steps, 3, dev)
+    rows = np.mean([_rows_linear(fn(c)["n"].cpu().numpy(), GAMMA, False)
+                    for c in sets])
+    entry("filtered_k50_p0.9", ms, rows, V, ELT, B * (2 * GAMMA + 1),
+          {"top_k": 50, "top_p": 0.9, "T": 1.0})
+    del sets
 
 
 def uniform_schedule(K, budget):
@@ -585,7 +606,8 @@ def main():
     ap.add_argument("--impl", default="native",
                     choices=["native", "reference"])
     ap.add_argument("--only", default=None,
-                    choices=["tiny", "linear", "kcand", "tree", "cache_hit"],
+                    choices=["tiny", "linear", "kcand", "tree", "filtered",
+                             "cache_hit"],
                     help="time only this other workload (profiling runs); "
                          "no main line")
     ap.add_argument("--batch", type=int, default=256,

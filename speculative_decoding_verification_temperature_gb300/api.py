@@ -67,6 +67,9 @@ def _declare(L):
         "sd_verify_linear_static": ([P, P, I, P, P, I, I, I, F, P, P, P, P,
                                      P, P, P], I),
         "sd_fanout_hits": ([P, P, P, I, I, P, P, P], I),
+        "sd_verify_linear_filtered_workspace": ([I, I, I, I], Z),
+        "sd_verify_linear_filtered": ([P, P, I, P, P, I, I, I, F, I, F, P, P,
+                                       P, P, P, Z, P], I),
         "sd_verify_linear_fanout_workspace": ([I, I, I, I], Z),
         "sd_verify_linear_fanout": ([P, P, I, P, P, I, I, I, F, P, P, P, P,
                                      P, P, P, P, Z, P], I),
@@ -213,6 +216,34 @@ def verify_linear_static(target, draft, tokens, uniforms, T, *,
     if want_accept:
         r["accept"] = acc[:, :gamma]
     return r
+
+
+def verify_linear_filtered(target, draft, tokens, uniforms, T, top_k,
+                           top_p=1.0, *, status=None, workspace=None):
+    """Linear verify with top_k / top_p filtered sampling applied to p and q
+    before the ratio (sd_verify_linear_filtered); same shapes as
+    verify_linear.  Returns n, tokens, prob."""
+    dev = target.device
+    _dev(target, dev, "target")
+    B, G1, V = target.shape
+    gamma = G1 - 1
+    if draft is not None:
+        _dev(draft, dev, "draft", target.dtype)
+        if tuple(draft.shape) != (B, gamma, V):
+            raise ValueError("draft must be [B, gamma, V]")
+    tokens = _dev(tokens, dev, "tokens", torch.int32)
+    uniforms = _dev(uniforms, dev, "uniforms", torch.float32)
+    n = torch.empty(B, dtype=torch.int32, device=dev)
+    toks = torch.empty((B, G1), dtype=torch.int32, device=dev)
+    prob = torch.empty(B, dtype=torch.float32, device=dev)
+    L = lib()
+    nbytes = L.sd_verify_linear_filtered_workspace(B, gamma, V, _dt(target))
+    ws = (workspace or _default_ws).get(dev, nbytes)
+    _check(L.sd_verify_linear_filtered(
+        _p(target), _p(draft), _dt(target), _p(tokens), _p(uniforms), B,
+        gamma, V, float(T), int(top_k), float(top_p), _p(n), _p(toks),
+        _p(prob), _p(status), _p(ws), ws.numel(), _stream(dev)))
+    return {"n": n, "tokens": toks, "prob": prob}
 
 
 def verify_kcand(target, draft, tokens, uniforms, T, *, status=None,

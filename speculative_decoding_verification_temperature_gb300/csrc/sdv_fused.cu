@@ -227,7 +227,7 @@ __device__ __forceinline__ void d_vec(MS &q, WarpFilter &wf, uint32_t *cta_th,
   }
   if constexpr (FILT) {
     wf.nseen = max_nan(wf.nseen, vmax);
-    if (__builtin_expect(!wf.seeded, 0)) wf_seed(wf, vmax);
+    if (__builtin_expect(!wf.seeded, 0)) wf_seed_vec<VW>(wf, z);
     if (__builtin_expect(__any_sync(0xffffffffu, vmax >= wf.th), 0)) {
 #pragma unroll
       for (int e = 0; e < VW; ++e) {
@@ -408,18 +408,16 @@ __global__ void __launch_bounds__(kThreads, SDV_FUSED_MINB)
               // seed every warp's threshold from the whole first chunk: the
               // CTA takes the largest value that F lane maxima of one warp
               // reach, so the warps start from a common high threshold
-              float lm = -__builtin_huge_valf();
+              float m1 = -__builtin_huge_valf(), m2 = -__builtin_huge_valf();
               for (int base = warp * 32; base < cn; base += kThreads) {
                 const int i = base + lane;
                 if (i < cn) {
                   const Raw<DT, VW> r = sget<DT, VW>(A, i);
-                  float z[VW];
 #pragma unroll
-                  for (int e = 0; e < VW; ++e) z[e] = elt<DT, VW>(r, e);
-                  lm = max_nan(lm, vmax_nan_of<VW>(z));
+                  for (int e = 0; e < VW; ++e) top2_add(m1, m2, elt<DT, VW>(r, e));
                 }
               }
-              wf_seed(wf, lm);
+              wf_seed2(wf, m1, m2);
               if (lane == 0 && wf.th > -__builtin_huge_valf())
                 atomicMax(&sh.top.th, ord32(wf.th));
               __syncthreads();

@@ -115,19 +115,42 @@ __device__ __forceinline__ void wf_sync(WarpFilter &w, const uint32_t *cta_th) {
   if (o != 0) w.th = fmaxf(w.th, unord32(o));
 }
 
-// Seed the threshold from the lanes' vector maxima m (-inf for idle lanes,
-// NaN never counts): the largest m that at least F lanes reach.  Full warp.
-__device__ __forceinline__ void wf_seed(WarpFilter &w, float m) {
+// Seed the threshold from each lane's largest value m1 and second largest
+// m2 among its first elements (-inf for none; NaN never counts): the
+// largest value s such that at least F of those elements reach it.  With
+// F <= 32 the candidates are the m1 (F lanes reach s); with F > 32 the m2,
+// counting both values of every lane.  Full warp.
+__device__ __forceinline__ void wf_seed2(WarpFilter &w, float m1, float m2) {
   w.seeded = true;
-  if (w.two) return;
+  const float cand = w.two ? m2 : m1;
   int c = 0;
 #pragma unroll 8
-  for (int j = 0; j < 32; ++j) c += __shfl_sync(0xffffffffu, m, j) >= m;
-  float s = c >= w.F ? m : -__builtin_huge_valf();
+  for (int j = 0; j < 32; ++j) {
+    const float a = __shfl_sync(0xffffffffu, m1, j);
+    c += a >= cand;
+    if (w.two) c += __shfl_sync(0xffffffffu, m2, j) >= cand;
+  }
+  float s = c >= w.F ? cand : -__builtin_huge_valf();
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1)
     s = fmaxf(s, __shfl_xor_sync(0xffffffffu, s, o));
   w.th = fmaxf(w.th, s);
+}
+
+// Fold value z into a lane's two largest values (m1 >= m2; NaN skipped).
+__device__ __forceinline__ void top2_add(float &m1, float &m2, float z) {
+  const float lo = fminf(m1, z);  // fminf/fmaxf drop a NaN operand
+  m1 = fmaxf(m1, z);
+  m2 = fmaxf(m2, lo);
+}
+
+// The per-round seed: the lane's vector maxima.
+template <int VW>
+__device__ __forceinline__ void wf_seed_vec(WarpFilter &w, const float (&z)[VW]) {
+  float m1 = -__builtin_huge_valf(), m2 = -__builtin_huge_valf();
+#pragma unroll
+  for (int e = 0; e < VW; ++e) top2_add(m1, m2, z[e]);
+  wf_seed2(w, m1, m2);
 }
 
 // Offer one vector per lane (ok = false for idle lanes); j0 is the token id
@@ -142,7 +165,7 @@ __device__ __forceinline__ void wf_offer(WarpFilter &w, uint32_t *cta_th,
     z[e] = ok ? elt<DT, VW>(r, e) : -__builtin_huge_valf();
   const float vmax = vmax_nan_of<VW>(z);  // NaN: never >= th
   w.nseen = max_nan(w.nseen, vmax);
-  if (__builtin_expect(!w.seeded, 0)) wf_seed(w, vmax);
+  if (__builtin_expect(!w.seeded, 0)) wf_seed_vec<VW>(w, z);
   if (__builtin_expect(__any_sync(0xffffffffu, vmax >= w.th), 0)) {
 #pragma unroll
     for (int e = 0; e < VW; ++e) {
