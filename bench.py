@@ -137,20 +137,38 @@ def workload_name():
     return WORKLOAD.replace("B=256", "B=%d (profiling case)" % B)
 
 
-def make_sets(nsets, device):
+def make_sets(nsets, device, rank=0):
+    """The rotated input sets of one rank (each rank verifies its own
+    batches)."""
     sets = []
     for s in range(nsets):
-        c = synth.large(s, device=device, B=B)
+        c = synth.large(s + 16 * rank, device=device, B=B)
         c.draft_v = c.draft[:, :GAMMA].contiguous()
         sets.append(c)
     return sets
+
+
+def max_over_ranks(ms, world, dev):
+    """The timed region's length as the slowest rank saw it."""
+    if world <= 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(steps, total_ms, world):
+    """Rounds per second of the whole job: every rank verifies its own batch
+    each step (replicas, weak scaling), so world * steps rounds took
+    total_ms (the slowest rank's time)."""
+    return world * steps / (total_ms / 1e3)
 
 
 def gpu_arm(args, rank, world):
     from speculative_decoding_verification_temperature_gb300 import api
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
-    sets = make_sets(args.sets, dev)
+    sets = make_sets(args.sets, dev, rank)
     stream = torch.cuda.current_stream(dev)
     ws = api.Workspace()
     F = api.fanout_schedule(FAN["K"], FAN["budget"], FAN["a"], FAN["r"])
@@ -196,15 +214,11 @@ def gpu_arm(args, rank, world):
     per = [e[0].elapsed_time(e[2]) for e in ev]       # ms per step (device)
     per_v = [e[0].elapsed_time(e[1]) for e in ev]     # of which verify
     per_f = [e[1].elapsed_time(e[2]) for e in ev]     # of which fan-out
-    total_ms = sum(per)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(per), world, dev)
     ms = total_ms / args.steps
     ms_v = sum(per_v) / args.steps
     ms_f = sum(per_f) / args.steps
-    rounds_s = world * args.steps / (total_ms / 1e3)
+    rounds_s = whole_job_rate(args.steps, total_ms, world)
     avg = lambda xs: sum(xs[i % len(sets)] for i in range(args.steps)) / args.steps
     need_avg, need_v_avg = avg(need), avg(need_v)
     fan_bytes = B * (FAN["K"] + 1) * V * ELT
