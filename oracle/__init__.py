@@ -52,6 +52,8 @@ def _bind(path):
                                      P, P, P, P, P, P, P, P, P, P]
     lib.orc_verify_tree.argtypes = [P, P, I, P, P, P, I, I, I, D,
                                     P, P, P, P, P, P, P, P, P]
+    lib.orc_verify_tree_det.argtypes = [P, I, P, P, P, I, I, I, D,
+                                        P, P, P, P, P, P, P, P, P]
     lib.orc_fanout_schedule.argtypes = [I, I, D, D, P]
     lib.orc_fanout_topk.argtypes = [P, I, I, I, I, P, P, P, P]
     lib.orc_fanout_hits.argtypes = [P, P, P, P, I, I, P]
@@ -267,6 +269,33 @@ def verify_tree(target, draft, parent, node_tokens, uniforms, T):
         _ptr(uniforms), B, N, V, float(T), _ptr(out["n"]),
         _ptr(out["tokens"]), _ptr(out["nodes"]), _ptr(out["prob"]),
         *_margin_ptrs(m), _ptr(out["status"]))
+    if rc:
+        raise MemoryError("oracle allocation failed")
+    return _finish(out, m)
+
+
+def verify_tree_det(target, parent, node_tokens, uniforms, T):
+    """Token-tree verify with deterministic drafts: child v is accepted with
+    the current p(t_v); a rejected token is removed from p, which is
+    renormalised.  target [B, N, V]; the rest as verify_tree."""
+    target, dt = _logits(target)
+    B, N, V = target.shape
+    parent = np.ascontiguousarray(parent, np.int32).reshape(B, N)
+    node_tokens = np.ascontiguousarray(node_tokens, np.int32).reshape(B, N)
+    uniforms = np.ascontiguousarray(uniforms, np.float32).reshape(B, N)
+    out = {
+        "n": np.empty(B, np.int32),
+        "tokens": np.empty((B, N), np.int32),
+        "nodes": np.empty((B, N), np.int32),
+        "prob": np.empty(B, np.float64),
+        "status": np.empty(B, np.int32),
+    }
+    m = _margins(B)
+    rc = _load().orc_verify_tree_det(
+        _ptr(target), dt, _ptr(parent), _ptr(node_tokens), _ptr(uniforms),
+        B, N, V, float(T), _ptr(out["n"]), _ptr(out["tokens"]),
+        _ptr(out["nodes"]), _ptr(out["prob"]), *_margin_ptrs(m),
+        _ptr(out["status"]))
     if rc:
         raise MemoryError("oracle allocation failed")
     return _finish(out, m)

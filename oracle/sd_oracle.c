@@ -23,6 +23,9 @@
  *    the candidate with the longest accepted streak.
  *  - PRESTO, section 2.1 "tree-based speculative decoding": prefix-wise
  *    verification from the root, acceptance factorised along the path.
+ *  - SpecDiff-2, "core method", greedy acceptance: a drafted token is
+ *    accepted with the verifier's probability of it, independently of the
+ *    drafter, and a rejected position is resampled from the residual.
  *  - Speculative Speculative Decoding / Saguaro, "speculation cache
  *    strategy": Definition 11 (power-law cache miss) and Theorem 12
  *    (geometric fan-out F_k = F_0 a^{k/(1+r)}, capped at position K), and
@@ -52,6 +55,10 @@
  *  - tree siblings are tried in increasing node index against the fixed
  *    draft row of their parent, with p <- norm(max(0, p - q)) after each
  *    rejection; the final draw of a tree uses uniform slot 0;
+ *  - greedy acceptance is read as Algorithm 1 with the draft distribution
+ *    the point mass on the drafted token (the deterministic-draft tree
+ *    rule): accept iff r <= p(x), residual = p with x removed and
+ *    renormalised, siblings tried in increasing node index;
  *  - kcand selection: the largest accepted count, ties to the lowest k; the
  *    final draw uses uniform slot [b][k*][gamma];
  *  - fan-out integerisation: floor of F_0 w_k, the remainder handed out by
@@ -827,5 +834,108 @@ int orc_verify_linear_filtered(const void *target, const void *draft,
     status[b] = st;
   }
   free(p); free(q); free(w); free(e);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------
+ * Tree verify with deterministic drafts (SpecDiff-2, "greedy acceptance":
+ * each drafted token is accepted with the verifier's probability of it,
+ * independently of the drafter; on rejection the token is resampled from
+ * the verifier's residual).  This is the tree rule above with the draft
+ * distribution of child v replaced by the point mass on t_v: the ratio
+ * p(t_v)/1 is p(t_v), and norm(max(0, p - delta_{t_v})) is p with t_v
+ * removed and renormalised.  Arguments as orc_verify_tree, without draft.
+ * A child whose token was removed already has p(t_v) = 0.  A token out of
+ * range is rejected and removes nothing.
+ * ---------------------------------------------------------------------- */
+int orc_verify_tree_det(const void *target, int dtype, const int32_t *parent,
+                        const int32_t *node_tokens, const float *uniforms,
+                        int B, int N, int V, double T, int32_t *n_acc,
+                        int32_t *out_tokens, int32_t *out_nodes,
+                        double *out_prob, double *margin_acc,
+                        double *margin_cdf, int32_t *cdf_lo, int32_t *cdf_hi,
+                        int32_t *status) {
+  double *p = malloc(sizeof(double) * (size_t)V);
+  if (!p) return 1;
+  for (int b = 0; b < B; ++b) {
+    const int32_t *par = parent + (size_t)b * N;
+    const int32_t *tok = node_tokens + (size_t)b * N;
+    const float *U = uniforms + (size_t)b * N;
+    int st = 0, invalid = 0, depth = 0, t = -1, lo = -1, hi = -1;
+    double mg = INFINITY, mc = INFINITY, prob = 0.0;
+    for (int i = 0; i < N; ++i) {
+      out_nodes[(size_t)b * N + i] = -1;
+      out_tokens[(size_t)b * N + i] = -1;
+    }
+    if (par[0] != -1) invalid = 4;
+    for (int v = 1; v < N && !invalid; ++v)
+      if (par[v] < 0 || par[v] >= v) invalid = 4;
+    int cur = 0;
+    while (!invalid) {
+      size_t off = ((size_t)b * N + cur) * (size_t)V;
+      int next = -1;
+      if (T == 0.0) {
+        int a = argmax_row(target, dtype, off, V);
+        if (a < 0) { invalid = 2; break; }
+        for (int v = cur + 1; v < N; ++v) {
+          if (par[v] != cur) continue;
+          if (tok[v] < 0 || tok[v] >= V) st |= ORC_ST_BAD_TOKEN;
+          if (tok[v] == a) { next = v; break; }
+        }
+        if (next < 0) { t = a; prob = 1.0; lo = hi = a; break; }
+      } else {
+        if (!softmax_row(target, dtype, off, V, T, p)) { invalid = 2; break; }
+        int zero_mass = 0;
+        for (int v = cur + 1; v < N && !zero_mass; ++v) {
+          if (par[v] != cur) continue;
+          int x = tok[v];
+          if (x < 0 || x >= V) { st |= ORC_ST_BAD_TOKEN; continue; }
+          double rho = p[x];
+          note_margin(&mg, fabs((double)U[v] - rho));
+          if ((double)U[v] <= rho) { next = v; break; }
+          /* rejected: remove x and renormalise */
+          p[x] = 0.0;
+          double S = 0.0;
+          for (int j = 0; j < V; ++j) S += p[j];
+          if (S == 0.0) {
+            st |= ORC_ST_ZERO_MASS;
+            softmax_row(target, dtype, off, V, T, p);
+            zero_mass = 1;
+          } else {
+            for (int j = 0; j < V; ++j) p[j] /= S;
+          }
+        }
+        if (next < 0) {
+          t = sample_icdf(p, V, (double)U[0], &prob, &mc, &lo, &hi);
+          break;
+        }
+      }
+      out_nodes[(size_t)b * N + depth] = next;
+      out_tokens[(size_t)b * N + depth] = tok[next];
+      ++depth;
+      cur = next;
+    }
+    if (invalid) {
+      st |= invalid == 4 ? ORC_ST_BAD_PARENT : ORC_ST_NONFINITE;
+      for (int i = 0; i < N; ++i) {
+        out_nodes[(size_t)b * N + i] = -1;
+        out_tokens[(size_t)b * N + i] = -1;
+      }
+      n_acc[b] = -1;
+      prob = 0.0;
+      mg = mc = INFINITY;
+      lo = hi = -1;
+    } else {
+      n_acc[b] = depth;
+      out_tokens[(size_t)b * N + depth] = t;
+    }
+    out_prob[b] = prob;
+    margin_acc[b] = (T == 0.0) ? INFINITY : mg;
+    margin_cdf[b] = (T == 0.0) ? INFINITY : mc;
+    cdf_lo[b] = lo;
+    cdf_hi[b] = hi;
+    status[b] = st;
+  }
+  free(p);
   return 0;
 }

@@ -87,6 +87,19 @@ MUTANTS = [
     ("topk_tie_order", "return (a->idx > b->idx) - (a->idx < b->idx);",
      "return (a->idx < b->idx) - (a->idx > b->idx);", 1,
      ["test_fanout_topk_against_stable_sort_and_ties"]),
+    ("det_accept_direction", "if ((double)U[v] <= rho) { next = v; break; }",
+     "if ((double)U[v] >= rho) { next = v; break; }", 1,
+     ["test_tree_det_golden", "test_tree_det_topk_siblings_lossless"]),
+    ("det_rejected_token_kept", "p[x] = 0.0;", "p[x] = p[x];", 1,
+     ["test_tree_det_golden", "test_tree_det_quadrature_bruteforce"]),
+    ("det_not_renormalised", "for (int j = 0; j < V; ++j) p[j] /= S;",
+     "for (int j = 0; j < V; ++j) p[j] /= 1.0;", 2,
+     ["test_tree_det_topk_siblings_lossless",
+      "test_tree_det_quadrature_bruteforce"]),
+    ("det_child_reads_root_row",
+     "size_t off = ((size_t)b * N + cur) * (size_t)V;",
+     "size_t off = ((size_t)b * N + 0) * (size_t)V;", 2,
+     ["test_tree_det_two_level_joint_is_p", "test_tree_det_golden"]),
 ]
 
 

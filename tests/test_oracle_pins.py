@@ -668,3 +668,123 @@ def test_filtered_first_token_marginal_is_filtered_p(top_k, top_p):
     first = out["tokens"][:, 0]
     p0 = filtered(zt[0], T, top_k, top_p)
     assert chi2_p(np.bincount(first, minlength=V), p0) > P_MIN
+
+
+# ------------------------------- deterministic drafts (greedy acceptance)
+def test_tree_det_golden():
+    """Hand-worked trees of tests/golden/tree_deterministic_drafts.json."""
+    g = _golden("tree_deterministic_drafts.json")
+    rows = np.log(np.array([g["rows"][f"p{i}"] for i in range(4)]))
+    for ex in g["cases"]:
+        o = oracle.verify_tree_det(
+            rows.astype(np.float32)[None], np.array([g["parent"]], np.int32),
+            np.array([ex["node_tokens"]], np.int32),
+            np.array([ex["uniforms"]], np.float32), g["T"])
+        assert o["n"][0] == ex["n"], ex["why"]
+        np.testing.assert_array_equal(o["tokens"][0], ex["tokens"])
+        np.testing.assert_array_equal(o["nodes"][0], ex["nodes"])
+        np.testing.assert_allclose(o["prob"][0], ex["prob"], atol=1e-6)
+
+
+def _one_hot_logits(tok, V):
+    z = np.full(V, -np.inf)
+    if 0 <= tok < V:
+        z[tok] = 0.0
+    return z
+
+
+@pytest.mark.parametrize("T", [0.6, 1.0])
+def test_tree_det_chain_equals_tree_rule_with_point_mass_drafts(T):
+    """On a chain (one child per node) the deterministic-draft rule is the
+    sibling rule of the tree verify with q of every node the point mass on
+    its child's token (logits 0 there, -inf elsewhere): accept iff
+    U <= p(x)/1, residual max(0, p - delta_x) renormalised."""
+    c = synth.linear_case(200, 5, 97, T=T, seed=131)
+    tg, dr = synth.host_logits(c.target), synth.host_logits(c.draft)
+    xs, u = c.tokens.numpy(), c.uniforms.numpy()
+    target, _, parent, ntok, uni = chain_tree_from_linear(tg, dr, xs, u)
+    B, N, V = target.shape
+    onehot = np.zeros((B, N, V), np.float32)
+    for b in range(B):
+        for v in range(N - 1):  # node v's only child is node v + 1
+            onehot[b, v] = _one_hot_logits(ntok[b, v + 1], V)
+    ot = oracle.verify_tree(target, onehot, parent, ntok, uni, T)
+    od = oracle.verify_tree_det(target, parent, ntok, uni, T)
+    np.testing.assert_array_equal(od["n"], ot["n"])
+    np.testing.assert_array_equal(od["tokens"], ot["tokens"])
+    np.testing.assert_array_equal(od["nodes"], ot["nodes"])
+    np.testing.assert_allclose(od["prob"], ot["prob"], rtol=1e-12)
+
+
+def test_tree_det_topk_siblings_lossless():
+    """Deterministic top-k siblings (the case the sibling rule with a fixed
+    q gets wrong, above) keep the emitted token's marginal equal to p under
+    the deterministic-draft rule.  V = 8, the root's children are the three
+    most likely draft tokens, 1e6 trials, chi-square."""
+    rng = np.random.default_rng(133)
+    V, S, B = 8, 3, 1_000_000
+    zt = rng.normal(0, 1.5, V)
+    zq = zt + rng.normal(0, 1.2, V)
+    top = np.argsort(-zq, kind="stable")[:S].astype(np.int32)
+    tg = tile_rows([zt] + [rng.normal(0, 1, V)] * S, B)
+    parent = np.tile(np.array([-1] + [0] * S, np.int32), (B, 1))
+    ntok = np.tile(np.concatenate([[-1], top]).astype(np.int32), (B, 1))
+    o = oracle.verify_tree_det(tg, parent, ntok,
+                               synth.uniforms(134, (B, S + 1)), 1.0)
+    assert chi2_p(np.bincount(o["tokens"][:, 0], minlength=V),
+                  softmax(zt)) > P_MIN
+
+
+def test_tree_det_two_level_joint_is_p():
+    """Two levels of deterministic children with distinct target rows per
+    node: the pair (first, second) emitted tokens has the law
+    p_root(a) p_a(b), where p_a is the row of a's node when a was drafted
+    and the root's row p_root(b | a) is irrelevant otherwise.  Root with
+    children tokens 0, 1; each with children tokens 2, 0; V = 4; 1e6
+    trials, chi-square over the 16 pairs."""
+    rng = np.random.default_rng(135)
+    V, B = 4, 1_000_000
+    # nodes: 0 root; 1 (tok 0), 2 (tok 1) under the root; 3, 4 under 1;
+    # 5, 6 under 2 (tokens 2, 0)
+    parent = np.array([-1, 0, 0, 1, 1, 2, 2], np.int32)
+    ntok = np.array([-1, 0, 1, 2, 0, 2, 0], np.int32)
+    rows = rng.normal(0, 1.0, (7, V))
+    # the row after a prefix that was not drafted: a fresh row per prefix
+    # is what the target would give; rows 3..6 are leaves whose row is the
+    # distribution of the token after two, irrelevant for the pair law
+    o = oracle.verify_tree_det(tile_rows(rows, B), np.tile(parent, (B, 1)),
+                               np.tile(ntok, (B, 1)),
+                               synth.uniforms(136, (B, 7)), 1.0)
+    p0 = softmax(rows[0])
+    n = o["n"]
+    a = o["tokens"][:, 0]
+    b = o["tokens"][:, 1]
+    # the second token's law given a: node 1's row for a = 0, node 2's for
+    # a = 1; otherwise (a not drafted) the second token is not emitted
+    drafted = np.isin(a, [0, 1])
+    assert np.all((n >= 1) == drafted)
+    pairs = a[drafted] * V + b[drafted]
+    law = np.zeros(V * V)
+    for tok, node in ((0, 1), (1, 2)):
+        law[tok * V:(tok + 1) * V] = p0[tok] * softmax(rows[node])
+    law /= law.sum()
+    assert chi2_p(np.bincount(pairs, minlength=V * V), law) > P_MIN
+    assert chi2_p(np.bincount(a, minlength=V), p0) > P_MIN
+
+
+def test_tree_det_quadrature_bruteforce():
+    """Exact marginal by quadrature: V = 3, two children (tokens 2, 0),
+    uniforms on a G x G x G grid of cell midpoints.  Each decision is a
+    threshold on one coordinate, so the grid estimate of P(first token = y)
+    is within 3/G of the true value, which must be p."""
+    G = 64
+    p = np.array([0.5, 0.2, 0.3])
+    g = (np.arange(G) + 0.5) / G
+    U = np.stack(np.meshgrid(g, g, g, indexing="ij"), -1).reshape(-1, 3)
+    B = U.shape[0]
+    tg = tile_rows(np.log(np.stack([p, p, p])), B)
+    parent = np.tile(np.array([-1, 0, 0], np.int32), (B, 1))
+    ntok = np.tile(np.array([-1, 2, 0], np.int32), (B, 1))
+    o = oracle.verify_tree_det(tg, parent, ntok, U.astype(np.float32), 1.0)
+    est = np.bincount(o["tokens"][:, 0], minlength=3) / B
+    np.testing.assert_allclose(est, p, atol=3.0 / G)
