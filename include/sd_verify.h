@@ -229,6 +229,36 @@ sd_status sd_verify_tree(const void *target_logits, const void *draft_logits,
                          void *workspace, size_t ws_bytes, void *stream);
 
 /* ---------------------------------------------------------------------
+ * Token-tree verify with deterministic drafts (SpecDiff-2, "core method",
+ * greedy acceptance: each drafted token is accepted with the verifier's
+ * probability of it, independently of the drafter, and a rejection is
+ * resampled from the verifier's residual).  This is the tree rule of
+ * sd_verify_tree with the draft distribution of every child the point mass
+ * on its token: child v is accepted iff uniforms[b][v] <= p'(t_v), where
+ * p' is softmax(target row / T) with the tokens of the rejected siblings
+ * removed and renormalised; a child whose token was removed already has
+ * p'(t_v) = 0; a token outside [0, V) is rejected, removes nothing and sets
+ * SD_DEV_BAD_TOKEN.  When every child is rejected, or at a leaf, the last
+ * token is drawn from p' by inverse CDF with uniforms[b][0].  Lossless for
+ * any deterministic choice of children (top-k trees included).  T == 0 is
+ * the greedy walk of sd_verify_tree.
+ *
+ * Arguments, layouts, outputs, ownership and errors as sd_verify_tree,
+ * without draft_logits (no draft row is read).  A removed mass that leaves
+ * nothing falls back to p and sets SD_DEV_ZERO_MASS.
+ * ------------------------------------------------------------------- */
+size_t sd_verify_tree_det_workspace(int B, int N, int V, sd_dtype dt);
+
+sd_status sd_verify_tree_det(const void *target_logits, sd_dtype dt,
+                             const int32_t *parent,
+                             const int32_t *node_tokens,
+                             const float *uniforms, int B, int N, int V,
+                             float T, int32_t *n_accepted,
+                             int32_t *out_tokens, int32_t *out_nodes,
+                             float *out_prob, int32_t *dev_status,
+                             void *workspace, size_t ws_bytes, void *stream);
+
+/* ---------------------------------------------------------------------
  * Geometric fan-out schedule (Saguaro, Theorem 12).  Host only.
  * F (host) [K+1]: F_0 w_k made integer by largest remainder (ties to the
  * lower k); sum F == budget.  Requires 0 <= K <= SD_MAX_K, budget >= 0,

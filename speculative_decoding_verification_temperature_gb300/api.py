@@ -61,6 +61,9 @@ def _declare(L):
         "sd_verify_tree_workspace": ([I, I, I, I], Z),
         "sd_verify_tree": ([P, P, I, P, P, P, I, I, I, F, P, P, P, P, P, P,
                             Z, P], I),
+        "sd_verify_tree_det_workspace": ([I, I, I, I], Z),
+        "sd_verify_tree_det": ([P, I, P, P, P, I, I, I, F, P, P, P, P, P, P,
+                                Z, P], I),
         "sd_fanout_schedule": ([I, I, D, D, P], I),
         "sd_fanout_topk_workspace": ([I, I, I, I], Z),
         "sd_fanout_topk": ([P, I, I, I, I, P, P, P, P, P, Z, P], I),
@@ -302,6 +305,31 @@ def verify_tree(target, draft, parent, node_tokens, uniforms, T, *,
         _p(target), _p(draft), _dt(target), _p(parent), _p(node_tokens),
         _p(uniforms), B, N, V, float(T), _p(n), _p(toks), _p(nodes),
         _p(prob), _p(status), _p(ws), ws.numel(), _stream(dev)))
+    return {"n": n, "tokens": toks, "nodes": nodes, "prob": prob}
+
+
+def verify_tree_det(target, parent, node_tokens, uniforms, T, *,
+                    status=None, workspace=None):
+    """Token-tree verify with deterministic drafts (sd_verify_tree_det):
+    child v accepted with the current p(t_v), a rejected token removed from
+    p.  target [B, N, V]; the rest as verify_tree."""
+    dev = target.device
+    _dev(target, dev, "target")
+    B, N, V = target.shape
+    parent = _dev(parent, dev, "parent", torch.int32)
+    node_tokens = _dev(node_tokens, dev, "node_tokens", torch.int32)
+    uniforms = _dev(uniforms, dev, "uniforms", torch.float32)
+    n = torch.empty(B, dtype=torch.int32, device=dev)
+    toks = torch.empty((B, N), dtype=torch.int32, device=dev)
+    nodes = torch.empty((B, N), dtype=torch.int32, device=dev)
+    prob = torch.empty(B, dtype=torch.float32, device=dev)
+    L = lib()
+    nbytes = L.sd_verify_tree_det_workspace(B, N, V, _dt(target))
+    ws = (workspace or _default_ws).get(dev, nbytes)
+    _check(L.sd_verify_tree_det(
+        _p(target), _dt(target), _p(parent), _p(node_tokens), _p(uniforms),
+        B, N, V, float(T), _p(n), _p(toks), _p(nodes), _p(prob), _p(status),
+        _p(ws), ws.numel(), _stream(dev)))
     return {"n": n, "tokens": toks, "nodes": nodes, "prob": prob}
 
 

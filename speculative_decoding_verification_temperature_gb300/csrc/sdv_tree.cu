@@ -55,14 +55,116 @@ struct TreeSmem {
   int tok[SD_MAX_TREE_NODES];
   float uni[SD_MAX_TREE_NODES];
   int kids[SD_MAX_TREE_NODES];
-  float gzt[SD_MAX_TREE_NODES], gzd[SD_MAX_TREE_NODES];
+  float gzt[SD_MAX_TREE_NODES];
+  union {
+    float gzd[SD_MAX_TREE_NODES];  // draft logits of the children's tokens
+    int ex[SD_MAX_TREE_NODES];     // deterministic drafts: removed tokens
+  };
   int path[SD_MAX_TREE_NODES];
   int nkids;
   int next_seq[2];
   DrawSmem draw;
 };
 
-template <int DT, int VW, bool GREEDY, bool TMA>
+// Deterministic drafts.  The weights are p over the row without the
+// removed tokens ex[0..ne).  mass_pass sums every token; the segments that
+// hold a removed token are then summed again without them (one warp per
+// segment), so every mass stays a sum of non-negative terms.
+__device__ __forceinline__ bool is_removed(const int *ex, int ne, int j) {
+  bool r = false;
+  for (int i = 0; i < ne; ++i) r |= ex[i] == j;
+  return r;
+}
+
+template <int DT, int VW, class Row>
+__device__ __forceinline__ void det_weights(const Row &ra, const Weight &W,
+                                            const int *ex, int ne, int v,
+                                            float (&w)[VW]) {
+  const Raw<DT, VW> a = ra.get(v);
+  weights<DT, VW>(a, a, false, W, w);
+#pragma unroll
+  for (int e = 0; e < VW; ++e)
+    if (is_removed(ex, ne, v * VW + e)) w[e] = 0.f;
+}
+
+template <int DT, int VW, class Row>
+__device__ void det_fill(const Row &ra, const Weight &W, const Slice &sl,
+                         float *segmass, const int *ex, int ne) {
+  mass_pass<DT, VW>(ra, ra, false, W, sl, segmass);
+  if (ne == 0) return;
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  auto seg_of = [&](int j) {  // segment of token j in this slice, or -1
+    const int v = j / VW;
+    return (v >= sl.vbeg && v < sl.vend) ? (v - sl.vbeg) / 32 : -1;
+  };
+  for (int i = warp; i < ne; i += kWarps) {
+    const int s = seg_of(ex[i]);
+    bool first = s >= 0;  // the first removed token of its segment redoes it
+    for (int r = 0; r < i && first; ++r) first = seg_of(ex[r]) != s;
+    if (!first) continue;  // warp-uniform
+    const int v = sl.vbeg + s * 32 + lane;
+    float acc = 0.f;
+    if (v < sl.vend) {
+      float w[VW];
+      det_weights<DT, VW>(ra, W, ex, ne, v, w);
+#pragma unroll
+      for (int e = 0; e < VW; ++e) acc += w[e];
+    }
+    acc = warp_down_sum(acc);
+    if (lane == 0) segmass[s] = acc;
+  }
+}
+
+template <int DT, int VW, class Row>
+__device__ double det_mass(cg::cluster_group &cluster, DrawSmem &ds,
+                           float *segmass, const Row &ra, const Weight &W,
+                           const Slice &sl, const int *ex, int ne, float u,
+                           int &par) {
+  return cluster_total(cluster, ds, segmass, sl, u, par, [&] {
+    det_fill<DT, VW>(ra, W, sl, segmass, ex, ne);
+  });
+}
+
+// Inverse-CDF draw from p without the removed tokens (cluster-wide, every
+// thread of every CTA calls it; see cluster_draw).
+template <int DT, int VW, class Row>
+__device__ DrawOut det_draw(cg::cluster_group &cluster, DrawSmem &ds,
+                            float *segmass, const Row &ra, const Weight &W,
+                            const Slice &sl, const int *ex, int ne, float u,
+                            int &par) {
+  det_mass<DT, VW>(cluster, ds, segmass, ra, W, sl, ex, ne, u, par);
+  const int tid = threadIdx.x;
+  const int rank = (int)cluster.block_rank();
+  DrawOut out;
+  out.N = ds.N;
+  out.owner = ds.owner;
+  out.t = -1;
+  out.wt = 0.f;
+  if (out.owner == rank) {
+    if (tid == 0) {
+      double tin = 0.0;
+      ds.seg = find_segment(segmass, sl.nseg, ds.chunk_pre, ds.tau, &tin);
+      ds.tau_seg = (float)tin;
+    }
+    __syncthreads();
+    if (tid < 32) {
+      const int s = ds.seg;
+      const int v = sl.vbeg + s * 32 + tid;
+      float w[VW];
+      if (v < sl.vend) {
+        det_weights<DT, VW>(ra, W, ex, ne, v, w);
+      } else {
+#pragma unroll
+        for (int e = 0; e < VW; ++e) w[e] = 0.f;
+      }
+      out.t = warp_pick<VW>(w, ds.tau_seg, (sl.vbeg + s * 32) * VW, &out.wt);
+    }
+  }
+  return out;
+}
+
+template <int DT, int VW, bool GREEDY, bool TMA, bool DET>
 __global__ void __launch_bounds__(kThreads, 2)
     tree_verify_kernel(const TreeParams p) {
   extern __shared__ __align__(128) unsigned char dsm[];
@@ -136,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       __syncthreads();
       const int nk = sh.nkids;
-      const bool has_q = (!GREEDY) && nk > 0;
+      const bool has_q = (!GREEDY) && (!DET) && nk > 0;
       const char *trow = tbase + ((size_t)b * N + cur) * rowb;
       const char *drow = dbase + ((size_t)b * N + cur) * rowb;
       if (TMA && tid == 0) {
@@ -153,10 +255,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         float zt = 0.f, zd = 0.f;
         if (!GREEDY && x >= 0 && x < V) {
           zt = load_logit<DT>(trow, x);
-          zd = load_logit<DT>(drow, x);
+          if (!DET) zd = load_logit<DT>(drow, x);
         }
         sh.gzt[i] = zt;
-        sh.gzd[i] = zd;
+        if (!DET) sh.gzd[i] = zd;
       }
       if (TMA) {
         mbar_wait(&bar, phase, p.dev_status);
@@ -221,6 +323,63 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (next < 0) {
           t = a;
           prob = 1.f;
+          break;
+        }
+      } else if constexpr (DET) {
+        // deterministic drafts: child v is accepted iff U[v] <= p'(t_v),
+        // p' = p outside the tokens removed so far (sh.ex), renormalised
+        Weight W;
+        W.k2 = k2;
+        W.mtk = sh.mt.m * k2;
+        W.ist = 1.f / sh.mt.s;
+        W.mdk = 0.f;
+        W.cq = 0.f;
+        int ne = 0;
+        double Nr = 1.0;  // mass of p outside the removed tokens
+        bool zm = false;
+        for (int i = 0; i < nk; ++i) {
+          const int v = sh.kids[i];
+          const int x = sh.tok[v];
+          if (x < 0 || x >= V) continue;  // rejected, removes nothing
+          bool removed = false;
+          for (int r = 0; r < ne; ++r) removed |= sh.ex[r] == x;
+          const float wx =
+              removed ? 0.f
+                      : __fmul_rn(ex2(fmaf(sh.gzt[i], k2, -W.mtk)), W.ist);
+          const float rho = (float)((double)wx / Nr);
+          if (sh.uni[v] <= rho) {
+            next = v;
+            break;
+          }
+          if (removed) continue;
+          if (tid == 0) sh.ex[ne] = x;
+          ++ne;
+          if (i + 1 < nk) {  // (the final draw forms its own mass)
+            __syncthreads();
+            Nr = det_mass<DT, VW>(cluster, sh.draw, segmass, ra, W, sl,
+                                  sh.ex, ne, -1.f, par);
+            __syncthreads();
+            if (!(Nr > 0.0)) {
+              zm = true;
+              break;
+            }
+          }
+        }
+        if (next < 0) {
+          __syncthreads();
+          const float u = sh.uni[0];
+          DrawOut o = det_draw<DT, VW>(cluster, sh.draw, segmass, ra, W, sl,
+                                       sh.ex, zm ? 0 : ne, u, par);
+          if (o.owner < 0) {
+            zm = true;
+            __syncthreads();
+            o = det_draw<DT, VW>(cluster, sh.draw, segmass, ra, W, sl, sh.ex,
+                                 0, u, par);
+          }
+          zero_mass = zm;
+          writer = (o.owner == rank && warp == 0);
+          t = o.t;
+          prob = (float)((double)o.wt / o.N);
           break;
         }
       } else {
@@ -321,20 +480,22 @@ __global__ void __launch_bounds__(kThreads, 2)
 using TreeKernel = void (*)(const TreeParams);
 
 template <int DT, int VW, bool TMA>
-static TreeKernel pick_tree_t(bool greedy) {
-  return greedy ? tree_verify_kernel<DT, VW, true, TMA>
-                : tree_verify_kernel<DT, VW, false, TMA>;
+static TreeKernel pick_tree_t(bool greedy, bool det) {
+  if (greedy) return tree_verify_kernel<DT, VW, true, TMA, false>;
+  return det ? tree_verify_kernel<DT, VW, false, TMA, true>
+             : tree_verify_kernel<DT, VW, false, TMA, false>;
 }
 
-static TreeKernel pick_tree(int dt, bool vec, bool tma, bool greedy) {
+static TreeKernel pick_tree(int dt, bool vec, bool tma, bool greedy,
+                            bool det) {
   if (dt == SD_F32) {
-    if (!vec) return pick_tree_t<0, 1, false>(greedy);
-    return tma ? pick_tree_t<0, 4, true>(greedy)
-               : pick_tree_t<0, 4, false>(greedy);
+    if (!vec) return pick_tree_t<0, 1, false>(greedy, det);
+    return tma ? pick_tree_t<0, 4, true>(greedy, det)
+               : pick_tree_t<0, 4, false>(greedy, det);
   }
-  if (!vec) return pick_tree_t<1, 1, false>(greedy);
-  return tma ? pick_tree_t<1, 8, true>(greedy)
-             : pick_tree_t<1, 8, false>(greedy);
+  if (!vec) return pick_tree_t<1, 1, false>(greedy, det);
+  return tma ? pick_tree_t<1, 8, true>(greedy, det)
+             : pick_tree_t<1, 8, false>(greedy, det);
 }
 
 constexpr size_t kTreeTmaSmemMax = 96 * 1024;
@@ -349,12 +510,12 @@ extern "C" size_t sd_verify_tree_workspace(int B, int N, int V, sd_dtype dt) {
   return 256;
 }
 
-extern "C" sd_status sd_verify_tree(
+static sd_status tree_launch(
     const void *target_logits, const void *draft_logits, sd_dtype dt,
     const int32_t *parent, const int32_t *node_tokens, const float *uniforms,
-    int B, int N, int V, float T, int32_t *n_accepted, int32_t *out_tokens,
-    int32_t *out_nodes, float *out_prob, int32_t *dev_status,
-    void *workspace, size_t ws_bytes, void *stream) {
+    int B, int N, int V, float T, bool det, int32_t *n_accepted,
+    int32_t *out_tokens, int32_t *out_nodes, float *out_prob,
+    int32_t *dev_status, void *workspace, size_t ws_bytes, void *stream) {
   using namespace sdv;
   SDV_REQUIRE(dt == SD_F32 || dt == SD_BF16, "bad dtype %d", (int)dt);
   SDV_REQUIRE(B >= 0, "B < 0");
@@ -367,29 +528,31 @@ extern "C" sd_status sd_verify_tree(
   SDV_REQUIRE(target_logits && parent && node_tokens && n_accepted &&
                   out_tokens && out_nodes,
               "null pointer");
-  SDV_REQUIRE(T == 0.f || (uniforms && draft_logits),
+  SDV_REQUIRE(T == 0.f || (uniforms && (det || draft_logits)),
               "uniforms and draft_logits are required when T > 0");
   int sms = 0;
   sd_status st = check_device(&sms);
   if (st != SD_OK) return st;
   const bool greedy = (T == 0.f);
   const int eb = dt == SD_F32 ? 4 : 2, vw = dt == SD_F32 ? 4 : 8;
+  const bool one_row = greedy || det;  // no draft rows are read
   const bool vec = aligned16(target_logits) &&
-                   (greedy || aligned16(draft_logits)) &&
+                   (one_row || aligned16(draft_logits)) &&
                    ((size_t)V * eb) % 16 == 0;
   const long long nvec = V / (vec ? vw : 1);
   const int CL = choose_cluster(nvec);
   const long long per_cta = (nvec + CL - 1) / CL;
   const size_t seg_bytes =
       ((size_t)((per_cta + 31) / 32) * 4 + 127) / 128 * 128;
-  const size_t tma_smem = seg_bytes + 2 * (size_t)per_cta * 16;
+  const size_t tma_smem =
+      seg_bytes + (one_row ? 1 : 2) * (size_t)per_cta * 16;
   const bool tma = vec && tma_smem <= kTreeTmaSmemMax &&
                    env_int("SDV_NO_TMA", 0) == 0;
   const size_t smem = tma ? tma_smem : seg_bytes;
   if (smem > 96 * 1024)
     return fail(SD_ERR_UNSUPPORTED, "V=%d needs %zu B of shared memory", V,
                 smem);
-  TreeKernel kern = pick_tree(dt, vec, tma, greedy);
+  TreeKernel kern = pick_tree(dt, vec, tma, greedy, det);
   int maxc = 0;
   st = max_active_clusters((const void *)kern, CL, smem, &maxc);
   if (st != SD_OK) return st;
@@ -422,4 +585,33 @@ extern "C" sd_status sd_verify_tree(
   }
   void *args[] = {&prm};
   return launch_clusters((const void *)kern, nclusters, CL, smem, s, args);
+}
+
+extern "C" sd_status sd_verify_tree(
+    const void *target_logits, const void *draft_logits, sd_dtype dt,
+    const int32_t *parent, const int32_t *node_tokens, const float *uniforms,
+    int B, int N, int V, float T, int32_t *n_accepted, int32_t *out_tokens,
+    int32_t *out_nodes, float *out_prob, int32_t *dev_status,
+    void *workspace, size_t ws_bytes, void *stream) {
+  return tree_launch(target_logits, draft_logits, dt, parent, node_tokens,
+                     uniforms, B, N, V, T, false, n_accepted, out_tokens,
+                     out_nodes, out_prob, dev_status, workspace, ws_bytes,
+                     stream);
+}
+
+extern "C" size_t sd_verify_tree_det_workspace(int B, int N, int V,
+                                               sd_dtype dt) {
+  return sd_verify_tree_workspace(B, N, V, dt);
+}
+
+extern "C" sd_status sd_verify_tree_det(
+    const void *target_logits, sd_dtype dt, const int32_t *parent,
+    const int32_t *node_tokens, const float *uniforms, int B, int N, int V,
+    float T, int32_t *n_accepted, int32_t *out_tokens, int32_t *out_nodes,
+    float *out_prob, int32_t *dev_status, void *workspace, size_t ws_bytes,
+    void *stream) {
+  return tree_launch(target_logits, nullptr, dt, parent, node_tokens,
+                     uniforms, B, N, V, T, true, n_accepted, out_tokens,
+                     out_nodes, out_prob, dev_status, workspace, ws_bytes,
+                     stream);
 }
