@@ -529,13 +529,29 @@ def _tree(args, dev, entry, steps):
     fn = lambda c: api.verify_tree(c.target, c.draft, c.parent,
                                    c.node_tokens, c.uniforms, 0.8)
     ms = _time(fn, sets, steps, 3, dev)
-    rows = []
+    rows, acc = [], []
     for c in sets:
         o = fn(c)
         rows.append(_rows_tree(c.parent.cpu().numpy(),
                                o["nodes"].cpu().numpy(),
                                o["n"].cpu().numpy(), False))
-    entry("tree", ms, np.mean(rows), 151936, 2, 16 * 128)
+        acc.append(float(o["n"].float().mean()))
+    entry("tree", ms, np.mean(rows), 151936, 2, 16 * 128,
+          {"mean_accepted": float(np.mean(acc))})
+    # the same top-k trees under the deterministic-draft rule (greedy
+    # acceptance): target rows of the visited nodes only
+    fd = lambda c: api.verify_tree_det(c.target, c.parent, c.node_tokens,
+                                       c.uniforms, 0.8)
+    ms = _time(fd, sets, steps, 3, dev)
+    rows, acc = [], []
+    for c in sets:
+        o = fd(c)
+        rows.append(_rows_tree(c.parent.cpu().numpy(),
+                               o["nodes"].cpu().numpy(),
+                               o["n"].cpu().numpy(), True))
+        acc.append(float(o["n"].float().mean()))
+    entry("tree_deterministic", ms, np.mean(rows), 151936, 2, 16 * 64,
+          {"mean_accepted": float(np.mean(acc))})
     del sets
 
 

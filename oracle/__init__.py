@@ -54,6 +54,7 @@ def _bind(path):
                                     P, P, P, P, P, P, P, P, P]
     lib.orc_verify_tree_det.argtypes = [P, I, P, P, P, I, I, I, D,
                                         P, P, P, P, P, P, P, P, P]
+    lib.orc_kcand_trie.argtypes = [P, P, I, I, I, P, P, P, P, P, P, P]
     lib.orc_fanout_schedule.argtypes = [I, I, D, D, P]
     lib.orc_fanout_topk.argtypes = [P, I, I, I, I, P, P, P, P]
     lib.orc_fanout_hits.argtypes = [P, P, P, P, I, I, P]
@@ -299,6 +300,62 @@ def verify_tree_det(target, parent, node_tokens, uniforms, T):
     if rc:
         raise MemoryError("oracle allocation failed")
     return _finish(out, m)
+
+
+def kcand_trie(tokens, uniforms):
+    """K candidates as one token tree (orc_kcand_trie).  tokens [B, K,
+    gamma] int32, uniforms [B, K, gamma+1] float32.  Returns the tree's
+    parent, node_tokens, uniforms, target_row, draft_row, node_cand and
+    is_dup, each [B, 1 + K gamma]."""
+    tokens = np.ascontiguousarray(tokens, np.int32)
+    B, K, gamma = tokens.shape
+    uniforms = np.ascontiguousarray(uniforms, np.float32).reshape(
+        B, K, gamma + 1)
+    N = 1 + K * gamma
+    out = {k: np.empty((B, N), np.int32) for k in
+           ("parent", "node_tokens", "target_row", "draft_row", "node_cand",
+            "is_dup")}
+    out["uniforms"] = np.empty((B, N), np.float32)
+    if _load().orc_kcand_trie(
+            _ptr(tokens), _ptr(uniforms), B, K, gamma, _ptr(out["parent"]),
+            _ptr(out["node_tokens"]), _ptr(out["uniforms"]),
+            _ptr(out["target_row"]), _ptr(out["draft_row"]),
+            _ptr(out["node_cand"]), _ptr(out["is_dup"])):
+        raise MemoryError("oracle allocation failed")
+    return out
+
+
+def verify_kcand_trie(target, draft, tokens, uniforms, T):
+    """K candidates verified as one token tree: the tree of kcand_trie with
+    node u's target row target[b].reshape(K (gamma+1), V)[target_row] and
+    draft row draft[b][draft_row] (zeros for none), through verify_tree.
+    target [B, K, gamma+1, V], draft [B, gamma, V] (None when T == 0).
+    Returns verify_tree's outputs, tokens cut to [B, gamma+1], and sel_k:
+    node_cand of the last accepted node (0 when none was accepted)."""
+    target, dt = _logits(target)
+    B, K, G1, V = target.shape
+    gamma = G1 - 1
+    tr = kcand_trie(tokens, uniforms)
+    N = 1 + K * gamma
+    rows_b = np.arange(B)[:, None]
+    tt = np.ascontiguousarray(
+        target.reshape(B, K * G1, V)[rows_b, tr["target_row"]])
+    dd = np.zeros((B, N, V), target.dtype)
+    if draft is not None:
+        draft, dt2 = _logits(draft)
+        if dt2 != dt or draft.shape != (B, gamma, V):
+            raise ValueError("draft must be [B, gamma, V] of target's dtype")
+        has = tr["draft_row"] >= 0
+        dd[has] = draft[rows_b, np.maximum(tr["draft_row"], 0)][has]
+    o = verify_tree(tt, dd, tr["parent"], tr["node_tokens"], tr["uniforms"],
+                    T)
+    o["tokens"] = np.ascontiguousarray(o["tokens"][:, :G1])
+    n = o["n"]
+    last = np.where(n > 0, o["nodes"][np.arange(B), np.maximum(n - 1, 0)], 0)
+    o["sel_k"] = np.where(n >= 0, tr["node_cand"][np.arange(B), last],
+                          -1).astype(np.int32)
+    o["trie"] = tr
+    return o
 
 
 def fanout_schedule(K, budget, a, r):

@@ -59,6 +59,11 @@
  *    the point mass on the drafted token (the deterministic-draft tree
  *    rule): accept iff r <= p(x), residual = p with x removed and
  *    renormalised, siblings tried in increasing node index;
+ *  - K candidates as one tree: candidate k's token at position j is node
+ *    1 + j K + k, below the node of its prefix; a token repeated under the
+ *    same prefix is a leaf duplicate (the sibling rule must see every iid
+ *    draw) and the candidate continues below the first copy; a node takes
+ *    the target row of the candidate that created it;
  *  - kcand selection: the largest accepted count, ties to the lowest k; the
  *    final draw uses uniform slot [b][k*][gamma];
  *  - fan-out integerisation: floor of F_0 w_k, the remainder handed out by
@@ -937,5 +942,78 @@ int orc_verify_tree_det(const void *target, int dtype, const int32_t *parent,
     status[b] = st;
   }
   free(p);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------
+ * K candidates verified as one token tree (the multi-draft reading of
+ * SpecDiff-2's K iid candidates from shared position-wise marginals, with
+ * PRESTO section 2.1's prefix-wise tree verification).  Candidate k's
+ * token at position j (tokens [B, K, gamma]) is one node, N = 1 + K gamma
+ * nodes per sequence, created position by position and, within a
+ * position, in increasing k:
+ *  - its parent is the node of candidate k's prefix (the root for j = 0);
+ *  - if an earlier candidate with the same prefix has the same token at j,
+ *    the node is a leaf duplicate (a repeated iid draw, kept so that the
+ *    sibling rule sees every draw) and candidate k continues below the
+ *    earlier candidate's node;
+ *  - otherwise it is the node of the prefix through position j, with
+ *    target row (k, j + 1) and draft row j + 1 (none at j + 1 == gamma).
+ * The root has target row (0, 0) and draft row 0.  A duplicate copies the
+ * rows of the node it repeats.  Node (k, j) tests with uniforms[b][k][j];
+ * the final draw (tree slot 0) uses uniforms[b][0][gamma].  node_cand is
+ * the candidate that created the node (the lowest k through a non-duplicate
+ * node).  Row indices: target_row into the K (gamma + 1) rows of sequence
+ * b (k (gamma + 1) + j), draft_row into its gamma rows, -1 for none.
+ * ---------------------------------------------------------------------- */
+int orc_kcand_trie(const int32_t *tokens, const float *uniforms, int B, int K,
+                   int gamma, int32_t *parent, int32_t *node_tokens,
+                   float *node_uniforms, int32_t *target_row,
+                   int32_t *draft_row, int32_t *node_cand, int32_t *is_dup) {
+  const int N = 1 + K * gamma, G1 = gamma + 1;
+  int *at = malloc(sizeof(int) * (size_t)(K > 0 ? K : 1));
+  if (!at) return 1;
+  for (int b = 0; b < B; ++b) {
+    int32_t *par = parent + (size_t)b * N, *tok = node_tokens + (size_t)b * N;
+    float *U = node_uniforms + (size_t)b * N;
+    int32_t *tr = target_row + (size_t)b * N, *dr = draft_row + (size_t)b * N;
+    int32_t *nc = node_cand + (size_t)b * N, *dup = is_dup + (size_t)b * N;
+    const int32_t *x = tokens + (size_t)b * K * gamma;
+    const float *u = uniforms + (size_t)b * K * G1;
+    par[0] = -1;
+    tok[0] = -1;
+    U[0] = u[gamma]; /* candidate 0, slot gamma */
+    tr[0] = 0;
+    dr[0] = gamma > 0 ? 0 : -1;
+    nc[0] = 0;
+    dup[0] = 0;
+    for (int k = 0; k < K; ++k) at[k] = 0;
+    int v = 1;
+    for (int j = 0; j < gamma; ++j) {
+      const int first = v; /* nodes of position j start here */
+      for (int k = 0; k < K; ++k, ++v) {
+        const int t = x[(size_t)k * gamma + j];
+        int same = -1; /* an earlier non-duplicate node: same parent, token */
+        for (int w = first; w < v && same < 0; ++w)
+          if (!dup[w] && par[w] == at[k] && tok[w] == t) same = w;
+        par[v] = at[k];
+        tok[v] = t;
+        U[v] = u[(size_t)k * G1 + j];
+        nc[v] = k;
+        if (same >= 0) {
+          dup[v] = 1;
+          tr[v] = tr[same];
+          dr[v] = dr[same];
+          at[k] = same;
+        } else {
+          dup[v] = 0;
+          tr[v] = k * G1 + j + 1;
+          dr[v] = j + 1 < gamma ? j + 1 : -1;
+          at[k] = v;
+        }
+      }
+    }
+  }
+  free(at);
   return 0;
 }

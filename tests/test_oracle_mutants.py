@@ -100,6 +100,16 @@ MUTANTS = [
      "size_t off = ((size_t)b * N + cur) * (size_t)V;",
      "size_t off = ((size_t)b * N + 0) * (size_t)V;", 2,
      ["test_tree_det_two_level_joint_is_p", "test_tree_det_golden"]),
+    ("trie_duplicate_below_its_twin", "dup[v] = 1;\n          tr[v]",
+     "dup[v] = 1; par[v] = same;\n          tr[v]", 1,
+     ["test_kcand_trie_golden",
+      "test_kcand_trie_lossless_first_and_second_token"]),
+    ("trie_target_row_off_by_one", "tr[v] = k * G1 + j + 1;",
+     "tr[v] = k * G1 + j;", 1,
+     ["test_kcand_trie_one_candidate_equals_linear",
+      "test_kcand_trie_lossless_first_and_second_token"]),
+    ("trie_final_uniform_slot", "U[0] = u[gamma];", "U[0] = u[0];", 1,
+     ["test_kcand_trie_one_candidate_equals_linear"]),
 ]
 
 
@@ -124,6 +134,7 @@ def _run_pin(name):
         "test_bruteforce_enumeration": [dict(V=3, gamma=3),
                                         dict(V=5, gamma=2)],
         "test_tree_chain_equals_linear": [dict(T=1.0)],
+        "test_kcand_trie_one_candidate_equals_linear": [dict(T=1.0)],
         "test_filtered_first_token_marginal_is_filtered_p": [
             dict(top_k=5, top_p=1.0), dict(top_k=4, top_p=0.6)],
     }.get(name, [dict()])

@@ -788,3 +788,76 @@ def test_tree_det_quadrature_bruteforce():
     o = oracle.verify_tree_det(tg, parent, ntok, U.astype(np.float32), 1.0)
     est = np.bincount(o["tokens"][:, 0], minlength=3) / B
     np.testing.assert_allclose(est, p, atol=3.0 / G)
+
+
+# ------------------------------ K candidates verified as one token tree
+def test_kcand_trie_golden():
+    """Hand-worked construction of tests/golden/kcand_trie.json."""
+    g = _golden("kcand_trie.json")
+    o = oracle.kcand_trie(np.array([g["tokens"]], np.int32),
+                          np.array([g["uniforms"]], np.float32))
+    for k in ("parent", "node_tokens", "target_row", "draft_row",
+              "node_cand", "is_dup"):
+        np.testing.assert_array_equal(o[k][0], g[k], err_msg=k)
+    np.testing.assert_array_equal(o["uniforms"][0],
+                                  np.float32(g["uniforms_out"]))
+
+
+@pytest.mark.parametrize("T", [0.0, 1.0])
+def test_kcand_trie_one_candidate_equals_linear(T):
+    """With K = 1 the tree is the candidate's chain, its tests use the
+    candidate's uniforms and the final draw its slot gamma: the linear
+    verify exactly."""
+    c = synth.linear_case(200, 5, 131, T=T, seed=141)
+    tg, dr = synth.host_logits(c.target), synth.host_logits(c.draft)
+    xs, u = c.tokens.numpy(), c.uniforms.numpy()
+    ol = oracle.verify_linear(tg, dr, xs, u, T)
+    ok = oracle.verify_kcand_trie(tg[:, None], None if T == 0 else dr,
+                                  xs[:, None], u[:, None], T)
+    np.testing.assert_array_equal(ok["n"], ol["n"])
+    np.testing.assert_array_equal(ok["tokens"], ol["tokens"])
+    np.testing.assert_allclose(ok["prob"], ol["prob"], rtol=1e-12)
+    assert np.all(ok["sel_k"] == 0)
+
+
+def _trie_law_case(B, seed):
+    """K = 4 iid candidates from shared marginals q_0, q_1 (V = 6, gamma =
+    2); target rows that depend on the prefix only: p_0 at position 0, row
+    P1[a] after first token a, a fixed row at position 2."""
+    rng = np.random.default_rng(seed)
+    V, K, gamma = 6, 4, 2
+    z0 = rng.normal(0, 1.5, V)
+    Z1 = rng.normal(0, 1.5, (V, V))
+    z2 = rng.normal(0, 1.0, V)
+    q0 = rng.normal(0, 1.5, V)
+    q1 = rng.normal(0, 1.5, V)
+    x = np.stack([np.stack([draw_from(softmax(q), B, seed + 10 * k + j)
+                            for j, q in enumerate((q0, q1))], 1)
+                  for k in range(K)], 1)  # [B, K, gamma]
+    target = np.empty((B, K, gamma + 1, V), np.float32)
+    target[:, :, 0] = z0
+    target[:, :, 1] = Z1[x[:, :, 0]]
+    target[:, :, 2] = z2
+    draft = np.ascontiguousarray(
+        np.broadcast_to(np.stack([q0, q1]).astype(np.float32),
+                        (B, gamma, V)))
+    U = synth.uniforms(seed + 99, (B, K, gamma + 1))
+    return z0, Z1, target, draft, x.astype(np.int32), U
+
+
+def test_kcand_trie_lossless_first_and_second_token():
+    """Lossless: the first emitted token follows p_0, and the second,
+    given an accepted first token a, follows P1[a] (chi-square, 3e5
+    sequences)."""
+    B = 300_000
+    z0, Z1, target, draft, x, U = _trie_law_case(B, 143)
+    o = oracle.verify_kcand_trie(target, draft, x, U, 1.0)
+    V = len(z0)
+    assert chi2_p(np.bincount(o["tokens"][:, 0], minlength=V),
+                  softmax(z0)) > P_MIN
+    acc = o["n"] >= 1
+    a, b = o["tokens"][acc, 0], o["tokens"][acc, 1]
+    na = np.bincount(a, minlength=V)
+    law = (na[:, None] * np.stack([softmax(Z1[i]) for i in range(V)]))
+    assert chi2_p(np.bincount(a * V + b, minlength=V * V),
+                  (law / law.sum()).ravel()) > P_MIN
