@@ -518,7 +518,21 @@ def _kcand(args, dev, entry, steps):
         o = fn(c)
         rows.append(_rows_kcand(o["n_per_cand"].cpu().numpy(),
                                 o["n"].cpu().numpy(), 16))
-    entry("kcand", ms, np.mean(rows), 152064, 2, 64 * (8 * 17 + 16))
+    acc = [float(fn(c)["n"].float().mean()) for c in sets]
+    entry("kcand", ms, np.mean(rows), 152064, 2, 64 * (8 * 17 + 16),
+          {"mean_accepted": float(np.mean(acc))})
+    # the same candidates verified as one token tree (distribution-
+    # preserving): target and draft rows of the visited nodes
+    ft = lambda c: api.verify_kcand_trie(c.target, c.draft, c.tokens,
+                                         c.uniforms, 1.0)
+    ms = _time(ft, sets, steps, 3, dev)
+    rows, acc = [], []
+    for c in sets:
+        n = ft(c)["n"].cpu().numpy().astype(np.int64)
+        rows.append(int(((n + 1) + np.minimum(n + 1, 16)).sum()))
+        acc.append(float(n.mean()))
+    entry("kcand_trie", ms, np.mean(rows), 152064, 2, 64 * (8 * 17 + 16),
+          {"mean_accepted": float(np.mean(acc))})
     del sets
 
 

@@ -229,6 +229,42 @@ sd_status sd_verify_tree(const void *target_logits, const void *draft_logits,
                          void *workspace, size_t ws_bytes, void *stream);
 
 /* ---------------------------------------------------------------------
+ * K candidate drafts verified as one token tree (SpecDiff-2, "core
+ * method": K candidates drawn independently from the shared position-wise
+ * marginals; PRESTO section 2.1: a token tree is verified prefix-wise from
+ * the root).  Unlike sd_verify_kcand's self-selection, the output is
+ * distributed as the target.
+ *
+ * Arguments as sd_verify_kcand (target_logits [B, K, gamma+1, V],
+ * draft_logits [B, gamma, V], draft_tokens [B, K, gamma], uniforms
+ * [B, K, gamma+1]), with K <= 32 and 1 + K gamma <= SD_MAX_TREE_NODES.
+ * The tree: candidate k's token at position j is node 1 + j K + k, below
+ * the node of its prefix (node 0, the root, for j = 0).  A token repeating
+ * an earlier candidate's token under the same prefix is a leaf duplicate
+ * and that candidate continues below the first copy; any other node reads
+ * target row (k, j+1) and draft row j+1.  The root reads target row (0, 0)
+ * and draft row 0.  The walk is sd_verify_tree's: node (k, j) tests with
+ * uniforms[b][k][j], the final draw uses uniforms[b][0][gamma].
+ * Outputs: n_accepted [B], out_tokens [B, gamma+1] (accepted tokens, the
+ *   final token, -1 padding), selected_k [B] (nullable: the candidate that
+ *   created the last accepted node, 0 when none was accepted, -1 for an
+ *   invalid sequence), out_prob [B] (nullable).
+ * Workspace: sd_verify_kcand_trie_workspace bytes (the tree, 24 B a node).
+ * ------------------------------------------------------------------- */
+size_t sd_verify_kcand_trie_workspace(int B, int K, int gamma, int V,
+                                      sd_dtype dt);
+
+sd_status sd_verify_kcand_trie(const void *target_logits,
+                               const void *draft_logits, sd_dtype dt,
+                               const int32_t *draft_tokens,
+                               const float *uniforms, int B, int K,
+                               int gamma, int V, float T,
+                               int32_t *n_accepted, int32_t *selected_k,
+                               int32_t *out_tokens, float *out_prob,
+                               int32_t *dev_status, void *workspace,
+                               size_t ws_bytes, void *stream);
+
+/* ---------------------------------------------------------------------
  * Token-tree verify with deterministic drafts (SpecDiff-2, "core method",
  * greedy acceptance: each drafted token is accepted with the verifier's
  * probability of it, independently of the drafter, and a rejection is

@@ -330,7 +330,7 @@ def verify_kcand_trie(target, draft, tokens, uniforms, T):
     node u's target row target[b].reshape(K (gamma+1), V)[target_row] and
     draft row draft[b][draft_row] (zeros for none), through verify_tree.
     target [B, K, gamma+1, V], draft [B, gamma, V] (None when T == 0).
-    Returns verify_tree's outputs, tokens cut to [B, gamma+1], and sel_k:
+    Returns verify_tree's outputs, tokens cut to [B, gamma+1], and k:
     node_cand of the last accepted node (0 when none was accepted)."""
     target, dt = _logits(target)
     B, K, G1, V = target.shape
@@ -341,7 +341,7 @@ def verify_kcand_trie(target, draft, tokens, uniforms, T):
     tt = np.ascontiguousarray(
         target.reshape(B, K * G1, V)[rows_b, tr["target_row"]])
     dd = np.zeros((B, N, V), target.dtype)
-    if draft is not None:
+    if draft is not None and gamma > 0:
         draft, dt2 = _logits(draft)
         if dt2 != dt or draft.shape != (B, gamma, V):
             raise ValueError("draft must be [B, gamma, V] of target's dtype")
@@ -352,7 +352,7 @@ def verify_kcand_trie(target, draft, tokens, uniforms, T):
     o["tokens"] = np.ascontiguousarray(o["tokens"][:, :G1])
     n = o["n"]
     last = np.where(n > 0, o["nodes"][np.arange(B), np.maximum(n - 1, 0)], 0)
-    o["sel_k"] = np.where(n >= 0, tr["node_cand"][np.arange(B), last],
+    o["k"] = np.where(n >= 0, tr["node_cand"][np.arange(B), last],
                           -1).astype(np.int32)
     o["trie"] = tr
     return o

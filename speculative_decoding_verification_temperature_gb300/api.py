@@ -58,6 +58,9 @@ def _declare(L):
         "sd_verify_kcand_workspace": ([I, I, I, I, I], Z),
         "sd_verify_kcand": ([P, P, I, P, P, I, I, I, I, F, P, P, P, P, P, P,
                              P, Z, P], I),
+        "sd_verify_kcand_trie_workspace": ([I, I, I, I, I], Z),
+        "sd_verify_kcand_trie": ([P, P, I, P, P, I, I, I, I, F, P, P, P, P,
+                                  P, P, Z, P], I),
         "sd_verify_tree_workspace": ([I, I, I, I], Z),
         "sd_verify_tree": ([P, P, I, P, P, P, I, I, I, F, P, P, P, P, P, P,
                             Z, P], I),
@@ -278,6 +281,36 @@ def verify_kcand(target, draft, tokens, uniforms, T, *, status=None,
         gamma, V, float(T), _p(n), _p(ks), _p(toks), _p(npc), _p(prob),
         _p(status), _p(ws), ws.numel(), _stream(dev)))
     return {"n": n, "k": ks, "tokens": toks, "n_per_cand": npc, "prob": prob}
+
+
+def verify_kcand_trie(target, draft, tokens, uniforms, T, *, status=None,
+                      workspace=None):
+    """K candidates verified as one token tree (sd_verify_kcand_trie).
+    Arguments as verify_kcand (draft may be None when T == 0).  Returns n,
+    k (the candidate that created the last accepted node), tokens
+    [B, gamma+1], prob."""
+    dev = target.device
+    _dev(target, dev, "target")
+    B, K, G1, V = target.shape
+    gamma = G1 - 1
+    if draft is not None:
+        _dev(draft, dev, "draft", target.dtype)
+        if tuple(draft.shape) != (B, gamma, V):
+            raise ValueError("draft must be [B, gamma, V]")
+    tokens = _dev(tokens, dev, "tokens", torch.int32)
+    uniforms = _dev(uniforms, dev, "uniforms", torch.float32)
+    n = torch.empty(B, dtype=torch.int32, device=dev)
+    ks = torch.empty(B, dtype=torch.int32, device=dev)
+    toks = torch.empty((B, G1), dtype=torch.int32, device=dev)
+    prob = torch.empty(B, dtype=torch.float32, device=dev)
+    L = lib()
+    nbytes = L.sd_verify_kcand_trie_workspace(B, K, gamma, V, _dt(target))
+    ws = (workspace or _default_ws).get(dev, nbytes)
+    _check(L.sd_verify_kcand_trie(
+        _p(target), _p(draft), _dt(target), _p(tokens), _p(uniforms), B, K,
+        gamma, V, float(T), _p(n), _p(ks), _p(toks), _p(prob), _p(status),
+        _p(ws), ws.numel(), _stream(dev)))
+    return {"n": n, "k": ks, "tokens": toks, "prob": prob}
 
 
 def verify_tree(target, draft, parent, node_tokens, uniforms, T, *,

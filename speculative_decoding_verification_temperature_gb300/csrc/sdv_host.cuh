@@ -59,4 +59,28 @@ sd_status max_active_clusters(const void *kernel, int cl, size_t smem,
 sd_status launch_clusters(const void *kernel, int nclusters, int cl,
                           size_t smem, cudaStream_t stream, void **args);
 
+// Row maps and output shape of a token tree whose nodes read rows of
+// another tensor (sdv_trie.cu): node u of sequence b reads target row
+// trow[b][u] of the sequence's trows rows and draft row drow[b][u] of its
+// drows rows (-1: none); out_tokens has out_cols columns; out_cand[b]
+// (nullable) gets node_cand[b][last accepted node], 0 when none.
+struct TreeMaps {
+  const int32_t *trow, *drow;
+  int trows, drows;
+  int out_cols;
+  const int32_t *node_cand;
+  int32_t *out_cand;
+};
+
+// The tree walk of sd_verify_tree (det = false) or sd_verify_tree_det
+// (det = true), with optional row maps (sdv_tree.cu).
+sd_status tree_launch(const void *target_logits, const void *draft_logits,
+                      sd_dtype dt, const int32_t *parent,
+                      const int32_t *node_tokens, const float *uniforms,
+                      int B, int N, int V, float T, bool det,
+                      int32_t *n_accepted, int32_t *out_tokens,
+                      int32_t *out_nodes, float *out_prob,
+                      int32_t *dev_status, void *workspace, size_t ws_bytes,
+                      void *stream, const TreeMaps *maps = nullptr);
+
 }  // namespace sdv

@@ -36,6 +36,14 @@ struct TreeParams {
   int B, N, V;
   float k2;
   int32_t *n_acc, *out_tokens, *out_nodes;
+  // Optional row maps (null: node u reads row u of its sequence's N rows):
+  // node u reads target row trow[b][u] of the sequence's trows rows and
+  // draft row drow[b][u] of its drows rows.
+  const int32_t *trow, *drow;
+  int trows, drows;
+  int out_cols;  // columns of out_tokens / out_nodes (<= N)
+  const int32_t *node_cand;  // optional: out_cand[b] = node_cand of the
+  int32_t *out_cand;         // last accepted node (0 when none)
   float *out_prob;
   int32_t *dev_status;
   int *queue;
@@ -239,8 +247,14 @@ __global__ void __launch_bounds__(kThreads, 2)
       __syncthreads();
       const int nk = sh.nkids;
       const bool has_q = (!GREEDY) && (!DET) && nk > 0;
-      const char *trow = tbase + ((size_t)b * N + cur) * rowb;
-      const char *drow = dbase + ((size_t)b * N + cur) * rowb;
+      const size_t tr_i =
+          p.trow ? (size_t)b * p.trows + p.trow[(size_t)b * N + cur]
+                 : (size_t)b * N + cur;
+      const size_t dr_i =
+          p.drow ? (size_t)b * p.drows + max(p.drow[(size_t)b * N + cur], 0)
+                 : (size_t)b * N + cur;
+      const char *trow = tbase + tr_i * rowb;
+      const char *drow = dbase + dr_i * rowb;
       if (TMA && tid == 0) {
         fence_proxy_async();
         mbar_expect_tx(&bar, slice_bytes * (has_q ? 2u : 1u));
@@ -446,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     const bool bad_seq = bad_parent || kind == 3;
     if (writer) {
-      for (int i = lane; i < N; i += 32) {
+      for (int i = lane; i < p.out_cols; i += 32) {
         int nd = -1, tk = -1;
         if (!bad_seq) {
           if (i < depth) {
@@ -456,11 +470,17 @@ __global__ void __launch_bounds__(kThreads, 2)
             tk = t;
           }
         }
-        p.out_nodes[(size_t)b * N + i] = nd;
-        p.out_tokens[(size_t)b * N + i] = tk;
+        if (p.out_nodes) p.out_nodes[(size_t)b * p.out_cols + i] = nd;
+        p.out_tokens[(size_t)b * p.out_cols + i] = tk;
       }
       if (lane == 0) {
         p.n_acc[b] = bad_seq ? -1 : depth;
+        if (p.out_cand)
+          p.out_cand[b] =
+              bad_seq ? -1
+                      : (depth ? p.node_cand[(size_t)b * N +
+                                             sh.path[depth - 1]]
+                               : 0);
         if (p.out_prob) p.out_prob[b] = bad_seq ? 0.f : prob;
         status_or(p.dev_status,
                   (bad_token ? SD_DEV_BAD_TOKEN : 0) |
@@ -500,6 +520,7 @@ static TreeKernel pick_tree(int dt, bool vec, bool tma, bool greedy,
 
 constexpr size_t kTreeTmaSmemMax = 96 * 1024;
 
+
 }  // namespace sdv
 
 extern "C" size_t sd_verify_tree_workspace(int B, int N, int V, sd_dtype dt) {
@@ -510,12 +531,13 @@ extern "C" size_t sd_verify_tree_workspace(int B, int N, int V, sd_dtype dt) {
   return 256;
 }
 
-static sd_status tree_launch(
+sd_status sdv::tree_launch(
     const void *target_logits, const void *draft_logits, sd_dtype dt,
     const int32_t *parent, const int32_t *node_tokens, const float *uniforms,
     int B, int N, int V, float T, bool det, int32_t *n_accepted,
     int32_t *out_tokens, int32_t *out_nodes, float *out_prob,
-    int32_t *dev_status, void *workspace, size_t ws_bytes, void *stream) {
+    int32_t *dev_status, void *workspace, size_t ws_bytes, void *stream,
+    const sdv::TreeMaps *maps) {
   using namespace sdv;
   SDV_REQUIRE(dt == SD_F32 || dt == SD_BF16, "bad dtype %d", (int)dt);
   SDV_REQUIRE(B >= 0, "B < 0");
@@ -526,7 +548,7 @@ static sd_status tree_launch(
   SDV_REQUIRE(T >= 0.f && std::isfinite(T), "T must be finite and >= 0");
   if (B == 0) return SD_OK;
   SDV_REQUIRE(target_logits && parent && node_tokens && n_accepted &&
-                  out_tokens && out_nodes,
+                  out_tokens && (out_nodes || maps),
               "null pointer");
   SDV_REQUIRE(T == 0.f || (uniforms && (det || draft_logits)),
               "uniforms and draft_logits are required when T > 0");
@@ -570,6 +592,13 @@ static sd_status tree_launch(
   prm.n_acc = n_accepted;
   prm.out_tokens = out_tokens;
   prm.out_nodes = out_nodes;
+  prm.trow = maps ? maps->trow : nullptr;
+  prm.drow = maps ? maps->drow : nullptr;
+  prm.trows = maps ? maps->trows : N;
+  prm.drows = maps ? maps->drows : N;
+  prm.out_cols = maps ? maps->out_cols : N;
+  prm.node_cand = maps ? maps->node_cand : nullptr;
+  prm.out_cand = maps ? maps->out_cand : nullptr;
   prm.out_prob = out_prob;
   prm.dev_status = dev_status;
   prm.queue = nullptr;
@@ -593,10 +622,10 @@ extern "C" sd_status sd_verify_tree(
     int B, int N, int V, float T, int32_t *n_accepted, int32_t *out_tokens,
     int32_t *out_nodes, float *out_prob, int32_t *dev_status,
     void *workspace, size_t ws_bytes, void *stream) {
-  return tree_launch(target_logits, draft_logits, dt, parent, node_tokens,
-                     uniforms, B, N, V, T, false, n_accepted, out_tokens,
-                     out_nodes, out_prob, dev_status, workspace, ws_bytes,
-                     stream);
+  return sdv::tree_launch(target_logits, draft_logits, dt, parent, node_tokens,
+                          uniforms, B, N, V, T, false, n_accepted,
+                          out_tokens, out_nodes, out_prob, dev_status,
+                          workspace, ws_bytes, stream);
 }
 
 extern "C" size_t sd_verify_tree_det_workspace(int B, int N, int V,
@@ -610,8 +639,8 @@ extern "C" sd_status sd_verify_tree_det(
     float T, int32_t *n_accepted, int32_t *out_tokens, int32_t *out_nodes,
     float *out_prob, int32_t *dev_status, void *workspace, size_t ws_bytes,
     void *stream) {
-  return tree_launch(target_logits, nullptr, dt, parent, node_tokens,
-                     uniforms, B, N, V, T, true, n_accepted, out_tokens,
-                     out_nodes, out_prob, dev_status, workspace, ws_bytes,
-                     stream);
+  return sdv::tree_launch(target_logits, nullptr, dt, parent, node_tokens,
+                          uniforms, B, N, V, T, true, n_accepted,
+                          out_tokens, out_nodes, out_prob, dev_status,
+                          workspace, ws_bytes, stream);
 }

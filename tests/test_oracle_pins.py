@@ -817,7 +817,7 @@ def test_kcand_trie_one_candidate_equals_linear(T):
     np.testing.assert_array_equal(ok["n"], ol["n"])
     np.testing.assert_array_equal(ok["tokens"], ol["tokens"])
     np.testing.assert_allclose(ok["prob"], ol["prob"], rtol=1e-12)
-    assert np.all(ok["sel_k"] == 0)
+    assert np.all(ok["k"] == 0)
 
 
 def _trie_law_case(B, seed):
