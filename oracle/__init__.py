@@ -55,6 +55,9 @@ def _bind(path):
     lib.orc_verify_tree_det.argtypes = [P, I, P, P, P, I, I, I, D,
                                         P, P, P, P, P, P, P, P, P]
     lib.orc_kcand_trie.argtypes = [P, P, I, I, I, P, P, P, P, P, P, P]
+    lib.orc_presto_expand.argtypes = [P, P, I, ctypes.c_longlong, I, I, I,
+                                      D, D, I, I, P, P, P, P, P, P, P, P]
+    lib.orc_branch_fork.argtypes = [P, I, P, I, I, D, I, P, P, P, P]
     lib.orc_fanout_schedule.argtypes = [I, I, D, D, P]
     lib.orc_fanout_topk.argtypes = [P, I, I, I, I, P, P, P, P]
     lib.orc_fanout_hits.argtypes = [P, P, P, P, I, I, P]
@@ -356,6 +359,68 @@ def verify_kcand_trie(target, draft, tokens, uniforms, T):
                           -1).astype(np.int32)
     o["trie"] = tr
     return o
+
+
+class PrestoTree:
+    """Host state of PRESTO trees under construction (the oracle's copy):
+    node arrays [B, budget] and the frontier [B, W].  Node 0 is the root
+    (parent -1, token -1, score 0) and the only frontier path."""
+
+    def __init__(self, B, W, budget):
+        self.B, self.W, self.budget = B, W, budget
+        self.n_nodes = np.ones(B, np.int32)
+        self.parent = np.full((B, budget), -1, np.int32)
+        self.node_tokens = np.full((B, budget), -1, np.int32)
+        self.node_score = np.zeros((B, budget), np.float64)
+        self.frontier_node = np.full((B, W), -1, np.int32)
+        self.frontier_node[:, 0] = 0
+        self.frontier_score = np.zeros((B, W), np.float64)
+        self.node_depth = np.zeros((B, budget), np.int32)
+
+
+def presto_expand(tree, q_logits, log_rho, T, lam, b_top):
+    """One depth of PRESTO's beam construction on `tree` (a PrestoTree,
+    updated in place).  q_logits [B, V] the drafter's marginal at this
+    depth; log_rho [B, W, V] the frontier paths' prefix signals.  Returns
+    (margin [B], status [B])."""
+    q_logits, dt = _logits(q_logits)
+    B, V = q_logits.shape
+    log_rho, dt2 = _logits(log_rho)
+    if dt2 != dt or log_rho.shape != (B, tree.W, V):
+        raise ValueError("log_rho must be [B, W, V] of q's dtype")
+    margin = np.empty(B, np.float64)
+    status = np.empty(B, np.int32)
+    n_before = tree.n_nodes.copy()
+    if _load().orc_presto_expand(
+            _ptr(q_logits), _ptr(log_rho), dt, V, B, tree.W, V, float(T),
+            float(lam), int(b_top), tree.budget, _ptr(tree.n_nodes),
+            _ptr(tree.parent), _ptr(tree.node_tokens),
+            _ptr(tree.node_score), _ptr(tree.frontier_node),
+            _ptr(tree.frontier_score), _ptr(margin), _ptr(status)):
+        raise ValueError("bad PRESTO arguments")
+    for b in range(B):
+        for v in range(max(n_before[b], 0), max(tree.n_nodes[b], 0)):
+            tree.node_depth[b, v] = tree.node_depth[b, tree.parent[b, v]] + 1
+    return margin, status
+
+
+def branch_fork(draft, x_b, T, k_max):
+    """SpecBranch fork: k = max(1, floor(k_max (1 - q(x_b)))) (capped at V)
+    and the top-k tokens of each draft row.  draft [B, V]; x_b [B].
+    Returns k [B], tokens [B, k_max] (-1 padded), margin, status."""
+    draft, dt = _logits(draft)
+    B, V = draft.shape
+    x_b = np.ascontiguousarray(x_b, np.int32).reshape(B)
+    out = {"k": np.empty(B, np.int32),
+           "tokens": np.empty((B, k_max), np.int32),
+           "margin": np.empty(B, np.float64),
+           "status": np.empty(B, np.int32)}
+    if _load().orc_branch_fork(_ptr(draft), dt, _ptr(x_b), B, V, float(T),
+                               int(k_max), _ptr(out["k"]),
+                               _ptr(out["tokens"]), _ptr(out["margin"]),
+                               _ptr(out["status"])):
+        raise ValueError("bad fork arguments")
+    return out
 
 
 def fanout_schedule(K, budget, a, r):

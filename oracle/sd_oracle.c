@@ -23,6 +23,12 @@
  *    the candidate with the longest accepted streak.
  *  - PRESTO, section 2.1 "tree-based speculative decoding": prefix-wise
  *    verification from the root, acceptance factorised along the path.
+ *  - PRESTO, section 4.1 (prefix-aligned score s = log q_d + lambda log
+ *    rho_d, path score S(P), Eq. 10), section 4.2 and Algorithm 1 (beam
+ *    search with global retention under a node budget), section 4.4 (the
+ *    score is the log of the KL-regularised proxy q rho^lambda / Z).
+ *  - SpecBranch, branch resampling: k = max(1, floor(k_max (1 - q(x_b))))
+ *    branches, the Top-k of the draft distribution at the branch point.
  *  - SpecDiff-2, "core method", greedy acceptance: a drafted token is
  *    accepted with the verifier's probability of it, independently of the
  *    drafter, and a rejected position is resampled from the residual.
@@ -64,6 +70,15 @@
  *    same prefix is a leaf duplicate (the sibling rule must see every iid
  *    draw) and the candidate continues below the first copy; a node takes
  *    the target row of the candidate that created it;
+ *  - PRESTO construction, one depth per call: each frontier path proposes
+ *    its b tokens of largest s (ties to the lower id, s = -inf excluded);
+ *    all proposals are ordered by (S + s desc, path slot asc, token asc)
+ *    and added while the budget lasts; the first W added form the next
+ *    frontier; rho is given (log rho rows), its learned predictor is not
+ *    part of this;
+ *  - SpecBranch fork: q(x_b) is the drafted token's probability under
+ *    softmax(z / T) (the point mass on the argmax at T == 0); k is capped
+ *    at V; the branches are ordered by (logit desc, id asc);
  *  - kcand selection: the largest accepted count, ties to the lowest k; the
  *    final draw uses uniform slot [b][k*][gamma];
  *  - fan-out integerisation: floor of F_0 w_k, the remainder handed out by
@@ -1015,5 +1030,177 @@ int orc_kcand_trie(const int32_t *tokens, const float *uniforms, int B, int K,
     }
   }
   free(at);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------
+ * PRESTO tree construction, one depth ("PRESTO", section 4.1: the
+ * prefix-aligned score s_{d,t}(c_d) = log q_d(t) + lambda_d log rho_d(t |
+ * c_d) and the path score S(P), Eq. 10, the sum of s along the path;
+ * section 4.2 and its Algorithm 1: beam search with global retention under
+ * a node budget).  One call expands depth d of every sequence's tree:
+ *  - the frontier holds up to W paths (frontier_node[b][w] >= 0, their
+ *    path scores frontier_score[b][w]); path w's prefix signal is the row
+ *    log_rho[b][w] (log rho, <= 0; -inf for rho = 0);
+ *  - path w proposes its b_top tokens of largest s (ties to the lower id),
+ *    tokens with s = -inf excluded, each with candidate score S_w + s;
+ *  - all candidates of the sequence are ordered by (score desc, w asc,
+ *    token asc) and the first min(count, budget - n_nodes) become nodes
+ *    n_nodes, n_nodes + 1, ... (parent: the path's node);
+ *  - the new frontier is the first min(W, added) of them, in that order.
+ * log q_d is log softmax(z / T) of the drafter's marginal row q_logits[b]
+ * (row stride q_stride elements).  A NaN or +inf in a row read makes the
+ * sequence invalid: n_nodes = -1, frontier cleared (status 2).  margin[b]
+ * is the smallest score gap that decided the outcome: at each path's top-b
+ * cut, and between consecutive candidates of the merged order up to one
+ * past the last added (INFINITY when nothing was decided).
+ * ---------------------------------------------------------------------- */
+#define SD_ORC_MAX_W 64
+typedef struct { double s; int w, tok; } orc_cand;
+
+static int cand_cmp(const void *x, const void *y) {
+  const orc_cand *a = x, *b = y;
+  if (a->s != b->s) return a->s < b->s ? 1 : -1;
+  if (a->w != b->w) return a->w - b->w;
+  return a->tok - b->tok;
+}
+
+int orc_presto_expand(const void *q_logits, const void *log_rho, int dtype,
+                      long long q_stride, int B, int W, int V, double T,
+                      double lambda, int b_top, int budget, int32_t *n_nodes,
+                      int32_t *parent, int32_t *node_tokens,
+                      double *node_score, int32_t *frontier_node,
+                      double *frontier_score, double *margin,
+                      int32_t *status) {
+  if (W < 1 || W > SD_ORC_MAX_W || b_top < 1 || budget < 1 || lambda < 0.0)
+    return 1;
+  orc_cand *row = malloc(sizeof(orc_cand) * (size_t)V);
+  orc_cand *all = malloc(sizeof(orc_cand) * (size_t)(W * b_top + 1));
+  double *lq = malloc(sizeof(double) * (size_t)V);
+  if (!row || !all || !lq) { free(row); free(all); free(lq); return 1; }
+  for (int b = 0; b < B; ++b) {
+    int32_t *fn = frontier_node + (size_t)b * W;
+    double *fs = frontier_score + (size_t)b * W;
+    double mg = INFINITY;
+    int st = 0;
+    const int n0 = n_nodes[b];
+    if (n0 < 0 || n0 >= budget) { margin[b] = mg; status[b] = 0; continue; }
+    const size_t qoff = (size_t)b * (size_t)q_stride;
+    int invalid = !softmax_row(q_logits, dtype, qoff, V, T, lq);
+    for (int j = 0; j < V && !invalid; ++j) lq[j] = log(lq[j]);
+    int nc = 0;
+    for (int w = 0; w < W && !invalid; ++w) {
+      if (fn[w] < 0) continue;
+      const size_t roff = ((size_t)b * W + w) * (size_t)V;
+      for (int j = 0; j < V; ++j) {
+        double r = logit_at(log_rho, dtype, roff + (size_t)j);
+        if (isnan(r) || r == INFINITY) { invalid = 1; break; }
+        /* lambda * (-inf) is -inf for lambda > 0; for lambda == 0 the
+         * prefix signal is not used */
+        double s = lq[j] + (lambda == 0.0 ? 0.0 : lambda * r);
+        row[j].s = s;
+        row[j].w = w;
+        row[j].tok = j;
+      }
+      if (invalid) break;
+      qsort(row, (size_t)V, sizeof(orc_cand), cand_cmp);
+      int take = 0;
+      while (take < b_top && take < V && row[take].s > -INFINITY) ++take;
+      if (take == b_top && take < V && row[take].s > -INFINITY)
+        note_margin(&mg, row[take - 1].s - row[take].s);
+      for (int i = 0; i < take; ++i) {
+        all[nc] = row[i];
+        all[nc].s = fs[w] + row[i].s;
+        ++nc;
+      }
+    }
+    if (invalid) {
+      n_nodes[b] = -1;
+      for (int w = 0; w < W; ++w) { fn[w] = -1; fs[w] = 0.0; }
+      margin[b] = INFINITY;
+      status[b] = ORC_ST_NONFINITE;
+      continue;
+    }
+    qsort(all, (size_t)nc, sizeof(orc_cand), cand_cmp);
+    int add = budget - n0 < nc ? budget - n0 : nc;
+    for (int i = 0; i + 1 < nc && i < add; ++i)
+      note_margin(&mg, all[i].s - all[i + 1].s);
+    int32_t old_fn[SD_ORC_MAX_W];
+    for (int w = 0; w < W; ++w) old_fn[w] = fn[w];
+    for (int i = 0; i < add; ++i) {
+      const size_t v = (size_t)b * budget + (size_t)(n0 + i);
+      parent[v] = old_fn[all[i].w];
+      node_tokens[v] = all[i].tok;
+      node_score[v] = all[i].s;
+    }
+    for (int w = 0; w < W; ++w) {
+      fn[w] = w < add ? n0 + w : -1;
+      fs[w] = w < add ? all[w].s : 0.0;
+    }
+    n_nodes[b] = n0 + add;
+    margin[b] = mg;
+    status[b] = st;
+  }
+  free(row); free(all); free(lq);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------
+ * SpecBranch branch resampling ("SpecBranch", branch resampling: at the
+ * branch point x_b fork k = max(1, floor(k_max (1 - q(x_b)))) parallel
+ * branches, the Top-k of the draft distribution there).  q = softmax(z / T)
+ * of draft row b (T == 0: the point mass on the argmax); q(x_b) is the
+ * drafted token's probability.  k is capped at V.  out_tokens [B, k_max]:
+ * the k tokens of largest logit (ties to the lower id), then -1.
+ * margin[b]: distance of k_max (1 - q(x_b)) to the nearest integer (where
+ * the floor could go either way in finite precision); INFINITY at T == 0.
+ * An x_b outside [0, V) or an unusable row: k = -1, tokens -1, status.
+ * ---------------------------------------------------------------------- */
+int orc_branch_fork(const void *draft, int dtype, const int32_t *x_b, int B,
+                    int V, double T, int k_max, int32_t *out_k,
+                    int32_t *out_tokens, double *margin, int32_t *status) {
+  if (k_max < 1) return 1;
+  double *q = malloc(sizeof(double) * (size_t)V);
+  orc_entry *e = malloc(sizeof(orc_entry) * (size_t)V);
+  if (!q || !e) { free(q); free(e); return 1; }
+  for (int b = 0; b < B; ++b) {
+    const size_t off = (size_t)b * V;
+    int32_t *ot = out_tokens + (size_t)b * k_max;
+    for (int i = 0; i < k_max; ++i) ot[i] = -1;
+    margin[b] = INFINITY;
+    status[b] = 0;
+    out_k[b] = -1;
+    const int x = x_b[b];
+    double qx;
+    if (T == 0.0) {
+      int a = argmax_row(draft, dtype, off, V);
+      if (a < 0) { status[b] = ORC_ST_NONFINITE; continue; }
+      qx = (x == a) ? 1.0 : 0.0;
+    } else {
+      if (!softmax_row(draft, dtype, off, V, T, q)) {
+        status[b] = ORC_ST_NONFINITE;
+        continue;
+      }
+      qx = (x >= 0 && x < V) ? q[x] : 0.0;
+    }
+    if (x < 0 || x >= V) { status[b] = ORC_ST_BAD_TOKEN; continue; }
+    const double f = (double)k_max * (1.0 - qx);
+    int k = (int)floor(f);
+    if (k < 1) k = 1;
+    if (k > V) k = V;
+    if (T != 0.0) {
+      const double fr = f - floor(f);
+      margin[b] = fr < 1.0 - fr ? fr : 1.0 - fr;
+    }
+    for (int j = 0; j < V; ++j) {
+      e[j].v = logit_at(draft, dtype, off + (size_t)j);
+      if (e[j].v == 0.0) e[j].v = 0.0; /* -0 equals +0 */
+      e[j].idx = j;
+    }
+    qsort(e, (size_t)V, sizeof(orc_entry), entry_cmp);
+    for (int i = 0; i < k; ++i) ot[i] = e[i].idx;
+    out_k[b] = k;
+  }
+  free(q); free(e);
   return 0;
 }

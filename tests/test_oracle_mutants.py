@@ -110,6 +110,22 @@ MUTANTS = [
       "test_kcand_trie_lossless_first_and_second_token"]),
     ("trie_final_uniform_slot", "U[0] = u[gamma];", "U[0] = u[0];", 1,
      ["test_kcand_trie_one_candidate_equals_linear"]),
+    ("presto_rho_sign",
+     "double s = lq[j] + (lambda == 0.0 ? 0.0 : lambda * r);",
+     "double s = lq[j] - (lambda == 0.0 ? 0.0 : lambda * r);", 1,
+     ["test_presto_golden", "test_presto_score_is_the_kl_minimiser"]),
+    ("presto_path_score_dropped", "all[nc].s = fs[w] + row[i].s;",
+     "all[nc].s = row[i].s;", 1,
+     ["test_presto_golden", "test_presto_construction_invariants"]),
+    ("presto_parent_slot", "parent[v] = old_fn[all[i].w];",
+     "parent[v] = old_fn[0];", 1,
+     ["test_presto_golden", "test_presto_construction_invariants"]),
+    ("fork_ceil", "int k = (int)floor(f);", "int k = (int)ceil(f);", 1,
+     ["test_branch_fork_golden"]),
+    ("fork_confidence_complement", "qx = (x >= 0 && x < V) ? q[x] : 0.0;",
+     "qx = (x >= 0 && x < V) ? 1.0 - q[x] : 0.0;", 1,
+     ["test_branch_fork_golden",
+      "test_branch_fork_topk_is_a_stable_sort_and_k_law"]),
 ]
 
 

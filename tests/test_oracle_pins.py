@@ -861,3 +861,169 @@ def test_kcand_trie_lossless_first_and_second_token():
     law = (na[:, None] * np.stack([softmax(Z1[i]) for i in range(V)]))
     assert chi2_p(np.bincount(a * V + b, minlength=V * V),
                   (law / law.sum()).ravel()) > P_MIN
+
+
+# ------------------------------------------ PRESTO tree construction
+def _presto_run(g, q, rho, depths):
+    tree = oracle.PrestoTree(q.shape[0], g["W"], g["budget"])
+    for d in range(depths):
+        oracle.presto_expand(tree, q[:, d], rho[:, d], g["T"], g["lambda"],
+                             g["b"])
+        yield tree
+
+
+def test_presto_golden():
+    """Hand-worked two-depth construction, tests/golden/presto_tree.json."""
+    g = _golden("presto_tree.json")
+    q = np.log(np.array(g["q"]))[None].astype(np.float32)       # [1, D, V]
+    rho = np.log(np.array(g["rho"]))[None].astype(np.float32)   # [1, D, W, V]
+    for tree, want in zip(_presto_run(g, q, rho, 2), g["after_depth"]):
+        n = want["n_nodes"]
+        assert tree.n_nodes[0] == n, want["why"]
+        np.testing.assert_array_equal(tree.parent[0, :n], want["parent"])
+        np.testing.assert_array_equal(tree.node_tokens[0, :n], want["tokens"])
+        np.testing.assert_allclose(tree.node_score[0, :n], want["score"],
+                                   atol=1e-6)
+        np.testing.assert_array_equal(tree.frontier_node[0], want["frontier"])
+
+
+def test_presto_greedy_chain_is_top1_of_each_marginal():
+    """lambda = 0, one path, one token per path: the tree is the chain of
+    the argmax of each depth's marginal (linear diffusion drafting), and
+    the path scores are the running sums of its log probabilities."""
+    from scipy.special import log_softmax
+    rng = np.random.default_rng(161)
+    B, D, V = 30, 5, 200
+    q = rng.normal(0, 2, (B, D, V)).astype(np.float32)
+    rho = np.log(rng.random((B, D, 1, V))).astype(np.float32)
+    tree = oracle.PrestoTree(B, 1, D + 1)
+    for d in range(D):
+        oracle.presto_expand(tree, q[:, d], rho[:, d], 0.8, 0.0, 1)
+    np.testing.assert_array_equal(tree.n_nodes, D + 1)
+    want_tok = np.argmax(q, axis=2)
+    np.testing.assert_array_equal(tree.node_tokens[:, 1:], want_tok)
+    np.testing.assert_array_equal(tree.parent[:, 1:],
+                                  np.tile(np.arange(D), (B, 1)))
+    lp = log_softmax(q.astype(np.float64) / 0.8, axis=2)
+    want = np.cumsum(np.take_along_axis(lp, want_tok[:, :, None], 2)[:, :, 0],
+                     axis=1)
+    np.testing.assert_allclose(tree.node_score[:, 1:], want, rtol=1e-12)
+
+
+def test_presto_score_is_the_kl_minimiser():
+    """PRESTO section 4.4: the proxy minimising KL(p || q) - lambda
+    E_p[log rho] over the simplex.  Found here by numerical minimisation
+    (scipy), it must equal the oracle's scores of all V children of the
+    root, normalised."""
+    from scipy.optimize import minimize
+    from scipy.special import logsumexp, softmax as sm
+    rng = np.random.default_rng(162)
+    V = 7
+    for lam in (0.5, 1.0, 2.0):
+        zq = rng.normal(0, 1.5, V)
+        rho = rng.uniform(0.05, 1.0, V)
+        q = sm(zq)
+
+        def J(a):
+            p = sm(a)
+            return np.sum(p * (np.log(p) - np.log(q))) - lam * np.sum(
+                p * np.log(rho))
+        a = minimize(J, np.zeros(V), method="BFGS", options={"gtol": 1e-12}).x
+        logp = a - logsumexp(a)
+        tree = oracle.PrestoTree(1, 1, V + 1)
+        oracle.presto_expand(tree, zq[None].astype(np.float32),
+                             np.log(rho)[None, None].astype(np.float32), 1.0,
+                             lam, V)
+        s = np.empty(V)
+        s[tree.node_tokens[0, 1:]] = tree.node_score[0, 1:]
+        np.testing.assert_allclose(s - logsumexp(s), logp, atol=1e-5)
+
+
+def test_presto_construction_invariants():
+    """Several depths, W = 3 paths, b = 2 tokens each, budget 16: every
+    path's children are its top-b tokens of q_d rho^lambda (probability
+    products, not log sums); the nodes added at a depth are the best
+    candidates of that depth; the frontier is the W best new nodes; the
+    budget is respected."""
+    rng = np.random.default_rng(163)
+    B, D, W, V, b, budget, lam, T = 20, 5, 3, 40, 2, 16, 0.7, 1.0
+    q = rng.normal(0, 1.5, (B, D, V)).astype(np.float32)
+    rho = np.log(rng.uniform(0.01, 1, (B, D, W, V))).astype(np.float32)
+    tree = oracle.PrestoTree(B, W, budget)
+    for d in range(D):
+        prev_fn = tree.frontier_node.copy()
+        prev_fs = tree.frontier_score.copy()
+        n0 = tree.n_nodes.copy()
+        oracle.presto_expand(tree, q[:, d], rho[:, d], T, lam, b)
+        qd = np.exp(q[:, d].astype(np.float64) / T)
+        qd /= qd.sum(1, keepdims=True)
+        for s in range(B):
+            cands = []
+            for w in range(W):
+                if prev_fn[s, w] < 0 or n0[s] >= budget:
+                    continue
+                prod = qd[s] * np.exp(rho[s, d, w].astype(np.float64)) ** lam
+                top = np.lexsort((np.arange(V), -prod))[:b]
+                cands += [(prev_fs[s, w] + np.log(prod[t]), w, t) for t in top]
+            cands.sort(key=lambda c: (-c[0], c[1], c[2]))
+            add = min(len(cands), budget - n0[s])
+            assert tree.n_nodes[s] == n0[s] + add
+            for i in range(add):
+                v = n0[s] + i
+                sc, w, t = cands[i]
+                assert tree.node_tokens[s, v] == t
+                assert tree.parent[s, v] == prev_fn[s, w]
+                np.testing.assert_allclose(tree.node_score[s, v], sc,
+                                           rtol=1e-9)
+            want_fn = [n0[s] + i if i < add else -1 for i in range(W)]
+            if n0[s] < budget:
+                np.testing.assert_array_equal(tree.frontier_node[s], want_fn)
+    assert np.all(tree.n_nodes <= budget)
+
+
+def test_presto_nonfinite_row_invalidates():
+    q = np.zeros((3, 8), np.float32)
+    rho = np.zeros((3, 2, 8), np.float32)
+    q[1, 3] = np.nan
+    rho[2, 0, 5] = np.inf
+    tree = oracle.PrestoTree(3, 2, 6)
+    _, st = oracle.presto_expand(tree, q, rho, 1.0, 1.0, 2)
+    np.testing.assert_array_equal(tree.n_nodes, [3, -1, -1])
+    assert st[1] & 2 and st[2] & 2 and st[0] == 0
+
+
+# ------------------------------------------- SpecBranch branch resampling
+def test_branch_fork_golden():
+    """Hand-worked cases of tests/golden/branch_fork.json."""
+    g = _golden("branch_fork.json")
+    z = np.log(np.array(g["q"]))[None].astype(np.float32)
+    for ex in g["cases"]:
+        o = oracle.branch_fork(z, np.array([ex["x_b"]]), ex["T"], ex["k_max"])
+        assert o["k"][0] == ex["k"], ex["why"]
+        np.testing.assert_array_equal(o["tokens"][0], ex["tokens"])
+
+
+def test_branch_fork_topk_is_a_stable_sort_and_k_law():
+    """The branches are the first k of a stable descending sort of the
+    logits; k is non-increasing in q(x_b) and spans 1..k_max - 1 (at T > 0
+    every q(x_b) is positive, so k_max itself needs q(x_b) = 0)."""
+    rng = np.random.default_rng(164)
+    B, V, km = 400, 300, 16
+    z = rng.normal(0, 2, (B, V)).astype(np.float32)
+    z[:, 10] = z[:, 11]  # ties
+    x = rng.integers(0, V, B).astype(np.int32)
+    x[:100] = np.argmax(z[:100], 1)  # confident branch points
+    z[:20, 0] = 30.0  # very confident: q(x_b) ~ 1, one branch
+    x[:20] = 0
+    o = oracle.branch_fork(z, x, 1.0, km)
+    order = np.argsort(-z, axis=1, kind="stable")
+    for b in range(B):
+        k = o["k"][b]
+        assert 1 <= k <= km
+        np.testing.assert_array_equal(o["tokens"][b, :k], order[b, :k])
+        assert np.all(o["tokens"][b, k:] == -1)
+    from scipy.special import softmax as sm
+    qx = sm(z.astype(np.float64), axis=1)[np.arange(B), x]
+    srt = np.argsort(qx)
+    assert np.all(np.diff(o["k"][srt]) <= 0)
+    assert o["k"].max() == km - 1 and o["k"].min() == 1
