@@ -295,6 +295,73 @@ sd_status sd_verify_tree_det(const void *target_logits, sd_dtype dt,
                              void *workspace, size_t ws_bytes, void *stream);
 
 /* ---------------------------------------------------------------------
+ * PRESTO tree construction, one depth per call ("PRESTO", section 4.1:
+ * prefix-aligned score s_{d,t}(c_d) = log q_d(t) + lambda log rho_d(t |
+ * c_d), path score S(P) (Eq. 10) the sum of s along the path; section 4.2
+ * and Algorithm 1: beam search with global retention under a node budget;
+ * section 4.4: s is the log of the product of experts q rho^lambda up to
+ * a constant).  rho is given; its learned predictor is not part of this.
+ *
+ * Tree state (device, caller-owned, updated in place):
+ *   n_nodes [B] (nodes so far; -1 for an invalid sequence), parent,
+ *   node_tokens [B, budget] int32, node_score [B, budget] float (S of the
+ *   node's path), frontier_node [B, W] (node of frontier path w, -1 for an
+ *   empty slot), frontier_score [B, W].  sd_presto_init sets the root:
+ *   node 0 (parent -1, token -1, score 0), the only frontier path.
+ * One depth: q_logits row b (at q_logits + b q_stride elements, q_stride
+ *   >= V, so a [B, D, V] tensor's depth d is passed without a copy) is the
+ *   drafter's marginal at this depth, log q_d = log softmax(z / T);
+ *   log_rho [B, W, V] (not read when lambda == 0): log rho of frontier path
+ *   w's prefix (<= 0, -inf for rho = 0).  Path w proposes its b_top tokens
+ *   of largest s (ties to the lower id; s = -inf never), each with score
+ *   S_w + s.  The proposals of a sequence are ordered by (score desc, w
+ *   asc, token asc); the first min(count, budget - n_nodes) become nodes
+ *   n_nodes, n_nodes + 1, ... in that order; the first min(W, added) of
+ *   them are the new frontier (the other slots -1).  A sequence with
+ *   n_nodes >= budget or < 0 is left as is.  A NaN or +inf in a row read
+ *   makes the sequence invalid: n_nodes = -1, frontier cleared,
+ *   SD_DEV_NONFINITE.  Requires T > 0, lambda >= 0, 1 <= W, b_top <= 64,
+ *   W b_top <= 1024.  Scores are fp32.
+ * ------------------------------------------------------------------- */
+sd_status sd_presto_init(int B, int W, int budget, int32_t *n_nodes,
+                         int32_t *parent, int32_t *node_tokens,
+                         float *node_score, int32_t *frontier_node,
+                         float *frontier_score, void *stream);
+
+size_t sd_presto_expand_workspace(int B, int W, int V, int b_top,
+                                  sd_dtype dt);
+
+sd_status sd_presto_expand(const void *q_logits, long long q_stride,
+                           const void *log_rho, sd_dtype dt, int B, int W,
+                           int V, float T, float lambda, int b_top,
+                           int budget, int32_t *n_nodes, int32_t *parent,
+                           int32_t *node_tokens, float *node_score,
+                           int32_t *frontier_node, float *frontier_score,
+                           int32_t *dev_status, void *workspace,
+                           size_t ws_bytes, void *stream);
+
+/* ---------------------------------------------------------------------
+ * SpecBranch branch resampling ("SpecBranch", branch resampling: at the
+ * branch point x_b fork k = max(1, floor(k_max (1 - q(x_b)))) parallel
+ * branches, the Top-k of the draft distribution there).
+ *
+ * draft_logits [B, V]: the draft row at each sequence's branch point;
+ * x_b [B]: the drafted token there.  q = softmax(z / T); T == 0 makes q
+ * the point mass on the argmax.  k is capped at V.
+ * Outputs: out_k [B] (-1 for an unusable row, SD_DEV_NONFINITE, or an x_b
+ *   outside [0, V), SD_DEV_BAD_TOKEN); out_tokens [B, k_max]: the k tokens
+ *   of largest logit (ties to the lower id; -0 equals +0), then -1.
+ * 1 <= k_max <= 64.  One read of each row.
+ * ------------------------------------------------------------------- */
+size_t sd_branch_fork_workspace(int B, int V, int k_max, sd_dtype dt);
+
+sd_status sd_branch_fork(const void *draft_logits, sd_dtype dt,
+                         const int32_t *x_b, int B, int V, float T, int k_max,
+                         int32_t *out_k, int32_t *out_tokens,
+                         int32_t *dev_status, void *workspace,
+                         size_t ws_bytes, void *stream);
+
+/* ---------------------------------------------------------------------
  * Geometric fan-out schedule (Saguaro, Theorem 12).  Host only.
  * F (host) [K+1]: F_0 w_k made integer by largest remainder (ties to the
  * lower k); sum F == budget.  Requires 0 <= K <= SD_MAX_K, budget >= 0,

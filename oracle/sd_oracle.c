@@ -1051,9 +1051,11 @@ int orc_kcand_trie(const int32_t *tokens, const float *uniforms, int B, int K,
  * log q_d is log softmax(z / T) of the drafter's marginal row q_logits[b]
  * (row stride q_stride elements).  A NaN or +inf in a row read makes the
  * sequence invalid: n_nodes = -1, frontier cleared (status 2).  margin[b]
- * is the smallest score gap that decided the outcome: at each path's top-b
- * cut, and between consecutive candidates of the merged order up to one
- * past the last added (INFINITY when nothing was decided).
+ * is the smallest nonzero score gap that decided the outcome: at each
+ * path's top-b cut, and between consecutive candidates of the merged order
+ * up to one past the last added (INFINITY when nothing was decided).
+ * Exact ties (equal inputs, e.g. repeated bf16 logits) are decided by the
+ * stated order, not by rounding, so they set no margin.
  * ---------------------------------------------------------------------- */
 #define SD_ORC_MAX_W 64
 typedef struct { double s; int w, tok; } orc_cand;
@@ -1093,10 +1095,11 @@ int orc_presto_expand(const void *q_logits, const void *log_rho, int dtype,
       if (fn[w] < 0) continue;
       const size_t roff = ((size_t)b * W + w) * (size_t)V;
       for (int j = 0; j < V; ++j) {
-        double r = logit_at(log_rho, dtype, roff + (size_t)j);
+        /* lambda == 0: the prefix signal is not used (nor read);
+         * lambda * (-inf) is -inf for lambda > 0 */
+        double r = lambda == 0.0 ? 0.0 : logit_at(log_rho, dtype,
+                                                  roff + (size_t)j);
         if (isnan(r) || r == INFINITY) { invalid = 1; break; }
-        /* lambda * (-inf) is -inf for lambda > 0; for lambda == 0 the
-         * prefix signal is not used */
         double s = lq[j] + (lambda == 0.0 ? 0.0 : lambda * r);
         row[j].s = s;
         row[j].w = w;
@@ -1106,7 +1109,8 @@ int orc_presto_expand(const void *q_logits, const void *log_rho, int dtype,
       qsort(row, (size_t)V, sizeof(orc_cand), cand_cmp);
       int take = 0;
       while (take < b_top && take < V && row[take].s > -INFINITY) ++take;
-      if (take == b_top && take < V && row[take].s > -INFINITY)
+      if (take == b_top && take < V && row[take].s > -INFINITY &&
+          row[take - 1].s != row[take].s)
         note_margin(&mg, row[take - 1].s - row[take].s);
       for (int i = 0; i < take; ++i) {
         all[nc] = row[i];
@@ -1124,7 +1128,7 @@ int orc_presto_expand(const void *q_logits, const void *log_rho, int dtype,
     qsort(all, (size_t)nc, sizeof(orc_cand), cand_cmp);
     int add = budget - n0 < nc ? budget - n0 : nc;
     for (int i = 0; i + 1 < nc && i < add; ++i)
-      note_margin(&mg, all[i].s - all[i + 1].s);
+      if (all[i].s != all[i + 1].s) note_margin(&mg, all[i].s - all[i + 1].s);
     int32_t old_fn[SD_ORC_MAX_W];
     for (int w = 0; w < W; ++w) old_fn[w] = fn[w];
     for (int i = 0; i < add; ++i) {
@@ -1152,8 +1156,10 @@ int orc_presto_expand(const void *q_logits, const void *log_rho, int dtype,
  * of draft row b (T == 0: the point mass on the argmax); q(x_b) is the
  * drafted token's probability.  k is capped at V.  out_tokens [B, k_max]:
  * the k tokens of largest logit (ties to the lower id), then -1.
- * margin[b]: distance of k_max (1 - q(x_b)) to the nearest integer (where
- * the floor could go either way in finite precision); INFINITY at T == 0.
+ * margin[b]: relative distance of k_max q(x_b) to the nearest integer at
+ * which k = max(1, min(V, k_max - ceil(k_max q))) steps (a finite-
+ * precision q could go either way there); INFINITY at T == 0 or when k
+ * cannot step.
  * An x_b outside [0, V) or an unusable row: k = -1, tokens -1, status.
  * ---------------------------------------------------------------------- */
 int orc_branch_fork(const void *draft, int dtype, const int32_t *x_b, int B,
@@ -1184,13 +1190,27 @@ int orc_branch_fork(const void *draft, int dtype, const int32_t *x_b, int B,
       qx = (x >= 0 && x < V) ? q[x] : 0.0;
     }
     if (x < 0 || x >= V) { status[b] = ORC_ST_BAD_TOKEN; continue; }
-    const double f = (double)k_max * (1.0 - qx);
-    int k = (int)floor(f);
+    /* floor(k_max (1 - q)) written as k_max - ceil(k_max q): the same
+     * integer, without 1 - q rounding to 1 when q is tiny */
+    const double y = (double)k_max * qx;
+    int k = k_max - (int)ceil(y);
     if (k < 1) k = 1;
     if (k > V) k = V;
     if (T != 0.0) {
-      const double fr = f - floor(f);
-      margin[b] = fr < 1.0 - fr ? fr : 1.0 - fr;
+      /* relative distance of y to the nearest integer n at which the
+       * clamped k steps (ceil(y) going from n to n + 1 changes k: n in
+       * [max(1, k_max - V), k_max - 2]); y below ~1e-30 could vanish in
+       * finite precision */
+      const double lo = k_max - V > 1 ? (double)(k_max - V) : 1.0;
+      const double hi = (double)(k_max - 2);
+      if (lo > hi) {
+        margin[b] = INFINITY;
+      } else {
+        double n = floor(y + 0.5);
+        if (n < lo) n = lo;
+        if (n > hi) n = hi;
+        margin[b] = y < 1e-30 ? 0.0 : fabs(y - n) / y;
+      }
     }
     for (int j = 0; j < V; ++j) {
       e[j].v = logit_at(draft, dtype, off + (size_t)j);

@@ -61,6 +61,12 @@ def _declare(L):
         "sd_verify_kcand_trie_workspace": ([I, I, I, I, I], Z),
         "sd_verify_kcand_trie": ([P, P, I, P, P, I, I, I, I, F, P, P, P, P,
                                   P, P, Z, P], I),
+        "sd_presto_init": ([I, I, I, P, P, P, P, P, P, P], I),
+        "sd_presto_expand_workspace": ([I, I, I, I, I], Z),
+        "sd_presto_expand": ([P, ctypes.c_longlong, P, I, I, I, I, F, F, I,
+                              I, P, P, P, P, P, P, P, P, Z, P], I),
+        "sd_branch_fork_workspace": ([I, I, I, I], Z),
+        "sd_branch_fork": ([P, I, P, I, I, F, I, P, P, P, P, Z, P], I),
         "sd_verify_tree_workspace": ([I, I, I, I], Z),
         "sd_verify_tree": ([P, P, I, P, P, P, I, I, I, F, P, P, P, P, P, P,
                             Z, P], I),
@@ -364,6 +370,73 @@ def verify_tree_det(target, parent, node_tokens, uniforms, T, *,
         B, N, V, float(T), _p(n), _p(toks), _p(nodes), _p(prob), _p(status),
         _p(ws), ws.numel(), _stream(dev)))
     return {"n": n, "tokens": toks, "nodes": nodes, "prob": prob}
+
+
+class PrestoTree:
+    """Device state of PRESTO trees under construction (sd_presto_init):
+    node arrays [B, budget], frontier [B, W]."""
+
+    def __init__(self, B, W, budget, device):
+        self.B, self.W, self.budget = B, W, budget
+        i32 = dict(dtype=torch.int32, device=device)
+        f32 = dict(dtype=torch.float32, device=device)
+        self.n_nodes = torch.empty(B, **i32)
+        self.parent = torch.empty((B, budget), **i32)
+        self.node_tokens = torch.empty((B, budget), **i32)
+        self.node_score = torch.empty((B, budget), **f32)
+        self.frontier_node = torch.empty((B, W), **i32)
+        self.frontier_score = torch.empty((B, W), **f32)
+        _check(lib().sd_presto_init(
+            B, W, budget, _p(self.n_nodes), _p(self.parent),
+            _p(self.node_tokens), _p(self.node_score),
+            _p(self.frontier_node), _p(self.frontier_score),
+            _stream(torch.device(device))))
+
+
+def presto_expand(tree, q_logits, log_rho, T, lam, b_top, *, status=None,
+                  workspace=None):
+    """One depth of PRESTO's beam construction (sd_presto_expand) on `tree`
+    (a PrestoTree, updated in place).  q_logits [B, V] (rows may be strided,
+    e.g. q[:, d] of a [B, D, V] tensor); log_rho [B, W, V] (None when
+    lam == 0)."""
+    dev = q_logits.device
+    B, V = q_logits.shape
+    if not q_logits.is_cuda or q_logits.stride(1) != 1:
+        raise ValueError("q_logits must be CUDA rows with unit stride")
+    if log_rho is not None:
+        _dev(log_rho, dev, "log_rho", q_logits.dtype)
+        if tuple(log_rho.shape) != (B, tree.W, V):
+            raise ValueError("log_rho must be [B, W, V]")
+    L = lib()
+    nbytes = L.sd_presto_expand_workspace(B, tree.W, V, int(b_top),
+                                          _dt(q_logits))
+    ws = (workspace or _default_ws).get(dev, nbytes)
+    _check(L.sd_presto_expand(
+        _p(q_logits), q_logits.stride(0), _p(log_rho), _dt(q_logits), B,
+        tree.W, V, float(T), float(lam), int(b_top), tree.budget,
+        _p(tree.n_nodes), _p(tree.parent), _p(tree.node_tokens),
+        _p(tree.node_score), _p(tree.frontier_node), _p(tree.frontier_score),
+        _p(status), _p(ws), ws.numel(), _stream(dev)))
+    return tree
+
+
+def branch_fork(draft, x_b, T, k_max, *, status=None, workspace=None):
+    """SpecBranch fork (sd_branch_fork): k = max(1, floor(k_max (1 -
+    q(x_b)))) (capped at V) and the top-k tokens of each row.  draft
+    [B, V]; x_b [B].  Returns k [B], tokens [B, k_max]."""
+    dev = draft.device
+    _dev(draft, dev, "draft")
+    B, V = draft.shape
+    x_b = _dev(x_b, dev, "x_b", torch.int32)
+    k = torch.empty(B, dtype=torch.int32, device=dev)
+    toks = torch.empty((B, k_max), dtype=torch.int32, device=dev)
+    L = lib()
+    nbytes = L.sd_branch_fork_workspace(B, V, int(k_max), _dt(draft))
+    ws = (workspace or _default_ws).get(dev, nbytes)
+    _check(L.sd_branch_fork(_p(draft), _dt(draft), _p(x_b), B, V, float(T),
+                            int(k_max), _p(k), _p(toks), _p(status), _p(ws),
+                            ws.numel(), _stream(dev)))
+    return {"k": k, "tokens": toks}
 
 
 def fanout_schedule(K, budget, a, r):

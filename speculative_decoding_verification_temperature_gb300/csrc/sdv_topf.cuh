@@ -153,16 +153,12 @@ __device__ __forceinline__ void wf_seed_vec(WarpFilter &w, const float (&z)[VW])
   wf_seed2(w, m1, m2);
 }
 
-// Offer one vector per lane (ok = false for idle lanes); j0 is the token id
-// of the vector's first element.  Full, converged warp.
-template <int DT, int VW>
-__device__ __forceinline__ void wf_offer(WarpFilter &w, uint32_t *cta_th,
-                                         const Raw<DT, VW> &r, bool ok,
-                                         int j0) {
-  float z[VW];
-#pragma unroll
-  for (int e = 0; e < VW; ++e)
-    z[e] = ok ? elt<DT, VW>(r, e) : -__builtin_huge_valf();
+// Offer VW values per lane (ok = false for idle lanes, whose values must be
+// -inf); j0 is the token id of the first.  Full, converged warp.
+template <int VW>
+__device__ __forceinline__ void wf_offer_vals(WarpFilter &w, uint32_t *cta_th,
+                                              const float (&z)[VW], bool ok,
+                                              int j0) {
   const float vmax = vmax_nan_of<VW>(z);  // NaN: never >= th
   w.nseen = max_nan(w.nseen, vmax);
   if (__builtin_expect(!w.seeded, 0)) wf_seed_vec<VW>(w, z);
@@ -181,6 +177,18 @@ __device__ __forceinline__ void wf_offer(WarpFilter &w, uint32_t *cta_th,
       wf_raise(w, cta_th);
     }
   }
+}
+
+// Offer one vector of logits per lane.
+template <int DT, int VW>
+__device__ __forceinline__ void wf_offer(WarpFilter &w, uint32_t *cta_th,
+                                         const Raw<DT, VW> &r, bool ok,
+                                         int j0) {
+  float z[VW];
+#pragma unroll
+  for (int e = 0; e < VW; ++e)
+    z[e] = ok ? elt<DT, VW>(r, e) : -__builtin_huge_valf();
+  wf_offer_vals<VW>(w, cta_th, z, ok, j0);
 }
 
 // Write the warp's best F keys to s.flat[warp * F ..].

@@ -120,7 +120,8 @@ MUTANTS = [
     ("presto_parent_slot", "parent[v] = old_fn[all[i].w];",
      "parent[v] = old_fn[0];", 1,
      ["test_presto_golden", "test_presto_construction_invariants"]),
-    ("fork_ceil", "int k = (int)floor(f);", "int k = (int)ceil(f);", 1,
+    ("fork_floor", "int k = k_max - (int)ceil(y);",
+     "int k = k_max - (int)floor(y);", 1,
      ["test_branch_fork_golden"]),
     ("fork_confidence_complement", "qx = (x >= 0 && x < V) ? q[x] : 0.0;",
      "qx = (x >= 0 && x < V) ? 1.0 - q[x] : 0.0;", 1,
