@@ -420,7 +420,84 @@ def other_workloads(args, dev, peak):
         _filtered(args, dev, entry, steps)
     if want("cache_hit"):
         out["cache_hit"] = _cache_hit(args, dev)
+    if want("presto"):
+        _presto(args, dev, entry, steps)
+    if want("fork"):
+        _fork(args, dev, entry, steps)
     return out
+
+
+def _presto(args, dev, entry, steps):
+    """PRESTO tree construction on the tree workload's shape: B=16, V=151936
+    bf16, 8 depths, W=8 paths, b=4 tokens per path, a 64-node budget,
+    T=0.8, lambda=1; synthetic drafter marginals N(0, 2^2) and log rho of
+    U(0.01, 1).  One round = sd_presto_init + 8 sd_presto_expand calls."""
+    from speculative_decoding_verification_temperature_gb300 import api
+    B, D, W, V, b_top, budget = 16, 8, 8, 151936, 4, 64
+    sets = []
+    for r in range(2):
+        g = torch.Generator(device=dev).manual_seed(700 + r)
+        q = (torch.randn((B, D, V), generator=g, device=dev) * 2.0).to(
+            torch.bfloat16)
+        rho = torch.log(torch.rand((D, B, W, V), generator=g, device=dev) *
+                        0.99 + 0.01).to(torch.bfloat16)  # depth-major
+        sets.append((q, rho))
+    state = {}
+
+    def fn(c):
+        q, rho = c
+        t = api.PrestoTree(B, W, budget, dev)
+        for d in range(D):
+            api.presto_expand(t, q[:, d], rho[d], 0.8, 1.0, b_top)
+        state["t"] = t
+    # one round is 17 small launches: timed as a CUDA graph, as a serving
+    # loop with a fixed depth would run it (the host's per-call cost is
+    # larger than a depth's device time)
+    ms, how = _time_graph(fn, sets, 20, 3, dev)
+    # bytes: a depth that runs (node budget not yet spent) reads the
+    # sequence's q row once and the log rho rows of its frontier paths (the
+    # nodes of that depth, at most W), counted from the built trees
+    rows = 0
+    for c in sets:
+        fn(c)
+        par = state["t"].parent.cpu().numpy()
+        n = state["t"].n_nodes.cpu().numpy()
+        for bi in range(B):
+            depth = np.zeros(n[bi], np.int64)
+            for v in range(1, n[bi]):
+                depth[v] = depth[par[bi, v]] + 1
+            for d in range(D):
+                if (depth <= d).sum() >= budget:
+                    break
+                rows += 1 + min(W, int((depth == d).sum()))
+    entry("presto_build", ms, rows / len(sets), V, 2, B * D + B * D * W,
+          {"nodes": int(n.sum()), "timing": how})
+
+
+def _fork(args, dev, entry, steps):
+    """SpecBranch fork on B=64 rows of V=152064 bf16 (N(0, 2.5^2) logits),
+    k_max=8, T=1, x_b the drafted (argmax) token for half the rows and a
+    random one for the rest; timed as a CUDA graph."""
+    from speculative_decoding_verification_temperature_gb300 import api
+    B, V = 64, 152064
+    sets = []
+    for r in range(8):
+        g = torch.Generator(device=dev).manual_seed(800 + r)
+        z = (torch.randn((B, V), generator=g, device=dev) * 2.5).to(
+            torch.bfloat16)
+        x = torch.randint(0, V, (B,), generator=g, device=dev,
+                          dtype=torch.int32)
+        x[: B // 2] = torch.argmax(z[: B // 2].float(), 1).int()
+        sets.append((z, x))
+    out = {}
+
+    def fn(c):
+        out["o"] = api.branch_fork(c[0], c[1], 1.0, 8)
+    ms, how = _time_graph(fn, sets, 200, 5, dev)
+    fn(sets[0])
+    entry("branch_fork", ms, B, V, 2, B,
+          {"timing": how,
+           "mean_k": float(out["o"]["k"].float().mean())})
 
 
 def _filtered(args, dev, entry, steps):
@@ -651,7 +728,7 @@ def main():
                     choices=["native", "reference"])
     ap.add_argument("--only", default=None,
                     choices=["tiny", "linear", "kcand", "tree", "filtered",
-                             "cache_hit"],
+                             "cache_hit", "presto", "fork"],
                     help="time only this other workload (profiling runs); "
                          "no main line")
     ap.add_argument("--batch", type=int, default=256,

@@ -92,12 +92,10 @@ __global__ void __launch_bounds__(kThreads)
         if (RHO) xr[u] = load_vec<DT, VW>(rrow, v);
       }
     }
-    wf_sync(wf, &top.th);
+    float z[kSelUF][VW];
 #pragma unroll
     for (int u = 0; u < kSelUF; ++u) {
-      const int v = vb + u * 32 + lane;
-      const bool ok = v < sl.vend;
-      float z[VW];
+      const bool ok = vb + u * 32 + lane < sl.vend;
 #pragma unroll
       for (int e = 0; e < VW; ++e) {
         float x = -__builtin_huge_valf();
@@ -105,13 +103,26 @@ __global__ void __launch_bounds__(kThreads)
           x = elt<DT, VW>(xq[u], e) * p.scale;
           if (RHO) x = fmaf(p.lambda, elt<DT, VW>(xr[u], e), x);
         }
-        z[e] = x;
+        z[u][e] = x;
       }
       if (ok) {
         ms_add<DT, VW>(st, xq[u], p.k2);
-        worst = max_nan(worst, vmax_nan_of<VW>(z));
+        worst = max_nan(worst, vmax_nan_of<VW>(z[u]));
       }
-      wf_offer_vals<VW>(wf, &top.th, z, ok, v * VW);
+    }
+    if (!wf.seeded) {  // seed from the whole first batch (kSelUF VW values)
+      float m1 = -__builtin_huge_valf(), m2 = -__builtin_huge_valf();
+#pragma unroll
+      for (int u = 0; u < kSelUF; ++u)
+#pragma unroll
+        for (int e = 0; e < VW; ++e) top2_add(m1, m2, z[u][e]);
+      wf_seed2(wf, m1, m2);
+    }
+    wf_sync(wf, &top.th);
+#pragma unroll
+    for (int u = 0; u < kSelUF; ++u) {
+      const int v = vb + u * 32 + lane;
+      wf_offer_vals<VW>(wf, &top.th, z[u], v < sl.vend, v * VW);
     }
   }
   // a NaN anywhere, or +inf (in q, or in log rho), makes the row unusable
@@ -350,9 +361,28 @@ int slice_bound(long long nvec, int F) {
   return (int)(s < cap ? s : cap);
 }
 
-int choose_slices(long long nvec, long long items, int F, int sms) {
+// Resident CTAs per SM of a kernel at kThreads threads (cached).
+int resident_per_sm(const void *kern) {
+  static std::mutex mu;
+  static std::unordered_map<const void *, int> cache;
+  std::lock_guard<std::mutex> lk(mu);
+  auto it = cache.find(kern);
+  if (it != cache.end()) return it->second;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, 0) !=
+          cudaSuccess ||
+      n < 1)
+    n = 1;
+  cache[kern] = n;
+  return n;
+}
+
+// As many slices as one full wave of CTAs allows (no partial wave), within
+// the bound above.
+int choose_slices(long long nvec, long long items, int F, int sms,
+                  const void *kern) {
   const int bound = slice_bound(nvec, F);
-  long long s = (4LL * sms + items - 1) / items;
+  long long s = (long long)resident_per_sm(kern) * sms / items;
   if (s < 1) s = 1;
   return (int)(s < bound ? s : bound);
 }
@@ -488,7 +518,8 @@ extern "C" sd_status sd_presto_expand(
                    ((size_t)V * eb) % 16 == 0 && (!rho || aligned16(log_rho));
   const long long nvec = vec ? V / vw : V;
   const long long items = (long long)B * W;
-  const int S = choose_slices(nvec, items, b_top, sms);
+  const SelKernel kern = pick_sel(dt, vec, rho);
+  const int S = choose_slices(nvec, items, b_top, sms, (const void *)kern);
   const size_t need = sel_ws_bytes(items, S, b_top);
   if (!workspace || ws_bytes < need)
     return fail(SD_ERR_INVALID_ARG, "workspace of >= %zu bytes required",
@@ -513,7 +544,7 @@ extern "C" sd_status sd_presto_expand(
   sp.stats = w.stats;
   sp.bad = w.bad;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  pick_sel(dt, vec, rho)<<<(unsigned)(items * S), kThreads, 0, s>>>(sp);
+  kern<<<(unsigned)(items * S), kThreads, 0, s>>>(sp);
   SDV_CUDA(cudaGetLastError());
   MergeParams mp;
   mp.keys = w.keys;
@@ -565,7 +596,8 @@ extern "C" sd_status sd_branch_fork(const void *draft_logits, sd_dtype dt,
   const int eb = dt == SD_F32 ? 4 : 2, vw = dt == SD_F32 ? 4 : 8;
   const bool vec = aligned16(draft_logits) && ((size_t)V * eb) % 16 == 0;
   const long long nvec = vec ? V / vw : V;
-  const int S = choose_slices(nvec, B, k_max, sms);
+  const SelKernel kern = pick_sel(dt, vec, false);
+  const int S = choose_slices(nvec, B, k_max, sms, (const void *)kern);
   const size_t need = sel_ws_bytes(B, S, k_max);
   if (!workspace || ws_bytes < need)
     return fail(SD_ERR_INVALID_ARG, "workspace of >= %zu bytes required",
@@ -590,8 +622,7 @@ extern "C" sd_status sd_branch_fork(const void *draft_logits, sd_dtype dt,
   sp.stats = w.stats;
   sp.bad = w.bad;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  pick_sel(dt, vec, false)<<<(unsigned)((long long)B * S), kThreads, 0, s>>>(
-      sp);
+  kern<<<(unsigned)((long long)B * S), kThreads, 0, s>>>(sp);
   SDV_CUDA(cudaGetLastError());
   ForkParams fp;
   fp.keys = w.keys;
