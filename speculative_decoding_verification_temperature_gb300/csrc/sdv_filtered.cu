@@ -8,8 +8,8 @@
 // the kept keys (m the row maximum, k2 = log2(e)/T), the nucleus is a
 // prefix of them, and the residual max(0, p~ - q~) is zero outside the
 // target's kept tokens.  So each row is read once, through the exact top-k
-// selection of sdv_topf.cuh (per-warp lists against a CTA-wide threshold),
-// and the accept test, the correction and the bonus are computed by one
+// selection of sdv_topf.cuh (one CTA-wide candidate buffer above a seeded,
+// rising threshold: a compare per element), and the accept test, the correction and the bonus are computed by one
 // warp on at most 64 keys per row: there is no second pass over a row.
 //
 // One thread-block cluster verifies one sequence at a time (work counter).
@@ -311,47 +311,30 @@ __global__ void __launch_bounds__(kThreads, 4)
   };
   // One row through the ring into this CTA's list clist[par][r].
   auto select_row = [&](int r) {
-    WarpFilter wf;
-    wf_init(wf, K);
+    cta_reset(sh.top);
+    bool nan = false;
     for (int c = 0; c < nch; ++c) {
       const int v0 = sl.vbeg + c * kStageVecs;
       const int cn = min(kStageVecs, nv - c * kStageVecs);
       consume([&](const uint4 *A) {
-        if (c == 0) {
-          // seed every warp's threshold from the whole first chunk
+        if (c == 0) {  // seed the threshold from the whole first chunk
           float m1 = -__builtin_huge_valf(), m2 = -__builtin_huge_valf();
-          for (int base = warp * 32; base < cn; base += kThreads) {
-            const int i = base + lane;
-            if (i < cn) {
-              const Raw<DT, VW> x = sget<DT, VW>(A, i);
+          for (int i = tid; i < cn; i += kThreads) {
+            const Raw<DT, VW> x = sget<DT, VW>(A, i);
 #pragma unroll
-              for (int e = 0; e < VW; ++e) top2_add(m1, m2, elt<DT, VW>(x, e));
-            }
+            for (int e = 0; e < VW; ++e) top2_add(m1, m2, elt<DT, VW>(x, e));
           }
-          wf_seed2(wf, m1, m2);
-          if (lane == 0 && wf.th > -__builtin_huge_valf())
-            atomicMax(&sh.top.th, ord32(wf.th));
-          __syncthreads();
+          cta_seed(sh.top, m1, m2, K);
         }
-        wf_sync(wf, &sh.top.th);
-        for (int base = warp * 32; base < cn; base += kThreads) {
-          const int i = base + lane;
-          Raw<DT, VW> x{};
-          if (i < cn) x = sget<DT, VW>(A, i);
-          wf_offer<DT, VW>(wf, &sh.top.th, x, i < cn, (v0 + i) * VW);
-        }
+        nan |= cta_offer_chunk<DT, VW>(sh.top, A, cn, v0, K);
       });
     }
-    const int anynan = __syncthreads_or(wf.nseen != wf.nseen);
-    wf_export(wf, sh.top);
-    __syncthreads();
-    const int nout = rank_select(sh.top, kWarps * K, K);
+    const int anynan = __syncthreads_or(nan);
+    cta_compact(sh.top, K);  // the slice's best K, descending
+    const int nout = sh.top.nbuf;
     for (int i = tid; i < K; i += kThreads)
-      sh.clist[par][r][i] = i < nout ? sh.top.out[i] : 0ull;
-    if (tid == 0) {
-      sh.cnan[par][r] = anynan;
-      sh.top.th = 0;
-    }
+      sh.clist[par][r][i] = i < nout ? sh.top.flat[i] : 0ull;
+    if (tid == 0) sh.cnan[par][r] = anynan;
     __syncthreads();
   };
   // Exchange rows [r0, r0 + nr): every CTA ranks the CL lists of each row
@@ -367,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 4)
         if (i % K == 0 && peer->cnan[par][r]) sh.rnan[r] = 1;
       }
       __syncthreads();
-      const int n = rank_select(sh.top, CL * K, K);
+      const int n = cta_merge_lists(sh.top.flat, CL, K, sh.top.out);
       for (int i = tid; i < K; i += kThreads)
         sh.rk[r][i] = i < n ? sh.top.out[i] : 0ull;
       __syncthreads();
@@ -404,7 +387,10 @@ __global__ void __launch_bounds__(kThreads, 4)
         sh.gu = gu;
       }
       exchange(0, 2);
-      if (warp == 0) {  // the accept test of position j
+      // the accept test of position j, on the last warp: warp 0 holds the
+      // ring's producer (thread 0), whose own work would hold up the
+      // warp-wide shuffles
+      if (warp == kWarps - 1) {
         const int x = sh.gx;
         const bool bad = x < 0 || x >= V;
         int kd;
@@ -448,24 +434,24 @@ __global__ void __launch_bounds__(kThreads, 4)
             if (lane == 0) sh.zero_mass = zm;
           }
         }
-        if (lane == 0) {
-          sh.kind = kd;
-          FSched &sc = sh.sc;
-          sc.decided = j + 1;
-          if (kd) sc.final = 1;
-          fu.pump(sc, ps, consumed);
-        }
+        if (lane == 0) sh.kind = kd;
         if (bad) bad_token = 1;
       }
       __syncthreads();
       kind = sh.kind;
+      if (tid == 0) {  // the producer learns the decision
+        FSched &sc = sh.sc;
+        sc.decided = j + 1;
+        if (kind) sc.final = 1;
+        fu.pump(sc, ps, consumed);
+      }
       if (kind) break;
       n = j + 1;
     }
     if (!kind) {  // every draft accepted: the bonus from p~_gamma
       select_row(1);
       exchange(1, 1);
-      if (warp == 0) {
+      if (warp == kWarps - 1) {
         int kd = 2;
         if (!row_ok(1)) {
           kd = 3;

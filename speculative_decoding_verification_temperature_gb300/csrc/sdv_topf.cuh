@@ -44,6 +44,10 @@ struct TopSmem {
   uint64_t out[SD_MAX_FANOUT];            // result, descending
   uint32_t th;                            // ord32 of the CTA threshold, 0 = none
   int nan;
+  // CTA-wide candidate buffer (cta_* below): flat[0..nbuf) holds keys
+  // above thk
+  uint64_t thk;
+  int nbuf, tot;
 };
 
 // Per-thread view of its warp's filter.  All fields but nseen are
@@ -216,6 +220,196 @@ __device__ __forceinline__ int rank_select(TopSmem &s, int C, int F) {
   }
   __syncthreads();
   return nz < F ? nz : F;
+}
+
+// ------------------------------------------------------------------------
+// CTA-wide candidate buffer, for large F.  The warp lists above keep each
+// warp's own best F, so with F in the tens every warp inserts about F ln(n)
+// keys one at a time.  Here the CTA keeps one buffer of candidates (the
+// keys above thk, a lower bound on the CTA's F-th best) in s.flat; a chunk
+// of elements costs one compare per element and an append per candidate,
+// and the buffer is compacted to its best F (raising thk to the F-th) when
+// a chunk's candidates would not fit.  Keys order as above.
+constexpr int kCtaCap = kWarps * SD_MAX_FANOUT;
+static_assert(SD_MAX_FANOUT + kThreads <= kCtaCap, "a round fits");
+
+__device__ __forceinline__ void cta_reset(TopSmem &s) {
+  if (threadIdx.x == 0) {
+    s.th = 0;
+    s.thk = 0;
+    s.nbuf = 0;
+    s.tot = 0;
+  }
+  __syncthreads();
+}
+
+// Sort a[0..n) (n <= kCtaCap) in descending order in place: a bitonic sort
+// of the P = max(2, next power of two >= n) leading entries, a[n..P)
+// padded with empty keys (which sort last); log2(P) (log2(P) + 1) / 2
+// compare-exchange stages, threads < P / 2 taking one pair each.
+// Block-wide.
+__device__ __forceinline__ void cta_sort_desc(uint64_t *a, int n) {
+  static_assert(kCtaCap <= 2 * kThreads, "one pair per thread per stage");
+  int P = 2;
+  while (P < n) P <<= 1;
+  for (int i = n + (int)threadIdx.x; i < P; i += kThreads) a[i] = 0;
+  __syncthreads();
+  const int i = threadIdx.x;
+  for (int k = 2; k <= P; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      if (i < P / 2) {
+        const int lo = 2 * i - (i & (j - 1));  // pair (lo, lo + j)
+        const int hi = lo + j;
+        const uint64_t x = a[lo], y = a[hi];
+        if ((x < y) == ((lo & k) == 0)) {  // descending where lo & k == 0
+          a[lo] = y;
+          a[hi] = x;
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+// Merge nl lists of F keys each, every list descending with empty keys
+// last, stored at a[l F ..]: a key's place in the union is its index in
+// its own list plus, for every other list, the number of its keys above it
+// (a binary search; non-empty keys are unique).  The best F go to out
+// (descending); returns how many there are.  Block-wide.
+__device__ __forceinline__ int cta_merge_lists(const uint64_t *a, int nl,
+                                               int F, uint64_t *out) {
+  int nz = 0;
+  for (int i0 = 0; i0 < nl * F; i0 += kThreads) {
+    const int idx = i0 + (int)threadIdx.x;
+    const uint64_t me = idx < nl * F ? a[idx] : 0ull;
+    if (me != 0) {
+      const int l = idx / F;
+      int r = idx - l * F;
+      for (int o = 0; o < nl && r < F; ++o) {
+        if (o == l) continue;
+        const uint64_t *b = a + o * F;
+        int lo = 0, hi = F;
+        while (lo < hi) {
+          const int mid = (lo + hi) >> 1;
+          if (b[mid] > me) lo = mid + 1;
+          else hi = mid;
+        }
+        r += lo;
+      }
+      if (r < F) out[r] = me;
+    }
+    nz += __syncthreads_count(me != 0);
+  }
+  __syncthreads();
+  return nz < F ? nz : F;
+}
+
+// Compact s.flat[0..nbuf) (unique non-empty keys) to its best F, in
+// descending order, and raise thk to the F-th.  Block-wide.
+__device__ __forceinline__ void cta_compact(TopSmem &s, int F) {
+  const int n = s.nbuf;
+  cta_sort_desc(s.flat, n);
+  if (threadIdx.x == 0) {
+    const int m = n < F ? n : F;
+    s.nbuf = m;
+    if (m == F && s.flat[F - 1] > s.thk) s.thk = s.flat[F - 1];
+  }
+  __syncthreads();
+}
+
+// Seed thk from per-thread top-2 values (m1 >= m2; -inf for none) of the
+// first elements: the F-th largest of these 2 kThreads samples has at least
+// F elements at or above it, so keys of smaller value can be skipped.
+// -inf samples may be placeholders and do not count.  Uses s.flat as
+// scratch (one sort); leaves the buffer empty.  Block-wide.
+__device__ __forceinline__ void cta_seed(TopSmem &s, float m1, float m2,
+                                         int F) {
+  const int t = threadIdx.x;
+  // value keys made unique by their sample slot
+  s.flat[2 * t] = m1 > -__builtin_huge_valf()
+                      ? make_key(ord32(m1), (uint32_t)(2 * t)) : 0ull;
+  s.flat[2 * t + 1] = m2 > -__builtin_huge_valf()
+                          ? make_key(ord32(m2), (uint32_t)(2 * t + 1)) : 0ull;
+  cta_sort_desc(s.flat, 2 * kThreads);
+  if (t == 0 && s.flat[F - 1] != 0)  // admit values >= the F-th sample
+    s.thk = ((s.flat[F - 1] >> 32) << 32) - 1ull;
+  __syncthreads();
+}
+
+// Offer this thread's part of a chunk: vectors i = threadIdx.x, + kThreads,
+// ... < cn of A, element ids (v0 + i) VW + e.  Returns whether a NaN was
+// seen.  Block-wide.
+template <int DT, int VW>
+__device__ __forceinline__ bool cta_offer_chunk(TopSmem &s, const uint4 *A,
+                                                int cn, int v0, int F) {
+  const int t = threadIdx.x, lane = t & 31;
+  const uint64_t thk = s.thk;
+  // a key can beat thk only if its value reaches thk's (NaN never does)
+  const float thv = thk ? unord32((uint32_t)(thk >> 32)) : -__builtin_huge_valf();
+  int cnt = 0;
+  bool nan = false;
+  for (int i = t; i < cn; i += kThreads) {
+    Raw<DT, VW> x;
+    x.w = A[i];
+#pragma unroll
+    for (int e = 0; e < VW; ++e) {
+      const float z = elt<DT, VW>(x, e);
+      nan |= z != z;
+      if (__builtin_expect(z >= thv, 0))
+        cnt += make_key(ord32(z), (uint32_t)((v0 + i) * VW + e)) > thk;
+    }
+  }
+  const int wsum = __reduce_add_sync(0xffffffffu, cnt);
+  if (lane == 0 && wsum) atomicAdd(&s.tot, wsum);
+  __syncthreads();
+  const int tot = s.tot;
+  if (tot == 0) return nan;  // block-uniform
+  if (s.nbuf + tot > kCtaCap) cta_compact(s, F);
+  const int nb = s.nbuf;
+  __syncthreads();  // every thread has read nb before the appends below
+  if (nb + tot <= kCtaCap) {  // append this chunk's candidates
+    if (cnt) {
+      int off = atomicAdd(&s.nbuf, cnt);
+      for (int i = t; i < cn; i += kThreads) {
+        Raw<DT, VW> x;
+        x.w = A[i];
+#pragma unroll
+        for (int e = 0; e < VW; ++e) {
+          const float z = elt<DT, VW>(x, e);
+          if (z >= thv) {
+            const uint64_t k =
+                make_key(ord32(z), (uint32_t)((v0 + i) * VW + e));
+            if (k > thk) s.flat[off++] = k;
+          }
+        }
+      }
+    }
+  } else {
+    // more candidates than the buffer takes (ties, rising values): one
+    // element per thread per round, compacting between rounds
+    const int per = (cn + kThreads - 1) / kThreads;
+    for (int u = 0; u < per; ++u) {
+      const int i = t + u * kThreads;
+      for (int e = 0; e < VW; ++e) {
+        if (s.nbuf + kThreads > kCtaCap) cta_compact(s, F);
+        const uint64_t th2 = s.thk;
+        uint64_t k = 0;
+        bool take = false;
+        if (i < cn) {
+          Raw<DT, VW> x;
+          x.w = A[i];
+          const float z = elt<DT, VW>(x, e);
+          k = make_key(ord32(z), (uint32_t)((v0 + i) * VW + e));
+          take = z == z && k > th2;
+        }
+        if (take) s.flat[atomicAdd(&s.nbuf, 1)] = k;
+        __syncthreads();
+      }
+    }
+  }
+  __syncthreads();
+  if (t == 0) s.tot = 0;
+  return nan;
 }
 
 }  // namespace sdv
