@@ -262,6 +262,10 @@ extern "C" sd_status sd_fanout_topk(const void *draft_logits, sd_dtype dt,
   int maxc = 0;
   st = max_active_clusters((const void *)kern, CL, smem, &maxc);
   if (st != SD_OK) return st;
+  // SDV_FANOUT_MAXC caps the clusters (tuning: room for a kernel that runs
+  // beside this one on another stream)
+  const int cap = env_int("SDV_FANOUT_MAXC", 0);
+  if (cap > 0 && cap < maxc) maxc = cap;
   // rows of equal cost: give every cluster the same number of them
   const long long per = (rows + maxc - 1) / maxc;
   const long long want = (rows + per - 1) / per;
