@@ -92,6 +92,17 @@ __device__ __forceinline__ float load_logit(const void *row, int j) {
   return __uint_as_float((uint32_t)h << 16);
 }
 
+// ------------------------------------------- programmatic dependent launch
+// Wait until the grids this one depends on have completed and their writes
+// are visible (a no-op when the kernel was launched without programmatic
+// serialisation); let the next grid in the stream start launching.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" :::);
+}
+
 // ----------------------------------------------------------- fast exp2
 // The SFU's approximate 2^x (ex2.approx, flush-to-zero): relative error a
 // few ulp, far inside the 1e-5 decision margins the tests allow.

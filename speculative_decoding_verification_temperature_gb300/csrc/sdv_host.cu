@@ -144,6 +144,22 @@ sd_status launch_clusters(const void *kernel, int nclusters, int cl,
   return SD_OK;
 }
 
+sd_status launch_pdl(const void *kernel, unsigned grid, unsigned block,
+                     size_t smem, cudaStream_t stream, void **args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(block, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  SDV_CUDA(cudaLaunchKernelExC(&cfg, kernel, args));
+  return SD_OK;
+}
+
 }  // namespace sdv
 
 extern "C" const char *sd_version(void) { return "sdverify 0.1 (sm_103a)"; }

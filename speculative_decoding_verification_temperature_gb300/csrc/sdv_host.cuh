@@ -59,6 +59,12 @@ sd_status max_active_clusters(const void *kernel, int cl, size_t smem,
 sd_status launch_clusters(const void *kernel, int nclusters, int cl,
                           size_t smem, cudaStream_t stream, void **args);
 
+// Launch `kernel` (1-D grid) with programmatic stream serialisation: it may
+// start while the previous kernel in the stream is finishing, so it must
+// wait (griddep_wait) before reading anything that kernel writes.
+sd_status launch_pdl(const void *kernel, unsigned grid, unsigned block,
+                     size_t smem, cudaStream_t stream, void **args);
+
 // Row maps and output shape of a token tree whose nodes read rows of
 // another tensor (sdv_trie.cu): node u of sequence b reads target row
 // trow[b][u] of the sequence's trows rows and draft row drow[b][u] of its

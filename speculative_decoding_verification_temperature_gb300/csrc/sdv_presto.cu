@@ -56,6 +56,7 @@ __global__ void __launch_bounds__(kThreads)
   const int item = blockIdx.x / p.S, s = blockIdx.x % p.S;
   const int b = item / p.W, w = item % p.W;
   const size_t slot = (size_t)item * p.S + s;
+  griddep_wait();  // the previous merge's tree state and keys are final
   const bool active =
       (!p.frontier_node || p.frontier_node[(size_t)b * p.W + w] >= 0) &&
       (!p.n_nodes || (p.n_nodes[b] >= 0 && p.n_nodes[b] < p.budget));
@@ -125,6 +126,7 @@ __global__ void __launch_bounds__(kThreads)
       wf_offer_vals<VW>(wf, &top.th, z[u], v < sl.vend, v * VW);
     }
   }
+  griddep_launch_dependents();  // the merge may start launching
   // a NaN anywhere, or +inf (in q, or in log rho), makes the row unusable
   const int anybad =
       __syncthreads_or(!(worst < __builtin_huge_valf()) &&
@@ -199,6 +201,8 @@ __global__ void __launch_bounds__(kThreads)
   __shared__ int invalid_s;
   const int tid = threadIdx.x;
   const int b = blockIdx.x;
+  griddep_wait();  // every slice list of this depth is written
+  griddep_launch_dependents();
   const int n0 = p.n_nodes[b];
   if (n0 < 0 || n0 >= p.budget) return;  // block-uniform
   const int W = p.W, S = p.S, F = p.F;
@@ -303,6 +307,7 @@ __global__ void __launch_bounds__(kThreads)
   const int tid = threadIdx.x;
   const int b = blockIdx.x;
   const int S = p.S, F = p.F;
+  griddep_wait();  // every slice list is written
   for (int i = tid; i < S * F; i += kThreads)
     kbuf[i] = p.keys[(size_t)b * S * F + i];
   __syncthreads();
@@ -544,8 +549,13 @@ extern "C" sd_status sd_presto_expand(
   sp.stats = w.stats;
   sp.bad = w.bad;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  kern<<<(unsigned)(items * S), kThreads, 0, s>>>(sp);
-  SDV_CUDA(cudaGetLastError());
+  {
+    void *args[] = {&sp};
+    const sd_status st2 =
+        launch_pdl((const void *)kern, (unsigned)(items * S), kThreads, 0, s,
+                   args);
+    if (st2 != SD_OK) return st2;
+  }
   MergeParams mp;
   mp.keys = w.keys;
   mp.stats = w.stats;
@@ -564,9 +574,9 @@ extern "C" sd_status sd_presto_expand(
   mp.frontier_node = frontier_node;
   mp.frontier_score = frontier_score;
   mp.dev_status = dev_status;
-  presto_merge_kernel<<<B, kThreads, 0, s>>>(mp);
-  SDV_CUDA(cudaGetLastError());
-  return SD_OK;
+  void *margs[] = {&mp};
+  return launch_pdl((const void *)presto_merge_kernel, (unsigned)B, kThreads,
+                    0, s, margs);
 }
 
 extern "C" size_t sd_branch_fork_workspace(int B, int V, int k_max,
@@ -622,8 +632,13 @@ extern "C" sd_status sd_branch_fork(const void *draft_logits, sd_dtype dt,
   sp.stats = w.stats;
   sp.bad = w.bad;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  kern<<<(unsigned)((long long)B * S), kThreads, 0, s>>>(sp);
-  SDV_CUDA(cudaGetLastError());
+  {
+    void *args[] = {&sp};
+    const sd_status st2 = launch_pdl((const void *)kern,
+                                     (unsigned)((long long)B * S), kThreads,
+                                     0, s, args);
+    if (st2 != SD_OK) return st2;
+  }
   ForkParams fp;
   fp.keys = w.keys;
   fp.stats = w.stats;
@@ -640,7 +655,7 @@ extern "C" sd_status sd_branch_fork(const void *draft_logits, sd_dtype dt,
   fp.out_k = out_k;
   fp.out_tokens = out_tokens;
   fp.dev_status = dev_status;
-  fork_merge_kernel<<<B, kThreads, 0, s>>>(fp);
-  SDV_CUDA(cudaGetLastError());
-  return SD_OK;
+  void *fargs[] = {&fp};
+  return launch_pdl((const void *)fork_merge_kernel, (unsigned)B, kThreads, 0,
+                    s, fargs);
 }
