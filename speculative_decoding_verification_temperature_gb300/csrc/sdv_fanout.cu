@@ -26,6 +26,7 @@ struct FanParams {
   int32_t *dev_status;
   int nclusters;
   int seg_bytes;
+  int evict_first;  // read the rows with an L2 evict-first policy
 };
 
 struct FanSmem {
@@ -166,7 +167,12 @@ __global__ void __launch_bounds__(kThreads, SDV_FAN_MINB)
   rg.empty = bars + kStages;
   rg.dev_status = p.dev_status;
   if (threadIdx.x == 0) sh.top.th = 0;
-  if (RING) ring_init(rg);
+  if (RING) {
+    ring_init(rg);
+    // every row is read once: keep it from pushing out lines that a kernel
+    // running beside this one reads again
+    if (p.evict_first) rg.policy = l2_evict_first_policy();
+  }
   else __syncthreads();
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank(), CL = (int)cluster.num_blocks();
@@ -278,6 +284,7 @@ extern "C" sd_status sd_fanout_topk(const void *draft_logits, sd_dtype dt,
   prm.dev_status = dev_status;
   prm.nclusters = (int)want;
   prm.seg_bytes = 128;
+  prm.evict_first = env_int("SDV_FANOUT_L2_FIRST", 1) != 0;
   void *args[] = {&prm};
   return launch_clusters((const void *)kern, (int)want, CL, smem,
                          static_cast<cudaStream_t>(stream), args);

@@ -39,6 +39,7 @@ struct Ring {
   uint32_t used;       // thread 0: bit s set once stage s was filled
   uint32_t epar;       // thread 0: bit s: parity of the "empty" wait due
   int32_t *dev_status;
+  uint64_t policy;     // L2 cache policy of the copies (0: the default)
 };
 
 __device__ __forceinline__ void ring_init(Ring &rg) {
@@ -52,6 +53,7 @@ __device__ __forceinline__ void ring_init(Ring &rg) {
   rg.phase = 0;
   rg.used = 0;
   rg.epar = 0;
+  rg.policy = 0;
   __syncthreads();
 }
 
@@ -79,11 +81,21 @@ __device__ __forceinline__ void ring_pass(Ring &rg, const char *rowA,
     rg.used |= 1u << s;
     fence_proxy_async();
     mbar_expect_tx(&rg.full[s], bytes * ((STG == kStg && rowB) ? 2u : 1u));
-    bulk_g2s(rg.buf + (size_t)s * kStageVecs,
-             rowA + (size_t)(sl.vbeg + v0) * 16, bytes, &rg.full[s]);
-    if (STG == kStg && rowB)
-      bulk_g2s(rg.buf + (size_t)s * kStageVecs + kStg,
-               rowB + (size_t)(sl.vbeg + v0) * 16, bytes, &rg.full[s]);
+    if (rg.policy) {
+      bulk_g2s_hint(rg.buf + (size_t)s * kStageVecs,
+                    rowA + (size_t)(sl.vbeg + v0) * 16, bytes, &rg.full[s],
+                    rg.policy);
+      if (STG == kStg && rowB)
+        bulk_g2s_hint(rg.buf + (size_t)s * kStageVecs + kStg,
+                      rowB + (size_t)(sl.vbeg + v0) * 16, bytes, &rg.full[s],
+                      rg.policy);
+    } else {
+      bulk_g2s(rg.buf + (size_t)s * kStageVecs,
+               rowA + (size_t)(sl.vbeg + v0) * 16, bytes, &rg.full[s]);
+      if (STG == kStg && rowB)
+        bulk_g2s(rg.buf + (size_t)s * kStageVecs + kStg,
+                 rowB + (size_t)(sl.vbeg + v0) * 16, bytes, &rg.full[s]);
+    }
   };
   if (threadIdx.x == 0)
     for (int c = 0; c < nch && c < kStages; ++c) issue(c);

@@ -59,6 +59,26 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src,
       : "memory");
 }
 
+// An L2 policy that marks the lines it loads first to be evicted: for data
+// read once, so that it does not push out lines another phase re-reads.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;"
+               : "=l"(pol));
+  return pol;
+}
+
+// bulk_g2s with an L2 cache policy for the lines it reads.
+__device__ __forceinline__ void bulk_g2s_hint(void *dst, const void *src,
+                                              uint32_t bytes, uint64_t *bar,
+                                              uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(pol)
+      : "memory");
+}
+
 // Hint: bring `bytes` (multiple of 16, 16-byte aligned) into L2.
 __device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src),
