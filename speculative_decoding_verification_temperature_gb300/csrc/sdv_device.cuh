@@ -188,7 +188,10 @@ __device__ __forceinline__ void ms_add(MS &st, const Raw<DT, VW> &r,
     st.s *= ex2((st.m - vmax) * k2);
     st.m = vmax;
   }
-  const float mk = -st.m * k2;
+  // while nothing finite has been seen (m still the empty value, every
+  // element so far -inf) the offset would overflow (-m k2 = +inf, and
+  // -inf k2 + inf is NaN); 0 gives those elements their weight 0
+  const float mk = st.m > kMEmpty ? -st.m * k2 : 0.f;
   if constexpr (VW == 1) {
     st.s += ex2(fmaf(z[0], k2, mk));
   } else {

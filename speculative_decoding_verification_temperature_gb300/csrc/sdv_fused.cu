@@ -211,7 +211,8 @@ __device__ __forceinline__ void d_vec(MS &q, WarpFilter &wf, uint32_t *cta_th,
       q.s *= ex2((q.m - vmax) * k2);
       q.m = vmax;
     }
-    const float mk = -q.m * k2;
+    // nothing finite seen yet: offset 0 (the -inf elements weigh 0)
+    const float mk = q.m > kMEmpty ? -q.m * k2 : 0.f;
     if constexpr (VW == 1) {
       q.s += ex2(fmaf(z[0], k2, mk));
     } else {

@@ -370,6 +370,18 @@ static LinearKernel pick_linear(int dt, bool vec, bool ring, bool greedy) {
               : pick_linear_t<1, 8, false>(greedy);
 }
 
+size_t allrows_workspace(int B, int gamma, int V, sd_dtype dt);
+bool use_allrows(int B, int gamma, int V, sd_dtype dt, const void *target,
+                 const void *draft, float T, const float *out_resid,
+                 size_t ws_bytes);
+sd_status allrows_launch(const void *target, const void *draft, sd_dtype dt,
+                         long long d_seq_rows, const int32_t *tokens,
+                         const float *uniforms, int B, int gamma, int V,
+                         float T, int32_t *n_acc, int32_t *out_tokens,
+                         float *out_prob, float *out_accept,
+                         int32_t *dev_status, void *ws, size_t ws_bytes,
+                         cudaStream_t stream);
+
 sd_status linear_launch(const void *target, const void *draft, sd_dtype dt,
                         long long d_seq_rows, const int32_t *tokens,
                         const float *uniforms, int B, int gamma, int V,
@@ -377,6 +389,12 @@ sd_status linear_launch(const void *target, const void *draft, sd_dtype dt,
                         float *out_prob, float *out_accept, float *out_resid,
                         int32_t *dev_status, void *ws, size_t ws_bytes,
                         cudaStream_t stream) {
+  // small inputs: every row at once, then one decision per sequence
+  // (sdv_allrows.cu), instead of a barrier and a decision per position
+  if (use_allrows(B, gamma, V, dt, target, draft, T, out_resid, ws_bytes))
+    return allrows_launch(target, draft, dt, d_seq_rows, tokens, uniforms, B,
+                          gamma, V, T, n_acc, out_tokens, out_prob,
+                          out_accept, dev_status, ws, ws_bytes, stream);
   int sms = 0;
   sd_status st = check_device(&sms);
   if (st != SD_OK) return st;
@@ -460,9 +478,11 @@ bool use_wide(int B, int V, sd_dtype dt, const void *target,
 
 extern "C" size_t sd_verify_linear_workspace(int B, int gamma, int V,
                                              sd_dtype dt) {
-  const size_t w = (B > 0 && V > 0 && gamma >= 0)
-                       ? sdv::wide_workspace(B, gamma, V, dt)
-                       : 0;
+  size_t w = (B > 0 && V > 0 && gamma >= 0)
+                 ? sdv::wide_workspace(B, gamma, V, dt)
+                 : 0;
+  const size_t a = sdv::allrows_workspace(B, gamma, V, dt);
+  if (a > w) w = a;
   return w > 256 ? w : 256;
 }
 
