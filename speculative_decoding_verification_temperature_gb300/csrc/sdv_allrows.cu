@@ -88,7 +88,9 @@ struct ARSmem {
   DrawSmem draw;
 };
 
-// One CTA per sequence (launched as clusters of one CTA, for the draw).
+// One cluster per sequence: every CTA makes the same decision, and the
+// draw's pass over the two rows of position n is cut into one slice per
+// CTA (cluster_draw).
 template <int DT, int VW, bool GREEDY>
 __global__ void __launch_bounds__(kThreads)
     allrows_decide_kernel(const ARParams p) {
@@ -96,7 +98,8 @@ __global__ void __launch_bounds__(kThreads)
   __shared__ ARSmem sh;
   cg::cluster_group cluster = cg::this_cluster();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int b = blockIdx.x;
+  const int rank = (int)cluster.block_rank(), CL = (int)cluster.num_blocks();
+  const int b = (int)(blockIdx.x / CL);
   const int gamma = p.gamma, G1 = gamma + 1, V = p.V;
   const float k2 = p.k2;
   float *segmass = reinterpret_cast<float *>(dsm);
@@ -156,7 +159,7 @@ __global__ void __launch_bounds__(kThreads)
           accp = fminf(1.f, rho);
         }
       }
-      if (p.out_accept && j < gamma && !invalid)
+      if (rank == 0 && p.out_accept && j < gamma && !invalid)
         p.out_accept[(size_t)b * gamma + j] = accp;
       if (invalid) kind = 3;
       else if (j == gamma) kind = 2;
@@ -173,6 +176,7 @@ __global__ void __launch_bounds__(kThreads)
   __syncthreads();
   const int n = sh.n, kind = sh.kind, bad_token = sh.bad;
   if (kind == 3) {  // unusable row: outputs -1
+    if (rank != 0) return;
     for (int t = tid; t <= gamma; t += kThreads)
       p.out_tokens[(size_t)b * G1 + t] = -1;
     if (p.out_accept)
@@ -202,7 +206,7 @@ __global__ void __launch_bounds__(kThreads)
     W.mdk = sh.md.m * k2;
     W.cq = 1.f / sh.md.s;
     const float u = p.uniforms[(size_t)b * G1 + gamma];
-    const Slice sl = make_slice(V / VW, 0, 1);
+    const Slice sl = make_slice(V / VW, rank, CL);
     int par = 0;
     DrawOut o;
     for (int attempt = 0; attempt < 2; ++attempt) {
@@ -213,11 +217,13 @@ __global__ void __launch_bounds__(kThreads)
       has_q = false;
       __syncthreads();
     }
-    if (warp != 0) return;  // warp 0 holds the drawn token
+    // no CTA leaves while a peer may still read its shared memory
+    cluster.sync();
+    if (o.owner != rank || warp != 0) return;  // it holds the drawn token
     tok = o.t;
     prob = (float)((double)o.wt / o.N);
   } else {
-    if (warp != 0) return;
+    if (rank != 0 || warp != 0) return;
   }
   for (int t = lane; t <= gamma; t += 32) {
     int v = -1;
@@ -355,14 +361,13 @@ sd_status allrows_launch(const void *target, const void *draft, sd_dtype dt,
   }
   stats<<<(unsigned)((long long)B * rows * S), kThreads, 0, stream>>>(prm);
   SDV_CUDA(cudaGetLastError());
-  const size_t smem = ((size_t)((nvec + 31) / 32) * 4 + 127) / 128 * 128;
-  if (smem > 48 * 1024) {
-    SDV_CUDA(cudaFuncSetAttribute((const void *)decide,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)smem));
-  }
+  // the decision's cluster: the draw's slices of at least ~512 vectors
+  int CLd = 1;
+  while (CLd < 8 && nvec / (2 * CLd) >= 512) CLd *= 2;
+  const long long per = (nvec + CLd - 1) / CLd;
+  const size_t smem = ((size_t)((per + 31) / 32) * 4 + 127) / 128 * 128;
   void *args[] = {&prm};
-  return launch_clusters((const void *)decide, B, 1, smem, stream, args);
+  return launch_clusters((const void *)decide, B, CLd, smem, stream, args);
 }
 
 }  // namespace sdv
