@@ -79,3 +79,57 @@ def test_fanout_schedule_matches_oracle(K, budget, a, r):
 def test_fanout_schedule_rejects(K, budget, a, r):
     with pytest.raises(api.SdError):
         api.fanout_schedule(K, budget, a, r)
+
+
+@pytest.mark.parametrize("B,gamma,V,dt", [
+    (1, 4, 1000, 0), (32, 8, 32000, 1), (7, 3, 1001, 0), (300, 2, 640, 0),
+    (256, 8, 128256, 0), (64, 16, 152064, 1)])
+def test_linear_workspace_covers_both_paths(B, gamma, V, dt):
+    """The workspace query is host-only: it covers the all-rows path's
+    slice states (B rows S AM entries) whenever that path may be taken, and
+    never asks for less than 256 bytes."""
+    L = api.lib()
+    w = L.sd_verify_linear_workspace(B, gamma, V, dt)
+    assert w >= 256
+    eb = 4 if dt == 0 else 2
+    rows = 2 * gamma + 1
+    if B * rows * V * eb <= 64 << 20:
+        smax = min(32, max(1, V // 256))
+        assert w >= B * rows * smax * 12
+
+
+def test_later_workspace_queries_are_host_only():
+    L = api.lib()
+    assert L.sd_verify_kcand_trie_workspace(64, 8, 16, 152064, 1) >= \
+        256 + 6 * 64 * (1 + 8 * 16) * 4
+    assert L.sd_presto_expand_workspace(16, 8, 151936, 4, 1) >= 16 * 8 * 4 * 8
+    assert L.sd_branch_fork_workspace(64, 152064, 8, 1) >= 64 * 8 * 8
+    assert L.sd_verify_tree_det_workspace(16, 64, 151936, 1) >= 256
+
+
+def test_later_entry_points_validate_before_launch():
+    """Bad arguments are refused on the host (no device needed)."""
+    L = api.lib()
+    p = ctypes.c_void_p(16)
+    # K = 33 candidates (at most 32)
+    assert L.sd_verify_kcand_trie(p, p, 0, p, p, 1, 33, 2, 64, 1.0, p, p, p,
+                                  None, None, p, 1 << 20, None) \
+        == api.SD_ERR_INVALID_ARG
+    # 1 + K gamma above the tree node cap
+    assert L.sd_verify_kcand_trie(p, p, 0, p, p, 1, 32, 40, 64, 1.0, p, p, p,
+                                  None, None, p, 1 << 20, None) \
+        == api.SD_ERR_UNSUPPORTED
+    # PRESTO: T = 0 has no log q; W b above 1024
+    assert L.sd_presto_expand(p, 64, p, 0, 1, 4, 64, 0.0, 1.0, 2, 10, p, p,
+                              p, p, p, p, None, p, 1 << 20, None) \
+        == api.SD_ERR_INVALID_ARG
+    assert L.sd_presto_expand(p, 64, p, 0, 1, 64, 64, 1.0, 1.0, 17, 10, p,
+                              p, p, p, p, p, None, p, 1 << 20, None) \
+        == api.SD_ERR_UNSUPPORTED
+    # fork: k_max above 64
+    assert L.sd_branch_fork(p, 0, p, 1, 64, 1.0, 65, p, p, None, p, 1 << 20,
+                            None) == api.SD_ERR_INVALID_ARG
+    # empty batches are no-ops
+    assert L.sd_verify_tree_det(None, 0, None, None, None, 0, 3, 64, 1.0,
+                                None, None, None, None, None, None, 0,
+                                None) == api.SD_OK
