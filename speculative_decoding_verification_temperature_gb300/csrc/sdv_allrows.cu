@@ -151,10 +151,7 @@ __global__ void __launch_bounds__(kThreads)
         md = j < gamma ? sh.mrg[G1 + j] : ms_empty();
         invalid = !ms_valid(mt) || (j < gamma && !ms_valid(md));
         if (!invalid && j < gamma && !bad) {
-          // p(x)/q(x) with the same scaled exponents the draw uses
-          const float e = fmaf(sh.gzt[j], k2, -mt.m * k2) -
-                          fmaf(sh.gzd[j], k2, -md.m * k2);
-          const float rho = exp2f(e) * (md.s / mt.s);
+          const float rho = accept_ratio(sh.gzt[j], sh.gzd[j], mt, md, k2);
           acc = sh.gr[j] <= rho;
           accp = fminf(1.f, rho);
         }

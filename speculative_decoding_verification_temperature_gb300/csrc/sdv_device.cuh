@@ -207,6 +207,16 @@ __device__ __forceinline__ void ms_add(MS &st, const Raw<DT, VW> &r,
   }
 }
 
+// p(x)/q(x) of the draft token x from its target and draft logits zt, zd
+// and the rows' merged states: 2^((zt - m_t) k2 - (zd - m_d) k2) s_d / s_t,
+// with the same scaled exponents (fmaf(z, k2, -m k2)) that the draw's
+// weights use.  Every verify kernel takes its accept test from here.
+__device__ __forceinline__ float accept_ratio(float zt, float zd, MS mt,
+                                             MS md, float k2) {
+  const float e = fmaf(zt, k2, -mt.m * k2) - fmaf(zd, k2, -md.m * k2);
+  return exp2f(e) * (md.s / mt.s);
+}
+
 __device__ __forceinline__ bool ms_valid(MS st) {
   return st.m > -1.0e38f && isfinite(st.m) && isfinite(st.s) && st.s > 0.f;
 }

@@ -522,10 +522,7 @@ __global__ void __launch_bounds__(kThreads, SDV_FUSED_MINB)
           const MS mt = sh.mrg[0], md = sh.mrg[1];
           invalid = !ms_valid(mt) || (k < gamma && !ms_valid(md));
           if (!invalid && k < gamma && !bad) {
-            // p(x)/q(x) with the same scaled exponents the draw uses
-            const float e = fmaf(sh.gzt, k2, -mt.m * k2) -
-                            fmaf(sh.gzd, k2, -md.m * k2);
-            const float rho = exp2f(e) * (md.s / mt.s);
+            const float rho = accept_ratio(sh.gzt, sh.gzd, mt, md, k2);
             acc = sh.gr <= rho;
           }
           sh.mt = mt;

@@ -185,9 +185,8 @@ __global__ void __launch_bounds__(kThreads, 2)
             const MS mt = sh.mrg[r], md = sh.mrg[0];
             inv = !ms_valid(mt) || !ms_valid(md);
             if (!inv && !bad) {
-              const float e = fmaf(sh.gzt[k], k2, -mt.m * k2) -
-                              fmaf(sh.gzd[k], k2, -md.m * k2);
-              const float rho = exp2f(e) * (md.s / mt.s);
+              const float rho =
+                  accept_ratio(sh.gzt[k], sh.gzd[k], mt, md, k2);
               acc = sh.gr[k] <= rho;
             }
             if (!acc) {

@@ -226,10 +226,8 @@ __global__ void __launch_bounds__(kThreads, RING ? 4 : 2)
             const MS mt = sh.mrg[2 * t], md = sh.mrg[2 * t + 1];
             invalid = !ms_valid(mt) || (j < gamma && !ms_valid(md));
             if (!invalid && j < gamma && !bad) {
-              // p(x)/q(x) with the same scaled exponents the draw uses
-              const float e = fmaf(sh.gzt[t], k2, -mt.m * k2) -
-                              fmaf(sh.gzd[t], k2, -md.m * k2);
-              const float rho = exp2f(e) * (md.s / mt.s);
+              const float rho =
+                  accept_ratio(sh.gzt[t], sh.gzd[t], mt, md, k2);
               acc = sh.gr[t] <= rho;
               accp = fminf(1.f, rho);
             }

@@ -410,9 +410,8 @@ __global__ void __launch_bounds__(kThreads, 2)
           const int x = sh.tok[v];
           float rho = 0.f;
           if (x >= 0 && x < V) {
-            const float e = fmaf(sh.gzt[i], k2, -W.mtk) -
-                            fmaf(sh.gzd[i], k2, -W.mdk);
-            const double ratio = (double)(exp2f(e) * (md.s / mt.s));
+            const double ratio =
+                (double)accept_ratio(sh.gzt[i], sh.gzd[i], mt, md, k2);
             rho = (float)(fmax(0.0, ratio - c) / Nc);
           }
           if (sh.uni[v] <= rho) {
