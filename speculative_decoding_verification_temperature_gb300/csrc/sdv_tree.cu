@@ -369,13 +369,21 @@ __global__ void __launch_bounds__(kThreads, 2)
           if (tid == 0) sh.ex[ne] = x;
           ++ne;
           if (i + 1 < nk) {  // (the final draw forms its own mass)
-            __syncthreads();
-            Nr = det_mass<DT, VW>(cluster, sh.draw, segmass, ra, W, sl,
-                                  sh.ex, ne, -1.f, par);
-            __syncthreads();
-            if (!(Nr > 0.0)) {
-              zm = true;
-              break;
+            if ((double)wx <= 0.5 * Nr) {
+              // a minor token: N - w(x) loses at most a factor 2 of
+              // relative precision, and no pass or cluster barrier is
+              // needed (every CTA subtracts the same w(x))
+              Nr -= (double)wx;
+              __syncthreads();  // sh.ex[ne - 1] is seen by every thread
+            } else {  // a dominant one: sum the rest again
+              __syncthreads();
+              Nr = det_mass<DT, VW>(cluster, sh.draw, segmass, ra, W, sl,
+                                    sh.ex, ne, -1.f, par);
+              __syncthreads();
+              if (!(Nr > 0.0)) {
+                zm = true;
+                break;
+              }
             }
           }
         }
