@@ -22,7 +22,23 @@
  *  - Speculative Speculative Decoding / Saguaro, "speculation cache
  *    strategy", Theorem 12: geometric fan-out F_k = F_0 a^{k/(1+r)} (k < K),
  *    F_K = F_0 a^{K/(1+r)} (1-a)^{-1/(1+r)}, sum F_k = budget; the cache holds
- *    the top-F_k draft tokens of each lookahead position k.
+ *    the top-F_k draft tokens of each lookahead position k; "technical
+ *    architecture": a verification outcome is served from the cache when it
+ *    is in it.
+ *  - SpecDiff-2, "core method", greedy acceptance: a drafted token accepted
+ *    with the verifier's probability of it (deterministic drafts).
+ *  - "01 · Draft-then-verify", section 4 (standardised sampling): top-k and
+ *    nucleus filtering act on p and q before the ratio.
+ *  - PRESTO, sections 4.1-4.4: tree construction with the prefix-aligned
+ *    score log q + lambda log rho (a product of experts) under a node budget.
+ *  - SpecBranch, branch resampling: k = max(1, floor(k_max (1 - q(x_b))))
+ *    top-k branches at a branch point.
+ *
+ * Entry points: sd_verify_linear (and _static, _filtered), sd_verify_kcand,
+ * sd_verify_kcand_trie, sd_verify_tree, sd_verify_tree_det,
+ * sd_fanout_schedule (host), sd_fanout_topk, sd_fanout_hits,
+ * sd_verify_linear_fanout, sd_presto_init, sd_presto_expand,
+ * sd_branch_fork; each call with a workspace has a *_workspace query.
  *
  * Conventions shared by every call:
  *  - Every tensor argument is a DEVICE pointer owned by the caller, row-major
