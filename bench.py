@@ -5,7 +5,7 @@ Workload (one "step" = one verify round over the whole batch):
   fp32 logits; target ~ N(0, 3^2), draft = target + N(0, 1); draft tokens
   drawn from softmax(draft / T); T = 1.0; uniforms from splitmix64.
   Geometric fan-out a = 0.8, r = 1, K = 8, budget 64 -> F = [10,9,8,7,6,6,
-  5,4,9] on the 9 draft rows when the fused call is available.
+  5,4,9] on the 9 draft rows, on a second stream beside the verify.
 
 Prints one JSON line (rank 0).  `--impl reference` times the fp64 CPU
 oracle on the same workload instead (the only reference this method has).
