@@ -27,6 +27,7 @@
 #include <type_traits>
 
 #include "sdv_device.cuh"
+#include "sdv_hold.cuh"
 #include "sdv_host.cuh"
 #include "sdv_ring.cuh"
 #include "sdv_tma.cuh"
@@ -56,6 +57,7 @@ struct LinearParams {
   int seg_bytes;   // bytes of the segment-mass array (multiple of 128)
   int slice_vecs;  // capacity of each slice buffer in 16-byte vectors (TMA)
   int spec;        // let a cluster's last sequence read ahead (0: never)
+  int hold;        // sampled, TMA: keep each position's slices for the draw
 };
 
 constexpr int kMaxW = 4;  // positions per step when a cluster speculates
@@ -92,6 +94,7 @@ __global__ void __launch_bounds__(kThreads, RING ? 4 : 2)
   extern __shared__ __align__(128) unsigned char dsm[];
   __shared__ LinearSmem sh;
   __shared__ uint64_t bars[2 * kStages];
+  __shared__ uint64_t hbars[kHoldMax];
   using GR = GRow<DT, VW>;
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
@@ -111,6 +114,14 @@ __global__ void __launch_bounds__(kThreads, RING ? 4 : 2)
   rg.empty = bars + kStages;
   rg.dev_status = p.dev_status;
   if (RING) ring_init(rg);
+  // hold mode (sampled, TMA, one position per step): the position's slices
+  // stay in the same shared memory as the ring's stages until the draw
+  Hold hd;
+  hd.buf = rg.buf;
+  hd.full = hbars;
+  hd.dev_status = p.dev_status;
+  const bool hold = RING && !GREEDY && p.hold;
+  if (hold) hold_init(hd);
   auto trow_of = [&](int s, int j) {
     return tbase + ((size_t)s * (gamma + 1) + j) * rowb;
   };
@@ -154,7 +165,7 @@ __global__ void __launch_bounds__(kThreads, RING ? 4 : 2)
         sh.gzd[tid - 32] = zd;
         sh.gr[tid - 32] = r;
       }
-      if (RING && last_seq && p.spec >= 2 && tid == 0) {
+      if (RING && !hold && last_seq && p.spec >= 2 && tid == 0) {
         // the GPU is emptying out: ask for this step's and the next step's
         // rows at once (into L2), so the ring below streams from L2
         const uint32_t sb = (uint32_t)(sl.vend - sl.vbeg) * 16u;
@@ -178,8 +189,12 @@ __global__ void __launch_bounds__(kThreads, RING ? 4 : 2)
           if (tid == 0) sh.apart[par][t] = a;
         } else {
           MS st[2] = {ms_empty(), ms_empty()};
-          if constexpr (RING) ring_stats<DT, VW>(rg, trow, drow, sl, k2, st[0], st[1]);
-          else stats_pass<DT, VW>(GR{trow}, GR{drow}, has_d, sl, k2, st[0], st[1]);
+          if constexpr (RING) {
+            if (hold) hold_stats<DT, VW>(hd, trow, drow, sl, k2, st[0], st[1]);
+            else ring_stats<DT, VW>(rg, trow, drow, sl, k2, st[0], st[1]);
+          } else {
+            stats_pass<DT, VW>(GR{trow}, GR{drow}, has_d, sl, k2, st[0], st[1]);
+          }
           block_reduce_ms<2>(st, k2, sh.red);
           if (tid == 0) {
             sh.part[par][2 * t] = st[0];
@@ -251,7 +266,9 @@ __global__ void __launch_bounds__(kThreads, RING ? 4 : 2)
         last_seq = cluster.map_shared_rank(&sh, 0)->next_seq[seqpar] >= p.B;
         first = false;
       }
-      w = (last_seq && p.spec) ? min(2 * w, kMaxW) : 1;
+      // (hold mode keeps one position per step: the draw needs the slices
+      // of the position that decided)
+      w = (last_seq && p.spec && !hold) ? min(2 * w, kMaxW) : 1;
     }
     const int n = R.n, kind = R.kind, bad_token = R.bad;
 
@@ -309,8 +326,12 @@ __global__ void __launch_bounds__(kThreads, RING ? 4 : 2)
       DrawOut o;
       for (int attempt = 0; attempt < 2; ++attempt) {
         cluster_total(cluster, sh.draw, segmass, sl, u, par, [&] {
-          if constexpr (RING) ring_mass<DT, VW>(rg, trow, drow, has_q, W, sl, segmass);
-          else mass_pass<DT, VW>(ra, rb, has_q, W, sl, segmass);
+          if constexpr (RING) {
+            if (hold) held_mass<DT, VW>(hd, has_q, W, sl, segmass);
+            else ring_mass<DT, VW>(rg, trow, drow, has_q, W, sl, segmass);
+          } else {
+            mass_pass<DT, VW>(ra, rb, has_q, W, sl, segmass);
+          }
         });
         o = draw_pick<DT, VW>(cluster, sh.draw, segmass, ra, rb, has_q, W, sl);
         if (o.owner >= 0) break;
@@ -407,11 +428,30 @@ sd_status linear_launch(const void *target, const void *draft, sd_dtype dt,
   // on the 256 x 128256 fp32 workload: 8 beats 16)
   int CL = choose_cluster(nvec);
   if (B >= 128 && CL > 8 && env_int("SDV_CLUSTER", 0) == 0) CL = 8;
+  const bool ring = vec && env_int("SDV_NO_TMA", 0) == 0;
+  // hold mode (SDV_HOLD=1; sampled, TMA): every CTA keeps its slices of the
+  // current position in shared memory for the draw.  Clusters grow until a
+  // held slice takes at most 64 KB (three CTAs per SM).
+  auto held_bytes = [&](int cl) {
+    const long long pc = (nvec + cl - 1) / cl;
+    return (size_t)((pc + kStg - 1) / kStg) * kStageVecs * 16;
+  };
+  bool hold = ring && !greedy && env_int("SDV_HOLD", 0) != 0;
+  if (hold) {
+    int cl = CL;
+    if (env_int("SDV_CLUSTER", 0) == 0)
+      while (cl < 16 && held_bytes(cl) > 64 * 1024) cl *= 2;
+    const long long pc = (nvec + cl - 1) / cl;
+    if ((pc + kStg - 1) / kStg <= kHoldMax && held_bytes(cl) <= 192 * 1024)
+      CL = cl;
+    else
+      hold = false;
+  }
   const long long per_cta = (nvec + CL - 1) / CL;
   const size_t seg_bytes = ((size_t)((per_cta + 31) / 32) * 4 + 127) / 128 * 128;
-  const bool ring = vec && env_int("SDV_NO_TMA", 0) == 0;
-  const size_t smem = seg_bytes + (ring ? kRingBytes : 0);
-  if (smem > 96 * 1024)
+  const size_t smem =
+      seg_bytes + (hold ? held_bytes(CL) : ring ? (size_t)kRingBytes : 0);
+  if (smem > (hold ? 200 : 96) * 1024)
     return fail(SD_ERR_UNSUPPORTED, "V=%d needs %zu B of shared memory", V,
                 smem);
   LinearKernel kern = pick_linear(dt, vec, ring, greedy);
@@ -439,7 +479,8 @@ sd_status linear_launch(const void *target, const void *draft, sd_dtype dt,
   prm.nclusters = nclusters;
   prm.seg_bytes = (int)seg_bytes;
   prm.slice_vecs = (int)per_cta;
-  prm.spec = env_int("SDV_SPEC", 1);
+  prm.spec = hold ? 0 : env_int("SDV_SPEC", 1);
+  prm.hold = hold ? 1 : 0;
   if (B > nclusters) {
     if (!ws || ws_bytes < 256)
       return fail(SD_ERR_INVALID_ARG, "workspace of >= 256 bytes required");

@@ -1,9 +1,11 @@
 """Both paths of sd_verify_linear against the oracle on the same inputs:
 the per-position cluster kernel (SDV_ALLROWS=0) and the all-rows path for
 small inputs (SDV_ALLROWS=2 forces it wherever its workspace and shared
-memory allow).  Small and odd sizes, both dtypes, unaligned rows, gamma 0,
-T in {0, 0.7, 1}, bad tokens and non-finite rows, the queue path, the
-accept-probability output; and the two paths agree with each other."""
+memory allow), plus the cluster kernel's hold mode (SDV_HOLD=1: each
+position's slices kept in shared memory for the draw).  Small and odd
+sizes, both dtypes, unaligned rows, gamma 0, T in {0, 0.7, 1}, bad tokens
+and non-finite rows, the queue path, the accept-probability output; and
+the two paths agree with each other."""
 import numpy as np
 import pytest
 import torch
@@ -21,14 +23,16 @@ def run(case, **kw):
                              case.T, **kw)
 
 
-@pytest.mark.parametrize("mode", ["0", "2"])
+@pytest.mark.parametrize("mode", ["0", "2", "0-hold"])
 @pytest.mark.parametrize("T", [0.0, 0.7, 1.0])
 @pytest.mark.parametrize("B,gamma,V,dtype", [
     (1, 4, 1000, torch.float32), (32, 8, 32000, torch.bfloat16),
     (7, 3, 1001, torch.float32), (5, 0, 4096, torch.bfloat16),
     (300, 2, 640, torch.float32), (3, 16, 50000, torch.float32)])
 def test_paths_against_oracle(monkeypatch, mode, T, B, gamma, V, dtype):
-    monkeypatch.setenv("SDV_ALLROWS", mode)
+    monkeypatch.setenv("SDV_ALLROWS", mode.split("-")[0])
+    if mode.endswith("hold"):
+        monkeypatch.setenv("SDV_HOLD", "1")
     c = to_device(synth.linear_case(B, gamma, V, dtype, T, seed=B + V + gamma,
                                     sigma_t=2.0, sigma_d=1.0))
     g = run(c, want_accept=True)
@@ -42,9 +46,11 @@ def test_paths_against_oracle(monkeypatch, mode, T, B, gamma, V, dtype):
         assert np.all(host(g["accept"])[~ev] == -1)
 
 
-@pytest.mark.parametrize("mode", ["0", "2"])
+@pytest.mark.parametrize("mode", ["0", "2", "0-hold"])
 def test_paths_edge_rows(monkeypatch, mode):
-    monkeypatch.setenv("SDV_ALLROWS", mode)
+    monkeypatch.setenv("SDV_ALLROWS", mode.split("-")[0])
+    if mode.endswith("hold"):
+        monkeypatch.setenv("SDV_HOLD", "1")
     c = synth.linear_case(8, 4, 2000, torch.float32, 1.0, seed=77)
     c.tokens[1, 0] = 10**6            # bad token, tested first
     c.target[2, 1, 5] = float("nan")  # unusable target row
