@@ -120,6 +120,10 @@ MUTANTS = [
     ("presto_parent_slot", "parent[v] = old_fn[all[i].w];",
      "parent[v] = old_fn[0];", 1,
      ["test_presto_golden", "test_presto_construction_invariants"]),
+    ("softmax_no_max_subtraction",
+     "p[j] = exp((logit_at(base, dtype, off + (size_t)j) - m) / T);",
+     "p[j] = exp(logit_at(base, dtype, off + (size_t)j) / T);", 1,
+     ["test_softmax_shift_invariance"]),
     ("fork_floor", "int k = k_max - (int)ceil(y);",
      "int k = k_max - (int)floor(y);", 1,
      ["test_branch_fork_golden"]),
@@ -152,6 +156,7 @@ def _run_pin(name):
                                         dict(V=5, gamma=2)],
         "test_tree_chain_equals_linear": [dict(T=1.0)],
         "test_kcand_trie_one_candidate_equals_linear": [dict(T=1.0)],
+        "test_softmax_shift_invariance": [dict(T=1.0)],
         "test_filtered_first_token_marginal_is_filtered_p": [
             dict(top_k=5, top_p=1.0), dict(top_k=4, top_p=0.6)],
     }.get(name, [dict()])

@@ -234,6 +234,40 @@ def test_truncated_geometric_length_law():
 
 
 # ------------------------------------------------------ greedy (2.2)
+@pytest.mark.parametrize("T", [1.0, 0.7, 0.0])
+def test_softmax_shift_invariance(T):
+    """The verify reads p = softmax(z / T) and q = softmax(z_d / T) only
+    ("01 · Draft-then-verify" section 1), and a softmax does not change
+    when every logit of its row moves by the same constant; the greedy rule
+    compares argmaxes, which do not change either.  On a 2^-10 grid the
+    logits stay exact in fp32 after shifts of -1024, 1024 or 4096, and the
+    shift cancels exactly in (z + c) - (m + c), so the oracle must return
+    the same counts, tokens and probabilities bit for bit, row by row.  (A
+    softmax without its max subtraction overflows at exp(1024).)"""
+    rng = np.random.default_rng(2024)
+    B, gamma, V = 48, 4, 50
+    grid = lambda x: np.round(x * 1024.0) / 1024.0
+    zt = grid(rng.normal(0.0, 3.0, (B, gamma + 1, V)))
+    zd = grid(zt[:, :gamma] + rng.normal(0.0, 1.0, (B, gamma, V)))
+    x = rng.integers(0, V, (B, gamma)).astype(np.int32)
+    # draft tokens that are often accepted: the draft row's argmax
+    x[::2] = np.argmax(zd[::2], axis=2)
+    u = ((rng.integers(0, 2**23, (B, gamma + 1)) + 0.5) / 2**23).astype(
+        np.float32)
+    ct = rng.choice([-1024.0, 1024.0, 4096.0], (B, gamma + 1, 1))
+    cd = rng.choice([-1024.0, 1024.0, 4096.0], (B, gamma, 1))
+    f = lambda z: np.ascontiguousarray(z, np.float32)
+    assert np.array_equal(f(zt + ct).astype(np.float64), zt + ct)
+    assert np.array_equal(f(zd + cd).astype(np.float64), zd + cd)
+    d0 = None if T == 0 else f(zd)
+    d1 = None if T == 0 else f(zd + cd)
+    a = oracle.verify_linear(f(zt), d0, x, u, T)
+    b = oracle.verify_linear(f(zt + ct), d1, x, u, T)
+    assert np.all(a["n"] >= 0) and 0 < a["n"].sum() < B * gamma
+    for k in ("n", "tokens", "prob"):
+        np.testing.assert_array_equal(a[k], b[k], err_msg=k)
+
+
 def test_greedy_is_id_equality_with_argmax():
     """T = 0: accept iff the draft id equals argmax p (section 2.2), ties to
     the lowest index; the correction/bonus is argmax of row n.  Compared with
