@@ -120,6 +120,15 @@ MUTANTS = [
     ("presto_parent_slot", "parent[v] = old_fn[all[i].w];",
      "parent[v] = old_fn[0];", 1,
      ["test_presto_golden", "test_presto_construction_invariants"]),
+    ("scan_reads_past_rejection", "if (!ok) { rejected = 1; break; }",
+     "if (!ok) { rejected = 1; continue; }", 1,
+     ["test_rows_after_the_decision_are_never_read"]),
+    ("greedy_scan_reads_past_rejection", "if (!ok) break;",
+     "if (!ok) continue;", 1,
+     ["test_rows_after_the_decision_are_never_read"]),
+    ("masked_token_invalidates_row", "if (isnan(z) || z == INFINITY) return 0;",
+     "if (isnan(z) || isinf(z)) return 0;", 1,
+     ["test_minus_infinity_is_a_token_of_probability_zero"]),
     ("softmax_no_max_subtraction",
      "p[j] = exp((logit_at(base, dtype, off + (size_t)j) - m) / T);",
      "p[j] = exp(logit_at(base, dtype, off + (size_t)j) / T);", 1,
@@ -157,6 +166,9 @@ def _run_pin(name):
         "test_tree_chain_equals_linear": [dict(T=1.0)],
         "test_kcand_trie_one_candidate_equals_linear": [dict(T=1.0)],
         "test_softmax_shift_invariance": [dict(T=1.0)],
+        "test_rows_after_the_decision_are_never_read": [dict(T=1.0),
+                                                        dict(T=0.0)],
+        "test_minus_infinity_is_a_token_of_probability_zero": [dict(T=1.0)],
         "test_filtered_first_token_marginal_is_filtered_p": [
             dict(top_k=5, top_p=1.0), dict(top_k=4, top_p=0.6)],
     }.get(name, [dict()])

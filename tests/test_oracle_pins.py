@@ -268,6 +268,71 @@ def test_softmax_shift_invariance(T):
         np.testing.assert_array_equal(a[k], b[k], err_msg=k)
 
 
+def _linear_case(seed, B=40, gamma=5, V=60):
+    rng = np.random.default_rng(seed)
+    zt = rng.normal(0.0, 2.0, (B, gamma + 1, V)).astype(np.float32)
+    zd = (zt[:, :gamma] + rng.normal(0.0, 1.0, (B, gamma, V))).astype(
+        np.float32)
+    x = np.argmax(zd, axis=2).astype(np.int32)
+    x[::3] = rng.integers(0, V, (len(x[::3]), gamma))
+    u = ((rng.integers(0, 2**23, (B, gamma + 1)) + 0.5) / 2**23).astype(
+        np.float32)
+    return zt, zd, x, u
+
+
+@pytest.mark.parametrize("T", [1.0, 0.0])
+def test_rows_after_the_decision_are_never_read(T):
+    """Algorithm 1 ("01 · Draft-then-verify" section 1) stops at the first
+    rejection: what the rows after it hold cannot change the round.  Those
+    rows are overwritten with NaN and +inf (which would invalidate a round
+    that read them) and every output stays the same; a NaN in target row n,
+    which the round does read, invalidates it (n = -1, every token -1,
+    status bit 2: the reading for unusable rows)."""
+    zt, zd, x, u = _linear_case(7)
+    B, G1, V = zt.shape
+    gamma = G1 - 1
+    d = None if T == 0 else zd
+    a = oracle.verify_linear(zt, d, x, u, T)
+    n = a["n"]
+    assert np.all(n >= 0) and np.any(n < gamma) and np.any(n > 0)
+    zt2, zd2 = zt.copy(), zd.copy()
+    for b in range(B):
+        zt2[b, n[b] + 1:, ::2] = np.nan
+        zt2[b, n[b] + 1:, 1::2] = np.inf
+        zd2[b, n[b] + 1:] = np.nan
+    b2 = oracle.verify_linear(zt2, None if T == 0 else zd2, x, u, T)
+    for k in ("n", "tokens", "prob", "status"):
+        np.testing.assert_array_equal(a[k], b2[k], err_msg=k)
+    zt3 = zt.copy()
+    zt3[np.arange(B), n, 3] = np.nan
+    c = oracle.verify_linear(zt3, d, x, u, T)
+    assert np.all(c["n"] == -1) and np.all(c["tokens"] == -1)
+    assert np.all(c["status"] & 2)
+
+
+@pytest.mark.parametrize("T", [1.0, 0.7])
+def test_minus_infinity_is_a_token_of_probability_zero(T):
+    """A -inf logit is a masked token (the reading for masked tokens): the
+    round equals the one where that logit is so low that exp underflows to
+    exactly 0 in double, and a masked draft token is never accepted."""
+    zt, zd, x, u = _linear_case(8)
+    B, G1, V = zt.shape
+    mask = np.zeros_like(zt, bool)
+    mask[:, :, V // 2:] = True
+    mask[:, :, 0] = False             # keep one low-id token unmasked
+    x[:, 0] = V - 1                   # the first draft token is masked
+    low = np.float32(-1e30)           # exp((-1e30 - m) / T) == 0.0 exactly
+    zinf, zlow = zt.copy(), zt.copy()
+    zinf[mask] = -np.inf
+    zlow[mask] = low
+    a = oracle.verify_linear(zinf, zd, x, u, T)
+    b = oracle.verify_linear(zlow, zd, x, u, T)
+    for k in ("n", "tokens", "prob", "status"):
+        np.testing.assert_array_equal(a[k], b[k], err_msg=k)
+    assert np.all(a["n"] == 0) and np.all(a["status"] == 0)
+    assert np.all(a["tokens"][:, 0] < V // 2)  # drawn among unmasked ones
+
+
 def test_greedy_is_id_equality_with_argmax():
     """T = 0: accept iff the draft id equals argmax p (section 2.2), ties to
     the lowest index; the correction/bonus is argmax of row n.  Compared with
