@@ -126,6 +126,13 @@ MUTANTS = [
     ("greedy_scan_reads_past_rejection", "if (!ok) break;",
      "if (!ok) continue;", 1,
      ["test_rows_after_the_decision_are_never_read"]),
+    ("kcand_scan_reads_past_rejection", "if (!ok) break;",
+     "if (!ok) continue;", 2,
+     ["test_kcand_rows_after_each_scan_are_never_read"]),
+    ("tree_reads_leaf_draft_row",
+     "if (has_child && !softmax_row(draft, dtype, off, V, T, q)) {",
+     "if (!softmax_row(draft, dtype, off, V, T, q)) {", 1,
+     ["test_tree_rows_off_the_path_are_never_read"]),
     ("masked_token_invalidates_row", "if (isnan(z) || z == INFINITY) return 0;",
      "if (isnan(z) || isinf(z)) return 0;", 1,
      ["test_minus_infinity_is_a_token_of_probability_zero"]),
@@ -169,6 +176,10 @@ def _run_pin(name):
         "test_rows_after_the_decision_are_never_read": [dict(T=1.0),
                                                         dict(T=0.0)],
         "test_minus_infinity_is_a_token_of_probability_zero": [dict(T=1.0)],
+        "test_kcand_rows_after_each_scan_are_never_read": [dict(T=1.0),
+                                                           dict(T=0.0)],
+        "test_tree_rows_off_the_path_are_never_read": [
+            dict(rule="sibling", T=1.0), dict(rule="det", T=1.0)],
         "test_filtered_first_token_marginal_is_filtered_p": [
             dict(top_k=5, top_p=1.0), dict(top_k=4, top_p=0.6)],
     }.get(name, [dict()])

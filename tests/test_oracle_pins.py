@@ -439,6 +439,37 @@ def test_kcand_max_streak_law_bruteforce():
         assert abs(got - expect) < 5 * math.sqrt(expect * (1 - expect) / B)
 
 
+@pytest.mark.parametrize("T", [1.0, 0.0])
+def test_kcand_rows_after_each_scan_are_never_read(T):
+    """Each candidate is scanned with the linear rule up to its first
+    rejection (SpecDiff-2, "core method"), and only the selected candidate
+    draws: its row at position n, or its bonus row gamma when its streak is
+    complete, and the shared draft row n.  Every other row is overwritten
+    with NaN and the round stays the same."""
+    import torch
+    c = synth.kcand_case(16, 4, 5, 200, torch.float32, 1.0, seed=9,
+                         sigma_t=1.0, sigma_d=0.4, sigma_k=0.3)
+    zt, zd = synth.host_logits(c.target), synth.host_logits(c.draft)
+    x, u = c.tokens.numpy(), c.uniforms.numpy()
+    B, K, G1, V = zt.shape
+    gamma = G1 - 1
+    o = oracle.verify_kcand(zt, zd, x, u, T)
+    npc, n, ks = o["n_per_cand"], o["n"], o["k"]
+    assert np.all(n >= 0) and np.any(n > 0) and np.any(n < gamma)
+    zt2, zd2 = np.full_like(zt, np.nan), np.full_like(zd, np.nan)
+    for b in range(B):
+        for k in range(K):
+            last = min(int(npc[b, k]), gamma - 1)
+            zt2[b, k, :last + 1] = zt[b, k, :last + 1]
+        zt2[b, ks[b], n[b]] = zt[b, ks[b], n[b]]
+        if T > 0:
+            zd2[b, :min(int(n[b]), gamma - 1) + 1] = \
+                zd[b, :min(int(n[b]), gamma - 1) + 1]
+    o2 = oracle.verify_kcand(zt2, zd2, x, u, T)
+    for k in ("n", "k", "n_per_cand", "tokens", "prob", "status"):
+        np.testing.assert_array_equal(o[k], o2[k], err_msg=k)
+
+
 def test_kcand_selection_bias_counterexample():
     """Longest-streak selection is not lossless for K > 1: V = 2,
     p = (1/2, 1/2), both candidates draft token 0 with q = delta_0.  Each
@@ -542,6 +573,47 @@ def test_tree_topk_sibling_counterexample():
     o = oracle.verify_tree(tile_rows(zt, B), tile_rows(zq, B), parent, ntok,
                            synth.uniforms(99, (B, 3)), 1.0)
     assert np.all(o["tokens"][:, 0] == 0) and np.all(o["nodes"][:, 0] == 1)
+
+
+@pytest.mark.parametrize("rule,T", [("sibling", 1.0), ("sibling", 0.0),
+                                    ("det", 1.0)])
+def test_tree_rows_off_the_path_are_never_read(rule, T):
+    """The walk reads the target row of the root and of each accepted node
+    and, under the sibling rule, the draft row of each of those that has
+    children: the q their children were drafted from (PRESTO section 2.1;
+    "01 · Draft-then-verify" section 2.1).  The deterministic-draft rule
+    reads no draft row.  Every other row is overwritten with NaN and the
+    round stays the same; a NaN in a visited node's target row makes it
+    unusable (status bit 2)."""
+    import torch
+    c = synth.tree_case(12, 40, 300, torch.float32, 1.0, seed=5,
+                        sigma_t=1.0, sigma_d=0.5, branch=4, max_depth=5)
+    zt, zd = synth.host_logits(c.target), synth.host_logits(c.draft)
+    par, tok, u = c.parent.numpy(), c.node_tokens.numpy(), c.uniforms.numpy()
+
+    def run(a, d):
+        if rule == "det":
+            return oracle.verify_tree_det(a, par, tok, u, T)
+        return oracle.verify_tree(a, d, par, tok, u, T)
+
+    o = run(zt, zd)
+    B = zt.shape[0]
+    assert np.all(o["n"] >= 0) and np.any(o["n"] > 0)
+    zt2, zd2 = np.full_like(zt, np.nan), np.full_like(zd, np.nan)
+    for b in range(B):
+        for v in [0] + [int(x) for x in o["nodes"][b, :o["n"][b]]]:
+            zt2[b, v] = zt[b, v]
+            if rule == "sibling" and T > 0 and np.any(par[b] == v):
+                zd2[b, v] = zd[b, v]
+    o2 = run(zt2, zd2)
+    for k in ("n", "tokens", "nodes", "prob", "status"):
+        np.testing.assert_array_equal(o[k], o2[k], err_msg=k)
+    zt3 = zt.copy()
+    last = [int(o["nodes"][b, o["n"][b] - 1]) if o["n"][b] else 0
+            for b in range(B)]
+    zt3[np.arange(B), last, 7] = np.nan
+    o3 = run(zt3, zd)
+    assert np.all(o3["n"] == -1) and np.all(o3["status"] & 2)
 
 
 def test_tree_greedy_follows_argmax_child():
