@@ -116,7 +116,10 @@ def _p(t):
 def _dev(t, device, name, dtype=None):
     if t is None:
         return None
-    if not t.is_cuda or t.device != device:
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor (there is no CPU path)"
+                         % name)
+    if t.device != device:
         raise ValueError("%s must live on %s" % (name, device))
     if not t.is_contiguous():
         raise ValueError("%s must be contiguous" % name)
@@ -377,6 +380,9 @@ class PrestoTree:
     node arrays [B, budget], frontier [B, W]."""
 
     def __init__(self, B, W, budget, device):
+        if torch.device(device).type != "cuda":
+            raise ValueError("PrestoTree must live on a CUDA device (there "
+                             "is no CPU path)")
         self.B, self.W, self.budget = B, W, budget
         i32 = dict(dtype=torch.int32, device=device)
         f32 = dict(dtype=torch.float32, device=device)

@@ -1,13 +1,15 @@
 """Host-side checks of the C ABI that need no GPU: the library loads and
 exports every entry point include/sd_verify.h declares, argument validation
-rejects bad calls before any launch, and the host-only fan-out schedule
-matches the oracle."""
+rejects bad calls before any launch, the host-only fan-out schedule
+matches the oracle, and the Python binding refuses host tensors (there is
+no CPU path)."""
 import ctypes
 import os
 import re
 
 import numpy as np
 import pytest
+import torch
 
 import oracle
 from speculative_decoding_verification_temperature_gb300 import api
@@ -133,3 +135,48 @@ def test_later_entry_points_validate_before_launch():
     assert L.sd_verify_tree_det(None, 0, None, None, None, 0, 3, 64, 1.0,
                                 None, None, None, None, None, None, 0,
                                 None) == api.SD_OK
+
+
+def _cpu_calls():
+    """One call of every Python entry point, with CPU tensors."""
+    from speculative_decoding_verification_temperature_gb300 import api
+    B, g, V = 2, 3, 64
+    i32 = dict(dtype=torch.int32)
+    t, d = torch.zeros(B, g + 1, V), torch.zeros(B, g, V)
+    x, u = torch.zeros(B, g, **i32), torch.full((B, g + 1), 0.5)
+    kt, kx = torch.zeros(B, 2, g + 1, V), torch.zeros(B, 2, g, **i32)
+    ku = torch.full((B, 2, g + 1), 0.5)
+    par = torch.tensor([[-1, 0, 0, 1]] * B, **i32)
+    nt, nu = torch.zeros(B, 4, **i32), torch.full((B, 4), 0.5)
+    return {
+        "verify_linear": lambda: api.verify_linear(t, d, x, u, 1.0),
+        "verify_linear_static":
+            lambda: api.verify_linear_static(t, d, x, u, 1.0),
+        "verify_linear_filtered":
+            lambda: api.verify_linear_filtered(t, d, x, u, 1.0, 5),
+        "verify_linear_fanout": lambda: api.verify_linear_fanout(
+            t, torch.zeros(B, g + 1, V), x, u, 1.0, [2] * (g + 1)),
+        "verify_kcand": lambda: api.verify_kcand(kt, d, kx, ku, 1.0),
+        "verify_kcand_trie":
+            lambda: api.verify_kcand_trie(kt, d, kx, ku, 1.0),
+        "verify_tree": lambda: api.verify_tree(
+            torch.zeros(B, 4, V), torch.zeros(B, 4, V), par, nt, nu, 1.0),
+        "verify_tree_det": lambda: api.verify_tree_det(
+            torch.zeros(B, 4, V), par, nt, nu, 1.0),
+        "branch_fork": lambda: api.branch_fork(
+            torch.zeros(B, V), torch.zeros(B, **i32), 1.0, 4),
+        "fanout_topk": lambda: api.fanout_topk(torch.zeros(B, 3, V),
+                                               [2, 2, 2]),
+        "fanout_hits": lambda: api.fanout_hits(
+            torch.zeros(B, **i32), torch.zeros(B, 3, **i32),
+            torch.zeros(B, 6, **i32), [2, 2, 2]),
+        "PrestoTree": lambda: api.PrestoTree(B, 2, 10, "cpu"),
+    }
+
+
+@pytest.mark.parametrize("name", sorted(_cpu_calls()))
+def test_binding_refuses_cpu_tensors(name):
+    """There is no CPU path: every entry point of the binding refuses host
+    tensors with a ValueError before anything reaches the library."""
+    with pytest.raises(ValueError, match="CUDA"):
+        _cpu_calls()[name]()
