@@ -315,10 +315,24 @@ def gpu_arm(args, rank, world):
     }
     if args.e2e_steps > 0:
         res["e2e"] = e2e_arm(args, sets, dev, ws, world, F)
+    checks = [] if rank == 0 and args.oracle_seqs > 0 else None
     if args.aux_steps > 0:
-        res["other_workloads"] = other_workloads(args, dev, peak)
+        res["other_workloads"] = other_workloads(args, dev, peak, checks)
     if rank == 0 and args.oracle_seqs > 0:
-        res["cpu_baseline"] = cpu_baseline(sets, args.oracle_seqs, F)
+        c = sets[0]
+        g = {k: v.cpu().numpy() for k, v in verify(c).items()}
+        g["fan_tokens"] = fanout(c)["tokens"].cpu().numpy()
+        res["cpu_baseline"], res["flagged"] = cpu_baseline(
+            sets, args.oracle_seqs, F, g)
+        res["flagged"]["what"] = (
+            "oracle over one round of the step's inputs: accept tests within "
+            "1e-5 of their threshold per accept test made, final draws "
+            "within 1e-5 of a CDF boundary per draw (and those whose token "
+            "differs from the oracle's, inside its admissible range); "
+            "mismatches = sequences differing from the oracle elsewhere")
+        for name, kind, case, out, Tw, extra in checks or []:
+            res["other_workloads"][name]["flagged"] = oracle_check(
+                kind, case, out, Tw, extra)
     return res
 
 
@@ -481,12 +495,15 @@ def _time(fn, sets, steps, warmup, dev):
     return a.elapsed_time(b) / steps  # ms per round
 
 
-def other_workloads(args, dev, peak):
+def other_workloads(args, dev, peak, checks=None):
     """rounds/s, logit bytes the method read (counted from the outputs) and
-    the HBM fraction for the other four workloads, measured in this run."""
+    the HBM fraction for the other workloads, measured in this run.  When
+    `checks` is a list, each workload appends one input set and its GPU
+    outputs to it, for the oracle comparison of the CPU-baseline leg."""
     from speculative_decoding_verification_temperature_gb300 import api
     out = {}
     steps = args.aux_steps
+    args.checks = checks
 
     def entry(name, ms, rows, V, elt, full_rows, extra=None):
         gbs = rows * V * elt / (ms / 1e3) / 1e9
@@ -607,6 +624,8 @@ def _filtered(args, dev, entry, steps):
                     for c in sets])
     entry("filtered_k50_p0.9", ms, rows, V, ELT, B * (2 * GAMMA + 1),
           {"top_k": 50, "top_p": 0.9, "T": 1.0})
+    _register(args, "filtered_k50_p0.9", "filtered", sets[0], fn(sets[0]),
+              1.0, top_k=50, top_p=0.9)
     del sets
 
 
@@ -654,6 +673,10 @@ def _tiny(args, dev, entry, steps):
                     for c in sets[:16]])
     entry("tiny", ms, rows, 1000, 4, 9, {"note": "launch-latency bound",
                                           "timing": how})
+    # the oracle check: 1000 tiny rounds in one batch (same inputs recipe)
+    big = synth.linear_case(1000, 4, 1000, torch.float32, 1.0, seed=1000,
+                            sigma_t=2.0, sigma_d=1.0, device=dev)
+    _register(args, "tiny", "linear", big, fn(big), 1.0)
 
 
 def _linear(args, dev, entry, steps):
@@ -671,6 +694,7 @@ def _linear(args, dev, entry, steps):
                         for c in sets])
         full = 32 * (9 if T == 0 else 17)
         entry("linear_T%g" % T, ms, rows, 32000, 2, full, {"timing": how})
+        _register(args, "linear_T%g" % T, "linear", sets[0], fn(sets[0]), T)
         del sets
 
 
@@ -689,6 +713,7 @@ def _kcand(args, dev, entry, steps):
     acc = [float(fn(c)["n"].float().mean()) for c in sets]
     entry("kcand", ms, np.mean(rows), 152064, 2, 64 * (8 * 17 + 16),
           {"mean_accepted": float(np.mean(acc))})
+    _register(args, "kcand", "kcand", sets[0], fn(sets[0]), 1.0)
     # the same candidates verified as one token tree (distribution-
     # preserving): target and draft rows of the visited nodes
     ft = lambda c: api.verify_kcand_trie(c.target, c.draft, c.tokens,
@@ -701,6 +726,7 @@ def _kcand(args, dev, entry, steps):
         acc.append(float(n.mean()))
     entry("kcand_trie", ms, np.mean(rows), 152064, 2, 64 * (8 * 17 + 16),
           {"mean_accepted": float(np.mean(acc))})
+    _register(args, "kcand_trie", "kcand_trie", sets[0], ft(sets[0]), 1.0)
     del sets
 
 
@@ -720,6 +746,7 @@ def _tree(args, dev, entry, steps):
         acc.append(float(o["n"].float().mean()))
     entry("tree", ms, np.mean(rows), 151936, 2, 16 * 128,
           {"mean_accepted": float(np.mean(acc))})
+    _register(args, "tree", "tree", sets[0], fn(sets[0]), 0.8)
     # the same top-k trees under the deterministic-draft rule (greedy
     # acceptance): target rows of the visited nodes only
     fd = lambda c: api.verify_tree_det(c.target, c.parent, c.node_tokens,
@@ -734,10 +761,106 @@ def _tree(args, dev, entry, steps):
         acc.append(float(o["n"].float().mean()))
     entry("tree_deterministic", ms, np.mean(rows), 151936, 2, 16 * 64,
           {"mean_accepted": float(np.mean(acc))})
+    _register(args, "tree_deterministic", "tree_det", sets[0], fd(sets[0]),
+              0.8)
     del sets
 
 
+def _register(args, name, kind, case, out, T, **extra):
+    """Keep one input set and its GPU outputs for the oracle comparison of
+    the CPU-baseline leg (when that leg runs)."""
+    if getattr(args, "checks", None) is None:
+        return
+    args.checks.append((name, kind, case, {k: v.cpu().numpy()
+                                           for k, v in out.items()}, T,
+                        extra))
+
+
 # --------------------------------------------------------- CPU oracle
+def _over_threads(fn, n):
+    """fn(lo, hi) -> dict of arrays over contiguous chunks of range(n) on
+    every host core (the C oracle releases the interpreter lock); the dicts
+    are concatenated in order."""
+    from concurrent.futures import ThreadPoolExecutor
+    nt = max(1, min(n, len(os.sched_getaffinity(0))))
+    bounds = [(n * i // nt, n * (i + 1) // nt) for i in range(nt)]
+    with ThreadPoolExecutor(max_workers=nt) as pool:
+        parts = list(pool.map(lambda b: fn(*b), bounds))
+    return {k: np.concatenate([p[k] for p in parts]) for k in parts[0]
+            if isinstance(parts[0][k], np.ndarray)}
+
+
+def flag_summary(o, g, T):
+    """Flagged draws of one oracle run and the parity of the GPU outputs g
+    (n, tokens) with it: accept tests made and those within 1e-5 of their
+    threshold; final inverse-CDF draws within 1e-5 of a CDF boundary and
+    those whose token differs from the oracle's (inside its admissible
+    range, as the tests require); sequences that differ anywhere else."""
+    import oracle
+    fm = oracle.FLAG_MARGIN
+    on, ot = o["n"], o["tokens"]
+    gn, gt = g["n"], g["tokens"][:, :ot.shape[1]]
+    valid = on >= 0
+    acc_seq = o["margin_acc"] < fm
+    cdf = (o["margin_cdf"] < fm) & valid & ~acc_seq
+    rows = np.arange(len(on))
+    fin = np.maximum(on, 0)
+    same_n = (gn == on)
+    cols = np.arange(ot.shape[1])[None, :]
+    exact = ~((cols == on[:, None]) & cdf[:, None])
+    tok_ok = ((gt == ot) | ~exact).all(axis=1)
+    g_fin = gt[rows, fin]
+    in_range = (g_fin >= o["cdf_lo"]) & (g_fin <= o["cdf_hi"])
+    bad = ~acc_seq & ~(same_n & tok_ok & (~cdf | in_range))
+    tests = int(o["acc_tests"].sum())
+    fl = int(o["acc_flagged"].sum())
+    draws = int(valid.sum()) if T > 0 else 0
+    return {"sequences": int(len(on)), "mismatches": int(bad.sum()),
+            "accept_tests": tests, "accept_flagged": fl,
+            "accept_frac": fl / tests if tests else 0.0,
+            "cdf_draws": draws, "cdf_flagged": int(cdf.sum()),
+            "cdf_frac": int(cdf.sum()) / draws if draws else 0.0,
+            "cdf_diff": int((cdf & same_n & (g_fin != ot[rows, fin])).sum()),
+            "sequences_set_aside": int(acc_seq.sum())}
+
+
+def oracle_check(kind, c, g, T, extra):
+    """The oracle over every sequence of one input set (host threads) and
+    its flag summary against the GPU outputs g."""
+    import oracle
+    t = synth.host_logits(c.target)
+    d = None if (T == 0 and kind in ("linear", "filtered", "kcand_trie")) \
+        else synth.host_logits(c.draft)
+    tk, u = c.tokens.cpu().numpy(), c.uniforms.cpu().numpy()
+    nseq = t.shape[0]
+    if kind == "linear":
+        gm = t.shape[1] - 1
+        o = _over_threads(lambda a, b: oracle.verify_linear(
+            t[a:b], None if d is None else np.ascontiguousarray(
+                d[a:b, :gm]), tk[a:b], u[a:b], T), nseq)
+    elif kind == "filtered":
+        gm = t.shape[1] - 1
+        o = _over_threads(lambda a, b: oracle.verify_linear_filtered(
+            t[a:b], np.ascontiguousarray(d[a:b, :gm]), tk[a:b], u[a:b], T,
+            extra["top_k"], extra["top_p"]), nseq)
+    elif kind == "kcand":
+        o = _over_threads(lambda a, b: oracle.verify_kcand(
+            t[a:b], d[a:b], tk[a:b], u[a:b], T), nseq)
+    elif kind == "kcand_trie":
+        o = _over_threads(lambda a, b: oracle.verify_kcand_trie(
+            t[a:b], None if d is None else d[a:b], tk[a:b], u[a:b], T),
+            nseq)
+    elif kind == "tree":
+        par, nt = c.parent.cpu().numpy(), c.node_tokens.cpu().numpy()
+        o = _over_threads(lambda a, b: oracle.verify_tree(
+            t[a:b], d[a:b], par[a:b], nt[a:b], u[a:b], T), nseq)
+    else:  # tree_det
+        par, nt = c.parent.cpu().numpy(), c.node_tokens.cpu().numpy()
+        o = _over_threads(lambda a, b: oracle.verify_tree_det(
+            t[a:b], par[a:b], nt[a:b], u[a:b], T), nseq)
+    return flag_summary(o, g, T)
+
+
 def oracle_sample(c, seqs, F):
     import oracle
     t = synth.host_logits(c.target[seqs])
@@ -767,29 +890,51 @@ def oracle_threads(c, seqs, F, nthreads):
 
     def work(x):
         t, d, dall, tk, u = x
-        oracle.verify_linear(t, d, tk, u, T)
-        oracle.fanout_topk(dall, np.array(F, np.int32))
+        return (oracle.verify_linear(t, d, tk, u, T),
+                oracle.fanout_topk(dall, np.array(F, np.int32)))
     with ThreadPoolExecutor(max_workers=len(chunks)) as pool:
         t0 = time.perf_counter()
-        list(pool.map(work, inputs))
-        return time.perf_counter() - t0
+        res = list(pool.map(work, inputs))
+        dt = time.perf_counter() - t0
+    # put the chunks' sequences back in order
+    order = np.argsort(np.concatenate([np.array(ch) for ch in chunks]))
+    cat = lambda i, k: np.concatenate([r[i][k] for r in res])[order]
+    ov = {k: cat(0, k) for k in res[0][0] if isinstance(res[0][0][k],
+                                                       np.ndarray)}
+    of = {k: cat(1, k) for k in ("tokens", "logit")}
+    return dt, ov, of
 
 
-def cpu_baseline(sets, nseq, F):
+def cpu_baseline(sets, nseq, F, gpu_out=None):
     """The oracle on the host cores: all of them, one thread per core over
-    the round's sequences, and (sub-field) one thread on a part of them."""
+    the round's sequences, and (sub-field) one thread on a part of them.
+    With the GPU's outputs of the same round (gpu_out: verify n, tokens and
+    the fan-out tokens), also their parity with the oracle's and the
+    flagged fractions (returned as a second value)."""
     cores = len(os.sched_getaffinity(0))
     n1 = max(1, min(nseq, 32))
     dt1 = oracle_sample(sets[0], list(range(n1)), F)
     seqs = list(range(nseq))
-    dtn = oracle_threads(sets[0], seqs, F, cores)
-    return {"value": nseq / dtn / B, "unit": "rounds/s", "cores": cores,
+    dtn, ov, of = oracle_threads(sets[0], seqs, F, cores)
+    flags = None
+    if gpu_out is not None:
+        g = {k: v[:nseq] for k, v in gpu_out.items()}
+        flags = flag_summary(ov, g, T)
+        flags["fanout_rows"] = int(nseq * (FAN["K"] + 1))
+        diff, off = 0, 0
+        for f in F:  # row k of each sequence: columns off .. off + F_k
+            diff += int((g["fan_tokens"][:, off:off + f] !=
+                         of["tokens"][:, off:off + f]).any(axis=1).sum())
+            off += f
+        flags["fanout_rows_differing"] = diff
+    base = {"value": nseq / dtn / B, "unit": "rounds/s", "cores": cores,
             "kind": "oracle",
             "sample": "fp64 C oracle (verify + fan-out), %d host threads "
                       "over %d of the %d sequences of one round (%.2f s "
                       "wall), scaled to a full round" % (cores, nseq, B, dtn),
             "single_thread": {"value": n1 / dt1 / B, "cores": 1,
                               "sample": "%d sequences, %.2f s" % (n1, dt1)}}
+    return base, flags
 
 
 def reference_arm(args):

@@ -101,6 +101,43 @@ const char *sd_version(void);
 const char *sd_last_error(void);
 
 /* ---------------------------------------------------------------------
+ * Tuning switches (no counterpart in the pages).  Each one picks among
+ * kernels or launch shapes that compute the same results; the defaults are
+ * the fastest measured on the workloads this library is tuned for.  They
+ * are process-wide, read by the next call that launches work, and never
+ * taken from the environment.  sd_tune_set returns SD_ERR_INVALID_ARG for
+ * an unknown key or a value outside the key's range; sd_tune_get returns
+ * the current value (-1 for an unknown key).  Not synchronised with calls
+ * running on other host threads: set them before such calls start.
+ * ------------------------------------------------------------------- */
+typedef enum {
+  SD_TUNE_CLUSTER = 0,         /* CTAs per cluster (linear, tree, fused,
+                                  filtered, kcand): 0 chosen, 1/2/4/8/16 */
+  SD_TUNE_NO_TMA = 1,          /* 1: plain 16-byte loads instead of the TMA
+                                  ring (linear, tree); default 0 */
+  SD_TUNE_ALLROWS = 2,         /* small linear inputs read every row in one
+                                  launch: 0 never, 1 up to 64 MB (default),
+                                  2 wherever its scratch fits */
+  SD_TUNE_SPEC = 3,            /* a cluster's last sequence reads ahead: 0
+                                  never, 1 (default), 2 also L2 prefetch */
+  SD_TUNE_FUSED = 4,           /* sd_verify_linear_fanout: 0 the two calls
+                                  (default), 1 the fused kernel */
+  SD_TUNE_KCAND_RING = 5,      /* 0: K-candidate verify without the TMA
+                                  ring; default 1 */
+  SD_TUNE_FANOUT_CLUSTER = 6,  /* fan-out CTAs per cluster: 0 chosen */
+  SD_TUNE_FANOUT_LDG = 7,      /* 1: fan-out with plain loads; default 0 */
+  SD_TUNE_FANOUT_MAXC = 8,     /* cap on the fan-out's clusters: 0 none */
+  SD_TUNE_FANOUT_L2_FIRST = 9, /* fan-out rows read evict-first: default 1 */
+  SD_TUNE_L2_KEEP = 10,        /* linear verify: a position's rows are read
+                                  with L2 evict_last until the draw no
+                                  longer needs them: 1 on, 0 off */
+  SD_TUNE_COUNT = 11
+} sd_tune;
+
+sd_status sd_tune_set(sd_tune key, int value);
+int sd_tune_get(sd_tune key);
+
+/* ---------------------------------------------------------------------
  * Linear verify ("01 · Draft-then-verify", Algorithm 1 / spec_step).
  *
  * target_logits [B, gamma+1, V]: row i is the target logits p_i given the
@@ -440,6 +477,22 @@ sd_status sd_verify_linear_fanout(
     int32_t *out_tokens, float *out_prob, int32_t *fan_tokens,
     float *fan_logit, int32_t *dev_status, void *workspace, size_t ws_bytes,
     void *stream);
+
+/* ---------------------------------------------------------------------
+ * Self-test of the failure path (no counterpart in the pages).  Every
+ * wait of a kernel on an asynchronous copy is bounded: after its poll
+ * limit it ORs SD_DEV_TIMEOUT into *dev_status and the kernel returns
+ * normally.  This call launches one CTA of 256 threads that waits, through
+ * that same wait, on a barrier nothing will ever complete (no copy is in
+ * flight), with a limit of `polls` in [1, 2^20] polls.
+ *
+ * dev_status (device, nullable): gets SD_DEV_TIMEOUT.
+ * out [2] (device int32): out[0] the number of threads whose wait gave up
+ *     (256), out[1] = 1 once the kernel has run to its end.
+ * Returns SD_ERR_INVALID_ARG for polls outside the range or a null `out`.
+ * ------------------------------------------------------------------- */
+sd_status sd_selftest_bounded_wait(int polls, int32_t *dev_status,
+                                   int32_t *out, void *stream);
 
 #ifdef __cplusplus
 }

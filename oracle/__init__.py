@@ -47,13 +47,13 @@ def _bind(path):
     I = ctypes.c_int
     D = ctypes.c_double
     lib.orc_verify_linear.argtypes = [P, P, I, P, P, I, I, I, D,
-                                      P, P, P, P, P, P, P, P, P, P]
+                                      P, P, P, P, P, P, P, P, P, P, P, P]
     lib.orc_verify_kcand.argtypes = [P, P, I, P, P, I, I, I, I, D,
-                                     P, P, P, P, P, P, P, P, P, P]
+                                     P, P, P, P, P, P, P, P, P, P, P, P]
     lib.orc_verify_tree.argtypes = [P, P, I, P, P, P, I, I, I, D,
-                                    P, P, P, P, P, P, P, P, P]
+                                    P, P, P, P, P, P, P, P, P, P, P]
     lib.orc_verify_tree_det.argtypes = [P, I, P, P, P, I, I, I, D,
-                                        P, P, P, P, P, P, P, P, P]
+                                        P, P, P, P, P, P, P, P, P, P, P]
     lib.orc_kcand_trie.argtypes = [P, P, I, I, I, P, P, P, P, P, P, P]
     lib.orc_presto_expand.argtypes = [P, P, I, ctypes.c_longlong, I, I, I,
                                       D, D, I, I, P, P, P, P, P, P, P, P]
@@ -62,7 +62,8 @@ def _bind(path):
     lib.orc_fanout_topk.argtypes = [P, I, I, I, I, P, P, P, P]
     lib.orc_fanout_hits.argtypes = [P, P, P, P, I, I, P]
     lib.orc_verify_linear_filtered.argtypes = [P, P, I, P, P, I, I, I, D, I,
-                                               D, P, P, P, P, P, P, P, P]
+                                               D, P, P, P, P, P, P, P, P, P,
+                                               P]
     for f in (lib.orc_verify_linear, lib.orc_verify_kcand,
               lib.orc_verify_tree, lib.orc_fanout_schedule,
               lib.orc_fanout_topk):
@@ -118,12 +119,14 @@ def _margins(B):
     return {"margin_acc": np.empty(B, np.float64),
             "margin_cdf": np.empty(B, np.float64),
             "cdf_lo": np.empty(B, np.int32),
-            "cdf_hi": np.empty(B, np.int32)}
+            "cdf_hi": np.empty(B, np.int32),
+            "acc_tests": np.empty(B, np.int32),
+            "acc_flagged": np.empty(B, np.int32)}
 
 
 def _margin_ptrs(m):
     return (_ptr(m["margin_acc"]), _ptr(m["margin_cdf"]), _ptr(m["cdf_lo"]),
-            _ptr(m["cdf_hi"]))
+            _ptr(m["cdf_hi"]), _ptr(m["acc_tests"]), _ptr(m["acc_flagged"]))
 
 
 def _finish(out, m):
@@ -477,4 +480,6 @@ def fanout_hits(n, tokens, fan_tokens, F):
 FLAG_MARGIN = 1e-5
 """A draw whose margin is below this is 'flagged': a correct fp32
 implementation may land on the other side of the threshold there (for an
-inverse-CDF draw it may then return any token in [cdf_lo, cdf_hi])."""
+inverse-CDF draw it may then return any token in [cdf_lo, cdf_hi]).
+Every verify result carries, per sequence, acc_tests (accept tests made,
+T > 0) and acc_flagged (those whose |r - p/q| is below this margin)."""

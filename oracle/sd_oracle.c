@@ -214,6 +214,26 @@ static void note_margin(double *margin, double m) {
   if (m < *margin) *margin = m;
 }
 
+/* One accept test r <= rho: counted in *tests; its margin |r - rho| noted
+ * (there is none when rho is infinite: q(x) == 0 < p(x) always accepts),
+ * and counted in *flagged when that margin is below ORC_BAND. */
+static void note_test(double *margin, int *tests, int *flagged, double r,
+                      double rho) {
+  ++*tests;
+  if (!isfinite(rho)) return;
+  const double m = fabs(r - rho);
+  note_margin(margin, m);
+  if (m < ORC_BAND) ++*flagged;
+}
+
+/* Per-sequence test counts (nullable outputs): none for greedy or invalid
+ * sequences, whose margins are infinite too. */
+static void put_tests(int32_t *acc_tests, int32_t *acc_flagged, int b,
+                      int none, int nt, int nf) {
+  if (acc_tests) acc_tests[b] = none ? 0 : nt;
+  if (acc_flagged) acc_flagged[b] = none ? 0 : nf;
+}
+
 /* ------------------------------------------------------------------------
  * Linear verify ("01 · Draft-then-verify", Algorithm 1 and spec_step).
  * target [B, gamma+1, V], draft [B, gamma, V] (unused when T == 0),
@@ -228,6 +248,7 @@ int orc_verify_linear(const void *target, const void *draft, int dtype,
                       int32_t *out_tokens, double *out_prob,
                       double *out_accept, double *margin_acc,
                       double *margin_cdf, int32_t *cdf_lo, int32_t *cdf_hi,
+                      int32_t *acc_tests, int32_t *acc_flagged,
                       double *out_resid, int32_t *status) {
   double *p = malloc(sizeof(double) * (size_t)V);
   double *q = malloc(sizeof(double) * (size_t)V);
@@ -235,7 +256,7 @@ int orc_verify_linear(const void *target, const void *draft, int dtype,
   if (!p || !q || !w) { free(p); free(q); free(w); return 1; }
   const int G1 = gamma + 1;
   for (int b = 0; b < B; ++b) {
-    int st = 0, n = 0, t = -1, invalid = 0, lo = -1, hi = -1;
+    int st = 0, n = 0, t = -1, invalid = 0, lo = -1, hi = -1, nt = 0, nf = 0;
     double mg = INFINITY, mc = INFINITY, prob = 0.0;
     for (int i = 0; i < gamma; ++i) out_accept[(size_t)b * gamma + i] = -1.0;
     if (T == 0.0) {
@@ -276,7 +297,7 @@ int orc_verify_linear(const void *target, const void *draft, int dtype,
           out_accept[(size_t)b * gamma + i] = 0.0;
         } else {
           double rho = accept_ratio(p[x], q[x]);
-          if (isfinite(rho)) note_margin(&mg, fabs(r - rho));
+          note_test(&mg, &nt, &nf, r, rho);
           ok = (r <= rho);
           out_accept[(size_t)b * gamma + i] = rho < 1.0 ? rho : 1.0;
         }
@@ -334,6 +355,7 @@ int orc_verify_linear(const void *target, const void *draft, int dtype,
     margin_cdf[b] = (T == 0.0) ? INFINITY : mc;
     cdf_lo[b] = lo;
     cdf_hi[b] = hi;
+    put_tests(acc_tests, acc_flagged, b, T == 0.0 || invalid, nt, nf);
     status[b] = st;
   }
   free(p); free(q); free(w);
@@ -355,6 +377,7 @@ int orc_verify_kcand(const void *target, const void *draft, int dtype,
                      int32_t *sel_k, int32_t *out_tokens, int32_t *n_per_cand,
                      double *out_prob, double *margin_acc,
                      double *margin_cdf, int32_t *cdf_lo, int32_t *cdf_hi,
+                     int32_t *acc_tests, int32_t *acc_flagged,
                      int32_t *status) {
   double *p = malloc(sizeof(double) * (size_t)V);
   double *q = malloc(sizeof(double) * (size_t)V);
@@ -364,7 +387,7 @@ int orc_verify_kcand(const void *target, const void *draft, int dtype,
 #define TROW(b, k, j) ((((size_t)(b) * K + (k)) * G1 + (j)) * (size_t)V)
 #define DROW(b, j) (((size_t)(b) * gamma + (j)) * (size_t)V)
   for (int b = 0; b < B; ++b) {
-    int st = 0, invalid = 0, lo = -1, hi = -1;
+    int st = 0, invalid = 0, lo = -1, hi = -1, nt = 0, nf = 0;
     double mg = INFINITY, mc = INFINITY, prob = 0.0;
     int best_k = 0, best_n = -1, t = -1;
     for (int k = 0; k < K && !invalid; ++k) {
@@ -389,7 +412,7 @@ int orc_verify_kcand(const void *target, const void *draft, int dtype,
           } else {
             double r = (double)uniforms[((size_t)b * K + k) * G1 + j];
             double rho = accept_ratio(p[x], q[x]);
-            if (isfinite(rho)) note_margin(&mg, fabs(r - rho));
+            note_test(&mg, &nt, &nf, r, rho);
             ok = (r <= rho);
           }
         }
@@ -461,6 +484,7 @@ int orc_verify_kcand(const void *target, const void *draft, int dtype,
     margin_cdf[b] = (T == 0.0) ? INFINITY : mc;
     cdf_lo[b] = lo;
     cdf_hi[b] = hi;
+    put_tests(acc_tests, acc_flagged, b, T == 0.0 || invalid, nt, nf);
     status[b] = st;
   }
 #undef TROW
@@ -488,7 +512,8 @@ int orc_verify_tree(const void *target, const void *draft, int dtype,
                     const float *uniforms, int B, int N, int V, double T,
                     int32_t *n_acc, int32_t *out_tokens, int32_t *out_nodes,
                     double *out_prob, double *margin_acc, double *margin_cdf,
-                    int32_t *cdf_lo, int32_t *cdf_hi, int32_t *status) {
+                    int32_t *cdf_lo, int32_t *cdf_hi, int32_t *acc_tests,
+                    int32_t *acc_flagged, int32_t *status) {
   double *p = malloc(sizeof(double) * (size_t)V);
   double *q = malloc(sizeof(double) * (size_t)V);
   if (!p || !q) { free(p); free(q); return 1; }
@@ -497,6 +522,7 @@ int orc_verify_tree(const void *target, const void *draft, int dtype,
     const int32_t *tok = node_tokens + (size_t)b * N;
     const float *U = uniforms + (size_t)b * N;
     int st = 0, invalid = 0, depth = 0, t = -1, lo = -1, hi = -1;
+    int nt = 0, nf = 0;
     double mg = INFINITY, mc = INFINITY, prob = 0.0;
     for (int i = 0; i < N; ++i) {
       out_nodes[(size_t)b * N + i] = -1;
@@ -536,7 +562,7 @@ int orc_verify_tree(const void *target, const void *draft, int dtype,
             st |= ORC_ST_BAD_TOKEN;
           } else {
             double rho = accept_ratio(p[x], q[x]);
-            if (isfinite(rho)) note_margin(&mg, fabs((double)U[v] - rho));
+            note_test(&mg, &nt, &nf, (double)U[v], rho);
             ok = ((double)U[v] <= rho);
           }
           if (ok) { next = v; break; }
@@ -584,6 +610,7 @@ int orc_verify_tree(const void *target, const void *draft, int dtype,
     margin_cdf[b] = (T == 0.0) ? INFINITY : mc;
     cdf_lo[b] = lo;
     cdf_hi[b] = hi;
+    put_tests(acc_tests, acc_flagged, b, T == 0.0 || invalid, nt, nf);
     status[b] = st;
   }
   free(p); free(q);
@@ -766,14 +793,15 @@ int orc_verify_linear_filtered(const void *target, const void *draft,
                                int32_t *n_acc, int32_t *out_tokens,
                                double *out_prob, double *margin_acc,
                                double *margin_cdf, int32_t *cdf_lo,
-                               int32_t *cdf_hi, int32_t *status) {
+                               int32_t *cdf_hi, int32_t *acc_tests,
+                               int32_t *acc_flagged, int32_t *status) {
   if (T == 0.0) {
     double *acc = malloc(sizeof(double) * (size_t)(B * (gamma > 0 ? gamma : 1)));
     if (!acc) return 1;
     int rc = orc_verify_linear(target, draft, dtype, tokens, uniforms, B,
                                gamma, V, T, n_acc, out_tokens, out_prob, acc,
-                               margin_acc, margin_cdf, cdf_lo, cdf_hi, NULL,
-                               status);
+                               margin_acc, margin_cdf, cdf_lo, cdf_hi,
+                               acc_tests, acc_flagged, NULL, status);
     free(acc);
     return rc;
   }
@@ -785,6 +813,7 @@ int orc_verify_linear_filtered(const void *target, const void *draft,
   const int G1 = gamma + 1;
   for (int b = 0; b < B; ++b) {
     int st = 0, n = 0, t = -1, invalid = 0, lo = -1, hi = -1, rejected = 0;
+    int nt = 0, nf = 0;
     double mg = INFINITY, mc = INFINITY, prob = 0.0;
     for (int i = 0; i < gamma; ++i) {
       if (!filtered_row(target, dtype, ((size_t)b * G1 + i) * V, V, T, top_k,
@@ -802,7 +831,7 @@ int orc_verify_linear_filtered(const void *target, const void *draft,
         ok = 0;
       } else {
         double rho = accept_ratio(p[x], q[x]);
-        if (isfinite(rho)) note_margin(&mg, fabs(r - rho));
+        note_test(&mg, &nt, &nf, r, rho);
         ok = (r <= rho);
       }
       if (!ok) { rejected = 1; break; }
@@ -851,6 +880,7 @@ int orc_verify_linear_filtered(const void *target, const void *draft,
     margin_cdf[b] = mc;
     cdf_lo[b] = lo;
     cdf_hi[b] = hi;
+    put_tests(acc_tests, acc_flagged, b, invalid, nt, nf);
     status[b] = st;
   }
   free(p); free(q); free(w); free(e);
@@ -874,6 +904,7 @@ int orc_verify_tree_det(const void *target, int dtype, const int32_t *parent,
                         int32_t *out_tokens, int32_t *out_nodes,
                         double *out_prob, double *margin_acc,
                         double *margin_cdf, int32_t *cdf_lo, int32_t *cdf_hi,
+                        int32_t *acc_tests, int32_t *acc_flagged,
                         int32_t *status) {
   double *p = malloc(sizeof(double) * (size_t)V);
   if (!p) return 1;
@@ -882,6 +913,7 @@ int orc_verify_tree_det(const void *target, int dtype, const int32_t *parent,
     const int32_t *tok = node_tokens + (size_t)b * N;
     const float *U = uniforms + (size_t)b * N;
     int st = 0, invalid = 0, depth = 0, t = -1, lo = -1, hi = -1;
+    int nt = 0, nf = 0;
     double mg = INFINITY, mc = INFINITY, prob = 0.0;
     for (int i = 0; i < N; ++i) {
       out_nodes[(size_t)b * N + i] = -1;
@@ -911,7 +943,7 @@ int orc_verify_tree_det(const void *target, int dtype, const int32_t *parent,
           int x = tok[v];
           if (x < 0 || x >= V) { st |= ORC_ST_BAD_TOKEN; continue; }
           double rho = p[x];
-          note_margin(&mg, fabs((double)U[v] - rho));
+          note_test(&mg, &nt, &nf, (double)U[v], rho);
           if ((double)U[v] <= rho) { next = v; break; }
           /* rejected: remove x and renormalise */
           p[x] = 0.0;
@@ -954,6 +986,7 @@ int orc_verify_tree_det(const void *target, int dtype, const int32_t *parent,
     margin_cdf[b] = (T == 0.0) ? INFINITY : mc;
     cdf_lo[b] = lo;
     cdf_hi[b] = hi;
+    put_tests(acc_tests, acc_flagged, b, T == 0.0 || invalid, nt, nf);
     status[b] = st;
   }
   free(p);

@@ -19,6 +19,7 @@ from . import build as _build
 SD_OK, SD_ERR_INVALID_ARG, SD_ERR_UNSUPPORTED, SD_ERR_CUDA = 0, 1, 2, 3
 SD_F32, SD_BF16 = 0, 1
 DEV_BAD_TOKEN, DEV_NONFINITE, DEV_BAD_PARENT, DEV_ZERO_MASS = 1, 2, 4, 8
+DEV_TIMEOUT = 16
 
 _lock = threading.Lock()
 _lib = None
@@ -85,6 +86,9 @@ def _declare(L):
         "sd_verify_linear_fanout_workspace": ([I, I, I, I], Z),
         "sd_verify_linear_fanout": ([P, P, I, P, P, I, I, I, F, P, P, P, P,
                                      P, P, P, P, Z, P], I),
+        "sd_tune_set": ([I, I], I),
+        "sd_selftest_bounded_wait": ([I, P, P, P], I),
+        "sd_tune_get": ([I], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -94,6 +98,39 @@ def _declare(L):
 
 def version() -> str:
     return lib().sd_version().decode()
+
+
+TUNE = {"cluster": 0, "no_tma": 1, "allrows": 2, "spec": 3, "fused": 4,
+        "kcand_ring": 5, "fanout_cluster": 6, "fanout_ldg": 7,
+        "fanout_maxc": 8, "fanout_l2_first": 9, "l2_keep": 10}
+"""Tuning switches of sd_tune_set, by name (see include/sd_verify.h)."""
+
+
+def tune_get(name: str) -> int:
+    return lib().sd_tune_get(TUNE[name])
+
+
+def tune_set(name: str, value: int) -> None:
+    _check(lib().sd_tune_set(TUNE[name], int(value)))
+
+
+class tuned:
+    """Context manager: set tuning switches (name=value) for the block and
+    restore the previous values after it."""
+
+    def __init__(self, **switches):
+        self.switches = switches
+
+    def __enter__(self):
+        self.saved = {k: tune_get(k) for k in self.switches}
+        for k, v in self.switches.items():
+            tune_set(k, v)
+        return self
+
+    def __exit__(self, *exc):
+        for k, v in self.saved.items():
+            tune_set(k, v)
+        return False
 
 
 def _check(rc):
@@ -443,6 +480,20 @@ def branch_fork(draft, x_b, T, k_max, *, status=None, workspace=None):
                             int(k_max), _p(k), _p(toks), _p(status), _p(ws),
                             ws.numel(), _stream(dev)))
     return {"k": k, "tokens": toks}
+
+
+def selftest_bounded_wait(polls, device="cuda"):
+    """The failure-path self-test (sd_selftest_bounded_wait): a wait that
+    can never complete, bounded by `polls` polls.  Returns (status word,
+    threads whose wait gave up, 1 if the kernel ran to its end)."""
+    dev = torch.device(device)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = torch.zeros(2, dtype=torch.int32, device=dev)
+    _check(lib().sd_selftest_bounded_wait(int(polls), _p(st), _p(out),
+                                          _stream(dev)))
+    torch.cuda.synchronize(dev)
+    o = out.tolist()
+    return int(st.item()), o[0], o[1]
 
 
 def fanout_schedule(K, budget, a, r):

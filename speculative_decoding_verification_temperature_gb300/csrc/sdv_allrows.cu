@@ -286,12 +286,12 @@ size_t allrows_workspace(int B, int gamma, int V, sd_dtype dt) {
   return w <= kARMaxWs ? w : 0;
 }
 
-// Whether the all-rows path takes this call: small inputs (SDV_ALLROWS=0
+// Whether the all-rows path takes this call: small inputs (SD_TUNE_ALLROWS 0
 // never, 2 whenever it fits), no residual output, workspace enough.
 bool use_allrows(int B, int gamma, int V, sd_dtype dt, const void *target,
                  const void *draft, float T, const float *out_resid,
                  size_t ws_bytes) {
-  const int mode = env_int("SDV_ALLROWS", 1);
+  const int mode = tune(SD_TUNE_ALLROWS);
   if (mode == 0 || out_resid || B <= 0) return false;
   const int eb = dt == SD_F32 ? 4 : 2;
   const bool greedy = T == 0.f;

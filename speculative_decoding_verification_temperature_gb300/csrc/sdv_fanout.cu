@@ -5,7 +5,7 @@
 //
 // One cluster (usually a single CTA) owns one row at a time; rows all have
 // the same cost, so clusters take them round-robin.  Each CTA streams its
-// slice once through the TMA ring (16-byte aligned rows; SDV_FANOUT_LDG=1
+// slice once through the TMA ring (16-byte aligned rows; SD_TUNE_FANOUT_LDG
 // takes 16-byte loads instead) or with scalar loads, filtering it through
 // per-warp sorted lists against a CTA-wide threshold (sdv_topf.cuh); the
 // warps' lists are ranked together, and for clusters of several CTAs rank 0
@@ -251,13 +251,13 @@ extern "C" sd_status sd_fanout_topk(const void *draft_logits, sd_dtype dt,
   const int eb = dt == SD_F32 ? 4 : 2, vw = dt == SD_F32 ? 4 : 8;
   const bool vec = aligned16(draft_logits) && ((size_t)V * eb) % 16 == 0;
   const long long nvec = V / (vec ? vw : 1);
-  const bool ring = vec && env_int("SDV_FANOUT_LDG", 0) == 0;
+  const bool ring = vec && tune(SD_TUNE_FANOUT_LDG) == 0;
   FanKernel kern = pick_fanout(dt, vec, ring);
   // rows of equal cost: a single CTA per row unless the rows are too few to
   // fill the GPU, then clusters that split each row
   const long long rows = (long long)B * (K + 1);
   int CL = 1;
-  const int forced = env_int("SDV_FANOUT_CLUSTER", 0);
+  const int forced = tune(SD_TUNE_FANOUT_CLUSTER);
   if (forced == 1 || forced == 2 || forced == 4 || forced == 8 || forced == 16)
     CL = forced;
   else
@@ -268,9 +268,9 @@ extern "C" sd_status sd_fanout_topk(const void *draft_logits, sd_dtype dt,
   int maxc = 0;
   st = max_active_clusters((const void *)kern, CL, smem, &maxc);
   if (st != SD_OK) return st;
-  // SDV_FANOUT_MAXC caps the clusters (tuning: room for a kernel that runs
+  // SD_TUNE_FANOUT_MAXC caps the clusters (tuning: room for a kernel that runs
   // beside this one on another stream)
-  const int cap = env_int("SDV_FANOUT_MAXC", 0);
+  const int cap = tune(SD_TUNE_FANOUT_MAXC);
   if (cap > 0 && cap < maxc) maxc = cap;
   // rows of equal cost: give every cluster the same number of them
   const long long per = (rows + maxc - 1) / maxc;
@@ -284,7 +284,7 @@ extern "C" sd_status sd_fanout_topk(const void *draft_logits, sd_dtype dt,
   prm.dev_status = dev_status;
   prm.nclusters = (int)want;
   prm.seg_bytes = 128;
-  prm.evict_first = env_int("SDV_FANOUT_L2_FIRST", 1) != 0;
+  prm.evict_first = tune(SD_TUNE_FANOUT_L2_FIRST) != 0;
   void *args[] = {&prm};
   return launch_clusters((const void *)kern, (int)want, CL, smem,
                          static_cast<cudaStream_t>(stream), args);

@@ -569,7 +569,7 @@ extern "C" sd_status sd_verify_linear_filtered(
   // slices beat one sequence each on small ones (measured at B=256,
   // V=128256: clusters of 1, 2, 4 -> 463, 401, 374 us)
   int CL = 1, maxc = 0;
-  const int forced = env_int("SDV_CLUSTER", 0);
+  const int forced = tune(SD_TUNE_CLUSTER);
   for (int c = 16; c >= 1; c /= 2) {
     if (forced && c != forced && c != 1) continue;
     if (c > 1 && nvec / c < kStageVecs && !forced) continue;

@@ -738,7 +738,7 @@ extern "C" sd_status sd_verify_linear_fanout(
   // slice of at least one full stage per CTA; CL * max F keys gathered in
   // one merge), else single CTAs taking sequences from the work counter
   int CL = 1, maxc = 0;
-  const int forced = env_int("SDV_CLUSTER", 0);
+  const int forced = tune(SD_TUNE_CLUSTER);
   for (int c = 16; c >= 1; c /= 2) {
     if (forced && c != forced && c != 1) continue;
     if (c > 1 && nvec / c < kStageVecs && !forced) continue;
@@ -757,7 +757,7 @@ extern "C" sd_status sd_verify_linear_fanout(
   const bool fused = vec && total > 0 && total <= kFusedMaxTotal &&
                      kStg % 32 == 0 &&
                      smem <= 64 * 1024 && maxc > 0 &&
-                     env_int("SDV_FUSED", 1) != 0;
+                     tune(SD_TUNE_FUSED) != 0;
   if (!fused) {
     // the two calls one after the other (same results)
     st = linear_launch(target_logits, draft_logits, dt, gamma + 1,

@@ -2,6 +2,7 @@
 // last error, geometric fan-out schedule).
 #include "sdv_host.cuh"
 
+#include <atomic>
 #include <mutex>
 #include <string>
 #include <tuple>
@@ -34,9 +35,42 @@ sd_status fail(sd_status st, const char *fmt, ...) {
   return st;
 }
 
-int env_int(const char *name, int dflt) {
-  const char *v = getenv(name);
-  return v ? atoi(v) : dflt;
+namespace {
+// defaults: the fastest measured configuration
+std::atomic<int> g_tune[SD_TUNE_COUNT] = {
+    {0},  // SD_TUNE_CLUSTER
+    {0},  // SD_TUNE_NO_TMA
+    {1},  // SD_TUNE_ALLROWS
+    {1},  // SD_TUNE_SPEC
+    {0},  // SD_TUNE_FUSED
+    {1},  // SD_TUNE_KCAND_RING
+    {0},  // SD_TUNE_FANOUT_CLUSTER
+    {0},  // SD_TUNE_FANOUT_LDG
+    {0},  // SD_TUNE_FANOUT_MAXC
+    {1},  // SD_TUNE_FANOUT_L2_FIRST
+    {0},  // SD_TUNE_L2_KEEP
+};
+
+bool tune_valid(int key, int v) {
+  switch (key) {
+    case SD_TUNE_CLUSTER:
+    case SD_TUNE_FANOUT_CLUSTER:
+      return v == 0 || v == 1 || v == 2 || v == 4 || v == 8 || v == 16;
+    case SD_TUNE_ALLROWS:
+    case SD_TUNE_SPEC:
+      return v >= 0 && v <= 2;
+    case SD_TUNE_FANOUT_MAXC:
+      return v >= 0;
+    default:
+      return v == 0 || v == 1;
+  }
+}
+}  // namespace
+
+int tune(sd_tune key) {
+  return (key >= 0 && key < SD_TUNE_COUNT)
+             ? g_tune[key].load(std::memory_order_relaxed)
+             : 0;
 }
 
 sd_status check_device(int *sm_count) {
@@ -165,6 +199,21 @@ sd_status launch_pdl(const void *kernel, unsigned grid, unsigned block,
 extern "C" const char *sd_version(void) { return "sdverify 0.1 (sm_103a)"; }
 
 extern "C" const char *sd_last_error(void) { return sdv::g_err; }
+
+extern "C" sd_status sd_tune_set(sd_tune key, int value) {
+  const int k = (int)key;
+  SDV_REQUIRE(k >= 0 && k < SD_TUNE_COUNT, "unknown tuning key %d", k);
+  SDV_REQUIRE(sdv::tune_valid(k, value), "value %d out of range for key %d",
+              value, k);
+  sdv::g_tune[k].store(value, std::memory_order_relaxed);
+  return SD_OK;
+}
+
+extern "C" int sd_tune_get(sd_tune key) {
+  const int k = (int)key;
+  if (k < 0 || k >= SD_TUNE_COUNT) return -1;
+  return sdv::g_tune[k].load(std::memory_order_relaxed);
+}
 
 // Saguaro, Theorem 12: w_k = a^{k/(1+r)} (k < K), w_K = a^{K/(1+r)}
 // (1-a)^{-1/(1+r)}; F_k = F_0 w_k with F_0 = budget / sum w, made integer by

@@ -18,7 +18,9 @@ namespace sdv {
 
 sd_status fail(sd_status st, const char *fmt, ...);
 sd_status check_device(int *sm_count);
-int env_int(const char *name, int dflt);
+// Current value of a tuning switch (sd_tune_set); the defaults are the
+// measured best.
+int tune(sd_tune key);
 
 #define SDV_REQUIRE(cond, ...)                              \
   do {                                                      \
@@ -38,10 +40,10 @@ inline bool aligned16(const void *p) {
 }
 
 // Cluster size for rows of nvec vectors: slices of at least ~512 vectors
-// (one load batch per thread), at most 16 CTAs.  SDV_CLUSTER overrides it
-// (1, 2, 4, 8 or 16) for tuning.
+// (one load batch per thread), at most 16 CTAs.  SD_TUNE_CLUSTER overrides
+// it (1, 2, 4, 8 or 16).
 inline int choose_cluster(long long nvec) {
-  int forced = env_int("SDV_CLUSTER", 0);
+  int forced = tune(SD_TUNE_CLUSTER);
   if (forced == 1 || forced == 2 || forced == 4 || forced == 8 ||
       forced == 16)
     return forced;

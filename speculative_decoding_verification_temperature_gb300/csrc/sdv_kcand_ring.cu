@@ -590,7 +590,7 @@ sd_status kcand_ring_launch(const void *target, const void *draft,
                             size_t ws_bytes, cudaStream_t stream,
                             bool *launched) {
   *launched = false;
-  if (env_int("SDV_KCAND_RING", 1) == 0) return SD_OK;
+  if (tune(SD_TUNE_KCAND_RING) == 0) return SD_OK;
   const bool greedy = (T == 0.f);
   const int vw = dt == SD_F32 ? 4 : 8;
   const long long nvec = V / vw;
@@ -603,7 +603,7 @@ sd_status kcand_ring_launch(const void *target, const void *draft,
   // the largest cluster at which all B sequences are resident at once (at
   // least one full stage per slice), else single CTAs and the work counter
   int CL = 1, maxc = 0;
-  const int forced = env_int("SDV_CLUSTER", 0);
+  const int forced = tune(SD_TUNE_CLUSTER);
   for (int c = 16; c >= 1; c /= 2) {
     if (forced && c != forced && c != 1) continue;
     if (c > 1 && nvec / c < kStageVecs && !forced) continue;

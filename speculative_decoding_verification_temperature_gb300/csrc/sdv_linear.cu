@@ -27,7 +27,6 @@
 #include <type_traits>
 
 #include "sdv_device.cuh"
-#include "sdv_hold.cuh"
 #include "sdv_host.cuh"
 #include "sdv_ring.cuh"
 #include "sdv_tma.cuh"
@@ -57,7 +56,7 @@ struct LinearParams {
   int seg_bytes;   // bytes of the segment-mass array (multiple of 128)
   int slice_vecs;  // capacity of each slice buffer in 16-byte vectors (TMA)
   int spec;        // let a cluster's last sequence read ahead (0: never)
-  int hold;        // sampled, TMA: keep each position's slices for the draw
+  int l2keep;      // sampled, TMA: rows read evict_last until not needed
 };
 
 constexpr int kMaxW = 4;  // positions per step when a cluster speculates
@@ -94,7 +93,6 @@ __global__ void __launch_bounds__(kThreads, RING ? 4 : 2)
   extern __shared__ __align__(128) unsigned char dsm[];
   __shared__ LinearSmem sh;
   __shared__ uint64_t bars[2 * kStages];
-  __shared__ uint64_t hbars[kHoldMax];
   using GR = GRow<DT, VW>;
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
@@ -114,19 +112,23 @@ __global__ void __launch_bounds__(kThreads, RING ? 4 : 2)
   rg.empty = bars + kStages;
   rg.dev_status = p.dev_status;
   if (RING) ring_init(rg);
-  // hold mode (sampled, TMA, one position per step): the position's slices
-  // stay in the same shared memory as the ring's stages until the draw
-  Hold hd;
-  hd.buf = rg.buf;
-  hd.full = hbars;
-  hd.dev_status = p.dev_status;
-  const bool hold = RING && !GREEDY && p.hold;
-  if (hold) hold_init(hd);
   auto trow_of = [&](int s, int j) {
     return tbase + ((size_t)s * (gamma + 1) + j) * rowb;
   };
   auto drow_of = [&](int s, int j) {
     return dbase + ((size_t)s * p.d_seq_rows + j) * rowb;
+  };
+  // L2 priorities: a step's rows are read with evict_last, so they stay in
+  // L2 ahead of other clusters' lines until the step is decided; then they
+  // go back to the normal priority, except the deciding position's rows,
+  // which the draw reads again (demoted after it)
+  const bool l2keep = RING && !GREEDY && p.l2keep;
+  if (l2keep) rg.policy = l2_evict_last_policy();
+  auto demote = [&](int s, int j) {
+    const size_t off = (size_t)sl.vbeg * 16;
+    const size_t len = (size_t)(sl.vend - sl.vbeg) * 16;
+    l2_demote(trow_of(s, j) + off, len);
+    if (j < gamma) l2_demote(drow_of(s, j) + off, len);
   };
 
   int par = 0, seqpar = 0;
@@ -165,7 +167,7 @@ __global__ void __launch_bounds__(kThreads, RING ? 4 : 2)
         sh.gzd[tid - 32] = zd;
         sh.gr[tid - 32] = r;
       }
-      if (RING && !hold && last_seq && p.spec >= 2 && tid == 0) {
+      if (RING && last_seq && p.spec >= 2 && tid == 0) {
         // the GPU is emptying out: ask for this step's and the next step's
         // rows at once (into L2), so the ring below streams from L2
         const uint32_t sb = (uint32_t)(sl.vend - sl.vbeg) * 16u;
@@ -190,8 +192,7 @@ __global__ void __launch_bounds__(kThreads, RING ? 4 : 2)
         } else {
           MS st[2] = {ms_empty(), ms_empty()};
           if constexpr (RING) {
-            if (hold) hold_stats<DT, VW>(hd, trow, drow, sl, k2, st[0], st[1]);
-            else ring_stats<DT, VW>(rg, trow, drow, sl, k2, st[0], st[1]);
+            ring_stats<DT, VW>(rg, trow, drow, sl, k2, st[0], st[1]);
           } else {
             stats_pass<DT, VW>(GR{trow}, GR{drow}, has_d, sl, k2, st[0], st[1]);
           }
@@ -260,15 +261,18 @@ __global__ void __launch_bounds__(kThreads, RING ? 4 : 2)
       }
       __syncthreads();
       R = sh.res;
+      if (l2keep) {  // rows of this step that no draw will read again
+        const int keep = (R.kind == 1 || R.kind == 2) ? R.n : -1;
+        for (int j = i; j < jend; ++j)
+          if (j != keep) demote(seq, j);
+      }
       if (R.kind) break;
       i = jend;
       if (first) {  // after the first step: is this the cluster's last?
         last_seq = cluster.map_shared_rank(&sh, 0)->next_seq[seqpar] >= p.B;
         first = false;
       }
-      // (hold mode keeps one position per step: the draw needs the slices
-      // of the position that decided)
-      w = (last_seq && p.spec && !hold) ? min(2 * w, kMaxW) : 1;
+      w = (last_seq && p.spec) ? min(2 * w, kMaxW) : 1;
     }
     const int n = R.n, kind = R.kind, bad_token = R.bad;
 
@@ -327,8 +331,7 @@ __global__ void __launch_bounds__(kThreads, RING ? 4 : 2)
       for (int attempt = 0; attempt < 2; ++attempt) {
         cluster_total(cluster, sh.draw, segmass, sl, u, par, [&] {
           if constexpr (RING) {
-            if (hold) held_mass<DT, VW>(hd, has_q, W, sl, segmass);
-            else ring_mass<DT, VW>(rg, trow, drow, has_q, W, sl, segmass);
+            ring_mass<DT, VW>(rg, trow, drow, has_q, W, sl, segmass);
           } else {
             mass_pass<DT, VW>(ra, rb, has_q, W, sl, segmass);
           }
@@ -359,6 +362,7 @@ __global__ void __launch_bounds__(kThreads, RING ? 4 : 2)
       if (p.out_resid)
         write_resid<DT, VW>(p.out_resid + (size_t)seq * V, ra, rb, has_q, W,
                             sl, o.N);
+      if (l2keep) demote(seq, n);  // the draw has read them again
     }
     // next sequence (rank 0 published it before this sequence's first sync)
     seq = cluster.map_shared_rank(&sh, 0)->next_seq[seqpar];
@@ -427,31 +431,12 @@ sd_status linear_launch(const void *target, const void *draft, sd_dtype dt,
   // many sequences: smaller clusters keep more of them in flight (measured
   // on the 256 x 128256 fp32 workload: 8 beats 16)
   int CL = choose_cluster(nvec);
-  if (B >= 128 && CL > 8 && env_int("SDV_CLUSTER", 0) == 0) CL = 8;
-  const bool ring = vec && env_int("SDV_NO_TMA", 0) == 0;
-  // hold mode (SDV_HOLD=1; sampled, TMA): every CTA keeps its slices of the
-  // current position in shared memory for the draw.  Clusters grow until a
-  // held slice takes at most 64 KB (three CTAs per SM).
-  auto held_bytes = [&](int cl) {
-    const long long pc = (nvec + cl - 1) / cl;
-    return (size_t)((pc + kStg - 1) / kStg) * kStageVecs * 16;
-  };
-  bool hold = ring && !greedy && env_int("SDV_HOLD", 0) != 0;
-  if (hold) {
-    int cl = CL;
-    if (env_int("SDV_CLUSTER", 0) == 0)
-      while (cl < 16 && held_bytes(cl) > 64 * 1024) cl *= 2;
-    const long long pc = (nvec + cl - 1) / cl;
-    if ((pc + kStg - 1) / kStg <= kHoldMax && held_bytes(cl) <= 192 * 1024)
-      CL = cl;
-    else
-      hold = false;
-  }
+  if (B >= 128 && CL > 8 && tune(SD_TUNE_CLUSTER) == 0) CL = 8;
+  const bool ring = vec && tune(SD_TUNE_NO_TMA) == 0;
   const long long per_cta = (nvec + CL - 1) / CL;
   const size_t seg_bytes = ((size_t)((per_cta + 31) / 32) * 4 + 127) / 128 * 128;
-  const size_t smem =
-      seg_bytes + (hold ? held_bytes(CL) : ring ? (size_t)kRingBytes : 0);
-  if (smem > (hold ? 200 : 96) * 1024)
+  const size_t smem = seg_bytes + (ring ? (size_t)kRingBytes : 0);
+  if (smem > 96 * 1024)
     return fail(SD_ERR_UNSUPPORTED, "V=%d needs %zu B of shared memory", V,
                 smem);
   LinearKernel kern = pick_linear(dt, vec, ring, greedy);
@@ -479,8 +464,8 @@ sd_status linear_launch(const void *target, const void *draft, sd_dtype dt,
   prm.nclusters = nclusters;
   prm.seg_bytes = (int)seg_bytes;
   prm.slice_vecs = (int)per_cta;
-  prm.spec = hold ? 0 : env_int("SDV_SPEC", 1);
-  prm.hold = hold ? 1 : 0;
+  prm.spec = tune(SD_TUNE_SPEC);
+  prm.l2keep = (ring && !greedy) ? tune(SD_TUNE_L2_KEEP) : 0;
   if (B > nclusters) {
     if (!ws || ws_bytes < 256)
       return fail(SD_ERR_INVALID_ARG, "workspace of >= 256 bytes required");
@@ -492,36 +477,13 @@ sd_status linear_launch(const void *target, const void *draft, sd_dtype dt,
                          args);
 }
 
-size_t wide_workspace(int B, int gamma, int V, sd_dtype dt);
-sd_status wide_launch(const void *target, const void *draft, sd_dtype dt,
-                      long long d_seq_rows, const int32_t *tokens,
-                      const float *uniforms, int B, int gamma, int V, float T,
-                      int32_t *n_acc, int32_t *out_tokens, float *out_prob,
-                      float *out_accept, int32_t *dev_status, void *ws,
-                      size_t ws_bytes, cudaStream_t stream);
-
-// The position-by-position kernels over the whole batch (sdv_wide.cu) are
-// selected with SDV_WIDE=1; the cluster kernel below is faster on the
-// measured workloads, so that path is opt-in.
-bool use_wide(int B, int V, sd_dtype dt, const void *target,
-              const void *draft, float T, const float *out_resid) {
-  const int eb = dt == SD_F32 ? 4 : 2;
-  const bool vec = aligned16(target) && (T == 0.f || aligned16(draft)) &&
-                   ((size_t)V * eb) % 16 == 0;
-  if (!vec || out_resid) return false;
-  (void)B;
-  return env_int("SDV_WIDE", 0) != 0;
-}
-
 }  // namespace sdv
 
 extern "C" size_t sd_verify_linear_workspace(int B, int gamma, int V,
                                              sd_dtype dt) {
-  size_t w = (B > 0 && V > 0 && gamma >= 0)
-                 ? sdv::wide_workspace(B, gamma, V, dt)
-                 : 0;
-  const size_t a = sdv::allrows_workspace(B, gamma, V, dt);
-  if (a > w) w = a;
+  // the work-queue counter; for small inputs the all-rows path's slice
+  // states (at most 512 KB)
+  const size_t w = sdv::allrows_workspace(B, gamma, V, dt);
   return w > 256 ? w : 256;
 }
 
@@ -543,12 +505,6 @@ extern "C" sd_status sd_verify_linear(
   SDV_REQUIRE(T == 0.f || uniforms, "uniforms is null");
   SDV_REQUIRE(T == 0.f || gamma == 0 || draft_logits,
               "draft_logits is null with T > 0");
-  if (sdv::use_wide(B, V, dt, target_logits, draft_logits, T, out_resid))
-    return sdv::wide_launch(target_logits, draft_logits, dt, gamma,
-                            draft_tokens, uniforms, B, gamma, V, T,
-                            n_accepted, out_tokens, out_prob, out_accept_prob,
-                            dev_status, workspace, ws_bytes,
-                            static_cast<cudaStream_t>(stream));
   return sdv::linear_launch(target_logits, draft_logits, dt, gamma,
                             draft_tokens, uniforms, B, gamma, V, T,
                             n_accepted, out_tokens, out_prob, out_accept_prob,

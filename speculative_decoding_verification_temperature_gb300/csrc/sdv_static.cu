@@ -3,11 +3,14 @@
 // allocate (the method itself has no such requirement).
 //
 // The array exists once per device.  Its address is looked up with
-// cudaGetSymbolAddress the first time the call runs on a device (with that
-// device current) and cached; nothing is allocated or freed, here or in the
-// path it hands the array to (sd_verify_linear, which clears the counters
-// that must start at zero with a memset on the stream).  Two calls whose
-// work overlaps on the GPU share the array and race.
+// cudaGetSymbolAddress (with the device current) on every call made outside
+// a stream capture, so a device reset cannot leave a stale address behind;
+// a call made while its stream is being captured reuses the address found
+// by the last uncaptured call on that device (the first call on a device
+// must therefore come before any capture).  Nothing is allocated or freed,
+// here or in the path the array is handed to (sd_verify_linear, which
+// clears the counters that must start at zero with a memset on the stream).
+// Two calls whose work overlaps on the GPU share the array and race.
 #include <mutex>
 
 #include "sdv_host.cuh"
@@ -20,20 +23,26 @@ constexpr int kMaxDevices = 64;
 static std::mutex g_static_mu;
 static void *g_static_ptr[kMaxDevices];
 
-static sd_status static_scratch(void **out) {
+static sd_status static_scratch(cudaStream_t stream, void **out) {
   int dev = 0;
   SDV_CUDA(cudaGetDevice(&dev));
   if (dev < 0 || dev >= kMaxDevices)
     return fail(SD_ERR_UNSUPPORTED, "device ordinal %d >= %d", dev,
                 kMaxDevices);
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  SDV_CUDA(cudaStreamIsCapturing(stream, &cap));
   std::lock_guard<std::mutex> g(g_static_mu);
-  if (!g_static_ptr[dev]) {
+  if (cap == cudaStreamCaptureStatusNone) {
     void *p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_static_ws);
     if (e != cudaSuccess)
       return fail(SD_ERR_CUDA, "cudaGetSymbolAddress of the static scratch: %s",
                   cudaGetErrorString(e));
     g_static_ptr[dev] = p;
+  } else if (!g_static_ptr[dev]) {
+    return fail(SD_ERR_INVALID_ARG,
+                "first call on device %d inside a stream capture: make one "
+                "call outside the capture first", dev);
   }
   *out = g_static_ptr[dev];
   return SD_OK;
@@ -61,8 +70,11 @@ extern "C" sd_status sd_verify_linear_static(
                 "%zu B (SD_STATIC_WS_BYTES): use sd_verify_linear with a "
                 "workspace",
                 B, gamma, V, need, (size_t)SD_STATIC_WS_BYTES);
+  int sms = 0;
+  const sd_status dst = check_device(&sms);  // SD_ERR_UNSUPPORTED off sm_103
+  if (dst != SD_OK) return dst;
   void *ws = nullptr;
-  const sd_status st = static_scratch(&ws);
+  const sd_status st = static_scratch(static_cast<cudaStream_t>(stream), &ws);
   if (st != SD_OK) return st;
   return sd_verify_linear(target_logits, draft_logits, dt, draft_tokens,
                           uniforms, B, gamma, V, T, n_accepted, out_tokens,

@@ -584,7 +584,7 @@ sd_status sdv::tree_launch(
     seg_bytes = ((size_t)((per_cta + 31) / 32) * 4 + 127) / 128 * 128;
     const size_t tma_smem =
         seg_bytes + (one_row ? 1 : 2) * (size_t)per_cta * 16;
-    tma = vec && tma_smem <= kTreeTmaSmemMax && env_int("SDV_NO_TMA", 0) == 0;
+    tma = vec && tma_smem <= kTreeTmaSmemMax && tune(SD_TUNE_NO_TMA) == 0;
     smem = tma ? tma_smem : seg_bytes;
     if (smem > 96 * 1024)
       return fail(SD_ERR_UNSUPPORTED, "V=%d needs %zu B of shared memory", V,
@@ -592,7 +592,7 @@ sd_status sdv::tree_launch(
     kern = pick_tree(dt, vec, tma, greedy, det);
     st = max_active_clusters((const void *)kern, CL, smem, &maxc);
     if (st != SD_OK) return st;
-    if (CL > 8 && maxc < B && env_int("SDV_CLUSTER", 0) == 0) {
+    if (CL > 8 && maxc < B && tune(SD_TUNE_CLUSTER) == 0) {
       CL = 8;
       continue;
     }

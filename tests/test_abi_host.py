@@ -180,3 +180,27 @@ def test_binding_refuses_cpu_tensors(name):
     tensors with a ValueError before anything reaches the library."""
     with pytest.raises(ValueError, match="CUDA"):
         _cpu_calls()[name]()
+
+
+def test_tuning_switches_set_get_and_validate():
+    """sd_tune_set / sd_tune_get: defaults, a round trip, unknown keys and
+    out-of-range values refused, and nothing read from the environment."""
+    L = api.lib()
+    defaults = {"cluster": 0, "no_tma": 0, "allrows": 1, "spec": 1,
+                "fused": 0, "kcand_ring": 1, "fanout_cluster": 0,
+                "fanout_ldg": 0, "fanout_maxc": 0, "fanout_l2_first": 1}
+    for k, v in defaults.items():
+        assert api.tune_get(k) == v, k
+    assert api.tune_get("l2_keep") in (0, 1)
+    with api.tuned(cluster=4, allrows=2):
+        assert api.tune_get("cluster") == 4 and api.tune_get("allrows") == 2
+    assert api.tune_get("cluster") == 0 and api.tune_get("allrows") == 1
+    assert L.sd_tune_set(99, 1) == api.SD_ERR_INVALID_ARG
+    assert L.sd_tune_get(99) == -1
+    assert L.sd_tune_set(api.TUNE["cluster"], 3) == api.SD_ERR_INVALID_ARG
+    assert L.sd_tune_set(api.TUNE["spec"], 3) == api.SD_ERR_INVALID_ARG
+    assert L.sd_tune_set(api.TUNE["fused"], -1) == api.SD_ERR_INVALID_ARG
+    assert api.tune_get("cluster") == 0
+    src = "".join(open(f).read() for f in sorted(__import__("glob").glob(
+        os.path.join(os.path.dirname(api.__file__), "csrc", "*.cu*"))))
+    assert "getenv" not in src

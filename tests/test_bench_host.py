@@ -122,3 +122,38 @@ def test_traffic_constants_are_plausible():
     assert abs(fan_bytes / fan_rows - 128256 * 4) < 0.01 * 128256 * 4
     lin_traffic, lin_needed = bench.TRAFFIC["linear"]
     assert 1.0 < lin_traffic / lin_needed < 2.0
+
+
+def test_flag_summary_counts_and_mismatches():
+    """bench.flag_summary on oracle results: outputs equal to the oracle's
+    give no mismatch; a changed count or a changed token outside a flagged
+    draw is one mismatch each; a near-boundary final draw inside the
+    admissible range is counted in cdf_diff, not as a mismatch."""
+    import torch
+    import oracle
+    from speculative_decoding_verification_temperature_gb300 import synth
+    c = synth.linear_case(300, 4, 200, torch.float32, 1.0, seed=3,
+                          sigma_t=2.0, sigma_d=1.0)
+    o = oracle.verify_linear(synth.host_logits(c.target),
+                             synth.host_logits(c.draft), c.tokens.numpy(),
+                             c.uniforms.numpy(), 1.0)
+    g = {"n": o["n"].copy(), "tokens": o["tokens"].copy()}
+    s = bench.flag_summary(o, g, 1.0)
+    assert s["mismatches"] == 0 and s["sequences"] == 300
+    assert s["accept_tests"] == int(np.minimum(o["n"] + 1, 4).sum())
+    assert s["cdf_draws"] == 300
+    clean = np.nonzero((o["margin_acc"] >= 1e-5) &
+                       (o["margin_cdf"] >= 1e-5))[0]
+    g["n"][clean[0]] += 1
+    g["tokens"][clean[1], 0] ^= 1
+    assert bench.flag_summary(o, g, 1.0)["mismatches"] == 2
+    near = np.nonzero((o["margin_cdf"] < 1e-5) & (o["margin_acc"] >= 1e-5) &
+                      (o["cdf_hi"] > o["cdf_lo"]))[0]
+    if near.size:
+        b = near[0]
+        g = {"n": o["n"].copy(), "tokens": o["tokens"].copy()}
+        alt = o["cdf_lo"][b] if o["tokens"][b, o["n"][b]] != o["cdf_lo"][b] \
+            else o["cdf_hi"][b]
+        g["tokens"][b, o["n"][b]] = alt
+        s = bench.flag_summary(o, g, 1.0)
+        assert s["mismatches"] == 0 and s["cdf_diff"] == 1

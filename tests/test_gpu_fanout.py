@@ -8,7 +8,8 @@ import torch
 
 import oracle
 from speculative_decoding_verification_temperature_gb300 import api, synth
-from tests.parity import host
+from tests.parity import (assert_flag_fraction, compare, host,
+                          linear_oracle_full, oracle_over_threads)
 
 pytestmark = pytest.mark.gpu
 
@@ -23,15 +24,44 @@ def check(draft, F):
     return g, o
 
 
-def test_large_workload_rows_sampled():
-    """The 9 draft rows of 12 sequences of the large workload (V=128256
-    fp32), geometric F = [10,9,8,7,6,6,5,4,9]."""
+def test_large_step_every_row():
+    """The benchmark's step on the large workload (B=256, V=128256 fp32):
+    the fan-out over all 2304 draft rows on a second stream beside the
+    linear verify, each with its own workspace, exactly as timed; every
+    row's top-F_k (F = [10,9,8,7,6,6,5,4,9]) and every sequence's verify
+    against the oracle (host threads)."""
     c = synth.large(0, device="cuda")
     F = api.fanout_schedule(8, 64, 0.8, 1.0)
     assert F == [10, 9, 8, 7, 6, 6, 5, 4, 9]
-    idx = torch.tensor([0, 1, 2, 50, 100, 127, 128, 200, 250, 253, 254, 255],
-                       device="cuda")
-    check(c.draft[idx].contiguous(), F)
+    draft_v = c.draft[:, :8].contiguous()
+    main = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
+    ws_v, ws_f = api.Workspace(), api.Workspace()
+    st = torch.zeros(2, dtype=torch.int32, device="cuda")
+    fork = torch.cuda.Event()
+    fork.record(main)
+    side.wait_event(fork)
+    with torch.cuda.stream(side):
+        f = api.fanout_topk(c.draft, F, want_logit=True, status=st[1:],
+                            workspace=ws_f)
+    g = api.verify_linear(c.target, draft_v, c.tokens, c.uniforms, 1.0,
+                          status=st[:1], workspace=ws_v)
+    join = torch.cuda.Event()
+    join.record(side)
+    main.wait_event(join)
+    torch.cuda.synchronize()
+    assert host(st).tolist() == [0, 0]
+    d = synth.host_logits(c.draft)
+    Fa = np.array(F, np.int32)
+    of = oracle_over_threads(
+        lambda lo, hi: oracle.fanout_topk(d[lo:hi], Fa), d.shape[0])
+    np.testing.assert_array_equal(host(f["tokens"]), of["tokens"])
+    np.testing.assert_array_equal(host(f["logit"]).astype(np.float64),
+                                  of["logit"])
+    ov = linear_oracle_full(c.target, draft_v, c.tokens, c.uniforms, 1.0)
+    r = compare(g, ov)
+    assert r["seqs"] == 256
+    assert_flag_fraction(r)
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
@@ -111,17 +141,17 @@ def test_infinite_rows():
 
 @pytest.mark.parametrize("mode", ["ring", "ldg"])
 @pytest.mark.parametrize("cluster", ["1", "2", "16"])
-def test_streaming_variants_and_clusters(monkeypatch, mode, cluster):
+def test_streaming_variants_and_clusters(mode, cluster):
     """Both streaming variants (TMA ring, 16-byte loads) with rows split
     over clusters of 1, 2 and 16 CTAs (F = 64 caps the cluster at 8)."""
-    monkeypatch.setenv("SDV_FANOUT_LDG", "1" if mode == "ldg" else "0")
-    monkeypatch.setenv("SDV_FANOUT_CLUSTER", cluster)
     g = torch.Generator().manual_seed(int(cluster))
-    for dtype in (torch.float32, torch.bfloat16):
-        d = (torch.randn((3, 3, 50000), generator=g) * 2).to(dtype)
-        d[0, 1] = torch.arange(50000).to(dtype)  # best keys in the last warp
-        d[1, 2] = torch.randint(-3, 3, (50000,), generator=g).to(dtype)
-        check(d.cuda(), [64, 33, 10])
+    with api.tuned(fanout_ldg=int(mode == "ldg"),
+                   fanout_cluster=int(cluster)):
+        for dtype in (torch.float32, torch.bfloat16):
+            d = (torch.randn((3, 3, 50000), generator=g) * 2).to(dtype)
+            d[0, 1] = torch.arange(50000).to(dtype)  # best keys: last warp
+            d[1, 2] = torch.randint(-3, 3, (50000,), generator=g).to(dtype)
+            check(d.cuda(), [64, 33, 10])
 
 
 def test_best_keys_in_one_warp():

@@ -10,7 +10,8 @@ import torch
 
 import oracle
 from speculative_decoding_verification_temperature_gb300 import api, synth
-from tests.parity import compare, host, to_device
+from tests.parity import (assert_flag_fraction, compare, host,
+                          oracle_over_threads, to_device)
 
 pytestmark = pytest.mark.gpu
 
@@ -79,24 +80,30 @@ def test_small_cases(V, dtype, gamma, top_k, top_p):
 
 
 @pytest.mark.parametrize("cluster", ["1", "2", "8"])
-def test_cluster_sizes(monkeypatch, cluster):
-    monkeypatch.setenv("SDV_CLUSTER", cluster)
+def test_cluster_sizes(cluster):
     c = to_device(case(16, 3, 40000, torch.float32, 1.0, 40, 0.95,
                        seed=int(cluster)))
-    compare(run(c, 40, 0.95), orc(c, 40, 0.95))
+    with api.tuned(cluster=int(cluster)):
+        g = run(c, 40, 0.95)
+    compare(g, orc(c, 40, 0.95))
 
 
-def test_large_workload_shape_sampled():
+def test_large_workload_shape_every_sequence():
     """B=256, gamma=8, V=128256 fp32, T=1, top_k=50, top_p=0.9; drafts from
-    the workload's (unfiltered) draft sampler; 10 sequences checked."""
+    the workload's (unfiltered) draft sampler: all 256 sequences against
+    the oracle (host threads)."""
     c = synth.large(0, device="cuda")
     c.draft = c.draft[:, :8].contiguous()
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     g = run(c, 50, 0.9, status=st)
     assert int(st.item()) & ~api.DEV_ZERO_MASS == 0
-    idx = torch.tensor([0, 1, 2, 50, 100, 127, 128, 200, 254, 255],
-                       device="cuda")
-    compare({k: v[idx] for k, v in g.items()}, orc(c, 50, 0.9, idx))
+    t, d = synth.host_logits(c.target), synth.host_logits(c.draft)
+    tk, u = host(c.tokens), host(c.uniforms)
+    o = oracle_over_threads(lambda lo, hi: oracle.verify_linear_filtered(
+        t[lo:hi], d[lo:hi], tk[lo:hi], u[lo:hi], 1.0, 50, 0.9), 256)
+    r = compare(g, o)
+    assert r["seqs"] == 256
+    assert_flag_fraction(r)
 
 
 def test_nan_rows_and_greedy_and_misaligned():

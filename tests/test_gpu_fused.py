@@ -19,6 +19,14 @@ pytestmark = pytest.mark.gpu
 F_LARGE = [10, 9, 8, 7, 6, 6, 5, 4, 9]
 
 
+@pytest.fixture(autouse=True)
+def fused_kernel():
+    """These tests exercise the fused kernel (SD_TUNE_FUSED 1); the default
+    of sd_verify_linear_fanout is the two separate calls."""
+    with api.tuned(fused=1):
+        yield
+
+
 def run(c, F, **kw):
     return api.verify_linear_fanout(c.target, c.draft, c.tokens, c.uniforms,
                                     c.T, F, **kw)
@@ -77,12 +85,12 @@ def test_sizes(V, dtype, gamma):
 
 
 @pytest.mark.parametrize("cluster", ["1", "2", "4", "8", "16"])
-def test_cluster_sizes(monkeypatch, cluster):
-    monkeypatch.setenv("SDV_CLUSTER", cluster)
+def test_cluster_sizes(cluster):
     c = to_device(synth.linear_case(20, 6, 40000, torch.float32, 0.8,
                                     seed=int(cluster), sigma_t=2.0,
                                     sigma_d=1.0, draft_rows=7))
-    check(c, [64, 1, 5, 0, 33, 8, 2])
+    with api.tuned(cluster=int(cluster)):
+        check(c, [64, 1, 5, 0, 33, 8, 2])
 
 
 def test_queue_many_sequences():
@@ -110,14 +118,13 @@ def test_nan_rows():
     assert int(st.item()) & api.DEV_NONFINITE
 
 
-def test_fallback_path_matches(monkeypatch):
-    """SDV_FUSED=0 and an unaligned vocabulary take the two separate calls;
-    both agree with the oracle too."""
+def test_fallback_path_matches():
+    """The two separate calls (SD_TUNE_FUSED 0, the default) and an
+    unaligned vocabulary (no fused kernel); both agree with the oracle."""
     c = to_device(synth.linear_case(16, 3, 6000, torch.bfloat16, 1.0, seed=3,
                                     sigma_t=2.0, sigma_d=1.0, draft_rows=4))
-    monkeypatch.setenv("SDV_FUSED", "0")
-    check(c, [5, 4, 3, 2])
-    monkeypatch.delenv("SDV_FUSED")
+    with api.tuned(fused=0):
+        check(c, [5, 4, 3, 2])
     c = to_device(synth.linear_case(16, 3, 6001, torch.float32, 1.0, seed=4,
                                     sigma_t=2.0, sigma_d=1.0, draft_rows=4))
     check(c, [5, 4, 3, 2])

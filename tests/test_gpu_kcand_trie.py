@@ -11,7 +11,8 @@ from scipy import stats
 
 import oracle
 from speculative_decoding_verification_temperature_gb300 import api, synth
-from tests.parity import compare, host, to_device
+from tests.parity import (assert_flag_fraction, compare, host,
+                          oracle_over_threads, to_device)
 from tests.test_oracle_pins import _trie_law_case, softmax
 
 pytestmark = pytest.mark.gpu
@@ -65,16 +66,24 @@ def test_one_candidate_equals_linear():
     assert torch.all(g["k"] == 0)
 
 
-def test_kcand_workload_sampled():
-    """B=64, K=8, gamma=16, V=152064 bf16, T=1, full size on the device; 4
-    sequences checked against the oracle."""
+def test_kcand_workload_every_sequence():
+    """B=64, K=8, gamma=16, V=152064 bf16, T=1, full size on the device:
+    all 64 candidate trees against the oracle (host threads)."""
     c = synth.kcand(0, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     g = run(c, status=st)
     assert int(st.item()) & ~api.DEV_ZERO_MASS == 0
-    idx = torch.tensor([0, 21, 42, 63], device="cuda")
-    compare({k: v[idx] for k, v in g.items()}, tr_oracle(c, idx),
-            extra_equal=("k",))
+    t, d = synth.host_logits(c.target), synth.host_logits(c.draft)
+    tk, u = host(c.tokens), host(c.uniforms)
+
+    def part(lo, hi):
+        o = oracle.verify_kcand_trie(t[lo:hi], d[lo:hi], tk[lo:hi],
+                                     u[lo:hi], 1.0)
+        o.pop("trie")
+        return o
+    r = compare(g, oracle_over_threads(part, 64), extra_equal=("k",))
+    assert r["seqs"] == 64
+    assert_flag_fraction(r)
 
 
 def test_invalid_rows_and_tokens():

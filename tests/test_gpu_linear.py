@@ -4,7 +4,7 @@ Covers the two small workloads at full size (tiny: B=1, gamma=4, V=1000
 fp32; linear: B=32, gamma=8, V=32000 bf16 at T in {0, 0.7, 1}), ragged and
 unaligned vocabularies (scalar path), gamma 0 and 1, the queue path
 (B larger than the resident clusters), the large workload (B=256, gamma=8,
-V=128256 fp32) on sampled sequences, the edge cases (bad token, NaN and
+V=128256 fp32) on every sequence, the edge cases (bad token, NaN and
 +inf rows, -inf masks, zero-mass residual), the debug outputs, and the
 emitted-token law on the GPU (chi-square, 1e6 trials).
 """
@@ -17,7 +17,8 @@ from scipy import stats
 
 import oracle
 from speculative_decoding_verification_temperature_gb300 import api, synth
-from tests.parity import compare, host, linear_oracle, to_device
+from tests.parity import (assert_flag_fraction, compare, host,
+                          linear_oracle, linear_oracle_full, to_device)
 
 pytestmark = pytest.mark.gpu
 
@@ -51,7 +52,7 @@ def test_tiny_workload_batched_1000_rounds():
     c = to_device(synth.linear_case(1000, 4, 1000, torch.float32, 1.0,
                                     seed=1000, sigma_t=2.0, sigma_d=1.0))
     r = compare(run(c), linear_oracle(c))
-    assert r["acc_flagged"] / r["seqs"] < 5e-3
+    assert_flag_fraction(r)
 
 
 @pytest.mark.parametrize("T", [0.0, 0.7, 1.0])
@@ -62,6 +63,7 @@ def test_linear_workload(T):
     g = run(c, want_accept=True, status=st)
     o = linear_oracle(c)
     r = compare(g, o)
+    assert_flag_fraction(r)
     if T == 0:
         assert r["acc_flagged"] == 0 and r["cdf_flagged"] == 0
     assert int(st.item()) == 0
@@ -129,21 +131,22 @@ def test_resid_and_accept_debug_outputs():
                                    atol=1e-5)
 
 
-def test_large_workload_sampled():
-    """B=256, gamma=8, V=128256 fp32 (the bench workload, same launch) on
-    the device; 10 sequences checked against the oracle one by one."""
+def test_large_workload_every_sequence():
+    """B=256, gamma=8, V=128256 fp32 (the benchmark's workload and launch):
+    all 256 sequences against the oracle (run over host threads), and the
+    accept-flagged fraction held to the bar."""
     c = synth.large(0, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
-    g = api.verify_linear(c.target, c.draft[:, :8].contiguous(), c.tokens,
-                          c.uniforms, 1.0, status=st)
+    draft_v = c.draft[:, :8].contiguous()
+    g = api.verify_linear(c.target, draft_v, c.tokens, c.uniforms, 1.0,
+                          status=st)
     assert int(st.item()) == 0
     n = host(g["n"])
     assert n.min() >= 0 and n.max() <= 8
-    idx = [0, 1, 2, 3, 100, 128, 200, 254, 255] + [int(np.argmax(n))]
-    sub = synth.LinearCase(c.target[idx], c.draft[idx, :8], c.tokens[idx],
-                           c.uniforms[idx], 1.0)
-    o = linear_oracle(sub)
-    compare({k: v[idx] for k, v in g.items()}, o)
+    o = linear_oracle_full(c.target, draft_v, c.tokens, c.uniforms, 1.0)
+    r = compare(g, o)
+    assert r["seqs"] == 256 and r["tests"] > 0
+    assert_flag_fraction(r)
 
 
 def test_edge_cases():
@@ -200,13 +203,14 @@ def test_emitted_token_law_on_gpu():
 
 
 def test_flagged_fractions():
-    """Over 20000 sequences of the tiny workload: accept tests within 1e-5
-    of their threshold stay under 1e-3 of the sequences; every other
-    sequence matches exactly, and near-boundary final draws (counted) stay
-    inside the oracle's admissible range and almost always equal its
-    token."""
+    """Over 20000 sequences of the tiny workload (about 45000 accept tests):
+    accept tests within 1e-5 of their threshold stay below 1e-4 of the tests
+    made; every other sequence matches exactly, and near-boundary final
+    draws (counted) stay inside the oracle's admissible range and almost
+    always equal its token."""
     c = to_device(synth.linear_case(20000, 4, 1000, torch.float32, 1.0,
                                     seed=77, sigma_t=2.0, sigma_d=1.0))
     r = compare(run(c), linear_oracle(c))
-    assert r["acc_flagged"] / r["seqs"] < 1e-3
+    assert r["tests"] > 40000
+    assert r["tests_flagged"] / r["tests"] < 1e-4
     assert r["cdf_diff"] <= max(2, r["cdf_flagged"] // 20)

@@ -1,8 +1,8 @@
 """Both paths of sd_verify_linear against the oracle on the same inputs:
-the per-position cluster kernel (SDV_ALLROWS=0) and the all-rows path for
-small inputs (SDV_ALLROWS=2 forces it wherever its workspace and shared
-memory allow), plus the cluster kernel's hold mode (SDV_HOLD=1: each
-position's slices kept in shared memory for the draw).  Small and odd
+the per-position cluster kernel (SD_TUNE_ALLROWS 0) and the all-rows path
+for small inputs (SD_TUNE_ALLROWS 2 forces it wherever its workspace and
+shared memory allow), plus the cluster kernel with its rows held in L2 by
+evict_last until the draw (SD_TUNE_L2_KEEP 1) and without.  Small and odd
 sizes, both dtypes, unaligned rows, gamma 0, T in {0, 0.7, 1}, bad tokens
 and non-finite rows, the queue path, the accept-probability output; and
 the two paths agree with each other."""
@@ -23,19 +23,22 @@ def run(case, **kw):
                              case.T, **kw)
 
 
-@pytest.mark.parametrize("mode", ["0", "2", "0-hold"])
+def switches(mode):
+    return {"allrows": int(mode.split("-")[0]),
+            "l2_keep": int(mode.endswith("keep"))}
+
+
+@pytest.mark.parametrize("mode", ["0", "2", "0-keep"])
 @pytest.mark.parametrize("T", [0.0, 0.7, 1.0])
 @pytest.mark.parametrize("B,gamma,V,dtype", [
     (1, 4, 1000, torch.float32), (32, 8, 32000, torch.bfloat16),
     (7, 3, 1001, torch.float32), (5, 0, 4096, torch.bfloat16),
     (300, 2, 640, torch.float32), (3, 16, 50000, torch.float32)])
-def test_paths_against_oracle(monkeypatch, mode, T, B, gamma, V, dtype):
-    monkeypatch.setenv("SDV_ALLROWS", mode.split("-")[0])
-    if mode.endswith("hold"):
-        monkeypatch.setenv("SDV_HOLD", "1")
+def test_paths_against_oracle(mode, T, B, gamma, V, dtype):
     c = to_device(synth.linear_case(B, gamma, V, dtype, T, seed=B + V + gamma,
                                     sigma_t=2.0, sigma_d=1.0))
-    g = run(c, want_accept=True)
+    with api.tuned(**switches(mode)):
+        g = run(c, want_accept=True)
     o = linear_oracle(c)
     r = compare(g, o)
     assert r["acc_flagged"] <= max(1, B // 50)
@@ -46,11 +49,8 @@ def test_paths_against_oracle(monkeypatch, mode, T, B, gamma, V, dtype):
         assert np.all(host(g["accept"])[~ev] == -1)
 
 
-@pytest.mark.parametrize("mode", ["0", "2", "0-hold"])
-def test_paths_edge_rows(monkeypatch, mode):
-    monkeypatch.setenv("SDV_ALLROWS", mode.split("-")[0])
-    if mode.endswith("hold"):
-        monkeypatch.setenv("SDV_HOLD", "1")
+@pytest.mark.parametrize("mode", ["0", "2", "0-keep"])
+def test_paths_edge_rows(mode):
     c = synth.linear_case(8, 4, 2000, torch.float32, 1.0, seed=77)
     c.tokens[1, 0] = 10**6            # bad token, tested first
     c.target[2, 1, 5] = float("nan")  # unusable target row
@@ -58,7 +58,8 @@ def test_paths_edge_rows(monkeypatch, mode):
     c.target[4, :, 100:] = -float("inf")  # masked tokens
     c = to_device(c)
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
-    g = run(c, status=st, want_accept=True)
+    with api.tuned(**switches(mode)):
+        g = run(c, status=st, want_accept=True)
     compare(g, linear_oracle(c))
     s = int(st.item())
     assert s & api.DEV_NONFINITE and s & api.DEV_BAD_TOKEN
@@ -68,16 +69,13 @@ def test_paths_agree():
     """Away from the flagged draws the two paths return the same tokens."""
     c = to_device(synth.linear(1.0))
     outs = []
-    for mode in ("0", "2"):
-        import os
-        os.environ["SDV_ALLROWS"] = mode
-        try:
+    for mode in ("0", "2", "0-keep"):
+        with api.tuned(**switches(mode)):
             outs.append(run(c))
-        finally:
-            os.environ.pop("SDV_ALLROWS", None)
     o = linear_oracle(c)
     keep = host(o["margin_acc"]) >= 1e-5
     keep &= host(o["margin_cdf"]) >= 1e-5
     for k in ("n", "tokens"):
-        a, b = host(outs[0][k]), host(outs[1][k])
-        assert np.array_equal(a[keep], b[keep]), k
+        a = host(outs[0][k])
+        for other in outs[1:]:
+            assert np.array_equal(a[keep], host(other[k])[keep]), k

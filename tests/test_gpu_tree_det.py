@@ -62,14 +62,14 @@ def test_repeated_and_adjacent_sibling_tokens():
     compare(run(c), det_oracle(c), extra_equal=("nodes",))
 
 
-@pytest.mark.parametrize("env", [{"SDV_NO_TMA": "1"}, {"SDV_CLUSTER": "1"},
-                                 {"SDV_CLUSTER": "2"}, {"SDV_CLUSTER": "8"}])
-def test_load_paths_and_cluster_sizes(monkeypatch, env):
-    for k, v in env.items():
-        monkeypatch.setenv(k, v)
+@pytest.mark.parametrize("sw", [{"no_tma": 1}, {"cluster": 1},
+                                {"cluster": 2}, {"cluster": 8}])
+def test_load_paths_and_cluster_sizes(sw):
     c = to_device(synth.tree_case(10, 32, 20000, torch.bfloat16, 1.0,
                                   seed=9, sigma_t=1.0, sigma_d=1.0))
-    compare(run(c), det_oracle(c), extra_equal=("nodes",))
+    with api.tuned(**sw):
+        g = run(c)
+    compare(g, det_oracle(c), extra_equal=("nodes",))
 
 
 def test_unaligned_rows_plain_loads():

@@ -73,6 +73,11 @@ MUTANTS = [
      "const int32_t t = tokens[(size_t)b * (K + 1) + (n > 0 ? n - 1 : 0)];",
      1, ["test_cache_hits_golden",
          "test_cache_hit_rate_equals_top_f_mass_when_p_equals_q"]),
+    ("flag_without_margin", "if (m < ORC_BAND) ++*flagged;", "++*flagged;",
+     1, ["test_accept_test_counts_and_flags_planted"]),
+    ("flag_band_too_narrow", "if (m < ORC_BAND) ++*flagged;",
+     "if (m < 1e-6) ++*flagged;", 1,
+     ["test_accept_test_counts_and_flags_planted"]),
     ("nucleus_one_too_many", "if (f < top_p) keep = i + 1;",
      "if (f < top_p) keep = i + 2 < k ? i + 2 : k;", 1,
      ["test_filtered_sampling_golden"]),

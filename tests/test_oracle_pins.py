@@ -1198,3 +1198,41 @@ def test_branch_fork_topk_is_a_stable_sort_and_k_law():
     srt = np.argsort(qx)
     assert np.all(np.diff(o["k"][srt]) <= 0)
     assert o["k"].max() == km - 1 and o["k"].min() == 1
+
+
+def test_accept_test_counts_and_flags_planted():
+    """acc_tests counts the accept tests made (min(n + 1, gamma) per valid
+    sequence at T > 0, none at T == 0); acc_flagged counts those whose r lies
+    within 1e-5 of p/q.  Planted: r moved to 4e-6 below the first test's
+    ratio (still an accept, and flagged) on every other sequence whose first
+    ratio is below 1, and to 3e-5 below it (not flagged) on the rest."""
+    rng = np.random.default_rng(41)
+    B, gamma, V = 400, 3, 50
+    zt = rng.normal(0, 1.5, (B, gamma + 1, V)).astype(np.float32)
+    zd = (zt[:, :gamma] + rng.normal(0, 1.0, (B, gamma, V))).astype(
+        np.float32)
+    x = rng.integers(0, V, (B, gamma)).astype(np.int32)
+    u = synth.uniforms(42, (B, gamma + 1))
+    o = oracle.verify_linear(zt, zd, x, u, 1.0)
+    assert np.array_equal(o["acc_tests"], np.minimum(o["n"] + 1, gamma))
+    # the first test's ratio from plain numpy softmaxes (not the oracle)
+    def sm(z):
+        e = np.exp(z.astype(np.float64) - z.max(-1, keepdims=True))
+        return e / e.sum(-1, keepdims=True)
+    rho = sm(zt[:, 0])[np.arange(B), x[:, 0]] / \
+        sm(zd[:, 0])[np.arange(B), x[:, 0]]
+    low = np.nonzero(rho < 0.9)[0]
+    plant, far = low[::2], low[1::2]
+    u2 = u.copy()
+    u2[plant, 0] = (rho[plant] - 4e-6).astype(np.float32)
+    u2[far, 0] = (rho[far] - 3e-5).astype(np.float32)
+    o2 = oracle.verify_linear(zt, zd, x, u2, 1.0)
+    assert np.all(o2["n"][low] >= 1)  # r <= p/q: accepted
+    assert np.all(o2["acc_flagged"][plant] >= 1)
+    assert np.all(o2["margin_acc"][plant] < 1e-5)
+    # the far ones are not flagged unless a later test is (rare)
+    assert o2["acc_flagged"][far].sum() <= 1
+    assert o2["acc_flagged"].sum() >= len(plant)
+    assert o2["acc_flagged"].sum() <= len(plant) + 2
+    g = oracle.verify_linear(zt, None, x, u, 0.0)
+    assert g["acc_tests"].sum() == 0 and g["acc_flagged"].sum() == 0

@@ -1,7 +1,7 @@
 """sd_verify_linear_static (scratch in a static device array, no workspace)
 against sd_verify_linear on the same inputs: identical results on two calls
 in a row, with the work queue in use (more sequences than resident
-clusters), on both linear paths, and the size limit rejected on the host.
+clusters), on both linear paths; the scratch limit checked on the host.
 The file name makes pytest collect it last, so it also runs after every
 other test has used the library in the same process."""
 import pytest
@@ -21,21 +21,22 @@ def _same(a, b):
 @pytest.mark.parametrize("dtype,T", [(torch.float32, 1.0),
                                      (torch.bfloat16, 0.7),
                                      (torch.float32, 0.0)])
-@pytest.mark.parametrize("wide", ["0", "1"])
-def test_static_matches_workspace_entry_twice(monkeypatch, dtype, T, wide):
-    monkeypatch.setenv("SDV_WIDE", wide)
+@pytest.mark.parametrize("allrows", [0, 2])
+def test_static_matches_workspace_entry_twice(dtype, T, allrows):
     c = synth.linear_case(1024, 4, 4096, dtype=dtype, T=T, seed=11,
                           device="cuda")
     draft = None if T == 0.0 else c.draft
-    ref = api.verify_linear(c.target, draft, c.tokens, c.uniforms, T,
-                            want_accept=True)
-    for _ in range(2):
-        st = torch.zeros(1, dtype=torch.int32, device="cuda")
-        got = api.verify_linear_static(c.target, draft, c.tokens, c.uniforms,
-                                       T, want_accept=True, status=st)
-        torch.cuda.synchronize()
-        _same(got, ref)
-        assert int(st.item()) == 0
+    with api.tuned(allrows=allrows):
+        ref = api.verify_linear(c.target, draft, c.tokens, c.uniforms, T,
+                                want_accept=True)
+        for _ in range(2):
+            st = torch.zeros(1, dtype=torch.int32, device="cuda")
+            got = api.verify_linear_static(c.target, draft, c.tokens,
+                                           c.uniforms, T, want_accept=True,
+                                           status=st)
+            torch.cuda.synchronize()
+            _same(got, ref)
+            assert int(st.item()) == 0
 
 
 @pytest.mark.gpu
@@ -51,15 +52,21 @@ def test_static_large_workload_sequences():
     _same(api.verify_linear_static(t, d, tok, u, 1.0), ref)
 
 
-def test_static_scratch_limit_rejected_before_any_launch():
-    """A size whose scratch exceeds SD_STATIC_WS_BYTES is refused on the
-    host (null pointers: nothing may be touched)."""
+def test_static_scratch_covers_every_size():
+    """The scratch the verify needs (sd_verify_linear_workspace) stays within
+    SD_STATIC_WS_BYTES at every size up to the library's limits, so the
+    static entry accepts whatever the workspace entry accepts; a call is
+    still validated on the host before anything is launched (null pointers
+    with a bad gamma: refused without touching them)."""
     L = api.lib()
-    B, gamma, V = 65536, 8, 152064
-    need = L.sd_verify_linear_workspace(B, gamma, V, api.SD_BF16)
-    assert need > (1 << 20)
-    rc = L.sd_verify_linear_static(None, None, api.SD_BF16, None, None, B,
-                                   gamma, V, 1.0, None, None, None, None, None,
-                                   None, None)
-    assert rc == api.SD_ERR_UNSUPPORTED
-    assert b"SD_STATIC_WS_BYTES" in L.sd_last_error()
+    for B in (1, 7, 256, 4096, 65536, 1 << 20):
+        for gamma in (0, 1, 8, 64):
+            for V in (1, 1000, 32000, 152064, 1 << 24):
+                for dt in (api.SD_F32, api.SD_BF16):
+                    assert L.sd_verify_linear_workspace(B, gamma, V, dt) <= \
+                        (1 << 20), (B, gamma, V, dt)
+    rc = L.sd_verify_linear_static(None, None, api.SD_BF16, None, None, 4,
+                                   65, 1000, 1.0, None, None, None, None,
+                                   None, None, None)
+    assert rc == api.SD_ERR_INVALID_ARG
+    assert b"gamma" in L.sd_last_error()
