@@ -310,6 +310,7 @@ def gpu_arm(args, rank, world):
         "fanout": {"ms": ms_f, "bytes": fan_bytes,
                    "gbs": fan_bytes / (ms_f / 1e3) / 1e9},
         "gpu_launches": 2 * args.steps,
+        "tuning": {k: api.tune_get(k) for k in api.TUNE},
         "clocks": clk,
         "wall_s": wall,
     }
@@ -1015,6 +1016,10 @@ def main():
     ap.add_argument("--aux-steps", type=int, default=30,
                     help="timed rounds of each of the other workloads "
                          "(0: skip them)")
+    ap.add_argument("--tune", action="append", default=[],
+                    metavar="NAME=VALUE",
+                    help="set a library tuning switch (sd_tune_set) before "
+                         "timing, e.g. --tune l2_keep=1 (A/B measurements)")
     ap.add_argument("--oracle-seqs", type=int, default=256,
                     help="sequences of one round the CPU oracle times "
                          "(0: skip the CPU baseline)")
@@ -1028,6 +1033,11 @@ def main():
         if rank == 0:
             print(json.dumps(reference_arm(args)))
         return
+    if args.tune:
+        from speculative_decoding_verification_temperature_gb300 import api
+        for kv in args.tune:
+            k, v = kv.split("=")
+            api.tune_set(k, int(v))
     if args.only:  # one other workload alone (for profiler runs)
         dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
         torch.cuda.set_device(dev)
