@@ -832,7 +832,8 @@ def oracle_check(kind, c, g, T, extra):
     t = synth.host_logits(c.target)
     d = None if (T == 0 and kind in ("linear", "filtered", "kcand_trie")) \
         else synth.host_logits(c.draft)
-    tk, u = c.tokens.cpu().numpy(), c.uniforms.cpu().numpy()
+    u = c.uniforms.cpu().numpy()
+    tk = c.tokens.cpu().numpy() if hasattr(c, "tokens") else None
     nseq = t.shape[0]
     if kind == "linear":
         gm = t.shape[1] - 1
@@ -1019,7 +1020,7 @@ def main():
     ap.add_argument("--tune", action="append", default=[],
                     metavar="NAME=VALUE",
                     help="set a library tuning switch (sd_tune_set) before "
-                         "timing, e.g. --tune l2_keep=1 (A/B measurements)")
+                         "timing, e.g. --tune cluster=4 (A/B measurements)")
     ap.add_argument("--oracle-seqs", type=int, default=256,
                     help="sequences of one round the CPU oracle times "
                          "(0: skip the CPU baseline)")

@@ -56,7 +56,6 @@ struct LinearParams {
   int seg_bytes;   // bytes of the segment-mass array (multiple of 128)
   int slice_vecs;  // capacity of each slice buffer in 16-byte vectors (TMA)
   int spec;        // let a cluster's last sequence read ahead (0: never)
-  int l2keep;      // sampled, TMA: rows read evict_last until not needed
 };
 
 constexpr int kMaxW = 4;  // positions per step when a cluster speculates
@@ -117,18 +116,6 @@ __global__ void __launch_bounds__(kThreads, RING ? 4 : 2)
   };
   auto drow_of = [&](int s, int j) {
     return dbase + ((size_t)s * p.d_seq_rows + j) * rowb;
-  };
-  // L2 priorities: a step's rows are read with evict_last, so they stay in
-  // L2 ahead of other clusters' lines until the step is decided; then they
-  // go back to the normal priority, except the deciding position's rows,
-  // which the draw reads again (demoted after it)
-  const bool l2keep = RING && !GREEDY && p.l2keep;
-  if (l2keep) rg.policy = l2_evict_last_policy();
-  auto demote = [&](int s, int j) {
-    const size_t off = (size_t)sl.vbeg * 16;
-    const size_t len = (size_t)(sl.vend - sl.vbeg) * 16;
-    l2_demote(trow_of(s, j) + off, len);
-    if (j < gamma) l2_demote(drow_of(s, j) + off, len);
   };
 
   int par = 0, seqpar = 0;
@@ -261,11 +248,6 @@ __global__ void __launch_bounds__(kThreads, RING ? 4 : 2)
       }
       __syncthreads();
       R = sh.res;
-      if (l2keep) {  // rows of this step that no draw will read again
-        const int keep = (R.kind == 1 || R.kind == 2) ? R.n : -1;
-        for (int j = i; j < jend; ++j)
-          if (j != keep) demote(seq, j);
-      }
       if (R.kind) break;
       i = jend;
       if (first) {  // after the first step: is this the cluster's last?
@@ -362,7 +344,6 @@ __global__ void __launch_bounds__(kThreads, RING ? 4 : 2)
       if (p.out_resid)
         write_resid<DT, VW>(p.out_resid + (size_t)seq * V, ra, rb, has_q, W,
                             sl, o.N);
-      if (l2keep) demote(seq, n);  // the draw has read them again
     }
     // next sequence (rank 0 published it before this sequence's first sync)
     seq = cluster.map_shared_rank(&sh, 0)->next_seq[seqpar];
@@ -465,7 +446,6 @@ sd_status linear_launch(const void *target, const void *draft, sd_dtype dt,
   prm.seg_bytes = (int)seg_bytes;
   prm.slice_vecs = (int)per_cta;
   prm.spec = tune(SD_TUNE_SPEC);
-  prm.l2keep = (ring && !greedy) ? tune(SD_TUNE_L2_KEEP) : 0;
   if (B > nclusters) {
     if (!ws || ws_bytes < 256)
       return fail(SD_ERR_INVALID_ARG, "workspace of >= 256 bytes required");

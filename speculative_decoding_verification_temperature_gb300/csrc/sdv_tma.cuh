@@ -68,27 +68,6 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   return pol;
 }
 
-// An L2 policy that keeps the lines it loads ahead of other lines: for
-// data a later pass reads again; l2_demote puts them back to normal.
-__device__ __forceinline__ uint64_t l2_evict_last_policy() {
-  uint64_t pol;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;"
-               : "=l"(pol));
-  return pol;
-}
-
-// Every thread of the CTA: the 128-byte lines over [p, p + bytes) back to
-// the normal L2 eviction priority (the line holding p and every line that
-// starts inside the range).
-__device__ __forceinline__ void l2_demote(const void *p, size_t bytes) {
-  const uintptr_t a0 = (uintptr_t)p & ~(uintptr_t)127;
-  const uintptr_t a1 = (uintptr_t)p + bytes;
-  for (uintptr_t a = a0 + (uintptr_t)threadIdx.x * 128; a < a1;
-       a += (uintptr_t)blockDim.x * 128)
-    asm volatile("applypriority.global.L2::evict_normal [%0], 128;" ::"l"(a)
-                 : "memory");
-}
-
 // bulk_g2s with an L2 cache policy for the lines it reads.
 __device__ __forceinline__ void bulk_g2s_hint(void *dst, const void *src,
                                               uint32_t bytes, uint64_t *bar,

@@ -191,7 +191,6 @@ def test_tuning_switches_set_get_and_validate():
                 "fanout_ldg": 0, "fanout_maxc": 0, "fanout_l2_first": 1}
     for k, v in defaults.items():
         assert api.tune_get(k) == v, k
-    assert api.tune_get("l2_keep") in (0, 1)
     with api.tuned(cluster=4, allrows=2):
         assert api.tune_get("cluster") == 4 and api.tune_get("allrows") == 2
     assert api.tune_get("cluster") == 0 and api.tune_get("allrows") == 1

@@ -1,8 +1,8 @@
 """Both paths of sd_verify_linear against the oracle on the same inputs:
 the per-position cluster kernel (SD_TUNE_ALLROWS 0) and the all-rows path
 for small inputs (SD_TUNE_ALLROWS 2 forces it wherever its workspace and
-shared memory allow), plus the cluster kernel with its rows held in L2 by
-evict_last until the draw (SD_TUNE_L2_KEEP 1) and without.  Small and odd
+shared memory allow), plus the cluster kernel without its read-ahead of a
+cluster's last sequence (SD_TUNE_SPEC 0) and with L2 prefetch (2).  Small and odd
 sizes, both dtypes, unaligned rows, gamma 0, T in {0, 0.7, 1}, bad tokens
 and non-finite rows, the queue path, the accept-probability output; and
 the two paths agree with each other."""
@@ -24,11 +24,13 @@ def run(case, **kw):
 
 
 def switches(mode):
-    return {"allrows": int(mode.split("-")[0]),
-            "l2_keep": int(mode.endswith("keep"))}
+    sw = {"allrows": int(mode.split("-")[0])}
+    if "-spec" in mode:
+        sw["spec"] = int(mode[-1])
+    return sw
 
 
-@pytest.mark.parametrize("mode", ["0", "2", "0-keep"])
+@pytest.mark.parametrize("mode", ["0", "2", "0-spec0", "0-spec2"])
 @pytest.mark.parametrize("T", [0.0, 0.7, 1.0])
 @pytest.mark.parametrize("B,gamma,V,dtype", [
     (1, 4, 1000, torch.float32), (32, 8, 32000, torch.bfloat16),
@@ -49,7 +51,7 @@ def test_paths_against_oracle(mode, T, B, gamma, V, dtype):
         assert np.all(host(g["accept"])[~ev] == -1)
 
 
-@pytest.mark.parametrize("mode", ["0", "2", "0-keep"])
+@pytest.mark.parametrize("mode", ["0", "2", "0-spec0", "0-spec2"])
 def test_paths_edge_rows(mode):
     c = synth.linear_case(8, 4, 2000, torch.float32, 1.0, seed=77)
     c.tokens[1, 0] = 10**6            # bad token, tested first
@@ -69,7 +71,7 @@ def test_paths_agree():
     """Away from the flagged draws the two paths return the same tokens."""
     c = to_device(synth.linear(1.0))
     outs = []
-    for mode in ("0", "2", "0-keep"):
+    for mode in ("0", "2", "0-spec0", "0-spec2"):
         with api.tuned(**switches(mode)):
             outs.append(run(c))
     o = linear_oracle(c)
