@@ -610,23 +610,27 @@ def _fork(args, dev, entry, steps):
 
 
 def _filtered(args, dev, entry, steps):
-    """Filtered sampling (top_k = 50, top_p = 0.9) on the large workload's
-    shape: B=256, gamma=8, V=128256 fp32, T=1."""
+    """Filtered sampling on the large workload's shape: B=256, gamma=8,
+    V=128256 fp32, T=1: top_k = 50 with top_p = 0.9 (exact top-k lists),
+    top_p = 0.9 alone and top_k = 1000 alone (the threshold select)."""
     from speculative_decoding_verification_temperature_gb300 import api
     sets = []
     for r in range(min(2, args.sets)):
         c = synth.large(r, device=dev, B=B)
         c.draft = c.draft[:, :GAMMA].contiguous()
         sets.append(c)
-    fn = lambda c: api.verify_linear_filtered(c.target, c.draft, c.tokens,
-                                              c.uniforms, 1.0, 50, 0.9)
-    ms = _time(fn, sets, steps, 3, dev)
-    rows = np.mean([_rows_linear(fn(c)["n"].cpu().numpy(), GAMMA, False)
-                    for c in sets])
-    entry("filtered_k50_p0.9", ms, rows, V, ELT, B * (2 * GAMMA + 1),
-          {"top_k": 50, "top_p": 0.9, "T": 1.0})
-    _register(args, "filtered_k50_p0.9", "filtered", sets[0], fn(sets[0]),
-              1.0, top_k=50, top_p=0.9)
+    for name, top_k, top_p in (("filtered_k50_p0.9", 50, 0.9),
+                               ("filtered_p0.9", V, 0.9),
+                               ("filtered_k1000", 1000, 1.0)):
+        fn = (lambda c, k=top_k, pp=top_p: api.verify_linear_filtered(
+            c.target, c.draft, c.tokens, c.uniforms, 1.0, k, pp))
+        ms = _time(fn, sets, steps, 3, dev)
+        rows = np.mean([_rows_linear(fn(c)["n"].cpu().numpy(), GAMMA, False)
+                        for c in sets])
+        entry(name, ms, rows, V, ELT, B * (2 * GAMMA + 1),
+              {"top_k": top_k, "top_p": top_p, "T": 1.0})
+        _register(args, name, "filtered", sets[0], fn(sets[0]), 1.0,
+                  top_k=top_k, top_p=top_p)
     del sets
 
 

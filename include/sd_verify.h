@@ -201,16 +201,25 @@ sd_status sd_verify_linear_static(
  *
  * Arguments and outputs as sd_verify_linear (no out_accept_prob /
  * out_resid), plus:
- *   top_k in [1, min(V, SD_MAX_FANOUT)]: keep the top_k tokens by (logit
- *       desc, id asc);
+ *   top_k >= 1: keep the top_k tokens by (logit desc, id asc); top_k >= V
+ *       keeps every token;
  *   top_p in (0, 1]: then keep the smallest prefix of them, in that order,
- *       whose mass renormalised over the top_k reaches top_p (1: all).
+ *       whose mass renormalised over the top_k reaches top_p (a token stays
+ *       iff the mass before it is below top_p; 1: all).
+ *   out_keep [B, 2 gamma + 1] int32 (nullable, debug): the number of
+ *       tokens each row read kept (slot i: target row i, slot gamma + 1 + i:
+ *       draft row i; -1 for rows not read, or every slot of an unusable
+ *       sequence).
  * p~ and q~ are softmax(z / T) restricted to the kept tokens and
  * renormalised; x_i is accepted iff r_i <= p~_i(x_i) / q~_i(x_i); the
  * correction is drawn from norm(max(0, p~_n - q~_n)), the bonus from
  * p~_gamma.  T == 0 is greedy (the filters keep the argmax), as in
  * sd_verify_linear.  Rows must be 16-byte aligned (V * elt a multiple of
  * 16), else SD_ERR_UNSUPPORTED.  Each row the method needs is read once.
+ * With top_k <= SD_MAX_FANOUT the rows' exact top-k lists are kept in
+ * registers; above it (or with top_k >= V) a cluster holds each row pair
+ * in shared memory and selects the cut by histogram: V * elt may then be
+ * at most about 1.6 MB (SD_ERR_UNSUPPORTED beyond).
  * ------------------------------------------------------------------- */
 size_t sd_verify_linear_filtered_workspace(int B, int gamma, int V,
                                            sd_dtype dt);
@@ -219,8 +228,8 @@ sd_status sd_verify_linear_filtered(
     const void *target_logits, const void *draft_logits, sd_dtype dt,
     const int32_t *draft_tokens, const float *uniforms, int B, int gamma,
     int V, float T, int top_k, float top_p, int32_t *n_accepted,
-    int32_t *out_tokens, float *out_prob, int32_t *dev_status,
-    void *workspace, size_t ws_bytes, void *stream);
+    int32_t *out_tokens, float *out_prob, int32_t *out_keep,
+    int32_t *dev_status, void *workspace, size_t ws_bytes, void *stream);
 
 /* ---------------------------------------------------------------------
  * K-candidate verify with verifier self-selection (SpecDiff-2, "core

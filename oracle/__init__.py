@@ -63,7 +63,7 @@ def _bind(path):
     lib.orc_fanout_hits.argtypes = [P, P, P, P, I, I, P]
     lib.orc_verify_linear_filtered.argtypes = [P, P, I, P, P, I, I, I, D, I,
                                                D, P, P, P, P, P, P, P, P, P,
-                                               P]
+                                               P, P, P, P, P]
     for f in (lib.orc_verify_linear, lib.orc_verify_kcand,
               lib.orc_verify_tree, lib.orc_fanout_schedule,
               lib.orc_fanout_topk):
@@ -180,11 +180,18 @@ def verify_linear(target, draft, tokens, uniforms, T, want_resid=False):
 
 
 def verify_linear_filtered(target, draft, tokens, uniforms, T, top_k,
-                           top_p=1.0):
+                           top_p=1.0, keep_forced=None, want_keep=False):
     """Linear verify with top_k / top_p filtered sampling applied to p and q
-    before the ratio (same shapes as verify_linear).  Returns n, tokens,
-    prob, the margins (margin_acc also covers the nucleus cuts) and status.
-    """
+    before the ratio (same shapes as verify_linear; top_k >= V keeps every
+    token).  Returns n, tokens, prob, the margins and status.
+
+    want_keep: also return keep, keep_lo, keep_hi [B, 2 gamma + 1] (slot i
+    for target row i, gamma + 1 + i for draft row i; -1 for rows not read):
+    the kept count of each row and the range of counts whose nucleus cut
+    lies within FLAG_MARGIN of top_p; margin_acc then covers the accept
+    tests only.  Otherwise margin_acc also covers the nucleus cuts.
+    keep_forced [B, 2 gamma + 1] (entries >= 1): keep that many tokens of
+    the row (at most top_k) instead of the nucleus's count."""
     target, dt = _logits(target)
     B, G1, V = target.shape
     gamma = G1 - 1
@@ -199,20 +206,28 @@ def verify_linear_filtered(target, draft, tokens, uniforms, T, top_k,
         draft_p = _ptr(draft)
     tokens = np.ascontiguousarray(tokens, dtype=np.int32).reshape(B, gamma)
     uniforms = np.ascontiguousarray(uniforms, dtype=np.float32).reshape(B, G1)
+    NS = 2 * gamma + 1
     out = {
         "n": np.empty(B, np.int32),
         "tokens": np.empty((B, G1), np.int32),
         "prob": np.empty(B, np.float64),
         "status": np.empty(B, np.int32),
     }
+    kf = None if keep_forced is None else np.ascontiguousarray(
+        keep_forced, np.int32).reshape(B, NS)
+    kp = {k: np.empty((B, NS), np.int32) for k in ("keep", "keep_lo",
+                                                   "keep_hi")} \
+        if want_keep else {}
     m = _margins(B)
     rc = _load().orc_verify_linear_filtered(
         _ptr(target), draft_p, dt, _ptr(tokens), _ptr(uniforms), B, gamma, V,
         float(T), int(top_k), float(top_p), _ptr(out["n"]),
-        _ptr(out["tokens"]), _ptr(out["prob"]), *_margin_ptrs(m),
-        _ptr(out["status"]))
+        _ptr(out["tokens"]), _ptr(out["prob"]), *_margin_ptrs(m), _ptr(kf),
+        _ptr(kp.get("keep")), _ptr(kp.get("keep_lo")),
+        _ptr(kp.get("keep_hi")), _ptr(out["status"]))
     if rc:
         raise MemoryError("oracle allocation failed")
+    out.update(kp)
     return _finish(out, m)
 
 

@@ -164,6 +164,7 @@ static int argmax_row(const void *base, int dtype, size_t off, int V) {
  * whose interval [C_{j-1}/N, C_j/N] comes within ORC_BAND of u: the tokens a
  * correct finite-precision draw may return. */
 #define ORC_BAND 1e-5
+#define SD_ORC_MAX_GAMMA 64 /* longest draft the filtered verify takes */
 static int sample_icdf(const double *w, int V, double u, double *prob,
                        double *margin, int *lo, int *hi) {
   double N = 0.0;
@@ -743,10 +744,17 @@ int orc_fanout_hits(const int32_t *n_acc, const int32_t *tokens,
  * mass before it is below top_p); renormalise over the kept tokens.  p gets
  * the filtered distribution (0 outside the kept set).  *margin is lowered to
  * the distance of every prefix mass from top_p (where an fp32 computation
- * may cut the nucleus differently).  Returns 0 on an unusable row. */
+ * may cut the nucleus differently).  The kept count is written to *keep;
+ * *keep_lo / *keep_hi (nullable) get the range of kept counts whose cut
+ * lies within ORC_BAND of top_p (the counts an fp32 computation may reach:
+ * a token whose renormalised prefix mass is below top_p - ORC_BAND stays in
+ * every such count, one at or above top_p + ORC_BAND in none).  When
+ * forced >= 1 the nucleus keeps that many tokens instead (at most top_k).
+ * Returns 0 on an unusable row. */
 static int filtered_row(const void *base, int dtype, size_t off, int V,
                         double T, int top_k, double top_p, double *p,
-                        orc_entry *e, double *margin) {
+                        orc_entry *e, double *margin, int forced, int *keep_out,
+                        int *keep_lo, int *keep_hi) {
   if (!softmax_row(base, dtype, off, V, T, p)) return 0;
   for (int j = 0; j < V; ++j) {
     double z = logit_at(base, dtype, off + (size_t)j);
@@ -757,17 +765,23 @@ static int filtered_row(const void *base, int dtype, size_t off, int V,
   int k = top_k < V ? top_k : V;
   double mk = 0.0;
   for (int i = 0; i < k; ++i) mk += p[e[i].idx];
-  int keep = k;
+  int keep = k, lo = k, hi = k;
   if (top_p < 1.0) {
     double before = 0.0;
-    keep = 0;
+    keep = lo = hi = 0;
     for (int i = 0; i < k; ++i) {
       double f = before / mk;
       note_margin(margin, fabs(f - top_p));
       if (f < top_p) keep = i + 1;
+      if (f < top_p - ORC_BAND) lo = i + 1;
+      if (f < top_p + ORC_BAND) hi = i + 1;
       before += p[e[i].idx];
     }
   }
+  if (forced >= 1) keep = forced < k ? forced : k;
+  *keep_out = keep;
+  if (keep_lo) *keep_lo = lo;
+  if (keep_hi) *keep_hi = hi;
   double S = 0.0;
   for (int i = 0; i < keep; ++i) S += p[e[i].idx];
   double *kept = malloc(sizeof(double) * (size_t)keep);
@@ -794,7 +808,10 @@ int orc_verify_linear_filtered(const void *target, const void *draft,
                                double *out_prob, double *margin_acc,
                                double *margin_cdf, int32_t *cdf_lo,
                                int32_t *cdf_hi, int32_t *acc_tests,
-                               int32_t *acc_flagged, int32_t *status) {
+                               int32_t *acc_flagged, const int32_t *keep_forced,
+                               int32_t *keep, int32_t *keep_lo,
+                               int32_t *keep_hi, int32_t *status) {
+  if (gamma > SD_ORC_MAX_GAMMA) return 1;
   if (T == 0.0) {
     double *acc = malloc(sizeof(double) * (size_t)(B * (gamma > 0 ? gamma : 1)));
     if (!acc) return 1;
@@ -803,6 +820,15 @@ int orc_verify_linear_filtered(const void *target, const void *draft,
                                margin_acc, margin_cdf, cdf_lo, cdf_hi,
                                acc_tests, acc_flagged, NULL, status);
     free(acc);
+    /* greedy: the filters keep the argmax; target rows 0..n are read (one
+     * token kept each), draft rows are not */
+    for (int b = 0; b < B && (keep || keep_lo || keep_hi); ++b)
+      for (int i = 0; i < 2 * gamma + 1; ++i) {
+        const int32_t v = (n_acc[b] >= 0 && i <= n_acc[b]) ? 1 : -1;
+        if (keep) keep[(size_t)b * (2 * gamma + 1) + i] = v;
+        if (keep_lo) keep_lo[(size_t)b * (2 * gamma + 1) + i] = v;
+        if (keep_hi) keep_hi[(size_t)b * (2 * gamma + 1) + i] = v;
+      }
     return rc;
   }
   double *p = malloc(sizeof(double) * (size_t)V);
@@ -810,16 +836,23 @@ int orc_verify_linear_filtered(const void *target, const void *draft,
   double *w = malloc(sizeof(double) * (size_t)V);
   orc_entry *e = malloc(sizeof(orc_entry) * (size_t)V);
   if (!p || !q || !w || !e) { free(p); free(q); free(w); free(e); return 1; }
-  const int G1 = gamma + 1;
+  const int G1 = gamma + 1, NS = 2 * gamma + 1;
   for (int b = 0; b < B; ++b) {
     int st = 0, n = 0, t = -1, invalid = 0, lo = -1, hi = -1, rejected = 0;
     int nt = 0, nf = 0;
-    double mg = INFINITY, mc = INFINITY, prob = 0.0;
+    double mg = INFINITY, mc = INFINITY, mn = INFINITY, prob = 0.0;
+    /* per-row kept counts: slot i for target row i, gamma + 1 + i for draft
+     * row i; -1 for rows not read */
+    int32_t kk[2 * SD_ORC_MAX_GAMMA + 1], klo[2 * SD_ORC_MAX_GAMMA + 1],
+        khi[2 * SD_ORC_MAX_GAMMA + 1];
+    for (int i = 0; i < NS; ++i) kk[i] = klo[i] = khi[i] = -1;
+    const int32_t *fk = keep_forced ? keep_forced + (size_t)b * NS : NULL;
+#define FROW(base, off, slot, dst)                                         \
+  filtered_row(base, dtype, off, V, T, top_k, top_p, dst, e, &mn,          \
+               fk ? fk[slot] : -1, &kk[slot], &klo[slot], &khi[slot])
     for (int i = 0; i < gamma; ++i) {
-      if (!filtered_row(target, dtype, ((size_t)b * G1 + i) * V, V, T, top_k,
-                        top_p, p, e, &mg) ||
-          !filtered_row(draft, dtype, ((size_t)b * gamma + i) * V, V, T,
-                        top_k, top_p, q, e, &mg)) {
+      if (!FROW(target, ((size_t)b * G1 + i) * V, i, p) ||
+          !FROW(draft, ((size_t)b * gamma + i) * V, G1 + i, q)) {
         invalid = 1;
         break;
       }
@@ -849,8 +882,7 @@ int orc_verify_linear_filtered(const void *target, const void *draft,
           st |= ORC_ST_ZERO_MASS;
           for (int j = 0; j < V; ++j) w[j] = p[j];
         }
-      } else if (!filtered_row(target, dtype, ((size_t)b * G1 + gamma) * V, V,
-                               T, top_k, top_p, p, e, &mg)) {
+      } else if (!FROW(target, ((size_t)b * G1 + gamma) * V, gamma, p)) {
         invalid = 1;
       } else {
         for (int j = 0; j < V; ++j) w[j] = p[j];
@@ -875,12 +907,20 @@ int orc_verify_linear_filtered(const void *target, const void *draft,
       }
       out_tokens[(size_t)b * G1 + i] = v;
     }
+#undef FROW
     out_prob[b] = prob;
-    margin_acc[b] = mg;
+    /* the nucleus cuts count as flagged decisions unless the caller takes
+     * their admissible ranges instead */
+    margin_acc[b] = (keep_lo || mn > mg) ? mg : mn;
     margin_cdf[b] = mc;
     cdf_lo[b] = lo;
     cdf_hi[b] = hi;
     put_tests(acc_tests, acc_flagged, b, invalid, nt, nf);
+    for (int i = 0; i < NS; ++i) {
+      if (keep) keep[(size_t)b * NS + i] = invalid ? -1 : kk[i];
+      if (keep_lo) keep_lo[(size_t)b * NS + i] = invalid ? -1 : klo[i];
+      if (keep_hi) keep_hi[(size_t)b * NS + i] = invalid ? -1 : khi[i];
+    }
     status[b] = st;
   }
   free(p); free(q); free(w); free(e);

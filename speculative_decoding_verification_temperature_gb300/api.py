@@ -82,7 +82,7 @@ def _declare(L):
         "sd_fanout_hits": ([P, P, P, I, I, P, P, P], I),
         "sd_verify_linear_filtered_workspace": ([I, I, I, I], Z),
         "sd_verify_linear_filtered": ([P, P, I, P, P, I, I, I, F, I, F, P, P,
-                                       P, P, P, Z, P], I),
+                                       P, P, P, P, Z, P], I),
         "sd_verify_linear_fanout_workspace": ([I, I, I, I], Z),
         "sd_verify_linear_fanout": ([P, P, I, P, P, I, I, I, F, P, P, P, P,
                                      P, P, P, P, Z, P], I),
@@ -271,10 +271,13 @@ def verify_linear_static(target, draft, tokens, uniforms, T, *,
 
 
 def verify_linear_filtered(target, draft, tokens, uniforms, T, top_k,
-                           top_p=1.0, *, status=None, workspace=None):
+                           top_p=1.0, *, want_keep=False, status=None,
+                           workspace=None):
     """Linear verify with top_k / top_p filtered sampling applied to p and q
     before the ratio (sd_verify_linear_filtered); same shapes as
-    verify_linear.  Returns n, tokens, prob."""
+    verify_linear; top_k >= V keeps every token.  Returns n, tokens, prob
+    (and keep [B, 2 gamma + 1]: the kept count of each row read, -1 for the
+    rest, when want_keep)."""
     dev = target.device
     _dev(target, dev, "target")
     B, G1, V = target.shape
@@ -288,14 +291,19 @@ def verify_linear_filtered(target, draft, tokens, uniforms, T, top_k,
     n = torch.empty(B, dtype=torch.int32, device=dev)
     toks = torch.empty((B, G1), dtype=torch.int32, device=dev)
     prob = torch.empty(B, dtype=torch.float32, device=dev)
+    keep = torch.empty((B, 2 * gamma + 1), dtype=torch.int32,
+                       device=dev) if want_keep else None
     L = lib()
     nbytes = L.sd_verify_linear_filtered_workspace(B, gamma, V, _dt(target))
     ws = (workspace or _default_ws).get(dev, nbytes)
     _check(L.sd_verify_linear_filtered(
         _p(target), _p(draft), _dt(target), _p(tokens), _p(uniforms), B,
         gamma, V, float(T), int(top_k), float(top_p), _p(n), _p(toks),
-        _p(prob), _p(status), _p(ws), ws.numel(), _stream(dev)))
-    return {"n": n, "tokens": toks, "prob": prob}
+        _p(prob), _p(keep), _p(status), _p(ws), ws.numel(), _stream(dev)))
+    r = {"n": n, "tokens": toks, "prob": prob}
+    if want_keep:
+        r["keep"] = keep
+    return r
 
 
 def verify_kcand(target, draft, tokens, uniforms, T, *, status=None,

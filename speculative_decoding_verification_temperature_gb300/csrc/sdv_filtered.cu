@@ -38,6 +38,7 @@ struct FiltParams {
   float top_p;  // (0, 1]
   int32_t *n_acc, *out_tokens;
   float *out_prob;
+  int32_t *out_keep;  // [B, 2 gamma + 1] nullable: kept count per row read
   int32_t *dev_status;
   int *queue;
   int nclusters;
@@ -215,6 +216,12 @@ __device__ __forceinline__ FRow filtered_row(const uint64_t *keys, int k,
   for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
   r.Z = z;
   return r;
+}
+
+// Kept tokens of a filtered row (warp-uniform).
+__device__ __forceinline__ int fkept(const FRow &r) {
+  return __popc(__ballot_sync(0xffffffffu, r.j0 >= 0)) +
+         __popc(__ballot_sync(0xffffffffu, r.j1 >= 0));
 }
 
 // Filtered probability of token x in a row (warp-uniform; 0 if not kept).
@@ -399,6 +406,11 @@ __global__ void __launch_bounds__(kThreads, 4)
         } else {
           const FRow fq = filtered_row(sh.rk[0], K, k2, p.top_p);
           const FRow fp = filtered_row(sh.rk[1], K, k2, p.top_p);
+          const int kq = fkept(fq), kp = fkept(fp);
+          if (p.out_keep && rank == 0 && lane == 0) {
+            p.out_keep[(size_t)b * (2 * gamma + 1) + j] = kp;
+            p.out_keep[(size_t)b * (2 * gamma + 1) + G1 + j] = kq;
+          }
           const float px = bad ? 0.f : fprob(fp, x);
           const float qx = bad ? 0.f : fprob(fq, x);
           const float r = sh.gr;
@@ -457,6 +469,9 @@ __global__ void __launch_bounds__(kThreads, 4)
           kd = 3;
         } else {
           const FRow fp = filtered_row(sh.rk[1], K, k2, p.top_p);
+          const int kp = fkept(fp);
+          if (p.out_keep && rank == 0 && lane == 0)
+            p.out_keep[(size_t)b * (2 * gamma + 1) + gamma] = kp;
           fdraw(sh, fp.e0, fp.j0, fp.e1, fp.j1,
                 p.uniforms[(size_t)b * G1 + gamma]);
           if (lane == 0) sh.zero_mass = 0;
@@ -467,6 +482,16 @@ __global__ void __launch_bounds__(kThreads, 4)
       kind = sh.kind;
     }
     bad_token = __syncthreads_or(bad_token);
+    if (rank == 0 && p.out_keep) {  // rows not read (or unusable): -1
+      __syncthreads();
+      const int NS = 2 * gamma + 1;
+      for (int t = tid; t < NS; t += kThreads) {
+        const bool tr = t <= gamma;
+        const int jj = tr ? t : t - G1;
+        const bool read = kind != 3 && (tr ? jj <= n : jj <= n && jj < gamma);
+        if (!read) p.out_keep[(size_t)b * NS + t] = -1;
+      }
+    }
     if (rank == 0 && warp == 0) {  // outputs
       const bool unusable = kind == 3;
       for (int t = lane; t <= gamma; t += 32) {
@@ -512,6 +537,16 @@ sd_status linear_launch(const void *target, const void *draft, sd_dtype dt,
                         int32_t *dev_status, void *ws, size_t ws_bytes,
                         cudaStream_t stream);
 
+sd_status filtered_any_launch(const void *target, const void *draft,
+                              sd_dtype dt, const int32_t *tokens,
+                              const float *uniforms, int B, int gamma, int V,
+                              float T, int top_k, float top_p, int32_t *n_acc,
+                              int32_t *out_tokens, float *out_prob,
+                              int32_t *out_keep, int32_t *dev_status,
+                              void *ws, size_t ws_bytes, cudaStream_t s);
+sd_status greedy_keep(const int32_t *n_acc, int B, int gamma,
+                      int32_t *out_keep, cudaStream_t s);
+
 }  // namespace sdv
 
 extern "C" size_t sd_verify_linear_filtered_workspace(int B, int gamma,
@@ -523,8 +558,8 @@ extern "C" sd_status sd_verify_linear_filtered(
     const void *target_logits, const void *draft_logits, sd_dtype dt,
     const int32_t *draft_tokens, const float *uniforms, int B, int gamma,
     int V, float T, int top_k, float top_p, int32_t *n_accepted,
-    int32_t *out_tokens, float *out_prob, int32_t *dev_status,
-    void *workspace, size_t ws_bytes, void *stream) {
+    int32_t *out_tokens, float *out_prob, int32_t *out_keep,
+    int32_t *dev_status, void *workspace, size_t ws_bytes, void *stream) {
   using namespace sdv;
   SDV_REQUIRE(dt == SD_F32 || dt == SD_BF16, "bad dtype %d", (int)dt);
   SDV_REQUIRE(B >= 0, "B < 0");
@@ -533,16 +568,18 @@ extern "C" sd_status sd_verify_linear_filtered(
   SDV_REQUIRE(V >= 1 && V <= SD_MAX_V, "V=%d outside [1, %d]", V, SD_MAX_V);
   SDV_REQUIRE(T >= 0.f && std::isfinite(T), "T must be finite and >= 0");
   SDV_REQUIRE(top_p > 0.f && top_p <= 1.f, "top_p outside (0, 1]");
-  if (top_k < 1 || top_k > SD_MAX_FANOUT || top_k > V)
-    return fail(SD_ERR_UNSUPPORTED, "top_k=%d outside [1, min(V, %d)]", top_k,
-                SD_MAX_FANOUT);
+  SDV_REQUIRE(top_k >= 1, "top_k=%d < 1", top_k);
+  if (top_k > V) top_k = V;  // no top-k cut
   if (B == 0) return SD_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (T == 0.f)  // greedy: the filters keep the argmax
-    return linear_launch(target_logits, draft_logits, dt, gamma, draft_tokens,
-                         uniforms, B, gamma, V, T, n_accepted, out_tokens,
-                         out_prob, nullptr, nullptr, dev_status, workspace,
-                         ws_bytes, s);
+  if (T == 0.f) {  // greedy: the filters keep the argmax
+    sd_status g = linear_launch(target_logits, draft_logits, dt, gamma,
+                                draft_tokens, uniforms, B, gamma, V, T,
+                                n_accepted, out_tokens, out_prob, nullptr,
+                                nullptr, dev_status, workspace, ws_bytes, s);
+    if (g != SD_OK || !out_keep) return g;
+    return greedy_keep(n_accepted, B, gamma, out_keep, s);
+  }
   SDV_REQUIRE(target_logits && n_accepted && out_tokens && uniforms,
               "null pointer");
   SDV_REQUIRE(gamma == 0 || (draft_tokens && draft_logits),
@@ -558,6 +595,13 @@ extern "C" sd_status sd_verify_linear_filtered(
     return fail(SD_ERR_UNSUPPORTED,
                 "filtered verify needs 16-byte aligned rows (V * %d bytes)",
                 eb);
+  // top_k above the exact-list limit, or no top-k cut: the general kernel
+  // (a threshold select on shared-memory resident rows)
+  if (top_k > SD_MAX_FANOUT)
+    return filtered_any_launch(target_logits, draft_logits, dt, draft_tokens,
+                               uniforms, B, gamma, V, T, top_k, top_p,
+                               n_accepted, out_tokens, out_prob, out_keep,
+                               dev_status, workspace, ws_bytes, s);
   const long long nvec = V / vw;
   FiltKernel kern = dt == SD_F32 ? filtered_verify_kernel<0, 4>
                                  : filtered_verify_kernel<1, 8>;
@@ -600,6 +644,7 @@ extern "C" sd_status sd_verify_linear_filtered(
   prm.n_acc = n_accepted;
   prm.out_tokens = out_tokens;
   prm.out_prob = out_prob;
+  prm.out_keep = out_keep;
   prm.dev_status = dev_status;
   prm.queue = static_cast<int *>(workspace);
   prm.nclusters = B < maxc ? B : maxc;

@@ -89,10 +89,11 @@ def test_linear_entries(guard, V, dtype, gamma, T):
 def test_filtered(guard, gamma):
     c = to_device(synth.linear_case(19, gamma, 4104, torch.float32, 1.0,
                                     seed=3 + gamma, sigma_t=2.0, sigma_d=1.0))
-    api.verify_linear_filtered(c.target, c.draft, c.tokens, c.uniforms, 1.0,
-                               7, 0.9, status=status(),
-                               workspace=api.Workspace())
-    assert guard.check() >= 3
+    for top_k in (7, 1 << 30):
+        api.verify_linear_filtered(c.target, c.draft, c.tokens, c.uniforms,
+                                   1.0, top_k, 0.9, want_keep=True,
+                                   status=status(), workspace=api.Workspace())
+        assert guard.check() >= 4
 
 
 @pytest.mark.parametrize("gamma", [0, 3])

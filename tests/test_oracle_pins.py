@@ -1236,3 +1236,53 @@ def test_accept_test_counts_and_flags_planted():
     assert o2["acc_flagged"].sum() <= len(plant) + 2
     g = oracle.verify_linear(zt, None, x, u, 0.0)
     assert g["acc_tests"].sum() == 0 and g["acc_flagged"].sum() == 0
+
+
+def test_filtered_keep_ranges_and_forced_cuts():
+    """The kept count of each row read, its admissible range (cuts within
+    1e-5 of top_p) and forced counts.  Row p = (1/2, 1/4, 1/4) by hand: with
+    top_p = 0.6 the nucleus keeps 2 tokens, unambiguously; with top_p = 0.75
+    the third token's prefix mass 0.75 sits on the cut, so 2 and 3 are both
+    admissible.  A forced count of 1 leaves the point mass on token 0 (the
+    bonus draw then returns it with probability 1)."""
+    ln2 = math.log(2.0)
+    zt = np.array([[[ln2, 0.0, 0.0]]], np.float32)  # gamma = 0: bonus only
+    tk = np.zeros((1, 0), np.int32)
+    u = np.array([[0.9]], np.float32)
+    o = oracle.verify_linear_filtered(zt, np.zeros((1, 0, 3), np.float32), tk,
+                                      u, 1.0, 3, 0.6, want_keep=True)
+    assert o["keep"].tolist() == [[2]]
+    assert o["keep_lo"].tolist() == [[2]] and o["keep_hi"].tolist() == [[2]]
+    assert o["tokens"][0, 0] == 1  # u = 0.9 over (2/3, 1/3): token 1
+    o = oracle.verify_linear_filtered(zt, np.zeros((1, 0, 3), np.float32), tk,
+                                      u, 1.0, 3, 0.75, want_keep=True)
+    assert o["keep_lo"].tolist() == [[2]] and o["keep_hi"].tolist() == [[3]]
+    o = oracle.verify_linear_filtered(zt, np.zeros((1, 0, 3), np.float32), tk,
+                                      u, 1.0, 3, 0.6, keep_forced=[[1]])
+    assert o["tokens"][0, 0] == 0 and abs(o["prob"][0] - 1.0) < 1e-15
+    # forced counts equal to the computed ones change nothing; rows not read
+    # are -1; lo <= keep <= hi
+    rng = np.random.default_rng(5)
+    B, gamma, V = 60, 3, 400
+    zt = rng.normal(0, 2, (B, gamma + 1, V)).astype(np.float32)
+    zd = (zt[:, :gamma] + rng.normal(0, 1, (B, gamma, V))).astype(np.float32)
+    x = rng.integers(0, 40, (B, gamma)).astype(np.int32)
+    uu = synth.uniforms(6, (B, gamma + 1))
+    for top_k, top_p in ((400, 0.9), (30, 0.95), (5, 1.0)):
+        a = oracle.verify_linear_filtered(zt, zd, x, uu, 1.0, top_k, top_p,
+                                          want_keep=True)
+        b = oracle.verify_linear_filtered(zt, zd, x, uu, 1.0, top_k, top_p,
+                                          keep_forced=a["keep"])
+        for k in ("n", "tokens", "prob"):
+            assert np.array_equal(a[k], b[k]), k
+        rd = a["keep"] >= 0
+        n = a["n"][:, None]
+        slot = np.arange(2 * gamma + 1)[None, :]
+        want = np.where(slot <= gamma, slot <= n,
+                        (slot - gamma - 1 <= n) & (slot - gamma - 1 < gamma))
+        assert np.array_equal(rd, want)
+        assert np.all(a["keep_lo"][rd] <= a["keep"][rd])
+        assert np.all(a["keep"][rd] <= a["keep_hi"][rd])
+        assert np.all(a["keep"][rd] <= min(top_k, V))
+        if top_p == 1.0:
+            assert np.all(a["keep"][rd] == min(top_k, V))
