@@ -25,7 +25,7 @@
 //    at the vocabularies of the pages a bucket holds tens), ranked exactly
 //    by key, and the cut, its count and its mass follow from their prefix.
 //    A larger bucket (ties of a constant row, or a deep top-k cut) is
-//    refined first: histograms of K - K_lo >> shift over the candidates'
+//    refined first: histograms of (K_hi - K) >> shift over the candidates'
 //    key interval, 1024 sub-buckets per level, until it fits.
 //  - Top-k first (the k-th key and the top-k mass M_k), then the nucleus
 //    against top_p M_k restricted to the top-k set; p~ = w / M over the kept
@@ -363,12 +363,12 @@ __global__ void __launch_bounds__(kThreads, 2)
               s.klo = sh.row[r].kk;  // inside the top-k set only
               bc = sh.row[r].lk - s.cnt_before;
             }
-          } else {
-            const uint64_t lo = s.klo + ((uint64_t)bucket << s.shift);
+          } else {  // sub-bucket b holds keys in (khi - (b+1) 2^shift, khi - b 2^shift]
+            const uint64_t hi = s.khi - ((uint64_t)bucket << s.shift);
             const uint64_t span = (s.shift >= 63) ? ~0ull
                                                   : ((1ull << s.shift) - 1);
-            s.klo = lo;
-            s.khi = (s.khi - lo > span) ? lo + span : s.khi;
+            s.khi = hi;
+            s.klo = (hi - s.klo > span) ? hi - span : s.klo;
           }
           s.cand = bc;
           s.gather = bc <= (uint32_t)kFaG || (s.level > 0 && s.shift == 0);
@@ -461,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 2)
               const float z = fa_elt<DT, VW>(sbuf[r], i, e);
               const uint64_t k = elem_key(z, (sl.vbeg + i) * VW + e);
               if (is_cand(s, r, z, k)) {
-                const int b = (int)((k - s.klo) >> s.shift);
+                const int b = (int)((s.khi - k) >> s.shift);  // 0: best
                 atomicAdd(&hc[r * kFaNB + b], 1u);
                 atomicAdd(&hm[r * kFaNB + b], fa_weight(z, k2, mk[r]));
               }
