@@ -629,8 +629,12 @@ def _filtered(args, dev, entry, steps):
                         for c in sets])
         entry(name, ms, rows, V, ELT, B * (2 * GAMMA + 1),
               {"top_k": top_k, "top_p": top_p, "T": 1.0})
-        _register(args, name, "filtered", sets[0], fn(sets[0]), 1.0,
-                  top_k=top_k, top_p=top_p)
+        _register(args, name, "filtered", sets[0],
+                  api.verify_linear_filtered(sets[0].target, sets[0].draft,
+                                             sets[0].tokens,
+                                             sets[0].uniforms, 1.0, top_k,
+                                             top_p, want_keep=True),
+                  1.0, top_k=top_k, top_p=top_p)
     del sets
 
 
@@ -845,10 +849,27 @@ def oracle_check(kind, c, g, T, extra):
             t[a:b], None if d is None else np.ascontiguousarray(
                 d[a:b, :gm]), tk[a:b], u[a:b], T), nseq)
     elif kind == "filtered":
+        # nucleus cuts: the GPU's kept count of every row must lie in the
+        # oracle's admissible range; the rest is compared with those counts
+        # forced on the oracle
         gm = t.shape[1] - 1
-        o = _over_threads(lambda a, b: oracle.verify_linear_filtered(
-            t[a:b], np.ascontiguousarray(d[a:b, :gm]), tk[a:b], u[a:b], T,
-            extra["top_k"], extra["top_p"]), nseq)
+
+        def run(forced):
+            return _over_threads(lambda a, b: oracle.verify_linear_filtered(
+                t[a:b], np.ascontiguousarray(d[a:b, :gm]), tk[a:b], u[a:b],
+                T, extra["top_k"], extra["top_p"], want_keep=True,
+                keep_forced=None if forced is None else forced[a:b]), nseq)
+        o0 = run(None)
+        gk = g["keep"]
+        both = (gk >= 0) & (o0["keep"] >= 0)
+        outside = both & ((gk < o0["keep_lo"]) | (gk > o0["keep_hi"]))
+        o = run(np.where(gk >= 1, gk, -1).astype(np.int32))
+        res = flag_summary(o, g, T)
+        res.update({"rows_cut": int(both.sum()),
+                    "cuts_outside_range": int(outside.sum()),
+                    "cuts_differing_from_oracle": int(
+                        (both & (gk != o0["keep"])).sum())})
+        return res
     elif kind == "kcand":
         o = _over_threads(lambda a, b: oracle.verify_kcand(
             t[a:b], d[a:b], tk[a:b], u[a:b], T), nseq)

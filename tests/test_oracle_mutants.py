@@ -78,6 +78,13 @@ MUTANTS = [
     ("flag_band_too_narrow", "if (m < ORC_BAND) ++*flagged;",
      "if (m < 1e-6) ++*flagged;", 1,
      ["test_accept_test_counts_and_flags_planted"]),
+    ("nucleus_range_band_sign", "if (f < top_p + ORC_BAND) hi = i + 1;",
+     "if (f < top_p - ORC_BAND) hi = i + 1;", 1,
+     ["test_filtered_keep_ranges_and_forced_cuts"]),
+    ("nucleus_forced_count_ignored",
+     "if (forced >= 1) keep = forced < k ? forced : k;",
+     "if (forced >= 1 && 0) keep = forced < k ? forced : k;", 1,
+     ["test_filtered_keep_ranges_and_forced_cuts"]),
     ("nucleus_one_too_many", "if (f < top_p) keep = i + 1;",
      "if (f < top_p) keep = i + 2 < k ? i + 2 : k;", 1,
      ["test_filtered_sampling_golden"]),
