@@ -112,7 +112,7 @@ struct FaSmem {
   // gathered candidates (rank 0's arrays are used)
   uint64_t gk[2][kFaG];
   float gw[2][kFaG];
-  int gn[2];
+  int gn[2][2];  // [gather parity][row]: appended candidates
   uint64_t res_k[2];
   uint32_t res_c[2];
   double res_m[2];
@@ -185,6 +185,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     fence_mbar_init();
     sh.zero_mass = 0;
   }
+  if (tid < 4) sh.gn[tid >> 1][tid & 1] = 0;
+  int gpar = 0;  // parity of the next gather's counters
   __syncthreads();
 
   auto elem_key = [&](float z, int j) { return make_key(ord32(z), (uint32_t)j); };
@@ -202,17 +204,29 @@ __global__ void __launch_bounds__(kThreads, 2)
   // barrier that follows the fill) into rc/rm and the range totals.
   auto range_reduce = [&](int r, uint32_t *rc, double *rm, uint32_t &tcr,
                           double &tmr) {
-    for (int i = tid; i < NR; i += kThreads) {
+    // GP consecutive threads per bucket, each reading every GP-th peer (the
+    // remote loads are all in flight at once), then a shuffle sum in a
+    // fixed order
+    const int GP = kThreads / NR;  // 2 (clusters of 8) or 4 (16)
+    {
+      const int i = tid / GP, g = tid % GP;
       uint32_t c = 0;
       double m = 0.0;
-      for (int q = 0; q < CL; ++q) {
+#pragma unroll 4
+      for (int q = g; q < CL; q += GP) {
         const uint32_t *phc = cluster.map_shared_rank(hc, q);
         const float *phm = cluster.map_shared_rank(hm, q);
         c += phc[r * kFaNB + r0 + i];
         m += (double)phm[r * kFaNB + r0 + i];
       }
-      rc[i] = c;
-      rm[i] = m;
+      for (int o = 1; o < GP; o <<= 1) {
+        c += __shfl_xor_sync(0xffffffffu, c, o);
+        m += __shfl_xor_sync(0xffffffffu, m, o);
+      }
+      if (g == 0) {
+        rc[i] = c;
+        rm[i] = m;
+      }
     }
     __syncthreads();
     if (warp == 0) {
@@ -432,16 +446,23 @@ __global__ void __launch_bounds__(kThreads, 2)
           sh.pkmax[tid] = b;
         }
         cluster.sync();
-        if (tid < 2) {
-          const int r = tid;
+        if (warp < 2) {  // warp r merges row r's key range: lane q, CTA q
+          const int r = warp;
+          uint64_t a = ~0ull, b = 0ull;
+          if (lane < CL) {
+            const FaSmem *ps = cluster.map_shared_rank(&sh, lane);
+            a = ps->pkmin[r];
+            b = ps->pkmax[r];
+          }
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            a = min(a, (uint64_t)__shfl_xor_sync(0xffffffffu,
+                                                 (unsigned long long)a, o));
+            b = max(b, (uint64_t)__shfl_xor_sync(0xffffffffu,
+                                                 (unsigned long long)b, o));
+          }
           FaSel s = sh.sel[r];
-          if (r >= rlo && r <= rhi && s.active && !s.gather) {
-            uint64_t a = ~0ull, b = 0ull;
-            for (int q = 0; q < CL; ++q) {
-              const FaSmem *ps = cluster.map_shared_rank(&sh, q);
-              a = min(a, ps->pkmin[r]);
-              b = max(b, ps->pkmax[r]);
-            }
+          if (lane == 0 && r >= rlo && r <= rhi && s.active && !s.gather) {
             if (a > s.klo) s.klo = a;
             if (b < s.khi) s.khi = b;
             const uint64_t span = s.khi - s.klo;
@@ -478,8 +499,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       if (any_gather) {
         // every CTA appends the candidates of the gathering rows to rank 0
-        if (tid < 2) sh.gn[tid] = 0;
-        cluster.sync();  // rank 0's counters are zero before any append
+        // (counters of this parity were zeroed by rank 0 at the previous
+        // gather, or at the start, before a cluster barrier)
         for (int r = rlo; r <= rhi; ++r) {
           const FaSel s = sh.sel[r];
           if (!s.active || !s.gather) continue;
@@ -490,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, 2)
               const float z = fa_elt<DT, VW>(sbuf[r], i, e);
               const uint64_t k = elem_key(z, (sl.vbeg + i) * VW + e);
               if (is_cand(s, r, z, k)) {
-                const int at = atomicAdd(&s0->gn[r], 1);
+                const int at = atomicAdd(&s0->gn[gpar][r], 1);
                 if (at < kFaG) {
                   s0->gk[r][at] = k;
                   s0->gw[r][at] = fa_weight(z, k2, mk[r]);
@@ -500,10 +521,11 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         cluster.sync();
         if (rank == 0) {
+          if (tid < 2) sh.gn[gpar ^ 1][tid] = 0;  // for the next gather
           for (int r = rlo; r <= rhi; ++r) {
             const FaSel s = sh.sel[r];
             if (!s.active || !s.gather) continue;
-            const int n = min(sh.gn[r], kFaG);
+            const int n = min(sh.gn[gpar][r], kFaG);
             // rank by counting (keys are distinct), then scatter
             uint64_t k = 0;
             float w = 0.f;
@@ -569,6 +591,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           }
         }
         cluster.sync();
+        gpar ^= 1;
         if (tid < 2) {
           const int r = tid;
           FaSel s = sh.sel[r];
@@ -657,16 +680,23 @@ __global__ void __launch_bounds__(kThreads, 2)
           sh.pbad[par][tid] = bb;
         }
         cluster.sync();
-        if (tid < 2) {
+        if (warp < 2) {  // warp r merges row r: lane q reads CTA q
           float a = -kInf;
           int bb = 0;
-          for (int q = 0; q < CL; ++q) {
-            const FaSmem *ps = cluster.map_shared_rank(&sh, q);
-            a = fmaxf(a, ps->pmax[par][tid]);
-            bb |= ps->pbad[par][tid];
+          if (lane < CL) {
+            const FaSmem *ps = cluster.map_shared_rank(&sh, lane);
+            a = ps->pmax[par][warp];
+            bb = ps->pbad[par][warp];
           }
-          sh.row[tid].m = a;
-          sh.row[tid].bad = bb || !(a > -kInf);
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+            bb |= __shfl_xor_sync(0xffffffffu, bb, o);
+          }
+          if (lane == 0) {
+            sh.row[warp].m = a;
+            sh.row[warp].bad = bb || !(a > -kInf);
+          }
         }
         par ^= 1;
         __syncthreads();
@@ -697,30 +727,38 @@ __global__ void __launch_bounds__(kThreads, 2)
         __syncthreads();
       }
       cluster.sync();
-      // totals, then the top-k selections
-      if (tid < 2 && tid >= rlo) {
-        const int r = tid;
+      // totals (warp r, lane q reads CTA q's range total, summed in a fixed
+      // order), then the top-k selections
+      if (warp < 2 && warp >= rlo) {
+        const int r = warp;
         uint32_t c = 0;
         double m = 0.0;
-        for (int q = 0; q < CL; ++q) {
-          const FaSmem *ps = cluster.map_shared_rank(&sh, q);
-          c += ps->tc1[r];
-          m += ps->tm1[r];
+        if (lane < CL) {
+          const FaSmem *ps = cluster.map_shared_rank(&sh, lane);
+          c = ps->tc1[r];
+          m = ps->tm1[r];
         }
-        FaRow &R = sh.row[r];
-        R.nfin = c;
-        R.total = m;
-        FaSel s = {};
-        s.mass_mode = 0;
-        s.bmax = kFaNB - 1;
-        s.tcount = (uint32_t)p.top_k;
-        s.active = (uint32_t)p.top_k < c;
-        sh.sel[r] = s;
-        if (!s.active) {  // no top-k cut: every finite token
-          R.kk = 0;
-          R.lk = c;
-          R.mk = m;
-          R.bk = kFaNB;  // no bucket holds the cut
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          c += __shfl_xor_sync(0xffffffffu, c, o);
+          m += __shfl_xor_sync(0xffffffffu, m, o);
+        }
+        if (lane == 0) {
+          FaRow &R = sh.row[r];
+          R.nfin = c;
+          R.total = m;
+          FaSel s = {};
+          s.mass_mode = 0;
+          s.bmax = kFaNB - 1;
+          s.tcount = (uint32_t)p.top_k;
+          s.active = (uint32_t)p.top_k < c;
+          sh.sel[r] = s;
+          if (!s.active) {  // no top-k cut: every finite token
+            R.kk = 0;
+            R.lk = c;
+            R.mk = m;
+            R.bk = kFaNB;  // no bucket holds the cut
+          }
         }
       }
       __syncthreads();
