@@ -128,11 +128,7 @@ typedef enum {
   SD_TUNE_FANOUT_LDG = 7,      /* 1: fan-out with plain loads; default 0 */
   SD_TUNE_FANOUT_MAXC = 8,     /* cap on the fan-out's clusters: 0 none */
   SD_TUNE_FANOUT_L2_FIRST = 9, /* fan-out rows read evict-first: default 1 */
-  SD_TUNE_PREFETCH_NEXT = 10,  /* linear verify: at a draw, ask L2 for the
-                                  next sequence's first rows: 0 or 1 */
-  SD_TUNE_TREE_CACHE = 11,     /* sampled tree walks keep fp32 exponentials
-                                  of the node's slices: 1 (default) or 0 */
-  SD_TUNE_COUNT = 12
+  SD_TUNE_COUNT = 10
 } sd_tune;
 
 sd_status sd_tune_set(sd_tune key, int value);

@@ -93,6 +93,7 @@ struct FaRow {
   double total;     // their mass (weights relative to the maximum)
   uint64_t ks;      // final threshold (kept iff finite and K >= ks)
   double ms;        // kept mass
+  float inv;        // 1 / ms (the draw multiplies: fp64 is slow)
   uint32_t ls;      // kept count
   uint64_t kk;      // top-k threshold
   double mk;        // top-k mass
@@ -796,6 +797,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         R.ms = t.mass;
       }
       __syncthreads();
+      if (tid < 2 && tid >= rlo) sh.row[tid].inv = (float)(1.0 / sh.row[tid].ms);
+      __syncthreads();
       if (rank == 0 && tid < 2 && tid >= rlo && p.out_keep)
         p.out_keep[(size_t)b * NS + (tid == 1 ? j : G1 + j)] =
             (int32_t)sh.row[tid].ls;
@@ -839,12 +842,12 @@ __global__ void __launch_bounds__(kThreads, 2)
             const float zt = fa_elt<DT, VW>(sbuf[1], i, e);
             float a = 0.f;
             if (zt > -kInf && elem_key(zt, jj) >= Rt.ks)
-              a = (float)((double)fa_weight(zt, k2, k2m_t) / Rt.ms);
+              a = __fmul_rn(fa_weight(zt, k2, k2m_t), Rt.inv);
             if (!use_q || a == 0.f) return a;
             const float zd = fa_elt<DT, VW>(sbuf[0], i, e);
             float q = 0.f;
             if (zd > -kInf && elem_key(zd, jj) >= Rd.ks)
-              q = (float)((double)fa_weight(zd, k2, k2m_d) / Rd.ms);
+              q = __fmul_rn(fa_weight(zd, k2, k2m_d), Rd.inv);
             return fmaxf(0.f, __fsub_rn(a, q));
           };
           cluster_total(cluster, sh.draw, segmass, sl, u, par, [&] {

@@ -56,7 +56,6 @@ struct LinearParams {
   int seg_bytes;   // bytes of the segment-mass array (multiple of 128)
   int slice_vecs;  // capacity of each slice buffer in 16-byte vectors (TMA)
   int spec;        // let a cluster's last sequence read ahead (0: never)
-  int pf_next;     // at a draw, prefetch the next sequence's first rows to L2
 };
 
 constexpr int kMaxW = 4;  // positions per step when a cluster speculates
@@ -297,18 +296,7 @@ __global__ void __launch_bounds__(kThreads, RING ? 4 : 2)
       }
     } else {
       // correction (kind 1) or bonus (kind 2) by inverse CDF over the rows
-      // of position n (streamed again: they were just read, so from L2).
-      // The cluster's next sequence always reads its position 0: ask for
-      // those rows now, so that they arrive while this draw runs
-      if (RING && p.pf_next && tid == 0) {
-        const int nxt = cluster.map_shared_rank(&sh, 0)->next_seq[seqpar];
-        const uint32_t sb = (uint32_t)(sl.vend - sl.vbeg) * 16u;
-        if (nxt < p.B && sb) {
-          prefetch_l2(trow_of(nxt, 0) + (size_t)sl.vbeg * 16, sb);
-          if (gamma > 0)
-            prefetch_l2(drow_of(nxt, 0) + (size_t)sl.vbeg * 16, sb);
-        }
-      }
+      // of position n (streamed again: they were just read, so from L2)
       const char *trow = trow_of(seq, n);
       const char *drow = kind == 1 ? drow_of(seq, n) : nullptr;
       const GR ra{trow}, rb{drow ? drow : trow};
@@ -458,7 +446,6 @@ sd_status linear_launch(const void *target, const void *draft, sd_dtype dt,
   prm.seg_bytes = (int)seg_bytes;
   prm.slice_vecs = (int)per_cta;
   prm.spec = tune(SD_TUNE_SPEC);
-  prm.pf_next = tune(SD_TUNE_PREFETCH_NEXT);
   if (B > nclusters) {
     if (!ws || ws_bytes < 256)
       return fail(SD_ERR_INVALID_ARG, "workspace of >= 256 bytes required");

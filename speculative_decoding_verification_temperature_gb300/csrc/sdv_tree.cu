@@ -58,7 +58,6 @@ struct TreeSmem {
   AM apart[2];
   MS mt, md;
   AM am;
-  float cmax[2];  // this CTA's maxima of the node's rows (cached mode)
   int invalid;
   int par_[SD_MAX_TREE_NODES];
   int tok[SD_MAX_TREE_NODES];
@@ -173,189 +172,8 @@ __device__ DrawOut det_draw(cg::cluster_group &cluster, DrawSmem &ds,
   return out;
 }
 
-// ---------------------------------------------------------------------
-// Cached exponentials.  In the sampled walks on shared-memory slices every
-// CTA replaces a node's slices, once they have landed, by
-// e_j = 2^((z_j - M) k2) in fp32, M the CTA's own maximum of the row (bf16
-// slices land in the upper half of the fp32 buffer and are widened front
-// to back, a block barrier between the reads and the writes of each round
-// of 256 vectors: a round's writes end below the next round's unread
-// vectors).  Every later pass over the node -- the mass after each
-// rejected sibling, the final draw -- then multiplies only: p_j = a_t e_j
-// and q_j = a_d e_j with a = 2^((M - m) k2) / s from the merged (m, s).
-struct ECache {
-  const float *et, *ed;  // this CTA's exponentials, element 0 = vector vbeg
-  float at, ad;
-  int vbeg;
-};
-
-template <int VW>
-__device__ __forceinline__ void e_load(const float *e, int i, float (&x)[VW]) {
-  const float4 *q = reinterpret_cast<const float4 *>(e) + (size_t)i * (VW / 4);
-#pragma unroll
-  for (int h = 0; h < VW / 4; ++h) {
-    const float4 a = q[h];
-    x[4 * h] = a.x;
-    x[4 * h + 1] = a.y;
-    x[4 * h + 2] = a.z;
-    x[4 * h + 3] = a.w;
-  }
-}
-
-// Weights of vector v (absolute index): p, or max(0, p - cq' e_d) with
-// cq' = a_d c (rounded products, so identical rows give exactly zero).
-template <int VW>
-__device__ __forceinline__ void e_weights(const ECache &E, int v, bool has_q,
-                                          float adc, float (&w)[VW]) {
-  float a[VW], b[VW];
-  e_load<VW>(E.et, v - E.vbeg, a);
-  if (has_q) e_load<VW>(E.ed, v - E.vbeg, b);
-#pragma unroll
-  for (int e = 0; e < VW; ++e) {
-    const float pt = __fmul_rn(E.at, a[e]);
-    w[e] = has_q ? fmaxf(0.f, __fsub_rn(pt, __fmul_rn(adc, b[e]))) : pt;
-  }
-}
-
-// Per-segment masses from the cached exponentials (one warp per segment).
-template <int VW, class WF>
-__device__ __forceinline__ void e_mass_pass(const Slice &sl, float *segmass,
-                                            WF &&wf) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int s = warp; s < sl.nseg; s += kWarps) {
-    const int v = sl.vbeg + s * 32 + lane;
-    float acc = 0.f;
-    if (v < sl.vend) {
-      float w[VW];
-      wf(v, w);
-#pragma unroll
-      for (int e = 0; e < VW; ++e) acc += w[e];
-    }
-    acc = warp_down_sum(acc);
-    if (lane == 0) segmass[s] = acc;
-  }
-}
-
-// After cluster_total: the owner CTA's warp 0 scans the crossing segment.
-template <int VW, class WF>
-__device__ DrawOut e_pick(cg::cluster_group &cluster, DrawSmem &ds,
-                          const float *segmass, const Slice &sl, WF &&wf) {
-  const int tid = threadIdx.x;
-  DrawOut out;
-  out.N = ds.N;
-  out.owner = ds.owner;
-  out.t = -1;
-  out.wt = 0.f;
-  if (out.owner == (int)cluster.block_rank()) {
-    if (tid == 0) {
-      double tin = 0.0;
-      ds.seg = find_segment(segmass, sl.nseg, ds.chunk_pre, ds.tau, &tin);
-      ds.tau_seg = (float)tin;
-    }
-    __syncthreads();
-    if (tid < 32) {
-      const int v = sl.vbeg + ds.seg * 32 + tid;
-      float w[VW];
-      if (v < sl.vend) {
-        wf(v, w);
-      } else {
-#pragma unroll
-        for (int e = 0; e < VW; ++e) w[e] = 0.f;
-      }
-      out.t = warp_pick<VW>(w, ds.tau_seg, (sl.vbeg + ds.seg * 32) * VW,
-                            &out.wt);
-    }
-  }
-  return out;
-}
-
-// The CTA's maximum of a landed raw slice (NaN-propagating) and the
-// widening of the slice into cached exponentials with their sum.  raw: the
-// slice's 16-byte vectors; e: the fp32 buffer (raw is its upper half for
-// bf16, the buffer itself for fp32).
-template <int DT, int VW>
-__device__ __forceinline__ float e_slice_max(const uint4 *raw, int nv) {
-  float mx = -kInf;
-  for (int i = threadIdx.x; i < nv; i += kThreads) {
-    Raw<DT, VW> r;
-    r.w = raw[i];
-    float z[VW];
-#pragma unroll
-    for (int e = 0; e < VW; ++e) z[e] = elt<DT, VW>(r, e);
-    mx = max_nan(mx, vmax_nan_of<VW>(z));
-  }
-  return mx;
-}
-
-template <int DT, int VW>
-__device__ __forceinline__ float e_convert(const uint4 *raw, float *e, int nv,
-                                           float k2, float mk) {
-  float s = 0.f;
-  for (int r0 = 0; r0 < nv; r0 += kThreads) {
-    const int i = r0 + (int)threadIdx.x;
-    Raw<DT, VW> r;
-    if (i < nv) r.w = raw[i];
-    if constexpr (DT == 1) __syncthreads();  // this round's reads first
-    if (i < nv) {
-      float x[VW];
-#pragma unroll
-      for (int k = 0; k < VW; ++k) {
-        x[k] = ex2(fmaf(elt<DT, VW>(r, k), k2, -mk));
-        s += x[k];
-      }
-      float4 *q = reinterpret_cast<float4 *>(e) + (size_t)i * (VW / 4);
-#pragma unroll
-      for (int h = 0; h < VW / 4; ++h)
-        q[h] = make_float4(x[4 * h], x[4 * h + 1], x[4 * h + 2], x[4 * h + 3]);
-    }
-  }
-  return s;
-}
-
-// Deterministic drafts on cached exponentials: p without the removed
-// tokens ex[0..ne) (as det_fill / det_draw above).
-template <int VW>
-__device__ __forceinline__ void e_det_weights(const ECache &E, const int *ex,
-                                              int ne, int v, float (&w)[VW]) {
-  e_weights<VW>(E, v, false, 0.f, w);
-#pragma unroll
-  for (int e = 0; e < VW; ++e)
-    if (is_removed(ex, ne, v * VW + e)) w[e] = 0.f;
-}
-
-template <int VW>
-__device__ void e_det_fill(const ECache &E, const Slice &sl, float *segmass,
-                           const int *ex, int ne) {
-  e_mass_pass<VW>(sl, segmass, [&](int v, float (&w)[VW]) {
-    e_weights<VW>(E, v, false, 0.f, w);
-  });
-  if (ne == 0) return;
-  __syncthreads();
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  auto seg_of = [&](int j) {
-    const int v = j / VW;
-    return (v >= sl.vbeg && v < sl.vend) ? (v - sl.vbeg) / 32 : -1;
-  };
-  for (int i = warp; i < ne; i += kWarps) {
-    const int s = seg_of(ex[i]);
-    bool first = s >= 0;
-    for (int r = 0; r < i && first; ++r) first = seg_of(ex[r]) != s;
-    if (!first) continue;  // warp-uniform
-    const int v = sl.vbeg + s * 32 + lane;
-    float acc = 0.f;
-    if (v < sl.vend) {
-      float w[VW];
-      e_det_weights<VW>(E, ex, ne, v, w);
-#pragma unroll
-      for (int e = 0; e < VW; ++e) acc += w[e];
-    }
-    acc = warp_down_sum(acc);
-    if (lane == 0) segmass[s] = acc;
-  }
-}
-
-template <int DT, int VW, bool GREEDY, bool TMA, bool DET, bool CACHE>
-__global__ void __launch_bounds__(kThreads, CACHE ? 1 : 2)
+template <int DT, int VW, bool GREEDY, bool TMA, bool DET>
+__global__ void __launch_bounds__(kThreads, 2)
     tree_verify_kernel(const TreeParams p) {
   extern __shared__ __align__(128) unsigned char dsm[];
   __shared__ TreeSmem sh;
@@ -371,19 +189,8 @@ __global__ void __launch_bounds__(kThreads, CACHE ? 1 : 2)
   const char *dbase = static_cast<const char *>(p.draft);
   const float k2 = p.k2;
   float *segmass = reinterpret_cast<float *>(dsm);
-  // buffers: raw slices, or (CACHE) fp32 exponentials of slice_vecs * VW
-  // elements each, with bf16 raw slices landing in their upper halves
-  constexpr int kBufVecs = CACHE ? (VW * 4) / 16 : 1;  // 16-byte units per vector
   uint4 *tbuf = reinterpret_cast<uint4 *>(dsm + p.seg_bytes);
-  uint4 *dbuf = tbuf + (size_t)p.slice_vecs * kBufVecs;
-  uint4 *traw = tbuf + (CACHE && DT == 1 ? p.slice_vecs : 0);
-  uint4 *draw = dbuf + (CACHE && DT == 1 ? p.slice_vecs : 0);
-  static_assert(!CACHE || (TMA && !GREEDY), "cache: sampled TMA walks only");
-  ECache E;
-  E.et = reinterpret_cast<const float *>(tbuf);
-  E.ed = reinterpret_cast<const float *>(dbuf);
-  E.vbeg = sl.vbeg;
-  E.at = E.ad = 0.f;
+  uint4 *dbuf = tbuf + p.slice_vecs;
   const uint32_t slice_bytes = (uint32_t)(sl.vend - sl.vbeg) * 16u;
   uint32_t phase = 0;
   if (TMA) {
@@ -452,8 +259,8 @@ __global__ void __launch_bounds__(kThreads, CACHE ? 1 : 2)
         fence_proxy_async();
         mbar_expect_tx(&bar, slice_bytes * (has_q ? 2u : 1u));
         if (slice_bytes) {
-          bulk_g2s(traw, trow + (size_t)sl.vbeg * 16, slice_bytes, &bar);
-          if (has_q) bulk_g2s(draw, drow + (size_t)sl.vbeg * 16, slice_bytes, &bar);
+          bulk_g2s(tbuf, trow + (size_t)sl.vbeg * 16, slice_bytes, &bar);
+          if (has_q) bulk_g2s(dbuf, drow + (size_t)sl.vbeg * 16, slice_bytes, &bar);
         }
       }
       // gathers of the children's logits (used after the merge)
@@ -477,54 +284,6 @@ __global__ void __launch_bounds__(kThreads, CACHE ? 1 : 2)
         argmax_pass<DT, VW>(ra, sl, a);
         a = block_reduce_am(a, sh.ared);
         if (tid == 0) sh.apart[par] = a;
-      } else if constexpr (CACHE) {
-        // the CTA's maxima, then the slices widened into exponentials
-        const int nv = sl.vend - sl.vbeg;
-        float mx[2] = {e_slice_max<DT, VW>(traw, nv),
-                       has_q ? e_slice_max<DT, VW>(draw, nv) : -kInf};
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1)
-            mx[r] = max_nan(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], o));
-          if (lane == 0) sh.red[r][warp].m = mx[r];
-        }
-        __syncthreads();
-        float M[2];
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          M[r] = sh.red[r][0].m;
-          for (int w = 1; w < kWarps; ++w) M[r] = max_nan(M[r], sh.red[r][w].m);
-        }
-        __syncthreads();  // sh.red is read before it is reused below
-        // an empty or all -inf slice: weights 0 (the offset must stay
-        // finite), state empty
-        const bool ok0 = M[0] > kMEmpty, ok1 = M[1] > kMEmpty;
-        float s0 = e_convert<DT, VW>(traw, reinterpret_cast<float *>(tbuf),
-                                     nv, k2, ok0 ? M[0] * k2 : 0.f);
-        float s1 = has_q ? e_convert<DT, VW>(draw,
-                                             reinterpret_cast<float *>(dbuf),
-                                             nv, k2, ok1 ? M[1] * k2 : 0.f)
-                         : 0.f;
-        s0 = warp_down_sum(s0);
-        s1 = warp_down_sum(s1);
-        if (lane == 0) {
-          sh.red[0][warp].s = s0;
-          sh.red[1][warp].s = s1;
-        }
-        __syncthreads();
-        if (tid == 0) {
-          float a = 0.f, b = 0.f;
-          for (int w = 0; w < kWarps; ++w) {
-            a += sh.red[0][w].s;
-            b += sh.red[1][w].s;
-          }
-          // a NaN or +inf maximum makes the state invalid, as in ms_add
-          sh.part[par][0] = ok0 || M[0] != M[0] ? MS{M[0], a} : ms_empty();
-          sh.part[par][1] = ok1 || M[1] != M[1] ? MS{M[1], b} : ms_empty();
-          sh.cmax[0] = M[0];
-          sh.cmax[1] = M[1];
-        }
       } else {
         MS st[2] = {ms_empty(), ms_empty()};
         stats_pass<DT, VW>(ra, rb, has_q, sl, k2, st[0], st[1]);
@@ -565,12 +324,6 @@ __global__ void __launch_bounds__(kThreads, CACHE ? 1 : 2)
       if (sh.invalid) {
         kind = 3;
         break;
-      }
-      if constexpr (CACHE) {  // p_j = at e_j, q_j = ad e_j on this CTA
-        const float M0 = sh.cmax[0], M1 = sh.cmax[1];
-        E.at = M0 > kMEmpty ? ex2((M0 - sh.mt.m) * k2) / sh.mt.s : 0.f;
-        E.ad = (has_q && M1 > kMEmpty) ? ex2((M1 - sh.md.m) * k2) / sh.md.s
-                                       : 0.f;
       }
       for (int i = 0; i < nk; ++i) {
         const int x = sh.tok[sh.kids[i]];
@@ -624,12 +377,8 @@ __global__ void __launch_bounds__(kThreads, CACHE ? 1 : 2)
               __syncthreads();  // sh.ex[ne - 1] is seen by every thread
             } else {  // a dominant one: sum the rest again
               __syncthreads();
-              if constexpr (CACHE)
-                Nr = cluster_total(cluster, sh.draw, segmass, sl, -1.f, par,
-                                   [&] { e_det_fill<VW>(E, sl, segmass, sh.ex, ne); });
-              else
-                Nr = det_mass<DT, VW>(cluster, sh.draw, segmass, ra, W, sl,
-                                      sh.ex, ne, -1.f, par);
+              Nr = det_mass<DT, VW>(cluster, sh.draw, segmass, ra, W, sl,
+                                    sh.ex, ne, -1.f, par);
               __syncthreads();
               if (!(Nr > 0.0)) {
                 zm = true;
@@ -641,25 +390,13 @@ __global__ void __launch_bounds__(kThreads, CACHE ? 1 : 2)
         if (next < 0) {
           __syncthreads();
           const float u = sh.uni[0];
-          auto ddraw = [&](int nrem) {
-            if constexpr (CACHE) {
-              cluster_total(cluster, sh.draw, segmass, sl, u, par, [&] {
-                e_det_fill<VW>(E, sl, segmass, sh.ex, nrem);
-              });
-              return e_pick<VW>(cluster, sh.draw, segmass, sl,
-                                [&](int v, float (&w)[VW]) {
-                                  e_det_weights<VW>(E, sh.ex, nrem, v, w);
-                                });
-            } else {
-              return det_draw<DT, VW>(cluster, sh.draw, segmass, ra, W, sl,
-                                      sh.ex, nrem, u, par);
-            }
-          };
-          DrawOut o = ddraw(zm ? 0 : ne);
+          DrawOut o = det_draw<DT, VW>(cluster, sh.draw, segmass, ra, W, sl,
+                                       sh.ex, zm ? 0 : ne, u, par);
           if (o.owner < 0) {
             zm = true;
             __syncthreads();
-            o = ddraw(0);
+            o = det_draw<DT, VW>(cluster, sh.draw, segmass, ra, W, sl, sh.ex,
+                                 0, u, par);
           }
           zero_mass = zm;
           writer = (o.owner == rank && warp == 0);
@@ -693,17 +430,8 @@ __global__ void __launch_bounds__(kThreads, CACHE ? 1 : 2)
           c += Nc;
           if (i + 1 < nk) {
             W.cq = (float)(c / (double)md.s);
-            if constexpr (CACHE) {
-              const float adc = (float)((double)E.ad * c);
-              Nc = cluster_total(cluster, sh.draw, segmass, sl, -1.f, par, [&] {
-                e_mass_pass<VW>(sl, segmass, [&](int v, float (&w)[VW]) {
-                  e_weights<VW>(E, v, true, adc, w);
-                });
-              });
-            } else {
-              Nc = cluster_mass<DT, VW>(cluster, sh.draw, segmass, ra, rb,
-                                        true, W, sl, -1.f, par);
-            }
+            Nc = cluster_mass<DT, VW>(cluster, sh.draw, segmass, ra, rb, true,
+                                      W, sl, -1.f, par);
             __syncthreads();
             if (!(Nc > 0.0)) {
               zm = true;
@@ -717,25 +445,13 @@ __global__ void __launch_bounds__(kThreads, CACHE ? 1 : 2)
           const bool use_q = has_q && !zm;
           W.cq = use_q ? (float)(c / (double)md.s) : 0.f;
           const float u = sh.uni[0];
-          auto sdraw = [&](bool uq) {
-            if constexpr (CACHE) {
-              const float adc = uq ? (float)((double)E.ad * c) : 0.f;
-              auto wf = [&](int v, float (&w)[VW]) {
-                e_weights<VW>(E, v, uq, adc, w);
-              };
-              cluster_total(cluster, sh.draw, segmass, sl, u, par,
-                            [&] { e_mass_pass<VW>(sl, segmass, wf); });
-              return e_pick<VW>(cluster, sh.draw, segmass, sl, wf);
-            } else {
-              return cluster_draw<DT, VW>(cluster, sh.draw, segmass, ra, rb,
-                                          uq, W, sl, u, par);
-            }
-          };
-          DrawOut o = sdraw(use_q);
+          DrawOut o = cluster_draw<DT, VW>(cluster, sh.draw, segmass, ra, rb,
+                                           use_q, W, sl, u, par);
           if (o.owner < 0) {
             zm = true;
             __syncthreads();
-            o = sdraw(false);
+            o = cluster_draw<DT, VW>(cluster, sh.draw, segmass, ra, rb, false,
+                                     W, sl, u, par);
           }
           zero_mass = zm;
           writer = (o.owner == rank && warp == 0);
@@ -791,31 +507,25 @@ __global__ void __launch_bounds__(kThreads, CACHE ? 1 : 2)
 using TreeKernel = void (*)(const TreeParams);
 
 template <int DT, int VW, bool TMA>
-static TreeKernel pick_tree_t(bool greedy, bool det, bool cache) {
-  if (greedy) return tree_verify_kernel<DT, VW, true, TMA, false, false>;
-  if constexpr (TMA) {
-    if (cache)
-      return det ? tree_verify_kernel<DT, VW, false, true, true, true>
-                 : tree_verify_kernel<DT, VW, false, true, false, true>;
-  }
-  return det ? tree_verify_kernel<DT, VW, false, TMA, true, false>
-             : tree_verify_kernel<DT, VW, false, TMA, false, false>;
+static TreeKernel pick_tree_t(bool greedy, bool det) {
+  if (greedy) return tree_verify_kernel<DT, VW, true, TMA, false>;
+  return det ? tree_verify_kernel<DT, VW, false, TMA, true>
+             : tree_verify_kernel<DT, VW, false, TMA, false>;
 }
 
-static TreeKernel pick_tree(int dt, bool vec, bool tma, bool greedy, bool det,
-                            bool cache) {
+static TreeKernel pick_tree(int dt, bool vec, bool tma, bool greedy,
+                            bool det) {
   if (dt == SD_F32) {
-    if (!vec) return pick_tree_t<0, 1, false>(greedy, det, false);
-    return tma ? pick_tree_t<0, 4, true>(greedy, det, cache)
-               : pick_tree_t<0, 4, false>(greedy, det, false);
+    if (!vec) return pick_tree_t<0, 1, false>(greedy, det);
+    return tma ? pick_tree_t<0, 4, true>(greedy, det)
+               : pick_tree_t<0, 4, false>(greedy, det);
   }
-  if (!vec) return pick_tree_t<1, 1, false>(greedy, det, false);
-  return tma ? pick_tree_t<1, 8, true>(greedy, det, cache)
-             : pick_tree_t<1, 8, false>(greedy, det, false);
+  if (!vec) return pick_tree_t<1, 1, false>(greedy, det);
+  return tma ? pick_tree_t<1, 8, true>(greedy, det)
+             : pick_tree_t<1, 8, false>(greedy, det);
 }
 
 constexpr size_t kTreeTmaSmemMax = 96 * 1024;
-constexpr size_t kTreeCacheSmemMax = 200 * 1024;  // one CTA per SM
 
 
 }  // namespace sdv
@@ -869,25 +579,17 @@ sd_status sdv::tree_launch(
   bool tma = false;
   TreeKernel kern = nullptr;
   int maxc = 0;
-  bool cache = false;
   for (;;) {
     per_cta = (nvec + CL - 1) / CL;
     seg_bytes = ((size_t)((per_cta + 31) / 32) * 4 + 127) / 128 * 128;
     const size_t tma_smem =
         seg_bytes + (one_row ? 1 : 2) * (size_t)per_cta * 16;
-    // sampled walks keep fp32 exponentials of the node's slices (each
-    // element 4 bytes: twice a bf16 slice)
-    const size_t cache_smem =
-        seg_bytes + (det ? 1 : 2) * (size_t)per_cta * vw * 4;
-    const bool tma_ok = vec && tune(SD_TUNE_NO_TMA) == 0;
-    cache = tma_ok && !greedy && cache_smem <= kTreeCacheSmemMax &&
-            tune(SD_TUNE_TREE_CACHE) != 0;
-    tma = tma_ok && (cache || tma_smem <= kTreeTmaSmemMax);
-    smem = cache ? cache_smem : tma ? tma_smem : seg_bytes;
-    if (smem > (cache ? kTreeCacheSmemMax : 96 * 1024))
+    tma = vec && tma_smem <= kTreeTmaSmemMax && tune(SD_TUNE_NO_TMA) == 0;
+    smem = tma ? tma_smem : seg_bytes;
+    if (smem > 96 * 1024)
       return fail(SD_ERR_UNSUPPORTED, "V=%d needs %zu B of shared memory", V,
                   smem);
-    kern = pick_tree(dt, vec, tma, greedy, det, cache);
+    kern = pick_tree(dt, vec, tma, greedy, det);
     st = max_active_clusters((const void *)kern, CL, smem, &maxc);
     if (st != SD_OK) return st;
     if (CL > 8 && maxc < B && tune(SD_TUNE_CLUSTER) == 0) {

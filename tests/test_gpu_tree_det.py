@@ -63,8 +63,7 @@ def test_repeated_and_adjacent_sibling_tokens():
 
 
 @pytest.mark.parametrize("sw", [{"no_tma": 1}, {"cluster": 1},
-                                {"cluster": 2}, {"cluster": 8},
-                                {"tree_cache": 0}])
+                                {"cluster": 2}, {"cluster": 8}])
 def test_load_paths_and_cluster_sizes(sw):
     c = to_device(synth.tree_case(10, 32, 20000, torch.bfloat16, 1.0,
                                   seed=9, sigma_t=1.0, sigma_d=1.0))
