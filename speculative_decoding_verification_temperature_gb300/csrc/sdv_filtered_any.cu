@@ -18,9 +18,7 @@
 //    weight 2^-e below the maximum, in steps of 1/32 (1024 buckets, the last
 //    one open-ended), holding counts and masses.  The CTAs' histograms are
 //    summed range by range across the cluster (each CTA owns 1024 / CL
-//    buckets; masses in integer fixed point, w * 2^((b+1)/32 + 16) rounded,
-//    at most ~2^16 per element, so the updates are integer atomics and a
-//    bucket's sum is exact), and every CTA finds where the criterion crosses:
+//    buckets), and every CTA finds the bucket where the criterion crosses:
 //    the top_k-th element (counts), or the element at which the prefix mass
 //    reaches top_p times the top-k mass (masses).
 //  - The crossing bucket's elements are gathered into rank 0 (at most 256:
@@ -116,11 +114,6 @@ struct FaSmem {
   uint64_t gk[2][kFaG];
   float gw[2][kFaG];
   int gn[2][2];  // [gather parity][row]: appended candidates
-  // this CTA's candidates before they go to rank 0 in one block
-  uint64_t lk[2][kFaG];
-  float lw[2][kFaG];
-  int ln[2], lbase[2];
-  float fs[kFaNB];  // fixed-point scale of bucket b: 2^((b+1)/32 + 16)
   uint64_t res_k[2];
   uint32_t res_c[2];
   double res_m[2];
@@ -183,7 +176,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   float *segmass = reinterpret_cast<float *>(sbuf[1] + p.slice_vecs);
   uint32_t *hc = reinterpret_cast<uint32_t *>(
       reinterpret_cast<unsigned char *>(segmass) + p.seg_bytes);  // [2][NB]
-  uint32_t *hm = hc + 2 * kFaNB;  // [2][NB] masses, fixed point
+  float *hm = reinterpret_cast<float *>(hc + 2 * kFaNB);          // [2][NB]
   const int NR = kFaNB / CL;  // buckets this CTA owns
   const int r0 = rank * NR;
   uint32_t phase = 0;
@@ -194,8 +187,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     sh.zero_mass = 0;
   }
   if (tid < 4) sh.gn[tid >> 1][tid & 1] = 0;
-  for (int b = tid; b < kFaNB; b += kThreads)
-    sh.fs[b] = exp2f((float)(b + 1) * (1.f / kFaRes) + 16.f);
   int gpar = 0;  // parity of the next gather's counters
   __syncthreads();
 
@@ -207,16 +198,13 @@ __global__ void __launch_bounds__(kThreads, 2)
   auto hist_clear = [&]() {
     for (int i = tid; i < 2 * kFaNB; i += kThreads) {
       hc[i] = 0;
-      hm[i] = 0u;
+      hm[i] = 0.f;
     }
   };
   // Sum this CTA's range of buckets over the cluster (after a cluster
   // barrier that follows the fill) into rc/rm and the range totals.
-  // fixb: the bucket whose scale every mass of this level carries (a
-  // refinement level: the candidates' level-1 bucket), or -1 for level 1
-  // (each bucket its own)
   auto range_reduce = [&](int r, uint32_t *rc, double *rm, uint32_t &tcr,
-                          double &tmr, int fixb) {
+                          double &tmr) {
     // GP consecutive threads per bucket, each reading every GP-th peer (the
     // remote loads are all in flight at once), then a shuffle sum in a
     // fixed order
@@ -224,13 +212,13 @@ __global__ void __launch_bounds__(kThreads, 2)
     {
       const int i = tid / GP, g = tid % GP;
       uint32_t c = 0;
-      unsigned long long m = 0;
+      double m = 0.0;
 #pragma unroll 4
       for (int q = g; q < CL; q += GP) {
         const uint32_t *phc = cluster.map_shared_rank(hc, q);
-        const uint32_t *phm = cluster.map_shared_rank(hm, q);
+        const float *phm = cluster.map_shared_rank(hm, q);
         c += phc[r * kFaNB + r0 + i];
-        m += phm[r * kFaNB + r0 + i];
+        m += (double)phm[r * kFaNB + r0 + i];
       }
       for (int o = 1; o < GP; o <<= 1) {
         c += __shfl_xor_sync(0xffffffffu, c, o);
@@ -238,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       if (g == 0) {
         rc[i] = c;
-        rm[i] = (double)m / (double)sh.fs[fixb >= 0 ? fixb : r0 + i];
+        rm[i] = m;
       }
     }
     __syncthreads();
@@ -497,9 +485,7 @@ __global__ void __launch_bounds__(kThreads, 2)
               if (is_cand(s, r, z, k)) {
                 const int b = (int)((s.khi - k) >> s.shift);  // 0: best
                 atomicAdd(&hc[r * kFaNB + b], 1u);
-                atomicAdd(&hm[r * kFaNB + b],
-                          __float2uint_rn(__fmul_rn(fa_weight(z, k2, mk[r]),
-                                                    sh.fs[s.b1])));
+                atomicAdd(&hm[r * kFaNB + b], fa_weight(z, k2, mk[r]));
               }
             }
         }
@@ -507,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int r = rlo; r <= rhi; ++r) {
           const FaSel s = sh.sel[r];
           if (!s.active || s.gather) continue;
-          range_reduce(r, sh.rcx[r], sh.rmx[r], sh.tcx[r], sh.tmx[r], s.b1);
+          range_reduce(r, sh.rcx[r], sh.rmx[r], sh.tcx[r], sh.tmx[r]);
           __syncthreads();
         }
         cluster.sync();
@@ -516,42 +502,23 @@ __global__ void __launch_bounds__(kThreads, 2)
         // every CTA appends the candidates of the gathering rows to rank 0
         // (counters of this parity were zeroed by rank 0 at the previous
         // gather, or at the start, before a cluster barrier)
-        // (staged in this CTA, then one reservation at rank 0 per row)
-        if (tid < 2) sh.ln[tid] = 0;
-        __syncthreads();
         for (int r = rlo; r <= rhi; ++r) {
           const FaSel s = sh.sel[r];
           if (!s.active || !s.gather) continue;
+          FaSmem *s0 = cluster.map_shared_rank(&sh, 0);
           for (int i = tid; i < nv; i += kThreads)
 #pragma unroll
             for (int e = 0; e < VW; ++e) {
               const float z = fa_elt<DT, VW>(sbuf[r], i, e);
               const uint64_t k = elem_key(z, (sl.vbeg + i) * VW + e);
               if (is_cand(s, r, z, k)) {
-                const int at = atomicAdd(&sh.ln[r], 1);
+                const int at = atomicAdd(&s0->gn[gpar][r], 1);
                 if (at < kFaG) {
-                  sh.lk[r][at] = k;
-                  sh.lw[r][at] = fa_weight(z, k2, mk[r]);
+                  s0->gk[r][at] = k;
+                  s0->gw[r][at] = fa_weight(z, k2, mk[r]);
                 }
               }
             }
-        }
-        __syncthreads();
-        FaSmem *s0 = cluster.map_shared_rank(&sh, 0);
-        if (tid < 2) {
-          const int cnt = min(sh.ln[tid], kFaG);
-          sh.lbase[tid] = cnt ? atomicAdd(&s0->gn[gpar][tid], cnt) : 0;
-        }
-        __syncthreads();
-        for (int r = rlo; r <= rhi; ++r) {
-          const int cnt = min(sh.ln[r], kFaG);
-          for (int i = tid; i < cnt; i += kThreads) {
-            const int at = sh.lbase[r] + i;
-            if (at < kFaG) {
-              s0->gk[r][at] = sh.lk[r][i];
-              s0->gw[r][at] = sh.lw[r][i];
-            }
-          }
         }
         cluster.sync();
         if (rank == 0) {
@@ -752,14 +719,12 @@ __global__ void __launch_bounds__(kThreads, 2)
             if (z > -kInf) {
               const int bk = fa_bucket1(z, k2, mk[r]);
               atomicAdd(&hc[r * kFaNB + bk], 1u);
-              atomicAdd(&hm[r * kFaNB + bk],
-                        __float2uint_rn(__fmul_rn(fa_weight(z, k2, mk[r]),
-                                                  sh.fs[bk])));
+              atomicAdd(&hm[r * kFaNB + bk], fa_weight(z, k2, mk[r]));
             }
           }
       cluster.sync();
       for (int r = rlo; r < 2; ++r) {
-        range_reduce(r, sh.rc1[r], sh.rm1[r], sh.tc1[r], sh.tm1[r], -1);
+        range_reduce(r, sh.rc1[r], sh.rm1[r], sh.tc1[r], sh.tm1[r]);
         __syncthreads();
       }
       cluster.sync();
