@@ -110,7 +110,7 @@ class ClockSampler:
 # (profiles/), with the units that launch processed: the fan-out reads every
 # row once, so its traffic scales with the rows; the verify's with the bytes
 # the method needs (its early exit decides how many rows it reads).
-TRAFFIC = {"fanout": (591.25e6, 128 * 9), "linear": (422.40e6, 343.73e6)}
+TRAFFIC = {"fanout": (591.25e6, 128 * 9), "linear": (421.20e6, 343.73e6)}
 
 
 def hbm_peak():
