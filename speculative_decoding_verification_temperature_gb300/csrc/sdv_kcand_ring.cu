@@ -36,7 +36,6 @@ struct KRParams {
   int *queue;
   int nclusters;
   int seg_bytes;
-  int pf_draft;  // while a decision is pending, ask L2 for the next draft row
 };
 
 constexpr int kKRows = SD_MAX_K + 1;  // draft row + one per candidate
@@ -56,7 +55,6 @@ struct KSched {
   int ksel, nsel;
   int bdone;     // bonus row exchanged: 1 valid, 2 unusable
   int next;      // the sequence after dseq, -1 until known
-  int pfj;       // position whose next draft row was prefetched (-1: none)
 };
 
 // The producer's current item (thread 0's registers).
@@ -139,18 +137,7 @@ struct KFu {
         sc.pk = k + 1;
         ra = trow(b, k, j);
       } else if (sc.pkind == 2) {  // wait for decision j
-        if (!(cur && sc.decided > j)) {
-          // the next position starts with its draft row whenever a
-          // candidate survives: bring it to L2 meanwhile (a hint; nothing
-          // depends on it)
-          if (!GREEDY && p.pf_draft && cur && sc.pfj != j &&
-              j + 1 < p.gamma && nv > 0) {
-            prefetch_l2(drow(b, j + 1) + (size_t)sl.vbeg * 16,
-                        (uint32_t)nv * 16u);
-            sc.pfj = j;
-          }
-          return false;
-        }
+        if (!(cur && sc.decided > j)) return false;
         if (sc.done) {
           sc.pkind = 3;
         } else {
@@ -183,7 +170,6 @@ struct KFu {
         sc.pseq = -1;
         sc.pj = 0;
         sc.pkind = 0;
-        sc.pfj = -1;
         continue;
       }
       if (ra && nv > 0) {  // (greedy reads no draft row)
@@ -303,7 +289,6 @@ __global__ void __launch_bounds__(kThreads, 4)
     sc.ksel = sc.nsel = 0;
     sc.bdone = 0;
     sc.next = -1;
-    sc.pfj = -1;
   }
   ring_init(rg);  // (a block barrier)
   int par = 0, seqpar = 0, consumed = 0;
@@ -654,7 +639,6 @@ sd_status kcand_ring_launch(const void *target, const void *draft,
   prm.queue = static_cast<int *>(ws);
   prm.nclusters = B < maxc ? B : maxc;
   prm.seg_bytes = (int)(smem - kRingBytes);
-  prm.pf_draft = tune(SD_TUNE_KCAND_PREFETCH);
   SDV_CUDA(cudaMemsetAsync(ws, 0, sizeof(int), stream));
   void *args[] = {&prm};
   *launched = true;

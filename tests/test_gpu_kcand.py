@@ -101,18 +101,6 @@ def test_streaming_kernel_work_queue():
     assert r["acc_flagged"] / r["seqs"] < 5e-3
 
 
-def test_draft_row_prefetch_switch():
-    """SD_TUNE_KCAND_PREFETCH 1 (an L2 hint during each decision) gives
-    the same results as without it, against the oracle."""
-    c = to_device(synth.kcand_case(24, 6, 9, 20000, torch.bfloat16, 1.0,
-                                   seed=21, sigma_t=2.0, sigma_d=1.0,
-                                   sigma_k=0.7))
-    with api.tuned(kcand_prefetch=1):
-        g = run(c)
-    compare(g, kc_oracle(c), extra_equal=("k", "n_per_cand"))
-    assert torch.equal(g["n_per_cand"], run(c)["n_per_cand"])
-
-
 def test_plain_load_kernel_on_aligned_rows():
     """SD_TUNE_KCAND_RING 0 sends aligned rows to the plain-load kernel."""
     c = to_device(synth.kcand_case(16, 4, 5, 4096, torch.bfloat16, 0.8,
