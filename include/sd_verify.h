@@ -162,6 +162,10 @@ int sd_tune_get(sd_tune key);
  *       token was drawn from (one-hot when T == 0).  Costs an extra pass.
  * The call reads only the rows the method needs: target rows 0..n, draft
  * rows 0..min(n, gamma-1).
+ * Workspace: sd_verify_linear_workspace(B, gamma, V, dt) bytes.  Which of
+ * the two paths runs (every row's statistics in one launch, or one cluster
+ * walk per sequence) depends on the sizes, the pointers' alignment and
+ * SD_TUNE_ALLROWS only, never on scratch handed over beyond that figure.
  * ------------------------------------------------------------------- */
 size_t sd_verify_linear_workspace(int B, int gamma, int V, sd_dtype dt);
 

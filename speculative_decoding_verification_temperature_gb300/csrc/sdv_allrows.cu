@@ -275,13 +275,15 @@ void ar_pick(bool greedy, ARKernel *stats, ARKernel *decide) {
 
 }  // namespace
 
-// Bytes of workspace the path may need at these sizes (0 when it would not
-// be taken); sampling rows assumed.
+// Bytes of workspace the path may need at these sizes under any setting of
+// SD_TUNE_ALLROWS (0 when it can never be taken); sampling rows assumed.
+// The path is chosen from the sizes and that switch alone, never from how
+// much scratch a caller hands over beyond this figure, so every entry that
+// sizes its scratch by the query takes the same path.
 size_t allrows_workspace(int B, int gamma, int V, sd_dtype dt) {
+  (void)dt;
   if (B <= 0 || V <= 0 || gamma < 0) return 0;
-  const int eb = dt == SD_F32 ? 4 : 2;
   const int rows = 2 * gamma + 1;
-  if ((long long)B * rows * V * eb > kARMaxBytes) return 0;
   const size_t w = ar_ws_bytes(B, rows, ar_smax(V));  // V >= nvec
   return w <= kARMaxWs ? w : 0;
 }
@@ -302,7 +304,8 @@ bool use_allrows(int B, int gamma, int V, sd_dtype dt, const void *target,
   const int rows = gamma + 1 + (greedy ? 0 : gamma);
   if (nvec > kARMaxVecs) return false;
   const size_t need = ar_ws_bytes(B, rows, ar_smax(nvec));
-  if (need > kARMaxWs || need > ws_bytes) return false;
+  const size_t query = allrows_workspace(B, gamma, V, dt);  // >= need if > 0
+  if (query == 0 || need > query || need > ws_bytes) return false;
   return mode == 2 || (long long)B * rows * V * eb <= kARMaxBytes;
 }
 

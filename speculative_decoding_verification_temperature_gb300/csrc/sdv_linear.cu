@@ -471,8 +471,8 @@ sd_status linear_launch(const void *target, const void *draft, sd_dtype dt,
 
 extern "C" size_t sd_verify_linear_workspace(int B, int gamma, int V,
                                              sd_dtype dt) {
-  // the work-queue counter; for small inputs the all-rows path's slice
-  // states (at most 512 KB)
+  // the work-queue counter; wherever the all-rows path could be taken (at
+  // any setting of SD_TUNE_ALLROWS), its slice states (at most 512 KB)
   const size_t w = sdv::allrows_workspace(B, gamma, V, dt);
   return w > 256 ? w : 256;
 }
