@@ -128,10 +128,7 @@ typedef enum {
   SD_TUNE_FANOUT_LDG = 7,      /* 1: fan-out with plain loads; default 0 */
   SD_TUNE_FANOUT_MAXC = 8,     /* cap on the fan-out's clusters: 0 none */
   SD_TUNE_FANOUT_L2_FIRST = 9, /* fan-out rows read evict-first: default 1 */
-  SD_TUNE_PREISSUE = 10,       /* linear verify: the next position's first
-                                  ring stages are issued before the decision
-                                  (drained unused on a rejection): 0 or 1 */
-  SD_TUNE_COUNT = 11
+  SD_TUNE_COUNT = 10
 } sd_tune;
 
 sd_status sd_tune_set(sd_tune key, int value);

@@ -48,7 +48,6 @@ std::atomic<int> g_tune[SD_TUNE_COUNT] = {
     {0},  // SD_TUNE_FANOUT_LDG
     {0},  // SD_TUNE_FANOUT_MAXC
     {1},  // SD_TUNE_FANOUT_L2_FIRST
-    {0},  // SD_TUNE_PREISSUE
 };
 
 bool tune_valid(int key, int v) {

@@ -56,7 +56,6 @@ struct LinearParams {
   int seg_bytes;   // bytes of the segment-mass array (multiple of 128)
   int slice_vecs;  // capacity of each slice buffer in 16-byte vectors (TMA)
   int spec;        // let a cluster's last sequence read ahead (0: never)
-  int preissue;    // issue the next position's first stages before deciding
 };
 
 constexpr int kMaxW = 4;  // positions per step when a cluster speculates
@@ -192,13 +191,6 @@ __global__ void __launch_bounds__(kThreads, RING ? 4 : 2)
         }
         __syncthreads();
       }
-      // the next position's first ring stages stream while the cluster
-      // decides (wasted, and drained, if this step ends the sequence)
-      if (RING && p.preissue && jend <= gamma) {
-        const char *nd =
-            (!GREEDY && jend < gamma) ? drow_of(seq, jend) : nullptr;
-        ring_preissue<kStg>(rg, trow_of(seq, jend), nd, sl);
-      }
       const int nrows = GREEDY ? np : 2 * np;
       cluster.sync();
       // every CTA merges the CL partials of every row in the same order
@@ -264,7 +256,6 @@ __global__ void __launch_bounds__(kThreads, RING ? 4 : 2)
       }
       w = (last_seq && p.spec) ? min(2 * w, kMaxW) : 1;
     }
-    if (RING && rg.pre) ring_drain(rg);  // stages issued ahead, unused
     const int n = R.n, kind = R.kind, bad_token = R.bad;
 
     if (kind == 3) {  // unusable row: outputs -1
@@ -455,7 +446,6 @@ sd_status linear_launch(const void *target, const void *draft, sd_dtype dt,
   prm.seg_bytes = (int)seg_bytes;
   prm.slice_vecs = (int)per_cta;
   prm.spec = tune(SD_TUNE_SPEC);
-  prm.preissue = tune(SD_TUNE_PREISSUE);
   if (B > nclusters) {
     if (!ws || ws_bytes < 256)
       return fail(SD_ERR_INVALID_ARG, "workspace of >= 256 bytes required");

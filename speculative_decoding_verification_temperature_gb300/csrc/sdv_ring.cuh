@@ -40,7 +40,6 @@ struct Ring {
   uint32_t epar;       // thread 0: bit s: parity of the "empty" wait due
   int32_t *dev_status;
   uint64_t policy;     // L2 cache policy of the copies (0: the default)
-  int pre;             // chunks of the next pass already issued (every thread)
 };
 
 __device__ __forceinline__ void ring_init(Ring &rg) {
@@ -55,70 +54,6 @@ __device__ __forceinline__ void ring_init(Ring &rg) {
   rg.used = 0;
   rg.epar = 0;
   rg.policy = 0;
-  rg.pre = 0;
-  __syncthreads();
-}
-
-// Chunk c of a pass over this CTA's slice of row A (and B) into stage
-// c % kStages (thread 0; the stage must be free).
-template <int STG>
-__device__ __forceinline__ void ring_issue(Ring &rg, const char *rowA,
-                                           const char *rowB, const Slice &sl,
-                                           int c) {
-  const int nv = sl.vend - sl.vbeg;
-  const int s = c % kStages;
-  const int v0 = c * STG;
-  const int cnt = min(STG, nv - v0);
-  const uint32_t bytes = (uint32_t)cnt * 16u;
-  if (!SDV_RING_SYNC && (rg.used >> s & 1u)) {  // every warp released it
-    mbar_wait(&rg.empty[s], (rg.epar >> s) & 1u, rg.dev_status);
-    rg.epar ^= 1u << s;
-  }
-  rg.used |= 1u << s;
-  fence_proxy_async();
-  mbar_expect_tx(&rg.full[s], bytes * ((STG == kStg && rowB) ? 2u : 1u));
-  if (rg.policy) {
-    bulk_g2s_hint(rg.buf + (size_t)s * kStageVecs,
-                  rowA + (size_t)(sl.vbeg + v0) * 16, bytes, &rg.full[s],
-                  rg.policy);
-    if (STG == kStg && rowB)
-      bulk_g2s_hint(rg.buf + (size_t)s * kStageVecs + kStg,
-                    rowB + (size_t)(sl.vbeg + v0) * 16, bytes, &rg.full[s],
-                    rg.policy);
-  } else {
-    bulk_g2s(rg.buf + (size_t)s * kStageVecs,
-             rowA + (size_t)(sl.vbeg + v0) * 16, bytes, &rg.full[s]);
-    if (STG == kStg && rowB)
-      bulk_g2s(rg.buf + (size_t)s * kStageVecs + kStg,
-               rowB + (size_t)(sl.vbeg + v0) * 16, bytes, &rg.full[s]);
-  }
-}
-
-// Every thread, between passes (all stages free: after the last block
-// barrier of a pass): issue the first chunks of the next pass now, so that
-// they stream while the block decides; ring_pass then skips them.  The
-// next pass must be over the same rows with the same STG.
-template <int STG = kStg>
-__device__ __forceinline__ void ring_preissue(Ring &rg, const char *rowA,
-                                              const char *rowB,
-                                              const Slice &sl) {
-  const int nv = sl.vend - sl.vbeg;
-  const int nch = (nv + STG - 1) / STG;
-  const int n = nch < kStages ? nch : kStages;
-  if (threadIdx.x == 0)
-    for (int c = 0; c < n; ++c) ring_issue<STG>(rg, rowA, rowB, sl, c);
-  rg.pre = n;
-}
-
-// Every thread: wait out chunks issued by ring_preissue that no pass will
-// use, leaving every stage free (ends with a block barrier).
-__device__ __forceinline__ void ring_drain(Ring &rg) {
-  for (int c = 0; c < rg.pre; ++c) {
-    const int s = c % kStages;
-    mbar_wait(&rg.full[s], (rg.phase >> s) & 1u, rg.dev_status);
-    rg.phase ^= 1u << s;
-  }
-  rg.pre = 0;
   __syncthreads();
 }
 
@@ -135,11 +70,35 @@ __device__ __forceinline__ void ring_pass(Ring &rg, const char *rowA,
   const int nv = sl.vend - sl.vbeg;
   const int nch = (nv + STG - 1) / STG;
   auto issue = [&](int c) {  // thread 0 only
-    ring_issue<STG>(rg, rowA, rowB, sl, c);
+    const int s = c % kStages;
+    const int v0 = c * STG;
+    const int cnt = min(STG, nv - v0);
+    const uint32_t bytes = (uint32_t)cnt * 16u;
+    if (!SDV_RING_SYNC && (rg.used >> s & 1u)) {  // every warp released it
+      mbar_wait(&rg.empty[s], (rg.epar >> s) & 1u, rg.dev_status);
+      rg.epar ^= 1u << s;
+    }
+    rg.used |= 1u << s;
+    fence_proxy_async();
+    mbar_expect_tx(&rg.full[s], bytes * ((STG == kStg && rowB) ? 2u : 1u));
+    if (rg.policy) {
+      bulk_g2s_hint(rg.buf + (size_t)s * kStageVecs,
+                    rowA + (size_t)(sl.vbeg + v0) * 16, bytes, &rg.full[s],
+                    rg.policy);
+      if (STG == kStg && rowB)
+        bulk_g2s_hint(rg.buf + (size_t)s * kStageVecs + kStg,
+                      rowB + (size_t)(sl.vbeg + v0) * 16, bytes, &rg.full[s],
+                      rg.policy);
+    } else {
+      bulk_g2s(rg.buf + (size_t)s * kStageVecs,
+               rowA + (size_t)(sl.vbeg + v0) * 16, bytes, &rg.full[s]);
+      if (STG == kStg && rowB)
+        bulk_g2s(rg.buf + (size_t)s * kStageVecs + kStg,
+                 rowB + (size_t)(sl.vbeg + v0) * 16, bytes, &rg.full[s]);
+    }
   };
   if (threadIdx.x == 0)
-    for (int c = rg.pre; c < nch && c < kStages; ++c) issue(c);
-  rg.pre = 0;
+    for (int c = 0; c < nch && c < kStages; ++c) issue(c);
   for (int c = 0; c < nch; ++c) {
     const int s = c % kStages;
     mbar_wait(&rg.full[s], (rg.phase >> s) & 1u, rg.dev_status);

@@ -131,18 +131,6 @@ def test_resid_and_accept_debug_outputs():
                                    atol=1e-5)
 
 
-@pytest.mark.parametrize("pre", [0, 1])
-def test_queue_path_stage_preissue(pre):
-    """More sequences than resident clusters, each cluster's stages issued
-    ahead of its decisions or not: identical results, equal to the
-    oracle's."""
-    c = to_device(synth.linear_case(700, 6, 20000, torch.float32, 1.0,
-                                    seed=31, sigma_t=2.0, sigma_d=1.0))
-    with api.tuned(preissue=pre, allrows=0):
-        g = run(c)
-    compare(g, linear_oracle(c))
-
-
 def test_large_workload_every_sequence():
     """B=256, gamma=8, V=128256 fp32 (the benchmark's workload and launch):
     all 256 sequences against the oracle (run over host threads), and the

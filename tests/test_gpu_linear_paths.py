@@ -2,9 +2,7 @@
 the per-position cluster kernel (SD_TUNE_ALLROWS 0) and the all-rows path
 for small inputs (SD_TUNE_ALLROWS 2 forces it wherever its workspace and
 shared memory allow), plus the cluster kernel without its read-ahead of a
-cluster's last sequence (SD_TUNE_SPEC 0) and with L2 prefetch (2), and
-with the next position's stages issued before each decision
-(SD_TUNE_PREISSUE 1).  Small and odd
+cluster's last sequence (SD_TUNE_SPEC 0) and with L2 prefetch (2).  Small and odd
 sizes, both dtypes, unaligned rows, gamma 0, T in {0, 0.7, 1}, bad tokens
 and non-finite rows, the queue path, the accept-probability output; and
 the two paths agree with each other."""
@@ -29,12 +27,10 @@ def switches(mode):
     sw = {"allrows": int(mode.split("-")[0])}
     if "-spec" in mode:
         sw["spec"] = int(mode[-1])
-    if "-pre" in mode:
-        sw["preissue"] = 1
     return sw
 
 
-@pytest.mark.parametrize("mode", ["0", "2", "0-spec0", "0-spec2", "0-pre"])
+@pytest.mark.parametrize("mode", ["0", "2", "0-spec0", "0-spec2"])
 @pytest.mark.parametrize("T", [0.0, 0.7, 1.0])
 @pytest.mark.parametrize("B,gamma,V,dtype", [
     (1, 4, 1000, torch.float32), (32, 8, 32000, torch.bfloat16),
@@ -55,7 +51,7 @@ def test_paths_against_oracle(mode, T, B, gamma, V, dtype):
         assert np.all(host(g["accept"])[~ev] == -1)
 
 
-@pytest.mark.parametrize("mode", ["0", "2", "0-spec0", "0-spec2", "0-pre"])
+@pytest.mark.parametrize("mode", ["0", "2", "0-spec0", "0-spec2"])
 def test_paths_edge_rows(mode):
     c = synth.linear_case(8, 4, 2000, torch.float32, 1.0, seed=77)
     c.tokens[1, 0] = 10**6            # bad token, tested first
@@ -75,7 +71,7 @@ def test_paths_agree():
     """Away from the flagged draws the two paths return the same tokens."""
     c = to_device(synth.linear(1.0))
     outs = []
-    for mode in ("0", "2", "0-spec0", "0-spec2", "0-pre"):
+    for mode in ("0", "2", "0-spec0", "0-spec2"):
         with api.tuned(**switches(mode)):
             outs.append(run(c))
     o = linear_oracle(c)
