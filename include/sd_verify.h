@@ -128,7 +128,10 @@ typedef enum {
   SD_TUNE_FANOUT_LDG = 7,      /* 1: fan-out with plain loads; default 0 */
   SD_TUNE_FANOUT_MAXC = 8,     /* cap on the fan-out's clusters: 0 none */
   SD_TUNE_FANOUT_L2_FIRST = 9, /* fan-out rows read evict-first: default 1 */
-  SD_TUNE_COUNT = 10
+  SD_TUNE_HELPERS = 10,        /* linear verify: clusters with no sequence
+                                  left compute row statistics ahead of the
+                                  scans still running: 0 or 1 (default 1) */
+  SD_TUNE_COUNT = 11
 } sd_tune;
 
 sd_status sd_tune_set(sd_tune key, int value);
@@ -157,8 +160,11 @@ int sd_tune_get(sd_tune key);
  *       rejection (never tested: their logits are never read).
  *   out_resid [B, V] (nullable, debug): the normalised distribution the last
  *       token was drawn from (one-hot when T == 0).  Costs an extra pass.
- * The call reads only the rows the method needs: target rows 0..n, draft
- * rows 0..min(n, gamma-1).
+ * The scan reads only the rows the method needs: target rows 0..n, draft
+ * rows 0..min(n, gamma-1).  With SD_TUNE_HELPERS on (the default), clusters
+ * that have no sequence left also read rows ahead of the scans still
+ * running (rows of positions up to gamma), so that a scan finds them done;
+ * the results are the same bits either way.
  * Workspace: sd_verify_linear_workspace(B, gamma, V, dt) bytes.  Which of
  * the two paths runs (every row's statistics in one launch, or one cluster
  * walk per sequence) depends on the sizes, the pointers' alignment and

@@ -102,7 +102,7 @@ def version() -> str:
 
 TUNE = {"cluster": 0, "no_tma": 1, "allrows": 2, "spec": 3, "fused": 4,
         "kcand_ring": 5, "fanout_cluster": 6, "fanout_ldg": 7,
-        "fanout_maxc": 8, "fanout_l2_first": 9}
+        "fanout_maxc": 8, "fanout_l2_first": 9, "helpers": 10}
 """Tuning switches of sd_tune_set, by name (see include/sd_verify.h)."""
 
 

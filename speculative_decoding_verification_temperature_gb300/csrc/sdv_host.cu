@@ -48,6 +48,7 @@ std::atomic<int> g_tune[SD_TUNE_COUNT] = {
     {0},  // SD_TUNE_FANOUT_LDG
     {0},  // SD_TUNE_FANOUT_MAXC
     {1},  // SD_TUNE_FANOUT_L2_FIRST
+    {1},  // SD_TUNE_HELPERS
 };
 
 bool tune_valid(int key, int v) {

@@ -56,9 +56,48 @@ struct LinearParams {
   int seg_bytes;   // bytes of the segment-mass array (multiple of 128)
   int slice_vecs;  // capacity of each slice buffer in 16-byte vectors (TMA)
   int spec;        // let a cluster's last sequence read ahead (0: never)
+  // Helping (all null when off).  Once the work counter is exhausted, a
+  // cluster with nothing left to verify computes row statistics for the
+  // sequences other clusters are still scanning: each of its CTAs takes a
+  // position ahead of a running scan, computes its own slice's partial of
+  // that position's rows (the same code and slice as the owner's CTA of the
+  // same rank, hence the same bits), stores it and raises a flag.  An owner
+  // CTA that finds the flag of its slice raised copies the partial instead
+  // of streaming the slice.  Nobody ever waits on a flag.
+  int *helping;     // set once a cluster has started helping
+  int *active;      // [nclusters]: sequence + 1 being verified, or 0
+  int *opos;        // [B]: the owner's current position
+  int *hpos;        // [B][kHelpRanks]: next position to hand to a helper
+  int *hflag;       // [B][gamma+1][kHelpRanks]: partial published
+  uint4 *hpart;     // [B][gamma+1][kHelpRanks]: the partials
 };
 
+constexpr int kHelpRanks = 16;  // record stride: the largest cluster
+
 constexpr int kMaxW = 4;  // positions per step when a cluster speculates
+
+// GPU-scope accesses for the helping records (plain loads could be served
+// from a stale L1 line)
+__device__ __forceinline__ int ld_acquire_gpu(const int *a) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(a)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ int ld_relaxed_gpu(const int *a) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(a)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu(int *a, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(a), "r"(v)
+               : "memory");
+}
+__device__ __forceinline__ void st_relaxed_gpu(int *a, int v) {
+  asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(a), "r"(v)
+               : "memory");
+}
 
 struct StepResult {
   int kind;   // 0 continue, 1 reject at n, 2 bonus, 3 unusable row
@@ -79,6 +118,16 @@ struct LinearSmem {
   MS mrg[2 * kMaxW];      // merged stats of this step's rows
   AM amrg[kMaxW];
   int next_seq[2];
+  // helping: flags of this step's positions, consecutive published
+  // positions after the step (this CTA's slice; peers read it), the
+  // cluster's minimum of those, a helper's assignment
+  int hready[kMaxW];
+  uint4 hv[kMaxW];  // the published partials of this step's positions
+  int rcnt[2];
+  int wready;
+  int hseen[2];  // rank 0: the helping flag as read at the step's start
+  int hnext;     // rank 0's, read by every CTA after the step's barrier
+  int hs, hj;
   // gathered for the accept tests of this step's positions
   int gx[kMaxW];
   float gzt[kMaxW], gzd[kMaxW], gr[kMaxW];
@@ -117,13 +166,46 @@ __global__ void __launch_bounds__(kThreads, RING ? 4 : 2)
   auto drow_of = [&](int s, int j) {
     return dbase + ((size_t)s * p.d_seq_rows + j) * rowb;
   };
+  // this CTA's partial of position j of sequence s, valid at thread 0:
+  // (max, sum) of the target and the draft row, or the target's argmax
+  auto slice_stats = [&](int s, int j) -> uint4 {
+    const char *trow = trow_of(s, j);
+    if constexpr (GREEDY) {
+      AM a = am_empty();
+      if constexpr (RING) ring_argmax<DT, VW>(rg, trow, sl, a);
+      else argmax_pass<DT, VW>(GR{trow}, sl, a);
+      a = block_reduce_am(a, sh.ared);
+      return make_uint4(__float_as_uint(a.v), (unsigned)a.i, (unsigned)a.bad,
+                        0u);
+    } else {
+      const bool has_d = j < gamma;
+      const char *drow = has_d ? drow_of(s, j) : nullptr;
+      MS st[2] = {ms_empty(), ms_empty()};
+      if constexpr (RING) {
+        ring_stats<DT, VW>(rg, trow, drow, sl, k2, st[0], st[1]);
+      } else {
+        stats_pass<DT, VW>(GR{trow}, GR{drow}, has_d, sl, k2, st[0], st[1]);
+      }
+      block_reduce_ms<2>(st, k2, sh.red);
+      return make_uint4(__float_as_uint(st[0].m), __float_as_uint(st[0].s),
+                        __float_as_uint(st[1].m), __float_as_uint(st[1].s));
+    }
+  };
+  const bool help = p.hflag != nullptr;
+  const int cid = (int)(blockIdx.x / CL);
+  auto hrec = [&](int s, int j) {  // index of this CTA's record
+    return ((size_t)s * (gamma + 1) + j) * kHelpRanks + rank;
+  };
+  bool hmode = false;  // helpers are running: look for their partials
 
   int par = 0, seqpar = 0;
   int seq = (int)(blockIdx.x / CL);
   while (seq < p.B) {
-    if (rank == 0 && tid == 0)
+    if (rank == 0 && tid == 0) {
       sh.next_seq[seqpar] =
           p.queue ? p.nclusters + atomicAdd(p.queue, 1) : p.B;
+      if (help) st_relaxed_gpu(p.active + cid, seq + 1);
+    }
     // ---------------- scan: positions [i, i + w) per step -----------------
     // w stays 1 while the work counter still hands out sequences; once this
     // cluster holds its last sequence (nothing else to overlap with), w
@@ -154,6 +236,22 @@ __global__ void __launch_bounds__(kThreads, RING ? 4 : 2)
         sh.gzd[tid - 32] = zd;
         sh.gr[tid - 32] = r;
       }
+      if (help) {
+        if (tid == 63 && rank == 0) sh.hseen[par] = ld_relaxed_gpu(p.helping);
+        if (tid == 0) {  // the owner computes [i, jend) unless published
+          atomicMax(p.hpos + (size_t)seq * kHelpRanks + rank, jend);
+          if (rank == 0) st_relaxed_gpu(p.opos + seq, i);
+        }
+        if (hmode) {
+          if (tid < np) {  // each lane reads its record after its flag
+            const size_t rec = hrec(seq, i + tid);
+            const int f = ld_acquire_gpu(p.hflag + rec);
+            sh.hready[tid] = f;
+            if (f) sh.hv[tid] = __ldcg(p.hpart + rec);
+          }
+          __syncthreads();
+        }
+      }
       if (RING && last_seq && p.spec >= 2 && tid == 0) {
         // the GPU is emptying out: ask for this step's and the next step's
         // rows at once (into L2), so the ring below streams from L2
@@ -166,30 +264,29 @@ __global__ void __launch_bounds__(kThreads, RING ? 4 : 2)
         }
       }
       for (int t = 0; t < np; ++t) {
-        const int j = i + t;
-        const bool has_d = (!GREEDY) && j < gamma;
-        const char *trow = trow_of(seq, j);
-        const char *drow = has_d ? drow_of(seq, j) : nullptr;
-        if constexpr (GREEDY) {
-          AM a = am_empty();
-          if constexpr (RING) ring_argmax<DT, VW>(rg, trow, sl, a);
-          else argmax_pass<DT, VW>(GR{trow}, sl, a);
-          a = block_reduce_am(a, sh.ared);
-          if (tid == 0) sh.apart[par][t] = a;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (hmode && sh.hready[t]) {
+          v = sh.hv[t];
         } else {
-          MS st[2] = {ms_empty(), ms_empty()};
-          if constexpr (RING) {
-            ring_stats<DT, VW>(rg, trow, drow, sl, k2, st[0], st[1]);
+          v = slice_stats(seq, i + t);
+        }
+        if (tid == 0) {
+          if constexpr (GREEDY) {
+            sh.apart[par][t] = AM{__uint_as_float(v.x), (int)v.y, (int)v.z};
           } else {
-            stats_pass<DT, VW>(GR{trow}, GR{drow}, has_d, sl, k2, st[0], st[1]);
-          }
-          block_reduce_ms<2>(st, k2, sh.red);
-          if (tid == 0) {
-            sh.part[par][2 * t] = st[0];
-            sh.part[par][2 * t + 1] = st[1];
+            sh.part[par][2 * t] = MS{__uint_as_float(v.x), __uint_as_float(v.y)};
+            sh.part[par][2 * t + 1] =
+                MS{__uint_as_float(v.z), __uint_as_float(v.w)};
           }
         }
         __syncthreads();
+      }
+      if (hmode && warp == 0) {  // published positions right after the step
+        const int j = jend + lane;
+        const bool ok = lane < kMaxW && j <= gamma &&
+                        ld_acquire_gpu(p.hflag + hrec(seq, j)) != 0;
+        const unsigned m = __ballot_sync(0xffffffffu, ok);
+        if (lane == 0) sh.rcnt[par] = __ffs(~m) - 1;
       }
       const int nrows = GREEDY ? np : 2 * np;
       cluster.sync();
@@ -207,6 +304,16 @@ __global__ void __launch_bounds__(kThreads, RING ? 4 : 2)
           if (lane == 0) sh.mrg[r] = m;
         }
       }
+      if (hmode && warp == kWarps - 1) {
+        int c = kMaxW;
+        if (lane < CL) c = cluster.map_shared_rank(&sh, lane)->rcnt[par];
+        for (int o = 16; o; o >>= 1) c = min(c, __shfl_xor_sync(0xffffffffu, c, o));
+        if (lane == 0) sh.wready = c;
+      }
+      // every CTA takes rank 0's reading, so the whole cluster switches to
+      // looking for published partials at the same step
+      if (help && !hmode && tid == kThreads - 32)
+        sh.hnext = cluster.map_shared_rank(&sh, 0)->hseen[par];
       __syncthreads();
       par ^= 1;
       if (tid == 0) {  // the accept tests of this step, in position order
@@ -255,6 +362,8 @@ __global__ void __launch_bounds__(kThreads, RING ? 4 : 2)
         first = false;
       }
       w = (last_seq && p.spec) ? min(2 * w, kMaxW) : 1;
+      if (hmode) w = max(w, sh.wready);
+      if (help && !hmode) hmode = sh.hnext != 0;
     }
     const int n = R.n, kind = R.kind, bad_token = R.bad;
 
@@ -345,10 +454,63 @@ __global__ void __launch_bounds__(kThreads, RING ? 4 : 2)
         write_resid<DT, VW>(p.out_resid + (size_t)seq * V, ra, rb, has_q, W,
                             sl, o.N);
     }
+    if (help && tid == 0)  // no more helpers for this sequence
+      atomicMax(p.hpos + (size_t)seq * kHelpRanks + rank, gamma + 1);
     // next sequence (rank 0 published it before this sequence's first sync)
     seq = cluster.map_shared_rank(&sh, 0)->next_seq[seqpar];
     seqpar ^= 1;
     __syncthreads();
+  }
+  if (help) {
+    // Nothing left to verify: compute this CTA's slice of positions ahead
+    // of the scans still running, nearest to its owner's position first.
+    if (tid == 0) {
+      if (rank == 0) st_relaxed_gpu(p.active + cid, 0);
+      st_relaxed_gpu(p.helping, 1);
+    }
+    for (int round = 0; round < (gamma + 1) * p.B; ++round) {
+      if (warp == 0) {  // candidates: the sequences clusters published
+        int bs = -1, bpri = 0x7fffffff;
+        for (int c = lane; c < p.nclusters; c += 32) {
+          const int a = ld_relaxed_gpu(p.active + c);
+          if (a <= 0) continue;
+          const int s = a - 1;
+          const int h = ld_relaxed_gpu(p.hpos + (size_t)s * kHelpRanks + rank);
+          if (h > gamma) continue;
+          const int pri = h - ld_relaxed_gpu(p.opos + s);
+          if (pri < bpri) { bpri = pri; bs = s; }
+        }
+        for (int o = 16; o; o >>= 1) {  // lowest priority, then lowest s
+          const int op = __shfl_xor_sync(0xffffffffu, bpri, o);
+          const int os = __shfl_xor_sync(0xffffffffu, bs, o);
+          if (op < bpri || (op == bpri && (unsigned)os < (unsigned)bs)) {
+            bpri = op;
+            bs = os;
+          }
+        }
+        if (lane == 0) {
+          int j = gamma + 1;
+          if (bs >= 0) {  // position 0 is always the owner's own
+            int *hp = p.hpos + (size_t)bs * kHelpRanks + rank;
+            j = atomicAdd(hp, 1);
+            if (j == 0) j = atomicAdd(hp, 1);
+          }
+          sh.hs = bs;
+          sh.hj = j;
+        }
+      }
+      __syncthreads();
+      const int s = sh.hs, j = sh.hj;
+      if (s < 0) break;
+      if (j <= gamma) {
+        const uint4 v = slice_stats(s, j);
+        if (tid == 0) {
+          __stcg(p.hpart + hrec(s, j), v);
+          st_release_gpu(p.hflag + hrec(s, j), 1);
+        }
+      }
+      __syncthreads();
+    }
   }
   cluster.sync();  // no CTA leaves while a peer may still read its smem
 }
@@ -375,6 +537,38 @@ static LinearKernel pick_linear(int dt, bool vec, bool ring, bool greedy) {
 }
 
 size_t allrows_workspace(int B, int gamma, int V, sd_dtype dt);
+
+// Workspace layout: the work counter (byte 0) and the helping flag (byte 4)
+// in the first 256 bytes, then the helping records; everything before the
+// partials is cleared on the stream before each launch.
+struct HelpLayout {
+  size_t active, opos, hpos, hflag, hpart, zero_end, total;
+};
+constexpr int kHelpMaxClusters = 1024;
+constexpr size_t kHelpMaxWs = 768 << 10;
+
+static HelpLayout help_layout(int B, int gamma) {
+  auto r256 = [](size_t x) { return (x + 255) / 256 * 256; };
+  const size_t recs = (size_t)B * (gamma + 1) * kHelpRanks;
+  HelpLayout L;
+  L.active = 256;
+  L.opos = L.active + r256((size_t)kHelpMaxClusters * 4);
+  L.hpos = L.opos + r256((size_t)B * 4);
+  L.hflag = L.hpos + r256((size_t)B * kHelpRanks * 4);
+  L.hpart = L.hflag + r256(recs * 4);
+  L.zero_end = L.hpart;
+  L.total = L.hpart + recs * 16;
+  return L;
+}
+
+// Bytes the helping records need (0: too many sequences x positions; the
+// call then runs without helping).
+size_t help_workspace(int B, int gamma) {
+  if (B <= 0 || gamma < 0) return 0;
+  const size_t t = help_layout(B, gamma).total;
+  return t <= kHelpMaxWs ? t : 0;
+}
+
 bool use_allrows(int B, int gamma, int V, sd_dtype dt, const void *target,
                  const void *draft, float T, const float *out_resid,
                  size_t ws_bytes);
@@ -425,6 +619,14 @@ sd_status linear_launch(const void *target, const void *draft, sd_dtype dt,
   st = max_active_clusters((const void *)kern, CL, smem, &maxc);
   if (st != SD_OK) return st;
   const int nclusters = B < maxc ? B : maxc;
+  // helping, in the tail of the work counter only (measured at B = 8..64
+  // sequences of 128256 fp32 columns: extra clusters helping from the start
+  // slowed the owners down by 5-16 %; at B = 128 and 256 helping in the
+  // tail took 2-6 % off)
+  const size_t hws = help_workspace(B, gamma);
+  const bool helpers = tune(SD_TUNE_HELPERS) != 0 && B > nclusters &&
+                       hws != 0 && ws && ws_bytes >= hws &&
+                       CL <= kHelpRanks && nclusters <= kHelpMaxClusters;
   LinearParams prm;
   prm.target = target;
   prm.draft = draft;
@@ -446,10 +648,24 @@ sd_status linear_launch(const void *target, const void *draft, sd_dtype dt,
   prm.seg_bytes = (int)seg_bytes;
   prm.slice_vecs = (int)per_cta;
   prm.spec = tune(SD_TUNE_SPEC);
+  prm.helping = prm.active = prm.opos = prm.hpos = prm.hflag = nullptr;
+  prm.hpart = nullptr;
   if (B > nclusters) {
     if (!ws || ws_bytes < 256)
       return fail(SD_ERR_INVALID_ARG, "workspace of >= 256 bytes required");
     prm.queue = static_cast<int *>(ws);
+  }
+  if (helpers) {
+    const HelpLayout L = help_layout(B, gamma);
+    char *w = static_cast<char *>(ws);
+    prm.helping = reinterpret_cast<int *>(w + 4);
+    prm.active = reinterpret_cast<int *>(w + L.active);
+    prm.opos = reinterpret_cast<int *>(w + L.opos);
+    prm.hpos = reinterpret_cast<int *>(w + L.hpos);
+    prm.hflag = reinterpret_cast<int *>(w + L.hflag);
+    prm.hpart = reinterpret_cast<uint4 *>(w + L.hpart);
+    SDV_CUDA(cudaMemsetAsync(ws, 0, L.zero_end, stream));
+  } else if (prm.queue) {
     SDV_CUDA(cudaMemsetAsync(ws, 0, sizeof(int), stream));
   }
   void *args[] = {&prm};
@@ -461,9 +677,12 @@ sd_status linear_launch(const void *target, const void *draft, sd_dtype dt,
 
 extern "C" size_t sd_verify_linear_workspace(int B, int gamma, int V,
                                              sd_dtype dt) {
-  // the work-queue counter; wherever the all-rows path could be taken (at
-  // any setting of SD_TUNE_ALLROWS), its slice states (at most 512 KB)
-  const size_t w = sdv::allrows_workspace(B, gamma, V, dt);
+  // the work counter and, up to 768 KB, the helping records; wherever the
+  // all-rows path could be taken (at any setting of SD_TUNE_ALLROWS), its
+  // slice states (at most 512 KB)
+  const size_t a = sdv::allrows_workspace(B, gamma, V, dt);
+  const size_t h = sdv::help_workspace(B, gamma);
+  const size_t w = a > h ? a : h;
   return w > 256 ? w : 256;
 }
 
