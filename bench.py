@@ -110,7 +110,8 @@ class ClockSampler:
 # (profiles/), with the units that launch processed: the fan-out reads every
 # row once, so its traffic scales with the rows; the verify's with the bytes
 # the method needs (its early exit decides how many rows it reads).
-TRAFFIC = {"fanout": (591.25e6, 128 * 9), "linear": (421.20e6, 343.73e6)}
+TRAFFIC = {"fanout": (591.25e6, 128 * 9), "linear": (421.20e6, 343.73e6),
+           "fused": (1008.3e6, 763.89e6)}
 
 
 def hbm_peak():
@@ -182,6 +183,12 @@ def gpu_arm(args, rank, world):
     def fanout(c):
         return api.fanout_topk(c.draft, F, workspace=ws_f)
 
+    ws_x = api.Workspace()
+
+    def fused(c):  # the verify and the fan-out in one launch
+        return api.verify_linear_fanout(c.target, c.draft, c.tokens,
+                                        c.uniforms, T, F, workspace=ws_x)
+
     # bytes the method needs per set (deterministic outputs): target rows
     # 0..n of every sequence and all K+1 draft rows (the fan-out reads them
     # all; the verify's draft rows are a subset)
@@ -194,25 +201,30 @@ def gpu_arm(args, rank, world):
     for i in range(args.warmup):
         verify(sets[i % len(sets)])
         fanout(sets[i % len(sets)])
+        fused(sets[i % len(sets)])
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    # the step: the fan-out on a second stream beside the verify (the two
-    # read the same draft rows but write nothing in common; each has its own
-    # workspace), joined before the next step; the verify's decision and
-    # draw phases leave HBM time that the fan-out's streaming fills
     side = torch.cuda.Stream(dev)
 
-    def step(c):
-        fork = torch.cuda.Event()
-        fork.record(stream)
-        side.wait_event(fork)
-        with torch.cuda.stream(side):
-            fanout(c)
-        verify(c)
-        join = torch.cuda.Event()
-        join.record(side)
-        stream.wait_event(join)
+    if args.step == "fused":
+        # the step: sd_verify_linear_fanout, one launch; CTAs left without a
+        # sequence to verify take the fan-out's rows
+        def step(c):
+            fused(c)
+    else:
+        # the two calls, the fan-out on a second stream beside the verify
+        # (each with its own workspace), joined before the next step
+        def step(c):
+            fork = torch.cuda.Event()
+            fork.record(stream)
+            side.wait_event(fork)
+            with torch.cuda.stream(side):
+                fanout(c)
+            verify(c)
+            join = torch.cuda.Event()
+            join.record(side)
+            stream.wait_event(join)
 
     for i in range(args.warmup):
         step(sets[i % len(sets)])
@@ -267,8 +279,14 @@ def gpu_arm(args, rank, world):
     fan_bytes = B * (FAN["K"] + 1) * V * ELT
     tensor_bytes = B * (GAMMA + 1) * V * ELT + fan_bytes
     peak, src = hbm_peak()
-    # dominant kernel: the larger of the two shares of the step
-    if ms_v >= ms_f:
+    # dominant kernel: the fused launch (the whole step), else the larger of
+    # the two calls' shares
+    if args.step == "fused":
+        kern, kb, kms = ("linear_verify_kernel<0,4,false,true,true> (fused "
+                         "with the fan-out)", need_avg, ms)
+        traffic = (TRAFFIC["fused"][0] / TRAFFIC["fused"][1] * need_avg
+                   if TRAFFIC.get("fused") else None)
+    elif ms_v >= ms_f:
         kern, kb, kms = "linear_verify_kernel<0,4,false,true>", need_v_avg, ms_v
         traffic = TRAFFIC["linear"][0] / TRAFFIC["linear"][1] * need_v_avg
     else:
@@ -282,8 +300,10 @@ def gpu_arm(args, rank, world):
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": workload_name(), "B": B, "gamma": GAMMA, "V": V,
                    "T": T, "fanout_F": F, "input_sets": len(sets),
-                   "step": "sd_verify_linear with sd_fanout_topk on a "
-                           "second stream (joined each step)",
+                   "step": ("sd_verify_linear_fanout: the verify and the "
+                            "fan-out in one launch" if args.step == "fused"
+                            else "sd_verify_linear with sd_fanout_topk on a "
+                                 "second stream (joined each step)"),
                    "l2": "inputs %.2f GB per set (> 129 MB L2), %d sets "
                          "rotated" % (2 * B * (GAMMA + 1) * V * ELT / 1e9,
                                       len(sets)),
@@ -309,7 +329,7 @@ def gpu_arm(args, rank, world):
                    "gbs": need_v_avg / (ms_v / 1e3) / 1e9},
         "fanout": {"ms": ms_f, "bytes": fan_bytes,
                    "gbs": fan_bytes / (ms_f / 1e3) / 1e9},
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": (1 if args.step == "fused" else 2) * args.steps,
         "tuning": {k: api.tune_get(k) for k in api.TUNE},
         "clocks": clk,
         "wall_s": wall,
@@ -321,8 +341,11 @@ def gpu_arm(args, rank, world):
         res["other_workloads"] = other_workloads(args, dev, peak, checks)
     if rank == 0 and args.oracle_seqs > 0:
         c = sets[0]
-        g = {k: v.cpu().numpy() for k, v in verify(c).items()}
-        g["fan_tokens"] = fanout(c)["tokens"].cpu().numpy()
+        if args.step == "fused":
+            g = {k: v.cpu().numpy() for k, v in fused(c).items()}
+        else:
+            g = {k: v.cpu().numpy() for k, v in verify(c).items()}
+            g["fan_tokens"] = fanout(c)["tokens"].cpu().numpy()
         res["cpu_baseline"], res["flagged"] = cpu_baseline(
             sets, args.oracle_seqs, F, g)
         res["flagged"]["what"] = (
@@ -375,14 +398,21 @@ def e2e_arm(args, sets, dev, ws, world, F):
                 d[s][k].copy_(h[k], non_blocking=True)
         copied[s].record(copy)
 
+    wsx = api.Workspace()
+
     def step(i):
         s = i % 2
         stream.wait_event(copied[s])
-        dv[s].copy_(d[s]["draft"][:, :GAMMA])
-        o = api.verify_linear(d[s]["target"], dv[s], d[s]["tokens"],
-                              d[s]["uniforms"], T, workspace=ws)
-        o["fan_tokens"] = api.fanout_topk(d[s]["draft"], F,
-                                          workspace=ws)["tokens"]
+        if args.step == "fused":
+            o = api.verify_linear_fanout(d[s]["target"], d[s]["draft"],
+                                         d[s]["tokens"], d[s]["uniforms"], T,
+                                         F, workspace=wsx)
+        else:
+            dv[s].copy_(d[s]["draft"][:, :GAMMA])
+            o = api.verify_linear(d[s]["target"], dv[s], d[s]["tokens"],
+                                  d[s]["uniforms"], T, workspace=ws)
+            o["fan_tokens"] = api.fanout_topk(d[s]["draft"], F,
+                                              workspace=ws)["tokens"]
         used[s].record(stream)
         for k in out_h:
             out_h[k].copy_(o[k], non_blocking=True)
@@ -1042,6 +1072,9 @@ def main():
     ap.add_argument("--aux-steps", type=int, default=30,
                     help="timed rounds of each of the other workloads "
                          "(0: skip them)")
+    ap.add_argument("--step", choices=("fused", "streams"), default="fused",
+                    help="the large step: one sd_verify_linear_fanout launch "
+                         "(default), or the two calls on two streams")
     ap.add_argument("--tune", action="append", default=[],
                     metavar="NAME=VALUE",
                     help="set a library tuning switch (sd_tune_set) before "

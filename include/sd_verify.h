@@ -120,8 +120,8 @@ typedef enum {
                                   2 wherever its scratch fits */
   SD_TUNE_SPEC = 3,            /* a cluster's last sequence reads ahead: 0
                                   never, 1 (default), 2 also L2 prefetch */
-  SD_TUNE_FUSED = 4,           /* sd_verify_linear_fanout: 0 the two calls
-                                  (default), 1 the fused kernel */
+  SD_TUNE_FUSED = 4,           /* sd_verify_linear_fanout: 1 one launch
+                                  (default), 0 the two calls */
   SD_TUNE_KCAND_RING = 5,      /* 0: K-candidate verify without the TMA
                                   ring; default 1 */
   SD_TUNE_FANOUT_CLUSTER = 6,  /* fan-out CTAs per cluster: 0 chosen */
@@ -477,7 +477,12 @@ sd_status sd_fanout_hits(const int32_t *n_accepted, const int32_t *out_tokens,
 
 /* ---------------------------------------------------------------------
  * Linear verify fused with the fan-out of the same draft logits, in one
- * pass over each draft row (the two calls above, same results).
+ * launch (the two calls above, same results): the scans of
+ * sd_verify_linear, and every CTA left without a sequence to verify (and
+ * every resident cluster beyond the B sequences) computes whole fan-out
+ * rows, so the fan-out fills the GPU while the last scans finish.  Rows
+ * that are not 16-byte aligned (or SD_TUNE_FUSED 0) take the two calls one
+ * after the other.
  *
  * draft_logits [B, K+1, V] with K == gamma: rows 0..gamma-1 are the draft
  * rows of the verify, all K+1 rows feed the fan-out.  Other arguments as in

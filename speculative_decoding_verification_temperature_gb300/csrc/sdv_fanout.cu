@@ -11,8 +11,7 @@
 // warps' lists are ranked together, and for clusters of several CTAs rank 0
 // merges the slice lists read through distributed shared memory.
 #include "sdv_host.cuh"
-#include "sdv_ring.cuh"
-#include "sdv_topf.cuh"
+#include "sdv_fanrow.cuh"
 
 namespace sdv {
 
@@ -60,35 +59,6 @@ __device__ __forceinline__ void filter_pass(const char *row, const Slice &sl,
       wf_offer<DT, VW>(w, cta_th, x[u], v < sl.vend, v * VW);
     }
   }
-}
-
-// The same through the TMA ring in chunks of kStageVecs vectors: warp w
-// takes vectors 32 w .. 32 w + 31, 32 (w + kWarps) .., ... of every chunk.
-template <int DT, int VW>
-__device__ __forceinline__ void filter_pass_ring(Ring &rg, const char *row,
-                                                 const Slice &sl,
-                                                 WarpFilter &w,
-                                                 uint32_t *cta_th) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  ring_pass<kStageVecs>(rg, row, nullptr, sl, [&](const uint4 *A,
-                                                  const uint4 *, int v0,
-                                                  int n) {
-    wf_sync(w, cta_th);
-    if (n == kStageVecs) {  // full chunk: no idle lanes
-#pragma unroll 2
-      for (int base = warp * 32; base < kStageVecs; base += kThreads) {
-        const int i = base + lane;
-        wf_offer<DT, VW>(w, cta_th, sget<DT, VW>(A, i), true, (v0 + i) * VW);
-      }
-    } else {
-      for (int base = warp * 32; base < n; base += kThreads) {  // warp-uniform
-        const int i = base + lane;
-        Raw<DT, VW> r{};
-        if (i < n) r = sget<DT, VW>(A, i);
-        wf_offer<DT, VW>(w, cta_th, r, i < n, (v0 + i) * VW);
-      }
-    }
-  });
 }
 
 // Select the exact top-F of a row over a cluster and (rank 0) write it.

@@ -42,7 +42,7 @@ std::atomic<int> g_tune[SD_TUNE_COUNT] = {
     {0},  // SD_TUNE_NO_TMA
     {1},  // SD_TUNE_ALLROWS
     {1},  // SD_TUNE_SPEC
-    {0},  // SD_TUNE_FUSED
+    {1},  // SD_TUNE_FUSED
     {1},  // SD_TUNE_KCAND_RING
     {0},  // SD_TUNE_FANOUT_CLUSTER
     {0},  // SD_TUNE_FANOUT_LDG

@@ -27,6 +27,7 @@
 #include <type_traits>
 
 #include "sdv_device.cuh"
+#include "sdv_fanrow.cuh"
 #include "sdv_host.cuh"
 #include "sdv_ring.cuh"
 #include "sdv_tma.cuh"
@@ -70,6 +71,16 @@ struct LinearParams {
   int *hpos;        // [B][kHelpRanks]: next position to hand to a helper
   int *hflag;       // [B][gamma+1][kHelpRanks]: partial published
   uint4 *hpart;     // [B][gamma+1][kHelpRanks]: the partials
+  // Fused fan-out (the FAN kernels; sd_verify_linear_fanout).  Draft row j
+  // of every sequence (j = 0..gamma, the draft tensor holding gamma + 1
+  // rows) gets its exact top-fF[j] keys.  A CTA with no sequence left to
+  // verify takes whole rows from the row counter, one CTA per row, the
+  // sequences handed out last first (their rows were read most recently).
+  int32_t *fan_tokens;  // [B, ftotal]
+  float *fan_logit;     // nullable
+  int fF[SD_MAX_K + 1], foff[SD_MAX_K + 1];
+  int ftotal;
+  int *fq;  // the row counter
 };
 
 constexpr int kHelpRanks = 16;  // record stride: the largest cluster
@@ -135,11 +146,20 @@ struct LinearSmem {
   DrawSmem draw;
 };
 
-template <int DT, int VW, bool GREEDY, bool RING>
+// The FAN kernels' shared memory: a row's top-F and the filters' state.
+struct LinearSmemFan : LinearSmem {
+  uint64_t fout[SD_MAX_FANOUT];
+  uint32_t fth;  // the warp filters' CTA threshold
+  int fitem;
+};
+
+template <int DT, int VW, bool GREEDY, bool RING, bool FAN = false>
 __global__ void __launch_bounds__(kThreads, RING ? 4 : 2)
     linear_verify_kernel(const LinearParams p) {
+  static_assert(RING || !FAN, "the fused fan-out needs the ring");
+  using SMT = std::conditional_t<FAN, LinearSmemFan, LinearSmem>;
   extern __shared__ __align__(128) unsigned char dsm[];
-  __shared__ LinearSmem sh;
+  __shared__ SMT sh;
   __shared__ uint64_t bars[2 * kStages];
   using GR = GRow<DT, VW>;
   cg::cluster_group cluster = cg::this_cluster();
@@ -159,7 +179,10 @@ __global__ void __launch_bounds__(kThreads, RING ? 4 : 2)
   rg.full = bars;
   rg.empty = bars + kStages;
   rg.dev_status = p.dev_status;
-  if (RING) ring_init(rg);
+  if constexpr (FAN) {
+    if (tid == 0) sh.fth = 0;
+  }
+  if (RING) ring_init(rg);  // (a block barrier)
   auto trow_of = [&](int s, int j) {
     return tbase + ((size_t)s * (gamma + 1) + j) * rowb;
   };
@@ -512,6 +535,27 @@ __global__ void __launch_bounds__(kThreads, RING ? 4 : 2)
       __syncthreads();
     }
   }
+  if constexpr (FAN) {
+    // the fan-out rows, one CTA per row: sequences from the last handed out
+    // (whose draft rows the scans read most recently, possibly still in L2)
+    // to the first, rows in order
+    const int K1 = gamma + 1, nitems = K1 * p.B;
+    uint64_t *scratch = reinterpret_cast<uint64_t *>(rg.buf);  // ring idle
+    for (;;) {
+      if (tid == 0) sh.fitem = atomicAdd(p.fq, 1);
+      __syncthreads();
+      const int q = sh.fitem;
+      __syncthreads();
+      if (q >= nitems) break;
+      const int s = p.B - 1 - q / K1, j = q % K1;
+      if (p.fF[j] == 0) continue;
+      const size_t o = (size_t)s * p.ftotal + p.foff[j];
+      cta_row_topf<DT, VW>(rg, &sh.fth, scratch, sh.fout, drow_of(s, j), V,
+                           p.fF[j], p.fan_tokens + o,
+                           p.fan_logit ? p.fan_logit + o : nullptr,
+                           p.dev_status);
+    }
+  }
   cluster.sync();  // no CTA leaves while a peer may still read its smem
 }
 
@@ -523,6 +567,14 @@ template <int DT, int VW, bool RING>
 static LinearKernel pick_linear_t(bool greedy) {
   return greedy ? linear_verify_kernel<DT, VW, true, RING>
                 : linear_verify_kernel<DT, VW, false, RING>;
+}
+
+static LinearKernel pick_linear_fan(int dt, bool greedy) {
+  if (dt == SD_F32)
+    return greedy ? linear_verify_kernel<0, 4, true, true, true>
+                  : linear_verify_kernel<0, 4, false, true, true>;
+  return greedy ? linear_verify_kernel<1, 8, true, true, true>
+                : linear_verify_kernel<1, 8, false, true, true>;
 }
 
 static LinearKernel pick_linear(int dt, bool vec, bool ring, bool greedy) {
@@ -580,6 +632,38 @@ sd_status allrows_launch(const void *target, const void *draft, sd_dtype dt,
                          int32_t *dev_status, void *ws, size_t ws_bytes,
                          cudaStream_t stream);
 
+// The fused fan-out's arguments (host F, device outputs).
+struct FanArgs {
+  const int32_t *F;  // [gamma + 1]
+  int32_t *fan_tokens;
+  float *fan_logit;
+};
+
+// Workspace of the fused verify + fan-out: the work and row counters.
+size_t fan_workspace(int B) {
+  (void)B;
+  return 256;
+}
+
+// Whether the fused kernel takes sd_verify_linear_fanout: 16-byte aligned
+// rows through the ring.
+bool fan_applicable(const void *target, const void *draft, sd_dtype dt,
+                    int V) {
+  const int eb = dt == SD_F32 ? 4 : 2;
+  return aligned16(target) && aligned16(draft) && ((size_t)V * eb) % 16 == 0 &&
+         tune(SD_TUNE_NO_TMA) == 0;
+}
+
+static sd_status cluster_launch(const void *target, const void *draft,
+                                sd_dtype dt, long long d_seq_rows,
+                                const int32_t *tokens, const float *uniforms,
+                                int B, int gamma, int V, float T,
+                                int32_t *n_acc, int32_t *out_tokens,
+                                float *out_prob, float *out_accept,
+                                float *out_resid, int32_t *dev_status,
+                                void *ws, size_t ws_bytes,
+                                cudaStream_t stream, const FanArgs *fan);
+
 sd_status linear_launch(const void *target, const void *draft, sd_dtype dt,
                         long long d_seq_rows, const int32_t *tokens,
                         const float *uniforms, int B, int gamma, int V,
@@ -593,6 +677,36 @@ sd_status linear_launch(const void *target, const void *draft, sd_dtype dt,
     return allrows_launch(target, draft, dt, d_seq_rows, tokens, uniforms, B,
                           gamma, V, T, n_acc, out_tokens, out_prob,
                           out_accept, dev_status, ws, ws_bytes, stream);
+  return cluster_launch(target, draft, dt, d_seq_rows, tokens, uniforms, B,
+                        gamma, V, T, n_acc, out_tokens, out_prob, out_accept,
+                        out_resid, dev_status, ws, ws_bytes, stream, nullptr);
+}
+
+// The verify fused with the fan-out of the draft tensor [B, gamma + 1, V]
+// (fan_applicable must hold; ws of fan_workspace(B) bytes at least).
+sd_status linear_fan_launch(const void *target, const void *draft,
+                            sd_dtype dt, const int32_t *tokens,
+                            const float *uniforms, int B, int gamma, int V,
+                            float T, const int32_t *F, int32_t *n_acc,
+                            int32_t *out_tokens, float *out_prob,
+                            int32_t *fan_tokens, float *fan_logit,
+                            int32_t *dev_status, void *ws, size_t ws_bytes,
+                            cudaStream_t stream) {
+  const FanArgs fa{F, fan_tokens, fan_logit};
+  return cluster_launch(target, draft, dt, gamma + 1, tokens, uniforms, B,
+                        gamma, V, T, n_acc, out_tokens, out_prob, nullptr,
+                        nullptr, dev_status, ws, ws_bytes, stream, &fa);
+}
+
+static sd_status cluster_launch(const void *target, const void *draft,
+                                sd_dtype dt, long long d_seq_rows,
+                                const int32_t *tokens, const float *uniforms,
+                                int B, int gamma, int V, float T,
+                                int32_t *n_acc, int32_t *out_tokens,
+                                float *out_prob, float *out_accept,
+                                float *out_resid, int32_t *dev_status,
+                                void *ws, size_t ws_bytes,
+                                cudaStream_t stream, const FanArgs *fan) {
   int sms = 0;
   sd_status st = check_device(&sms);
   if (st != SD_OK) return st;
@@ -614,17 +728,22 @@ sd_status linear_launch(const void *target, const void *draft, sd_dtype dt,
   if (smem > 96 * 1024)
     return fail(SD_ERR_UNSUPPORTED, "V=%d needs %zu B of shared memory", V,
                 smem);
-  LinearKernel kern = pick_linear(dt, vec, ring, greedy);
+  if (fan && !ring)
+    return fail(SD_ERR_UNSUPPORTED, "the fused fan-out needs aligned rows");
+  LinearKernel kern = fan ? pick_linear_fan(dt, greedy)
+                          : pick_linear(dt, vec, ring, greedy);
   int maxc = 0;
   st = max_active_clusters((const void *)kern, CL, smem, &maxc);
   if (st != SD_OK) return st;
-  const int nclusters = B < maxc ? B : maxc;
+  // fused fan-out: every resident cluster, those without a sequence take
+  // fan-out rows from the start
+  const int nclusters = (B < maxc && !fan) ? B : maxc;
   // helping, in the tail of the work counter only (measured at B = 8..64
   // sequences of 128256 fp32 columns: extra clusters helping from the start
   // slowed the owners down by 5-16 %; at B = 128 and 256 helping in the
   // tail took 2-6 % off)
   const size_t hws = help_workspace(B, gamma);
-  const bool helpers = tune(SD_TUNE_HELPERS) != 0 && B > nclusters &&
+  const bool helpers = !fan && tune(SD_TUNE_HELPERS) != 0 && B > nclusters &&
                        hws != 0 && ws && ws_bytes >= hws &&
                        CL <= kHelpRanks && nclusters <= kHelpMaxClusters;
   LinearParams prm;
@@ -650,6 +769,25 @@ sd_status linear_launch(const void *target, const void *draft, sd_dtype dt,
   prm.spec = tune(SD_TUNE_SPEC);
   prm.helping = prm.active = prm.opos = prm.hpos = prm.hflag = nullptr;
   prm.hpart = nullptr;
+  prm.fan_tokens = nullptr;
+  prm.fan_logit = nullptr;
+  prm.ftotal = 0;
+  prm.fq = nullptr;
+  if (fan) {
+    if (!ws || ws_bytes < fan_workspace(B))
+      return fail(SD_ERR_INVALID_ARG, "workspace of >= %zu bytes required",
+                  fan_workspace(B));
+    int o = 0;
+    for (int k = 0; k <= gamma; ++k) {
+      prm.fF[k] = fan->F[k];
+      prm.foff[k] = o;
+      o += fan->F[k];
+    }
+    prm.ftotal = o;
+    prm.fan_tokens = fan->fan_tokens;
+    prm.fan_logit = fan->fan_logit;
+    prm.fq = reinterpret_cast<int *>(static_cast<char *>(ws) + 4);
+  }
   if (B > nclusters) {
     if (!ws || ws_bytes < 256)
       return fail(SD_ERR_INVALID_ARG, "workspace of >= 256 bytes required");
@@ -665,6 +803,8 @@ sd_status linear_launch(const void *target, const void *draft, sd_dtype dt,
     prm.hflag = reinterpret_cast<int *>(w + L.hflag);
     prm.hpart = reinterpret_cast<uint4 *>(w + L.hpart);
     SDV_CUDA(cudaMemsetAsync(ws, 0, L.zero_end, stream));
+  } else if (fan) {
+    SDV_CUDA(cudaMemsetAsync(ws, 0, fan_workspace(B), stream));
   } else if (prm.queue) {
     SDV_CUDA(cudaMemsetAsync(ws, 0, sizeof(int), stream));
   }

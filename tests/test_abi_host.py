@@ -187,7 +187,7 @@ def test_tuning_switches_set_get_and_validate():
     out-of-range values refused, and nothing read from the environment."""
     L = api.lib()
     defaults = {"cluster": 0, "no_tma": 0, "allrows": 1, "spec": 1,
-                "fused": 0, "kcand_ring": 1, "fanout_cluster": 0,
+                "fused": 1, "kcand_ring": 1, "fanout_cluster": 0,
                 "fanout_ldg": 0, "fanout_maxc": 0, "fanout_l2_first": 1}
     for k, v in defaults.items():
         assert api.tune_get(k) == v, k

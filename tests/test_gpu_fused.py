@@ -5,7 +5,8 @@ V=128256 fp32, F=[10,9,8,7,6,6,5,4,9]) on sampled sequences, the linear
 workload's shape with a lookahead draft row at T in {0, 0.7, 1}, small and
 odd sizes, gamma 0 and 1, F with empty and 64-wide rows, every cluster
 size, the work queue, NaN rows in the draft and the target, and the
-two-call path taken when the fused kernel does not apply."""
+two-call path taken when the fused kernel does not apply (rows not 16-byte
+aligned, SD_TUNE_FUSED 0)."""
 import numpy as np
 import pytest
 import torch
@@ -21,8 +22,8 @@ F_LARGE = [10, 9, 8, 7, 6, 6, 5, 4, 9]
 
 @pytest.fixture(autouse=True)
 def fused_kernel():
-    """These tests exercise the fused kernel (SD_TUNE_FUSED 1); the default
-    of sd_verify_linear_fanout is the two separate calls."""
+    """These tests exercise the fused kernel (SD_TUNE_FUSED 1, the
+    default) unless a test switches it off."""
     with api.tuned(fused=1):
         yield
 
@@ -128,3 +129,30 @@ def test_fallback_path_matches():
     c = to_device(synth.linear_case(16, 3, 6001, torch.float32, 1.0, seed=4,
                                     sigma_t=2.0, sigma_d=1.0, draft_rows=4))
     check(c, [5, 4, 3, 2])
+
+
+@pytest.mark.parametrize("T", [0.0, 1.0])
+def test_large_workload_every_sequence(T):
+    """The bench's launch: all 256 sequences and all 2304 fan-out rows of the
+    large workload against the oracle, at T = 1 and greedy."""
+    c = synth.large(0, device="cuda")
+    if T == 0:
+        c.T = 0.0
+    r = check(c, F_LARGE)
+    assert r["acc_flagged"] <= 2
+
+
+def test_fused_matches_two_calls_bitwise():
+    """The fused kernel and the two calls give the same bits (verify and
+    fan-out), on a queue-sized batch."""
+    c = to_device(synth.linear_case(300, 8, 50000, torch.float32, 1.0,
+                                    seed=12, sigma_t=2.5, sigma_d=1.0,
+                                    draft_rows=9))
+    F = [10, 9, 8, 7, 6, 6, 5, 4, 9]
+    g = run(c, F)
+    with api.tuned(fused=0):
+        h = run(c, F)
+    for k in ("n", "tokens", "prob", "fan_tokens", "fan_logit"):
+        assert torch.equal(g[k], h[k]) or (
+            k == "fan_logit" and torch.equal(g[k].isnan(), h[k].isnan())
+            and torch.equal(g[k].nan_to_num(), h[k].nan_to_num())), k
