@@ -108,9 +108,11 @@ class ClockSampler:
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch
 # from one ncu capture of each kernel on B=128 sequences of this workload
 # (profiles/), with the units that launch processed: the fan-out reads every
-# row once, so its traffic scales with the rows; the verify's with the bytes
-# the method needs (its early exit decides how many rows it reads).
-TRAFFIC = {"fanout": (591.25e6, 128 * 9), "linear": (421.20e6, 343.73e6),
+# row once, so its traffic scales with the rows; the verify's and the fused
+# step's with the bytes the method needs (the early exit decides how many
+# rows they read).  The verify's includes the rows that clusters helping in
+# the tail read ahead.
+TRAFFIC = {"fanout": (591.25e6, 128 * 9), "linear": (565.0e6, 343.73e6),
            "fused": (1008.3e6, 763.89e6)}
 
 
