@@ -156,3 +156,21 @@ def test_fused_matches_two_calls_bitwise():
         assert torch.equal(g[k], h[k]) or (
             k == "fan_logit" and torch.equal(g[k].isnan(), h[k].isnan())
             and torch.equal(g[k].nan_to_num(), h[k].nan_to_num())), k
+
+
+@pytest.mark.parametrize("dtype,run_len", [(torch.float32, 4),
+                                           (torch.bfloat16, 8)])
+def test_top_run_in_one_vector(dtype, run_len):
+    """A run of large, decreasing logits inside one 16-byte vector of every
+    draft row: the row's best keys all come from one thread's elements.
+    F wider and narrower than the run, against the oracle."""
+    c = synth.linear_case(40, 4, 8192, dtype, 1.0, seed=21, sigma_t=2.0,
+                          sigma_d=1.0, draft_rows=5)
+    base = 64 * run_len  # the start of a vector
+    for b in range(c.draft.shape[0]):
+        for r in range(c.draft.shape[1]):
+            for e in range(run_len):
+                c.draft[b, r, base + e] = 40.0 - e
+    c = to_device(c)
+    check(c, [6, 6, 2, 9, 3])
+    check(c, [2, 2, 2, 2, 2])
