@@ -541,6 +541,9 @@ __global__ void __launch_bounds__(kThreads, RING ? 4 : 2)
     // to the first, rows in order
     const int K1 = gamma + 1, nitems = K1 * p.B;
     uint64_t *scratch = reinterpret_cast<uint64_t *>(rg.buf);  // ring idle
+    // each fan-out row is read once: keep it from pushing out the lines the
+    // scans still running read again (their draws)
+    rg.policy = l2_evict_first_policy();
     for (;;) {
       if (tid == 0) sh.fitem = atomicAdd(p.fq, 1);
       __syncthreads();
