@@ -178,12 +178,12 @@ __device__ __forceinline__ float vmax_of(const float (&z)[VW]) {
 }
 
 template <int DT, int VW>
-__device__ __forceinline__ void ms_add(MS &st, const Raw<DT, VW> &r,
-                                       float k2) {
+__device__ __forceinline__ void ms_add_v(MS &st, const Raw<DT, VW> &r,
+                                         float k2, float &vmax) {
   float z[VW];
 #pragma unroll
   for (int e = 0; e < VW; ++e) z[e] = elt<DT, VW>(r, e);
-  const float vmax = vmax_of<VW>(z);
+  vmax = vmax_of<VW>(z);
   if (__builtin_expect(vmax > st.m, 0)) {  // rare once the large values are in
     st.s *= ex2((st.m - vmax) * k2);
     st.m = vmax;
@@ -205,6 +205,14 @@ __device__ __forceinline__ void ms_add(MS &st, const Raw<DT, VW> &r,
     }
     st.s += acc.x + acc.y;
   }
+}
+
+// The same, for callers that do not need the vector's maximum.
+template <int DT, int VW>
+__device__ __forceinline__ void ms_add(MS &st, const Raw<DT, VW> &r,
+                                       float k2) {
+  float vmax;
+  ms_add_v<DT, VW>(st, r, k2, vmax);
 }
 
 // p(x)/q(x) of the draft token x from its target and draft logits zt, zd

@@ -5,14 +5,15 @@
 //
 // The fused kernel is the linear verify kernel's FAN instantiation
 // (sdv_linear.cu): the scans as in sd_verify_linear, and every CTA left
-// without a sequence takes whole fan-out rows, one CTA per row, so the
-// fan-out's rows fill the GPU while the last scans finish (and every
-// resident cluster beyond the B sequences does fan-out rows from the
-// start).  Filtering the draft rows inside the scans as well, to read rows
-// 0..n once, was measured slower: a CTA's slice of a row is too short for
-// the per-warp top-F lists, whose inserts then dominate the scan.  With
-// rows that are not 16-byte aligned or SD_TUNE_FUSED 0 the call runs
-// sd_verify_linear and sd_fanout_topk one after the other.
+// without a sequence takes fan-out rows, one CTA per row, so the fan-out's
+// rows fill the GPU while the last scans finish (and every resident
+// cluster beyond the B sequences does fan-out rows from the start).  The
+// draft rows 0..n that the scans stream are not read again when their
+// records settle them: each scan thread keeps its best vector of the row
+// (sdv_fanrow.cuh), from which the row's exact top-F follows unless a
+// check fails; only then is the row read whole.  With rows that are not
+// 16-byte aligned or SD_TUNE_FUSED 0 the call runs sd_verify_linear and
+// sd_fanout_topk one after the other.
 #include "sdv_host.cuh"
 
 namespace sdv {
@@ -32,7 +33,7 @@ sd_status linear_fan_launch(const void *target, const void *draft,
                             int32_t *fan_tokens, float *fan_logit,
                             int32_t *dev_status, void *ws, size_t ws_bytes,
                             cudaStream_t stream);
-size_t fan_workspace(int B);
+size_t fan_workspace(int B, int gamma, int V, sd_dtype dt);
 bool fan_applicable(const void *target, const void *draft, sd_dtype dt,
                     int V);
 
@@ -40,7 +41,7 @@ bool fan_applicable(const void *target, const void *draft, sd_dtype dt,
 
 extern "C" size_t sd_verify_linear_fanout_workspace(int B, int gamma, int V,
                                                     sd_dtype dt) {
-  const size_t a = sdv::fan_workspace(B);
+  const size_t a = sdv::fan_workspace(B, gamma, V, dt);
   const size_t b = sd_verify_linear_workspace(B, gamma, V, dt);
   return a > b ? a : b;
 }

@@ -73,14 +73,22 @@ struct LinearParams {
   uint4 *hpart;     // [B][gamma+1][kHelpRanks]: the partials
   // Fused fan-out (the FAN kernels; sd_verify_linear_fanout).  Draft row j
   // of every sequence (j = 0..gamma, the draft tensor holding gamma + 1
-  // rows) gets its exact top-fF[j] keys.  A CTA with no sequence left to
-  // verify takes whole rows from the row counter, one CTA per row, the
-  // sequences handed out last first (their rows were read most recently).
+  // rows) gets its exact top-fF[j] keys.  While a scan streams draft row j
+  // each of its threads also keeps its best vector (sdv_fanrow.cuh) and
+  // stores it; fcov[b] then says that rows 0..fcov[b]-1 of sequence b have
+  // their records.  A CTA with no sequence left to verify takes rows from
+  // the row counter, one CTA per row, the sequences handed out last first:
+  // a covered row from its records when they determine the top-F, any other
+  // row whole.
   int32_t *fan_tokens;  // [B, ftotal]
   float *fan_logit;     // nullable
   int fF[SD_MAX_K + 1], foff[SD_MAX_K + 1];
   int ftotal;
-  int *fq;  // the row counter
+  int *fq;        // the row counter
+  int *fcov;      // [B] (null: no records kept)
+  uint4 *cand_v;  // [B][gamma][CL][kThreads]: each thread's best vector
+  int *cand_i;    // its index in the row
+  float *cand_t;  // the thread's largest other vector maximum
 };
 
 constexpr int kHelpRanks = 16;  // record stride: the largest cluster
@@ -149,8 +157,9 @@ struct LinearSmem {
 // The FAN kernels' shared memory: a row's top-F and the filters' state.
 struct LinearSmemFan : LinearSmem {
   uint64_t fout[SD_MAX_FANOUT];
-  uint32_t fth;  // the warp filters' CTA threshold
-  int fitem;
+  uint32_t fth;    // the warp filters' CTA threshold
+  uint32_t t2max;  // ord32 of the largest t2 of a row's records
+  int fitem, fcov;
 };
 
 template <int DT, int VW, bool GREEDY, bool RING, bool FAN = false>
@@ -180,7 +189,10 @@ __global__ void __launch_bounds__(kThreads, RING ? 4 : 2)
   rg.empty = bars + kStages;
   rg.dev_status = p.dev_status;
   if constexpr (FAN) {
-    if (tid == 0) sh.fth = 0;
+    if (tid == 0) {
+      sh.fth = 0;
+      sh.t2max = 0;
+    }
   }
   if (RING) ring_init(rg);  // (a block barrier)
   auto trow_of = [&](int s, int j) {
@@ -212,6 +224,38 @@ __global__ void __launch_bounds__(kThreads, RING ? 4 : 2)
       block_reduce_ms<2>(st, k2, sh.red);
       return make_uint4(__float_as_uint(st[0].m), __float_as_uint(st[0].s),
                         __float_as_uint(st[1].m), __float_as_uint(st[1].s));
+    }
+  };
+  // FAN: the stats of position j while this CTA's threads also keep their
+  // best vectors of its draft row and store them (same arithmetic as
+  // slice_stats)
+  auto cand_stats = [&](int s, int j) -> uint4 {
+    if constexpr (FAN && !GREEDY) {
+      const char *trow = trow_of(s, j), *drow = drow_of(s, j);
+      MS st[2] = {ms_empty(), ms_empty()};
+      VecTop<DT, VW> T;
+      vec_top_init(T);
+      ring_pass(rg, trow, drow, sl, [&](const uint4 *A, const uint4 *Bp,
+                                        int v0, int n) {
+        for (int i = tid; i < n; i += kThreads) {
+          ms_add<DT, VW>(st[0], sget<DT, VW>(A, i), k2);
+          const Raw<DT, VW> d = sget<DT, VW>(Bp, i);
+          float vm;
+          ms_add_v<DT, VW>(st[1], d, k2, vm);
+          vec_top_add(T, d, vm, v0 + i);
+        }
+      });
+      const size_t r = ((size_t)s * gamma + j) * CL * kThreads +
+                       (size_t)rank * kThreads + tid;
+      // a NaN or an infinity among this thread's elements leaves its sum
+      // non-finite (the row is then read whole)
+      vec_top_store(T, isfinite(st[1].s), p.cand_v + r, p.cand_i + r,
+                    p.cand_t + r);
+      block_reduce_ms<2>(st, k2, sh.red);
+      return make_uint4(__float_as_uint(st[0].m), __float_as_uint(st[0].s),
+                        __float_as_uint(st[1].m), __float_as_uint(st[1].s));
+    } else {
+      return slice_stats(s, j);
     }
   };
   const bool help = p.hflag != nullptr;
@@ -290,6 +334,9 @@ __global__ void __launch_bounds__(kThreads, RING ? 4 : 2)
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (hmode && sh.hready[t]) {
           v = sh.hv[t];
+        } else if (FAN && !GREEDY && p.fcov && i + t < gamma &&
+                   p.fF[i + t] > 0) {
+          v = cand_stats(seq, i + t);
         } else {
           v = slice_stats(seq, i + t);
         }
@@ -378,6 +425,11 @@ __global__ void __launch_bounds__(kThreads, RING ? 4 : 2)
       }
       __syncthreads();
       R = sh.res;
+      if constexpr (FAN && !GREEDY) {
+        // every CTA stored the records of [i, jend) before the barrier
+        if (p.fcov && rank == 0 && tid == 0)
+          st_release_gpu(p.fcov + seq, min(jend, gamma));
+      }
       if (R.kind) break;
       i = jend;
       if (first) {  // after the first step: is this the cluster's last?
@@ -545,18 +597,33 @@ __global__ void __launch_bounds__(kThreads, RING ? 4 : 2)
     // scans still running read again (their draws)
     rg.policy = l2_evict_first_policy();
     for (;;) {
-      if (tid == 0) sh.fitem = atomicAdd(p.fq, 1);
+      if (tid == 0) {
+        const int q = atomicAdd(p.fq, 1);
+        sh.fitem = q;
+        sh.fcov = (q < nitems && p.fcov)
+                      ? ld_acquire_gpu(p.fcov + (p.B - 1 - q / K1)) : 0;
+      }
       __syncthreads();
-      const int q = sh.fitem;
+      const int q = sh.fitem, cov = sh.fcov;
       __syncthreads();
       if (q >= nitems) break;
       const int s = p.B - 1 - q / K1, j = q % K1;
       if (p.fF[j] == 0) continue;
       const size_t o = (size_t)s * p.ftotal + p.foff[j];
+      int32_t *otok = p.fan_tokens + o;
+      float *olog = p.fan_logit ? p.fan_logit + o : nullptr;
+      if constexpr (!GREEDY) {
+        if (j < cov) {  // the scan kept this row's best vectors
+          const size_t r0 = ((size_t)s * gamma + j) * CL * kThreads;
+          if (cta_vec_topf<DT, VW>(p.cand_v + r0, p.cand_i + r0,
+                                   p.cand_t + r0, CL * kThreads, &sh.fth,
+                                   &sh.t2max, scratch, sh.fout, p.fF[j],
+                                   otok, olog, p.dev_status))
+            continue;
+        }
+      }
       cta_row_topf<DT, VW>(rg, &sh.fth, scratch, sh.fout, drow_of(s, j), V,
-                           p.fF[j], p.fan_tokens + o,
-                           p.fan_logit ? p.fan_logit + o : nullptr,
-                           p.dev_status);
+                           p.fF[j], otok, olog, p.dev_status);
     }
   }
   cluster.sync();  // no CTA leaves while a peer may still read its smem
@@ -642,10 +709,40 @@ struct FanArgs {
   float *fan_logit;
 };
 
-// Workspace of the fused verify + fan-out: the work and row counters.
-size_t fan_workspace(int B) {
-  (void)B;
-  return 256;
+// The cluster size of the FAN kernels for these sizes (aligned rows: the
+// rule of cluster_launch).
+static int fan_cluster(int B, int V, sd_dtype dt) {
+  const long long nvec = V / (dt == SD_F32 ? 4 : 8);
+  int CL = choose_cluster(nvec);
+  if (B >= 128 && CL > 8 && tune(SD_TUNE_CLUSTER) == 0) CL = 8;
+  return CL;
+}
+
+// Workspace of the fused verify + fan-out: the work and row counters, the
+// coverage marks, then the scans' records (24 bytes a thread a draft row;
+// left out, and every row filtered whole, above 1 GB).
+struct FanLayout {
+  size_t fcov, cand_t, cand_i, cand_v, zero_end, total;
+  bool records;
+};
+static FanLayout fan_layout(int B, int gamma, int V, sd_dtype dt) {
+  auto r256 = [](size_t x) { return (x + 255) / 256 * 256; };
+  FanLayout L;
+  const size_t nb = B > 0 ? (size_t)B : 0;
+  L.fcov = 256;
+  L.zero_end = L.fcov + r256(nb * 4);
+  const size_t nrec = nb * (size_t)(gamma > 0 ? gamma : 0) *
+                      (size_t)fan_cluster(B, V, dt) * kThreads;
+  L.cand_t = L.zero_end;
+  L.cand_i = L.cand_t + r256(nrec * 4);
+  L.cand_v = L.cand_i + r256(nrec * 4);
+  L.total = L.cand_v + nrec * 16;
+  L.records = nrec > 0 && L.total <= ((size_t)1 << 30);
+  if (!L.records) L.total = L.zero_end;
+  return L;
+}
+size_t fan_workspace(int B, int gamma, int V, sd_dtype dt) {
+  return fan_layout(B, gamma, V, dt).total;
 }
 
 // Whether the fused kernel takes sd_verify_linear_fanout: 16-byte aligned
@@ -776,10 +873,15 @@ static sd_status cluster_launch(const void *target, const void *draft,
   prm.fan_logit = nullptr;
   prm.ftotal = 0;
   prm.fq = nullptr;
+  prm.fcov = nullptr;
+  prm.cand_t = nullptr;
+  prm.cand_i = nullptr;
+  prm.cand_v = nullptr;
   if (fan) {
-    if (!ws || ws_bytes < fan_workspace(B))
+    const FanLayout L = fan_layout(B, gamma, V, dt);
+    if (!ws || ws_bytes < L.zero_end)
       return fail(SD_ERR_INVALID_ARG, "workspace of >= %zu bytes required",
-                  fan_workspace(B));
+                  L.total);
     int o = 0;
     for (int k = 0; k <= gamma; ++k) {
       prm.fF[k] = fan->F[k];
@@ -789,7 +891,16 @@ static sd_status cluster_launch(const void *target, const void *draft,
     prm.ftotal = o;
     prm.fan_tokens = fan->fan_tokens;
     prm.fan_logit = fan->fan_logit;
-    prm.fq = reinterpret_cast<int *>(static_cast<char *>(ws) + 4);
+    char *w = static_cast<char *>(ws);
+    prm.fq = reinterpret_cast<int *>(w + 4);
+    // the records, when the workspace holds them for this cluster size
+    if (!greedy && L.records && ws_bytes >= L.total &&
+        fan_cluster(B, V, dt) == CL) {
+      prm.fcov = reinterpret_cast<int *>(w + L.fcov);
+      prm.cand_t = reinterpret_cast<float *>(w + L.cand_t);
+      prm.cand_i = reinterpret_cast<int *>(w + L.cand_i);
+      prm.cand_v = reinterpret_cast<uint4 *>(w + L.cand_v);
+    }
   }
   if (B > nclusters) {
     if (!ws || ws_bytes < 256)
@@ -807,7 +918,8 @@ static sd_status cluster_launch(const void *target, const void *draft,
     prm.hpart = reinterpret_cast<uint4 *>(w + L.hpart);
     SDV_CUDA(cudaMemsetAsync(ws, 0, L.zero_end, stream));
   } else if (fan) {
-    SDV_CUDA(cudaMemsetAsync(ws, 0, fan_workspace(B), stream));
+    SDV_CUDA(cudaMemsetAsync(ws, 0, fan_layout(B, gamma, V, dt).zero_end,
+                             stream));
   } else if (prm.queue) {
     SDV_CUDA(cudaMemsetAsync(ws, 0, sizeof(int), stream));
   }
