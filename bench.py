@@ -113,7 +113,7 @@ class ClockSampler:
 # rows they read).  The verify's includes the rows that clusters helping in
 # the tail read ahead.
 TRAFFIC = {"fanout": (591.25e6, 128 * 9), "linear": (565.0e6, 343.73e6),
-           "fused": (963.2e6, 763.89e6)}
+           "fused": (881.2e6, 763.89e6)}
 
 
 def hbm_peak():
