@@ -128,9 +128,10 @@ typedef enum {
   SD_TUNE_FANOUT_LDG = 7,      /* 1: fan-out with plain loads; default 0 */
   SD_TUNE_FANOUT_MAXC = 8,     /* cap on the fan-out's clusters: 0 none */
   SD_TUNE_FANOUT_L2_FIRST = 9, /* fan-out rows read evict-first: default 1 */
-  SD_TUNE_HELPERS = 10,        /* linear verify: clusters with no sequence
-                                  left compute row statistics ahead of the
-                                  scans still running: 0 or 1 (default 1) */
+  SD_TUNE_HELPERS = 10,        /* linear and K-candidate verify: clusters
+                                  with no sequence left compute row
+                                  statistics ahead of the scans still
+                                  running: 0 or 1 (default 1) */
   SD_TUNE_COUNT = 11
 } sd_tune;
 
@@ -257,6 +258,11 @@ sd_status sd_verify_linear_filtered(
  * Outputs: n_accepted [B], selected_k [B], out_tokens [B, gamma+1],
  *   n_per_cand [B, K] (nullable), out_prob [B] (nullable).
  * This selection is not distribution-preserving for K > 1.
+ * With SD_TUNE_HELPERS on (the default; sampled, aligned rows, K <= 31),
+ * clusters whose sequence is done also read rows of positions ahead of the
+ * scans still running; the results are the same bits either way.
+ * Workspace: sd_verify_kcand_workspace bytes (the work counter and up to
+ * 64 MB of helping records).
  * ------------------------------------------------------------------- */
 size_t sd_verify_kcand_workspace(int B, int K, int gamma, int V, sd_dtype dt);
 

@@ -325,6 +325,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   cluster.sync();
 }
 
+size_t kcand_help_workspace(int B, int K, int gamma);
 sd_status kcand_ring_launch(const void *target, const void *draft,
                             sd_dtype dt, const int32_t *tokens,
                             const float *uniforms, int B, int K, int gamma,
@@ -349,12 +350,12 @@ static KcandKernel pick_kcand(int dt, bool vec, bool greedy) {
 
 extern "C" size_t sd_verify_kcand_workspace(int B, int K, int gamma, int V,
                                             sd_dtype dt) {
-  (void)B;
-  (void)K;
-  (void)gamma;
   (void)V;
   (void)dt;
-  return 256;
+  // the work counter and, up to 64 MB, the helping records of the
+  // streaming kernel (sdv_kcand_ring.cu)
+  const size_t h = sdv::kcand_help_workspace(B, K, gamma);
+  return h > 256 ? h : 256;
 }
 
 extern "C" sd_status sd_verify_kcand(

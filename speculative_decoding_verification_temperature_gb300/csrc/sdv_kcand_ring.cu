@@ -36,9 +36,46 @@ struct KRParams {
   int *queue;
   int nclusters;
   int seg_bytes;
+  // Helping (sampled rows; all null when off).  A cluster whose sequence is
+  // done computes rows of positions ahead of the scans still running: each
+  // CTA claims a position of a running sequence for its rank, streams its
+  // slice of the position's draft-marginal row and of the target rows of
+  // the candidates alive at the claim, with the owner's own code (hence the
+  // same bits), stores each row's partial and raises its flag.  An owner CTA
+  // reads the flags of the next position's rows when it decides, and its
+  // producer skips the rows found done.  Nobody waits on a flag.
+  int *helping;   // set once a cluster has started helping
+  int *active;    // [nclusters]: sequence + 1 being verified, or 0
+  int *opos;      // [B]: the owner's next position
+  int *oalive;    // [B]: its live candidates
+  int *hpos;      // [B][kHelpRanks]: next position to hand to a helper
+  int *hflag;     // [B][gamma][K+1][kHelpRanks]: partial published
+  float2 *hpart;  // [B][gamma][K+1][kHelpRanks]: (m, s)
 };
 
 constexpr int kKRows = SD_MAX_K + 1;  // draft row + one per candidate
+constexpr int kHelpRanks = 16;        // record stride: the largest cluster
+
+__device__ __forceinline__ int kh_ld_acquire(const int *a) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(a)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ int kh_ld_relaxed(const int *a) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(a)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ void kh_st_release(int *a, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(a), "r"(v)
+               : "memory");
+}
+__device__ __forceinline__ void kh_st_relaxed(int *a, int v) {
+  asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(a), "r"(v)
+               : "memory");
+}
 
 // Ring schedule (thread 0 only, in shared memory).  Producer item kinds:
 // 0 the draft row of position pj, 1 the target rows of its live candidates
@@ -55,6 +92,8 @@ struct KSched {
   int ksel, nsel;
   int bdone;     // bonus row exchanged: 1 valid, 2 unusable
   int next;      // the sequence after dseq, -1 until known
+  unsigned skip;  // rows of position pj done by helpers: bit 0 the draft
+                  // row, bit 1 + k candidate k's target row
 };
 
 // The producer's current item (thread 0's registers).
@@ -86,6 +125,10 @@ struct KRSmem {
   int next_seq[2];
   KSched sc;
   DrawSmem draw;
+  MS hv[kKRows];  // helpers' partials of the next position's rows
+  int hs, hj;     // a helper's claim
+  unsigned halive;
+  int hseen;      // the helping flag, read at the position's start
 };
 
 template <int DT, int VW, bool GREEDY>
@@ -125,9 +168,9 @@ struct KFu {
         }
         sc.pkind = 1;
         sc.pk = 0;
-        if (!GREEDY) ra = drow(b, j);
+        if (!GREEDY && !(sc.skip & 1u)) ra = drow(b, j);
       } else if (sc.pkind == 1) {  // target rows of the live candidates
-        const unsigned alive = j == 0 ? full() : sc.alive;
+        const unsigned alive = (j == 0 ? full() : sc.alive) & ~(sc.skip >> 1);
         int k = sc.pk;
         while (k < p.K && !(alive >> k & 1u)) ++k;
         if (k >= p.K) {
@@ -170,6 +213,7 @@ struct KFu {
         sc.pseq = -1;
         sc.pj = 0;
         sc.pkind = 0;
+        sc.skip = 0;
         continue;
       }
       if (ra && nv > 0) {  // (greedy reads no draft row)
@@ -289,6 +333,7 @@ __global__ void __launch_bounds__(kThreads, 4)
     sc.ksel = sc.nsel = 0;
     sc.bdone = 0;
     sc.next = -1;
+    sc.skip = 0;
   }
   ring_init(rg);  // (a block barrier)
   int par = 0, seqpar = 0, consumed = 0;
@@ -355,8 +400,26 @@ __global__ void __launch_bounds__(kThreads, 4)
     par ^= 1;
   };
 
+  // a helper's row r: this CTA's partial, as the owner's exchange folds it
+  auto take_row = [&](int r, int row) {
+    if (tid == 0) {
+      sh.wpart[r][0] = sh.hv[row];
+      for (int w = 1; w < kWarps; ++w) sh.wpart[r][w] = ms_empty();
+    }
+  };
+  const bool help = !GREEDY && p.hflag != nullptr;
+  const int cid = (int)(blockIdx.x / CL);
+  auto hrec = [&](int s, int j, int row) {
+    return (((size_t)s * gamma + j) * (K + 1) + row) * kHelpRanks + rank;
+  };
+
   if (tid == 0) fu.pump(sh.sc, ps, consumed);
   while (b < p.B) {
+    if (help && tid == 0 && rank == 0) {
+      kh_st_relaxed(p.opos + b, 0);
+      kh_st_relaxed(p.oalive + b, (int)full);
+      kh_st_relaxed(p.active + cid, b + 1);
+    }
     if (tid == 0) {
       if (rank == 0)
         sh.next_seq[seqpar] = p.nclusters + atomicAdd(p.queue, 1);
@@ -391,10 +454,20 @@ __global__ void __launch_bounds__(kThreads, 4)
           gru = p.uniforms[((size_t)b * K + gk) * G1 + j];
         }
       }
+      // rows that helpers did for this CTA's slice are taken, not streamed;
+      // the helping flag is read here, for the decision after the exchange
+      const unsigned skip = help ? sh.sc.skip : 0u;
+      if (help && tid == 64) sh.hseen = kh_ld_relaxed(p.helping);
       int r = 0;
-      if (!GREEDY) stream_row(r++);
+      if (!GREEDY) {
+        if (skip & 1u) take_row(r++, 0);
+        else stream_row(r++);
+      }
       for (int k = 0; k < K; ++k)
-        if (alive >> k & 1u) stream_row(r++);
+        if (alive >> k & 1u) {
+          if (skip >> (1 + k) & 1u) take_row(r++, 1 + k);
+          else stream_row(r++);
+        }
       if (gath) {
         sh.gx[gk] = gx;
         sh.gzt[gk] = gzt;
@@ -432,12 +505,47 @@ __global__ void __launch_bounds__(kThreads, 4)
         const unsigned am = __ballot_sync(0xffffffffu, acc);
         const unsigned bm = __ballot_sync(0xffffffffu, bad);
         const unsigned im = __ballot_sync(0xffffffffu, inv);
+        // helpers: the next position's rows already published for this
+        // CTA's slice (each lane reads its candidate's record after its flag)
+        unsigned hmask = 0;
+        if (help) {
+          const int hm = sh.hseen;
+          const int jn = j + 1;
+          if (hm && jn < gamma && am && !im) {
+            bool ready = false;
+            if (k < K && (am >> k & 1u)) {
+              const size_t rec = hrec(b, jn, 1 + k);
+              if (kh_ld_acquire(p.hflag + rec)) {
+                const float2 v = __ldcg(p.hpart + rec);
+                sh.hv[1 + k] = MS{v.x, v.y};
+                ready = true;
+              }
+            }
+            hmask = __ballot_sync(0xffffffffu, ready) << 1;
+            if (lane == 0) {
+              const size_t rec = hrec(b, jn, 0);
+              if (kh_ld_acquire(p.hflag + rec)) {
+                const float2 v = __ldcg(p.hpart + rec);
+                sh.hv[0] = MS{v.x, v.y};
+                hmask |= 1u;
+              }
+            }
+          }
+          if (lane == 0) {  // publish progress; take the next position
+            atomicMax(p.hpos + (size_t)b * kHelpRanks + rank, j + 2);
+            if (rank == 0) {
+              kh_st_relaxed(p.oalive + b, (int)am);
+              kh_st_relaxed(p.opos + b, j + 1);
+            }
+          }
+        }
         __syncwarp();  // the lanes' n_k / rejection stats are visible
         if (lane == 0) {
           sh.alive = am;
           if (bm) sh.bad_token = 1;
           if (im) sh.invalid = 1;
           KSched &sc = sh.sc;
+          sc.skip = hmask;
           sc.decided = j + 1;
           sc.alive = am;
           if (!am || im || j == gamma - 1) fu.end_scan(sc, sh);
@@ -551,6 +659,8 @@ __global__ void __launch_bounds__(kThreads, 4)
                                     (zero_mass ? SD_DEV_ZERO_MASS : 0));
       }
     }
+    if (help && tid == 0)  // no more helpers for this sequence
+      atomicMax(p.hpos + (size_t)b * kHelpRanks + rank, gamma);
     __syncthreads();
     b = sh.sc.next;  // learnt at this sequence's first exchange
     seqpar ^= 1;
@@ -568,6 +678,81 @@ __global__ void __launch_bounds__(kThreads, 4)
     }
     __syncthreads();
   }
+  if (help) {
+    // Nothing left to verify (the ring is idle: everything issued was
+    // consumed): compute this CTA's slice of the rows of positions ahead of
+    // the scans still running, nearest to its owner's position first.
+    if (tid == 0) {
+      if (rank == 0) kh_st_relaxed(p.active + cid, 0);
+      kh_st_relaxed(p.helping, 1);
+    }
+    for (int round = 0; round < gamma * p.B; ++round) {
+      if (warp == 0) {
+        int bs = -1, bpri = 0x7fffffff;
+        for (int c = lane; c < p.nclusters; c += 32) {
+          const int a = kh_ld_relaxed(p.active + c);
+          if (a <= 0) continue;
+          const int s = a - 1;
+          const int h = kh_ld_relaxed(p.hpos + (size_t)s * kHelpRanks + rank);
+          if (h >= gamma) continue;
+          const int pri = h - kh_ld_relaxed(p.opos + s);
+          if (pri < bpri) {
+            bpri = pri;
+            bs = s;
+          }
+        }
+        for (int o = 16; o; o >>= 1) {  // lowest priority, then lowest s
+          const int op = __shfl_xor_sync(0xffffffffu, bpri, o);
+          const int os = __shfl_xor_sync(0xffffffffu, bs, o);
+          if (op < bpri || (op == bpri && (unsigned)os < (unsigned)bs)) {
+            bpri = op;
+            bs = os;
+          }
+        }
+        if (lane == 0) {
+          int jc = gamma;
+          unsigned al = 0;
+          if (bs >= 0) {  // position 0 is always the owner's own
+            int *hp = p.hpos + (size_t)bs * kHelpRanks + rank;
+            jc = atomicAdd(hp, 1);
+            if (jc == 0) jc = atomicAdd(hp, 1);
+            al = (unsigned)kh_ld_relaxed(p.oalive + bs);
+          }
+          sh.hs = bs;
+          sh.hj = jc;
+          sh.halive = al;
+        }
+      }
+      __syncthreads();
+      const int hs = sh.hs, hj = sh.hj;
+      const unsigned hal = sh.halive;
+      if (hs < 0) break;
+      if (hj < gamma) {
+        for (int row = 0; row <= K; ++row) {  // 0: the draft row; 1 + k
+          if (row > 0 && !(hal >> (row - 1) & 1u)) continue;
+          if (tid == 0) {  // the row as the producer's current item
+            const char *src = row == 0 ? fu.drow(hs, hj) : fu.trow(hs, row - 1, hj);
+            ps.pa = src + (size_t)sl.vbeg * 16;
+            ps.pb = nullptr;
+            ps.prem = nv;
+            ps.pstg = kStageVecs;
+            fu.pump(sh.sc, ps, consumed);
+          }
+          stream_row(0);
+          __syncthreads();
+          if (tid == 0) {  // folded as the owner's exchange folds
+            MS a = sh.wpart[0][0];
+            for (int w = 1; w < kWarps; ++w) a = ms_merge(a, sh.wpart[0][w], k2);
+            const size_t rec = hrec(hs, hj, row);
+            __stcg(p.hpart + rec, make_float2(a.m, a.s));
+            kh_st_release(p.hflag + rec, 1);
+          }
+          __syncthreads();
+        }
+      }
+      __syncthreads();
+    }
+  }
   cluster.sync();  // no CTA leaves while a peer may still read its smem
 }
 
@@ -577,6 +762,40 @@ static KRKernel pick_kr(int dt, bool greedy) {
   if (dt == SD_F32)
     return greedy ? kcand_ring_kernel<0, 4, true> : kcand_ring_kernel<0, 4, false>;
   return greedy ? kcand_ring_kernel<1, 8, true> : kcand_ring_kernel<1, 8, false>;
+}
+
+// Workspace layout: the work counter (byte 0) and the helping flag (byte 4),
+// then the helping records; everything before the partials is cleared on
+// the stream before each launch.
+struct KHelpLayout {
+  size_t active, opos, oalive, hpos, hflag, hpart, zero_end, total;
+};
+constexpr int kKHelpMaxClusters = 1024;
+constexpr size_t kKHelpMaxWs = (size_t)64 << 20;
+
+static KHelpLayout kh_layout(int B, int K, int gamma) {
+  auto r256 = [](size_t x) { return (x + 255) / 256 * 256; };
+  const size_t nb = B > 0 ? (size_t)B : 0;
+  const size_t recs = nb * (size_t)(gamma > 0 ? gamma : 0) * (size_t)(K + 1) *
+                      kHelpRanks;
+  KHelpLayout L;
+  L.active = 256;
+  L.opos = L.active + r256((size_t)kKHelpMaxClusters * 4);
+  L.oalive = L.opos + r256(nb * 4);
+  L.hpos = L.oalive + r256(nb * 4);
+  L.hflag = L.hpos + r256(nb * kHelpRanks * 4);
+  L.hpart = L.hflag + r256(recs * 4);
+  L.zero_end = L.hpart;
+  L.total = L.hpart + recs * 8;
+  return L;
+}
+
+// Bytes the helping records need (0: K of 32, or too large; the call then
+// runs without helping).
+size_t kcand_help_workspace(int B, int K, int gamma) {
+  if (B <= 0 || K < 1 || K > 31 || gamma < 1) return 0;
+  const size_t t = kh_layout(B, K, gamma).total;
+  return t <= kKHelpMaxWs ? t : 0;
 }
 
 // Launch for 16-byte aligned rows.  *launched = false (and SD_OK) when the
@@ -639,7 +858,25 @@ sd_status kcand_ring_launch(const void *target, const void *draft,
   prm.queue = static_cast<int *>(ws);
   prm.nclusters = B < maxc ? B : maxc;
   prm.seg_bytes = (int)(smem - kRingBytes);
-  SDV_CUDA(cudaMemsetAsync(ws, 0, sizeof(int), stream));
+  prm.helping = prm.active = prm.opos = prm.oalive = prm.hpos = nullptr;
+  prm.hflag = nullptr;
+  prm.hpart = nullptr;
+  const size_t hws = kcand_help_workspace(B, K, gamma);
+  if (!greedy && tune(SD_TUNE_HELPERS) != 0 && hws != 0 && ws_bytes >= hws &&
+      CL <= kHelpRanks && prm.nclusters <= kKHelpMaxClusters) {
+    const KHelpLayout L = kh_layout(B, K, gamma);
+    char *w = static_cast<char *>(ws);
+    prm.helping = reinterpret_cast<int *>(w + 4);
+    prm.active = reinterpret_cast<int *>(w + L.active);
+    prm.opos = reinterpret_cast<int *>(w + L.opos);
+    prm.oalive = reinterpret_cast<int *>(w + L.oalive);
+    prm.hpos = reinterpret_cast<int *>(w + L.hpos);
+    prm.hflag = reinterpret_cast<int *>(w + L.hflag);
+    prm.hpart = reinterpret_cast<float2 *>(w + L.hpart);
+    SDV_CUDA(cudaMemsetAsync(ws, 0, L.zero_end, stream));
+  } else {
+    SDV_CUDA(cudaMemsetAsync(ws, 0, sizeof(int), stream));
+  }
   void *args[] = {&prm};
   *launched = true;
   return launch_clusters((const void *)kern, prm.nclusters, CL, smem, stream,

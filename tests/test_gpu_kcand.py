@@ -109,3 +109,23 @@ def test_plain_load_kernel_on_aligned_rows():
     with api.tuned(kcand_ring=0):
         g = run(c)
     compare(g, kc_oracle(c), extra_equal=("k", "n_per_cand"))
+
+
+@pytest.mark.parametrize("B,K,gamma,V,dtype", [
+    (64, 8, 16, 152064, torch.bfloat16),  # the workload's shape: one wave
+    (300, 8, 8, 20000, torch.float32),    # the work counter
+    (40, 31, 6, 8192, torch.bfloat16)])   # the widest candidate mask helped
+def test_helping_same_bits(B, K, gamma, V, dtype):
+    """Clusters whose sequence is done compute rows of positions ahead of
+    the scans still running (SD_TUNE_HELPERS): the outputs with and without
+    helping are the same bits, and equal the oracle's."""
+    c = to_device(synth.kcand_case(B, K, gamma, V, dtype, 1.0, seed=B + K,
+                                   sigma_t=3.0, sigma_d=1.0, sigma_k=0.5))
+    outs = []
+    for h in (1, 0, 1):
+        with api.tuned(helpers=h):
+            outs.append(run(c))
+    for g in outs[1:]:
+        for k in outs[0]:
+            assert torch.equal(g[k], outs[0][k]), k
+    compare(outs[0], kc_oracle(c), extra_equal=("k", "n_per_cand"))
