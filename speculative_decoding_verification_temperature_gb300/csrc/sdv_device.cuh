@@ -740,6 +740,29 @@ __device__ __forceinline__ void write_resid(float *res, const Row &ra,
   }
 }
 
+// GPU-scope accesses to flags and counters that other CTAs write while this
+// kernel runs (a plain load could be served from a stale L1 line)
+__device__ __forceinline__ int ld_acquire_gpu(const int *a) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(a)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ int ld_relaxed_gpu(const int *a) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(a)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu(int *a, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(a), "r"(v)
+               : "memory");
+}
+__device__ __forceinline__ void st_relaxed_gpu(int *a, int v) {
+  asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(a), "r"(v)
+               : "memory");
+}
+
 __device__ __forceinline__ void status_or(int32_t *dev_status, int bits) {
   if (dev_status && bits) atomicOr(dev_status, bits);
 }

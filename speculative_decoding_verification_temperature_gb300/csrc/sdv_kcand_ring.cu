@@ -56,26 +56,6 @@ struct KRParams {
 constexpr int kKRows = SD_MAX_K + 1;  // draft row + one per candidate
 constexpr int kHelpRanks = 16;        // record stride: the largest cluster
 
-__device__ __forceinline__ int kh_ld_acquire(const int *a) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(a)
-               : "memory");
-  return v;
-}
-__device__ __forceinline__ int kh_ld_relaxed(const int *a) {
-  int v;
-  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(a)
-               : "memory");
-  return v;
-}
-__device__ __forceinline__ void kh_st_release(int *a, int v) {
-  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(a), "r"(v)
-               : "memory");
-}
-__device__ __forceinline__ void kh_st_relaxed(int *a, int v) {
-  asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(a), "r"(v)
-               : "memory");
-}
 
 // Ring schedule (thread 0 only, in shared memory).  Producer item kinds:
 // 0 the draft row of position pj, 1 the target rows of its live candidates
@@ -416,9 +396,9 @@ __global__ void __launch_bounds__(kThreads, 4)
   if (tid == 0) fu.pump(sh.sc, ps, consumed);
   while (b < p.B) {
     if (help && tid == 0 && rank == 0) {
-      kh_st_relaxed(p.opos + b, 0);
-      kh_st_relaxed(p.oalive + b, (int)full);
-      kh_st_relaxed(p.active + cid, b + 1);
+      st_relaxed_gpu(p.opos + b, 0);
+      st_relaxed_gpu(p.oalive + b, (int)full);
+      st_relaxed_gpu(p.active + cid, b + 1);
     }
     if (tid == 0) {
       if (rank == 0)
@@ -457,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 4)
       // rows that helpers did for this CTA's slice are taken, not streamed;
       // the helping flag is read here, for the decision after the exchange
       const unsigned skip = help ? sh.sc.skip : 0u;
-      if (help && tid == 64) sh.hseen = kh_ld_relaxed(p.helping);
+      if (help && tid == 64) sh.hseen = ld_relaxed_gpu(p.helping);
       int r = 0;
       if (!GREEDY) {
         if (skip & 1u) take_row(r++, 0);
@@ -515,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 4)
             bool ready = false;
             if (k < K && (am >> k & 1u)) {
               const size_t rec = hrec(b, jn, 1 + k);
-              if (kh_ld_acquire(p.hflag + rec)) {
+              if (ld_acquire_gpu(p.hflag + rec)) {
                 const float2 v = __ldcg(p.hpart + rec);
                 sh.hv[1 + k] = MS{v.x, v.y};
                 ready = true;
@@ -524,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 4)
             hmask = __ballot_sync(0xffffffffu, ready) << 1;
             if (lane == 0) {
               const size_t rec = hrec(b, jn, 0);
-              if (kh_ld_acquire(p.hflag + rec)) {
+              if (ld_acquire_gpu(p.hflag + rec)) {
                 const float2 v = __ldcg(p.hpart + rec);
                 sh.hv[0] = MS{v.x, v.y};
                 hmask |= 1u;
@@ -534,8 +514,8 @@ __global__ void __launch_bounds__(kThreads, 4)
           if (lane == 0) {  // publish progress; take the next position
             atomicMax(p.hpos + (size_t)b * kHelpRanks + rank, j + 2);
             if (rank == 0) {
-              kh_st_relaxed(p.oalive + b, (int)am);
-              kh_st_relaxed(p.opos + b, j + 1);
+              st_relaxed_gpu(p.oalive + b, (int)am);
+              st_relaxed_gpu(p.opos + b, j + 1);
             }
           }
         }
@@ -683,19 +663,19 @@ __global__ void __launch_bounds__(kThreads, 4)
     // consumed): compute this CTA's slice of the rows of positions ahead of
     // the scans still running, nearest to its owner's position first.
     if (tid == 0) {
-      if (rank == 0) kh_st_relaxed(p.active + cid, 0);
-      kh_st_relaxed(p.helping, 1);
+      if (rank == 0) st_relaxed_gpu(p.active + cid, 0);
+      st_relaxed_gpu(p.helping, 1);
     }
     for (int round = 0; round < gamma * p.B; ++round) {
       if (warp == 0) {
         int bs = -1, bpri = 0x7fffffff;
         for (int c = lane; c < p.nclusters; c += 32) {
-          const int a = kh_ld_relaxed(p.active + c);
+          const int a = ld_relaxed_gpu(p.active + c);
           if (a <= 0) continue;
           const int s = a - 1;
-          const int h = kh_ld_relaxed(p.hpos + (size_t)s * kHelpRanks + rank);
+          const int h = ld_relaxed_gpu(p.hpos + (size_t)s * kHelpRanks + rank);
           if (h >= gamma) continue;
-          const int pri = h - kh_ld_relaxed(p.opos + s);
+          const int pri = h - ld_relaxed_gpu(p.opos + s);
           if (pri < bpri) {
             bpri = pri;
             bs = s;
@@ -716,7 +696,7 @@ __global__ void __launch_bounds__(kThreads, 4)
             int *hp = p.hpos + (size_t)bs * kHelpRanks + rank;
             jc = atomicAdd(hp, 1);
             if (jc == 0) jc = atomicAdd(hp, 1);
-            al = (unsigned)kh_ld_relaxed(p.oalive + bs);
+            al = (unsigned)ld_relaxed_gpu(p.oalive + bs);
           }
           sh.hs = bs;
           sh.hj = jc;
@@ -745,7 +725,7 @@ __global__ void __launch_bounds__(kThreads, 4)
             for (int w = 1; w < kWarps; ++w) a = ms_merge(a, sh.wpart[0][w], k2);
             const size_t rec = hrec(hs, hj, row);
             __stcg(p.hpart + rec, make_float2(a.m, a.s));
-            kh_st_release(p.hflag + rec, 1);
+            st_release_gpu(p.hflag + rec, 1);
           }
           __syncthreads();
         }

@@ -17,7 +17,12 @@
 //
 // Clusters take sequences from a work counter, so short and long scans
 // balance across the GPU.  Greedy (T == 0) compares draft ids with the
-// row argmax (section 2.2) and reads no draft logits.
+// row argmax (section 2.2) and reads no draft logits.  Once the counter is
+// exhausted, clusters left without a sequence help the scans still running
+// (LinearParams: helping).  The FAN instantiation is the verify fused with
+// the Saguaro fan-out (sd_verify_linear_fanout): CTAs left without a
+// sequence compute the fan-out's top-F rows, settling the rows the scans
+// streamed from records the scans keep (LinearParams: fused fan-out).
 //
 // Two ways to read a step's slices: through a ring of shared-memory stages
 // filled by TMA bulk copies (cp.async.bulk, one mbarrier per stage), used
@@ -95,28 +100,6 @@ constexpr int kHelpRanks = 16;  // record stride: the largest cluster
 
 constexpr int kMaxW = 4;  // positions per step when a cluster speculates
 
-// GPU-scope accesses for the helping records (plain loads could be served
-// from a stale L1 line)
-__device__ __forceinline__ int ld_acquire_gpu(const int *a) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(a)
-               : "memory");
-  return v;
-}
-__device__ __forceinline__ int ld_relaxed_gpu(const int *a) {
-  int v;
-  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(a)
-               : "memory");
-  return v;
-}
-__device__ __forceinline__ void st_release_gpu(int *a, int v) {
-  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(a), "r"(v)
-               : "memory");
-}
-__device__ __forceinline__ void st_relaxed_gpu(int *a, int v) {
-  asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(a), "r"(v)
-               : "memory");
-}
 
 struct StepResult {
   int kind;   // 0 continue, 1 reject at n, 2 bonus, 3 unusable row
