@@ -48,7 +48,8 @@ struct KRParams {
   int *active;    // [nclusters]: sequence + 1 being verified, or 0
   int *opos;      // [B]: the owner's next position
   int *oalive;    // [B]: its live candidates
-  int *hpos;      // [B][kHelpRanks]: next position to hand to a helper
+  int *hpos;      // [B][kHelpRanks]: next (position, row) to hand to a
+                  // helper, as position * (K + 1) + row
   int *hflag;     // [B][gamma][K+1][kHelpRanks]: partial published
   float2 *hpart;  // [B][gamma][K+1][kHelpRanks]: (m, s)
 };
@@ -106,8 +107,7 @@ struct KRSmem {
   KSched sc;
   DrawSmem draw;
   MS hv[kKRows];  // helpers' partials of the next position's rows
-  int hs, hj;     // a helper's claim
-  unsigned halive;
+  int hs, hj, hr;  // a helper's claim: sequence, position, row
   int hseen;      // the helping flag, read at the position's start
 };
 
@@ -512,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 4)
             }
           }
           if (lane == 0) {  // publish progress; take the next position
-            atomicMax(p.hpos + (size_t)b * kHelpRanks + rank, j + 2);
+            atomicMax(p.hpos + (size_t)b * kHelpRanks + rank, (j + 2) * (K + 1));
             if (rank == 0) {
               st_relaxed_gpu(p.oalive + b, (int)am);
               st_relaxed_gpu(p.opos + b, j + 1);
@@ -640,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, 4)
       }
     }
     if (help && tid == 0)  // no more helpers for this sequence
-      atomicMax(p.hpos + (size_t)b * kHelpRanks + rank, gamma);
+      atomicMax(p.hpos + (size_t)b * kHelpRanks + rank, gamma * (K + 1));
     __syncthreads();
     b = sh.sc.next;  // learnt at this sequence's first exchange
     seqpar ^= 1;
@@ -666,14 +666,15 @@ __global__ void __launch_bounds__(kThreads, 4)
       if (rank == 0) st_relaxed_gpu(p.active + cid, 0);
       st_relaxed_gpu(p.helping, 1);
     }
-    for (int round = 0; round < gamma * p.B; ++round) {
+    for (int round = 0; round < gamma * (K + 1) * p.B; ++round) {
       if (warp == 0) {
         int bs = -1, bpri = 0x7fffffff;
         for (int c = lane; c < p.nclusters; c += 32) {
           const int a = ld_relaxed_gpu(p.active + c);
           if (a <= 0) continue;
           const int s = a - 1;
-          const int h = ld_relaxed_gpu(p.hpos + (size_t)s * kHelpRanks + rank);
+          const int h =
+              ld_relaxed_gpu(p.hpos + (size_t)s * kHelpRanks + rank) / (K + 1);
           if (h >= gamma) continue;
           const int pri = h - ld_relaxed_gpu(p.opos + s);
           if (pri < bpri) {
@@ -690,26 +691,29 @@ __global__ void __launch_bounds__(kThreads, 4)
           }
         }
         if (lane == 0) {
-          int jc = gamma;
-          unsigned al = 0;
-          if (bs >= 0) {  // position 0 is always the owner's own
+          int jc = gamma, rc = 0;
+          if (bs >= 0) {  // one row; position 0 and dead candidates skipped
             int *hp = p.hpos + (size_t)bs * kHelpRanks + rank;
-            jc = atomicAdd(hp, 1);
-            if (jc == 0) jc = atomicAdd(hp, 1);
-            al = (unsigned)ld_relaxed_gpu(p.oalive + bs);
+            const unsigned al = (unsigned)ld_relaxed_gpu(p.oalive + bs);
+            for (int t = 0; t < 2 * (K + 1); ++t) {
+              const int idx = atomicAdd(hp, 1);
+              jc = idx / (K + 1);
+              rc = idx % (K + 1);
+              if (jc >= gamma) break;
+              if (jc > 0 && (rc == 0 || (al >> (rc - 1) & 1u))) break;
+            }
           }
           sh.hs = bs;
           sh.hj = jc;
-          sh.halive = al;
+          sh.hr = rc;
         }
       }
       __syncthreads();
-      const int hs = sh.hs, hj = sh.hj;
-      const unsigned hal = sh.halive;
+      const int hs = sh.hs, hj = sh.hj, hr = sh.hr;
       if (hs < 0) break;
-      if (hj < gamma) {
-        for (int row = 0; row <= K; ++row) {  // 0: the draft row; 1 + k
-          if (row > 0 && !(hal >> (row - 1) & 1u)) continue;
+      if (hj > 0 && hj < gamma) {
+        {
+          const int row = hr;  // 0: the draft row; 1 + k: candidate k's
           if (tid == 0) {  // the row as the producer's current item
             const char *src = row == 0 ? fu.drow(hs, hj) : fu.trow(hs, row - 1, hj);
             ps.pa = src + (size_t)sl.vbeg * 16;
