@@ -100,6 +100,23 @@ def test_linear_workspace_covers_both_paths(B, gamma, V, dt):
         assert w >= B * rows * smax * 12
 
 
+def test_workspace_queries_cover_helping_and_records():
+    """The queries size the scratch of every path a call may take: the
+    linear verify's helping records (flags and 16-byte partials per
+    sequence, position and CTA rank), the fused step's scan records (24
+    bytes per scan thread and draft row, clusters of 8 at these sizes) and
+    the K-candidate verify's helping records (none for K = 32)."""
+    L = api.lib()
+    B, gamma = 256, 8
+    w = L.sd_verify_linear_workspace(B, gamma, 128256, 0)
+    assert w >= B * (gamma + 1) * 16 * (4 + 16)
+    f = L.sd_verify_linear_fanout_workspace(B, gamma, 128256, 0)
+    assert f >= B * gamma * 8 * 256 * 24 and f >= w
+    k = L.sd_verify_kcand_workspace(64, 8, 16, 152064, 1)
+    assert k >= 64 * 16 * 9 * 16 * (4 + 8)
+    assert L.sd_verify_kcand_workspace(64, 32, 16, 152064, 1) == 256
+
+
 def test_later_workspace_queries_are_host_only():
     L = api.lib()
     assert L.sd_verify_kcand_trie_workspace(64, 8, 16, 152064, 1) >= \
