@@ -316,32 +316,105 @@ __global__ void __launch_bounds__(kThreads, 4)
   auto consume = [&](auto &&f) {
     ft_consume(fu, rg, sh.sc, ps, consumed, phase, p.dev_status, f);
   };
-  // One row through the ring into this CTA's list clist[par][r].
-  auto select_row = [&](int r) {
-    cta_reset(sh.top);
+  // One row through the ring into this CTA's list clist[par][r] (rowp:
+  // the row in global memory).  The ring pass keeps each thread's largest
+  // element only.  Each warp's ceil(K / kWarps)-th largest lane maximum has
+  // that many of the warp's elements at or above it, so the least of those
+  // over the warps, th, has at least K of the slice's elements at or above
+  // it: the slice's best K are among the elements >= th.  A second pass
+  // reads the slice again (just streamed: from L2), gathers those elements
+  // and ranks them by counting.  When they overflow the buffer (ties,
+  // rows of -inf), the candidate-buffer selection of sdv_topf.cuh runs on
+  // the slice instead.
+  auto select_row = [&](int r, const char *rowp) {
+    float tmax = -__builtin_huge_valf();
     bool nan = false;
     for (int c = 0; c < nch; ++c) {
-      const int v0 = sl.vbeg + c * kStageVecs;
       const int cn = min(kStageVecs, nv - c * kStageVecs);
       consume([&](const uint4 *A) {
-        if (c == 0) {  // seed the threshold from the whole first chunk
+        for (int i = tid; i < cn; i += kThreads) {
+          const Raw<DT, VW> x = sget<DT, VW>(A, i);
+          float z[VW];
+#pragma unroll
+          for (int e = 0; e < VW; ++e) z[e] = elt<DT, VW>(x, e);
+          const float vm = vmax_nan_of<VW>(z);
+          nan |= vm != vm;
+          tmax = fmaxf(tmax, vm);  // (fmaxf drops a NaN)
+        }
+      });
+    }
+    if (tid == 0) {
+      sh.top.th = 0xffffffffu;
+      sh.top.nbuf = 0;
+    }
+    const int anynan = __syncthreads_or(nan);
+    {  // the warp's kw-th largest lane maximum; the least over the warps
+      const int kw = (K + kWarps - 1) / kWarps;
+      int cnt = 0;
+      for (int l = 0; l < 32; ++l)
+        cnt += __shfl_sync(0xffffffffu, tmax, l) >= tmax;
+      float sv = cnt >= kw ? tmax : -__builtin_huge_valf();
+      for (int o = 16; o; o >>= 1)
+        sv = fmaxf(sv, __shfl_xor_sync(0xffffffffu, sv, o));
+      if (lane == 0) atomicMin(&sh.top.th, ord32(sv));
+    }
+    __syncthreads();
+    const float th = unord32(sh.top.th);
+    const uint4 *src = reinterpret_cast<const uint4 *>(rowp) + sl.vbeg;
+    if (!anynan) {
+      for (int i = tid; i < nv; i += kThreads) {
+        Raw<DT, VW> x;
+        x.w = __ldcg(src + i);
+#pragma unroll
+        for (int e = 0; e < VW; ++e) {
+          const float z = elt<DT, VW>(x, e);
+          if (z >= th) {
+            const int slot = atomicAdd(&sh.top.nbuf, 1);
+            if (slot < kCtaCap)
+              sh.top.flat[slot] =
+                  make_key(ord32(z), (uint32_t)((sl.vbeg + i) * VW + e));
+          }
+        }
+      }
+    }
+    for (int i = tid; i < K; i += kThreads) sh.clist[par][r][i] = 0ull;
+    __syncthreads();
+    const int nc = sh.top.nbuf;
+    if (nc <= kCtaCap) {  // rank the gathered elements (unique keys)
+      for (int i = tid; i < nc; i += kThreads) {
+        const uint64_t me = sh.top.flat[i];
+        int rk = 0;
+        for (int q = 0; q < nc; ++q) rk += sh.top.flat[q] > me;
+        if (rk < K) sh.clist[par][r][rk] = me;
+      }
+    } else {  // too many: the candidate-buffer selection over the slice
+      __syncthreads();  // every thread has read nc before the reset
+      cta_reset(sh.top);
+      for (int c = 0; c * kStageVecs < nv; ++c) {
+        const int v0 = sl.vbeg + c * kStageVecs;
+        const int cn = min(kStageVecs, nv - c * kStageVecs);
+        const uint4 *A = src + c * kStageVecs;
+        if (c == 0) {
           float m1 = -__builtin_huge_valf(), m2 = -__builtin_huge_valf();
           for (int i = tid; i < cn; i += kThreads) {
-            const Raw<DT, VW> x = sget<DT, VW>(A, i);
+            Raw<DT, VW> x;
+            x.w = __ldcg(A + i);
 #pragma unroll
             for (int e = 0; e < VW; ++e) top2_add(m1, m2, elt<DT, VW>(x, e));
           }
           cta_seed(sh.top, m1, m2, K);
         }
-        nan |= cta_offer_chunk<DT, VW>(sh.top, A, cn, v0, K);
-      });
+        cta_offer_chunk<DT, VW>(sh.top, A, cn, v0, K);
+      }
+      cta_compact(sh.top, K);  // the slice's best K, descending
+      const int nout = sh.top.nbuf;
+      for (int i = tid; i < K; i += kThreads)
+        sh.clist[par][r][i] = i < nout ? sh.top.flat[i] : 0ull;
     }
-    const int anynan = __syncthreads_or(nan);
-    cta_compact(sh.top, K);  // the slice's best K, descending
-    const int nout = sh.top.nbuf;
-    for (int i = tid; i < K; i += kThreads)
-      sh.clist[par][r][i] = i < nout ? sh.top.flat[i] : 0ull;
-    if (tid == 0) sh.cnan[par][r] = anynan;
+    if (tid == 0) {
+      sh.cnan[par][r] = anynan;
+      sh.top.th = 0;
+    }
     __syncthreads();
   };
   // Exchange rows [r0, r0 + nr): every CTA ranks the CL lists of each row
@@ -386,8 +459,8 @@ __global__ void __launch_bounds__(kThreads, 4)
         gr = p.uniforms[(size_t)b * G1 + j];
         gu = p.uniforms[(size_t)b * G1 + gamma];
       }
-      select_row(0);  // draft row j
-      select_row(1);  // target row j
+      select_row(0, fu.row(0, b, j));  // draft row j
+      select_row(1, fu.row(1, b, j));  // target row j
       if (tid == 32) {
         sh.gx = gx;
         sh.gr = gr;
@@ -461,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 4)
       n = j + 1;
     }
     if (!kind) {  // every draft accepted: the bonus from p~_gamma
-      select_row(1);
+      select_row(1, fu.row(1, b, gamma));
       exchange(1, 1);
       if (warp == kWarps - 1) {
         int kd = 2;

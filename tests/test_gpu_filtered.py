@@ -150,6 +150,53 @@ def test_threshold_select_refinement(T, sigma, top_k, top_p):
     check_forced(c, top_k, top_p)
 
 
+def redraw(c, T, top_k, top_p, seed):
+    """Draft tokens drawn again from the filtered draft rows of c."""
+    d = synth.host_logits(c.draft)
+    if d.dtype == np.uint16:
+        d = (d.astype(np.uint32) << 16).view(np.float32)
+    B, gamma = c.tokens.shape
+    V = d.shape[-1]
+    rng = np.random.default_rng(seed)
+    for b in range(B):
+        for i in range(gamma):
+            q = filtered_np(d[b, i], T, top_k, top_p)
+            g = -np.log(-np.log(rng.random(V).clip(1e-300)))
+            with np.errstate(divide="ignore"):
+                c.tokens[b, i] = int(np.argmax(np.log(q) + g))
+    return c
+
+
+@pytest.mark.parametrize("V,dtype", [(4104, torch.bfloat16),
+                                     (32000, torch.float32),
+                                     (128256, torch.float32)])
+@pytest.mark.parametrize("top_k,top_p", [(50, 1.0), (64, 0.5), (7, 0.9)])
+def test_small_k_ties_and_masked_tails(V, dtype, top_k, top_p):
+    """top_k <= 64 (exact lists) on rows whose bound from the lane maxima
+    admits many elements: constant rows (every element ties), rows with
+    fewer finite logits than top_k (-inf tails, the bound is -inf), logits
+    on a coarse grid (many ties at the bound), and ordinary rows beside
+    them in the same launch."""
+    B, gamma, T = 8, 3, 1.0
+    c = synth.linear_case(B, gamma, V, dtype, T, seed=V + top_k,
+                          sigma_t=2.0, sigma_d=1.0)
+    c.target[0] = 0.25
+    c.draft[0] = 0.25
+    c.target[1, :, 30:] = -float("inf")
+    c.draft[1, :, 30:] = -float("inf")
+    c.target[2, :, :V - 5] = -float("inf")
+    c.draft[2, :, 7:] = -float("inf")
+    c.target[3] = torch.round(c.target[3].float() * 2).to(dtype) / 2
+    c.draft[3] = torch.round(c.draft[3].float() * 2).to(dtype) / 2
+    c.target[4, 1] = 0.25
+    c.draft[4, :, V // 2:] = c.target[4, :gamma, V // 2:]
+    c = to_device(redraw(c, T, top_k, top_p, seed=V))
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    r = compare(run(c, top_k, top_p, status=st), orc(c, top_k, top_p))
+    assert r["acc_flagged"] <= 2
+    assert int(st.item()) & api.DEV_NONFINITE == 0
+
+
 def test_threshold_select_edges():
     """Masked tails (-inf), a bad token, NaN and +inf rows, bf16 ties."""
     B, gamma, V = 10, 3, 8192
