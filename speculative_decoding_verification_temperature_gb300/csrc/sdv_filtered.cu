@@ -7,10 +7,12 @@
 // top_k (logit, id) keys: the filtered distribution is 2^((z - m) k2) over
 // the kept keys (m the row maximum, k2 = log2(e)/T), the nucleus is a
 // prefix of them, and the residual max(0, p~ - q~) is zero outside the
-// target's kept tokens.  So each row is read once, through the exact top-k
-// selection of sdv_topf.cuh (one CTA-wide candidate buffer above a seeded,
-// rising threshold: a compare per element), and the accept test, the correction and the bonus are computed by one
-// warp on at most 64 keys per row: there is no second pass over a row.
+// target's kept tokens.  So each row is read from HBM once, and each CTA
+// selects its slice's exact top-k: the ring pass keeps each thread's
+// maximum, a bound follows from those maxima, and a second pass over the
+// slice (from L2, just streamed) gathers and ranks the few elements at or
+// above it.  The accept test, the correction and the bonus are computed by
+// one warp on at most 64 keys per row.
 //
 // One thread-block cluster verifies one sequence at a time (work counter).
 // Position j streams the CTAs' slices of the draft row j and the target row
