@@ -25,6 +25,7 @@
 #include "sdv_host.cuh"
 #include "sdv_ring.cuh"
 #include "sdv_tma.cuh"
+#include "sdv_fanrow.cuh"
 #include "sdv_topf.cuh"
 
 namespace sdv {
@@ -284,8 +285,9 @@ __device__ __forceinline__ float fdraw(FiltSmem &sh, float w0, int j0,
   return N;
 }
 
+// (Three CTAs per SM: their shared memory allows no more.)
 template <int DT, int VW>
-__global__ void __launch_bounds__(kThreads, 4)
+__global__ void __launch_bounds__(kThreads, 3)
     filtered_verify_kernel(const FiltParams p) {
   extern __shared__ __align__(128) unsigned char dsm[];
   __shared__ FiltSmem sh;
@@ -319,19 +321,25 @@ __global__ void __launch_bounds__(kThreads, 4)
     ft_consume(fu, rg, sh.sc, ps, consumed, phase, p.dev_status, f);
   };
   // One row through the ring into this CTA's list clist[par][r] (rowp:
-  // the row in global memory).  The ring pass keeps each thread's largest
-  // element only.  Each warp's ceil(K / kWarps)-th largest lane maximum has
-  // that many of the warp's elements at or above it, so the least of those
-  // over the warps, th, has at least K of the slice's elements at or above
-  // it: the slice's best K are among the elements >= th.  A second pass
-  // reads the slice again (just streamed: from L2), gathers those elements
-  // and ranks them by counting.  When they overflow the buffer (ties,
-  // rows of -inf), the candidate-buffer selection of sdv_topf.cuh runs on
-  // the slice instead.
+  // the row in global memory).  During the ring pass each thread keeps the
+  // vector holding its largest element (16 bytes in registers) and t2, the
+  // largest maximum of its other vectors.  Each warp's ceil(K / kWarps)-th
+  // largest lane maximum has that many of the warp's elements at or above
+  // it, so the least of those over the warps, th, has at least K of the
+  // slice's elements at or above it: the slice's best K are among the
+  // elements >= th.  A thread with t2 < th holds all of its elements >= th
+  // in its kept vector and appends them from registers.  The part of the
+  // slice of any other thread is read again (from L2, just streamed) by
+  // its whole warp, one vector per lane, and its elements >= th appended.
+  // The gathered elements are ranked by counting.  When they overflow the
+  // buffer (ties, rows of -inf), the candidate-buffer selection of
+  // sdv_topf.cuh runs on the slice instead.
   auto select_row = [&](int r, const char *rowp) {
-    float tmax = -__builtin_huge_valf();
+    VecTop<DT, VW> vt;
+    vec_top_init(vt);
     bool nan = false;
     for (int c = 0; c < nch; ++c) {
+      const int v0 = sl.vbeg + c * kStageVecs;
       const int cn = min(kStageVecs, nv - c * kStageVecs);
       consume([&](const uint4 *A) {
         for (int i = tid; i < cn; i += kThreads) {
@@ -341,10 +349,11 @@ __global__ void __launch_bounds__(kThreads, 4)
           for (int e = 0; e < VW; ++e) z[e] = elt<DT, VW>(x, e);
           const float vm = vmax_nan_of<VW>(z);
           nan |= vm != vm;
-          tmax = fmaxf(tmax, vm);  // (fmaxf drops a NaN)
+          vec_top_add(vt, x, vm, v0 + i);  // (a NaN maximum is not kept)
         }
       });
     }
+    const float tmax = vt.t1;
     if (tid == 0) {
       sh.top.th = 0xffffffffu;
       sh.top.nbuf = 0;
@@ -364,18 +373,26 @@ __global__ void __launch_bounds__(kThreads, 4)
     const float th = unord32(sh.top.th);
     const uint4 *src = reinterpret_cast<const uint4 *>(rowp) + sl.vbeg;
     if (!anynan) {
-      for (int i = tid; i < nv; i += kThreads) {
-        Raw<DT, VW> x;
-        x.w = __ldcg(src + i);
+      auto append = [&](const Raw<DT, VW> &x, int vidx) {
 #pragma unroll
         for (int e = 0; e < VW; ++e) {
           const float z = elt<DT, VW>(x, e);
           if (z >= th) {
             const int slot = atomicAdd(&sh.top.nbuf, 1);
             if (slot < kCtaCap)
-              sh.top.flat[slot] =
-                  make_key(ord32(z), (uint32_t)((sl.vbeg + i) * VW + e));
+              sh.top.flat[slot] = make_key(ord32(z), (uint32_t)(vidx * VW + e));
           }
+        }
+      };
+      const bool whole = !(vt.t2 < th);  // (also when th is -inf)
+      if (!whole && vt.bidx >= 0 && vt.t1 >= th) append(vt.best, vt.bidx);
+      // the parts of the threads with more than one vector reaching th
+      for (unsigned m = __ballot_sync(0xffffffffu, whole); m; m &= m - 1) {
+        const int owner = warp * 32 + __ffs(m) - 1;
+        for (int i = owner + lane * kThreads; i < nv; i += 32 * kThreads) {
+          Raw<DT, VW> x;
+          x.w = __ldcg(src + i);
+          append(x, sl.vbeg + i);
         }
       }
     }
