@@ -21,6 +21,13 @@
 // candidates, the cluster exchanges the per-CTA lists through distributed
 // shared memory, and every CTA ranks the CL lists of both rows into the
 // rows' exact top-k.
+
+// This kernel's ring: two stages of 16 KB.  Its CTAs then fit four to an SM
+// (shared memory and 64 registers), and the more clusters in flight
+// verify fewer sequences each one after another: on the large shape
+// 149.8-153.5 us against 161.9-162.0 us with three stages and three CTAs
+// per SM.  (No other translation unit sees this value.)
+#define SDV_STAGES 2
 #include "sdv_device.cuh"
 #include "sdv_host.cuh"
 #include "sdv_ring.cuh"
@@ -285,9 +292,8 @@ __device__ __forceinline__ float fdraw(FiltSmem &sh, float w0, int j0,
   return N;
 }
 
-// (Three CTAs per SM: their shared memory allows no more.)
 template <int DT, int VW>
-__global__ void __launch_bounds__(kThreads, 3)
+__global__ void __launch_bounds__(kThreads, 4)
     filtered_verify_kernel(const FiltParams p) {
   extern __shared__ __align__(128) unsigned char dsm[];
   __shared__ FiltSmem sh;
