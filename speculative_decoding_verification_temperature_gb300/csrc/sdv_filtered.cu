@@ -292,6 +292,11 @@ __device__ __forceinline__ float fdraw(FiltSmem &sh, float w0, int j0,
   return N;
 }
 
+// The ring pass gives thread t the vectors at offsets t + kThreads m of its
+// slice (a stage holds a multiple of kThreads vectors), which the re-read of
+// a thread's part relies on.
+static_assert(kStageVecs % kThreads == 0, "stage not a multiple of the CTA");
+
 template <int DT, int VW>
 __global__ void __launch_bounds__(kThreads, 4)
     filtered_verify_kernel(const FiltParams p) {
